@@ -1,0 +1,453 @@
+"""fp64 oracle for the MosaicKV decode-time hot path.  TEST INFRASTRUCTURE.
+
+This module is the checker, not the product.  Only the test suite,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference arm
+may import it.  The CUDA library and its Python binding never do, and this
+module imports nothing from them: the two sides share only the seeded input
+generators, which hold none of the method's arithmetic.
+
+It restates the method step by step, in float64, with library primitives
+(matmul, eigh, stable argsort) as the only building blocks.  bf16-exact data
+(inputs, rotated vectors) are kept as float32 to save memory; every
+arithmetic step upcasts to float64.
+
+Sources (cited by page title and equation/section):
+  [N] "MosaicKV：面向超长上下文LLM服务的动态二维KV缓存压缩——阅读笔记"
+      (reading notes on zhongzhuzhou.org): Eq. (1), (4)-(9), (12)-(16),
+      Algorithm 1, the d=4 worked example of the SVD section.
+  [S] "MosaicKV: Serving Long-Context LLM with Dynamic Two-D KV Cache
+      Compression" (paperlayer.ai summary of arXiv 2607.00760v1):
+      sec. 4.2-4.3 (two-stage compression, per-segment strategy),
+      sec. 5.1 (packed format), sec. 5.3 (PackedAttention), sec. 6.3.
+
+Readings where the pages are silent (each is listed in the design doc):
+  * segments: sinks [0, S), recent window [T-W, T), middle [S, T-W) cut into
+    blocks of B tokens from S; the last block may be partial;
+  * per-vector top-r: magnitude descending, ties to the lower channel; the
+    kept channels are stored in ascending channel order as bf16 values plus
+    uint8 indices; a stored zero is +0;
+  * block metadata: per-channel min and max over the block of the
+    zero-filled compressed key (Quest-style bound on Eq. (12));
+  * GQA: a kv head's block score is the max over its query heads;
+  * top-k: k largest scores, ties to the lower block id, ids ascending;
+    k = min(topk_fixed, n) or ceil(retain * n / 1000) clamped to [1, n];
+  * strategy segments start at the first block boundary at or after
+    begin_permille/1000 of the prefill length; the last one is open-ended;
+  * decode append: the new token enters the window; the window's oldest
+    token, once more than W are held, moves into the middle.
+
+Parity status: every public function is pinned by tests/test_oracle_pins.py
+(worked example, brute force, closed forms, library routines, invariants).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+D_HEAD = 128
+
+
+# --------------------------------------------------------------------------
+# bf16 rounding (storage precision of K, V and the rotated vectors)
+# --------------------------------------------------------------------------
+def bf16_round(x):
+    """Round float64 values to the nearest bf16 value, ties to even.
+
+    bf16 keeps 8 significant bits and float32's exponent range, so for
+    2**(e-1) <= |x| < 2**e the spacing is 2**(e-8); below the smallest normal
+    (2**-126) the spacing stays 2**-133.  Zero is returned as +0.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    assert np.all(np.isfinite(x)), "NaN/Inf inputs are outside the contract"
+    _, e = np.frexp(x)
+    e = np.maximum(e, -125)
+    ulp = np.ldexp(1.0, e - 8)
+    y = np.round(x / ulp) * ulp
+    return y + 0.0
+
+
+def bf16_bits(y):
+    """uint16 bit pattern of bf16-exact float64 values."""
+    y = np.asarray(y, dtype=np.float64)
+    return (y.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bits_to_value(b):
+    b = np.asarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Rotation: [N] Eq. (4), (6)-(8); un-rotation Eq. (14)
+# --------------------------------------------------------------------------
+def rotation_from_keys(X):
+    """R = V^T from the eigendecomposition X^T X = V diag(lambda) V^T.
+
+    Eigenvalues are sorted descending, so row i of R is the i-th principal
+    direction.  Returns (R, eigenvalues).
+    """
+    X = np.asarray(X, dtype=np.float64)
+    lam, vecs = np.linalg.eigh(X.T @ X)
+    order = np.argsort(-lam, kind="stable")
+    return vecs[:, order].T.copy(), lam[order]
+
+
+def rotate(X, R, round_bf16=True):
+    """X' = X R^T ([N] Eq. (7)/(8)); rounded once, fp64 -> bf16, if asked."""
+    Y = np.asarray(X, dtype=np.float64) @ np.asarray(R, dtype=np.float64).T
+    return bf16_round(Y) if round_bf16 else Y
+
+
+def energy(R, X, r):
+    """Energy(r) of [N] Eq. (5), measured on the rotated columns of X."""
+    Xp = rotate(X, R, round_bf16=False)
+    col = np.sum(Xp * Xp, axis=0)
+    return col[:r].sum() / col.sum()
+
+
+# --------------------------------------------------------------------------
+# Channel selection: [N] Eq. (9) / Algorithm 1 and the global-mask contrast
+# --------------------------------------------------------------------------
+def topr_select(X, r):
+    """Per-vector top-r by magnitude ([N] Eq. (9), Algorithm 1).
+
+    X: [n, d] bf16-exact values.  Order channels by |x| descending, ties to
+    the lower channel (a stable sort keeps channel order among equals), keep
+    the first r, and return them in ascending channel order.
+    Returns (idx uint8 [n, r], vals float64 [n, r]).
+    """
+    X = np.asarray(X, dtype=np.float64)
+    if X.ndim == 1:
+        X = X[None, :]
+    order = np.argsort(-np.abs(X), axis=1, kind="stable")[:, :r]
+    idx = np.sort(order, axis=1)
+    vals = np.take_along_axis(X, idx, axis=1)
+    return idx.astype(np.uint8), vals
+
+
+def global_mask_energy(Xp, r):
+    """ThinK-style shared mask by channel energy sum_i x_ij^2 (contrast only)."""
+    e = np.sum(np.asarray(Xp, dtype=np.float64) ** 2, axis=0)
+    return np.sort(np.argsort(-e, kind="stable")[:r])
+
+
+def global_mask_variance(Xp, r):
+    """ThinK-style shared mask argtopk(var(K', axis 0), r) ([N] ThinK formula)."""
+    v = np.var(np.asarray(Xp, dtype=np.float64), axis=0)
+    return np.sort(np.argsort(-v, kind="stable")[:r])
+
+
+def densify(idx, vals, d=D_HEAD):
+    """Zero-filled dense vectors k~ from (idx, vals) pairs."""
+    idx = np.asarray(idx, dtype=np.int64)
+    out = np.zeros((idx.shape[0], d), dtype=np.float64)
+    np.put_along_axis(out, idx, np.asarray(vals, dtype=np.float64), axis=1)
+    return out
+
+
+# --------------------------------------------------------------------------
+# Segments and strategy ([S] sec. 4.3)
+# --------------------------------------------------------------------------
+@dataclass
+class Strategy:
+    n_sink: int
+    window: int
+    block: int
+    segments: list            # [(begin_permille, r, always)]
+    topk_fixed: int = 0
+    retain_permille: int = 0
+
+
+def n_middle_blocks(T, st: Strategy):
+    mid = max(0, T - st.window - st.n_sink)
+    return (mid + st.block - 1) // st.block
+
+
+def segment_first_blocks(T0, st: Strategy):
+    """First middle block of each strategy segment, fixed at prefill length T0."""
+    nb0 = n_middle_blocks(T0, st)
+    firsts = []
+    prev = 0
+    for i, (begin, _r, _a) in enumerate(st.segments):
+        if i == 0:
+            b = 0
+        else:
+            pos = (begin * T0) // 1000
+            b = (max(0, pos - st.n_sink) + st.block - 1) // st.block
+            b = min(max(b, prev), nb0)
+        firsts.append(b)
+        prev = b
+    return firsts
+
+
+def block_segment(b, firsts):
+    s = 0
+    for i, f in enumerate(firsts):
+        if b >= f:
+            s = i
+    return s
+
+
+def n_select(n_scored, st: Strategy):
+    """Number of blocks top-k keeps among n_scored candidates."""
+    if n_scored <= 0:
+        return 0
+    if st.topk_fixed > 0:
+        return min(st.topk_fixed, n_scored)
+    k = (st.retain_permille * n_scored + 999) // 1000
+    return min(max(k, 1), n_scored)
+
+
+# --------------------------------------------------------------------------
+# Block scoring and top-k ([N] Eq. (12); Quest min/max bound; [S] sec. 4.2)
+# --------------------------------------------------------------------------
+def block_scores(qr, mn, mx):
+    """Quest-style bound per block: (1/sqrt(d)) sum_j max(q'_j mn_j, q'_j mx_j).
+
+    qr: [G, d] rotated queries of one kv head's group; mn, mx: [nblk, d].
+    Returns (per_head [G, nblk], group max [nblk]).
+    """
+    qr = np.asarray(qr, dtype=np.float64)
+    mn = np.asarray(mn, dtype=np.float64)
+    mx = np.asarray(mx, dtype=np.float64)
+    d = qr.shape[1]
+    per = np.empty((qr.shape[0], mn.shape[0]))
+    for h in range(qr.shape[0]):
+        per[h] = np.sum(np.maximum(qr[h][None, :] * mn, qr[h][None, :] * mx), axis=1) / math.sqrt(d)
+    return per, per.max(axis=0)
+
+
+def block_max_exact(qr, Kt_block):
+    """[N] Eq. (12) taken literally: (1/sqrt(d)) max_i q' . k~_i over a block."""
+    qr = np.asarray(qr, dtype=np.float64)
+    return np.max(np.asarray(Kt_block, dtype=np.float64) @ qr.T, axis=0).max() / math.sqrt(qr.shape[1])
+
+
+def topk_blocks(scores, candidates, k):
+    """k highest scores among candidate block ids; ties to the lower id; ascending ids."""
+    cand = np.asarray(candidates, dtype=np.int64)
+    if k <= 0 or cand.size == 0:
+        return np.zeros(0, dtype=np.int64)
+    s = np.asarray(scores, dtype=np.float64)[cand]
+    order = np.lexsort((cand, -s))
+    return np.sort(cand[order[:k]])
+
+
+# --------------------------------------------------------------------------
+# Attention ([N] Eq. (1), (13), (14))
+# --------------------------------------------------------------------------
+def softmax_attention(qr, Kt, Vt):
+    """o = softmax(q' K^T / sqrt(d)) V for each row of qr, exact in fp64."""
+    qr = np.asarray(qr, dtype=np.float64)
+    if Kt.shape[0] == 0:
+        return np.zeros((qr.shape[0], qr.shape[1]))
+    logits = qr @ np.asarray(Kt, dtype=np.float64).T / math.sqrt(qr.shape[1])
+    logits -= logits.max(axis=1, keepdims=True)
+    p = np.exp(logits)
+    p /= p.sum(axis=1, keepdims=True)
+    return p @ np.asarray(Vt, dtype=np.float64)
+
+
+def dense_attention(q, K, V):
+    """[N] Eq. (1) on the unrotated, uncompressed cache."""
+    return softmax_attention(q, np.asarray(K, dtype=np.float64), np.asarray(V, dtype=np.float64))
+
+
+# --------------------------------------------------------------------------
+# The compressed cache of one (layer, sequence, kv head)
+# --------------------------------------------------------------------------
+class OracleCache:
+    """Sinks and window as dense rotated bf16; middle as per-vector top-r.
+
+    Built by appending tokens ([N] the decode-time rotation of each new
+    k/v; [S] sec. 4.2 stage 1, sec. 5.3 update buffer read as the window).
+    """
+
+    def __init__(self, st: Strategy, capacity: int, d: int = D_HEAD, round_bf16: bool = True):
+        self.st = st
+        self.d = d
+        self.cap = capacity
+        self.round = round_bf16
+        dt = np.float32 if round_bf16 else np.float64
+        self.Kr = np.zeros((capacity, d), dtype=dt)     # rotated tokens
+        self.Vr = np.zeros((capacity, d), dtype=dt)
+        self.Kt = np.zeros((capacity, d), dtype=dt)     # zero-filled compressed (middle rows)
+        self.Vt = np.zeros((capacity, d), dtype=dt)
+        rmax = max(r for _, r, _ in st.segments)
+        self.kidx = np.zeros((capacity, rmax), dtype=np.uint8)
+        self.vidx = np.zeros((capacity, rmax), dtype=np.uint8)
+        self.kval = np.zeros((capacity, rmax), dtype=dt)
+        self.vval = np.zeros((capacity, rmax), dtype=dt)
+        self.rtok = np.zeros(capacity, dtype=np.int64)
+        nb = n_middle_blocks(capacity, st) + 1
+        self.mn = np.zeros((nb, d), dtype=dt)
+        self.mx = np.zeros((nb, d), dtype=dt)
+        self.T = 0
+        self.T0 = None
+        self.firsts = None
+        self.n_mid = 0
+        self.Rk = None
+        self.Rv = None
+
+    def set_rotation(self, Rk, Rv):
+        self.Rk = np.asarray(Rk, dtype=np.float64)
+        self.Rv = np.asarray(Rv, dtype=np.float64)
+
+    # --- strategy helpers -------------------------------------------------
+    def r_of_block(self, b):
+        return self.st.segments[block_segment(b, self.firsts)][1]
+
+    def always_of_block(self, b):
+        return bool(self.st.segments[block_segment(b, self.firsts)][2])
+
+    def n_blocks(self):
+        return n_middle_blocks(self.T, self.st)
+
+    def block_tokens(self, b):
+        S, B = self.st.n_sink, self.st.block
+        lo = S + b * B
+        hi = min(lo + B, S + self.n_mid)
+        return lo, hi
+
+    # --- append -----------------------------------------------------------
+    def append(self, K_new, V_new):
+        K_new = np.asarray(K_new, dtype=np.float64)
+        V_new = np.asarray(V_new, dtype=np.float64)
+        n = K_new.shape[0]
+        assert self.Rk is not None, "rotation must be set before append"
+        assert self.T + n <= self.cap, "capacity exceeded"
+        if self.T == 0:
+            self.T0 = n
+            self.firsts = segment_first_blocks(n, self.st)
+        t0 = self.T
+        self.Kr[t0:t0 + n] = rotate(K_new, self.Rk, self.round)
+        self.Vr[t0:t0 + n] = rotate(V_new, self.Rv, self.round)
+        self.T += n
+        S, W, B = self.st.n_sink, self.st.window, self.st.block
+        target = max(0, self.T - W - S)
+        if target > self.n_mid:
+            lo, hi = S + self.n_mid, S + target
+            self._compress(lo, hi)
+            self.n_mid = target
+            # Block min/max over the zero-filled compressed keys, recomputed
+            # from the definition for every block that gained a token.
+            for b in range((lo - S) // B, (hi - 1 - S) // B + 1):
+                blo, bhi = self.block_tokens(b)
+                blk = self.Kt[blo:bhi].astype(np.float64)
+                self.mn[b] = blk.min(axis=0) + 0.0
+                self.mx[b] = blk.max(axis=0) + 0.0
+
+    def _compress(self, lo, hi):
+        S, B = self.st.n_sink, self.st.block
+        pos = np.arange(lo, hi)
+        blocks = (pos - S) // B
+        for b in np.unique(blocks):
+            sel = pos[blocks == b]
+            r = self.r_of_block(int(b))
+            for src, dst_idx, dst_val, dense in ((self.Kr, self.kidx, self.kval, self.Kt),
+                                                (self.Vr, self.vidx, self.vval, self.Vt)):
+                idx, vals = topr_select(src[sel].astype(np.float64), r)
+                dst_idx[sel, :r] = idx
+                dst_idx[sel, r:] = 0
+                dst_val[sel, :r] = vals
+                dst_val[sel, r:] = 0
+                dense[sel] = densify(idx, vals, self.d)
+            self.rtok[sel] = r
+
+    def n_blocks_mid(self):
+        return (self.n_mid + self.st.block - 1) // self.st.block
+
+    # --- views used by the tests ------------------------------------------
+    def sink_positions(self):
+        return np.arange(min(self.st.n_sink, self.T))
+
+    def window_positions(self):
+        return np.arange(self.st.n_sink + self.n_mid, self.T)
+
+    def ring_slot(self, p):
+        return (p - self.st.n_sink) % self.st.window
+
+    def meta(self):
+        nb = self.n_blocks_mid()
+        return self.mn[:nb].astype(np.float64), self.mx[:nb].astype(np.float64)
+
+    def page_bytes(self, b):
+        """The packed page of block b: [Kval B*r bf16][Kidx B*r u8][Vval B*r bf16][Vidx B*r u8].
+
+        Slots past the last live token are zero ([S] sec. 5.1 contiguous
+        packing; uint8 indices as the build's contract).
+        """
+        B = self.st.block
+        r = self.r_of_block(b)
+        lo, hi = self.block_tokens(b)
+        kv = np.zeros((B, r), dtype=np.uint16)
+        ki = np.zeros((B, r), dtype=np.uint8)
+        vv = np.zeros((B, r), dtype=np.uint16)
+        vi = np.zeros((B, r), dtype=np.uint8)
+        n = hi - lo
+        kv[:n] = bf16_bits(self.kval[lo:hi, :r])
+        ki[:n] = self.kidx[lo:hi, :r]
+        vv[:n] = bf16_bits(self.vval[lo:hi, :r])
+        vi[:n] = self.vidx[lo:hi, :r]
+        return np.concatenate([kv.reshape(-1).view(np.uint8), ki.reshape(-1),
+                               vv.reshape(-1).view(np.uint8), vi.reshape(-1)])
+
+    # --- decode-time select and attention ---------------------------------
+    def rotate_query(self, q):
+        """q' = q R_k^T, the query side of the rotation ([S] sec. 5.3)."""
+        return np.asarray(q, dtype=np.float64) @ self.Rk.T
+
+    def candidates(self):
+        nb = self.n_blocks_mid()
+        return np.array([b for b in range(nb) if not self.always_of_block(b)], dtype=np.int64)
+
+    def always_blocks(self):
+        nb = self.n_blocks_mid()
+        return np.array([b for b in range(nb) if self.always_of_block(b)], dtype=np.int64)
+
+    def scores(self, q):
+        """Group scores over every middle block (always-blocks included)."""
+        mn, mx = self.meta()
+        per, grp = block_scores(self.rotate_query(q), mn, mx)
+        return per, grp
+
+    def select(self, q):
+        cand = self.candidates()
+        k = n_select(len(cand), self.st)
+        _, grp = self.scores(q)
+        return topk_blocks(grp, cand, k), grp
+
+    def attend_tokens(self, ids):
+        """Token rows (rotated K, rotated V) that attention reads for these blocks."""
+        rows_k = [self.Kr[self.sink_positions()], self.Kr[self.window_positions()]]
+        rows_v = [self.Vr[self.sink_positions()], self.Vr[self.window_positions()]]
+        blocks = np.concatenate([np.asarray(ids, dtype=np.int64), self.always_blocks()])
+        for b in blocks:
+            lo, hi = self.block_tokens(int(b))
+            rows_k.append(self.Kt[lo:hi])
+            rows_v.append(self.Vt[lo:hi])
+        return (np.concatenate(rows_k).astype(np.float64),
+                np.concatenate(rows_v).astype(np.float64))
+
+    def attention(self, q, ids):
+        """[N] Eq. (13) on the kept tokens, then Eq. (14) output = o R_v."""
+        Kt, Vt = self.attend_tokens(ids)
+        o = softmax_attention(self.rotate_query(q), Kt, Vt)
+        return o @ self.Rv
+
+
+def speedup_bound(alpha, beta):
+    """[N] Eq. (15): T d / (s_sel r) = 1 / (alpha beta)."""
+    return 1.0 / (alpha * beta)
+
+
+def meta_overhead(block, d=D_HEAD, elem_bytes=2):
+    """Per-block min/max keys relative to the block's uncompressed K+V ([S] sec. 6.3)."""
+    return (2 * d * elem_bytes) / (2 * block * d * elem_bytes)
+
+
+def packed_bytes_per_token(r):
+    """K and V: r bf16 values plus r uint8 indices each."""
+    return 2 * (2 * r + r)

@@ -1,0 +1,310 @@
+"""Pins the fp64 oracle to facts fixed outside itself (runs without a GPU).
+
+Each test checks the oracle against a value the pages print, a closed form, a
+library routine, an invariant of the mathematics, or brute force on tiny
+inputs.  The mutation tests at the end plant plausible mistakes in copies of
+oracle functions and check that a pin catches each of them.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mosaickv_oracle as O
+from compressed_kv_cache_vector_gb300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- bf16 ----
+def test_bf16_round_matches_torch_conversion():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-30, 30, 20000))).astype(np.float32)
+    # exact halfway cases: a bf16 value plus half its spacing
+    base = torch.tensor(rng.standard_normal(2000), dtype=torch.float32).to(torch.bfloat16).float().numpy()
+    half = np.ldexp(1.0, np.frexp(base.astype(np.float64))[1] - 9).astype(np.float32)
+    ties = np.concatenate([base + half, base - half]).astype(np.float32)
+    for v in (x, ties, np.array([0.0, -0.0, 1.0, 2 ** -126, 3 * 2 ** -130], dtype=np.float32)):
+        want = torch.tensor(v).to(torch.bfloat16).double().numpy() + 0.0
+        got = O.bf16_round(v.astype(np.float64))
+        assert np.array_equal(got, want)
+        assert np.array_equal(O.bf16_bits(got), (want.astype(np.float32).view(np.uint32) >> 16))
+
+
+# ----------------------------------------------------- worked example ----
+def _read_golden():
+    vec, keep, glob = {}, {}, None
+    with open(os.path.join(GOLD, "worked_example_d4.txt"), encoding="utf-8") as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            p = line.split()
+            if p[0] == "vector":
+                vec[p[1]] = np.array([float(t) for t in p[2:]])
+            elif p[0] == "keep":
+                keep[p[1]] = int(p[2])
+            elif p[0] == "global":
+                glob = int(p[1])
+    return vec, keep, glob
+
+
+def test_worked_example_per_vector_vs_global_mask():
+    vec, keep, glob = _read_golden()
+    X = np.stack([vec["k1"], vec["k2"]])
+    idx, vals = O.topr_select(X, 1)
+    assert idx[0, 0] == keep["k1"] and idx[1, 0] == keep["k2"]
+    assert vals[0, 0] == 10 and vals[1, 0] == 9
+    # The page's global channel matches the energy (sum of squares) reading.
+    assert O.global_mask_energy(X, 1)[0] == glob
+    # Literal var(K', axis 0) on just these two vectors would pick channel 2
+    # (variance 19.36 against 16): a discrepancy recorded, not a failure.
+    assert O.global_mask_variance(X, 1)[0] == 2
+
+
+# ------------------------------------------------------------- top-r ----
+def _brute_topr(x, r):
+    d = len(x)
+    valid = []
+    for S in itertools.combinations(range(d), r):
+        out = [c for c in range(d) if c not in S]
+        ok = all(abs(x[c]) > abs(x[o]) or (abs(x[c]) == abs(x[o]) and c < o)
+                 for c in S for o in out)
+        if ok:
+            valid.append(S)
+    assert len(valid) == 1
+    return list(valid[0])
+
+
+def test_topr_brute_force_small_d_with_ties():
+    rng = np.random.default_rng(2)
+    for _ in range(400):
+        d = int(rng.integers(2, 9))
+        r = int(rng.integers(1, d + 1))
+        x = rng.integers(-3, 4, size=d).astype(np.float64)
+        x[rng.random(d) < 0.2] = -0.0
+        idx, vals = O.topr_select(x, r)
+        want = _brute_topr(x, r)
+        assert list(idx[0]) == want
+        assert np.array_equal(vals[0], x[want])
+
+
+def test_topr_d128_against_python_sort():
+    rng = np.random.default_rng(3)
+    X = O.bf16_round(rng.standard_normal((64, 128)) * np.exp(-0.05 * np.arange(128)))
+    X[:4, :] = 0.0                     # all-zero vectors keep channels 0..r-1
+    X[4, ::2] = X[4, 1::2]             # many exact magnitude ties
+    X[5, 10:20] = -X[5, 10:20]
+    for r in (1, 32, 38, 64, 128):
+        idx, vals = O.topr_select(X, r)
+        for i in range(X.shape[0]):
+            srt = sorted(range(128), key=lambda c: (-abs(X[i, c]), c))
+            assert list(idx[i]) == sorted(srt[:r])
+    idx, _ = O.topr_select(X[:4], 38)
+    assert np.array_equal(idx, np.tile(np.arange(38), (4, 1)))
+
+
+# ---------------------------------------------------------- rotation ----
+def _gen(T, decay, seed, outliers=True):
+    x = synth.lowrank_outlier(T, 128, decay, seed, n_outlier_channels=4 if outliers else 0)
+    return synth.bf16_values(x)
+
+
+def test_rotation_orthogonal_and_preserves_dot_products():
+    K = _gen(2048, 0.9, 11)
+    R, lam = O.rotation_from_keys(K)
+    assert np.allclose(R @ R.T, np.eye(128), atol=1e-12)
+    assert np.all(np.diff(lam) <= 1e-9 * lam[0])
+    q = np.random.default_rng(4).standard_normal((4, 128))
+    Kp = O.rotate(K, R, round_bf16=False)
+    qp = q @ R.T
+    assert np.allclose(qp @ Kp.T, q @ K.T, rtol=0, atol=1e-10)
+    assert np.allclose(np.linalg.norm(Kp, axis=1), np.linalg.norm(K, axis=1), rtol=1e-12)
+
+
+def test_energy_equals_eigenvalue_share_and_closed_form():
+    K = _gen(4096, 0.9, 12)
+    R, lam = O.rotation_from_keys(K)
+    for r in (1, 8, 32, 64):
+        assert abs(O.energy(R, K, r) - lam[:r].sum() / lam.sum()) < 1e-12
+    # Without outliers K^T K ~ T Q diag(s^2) Q^T, so Energy(r) ~ sum_{i<r} s_i^2 / sum s_i^2.
+    s2 = 0.9 ** (2 * np.arange(128))
+    K0 = _gen(20000, 0.9, 13, outliers=False)
+    R0, _ = O.rotation_from_keys(K0)
+    for r in (4, 16, 32):
+        assert abs(O.energy(R0, K0, r) - s2[:r].sum() / s2.sum()) < 0.01
+    s2b = 0.92 ** (2 * np.arange(128))
+    assert abs(s2b[:38].sum() / s2b.sum() - 0.9982) < 1e-3  # the closed form itself
+
+
+# ---------------------------------------------------------- segments ----
+def test_segment_boundaries_and_k_rule():
+    st = O.Strategy(4, 128, 16, [(0, 32, 0), (350, 64, 1), (650, 32, 0)], 0, 100)
+    assert O.n_middle_blocks(10000, st) == 617            # ceil(9868 / 16)
+    assert O.segment_first_blocks(10000, st) == [0, 219, 406]   # ceil(3496/16), ceil(6496/16)
+    assert O.n_select(2040, O.Strategy(4, 128, 16, [(0, 38, 0)], 0, 100)) == 204
+    assert O.n_select(4088, O.Strategy(4, 256, 32, [(0, 38, 0)], 0, 100)) == 409
+    assert O.n_select(16376, O.Strategy(4, 512, 64, [(0, 38, 0)], 0, 50)) == 819
+    assert O.n_select(252, O.Strategy(4, 64, 16, [(0, 32, 0)], 64, 0)) == 64
+    assert O.n_select(3, O.Strategy(4, 64, 16, [(0, 32, 0)], 0, 100)) == 1
+    assert O.n_select(0, O.Strategy(4, 64, 16, [(0, 32, 0)], 0, 100)) == 0
+
+
+def test_sizes_and_overheads_printed_on_the_pages():
+    assert O.meta_overhead(16) == 0.0625                  # Quest keys: 6.25% at block 16
+    assert abs(O.speedup_bound(0.10, 0.30) - 33.333) < 1e-3
+    assert O.packed_bytes_per_token(38) == 228
+    per_layer = (1048576 - 4 - 512) * 8 * O.packed_bytes_per_token(38)
+    assert 1.78 < per_layer / 2 ** 30 < 1.79                  # "about 1.8 GB" per layer
+
+
+# ------------------------------------------------------- cache build ----
+def _cache(T, st, seed, G=4, round_bf16=True, prefill=None, steps=()):
+    K = _gen(T, 0.9, seed)
+    V = _gen(T, 0.9, seed + 1)
+    Rk, _ = O.rotation_from_keys(K)
+    Rv, _ = O.rotation_from_keys(V)
+    c = O.OracleCache(st, T + 8, round_bf16=round_bf16)
+    c.set_rotation(Rk, Rv)
+    t0 = prefill if prefill is not None else T
+    c.append(K[:t0], V[:t0])
+    t = t0
+    for n in steps:
+        c.append(K[t:t + n], V[t:t + n])
+        t += n
+    assert t == T
+    return c, K, V
+
+
+def test_incremental_append_equals_batch_append():
+    st = O.Strategy(4, 64, 16, [(0, 32, 0), (400, 64, 1), (700, 24, 0)], 0, 100)
+    a, _, _ = _cache(1500, st, 20, prefill=1400, steps=(100,))
+    b, _, _ = _cache(1500, st, 20, prefill=1400, steps=(1,) * 37 + (50, 13))
+    assert a.T == b.T == 1500 and a.n_mid == b.n_mid == 1500 - 64 - 4
+    for name in ("Kr", "Vr", "Kt", "Vt", "kidx", "vidx", "kval", "vval", "rtok"):
+        assert np.array_equal(getattr(a, name), getattr(b, name)), name
+    ma, xa = a.meta()
+    mb, xb = b.meta()
+    assert np.array_equal(ma, mb) and np.array_equal(xa, xb)
+    # meta is the min/max of the zero-filled compressed keys of each block
+    for bi in range(a.n_blocks_mid()):
+        lo, hi = a.block_tokens(bi)
+        assert np.array_equal(ma[bi], a.Kt[lo:hi].min(axis=0))
+        assert np.array_equal(xa[bi], a.Kt[lo:hi].max(axis=0))
+    assert list(a.window_positions()) == list(range(1500 - 64, 1500))
+
+
+def test_page_byte_layout():
+    st = O.Strategy(0, 1, 16, [(0, 2, 0)])
+    c = O.OracleCache(st, 64)
+    c.set_rotation(np.eye(128), np.eye(128))
+    K = np.zeros((5, 128))
+    V = np.zeros((5, 128))
+    K[0, 7], K[0, 3], K[0, 100] = 1.5, -2.0, 0.25
+    V[0, 0], V[0, 127] = 3.0, -1.0
+    c.append(K, V)                        # 4 tokens in the middle, 1 in the window
+    pg = c.page_bytes(0)
+    assert pg.size == 6 * 16 * 2
+    kv = pg[:64].view(np.uint16).reshape(16, 2)
+    ki = pg[64:96].reshape(16, 2)
+    vv = pg[96:160].view(np.uint16).reshape(16, 2)
+    vi = pg[160:192].reshape(16, 2)
+    assert list(ki[0]) == [3, 7] and list(O.bits_to_value(kv[0])) == [-2.0, 1.5]
+    assert list(vi[0]) == [0, 127] and list(O.bits_to_value(vv[0])) == [3.0, -1.0]
+    assert list(ki[1]) == [0, 1] and list(kv[1]) == [0, 0]      # all-zero token
+    assert not pg[4 * 2 * 2:64].any() and not ki[4:].any()     # unused slots are zero
+
+
+# ------------------------------------------------------- scoring -------
+def test_block_size_one_score_is_exact_eq12():
+    st = O.Strategy(4, 16, 1, [(0, 32, 0)], 0, 100)
+    c, _, _ = _cache(300, st, 30)
+    q = np.random.default_rng(5).standard_normal((1, 128))
+    per, grp = c.scores(q)
+    qr = c.rotate_query(q)
+    for b in range(c.n_blocks_mid()):
+        lo, hi = c.block_tokens(b)
+        assert abs(grp[b] - O.block_max_exact(qr, c.Kt[lo:hi])) < 1e-12
+
+
+def test_block_score_bounds_every_token_and_head():
+    st = O.Strategy(4, 32, 16, [(0, 38, 0)], 0, 100)
+    c, _, _ = _cache(1200, st, 31)
+    q = np.random.default_rng(6).standard_normal((4, 128))
+    per, grp = c.scores(q)
+    qr = c.rotate_query(q)
+    for b in range(c.n_blocks_mid()):
+        lo, hi = c.block_tokens(b)
+        exact = (c.Kt[lo:hi].astype(np.float64) @ qr.T) / math.sqrt(128)
+        assert np.all(per[:, b] >= exact.max(axis=0) - 1e-12)
+        assert grp[b] == per[:, b].max()
+
+
+def test_topk_brute_force_with_ties():
+    rng = np.random.default_rng(7)
+    for _ in range(300):
+        n = int(rng.integers(1, 40))
+        s = rng.integers(-4, 5, size=n).astype(np.float64)
+        cand = np.sort(rng.choice(n, size=int(rng.integers(1, n + 1)), replace=False))
+        k = int(rng.integers(0, len(cand) + 1))
+        got = O.topk_blocks(s, cand, k)
+        want = sorted(sorted(cand.tolist(), key=lambda b: (-s[b], b))[:k])
+        assert got.tolist() == want
+
+
+# ------------------------------------------------------ attention ------
+@pytest.mark.parametrize("G", [1, 4])
+def test_full_channels_all_blocks_equals_dense_attention(G):
+    st = O.Strategy(4, 40, 16, [(0, 128, 0)], topk_fixed=10 ** 6)
+    c, K, V = _cache(700, st, 40, round_bf16=False, prefill=650, steps=(1,) * 50)
+    q = np.random.default_rng(8).standard_normal((G, 128))
+    ids, _ = c.select(q)
+    assert len(ids) == c.n_blocks_mid()
+    got = c.attention(q, ids)
+    want = O.dense_attention(q, K, V)
+    assert np.allclose(got, want, rtol=0, atol=1e-12 * np.abs(want).max())
+
+
+def test_always_segment_is_attended_without_selection():
+    st = O.Strategy(4, 32, 16, [(0, 128, 0), (300, 128, 1), (600, 128, 0)], topk_fixed=1)
+    c, K, V = _cache(1000, st, 41, round_bf16=False)
+    q = np.random.default_rng(9).standard_normal((1, 128))
+    ids, _ = c.select(q)
+    assert len(ids) == 1 and len(c.always_blocks()) > 0
+    assert not set(ids.tolist()) & set(c.always_blocks().tolist())
+    Kt, _ = c.attend_tokens(ids)
+    assert Kt.shape[0] == 4 + 32 + 16 * (1 + len(c.always_blocks()))
+
+
+# ----------------------------------------------- planted mistakes ------
+def test_pins_catch_planted_mistakes():
+    K = _gen(4096, 0.9, 50)
+    R, lam = O.rotation_from_keys(K)
+    # (a) rotation with R instead of R^T breaks the eigenvalue-share pin
+    Xp = K @ R
+    col = np.sum(Xp * Xp, axis=0)
+    assert abs(col[:8].sum() / col.sum() - lam[:8].sum() / lam.sum()) > 1e-3
+    # (b) un-rotation by R_v^T instead of R_v breaks the dense-attention pin
+    st = O.Strategy(4, 40, 16, [(0, 128, 0)], topk_fixed=10 ** 6)
+    c, Kd, Vd = _cache(500, st, 51, round_bf16=False)
+    q = np.random.default_rng(10).standard_normal((2, 128))
+    ids, _ = c.select(q)
+    Kt, Vt = c.attend_tokens(ids)
+    wrong = O.softmax_attention(c.rotate_query(q), Kt, Vt) @ c.Rv.T
+    assert not np.allclose(wrong, O.dense_attention(q, Kd, Vd), atol=1e-6)
+    # (c) ties toward the higher channel break the brute-force pin
+    x = np.array([1.0, -1.0, 0.5, 1.0])
+    order = np.argsort(-np.abs(x[::-1]), kind="stable")[:2]
+    wrong_idx = sorted((3 - order).tolist())
+    assert wrong_idx != _brute_topr(x, 2)
+    # (d) a min/max swap in the bound breaks the upper-bound pin
+    st = O.Strategy(4, 32, 16, [(0, 38, 0)], 0, 100)
+    c, _, _ = _cache(800, st, 52)
+    qr = c.rotate_query(np.random.default_rng(11).standard_normal((1, 128)))
+    mn, mx = c.meta()
+    wrong_s = np.sum(np.minimum(qr * mn, qr * mx), axis=1) / math.sqrt(128)
+    exact = np.array([O.block_max_exact(qr, c.Kt[slice(*c.block_tokens(b))])
+                      for b in range(c.n_blocks_mid())])
+    assert np.any(wrong_s < exact - 1e-9)
