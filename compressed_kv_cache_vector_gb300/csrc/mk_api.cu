@@ -1,0 +1,487 @@
+// Host side of the C ABI (include/mosaickv.h): configuration checks, arena
+// and workspace layout, per-call validation, the host view of sequence
+// lengths and strategy segments, and kernel launches.  No device memory is
+// allocated here: the caller owns the arena and the workspace.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "mk_internal.cuh"
+
+using mk::CallSeqs;
+using mk::Layout;
+using mk::UnitDesc;
+
+struct mk_ctx {
+  mk_config cfg;
+  Layout L;
+  size_t arena_bytes = 0, ws_bytes = 0;
+  int64_t n_units = 0;
+  std::vector<int32_t> T;            // [layers][max_seqs]
+  std::vector<int32_t> T0;           // prefill length, 0 = not started
+  std::vector<int32_t> firsts;       // [layers][max_seqs][MK_MAX_SEGMENTS]
+  std::vector<uint8_t> rot_set;      // [layers][max_seqs][n_kv]
+  int sel_layer = -1;                // last mk_block_select: layer and sequence list
+  std::vector<int32_t> sel_seqs;
+};
+
+namespace {
+
+constexpr int64_t kAlign = 256;
+inline int64_t align_up(int64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Plan {
+  Layout L;
+  int64_t n_units, units_off, arena_bytes, ws_bytes;
+};
+
+mk_status check_config(const mk_config* c) {
+  if (!c) return MK_EINVAL;
+  if (c->head_dim != MK_HEAD_DIM) return MK_EINVAL;
+  if (c->n_kv_heads < 1 || c->n_q_heads < 1 || c->n_q_heads % c->n_kv_heads) return MK_EINVAL;
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return MK_EINVAL;
+  if (c->n_layers < 1 || c->max_seqs < 1 || c->max_seqs > MK_MAX_CALL_SEQS) return MK_EINVAL;
+  if (c->max_tokens < 1 || c->n_sink < 0 || c->window < 1) return MK_EINVAL;
+  if (c->block != 16 && c->block != 32 && c->block != 64) return MK_EINVAL;
+  if (c->topk_fixed < 0 || c->retain_permille < 0 || c->retain_permille > 1000) return MK_EINVAL;
+  if (c->topk_fixed == 0 && c->retain_permille == 0) return MK_EINVAL;
+  if (c->n_segments < 1 || c->n_segments > MK_MAX_SEGMENTS) return MK_EINVAL;
+  int prev = 0;
+  for (int i = 0; i < c->n_segments; ++i) {
+    const mk_segment& s = c->seg[i];
+    if (s.r < 1 || s.r > MK_HEAD_DIM || (s.always != 0 && s.always != 1) || s.reserved != 0) return MK_EINVAL;
+    if (s.begin_permille < 0 || s.begin_permille > 1000) return MK_EINVAL;
+    if (i == 0 && s.begin_permille != 0) return MK_EINVAL;
+    if (s.begin_permille < prev) return MK_EINVAL;
+    prev = s.begin_permille;
+  }
+  return MK_OK;
+}
+
+Plan make_plan(const mk_config* c) {
+  Plan p{};
+  Layout& L = p.L;
+  L.S = c->n_sink;
+  L.W = c->window;
+  L.B = c->block;
+  L.n_kv = c->n_kv_heads;
+  L.G = c->n_q_heads / c->n_kv_heads;
+  L.max_seqs = c->max_seqs;
+  L.cap_tokens = c->max_tokens;
+  L.n_layers = c->n_layers;
+  L.topk_fixed = c->topk_fixed;
+  L.retain_permille = c->retain_permille;
+  int r_max = 0;
+  for (int i = 0; i < c->n_segments; ++i) r_max = std::max(r_max, (int)c->seg[i].r);
+  L.r_max = r_max;
+  L.nblk_cap = mk::n_mid_blocks(L, c->max_tokens);
+  L.k_max = std::max(1, mk::n_select(L, L.nblk_cap));
+  L.page_stride = (int64_t)6 * L.B * r_max;
+  const int64_t D = MK_HEAD_DIM;
+  int64_t off = 0;
+  L.off_rkt = off; off += D * D * 4;
+  L.off_rvt = off; off += D * D * 4;
+  L.off_rv = off; off += D * D * 4;
+  L.off_sink_k = off; off = align_up(off + std::max<int64_t>(1, L.S) * D * 2);
+  L.off_sink_v = off; off = align_up(off + std::max<int64_t>(1, L.S) * D * 2);
+  L.off_win_k = off; off = align_up(off + (int64_t)L.W * D * 2);
+  L.off_win_v = off; off = align_up(off + (int64_t)L.W * D * 2);
+  L.off_meta = off; off = align_up(off + (int64_t)std::max(1, L.nblk_cap) * 2 * D * 2);
+  L.off_pages = off; off = align_up(off + (int64_t)std::max(1, L.nblk_cap) * L.page_stride);
+  L.unit_stride = off;
+  p.n_units = (int64_t)c->n_layers * c->max_seqs * c->n_kv_heads;
+  p.units_off = align_up(kAlign + p.n_units * (int64_t)sizeof(UnitDesc));
+  p.arena_bytes = p.units_off + p.n_units * L.unit_stride;
+  const int64_t slots = (int64_t)c->max_seqs * c->n_kv_heads;
+  int64_t w = 0;
+  w = align_up(w + slots * L.G * D * 4);                       // qrot
+  w = align_up(w + slots * (int64_t)std::max(1, L.nblk_cap) * 4);  // scores
+  w = align_up(w + slots * MK_MAX_SPLITS * L.G * D * 4);       // part_acc
+  w = align_up(w + slots * MK_MAX_SPLITS * L.G * 2 * 4);       // part_ml
+  w = align_up(w + slots * 4);                                 // counters
+  p.ws_bytes = w;
+  return p;
+}
+
+void bind_pointers(Plan& p, void* arena, void* ws) {
+  Layout& L = p.L;
+  char* a = static_cast<char*>(arena);
+  L.arena = a;
+  L.err = reinterpret_cast<int32_t*>(a);
+  L.desc = reinterpret_cast<UnitDesc*>(a + kAlign);
+  L.units = a + p.units_off;
+  const int64_t D = MK_HEAD_DIM;
+  const int64_t slots = (int64_t)L.max_seqs * L.n_kv;
+  char* w = static_cast<char*>(ws);
+  int64_t o = 0;
+  L.qrot = reinterpret_cast<float*>(w + o); o = align_up(o + slots * L.G * D * 4);
+  L.scores = reinterpret_cast<float*>(w + o); o = align_up(o + slots * (int64_t)std::max(1, L.nblk_cap) * 4);
+  L.part_acc = reinterpret_cast<float*>(w + o); o = align_up(o + slots * MK_MAX_SPLITS * L.G * D * 4);
+  L.part_ml = reinterpret_cast<float*>(w + o); o = align_up(o + slots * MK_MAX_SPLITS * L.G * 2 * 4);
+  L.counters = reinterpret_cast<int32_t*>(w + o);
+}
+
+// Segment rule: segment i >= 1 starts at the first block boundary at or after
+// begin_permille/1000 of the prefill length T0, clamped to [previous start,
+// number of middle blocks at T0]; segment 0 starts at block 0.
+void segment_firsts(const mk_config& c, const Layout& L, int T0, int32_t* out) {
+  const int nb0 = mk::n_mid_blocks(L, T0);
+  int prev = 0;
+  for (int i = 0; i < MK_MAX_SEGMENTS; ++i) {
+    int b = 0;
+    if (i > 0 && i < c.n_segments) {
+      const int64_t pos = (int64_t)c.seg[i].begin_permille * T0 / 1000;
+      const int64_t rel = std::max<int64_t>(0, pos - L.S);
+      b = (int)((rel + L.B - 1) / L.B);
+      b = std::min(std::max(b, prev), nb0);
+    } else if (i >= c.n_segments) {
+      b = prev;
+    }
+    out[i] = b;
+    prev = b;
+  }
+}
+
+UnitDesc host_desc(const mk_ctx* ctx, int layer, int seq) {
+  UnitDesc d{};
+  const size_t i = (size_t)layer * ctx->cfg.max_seqs + seq;
+  d.T = ctx->T[i];
+  d.T0 = ctx->T0[i];
+  d.n_seg = ctx->cfg.n_segments;
+  for (int s = 0; s < MK_MAX_SEGMENTS; ++s) {
+    d.first_block[s] = ctx->firsts[i * MK_MAX_SEGMENTS + s];
+    d.r[s] = s < ctx->cfg.n_segments ? ctx->cfg.seg[s].r : 0;
+    d.always[s] = s < ctx->cfg.n_segments ? ctx->cfg.seg[s].always : 0;
+  }
+  return d;
+}
+
+mk_status check_seqs(const mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids) {
+  if (!ctx || !seq_ids) return MK_EINVAL;
+  if (layer < 0 || layer >= ctx->cfg.n_layers) return MK_EINVAL;
+  if (n_seqs < 1 || n_seqs > MK_MAX_CALL_SEQS || n_seqs > ctx->cfg.max_seqs) return MK_EINVAL;
+  std::vector<uint8_t> seen(ctx->cfg.max_seqs, 0);
+  for (int i = 0; i < n_seqs; ++i) {
+    const int s = seq_ids[i];
+    if (s < 0 || s >= ctx->cfg.max_seqs || seen[s]) return MK_EINVAL;
+    seen[s] = 1;
+  }
+  return MK_OK;
+}
+
+inline mk_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MK_OK : MK_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mk_status_str(mk_status s) {
+  switch (s) {
+    case MK_OK: return "ok";
+    case MK_EINVAL: return "invalid argument";
+    case MK_ENOMEM: return "buffer too small or capacity exceeded";
+    case MK_ESTATE: return "call out of order";
+    case MK_ECUDA: return "CUDA runtime error";
+    case MK_EDEVICE: return "device error word set";
+    case MK_ETIMEOUT: return "device wait timed out";
+    case MK_ENOTSUP: return "not supported";
+  }
+  return "unknown status";
+}
+
+mk_status mk_arena_bytes(const mk_config* cfg, size_t* bytes) {
+  mk_status st = check_config(cfg);
+  if (st != MK_OK || !bytes) return st != MK_OK ? st : MK_EINVAL;
+  *bytes = (size_t)make_plan(cfg).arena_bytes;
+  return MK_OK;
+}
+
+mk_status mk_workspace_bytes(const mk_config* cfg, size_t* bytes) {
+  mk_status st = check_config(cfg);
+  if (st != MK_OK || !bytes) return st != MK_OK ? st : MK_EINVAL;
+  *bytes = (size_t)make_plan(cfg).ws_bytes;
+  return MK_OK;
+}
+
+mk_status mk_max_select(const mk_config* cfg, int32_t* k_max) {
+  mk_status st = check_config(cfg);
+  if (st != MK_OK || !k_max) return st != MK_OK ? st : MK_EINVAL;
+  *k_max = make_plan(cfg).L.k_max;
+  return MK_OK;
+}
+
+mk_status mk_create(const mk_config* cfg, void* arena, size_t arena_bytes, void* workspace,
+                    size_t workspace_bytes, mk_ctx** out) {
+  mk_status st = check_config(cfg);
+  if (st != MK_OK) return st;
+  if (!arena || !workspace || !out) return MK_EINVAL;
+  if (((uintptr_t)arena % kAlign) || ((uintptr_t)workspace % kAlign)) return MK_EINVAL;
+  Plan p = make_plan(cfg);
+  if ((int64_t)arena_bytes < p.arena_bytes || (int64_t)workspace_bytes < p.ws_bytes) return MK_ENOMEM;
+  int r_min = MK_HEAD_DIM;
+  for (int i = 0; i < cfg->n_segments; ++i) r_min = std::min(r_min, (int)cfg->seg[i].r);
+  if (mk::attn_plan(p.L, r_min) == 0) return MK_ENOTSUP;
+  bind_pointers(p, arena, workspace);
+  mk_ctx* ctx = new (std::nothrow) mk_ctx();
+  if (!ctx) return MK_ENOMEM;
+  ctx->cfg = *cfg;
+  ctx->L = p.L;
+  ctx->arena_bytes = arena_bytes;
+  ctx->ws_bytes = workspace_bytes;
+  ctx->n_units = p.n_units;
+  const size_t ls = (size_t)cfg->n_layers * cfg->max_seqs;
+  ctx->T.assign(ls, 0);
+  ctx->T0.assign(ls, 0);
+  ctx->firsts.assign(ls * MK_MAX_SEGMENTS, 0);
+  ctx->rot_set.assign(ls * cfg->n_kv_heads, 0);
+  cudaError_t e = cudaMemset(arena, 0, (size_t)p.units_off);
+  if (e == cudaSuccess) e = cudaMemset(ctx->L.counters, 0, sizeof(int32_t) * cfg->max_seqs * cfg->n_kv_heads);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    delete ctx;
+    return MK_ECUDA;
+  }
+  *out = ctx;
+  return MK_OK;
+}
+
+mk_status mk_destroy(mk_ctx* ctx) {
+  delete ctx;
+  return MK_OK;
+}
+
+mk_status mk_set_rotation(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, const float* Rk,
+                          const float* Rv, mk_stream stream) {
+  if (!ctx || !Rk || !Rv) return MK_EINVAL;
+  if (layer < 0 || layer >= ctx->cfg.n_layers || seq < 0 || seq >= ctx->cfg.max_seqs || kv_head < 0 ||
+      kv_head >= ctx->cfg.n_kv_heads)
+    return MK_EINVAL;
+  const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq;
+  if (ctx->T[ls] != 0) return MK_ESTATE;
+  const int D = MK_HEAD_DIM;
+  std::vector<float> buf((size_t)3 * D * D);
+  for (int i = 0; i < D; ++i)
+    for (int j = 0; j < D; ++j) {
+      buf[(size_t)j * D + i] = Rk[(size_t)i * D + j];                 // R_k^T
+      buf[(size_t)D * D + (size_t)j * D + i] = Rv[(size_t)i * D + j];  // R_v^T
+      buf[(size_t)2 * D * D + (size_t)i * D + j] = Rv[(size_t)i * D + j];
+    }
+  const int64_t u = mk::unit_index(ctx->L, layer, seq, kv_head);
+  char* dst = ctx->L.units + u * ctx->L.unit_stride + ctx->L.off_rkt;
+  cudaError_t e = cudaMemcpyAsync(dst, buf.data(), buf.size() * sizeof(float), cudaMemcpyHostToDevice,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return MK_ECUDA;
+  ctx->rot_set[ls * ctx->cfg.n_kv_heads + kv_head] = 1;
+  return MK_OK;
+}
+
+mk_status mk_append_compress(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                             const int32_t* n_new, const void* k, const void* v, mk_stream stream) {
+  mk_status st = check_seqs(ctx, layer, n_seqs, seq_ids);
+  if (st != MK_OK) return st;
+  if (!n_new) return MK_EINVAL;
+  int64_t total = 0;
+  int max_new = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    if (n_new[i] < 0) return MK_EINVAL;
+    total += n_new[i];
+    max_new = std::max(max_new, (int)n_new[i]);
+    const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq_ids[i];
+    if ((int64_t)ctx->T[ls] + n_new[i] > ctx->cfg.max_tokens) return MK_ENOMEM;
+    for (int h = 0; h < ctx->cfg.n_kv_heads; ++h)
+      if (!ctx->rot_set[ls * ctx->cfg.n_kv_heads + h]) return MK_ESTATE;
+  }
+  if (total == 0) return MK_OK;
+  if (!k || !v || total > INT32_MAX) return MK_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  CallSeqs* cs = new (std::nothrow) CallSeqs();
+  if (!cs) return MK_ENOMEM;
+  cs->n = n_seqs;
+  int row = 0, tiles = 0;
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < n_seqs; ++i) {
+    const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq_ids[i];
+    cs->seq[i] = seq_ids[i];
+    cs->n_new[i] = n_new[i];
+    cs->row_off[i] = row;
+    cs->T_old[i] = ctx->T[ls];
+    cs->tile_off[i] = tiles;
+    row += n_new[i];
+    tiles += mk::n_tiles(ctx->T[ls], ctx->T[ls] + n_new[i], ctx->L.S);
+    if (ctx->T0[ls] == 0 && n_new[i] > 0) {
+      ctx->T0[ls] = n_new[i];
+      segment_firsts(ctx->cfg, ctx->L, n_new[i], &ctx->firsts[ls * MK_MAX_SEGMENTS]);
+      if (e == cudaSuccess) e = mk::launch_init_desc(ctx->L, layer, seq_ids[i], host_desc(ctx, layer, seq_ids[i]), s);
+    }
+  }
+  cs->tile_off[n_seqs] = tiles;
+  const uint16_t* kk = static_cast<const uint16_t*>(k);
+  const uint16_t* vv = static_cast<const uint16_t*>(v);
+  if (e == cudaSuccess) {
+    if (max_new <= mk::kSmallAppend) {
+      e = mk::launch_append_small(ctx->L, layer, *cs, kk, vv, 0, s);
+    } else {
+      e = mk::launch_append_small(ctx->L, layer, *cs, kk, vv, 1, s);
+      if (e == cudaSuccess && tiles > 0) e = mk::launch_append_bulk(ctx->L, layer, *cs, kk, vv, tiles, s);
+    }
+  }
+  delete cs;
+  if (e != cudaSuccess) return MK_ECUDA;
+  for (int i = 0; i < n_seqs; ++i) ctx->T[(size_t)layer * ctx->cfg.max_seqs + seq_ids[i]] += n_new[i];
+  return MK_OK;
+}
+
+mk_status mk_block_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids, const void* q,
+                          int32_t* ids, int32_t* n_sel, float* scores, mk_stream stream) {
+  mk_status st = check_seqs(ctx, layer, n_seqs, seq_ids);
+  if (st != MK_OK) return st;
+  if (!q || !ids || !n_sel) return MK_EINVAL;
+  CallSeqs* cs = new (std::nothrow) CallSeqs();
+  if (!cs) return MK_ENOMEM;
+  cs->n = n_seqs;
+  int max_nblk = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq_ids[i];
+    if (ctx->T[ls] == 0) {
+      delete cs;
+      return MK_ESTATE;
+    }
+    cs->seq[i] = seq_ids[i];
+    cs->T_old[i] = ctx->T[ls];
+    max_nblk = std::max(max_nblk, mk::n_mid_blocks(ctx->L, ctx->T[ls]));
+  }
+  cudaError_t e = mk::launch_block_select(ctx->L, layer, *cs, static_cast<const uint16_t*>(q), ids, n_sel, scores,
+                                          std::max(1, max_nblk), (cudaStream_t)stream);
+  delete cs;
+  if (e != cudaSuccess) return MK_ECUDA;
+  ctx->sel_layer = layer;
+  ctx->sel_seqs.assign(seq_ids, seq_ids + n_seqs);
+  return MK_OK;
+}
+
+mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids, const int32_t* ids,
+                         const int32_t* n_sel, void* out, mk_stream stream) {
+  mk_status st = check_seqs(ctx, layer, n_seqs, seq_ids);
+  if (st != MK_OK) return st;
+  if (!ids || !n_sel || !out) return MK_EINVAL;
+  if (ctx->sel_layer != layer || (int)ctx->sel_seqs.size() != n_seqs ||
+      !std::equal(ctx->sel_seqs.begin(), ctx->sel_seqs.end(), seq_ids))
+    return MK_ESTATE;
+  CallSeqs* cs = new (std::nothrow) CallSeqs();
+  if (!cs) return MK_ENOMEM;
+  cs->n = n_seqs;
+  for (int i = 0; i < n_seqs; ++i) cs->seq[i] = seq_ids[i];
+  const int cluster = mk::attn_cluster_size(n_seqs * ctx->cfg.n_kv_heads);
+  cudaError_t e = mk::launch_decode_attn(ctx->L, layer, *cs, ids, n_sel, static_cast<uint16_t*>(out), cluster,
+                                         (cudaStream_t)stream);
+  delete cs;
+  return cuda_status(e);
+}
+
+mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T, const void* q, const void* K,
+                               const void* V, int64_t t_stride, void* out, mk_stream stream) {
+  if (!ctx || !T || !q || !K || !V || !out) return MK_EINVAL;
+  if (n_seqs < 1 || n_seqs > ctx->cfg.max_seqs || t_stride < 1) return MK_EINVAL;
+  CallSeqs* cs = new (std::nothrow) CallSeqs();
+  if (!cs) return MK_ENOMEM;
+  cs->n = n_seqs;
+  for (int i = 0; i < n_seqs; ++i) {
+    if (T[i] < 1 || T[i] > t_stride) {
+      delete cs;
+      return MK_EINVAL;
+    }
+    cs->seq[i] = i;
+    cs->T_old[i] = T[i];
+  }
+  const int cluster = mk::attn_cluster_size(n_seqs * ctx->cfg.n_kv_heads);
+  cudaError_t e = mk::launch_dense_attn(ctx->L, *cs, static_cast<const uint16_t*>(q),
+                                        static_cast<const uint16_t*>(K), static_cast<const uint16_t*>(V), t_stride,
+                                        static_cast<uint16_t*>(out), cluster, (cudaStream_t)stream);
+  delete cs;
+  return cuda_status(e);
+}
+
+mk_status mk_gram(const void* x, int64_t n_rows, int64_t row_stride, float* gram, mk_stream stream) {
+  if (!x || !gram || n_rows < 1 || row_stride < MK_HEAD_DIM) return MK_EINVAL;
+  return cuda_status(mk::launch_gram(static_cast<const uint16_t*>(x), n_rows, row_stride, gram,
+                                     (cudaStream_t)stream));
+}
+
+mk_status mk_poll_error(mk_ctx* ctx, int32_t* detail) {
+  if (!ctx) return MK_EINVAL;
+  int32_t w[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(w, ctx->L.err, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return MK_ECUDA;
+  if (detail) *detail = w[1];
+  return w[0] == 0 ? MK_OK : (mk_status)w[0];
+}
+
+mk_status mk_clear_error(mk_ctx* ctx) {
+  if (!ctx) return MK_EINVAL;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemset(ctx->L.err, 0, 4 * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return cuda_status(e);
+}
+
+mk_status mk_sync_state(mk_ctx* ctx) {
+  if (!ctx) return MK_EINVAL;
+  std::vector<UnitDesc> d((size_t)ctx->n_units);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(d.data(), ctx->L.desc, d.size() * sizeof(UnitDesc), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return MK_ECUDA;
+  for (int l = 0; l < ctx->cfg.n_layers; ++l)
+    for (int s = 0; s < ctx->cfg.max_seqs; ++s) {
+      const size_t ls = (size_t)l * ctx->cfg.max_seqs + s;
+      if (ctx->T0[ls] > 0) ctx->T[ls] = d[(size_t)mk::unit_index(ctx->L, l, s, 0)].T;
+    }
+  return MK_OK;
+}
+
+mk_status mk_seq_length(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t* T) {
+  if (!ctx || !T || layer < 0 || layer >= ctx->cfg.n_layers || seq < 0 || seq >= ctx->cfg.max_seqs)
+    return MK_EINVAL;
+  *T = ctx->T[(size_t)layer * ctx->cfg.max_seqs + seq];
+  return MK_OK;
+}
+
+mk_status mk_layout(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, mk_layout_info* out) {
+  if (!ctx || !out || layer < 0 || layer >= ctx->cfg.n_layers || seq < 0 || seq >= ctx->cfg.max_seqs ||
+      kv_head < 0 || kv_head >= ctx->cfg.n_kv_heads)
+    return MK_EINVAL;
+  const Layout& L = ctx->L;
+  const int64_t base = (L.units - L.arena) + mk::unit_index(L, layer, seq, kv_head) * L.unit_stride;
+  std::memset(out, 0, sizeof(*out));
+  out->rkt = base + L.off_rkt;
+  out->rvt = base + L.off_rvt;
+  out->rv = base + L.off_rv;
+  out->sink_k = base + L.off_sink_k;
+  out->sink_v = base + L.off_sink_v;
+  out->win_k = base + L.off_win_k;
+  out->win_v = base + L.off_win_v;
+  out->meta = base + L.off_meta;
+  out->pages = base + L.off_pages;
+  out->page_stride = L.page_stride;
+  out->nblk_cap = L.nblk_cap;
+  const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq;
+  out->T = ctx->T[ls];
+  for (int s = 0; s < MK_MAX_SEGMENTS; ++s) out->seg_first_block[s] = ctx->firsts[ls * MK_MAX_SEGMENTS + s];
+  out->n_segments = ctx->cfg.n_segments;
+  return MK_OK;
+}
+
+mk_status mk_record_event(void* event, mk_stream stream) {
+  if (!event) return MK_EINVAL;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing((cudaStream_t)stream, &cap);
+  if (e != cudaSuccess) return MK_ECUDA;
+  const unsigned flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+  return cuda_status(cudaEventRecordWithFlags((cudaEvent_t)event, (cudaStream_t)stream, flags));
+}
+
+}  // extern "C"

@@ -1,0 +1,379 @@
+// Append + compress: rotate new K/V vectors into the head's basis, keep sink
+// and window tokens dense, and compress each token that leaves the window
+// into its middle block's packed page (per-vector top-r) while updating the
+// block's min/max keys.
+//
+// Method: "MosaicKV：...阅读笔记" (zhongzhuzhou.org), Eq. (7)/(8) for the
+// rotation of each new token, Eq. (9) and Algorithm 1 for the per-vector
+// top-r selection; "MosaicKV: Serving Long-Context LLM with Dynamic Two-D KV
+// Cache Compression" (paperlayer.ai), sec. 4.2 stage 1 and sec. 5.1 (packed
+// contiguous storage) and sec. 5.2 (prefill encoding of K, V and block keys).
+#include "mk_internal.cuh"
+
+namespace mk {
+
+// Per-vector top-r of 128 bf16 magnitudes held 4 per lane (channels
+// 4*lane .. 4*lane+3).  Keeps the r largest magnitudes, ties to the lower
+// channel.  Returns this lane's keep bits; rank0 receives the packed position
+// (ascending channel order) of the lane's first kept channel.
+//
+// The r-th largest magnitude t is found by a bitwise search from the most
+// significant bit (the largest t with #{m >= t} >= r); all m > t are kept and
+// the r - #{m > t} lowest channels with m == t.
+__device__ __forceinline__ unsigned warp_topr(const uint32_t m[4], int r, int lane, int& rank0) {
+  uint32_t t = 0;
+#pragma unroll
+  for (int bit = 14; bit >= 0; --bit) {
+    const uint32_t cand = t | (1u << bit);
+    const unsigned c = (unsigned)(m[0] >= cand) + (unsigned)(m[1] >= cand) +
+                       (unsigned)(m[2] >= cand) + (unsigned)(m[3] >= cand);
+    if ((int)__reduce_add_sync(FULL, c) >= r) t = cand;
+  }
+  const unsigned gt = (unsigned)(m[0] > t) + (unsigned)(m[1] > t) + (unsigned)(m[2] > t) + (unsigned)(m[3] > t);
+  const unsigned eq = (unsigned)(m[0] == t) + (unsigned)(m[1] == t) + (unsigned)(m[2] == t) + (unsigned)(m[3] == t);
+  const int need = r - (int)__reduce_add_sync(FULL, gt);
+  int run = warp_excl_scan((int)eq, lane);
+  unsigned keep = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (m[i] > t) {
+      keep |= 1u << i;
+    } else if (m[i] == t) {
+      if (run < need) keep |= 1u << i;
+      ++run;
+    }
+  }
+  rank0 = warp_excl_scan(__popc(keep), lane);
+  return keep;
+}
+
+// Compresses one rotated vector (128 bf16 words at `row`) of middle position
+// `pos` into its page; for a key also folds it into the block's min/max.
+// Called by one full warp.  Returns this lane's keep bits.
+__device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc& ud, char* base, int pos,
+                                                 const uint16_t* row, int is_v, int lane,
+                                                 bool update_meta) {
+  const int m = pos - L.S;
+  const int b = m / L.B;
+  const int t = m - b * L.B;
+  const int r = ud.r[seg_of_block(ud, b)];
+  char* page = base + L.off_pages + (int64_t)b * L.page_stride;
+  const int Br = L.B * r;
+  uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? 3 * Br : 0));
+  uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? 5 * Br : 2 * Br));
+  const uint2 raw = *reinterpret_cast<const uint2*>(row + 4 * lane);
+  uint16_t v[4] = {(uint16_t)(raw.x & 0xffff), (uint16_t)(raw.x >> 16), (uint16_t)(raw.y & 0xffff),
+                   (uint16_t)(raw.y >> 16)};
+  uint32_t mag[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) mag[i] = v[i] & 0x7fffu;
+  int rank;
+  const unsigned keep = warp_topr(mag, r, lane, rank);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (keep >> i & 1u) {
+      val[t * r + rank] = v[i];
+      idx[t * r + rank] = (uint8_t)(4 * lane + i);
+      ++rank;
+    }
+  }
+  if (update_meta) {
+    uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta) + (int64_t)b * 2 * D;
+    uint2 omn = make_uint2(0, 0), omx = make_uint2(0, 0);
+    if (t != 0) {
+      omn = *reinterpret_cast<const uint2*>(meta + 4 * lane);
+      omx = *reinterpret_cast<const uint2*>(meta + D + 4 * lane);
+    }
+    const uint16_t pmn[4] = {(uint16_t)(omn.x & 0xffff), (uint16_t)(omn.x >> 16), (uint16_t)(omn.y & 0xffff),
+                             (uint16_t)(omn.y >> 16)};
+    const uint16_t pmx[4] = {(uint16_t)(omx.x & 0xffff), (uint16_t)(omx.x >> 16), (uint16_t)(omx.y & 0xffff),
+                             (uint16_t)(omx.y >> 16)};
+    uint16_t nmn[4], nmx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float kt = (keep >> i & 1u) ? bf2f(v[i]) : 0.0f;
+      float lo = kt, hi = kt;
+      if (t != 0) {
+        lo = fminf(bf2f(pmn[i]), kt);
+        hi = fmaxf(bf2f(pmx[i]), kt);
+      }
+      nmn[i] = f2bf(lo);
+      nmx[i] = f2bf(hi);
+    }
+    *reinterpret_cast<uint2*>(meta + 4 * lane) =
+        make_uint2((uint32_t)nmn[0] | ((uint32_t)nmn[1] << 16), (uint32_t)nmn[2] | ((uint32_t)nmn[3] << 16));
+    *reinterpret_cast<uint2*>(meta + D + 4 * lane) =
+        make_uint2((uint32_t)nmx[0] | ((uint32_t)nmx[1] << 16), (uint32_t)nmx[2] | ((uint32_t)nmx[3] << 16));
+  }
+  return keep;
+}
+
+__global__ void k_init_desc(Layout L, int layer, int seq, UnitDesc d) {
+  const int kvh = threadIdx.x;
+  if (kvh < L.n_kv) L.desc[unit_index(L, layer, seq, kvh)] = d;
+}
+
+// Decode-path append: one CTA per (sequence, kv head).  Evicts the tokens
+// that leave the window into the middle, then rotates and stores the (few)
+// new tokens.  Reads and advances the device-resident length, so a captured
+// CUDA graph of it stays valid across replays.
+__global__ void __launch_bounds__(256) k_append_small(Layout L, int layer, CallSeqs cs,
+                                                      const uint16_t* __restrict__ kin,
+                                                      const uint16_t* __restrict__ vin, int evict_only) {
+  const int ci = blockIdx.x / L.n_kv;
+  const int kvh = blockIdx.x - ci * L.n_kv;
+  const int seq = cs.seq[ci];
+  const int n = cs.n_new[ci];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t u = unit_index(L, layer, seq, kvh);
+  __shared__ UnitDesc ud;
+  __shared__ float xs[kSmallAppend][2][D];
+  __shared__ __align__(16) uint16_t rot[kSmallAppend][2][D];
+  __shared__ int s_abort;
+  if (tid == 0) {
+    s_abort = has_error(L);
+    ud = L.desc[u];
+  }
+  __syncthreads();
+  if (s_abort) return;
+  const int T_old = ud.T;
+  const int T_new = T_old + n;
+  if (T_new > L.cap_tokens || (!evict_only && n > kSmallAppend)) {
+    if (tid == 0) set_error(L, ERR_CAPACITY, (int32_t)u, T_new);
+    return;
+  }
+  char* base = unit_base(L, u);
+  const int S = L.S, W = L.W;
+  uint16_t* win_k = reinterpret_cast<uint16_t*>(base + L.off_win_k);
+  uint16_t* win_v = reinterpret_cast<uint16_t*>(base + L.off_win_v);
+  // Stage R_k^T and R_v^T (contiguous in the unit) into shared memory while
+  // the eviction below runs.
+  extern __shared__ __align__(16) float Rs[];   // [2][128*128] when rotating
+  if (!evict_only && n > 0) {
+    const float4* src = reinterpret_cast<const float4*>(base + L.off_rkt);
+    for (int i = tid; i < 2 * D * D / 4; i += blockDim.x) cp_async16(reinterpret_cast<float4*>(Rs) + i, src + i);
+    cp_async_commit();
+  }
+
+  // Phase A: window tokens that leave the window, in position order.
+  const int e_lo = max(S, T_old - W), e_hi = min(T_old, T_new - W);
+  if (warp < 2) {
+    for (int e = e_lo; e < e_hi; ++e) {
+      const int slot = (e - S) % W;
+      const uint16_t* row = (warp == 0 ? win_k : win_v) + (int64_t)slot * D;
+      compress_vec(L, ud, base, e, row, warp, lane, warp == 0);
+    }
+  }
+  __syncthreads();
+  if (evict_only) {
+    if (tid == 0) L.desc[u].T = T_new;
+    return;
+  }
+
+  // Phase B: rotate the new tokens (k' = k R_k^T, v' = v R_v^T).
+  const int64_t in_stride = (int64_t)L.n_kv * D;
+  for (int i = tid; i < n * 2 * D; i += blockDim.x) {
+    const int t = i / (2 * D), w = (i / D) & 1, c = i % D;
+    const uint16_t* src = (w == 0 ? kin : vin) + (int64_t)(cs.row_off[ci] + t) * in_stride + (int64_t)kvh * D;
+    xs[t][w][c] = bf2f(src[c]);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  {
+    const int w = tid >> 7, ch = tid & 127;
+    const float* RT = Rs + w * D * D;
+    float acc[kSmallAppend];
+#pragma unroll
+    for (int i = 0; i < kSmallAppend; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < D; ++j) {
+      const float rr = RT[j * D + ch];
+#pragma unroll
+      for (int i = 0; i < kSmallAppend; ++i)
+        if (i < n) acc[i] = fmaf(xs[i][w][j], rr, acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < kSmallAppend; ++i)
+      if (i < n) rot[i][w][ch] = f2bf(acc[i]);
+  }
+  __syncthreads();
+
+  // Route: sinks and window dense, the rest compressed in position order.
+  uint16_t* sink_k = reinterpret_cast<uint16_t*>(base + L.off_sink_k);
+  uint16_t* sink_v = reinterpret_cast<uint16_t*>(base + L.off_sink_v);
+  for (int i = 0; i < n; ++i) {
+    const int p = T_old + i;
+    if (p < S || p >= T_new - W) {
+      uint16_t* dk = p < S ? sink_k + (int64_t)p * D : win_k + (int64_t)((p - S) % W) * D;
+      uint16_t* dv = p < S ? sink_v + (int64_t)p * D : win_v + (int64_t)((p - S) % W) * D;
+      if (tid < D) dk[tid] = rot[i][0][tid];
+      else dv[tid - D] = rot[i][1][tid - D];
+    } else if (warp < 2) {
+      compress_vec(L, ud, base, p, rot[i][warp], warp, lane, warp == 0);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) L.desc[u].T = T_new;
+}
+
+// Bulk append of new tokens (prefill): tiles of up to 64 positions aligned so
+// that every middle block lies in one tile; grid (tiles, kv heads).  The
+// length was already advanced by the eviction pass that precedes it.
+__global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSeqs cs,
+                                                     const uint16_t* __restrict__ kin,
+                                                     const uint16_t* __restrict__ vin) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* Rs = reinterpret_cast<float*>(smem);                          // [128][128]
+  float* xs = Rs + D * D;                                              // [64][128]
+  uint16_t* rot = reinterpret_cast<uint16_t*>(xs + kTileTokens * D);   // [2][64][128]
+  uint8_t* keepk = reinterpret_cast<uint8_t*>(rot + 2 * kTileTokens * D);  // [64][32] nibbles
+  __shared__ UnitDesc ud;
+  __shared__ int s_ci, s_abort;
+
+  const int tile = blockIdx.x, kvh = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    int lo = 0, hi = cs.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cs.tile_off[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    s_ci = lo;
+    s_abort = has_error(L);
+    ud = L.desc[unit_index(L, layer, cs.seq[lo], kvh)];
+  }
+  __syncthreads();
+  if (s_abort) return;
+  const int ci = s_ci;
+  const int seq = cs.seq[ci];
+  const int64_t u = unit_index(L, layer, seq, kvh);
+  const int T_old = cs.T_old[ci], T_new = T_old + cs.n_new[ci];
+  const int S = L.S, W = L.W, B = L.B;
+  const int j = tile - cs.tile_off[ci];
+  const int f = tile_first_boundary(T_old, S);
+  const int lo = j == 0 ? T_old : f + (j - 1) * kTileTokens;
+  const int hi = min(T_new, j == 0 ? f : lo + kTileTokens);
+  const int nt = hi - lo;
+  if (nt <= 0) return;
+  char* base = unit_base(L, u);
+  const int64_t in_stride = (int64_t)L.n_kv * D;
+
+  for (int w = 0; w < 2; ++w) {
+    __syncthreads();
+    const float4* RT = reinterpret_cast<const float4*>(base + (w == 0 ? L.off_rkt : L.off_rvt));
+    for (int i = tid; i < D * D / 4; i += blockDim.x) reinterpret_cast<float4*>(Rs)[i] = __ldg(RT + i);
+    const uint16_t* src = (w == 0 ? kin : vin);
+    for (int i = tid; i < nt * D; i += blockDim.x) {
+      const int t = i / D, c = i % D;
+      xs[t * D + c] = bf2f(src[(int64_t)(cs.row_off[ci] + (lo - T_old) + t) * in_stride + (int64_t)kvh * D + c]);
+    }
+    __syncthreads();
+    const int ch = tid & 127, th = tid >> 7;
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+    for (int jj = 0; jj < D; jj += 4) {
+      const float r0 = Rs[(jj + 0) * D + ch], r1 = Rs[(jj + 1) * D + ch];
+      const float r2 = Rs[(jj + 2) * D + ch], r3 = Rs[(jj + 3) * D + ch];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(xs + (th * 32 + i) * D + jj);
+        float a = acc[i];
+        a = fmaf(x.x, r0, a);
+        a = fmaf(x.y, r1, a);
+        a = fmaf(x.z, r2, a);
+        a = fmaf(x.w, r3, a);
+        acc[i] = a;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int t = th * 32 + i;
+      if (t < nt) rot[(w * kTileTokens + t) * D + ch] = f2bf(acc[i]);
+    }
+  }
+  __syncthreads();
+
+  uint16_t* sink_k = reinterpret_cast<uint16_t*>(base + L.off_sink_k);
+  uint16_t* sink_v = reinterpret_cast<uint16_t*>(base + L.off_sink_v);
+  uint16_t* win_k = reinterpret_cast<uint16_t*>(base + L.off_win_k);
+  uint16_t* win_v = reinterpret_cast<uint16_t*>(base + L.off_win_v);
+  for (int t = warp; t < nt; t += 8) {
+    const int p = lo + t;
+    const uint16_t* rk = rot + t * D;
+    const uint16_t* rv = rot + (kTileTokens + t) * D;
+    if (p < S || p >= T_new - W) {
+      uint16_t* dk = p < S ? sink_k + (int64_t)p * D : win_k + (int64_t)((p - S) % W) * D;
+      uint16_t* dv = p < S ? sink_v + (int64_t)p * D : win_v + (int64_t)((p - S) % W) * D;
+      reinterpret_cast<uint2*>(dk)[lane] = reinterpret_cast<const uint2*>(rk)[lane];
+      reinterpret_cast<uint2*>(dv)[lane] = reinterpret_cast<const uint2*>(rv)[lane];
+    } else {
+      const unsigned kk = compress_vec(L, ud, base, p, rk, 0, lane, false);
+      compress_vec(L, ud, base, p, rv, 1, lane, false);
+      keepk[t * 32 + lane] = (uint8_t)kk;
+    }
+  }
+  __syncthreads();
+
+  // Block min/max over the zero-filled compressed keys of this tile's middle tokens.
+  const int mlo = max(lo, S), mhi = min(hi, T_new - W);
+  if (mlo < mhi && tid < D) {
+    const int c = tid;
+    uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta);
+    const int b0 = (mlo - S) / B, b1 = (mhi - 1 - S) / B;
+    for (int b = b0; b <= b1; ++b) {
+      const int blo = S + b * B;
+      const int st = max(blo, mlo), en = min(blo + B, mhi);
+      float mn = 0.f, mx = 0.f;
+      bool have = st > blo;
+      if (have) {
+        mn = bf2f(meta[(int64_t)b * 2 * D + c]);
+        mx = bf2f(meta[(int64_t)b * 2 * D + D + c]);
+      }
+      for (int p = st; p < en; ++p) {
+        const int t = p - lo;
+        const bool kept = (keepk[t * 32 + (c >> 2)] >> (c & 3)) & 1;
+        const float kt = kept ? bf2f(rot[t * D + c]) : 0.0f;
+        if (!have) { mn = kt; mx = kt; have = true; }
+        else { mn = fminf(mn, kt); mx = fmaxf(mx, kt); }
+      }
+      meta[(int64_t)b * 2 * D + c] = f2bf(mn);
+      meta[(int64_t)b * 2 * D + D + c] = f2bf(mx);
+    }
+  }
+}
+
+cudaError_t launch_init_desc(const Layout& L, int layer, int seq, const UnitDesc& d, cudaStream_t s) {
+  k_init_desc<<<1, 32 * ((L.n_kv + 31) / 32), 0, s>>>(L, layer, seq, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
+                                const uint16_t* v, int evict_only, cudaStream_t s) {
+  const size_t smem = evict_only ? 0 : (size_t)2 * D * D * sizeof(float);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_append_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         2 * D * D * (int)sizeof(float));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  k_append_small<<<cs.n * L.n_kv, 256, smem, s>>>(L, layer, cs, k, v, evict_only);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
+                               const uint16_t* v, int total_tiles, cudaStream_t s) {
+  const size_t smem = (size_t)D * D * 4 + (size_t)kTileTokens * D * 4 + 2 * (size_t)kTileTokens * D * 2 +
+                      (size_t)kTileTokens * 32;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_append_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(total_tiles, L.n_kv);
+  k_append_bulk<<<grid, 256, smem, s>>>(L, layer, cs, k, v);
+  return cudaGetLastError();
+}
+
+}  // namespace mk

@@ -1,0 +1,193 @@
+// Internal declarations shared by the kernels and the host layer of
+// libmosaickv.so.  Not part of the public ABI (include/mosaickv.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/mosaickv.h"
+
+namespace mk {
+
+constexpr int D = MK_HEAD_DIM;
+constexpr int kDenseChunk = 16;        // tokens per dense work item in attention
+constexpr int kTileTokens = 64;        // tokens per bulk-append tile
+constexpr int kSmallAppend = 16;       // largest per-sequence append handled by the decode kernel
+constexpr uint32_t FULL = 0xffffffffu;
+
+// Device error codes (detail word); the status word holds MK_EDEVICE.
+enum DevErr : int32_t {
+  ERR_NONE = 0,
+  ERR_CAPACITY = 1,    // append past max_tokens
+  ERR_BAD_BLOCK = 2,   // selected block id out of range
+  ERR_BAD_NSEL = 3,    // n_sel larger than the ids row
+  ERR_NO_ROTATION = 4,
+};
+
+// Per (layer, seq, kv head) state kept on the device (64 bytes).
+struct UnitDesc {
+  int32_t T;                        // tokens held
+  int32_t T0;                       // prefill length (fixes the segments)
+  int32_t n_seg;
+  int32_t rot_set;
+  int32_t first_block[MK_MAX_SEGMENTS];
+  int32_t r[MK_MAX_SEGMENTS];
+  int32_t always[MK_MAX_SEGMENTS];
+};
+static_assert(sizeof(UnitDesc) == 64, "UnitDesc is 64 bytes");
+
+// Everything a kernel needs to find data in the arena and workspace.
+struct Layout {
+  char* arena;
+  int32_t* err;                 // [0] status, [1] detail, [2] unit, [3] aux
+  UnitDesc* desc;               // [n_layers][max_seqs][n_kv]
+  char* units;                  // first unit region
+  int64_t unit_stride;
+  int64_t off_rkt, off_rvt, off_rv, off_sink_k, off_sink_v, off_win_k, off_win_v;
+  int64_t off_meta, off_pages;
+  int64_t page_stride;
+  int32_t S, W, B, n_kv, G, max_seqs, nblk_cap, cap_tokens, n_layers, k_max;
+  int32_t topk_fixed, retain_permille, r_max;
+  int32_t attn_tg;              // attention: tokens per staged page group (32 or 16)
+  int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, accumulator copies, stage bytes
+  // workspace
+  float* qrot;                  // [max_seqs][n_kv][G][128]
+  float* scores;                // [max_seqs][n_kv][nblk_cap]
+  float* part_acc;              // [max_seqs][n_kv][MK_MAX_SPLITS][G][128]
+  float* part_ml;               // [max_seqs][n_kv][MK_MAX_SPLITS][G][2]
+  int32_t* counters;            // [max_seqs][n_kv]
+};
+
+// Per-call sequence list, passed by value.
+struct CallSeqs {
+  int32_t n;
+  int32_t seq[MK_MAX_CALL_SEQS];
+  int32_t n_new[MK_MAX_CALL_SEQS];
+  int32_t row_off[MK_MAX_CALL_SEQS];   // first input row of the sequence
+  int32_t T_old[MK_MAX_CALL_SEQS];     // host view, used by the bulk path only
+  int32_t tile_off[MK_MAX_CALL_SEQS + 1];
+};
+
+__host__ __device__ inline int64_t unit_index(const Layout& L, int layer, int seq, int kvh) {
+  return ((int64_t)layer * L.max_seqs + seq) * L.n_kv + kvh;
+}
+__host__ __device__ inline int n_mid_tokens(const Layout& L, int T) {
+  int m = T - L.W - L.S;
+  return m > 0 ? m : 0;
+}
+__host__ __device__ inline int n_mid_blocks(const Layout& L, int T) {
+  return (n_mid_tokens(L, T) + L.B - 1) / L.B;
+}
+__host__ __device__ inline int seg_of_block(const UnitDesc& u, int b) {
+  int s = 0;
+  for (int i = 1; i < u.n_seg; ++i)
+    if (b >= u.first_block[i]) s = i;
+  return s;
+}
+// Number of top-k candidates (blocks of scored segments) among the first nblk blocks.
+__host__ __device__ inline int n_scored_blocks(const UnitDesc& u, int nblk) {
+  int n = 0;
+  for (int i = 0; i < u.n_seg; ++i) {
+    int lo = u.first_block[i];
+    int hi = (i + 1 < u.n_seg) ? u.first_block[i + 1] : nblk;
+    if (hi > nblk) hi = nblk;
+    if (lo > nblk) lo = nblk;
+    if (!u.always[i] && hi > lo) n += hi - lo;
+  }
+  return n;
+}
+__host__ __device__ inline int n_select(const Layout& L, int n_scored) {
+  if (n_scored <= 0) return 0;
+  if (L.topk_fixed > 0) return L.topk_fixed < n_scored ? L.topk_fixed : n_scored;
+  long long k = ((long long)L.retain_permille * n_scored + 999) / 1000;
+  if (k < 1) k = 1;
+  if (k > n_scored) k = n_scored;
+  return (int)k;
+}
+// Bulk-append tiles: [T_old, f), [f, f+64), ... with f the first position
+// S + 64j (or S) past T_old, so that every middle block sits in one tile.
+__host__ __device__ inline int tile_first_boundary(int T_old, int S) {
+  if (T_old < S) return S;
+  return S + ((T_old - S) / kTileTokens + 1) * kTileTokens;
+}
+__host__ __device__ inline int n_tiles(int T_old, int T_new, int S) {
+  if (T_new <= T_old) return 0;
+  int f = tile_first_boundary(T_old, S);
+  if (T_new <= f) return 1;
+  return 1 + (T_new - f + kTileTokens - 1) / kTileTokens;
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ float bf2f(uint32_t b16) { return __uint_as_float(b16 << 16); }
+// Round to nearest even; a zero result is stored as +0.
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  uint16_t b = __bfloat16_as_ushort(h);
+  return b == 0x8000 ? (uint16_t)0 : b;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+__device__ __forceinline__ int warp_excl_scan(int v, int lane) {
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(FULL, x, o);
+    if (lane >= o) x += y;
+  }
+  return x - v;
+}
+__device__ __forceinline__ void set_error(const Layout& L, int32_t detail, int32_t unit, int32_t aux) {
+  if (atomicCAS(&L.err[0], 0, (int32_t)MK_EDEVICE) == 0) {
+    L.err[1] = detail;
+    L.err[2] = unit;
+    L.err[3] = aux;
+  }
+}
+__device__ __forceinline__ bool has_error(const Layout& L) {
+  return *(volatile int32_t*)L.err != 0;
+}
+// 16-byte asynchronous global -> shared copies (cp.async, L2-only caching).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+__device__ __forceinline__ char* unit_base(const Layout& L, int64_t u) {
+  return L.units + u * L.unit_stride;
+}
+#endif
+
+// Kernel launchers (defined in the .cu files); they return cudaGetLastError().
+cudaError_t launch_init_desc(const Layout& L, int layer, int seq, const UnitDesc& d, cudaStream_t s);
+cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
+                                const uint16_t* v, int evict_only, cudaStream_t s);
+cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
+                               const uint16_t* v, int total_tiles, cudaStream_t s);
+cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,
+                                int32_t* ids, int32_t* n_sel, float* scores_out, int max_nblk,
+                                cudaStream_t s);
+cudaError_t launch_decode_attn(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids,
+                               const int32_t* n_sel, uint16_t* out, int cluster, cudaStream_t s);
+cudaError_t launch_dense_attn(const Layout& L, const CallSeqs& cs, const uint16_t* q,
+                              const uint16_t* K, const uint16_t* V, int64_t t_stride,
+                              uint16_t* out, int cluster, cudaStream_t s);
+size_t attn_plan(Layout& L, int r_min);
+int attn_cluster_size(int n_units);
+cudaError_t launch_gram(const uint16_t* x, int64_t n_rows, int64_t row_stride, float* gram,
+                        cudaStream_t s);
+size_t attn_smem_bytes(const Layout& L, int r_max);
+
+}  // namespace mk

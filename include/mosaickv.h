@@ -1,0 +1,204 @@
+/*
+ * mosaickv.h -- C ABI of libmosaickv.so, the GB300 (sm_103a) decode-time hot
+ * path of MosaicKV's dynamic two-D KV-cache compression.
+ *
+ * Sources cited below:
+ *  [N] "MosaicKV：面向超长上下文LLM服务的动态二维KV缓存压缩——阅读笔记"
+ *      (reading notes, zhongzhuzhou.org).
+ *  [S] "MosaicKV: Serving Long-Context LLM with Dynamic Two-D KV Cache
+ *      Compression" (paperlayer.ai summary of arXiv 2607.00760v1).
+ *
+ * Conventions for every call
+ *  - Device pointers are plain CUDA device addresses owned by the caller.
+ *    The library never allocates device memory: the caller provides one
+ *    persistent "arena" (the compressed cache) and one "workspace" (scratch
+ *    reused by every call) sized by mk_arena_bytes / mk_workspace_bytes.
+ *  - bf16 tensors are passed as void* to raw 16-bit bf16 words.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    validate on the host and enqueue kernels; they do not synchronise.
+ *  - Errors found on the host return at once and change no state.  Errors
+ *    found by a kernel (capacity overrun, bad block id) set a sticky device
+ *    error word, make later kernels of the context return early, and are read
+ *    with mk_poll_error.  No call aborts, throws or traps.
+ *  - One context must be used by one host thread at a time.
+ *  - Positions: a sequence holds tokens 0..T-1.  Sink tokens [0, S) and the
+ *    recent window [T-W, T) are stored uncompressed (rotated bf16); the
+ *    middle [S, T-W) is cut into blocks of B tokens from position S.
+ */
+#ifndef MOSAICKV_H
+#define MOSAICKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_HEAD_DIM 128      /* head dimension d; the only one supported */
+#define MK_MAX_SEGMENTS 4    /* strategy segments per sequence */
+#define MK_MAX_GROUP 8       /* query heads per kv head (GQA group) */
+#define MK_MAX_CALL_SEQS 256 /* sequences per call */
+#define MK_MAX_SPLITS 64     /* split-T work items per (sequence, kv head) */
+
+typedef enum mk_status {
+  MK_OK = 0,
+  MK_EINVAL = 1,   /* bad argument or configuration */
+  MK_ENOMEM = 2,   /* arena/workspace too small, or capacity exceeded */
+  MK_ESTATE = 3,   /* call out of order (e.g. attention before a rotation) */
+  MK_ECUDA = 4,    /* a CUDA runtime call failed */
+  MK_EDEVICE = 5,  /* a kernel set the device error word */
+  MK_ETIMEOUT = 6, /* a bounded device-side wait gave up */
+  MK_ENOTSUP = 7   /* valid but not supported by this build */
+} mk_status;
+
+typedef struct mk_ctx mk_ctx;
+typedef void* mk_stream;
+
+/* One middle strategy segment ([S] sec. 4.3: each segment has its own channel
+ * retention and sequence retention).  It starts at the first block boundary
+ * at or after begin_permille/1000 of the sequence's prefill length (the first
+ * segment must start at 0); the last segment is open-ended and receives the
+ * tokens appended during decode. */
+typedef struct mk_segment {
+  int32_t begin_permille; /* 0..1000 */
+  int32_t r;              /* channels kept per vector, 1..128 */
+  int32_t always;         /* 1: attended in full, never scored; 0: top-k */
+  int32_t reserved;       /* must be 0 */
+} mk_segment;
+
+typedef struct mk_config {
+  int32_t head_dim;        /* must be 128 */
+  int32_t n_q_heads;       /* query heads per layer */
+  int32_t n_kv_heads;      /* kv heads per layer; n_q_heads/n_kv_heads <= 8 */
+  int32_t n_layers;
+  int32_t max_seqs;        /* sequence slots, <= MK_MAX_CALL_SEQS */
+  int32_t max_tokens;      /* capacity per sequence (every layer) */
+  int32_t n_sink;          /* S >= 0 */
+  int32_t window;          /* W >= 1 */
+  int32_t block;           /* B: 16, 32 or 64 tokens */
+  int32_t topk_fixed;      /* > 0: keep min(topk_fixed, n) scored blocks */
+  int32_t retain_permille; /* else keep ceil(retain*n/1000), clamped to [1, n] */
+  int32_t n_segments;      /* 1..MK_MAX_SEGMENTS */
+  mk_segment seg[MK_MAX_SEGMENTS];
+} mk_config;
+
+/* Byte offsets of one (layer, sequence, kv head) inside the arena, for tests
+ * and tools.  Pages: block b lives at pages + b*page_stride and holds
+ * [K values B*r bf16][K indices B*r u8][V values B*r bf16][V indices B*r u8],
+ * r being the block's segment r; token slot t of the block uses row t. */
+typedef struct mk_layout_info {
+  int64_t rkt, rvt, rv;      /* fp32 [128][128]: R_k^T, R_v^T, R_v */
+  int64_t sink_k, sink_v;    /* bf16 [S][128], rotated */
+  int64_t win_k, win_v;      /* bf16 [W][128], ring: position p at slot (p-S) mod W */
+  int64_t meta;              /* bf16 [nblk_cap][2][128]: per-block min, max */
+  int64_t pages;             /* packed pages */
+  int64_t page_stride;       /* bytes between consecutive blocks' pages */
+  int32_t nblk_cap;
+  int32_t T;                 /* current length (host view) */
+  int32_t seg_first_block[MK_MAX_SEGMENTS];
+  int32_t n_segments;
+  int32_t reserved;
+} mk_layout_info;
+
+/* Sizes of the caller-owned buffers for a configuration. */
+mk_status mk_arena_bytes(const mk_config* cfg, size_t* bytes);
+mk_status mk_workspace_bytes(const mk_config* cfg, size_t* bytes);
+/* Row length of the ids buffer of mk_block_select: the largest k any call
+ * can return under this configuration. */
+mk_status mk_max_select(const mk_config* cfg, int32_t* k_max);
+
+/* Creates a context over a caller-owned arena and workspace (device memory
+ * of at least the sizes above, 256-byte aligned).  Zeroes the sequence
+ * state; synchronises the device once.  The buffers must outlive the
+ * context. */
+mk_status mk_create(const mk_config* cfg, void* arena, size_t arena_bytes,
+                    void* workspace, size_t workspace_bytes, mk_ctx** out);
+mk_status mk_destroy(mk_ctx* ctx);
+
+/* Installs the rotations of one (layer, seq, kv head): R_k and R_v are d x d
+ * row-major fp32 host arrays whose rows are the eigenvectors of K^T K (resp.
+ * V^T V) by descending eigenvalue, so that k' = k R_k^T ([N] Eq. (4), (6)-(8))
+ * and output = o' R_v ([N] Eq. (14)).  Computing them (host eigensolver, once
+ * per head at prefill) is the caller's job, as on the pages.  Copies the data
+ * before returning.  Must precede the first append of that head. */
+mk_status mk_set_rotation(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head,
+                          const float* Rk_host, const float* Rv_host, mk_stream stream);
+
+/* Appends n_new[i] tokens to sequence seq_ids[i] of `layer`, for every kv
+ * head: rotates each new k, v into its head's basis (fp32 accumulation,
+ * rounded to bf16), stores sink and window tokens dense, and compresses each
+ * token leaving the window: per-vector top-r channels by magnitude, ties to
+ * the lower channel, stored in ascending channel order ([N] Eq. (9),
+ * Algorithm 1; [S] sec. 4.2, 5.1), plus the block's min/max keys.
+ * k, v: device bf16 [sum(n_new)][n_kv_heads][128], sequences in call order.
+ * The first append of a sequence is its prefill: it fixes the strategy
+ * segments.  seq_ids/n_new are host arrays; n_new[i] >= 0.
+ * Errors: MK_ENOMEM if a sequence would pass max_tokens; MK_ESTATE if a
+ * rotation is missing; MK_EINVAL for bad ids or duplicates. */
+mk_status mk_append_compress(mk_ctx* ctx, int32_t layer, int32_t n_seqs,
+                             const int32_t* seq_ids, const int32_t* n_new,
+                             const void* k, const void* v, mk_stream stream);
+
+/* Scores every middle block of each (sequence, kv head) from its min/max
+ * keys and the rotated query q' = q R_k^T:
+ *   s_b = max_h (1/sqrt(d)) sum_j max(q'_hj mn_bj, q'_hj mx_bj)
+ * (Quest-style bound on [N] Eq. (12)), over the group's query heads h, and
+ * keeps the top-k blocks of the scored segments ([S] sec. 4.2 stage 2),
+ * ties to the lower id, ids ascending.
+ * q: device bf16 [n_seqs][n_q_heads][128].  ids: device int32
+ * [n_seqs][n_kv_heads][k_max] (mk_max_select); n_sel: device int32
+ * [n_seqs][n_kv_heads].  scores: optional device fp32
+ * [n_seqs][n_kv_heads][nblk_cap] (NULL to skip).  Also stores q' in the
+ * workspace for the following mk_decode_attn of the same layer. */
+mk_status mk_block_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                          const void* q, int32_t* ids, int32_t* n_sel, float* scores,
+                          mk_stream stream);
+
+/* PackedAttention ([N] Eq. (13), (14); [S] sec. 5.3): for each query head,
+ * softmax attention of q' over the sink tokens, the window, the tokens of the
+ * selected blocks and of the always-attended segments, read straight from the
+ * packed pages; then output = o' R_v.  Must follow mk_block_select for the
+ * same layer and sequence list (it reads that call's q' from the workspace).
+ * ids/n_sel: as written by mk_block_select.  out: device bf16
+ * [n_seqs][n_q_heads][128]. */
+mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                         const int32_t* ids, const int32_t* n_sel, void* out, mk_stream stream);
+
+/* Uncompressed decode attention of our own, the roofline and speedup
+ * reference ([N] Eq. (1)): out = softmax(q K^T / sqrt(d)) V over
+ * K, V: device bf16 [n_seqs][n_kv_heads][t_stride][128], the first T[i]
+ * tokens of sequence i (T: host int32, 1 <= T[i] <= t_stride).  Uses the
+ * context's workspace and its head counts. */
+mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T,
+                               const void* q, const void* K, const void* V, int64_t t_stride,
+                               void* out, mk_stream stream);
+
+/* Set-up helper, not on the decode path: gram = X^T X (fp32 accumulation)
+ * for X: device bf16 rows of 128 values, row i at x + i*row_stride elements.
+ * gram: device fp32 [128][128], overwritten. */
+mk_status mk_gram(const void* x, int64_t n_rows, int64_t row_stride, float* gram, mk_stream stream);
+
+/* Waits for the device and reads the sticky error word: MK_OK, MK_EDEVICE or
+ * MK_ETIMEOUT; *detail (optional) receives the kernel's detail code. */
+mk_status mk_poll_error(mk_ctx* ctx, int32_t* detail);
+/* Clears the device error word (synchronising). */
+mk_status mk_clear_error(mk_ctx* ctx);
+/* Re-reads every sequence length from the device into the host view (needed
+ * after replaying a captured CUDA graph of appends).  Synchronises. */
+mk_status mk_sync_state(mk_ctx* ctx);
+mk_status mk_seq_length(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t* T);
+mk_status mk_layout(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, mk_layout_info* out);
+const char* mk_status_str(mk_status s);
+
+/* Measurement helper, not a step of the method: records `event` (a
+ * cudaEvent_t created by the caller with timing enabled) on `stream`.  While
+ * the stream is being captured into a CUDA graph the record becomes an
+ * event-record node of the graph, so kernel durations can be timed inside
+ * graph replays. */
+mk_status mk_record_event(void* event, mk_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOSAICKV_H */

@@ -1,0 +1,66 @@
+"""The C ABI library builds, loads and exports what include/mosaickv.h declares.
+
+CPU only: the calls made here do no device work (size queries, status text,
+configuration checks).
+"""
+import ctypes
+
+import pytest
+
+from compressed_kv_cache_vector_gb300 import build as B
+from compressed_kv_cache_vector_gb300 import binding as K
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return K.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = K.header_symbols()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(K._SIGS) | {"mk_status_str"} == set(names)
+
+
+def test_status_strings(lib):
+    assert lib.mk_status_str(0) == b"ok"
+    assert lib.mk_status_str(2).startswith(b"buffer too small")
+
+
+def _cfg(**kw):
+    base = dict(n_q_heads=32, n_kv_heads=8, n_layers=1, max_seqs=1, max_tokens=131072 + 64,
+                n_sink=4, window=256, block=32, segments=[(0, 38, 0)], retain_permille=100)
+    base.update(kw)
+    return K.make_config(**base)
+
+
+def test_sizes_follow_the_layout(lib):
+    a, w, k = K.sizes(_cfg())
+    nblk = (131072 + 64 - 4 - 256 + 31) // 32
+    assert k == (100 * nblk + 999) // 1000
+    per_unit_pages = nblk * 6 * 32 * 38
+    assert a > 8 * per_unit_pages and a < 8 * per_unit_pages * 1.5
+    # the 1M configuration: about 1.8 GB of packed pages per layer
+    a4, _, k4 = K.sizes(_cfg(max_tokens=1048576, window=512, block=64, retain_permille=50))
+    assert 1.9e9 < a4 < 2.2e9 and k4 == 819
+
+
+@pytest.mark.parametrize("bad", [
+    dict(block=24), dict(n_q_heads=24), dict(segments=[(100, 38, 0)]), dict(segments=[(0, 0, 0)]),
+    dict(segments=[(0, 129, 0)]), dict(retain_permille=0), dict(window=0),
+    dict(segments=[(0, 32, 0), (500, 64, 1), (400, 32, 0)]),
+])
+def test_bad_configs_rejected(lib, bad):
+    with pytest.raises(K.MosaicKVError) as e:
+        K.sizes(_cfg(**bad))
+    assert e.value.status == 1
+
+
+def test_head_dim_must_be_128(lib):
+    c = _cfg()
+    c.head_dim = 64
+    sz = ctypes.c_size_t()
+    assert lib.mk_arena_bytes(ctypes.byref(c), ctypes.byref(sz)) == 1

@@ -1,0 +1,278 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Bars:
+  * integer / byte work bit-exact: selected channel indices, packed pages,
+    stored sink/window rows, block min/max keys (both sides fed the same bf16
+    rotated vectors by using an exactly representable rotation: identity or a
+    signed permutation), and the top-k ids given the kernel's own fp32 scores;
+  * rotation with a general orthogonal R: within 1 bf16 ulp of the fp64 value
+    rounded once (the kernel accumulates in fp32);
+  * block scores: within the fp32 summation bound of the exact value; the
+    chosen block set equals the oracle's except at near-ties within that bound;
+  * attention output: relative L2 error per head <= 5e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from compressed_kv_cache_vector_gb300 import build as Bld
+from compressed_kv_cache_vector_gb300.binding import MosaicKVError, make_config, MosaicKV
+from oracle import mosaickv_oracle as O
+from tests.harness import D, Case, Pair, bits, page_rows, rel_l2, score_tolerance
+
+pytestmark = pytest.mark.gpu
+ATOL_REL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    Bld.build()
+
+
+def _check_storage(p: Pair, unit):
+    """Sinks, window ring, meta and pages bit-exact against the oracle."""
+    oc = p.orc[unit]
+    l, s, h = unit
+    views = p.mk.unit_views(l, s, h)
+    S, W, B = p.c.n_sink, p.c.window, p.c.block
+    sp = oc.sink_positions()
+    if len(sp):
+        assert np.array_equal(bits(views["sink_k"])[: len(sp)], O.bf16_bits(oc.Kr[sp]))
+        assert np.array_equal(bits(views["sink_v"])[: len(sp)], O.bf16_bits(oc.Vr[sp]))
+    wk, wv = bits(views["win_k"]), bits(views["win_v"])
+    for pos in oc.window_positions():
+        slot = (pos - S) % W
+        assert np.array_equal(wk[slot], O.bf16_bits(oc.Kr[pos])), pos
+        assert np.array_equal(wv[slot], O.bf16_bits(oc.Vr[pos])), pos
+    nb = oc.n_blocks_mid()
+    mn, mx = oc.meta()
+    meta = bits(views["meta"])[:nb]
+    assert np.array_equal(meta[:, 0], O.bf16_bits(mn))
+    assert np.array_equal(meta[:, 1], O.bf16_bits(mx))
+    pages = views["pages"].cpu().numpy()
+    for b in range(nb):
+        r = oc.r_of_block(b)
+        lo, hi = oc.block_tokens(b)
+        got = page_rows(pages[b], B, r, hi - lo)
+        want = page_rows(oc.page_bytes(b), B, r, hi - lo)
+        for g, w_, name in zip(got, want, ("kval", "kidx", "vval", "vidx")):
+            assert np.array_equal(g, w_), (b, name)
+
+
+@pytest.mark.parametrize("rot", ["identity", "perm"])
+def test_append_storage_bitexact_bulk_then_decode(rot):
+    case = Case(n_q=4, n_kv=2, seq_lens=[1000, 333], rot=rot, steps=[1] * 20 + [5, 17, 1, 70, 1],
+                segments=[(0, 32, 0)], seed=1)
+    p = Pair(case)
+    for u in p.units:
+        _check_storage(p, u)
+    p.run_steps()
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    for u in p.units:
+        _check_storage(p, u)
+    assert p.mk.seq_length(0, 0) == 1000 + sum(case.steps)
+
+
+def test_append_storage_multisegment_r128_block64():
+    case = Case(n_q=8, n_kv=1, seq_lens=[3000], rot="perm", block=64, window=100, n_sink=0,
+                segments=[(0, 128, 0), (300, 17, 1), (700, 64, 0)], steps=[1] * 40 + [3], seed=2)
+    p = Pair(case)
+    p.run_steps()
+    for u in p.units:
+        _check_storage(p, u)
+
+
+def test_append_from_empty_through_sinks_and_window():
+    # Starts below S+W; single-token appends walk through sinks, window, middle.
+    case = Case(n_q=2, n_kv=1, seq_lens=[2], rot="perm", n_sink=4, window=16, block=16,
+                steps=[1] * 60 + [2, 16, 9], seed=3)
+    p = Pair(case)
+    p.run_steps()
+    _check_storage(p, p.units[0])
+
+
+def test_rotation_within_fp32_accumulation_bound():
+    # The kernel sums 128 exact bf16 x fp32 products in fp32, then rounds to
+    # bf16 once.  Its result must be the bf16 rounding of some value within
+    # the fp32 summation bound of the exact product; away from rounding
+    # boundaries it equals the oracle's single fp64 -> bf16 rounding.
+    case = Case(n_q=4, n_kv=2, seq_lens=[600], window=600 - 4, rot="eigh", seed=4)
+    p = Pair(case)
+    flips, total = 0, 0
+    for u in p.units:
+        oc = p.orc[u]
+        X = p.K[u][:600].cpu().to(torch.float64).numpy()
+        R = oc.Rk
+        exact = X @ R.T
+        eps = (D + 2) * 2.0 ** -24 * (np.abs(X) @ np.abs(R).T)
+        lo, hi = O.bf16_round(exact - eps), O.bf16_round(exact + eps)
+        wk = bits(p.mk.unit_views(*u)["win_k"])
+        for pos in oc.window_positions():
+            got = O.bits_to_value(wk[(pos - 4) % case.window])
+            assert np.all((got >= lo[pos]) & (got <= hi[pos])), pos
+            flips += int(np.sum(got != oc.Kr[pos]))
+            total += 128
+    assert flips <= 0.05 * total
+
+
+@pytest.mark.parametrize("G,topk_fixed,retain", [(4, 0, 100), (1, 64, 0), (8, 0, 300)])
+def test_block_select_scores_and_ids(G, topk_fixed, retain):
+    case = Case(n_q=G * 2, n_kv=2, seq_lens=[4096, 2500], rot="perm", topk_fixed=topk_fixed,
+                retain_permille=retain, steps=[1, 1, 3], seed=5 + G)
+    p = Pair(case)
+    p.run_steps()
+    q = p.query(1)
+    nblk_cap = p.mk.nblk_cap
+    scores = torch.full((2, 2, nblk_cap), float("nan"), dtype=torch.float32, device="cuda")
+    ids, n_sel = p.mk.block_select(0, [0, 1], q, scores=scores)
+    torch.cuda.synchronize()
+    ids, n_sel, scores = ids.cpu().numpy(), n_sel.cpu().numpy(), scores.cpu().numpy()
+    near_ties = 0
+    for (l, s, h), oc in p.orc.items():
+        qs = q[s, h * G:(h + 1) * G].cpu().to(torch.float64).numpy()
+        per, grp = oc.scores(qs)
+        nb = oc.n_blocks_mid()
+        got_s = scores[s, h, :nb].astype(np.float64)
+        mn, mx = oc.meta()
+        tol = score_tolerance(oc.rotate_query(qs), mn, mx)
+        assert np.all(np.abs(got_s - grp) <= tol)
+        cand = oc.candidates()
+        k = O.n_select(len(cand), oc.st)
+        assert n_sel[s, h] == k
+        got_ids = ids[s, h, :k]
+        # bit-exact: the kernel's ids are the top-k of the kernel's own scores
+        assert np.array_equal(got_ids, O.topk_blocks(got_s, cand, k))
+        want_ids, _ = oc.select(qs)
+        if not np.array_equal(got_ids, want_ids):
+            srt = np.sort(grp[cand])[::-1]
+            assert k < len(cand) and srt[k - 1] - srt[k] <= 2 * tol.max()
+            near_ties += 1
+    assert near_ties <= 1
+
+
+@pytest.mark.parametrize("case", [
+    Case(n_q=4, n_kv=2, seq_lens=[2048, 700], rot="eigh", steps=[1] * 5 + [40], seed=11),
+    Case(n_q=8, n_kv=1, seq_lens=[5000], rot="eigh", block=64, window=256, segments=[(0, 38, 0)],
+         retain_permille=50, steps=[1, 1], seed=12),
+    Case(n_q=4, n_kv=1, seq_lens=[4000, 1200, 300], rot="eigh", block=16, window=128,
+         segments=[(0, 32, 0), (350, 64, 1), (650, 32, 0)], steps=[1, 2], seed=13),
+    Case(n_q=1, n_kv=1, seq_lens=[4096], rot="eigh", window=64, topk_fixed=64, retain_permille=0,
+         segments=[(0, 32, 0)], seed=14),
+    Case(n_q=4, n_kv=1, seq_lens=[40], rot="eigh", window=64, seed=15),          # empty middle
+    Case(n_q=2, n_kv=1, seq_lens=[3], rot="eigh", n_sink=4, window=8, seed=16),  # T < S
+    Case(n_q=4, n_kv=1, seq_lens=[1500], rot="eigh", segments=[(0, 128, 0)], topk_fixed=10 ** 6,
+         retain_permille=0, seed=17),                                              # r = d, all blocks
+], ids=["gqa4-2seq", "b64-5pct", "serving-segments", "single-head-c1", "empty-middle", "below-sinks",
+        "r128-allblocks"])
+def test_decode_attention_matches_oracle(case):
+    p = Pair(case)
+    p.run_steps()
+    q = p.query(2)
+    seqs = list(range(len(case.seq_lens)))
+    ids, n_sel = p.mk.block_select(0, seqs, q)
+    out = p.mk.decode_attn(0, seqs, ids, n_sel)
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    out = out.cpu().to(torch.float64).numpy()
+    ids, n_sel = ids.cpu().numpy(), n_sel.cpu().numpy()
+    G = case.G
+    worst = 0.0
+    for (l, s, h), oc in p.orc.items():
+        qs = q[s, h * G:(h + 1) * G].cpu().to(torch.float64).numpy()
+        got_ids = ids[s, h, :n_sel[s, h]]
+        want = oc.attention(qs, got_ids)
+        for g in range(G):
+            e = rel_l2(out[s, h * G + g], want[g])
+            worst = max(worst, e)
+            assert e <= ATOL_REL, (s, h, g, e)
+    print("worst relative L2", worst)
+
+
+def test_dense_reference_attention():
+    torch.manual_seed(0)
+    n, Hkv, G, T = 2, 2, 4, 3000
+    cfg = make_config(Hkv * G, Hkv, 1, n, 4096, 4, 64, 16, [(0, 32, 0)], 0, 100)
+    mk = MosaicKV(cfg)
+    K = torch.randn(n, Hkv, T, 128, device="cuda").to(torch.bfloat16)
+    V = torch.randn(n, Hkv, T, 128, device="cuda").to(torch.bfloat16)
+    q = torch.randn(n, Hkv * G, 128, device="cuda").to(torch.bfloat16)
+    lens = [T, 1777]
+    out = mk.dense_attn(lens, q, K, V).cpu().to(torch.float64).numpy()
+    for s in range(n):
+        for h in range(Hkv):
+            Kn = K[s, h, :lens[s]].cpu().to(torch.float64).numpy()
+            Vn = V[s, h, :lens[s]].cpu().to(torch.float64).numpy()
+            qn = q[s, h * G:(h + 1) * G].cpu().to(torch.float64).numpy()
+            want = O.dense_attention(qn, Kn, Vn)
+            for g in range(G):
+                assert rel_l2(out[s, h * G + g], want[g]) <= ATOL_REL
+
+
+def test_gram_and_host_rotation():
+    from compressed_kv_cache_vector_gb300 import binding, synth
+    x = synth.lowrank_outlier(5000, 128, 0.9, 99, device="cuda")
+    G = binding.gram(x, 5000, 128).cpu().numpy().astype(np.float64)
+    X = synth.bf16_values(x)
+    want = X.T @ X
+    assert np.max(np.abs(G - want)) <= 1e-5 * np.abs(want).max()
+    R = binding.rotation_from_gram(G)
+    Ro, lam = O.rotation_from_keys(X)
+    # same principal directions up to sign for well-separated eigenvalues
+    for i in range(8):
+        assert abs(abs(float(R[i] @ Ro[i])) - 1.0) < 1e-3
+
+
+def test_host_errors_leave_state_unchanged():
+    case = Case(n_q=4, n_kv=1, seq_lens=[200], rot="perm", window=32, seed=21)
+    p = Pair(case)
+    mk = p.mk
+    k = torch.zeros(1, 1, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(MosaicKVError) as e:
+        mk.append(0, [0, 0], [1, 1], k, k)                  # duplicate sequence
+    assert e.value.status == 1
+    with pytest.raises(MosaicKVError) as e:
+        mk.append(0, [0], [10 ** 6], k, k)                  # past capacity
+    assert e.value.status == 2
+    q = p.query(3)
+    ids, n_sel = mk.alloc_select(1)
+    out = torch.empty(1, 4, 128, dtype=torch.bfloat16, device="cuda")
+    # attention before any selection on this layer
+    with pytest.raises(MosaicKVError) as e:
+        mk.decode_attn(0, [0], ids, n_sel, out)
+    assert e.value.status == 3
+    assert mk.seq_length(0, 0) == 200
+    mk.block_select(0, [0], q, ids, n_sel)
+    mk.decode_attn(0, [0], ids, n_sel, out)
+    torch.cuda.synchronize()
+    assert mk.poll_error() == (0, 0)
+
+
+def test_device_error_word_on_bad_block_id():
+    # A corrupted ids row (out-of-range block) is caught by the kernel's own
+    # bounds check: it sets the error word and skips the page (no fault).
+    case = Case(n_q=4, n_kv=1, seq_lens=[800], rot="perm", window=32, seed=22)
+    p = Pair(case)
+    q = p.query(4)
+    ids, n_sel = p.mk.block_select(0, [0], q)
+    ids[0, 0, 0] = 10 ** 6
+    p.mk.decode_attn(0, [0], ids, n_sel)
+    st, detail = p.mk.poll_error()
+    assert st == 5 and detail == 2
+    p.mk.clear_error()
+    assert p.mk.poll_error() == (0, 0)
+
+
+def test_repeatable_bytes():
+    outs = []
+    for _ in range(2):
+        case = Case(n_q=4, n_kv=2, seq_lens=[1500], rot="eigh", steps=[1, 1], seed=23)
+        p = Pair(case)
+        p.run_steps()
+        q = p.query(5)
+        ids, n_sel = p.mk.block_select(0, [0], q)
+        out = p.mk.decode_attn(0, [0], ids, n_sel)
+        outs.append(bits(out))
+    assert np.array_equal(outs[0], outs[1])
