@@ -101,7 +101,7 @@ Plan make_plan(const mk_config* c) {
   w = align_up(w + slots * (int64_t)std::max(1, L.nblk_cap) * 4);  // scores
   w = align_up(w + slots * MK_MAX_SPLITS * L.G * D * 4);       // part_acc
   w = align_up(w + slots * MK_MAX_SPLITS * L.G * 2 * 4);       // part_ml
-  w = align_up(w + slots * 4);                                 // counters
+  w = align_up(w + slots * 4 * 2);                             // counters: attention, selection
   p.ws_bytes = w;
   return p;
 }
@@ -238,7 +238,7 @@ mk_status mk_create(const mk_config* cfg, void* arena, size_t arena_bytes, void*
   ctx->firsts.assign(ls * MK_MAX_SEGMENTS, 0);
   ctx->rot_set.assign(ls * cfg->n_kv_heads, 0);
   cudaError_t e = cudaMemset(arena, 0, (size_t)p.units_off);
-  if (e == cudaSuccess) e = cudaMemset(ctx->L.counters, 0, sizeof(int32_t) * cfg->max_seqs * cfg->n_kv_heads);
+  if (e == cudaSuccess) e = cudaMemset(ctx->L.counters, 0, sizeof(int32_t) * 2 * cfg->max_seqs * cfg->n_kv_heads);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     delete ctx;
@@ -374,9 +374,21 @@ mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32
   CallSeqs* cs = new (std::nothrow) CallSeqs();
   if (!cs) return MK_ENOMEM;
   cs->n = n_seqs;
-  for (int i = 0; i < n_seqs; ++i) cs->seq[i] = seq_ids[i];
-  const int cluster = mk::attn_cluster_size(n_seqs * ctx->cfg.n_kv_heads);
-  cudaError_t e = mk::launch_decode_attn(ctx->L, layer, *cs, ids, n_sel, static_cast<uint16_t*>(out), cluster,
+  int max_items = 1;
+  for (int i = 0; i < n_seqs; ++i) {
+    cs->seq[i] = seq_ids[i];
+    const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq_ids[i];
+    const int T = ctx->T[ls];
+    const int nblk = mk::n_mid_blocks(ctx->L, T);
+    const UnitDesc d = host_desc(ctx, layer, seq_ids[i]);
+    const int scored = mk::n_scored_blocks(d, nblk);
+    const int dense = std::min(ctx->L.S, T) + std::max(0, T - (ctx->L.S + mk::n_mid_tokens(ctx->L, T)));
+    const int groups = (ctx->L.B + mk::kDenseChunk - 1) / mk::kDenseChunk;
+    const int items = (dense + mk::kDenseChunk - 1) / mk::kDenseChunk +
+                      (mk::n_select(ctx->L, scored) + (nblk - scored)) * groups;
+    max_items = std::max(max_items, items);
+  }
+  cudaError_t e = mk::launch_decode_attn(ctx->L, layer, *cs, ids, n_sel, static_cast<uint16_t*>(out), max_items,
                                          (cudaStream_t)stream);
   delete cs;
   return cuda_status(e);
@@ -389,6 +401,7 @@ mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T, co
   CallSeqs* cs = new (std::nothrow) CallSeqs();
   if (!cs) return MK_ENOMEM;
   cs->n = n_seqs;
+  int max_items = 1;
   for (int i = 0; i < n_seqs; ++i) {
     if (T[i] < 1 || T[i] > t_stride) {
       delete cs;
@@ -396,11 +409,11 @@ mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T, co
     }
     cs->seq[i] = i;
     cs->T_old[i] = T[i];
+    max_items = std::max(max_items, (T[i] + mk::kDenseChunk - 1) / mk::kDenseChunk);
   }
-  const int cluster = mk::attn_cluster_size(n_seqs * ctx->cfg.n_kv_heads);
   cudaError_t e = mk::launch_dense_attn(ctx->L, *cs, static_cast<const uint16_t*>(q),
                                         static_cast<const uint16_t*>(K), static_cast<const uint16_t*>(V), t_stride,
-                                        static_cast<uint16_t*>(out), cluster, (cudaStream_t)stream);
+                                        static_cast<uint16_t*>(out), max_items, (cudaStream_t)stream);
   delete cs;
   return cuda_status(e);
 }

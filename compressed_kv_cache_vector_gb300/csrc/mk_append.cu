@@ -130,30 +130,32 @@ __global__ void __launch_bounds__(256) k_append_small(Layout L, int layer, CallS
   __shared__ float xs[kSmallAppend][2][D];
   __shared__ __align__(16) uint16_t rot[kSmallAppend][2][D];
   __shared__ int s_abort;
+  char* base = unit_base(L, u);
+  // Stage R_k^T and R_v^T (contiguous in the unit, written only by
+  // mk_set_rotation) while the previous kernel finishes and the eviction runs.
+  extern __shared__ __align__(16) float Rs[];   // [2][128*128] when rotating
+  if (!evict_only && n > 0 && n <= kSmallAppend) {
+    const float4* src = reinterpret_cast<const float4*>(base + L.off_rkt);
+    for (int i = tid; i < 2 * D * D / 4; i += blockDim.x) cp_async16(reinterpret_cast<float4*>(Rs) + i, src + i);
+    cp_async_commit();
+  }
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     s_abort = has_error(L);
     ud = L.desc[u];
   }
   __syncthreads();
-  if (s_abort) return;
   const int T_old = ud.T;
   const int T_new = T_old + n;
-  if (T_new > L.cap_tokens || (!evict_only && n > kSmallAppend)) {
-    if (tid == 0) set_error(L, ERR_CAPACITY, (int32_t)u, T_new);
+  if (s_abort || T_new > L.cap_tokens || (!evict_only && n > kSmallAppend)) {
+    if (!s_abort && tid == 0) set_error(L, ERR_CAPACITY, (int32_t)u, T_new);
+    cp_async_wait_all();
     return;
   }
-  char* base = unit_base(L, u);
   const int S = L.S, W = L.W;
   uint16_t* win_k = reinterpret_cast<uint16_t*>(base + L.off_win_k);
   uint16_t* win_v = reinterpret_cast<uint16_t*>(base + L.off_win_v);
-  // Stage R_k^T and R_v^T (contiguous in the unit) into shared memory while
-  // the eviction below runs.
-  extern __shared__ __align__(16) float Rs[];   // [2][128*128] when rotating
-  if (!evict_only && n > 0) {
-    const float4* src = reinterpret_cast<const float4*>(base + L.off_rkt);
-    for (int i = tid; i < 2 * D * D / 4; i += blockDim.x) cp_async16(reinterpret_cast<float4*>(Rs) + i, src + i);
-    cp_async_commit();
-  }
 
   // Phase A: window tokens that leave the window, in position order.
   const int e_lo = max(S, T_old - W), e_hi = min(T_old, T_new - W);
@@ -167,6 +169,7 @@ __global__ void __launch_bounds__(256) k_append_small(Layout L, int layer, CallS
   __syncthreads();
   if (evict_only) {
     if (tid == 0) L.desc[u].T = T_new;
+    cp_async_wait_all();
     return;
   }
 
@@ -180,20 +183,15 @@ __global__ void __launch_bounds__(256) k_append_small(Layout L, int layer, CallS
   cp_async_wait_all();
   __syncthreads();
   {
+    // thread (w, ch): channel ch of the rotated key (w = 0) or value (w = 1)
     const int w = tid >> 7, ch = tid & 127;
     const float* RT = Rs + w * D * D;
-    float acc[kSmallAppend];
-#pragma unroll
-    for (int i = 0; i < kSmallAppend; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < D; ++j) {
-      const float rr = RT[j * D + ch];
-#pragma unroll
-      for (int i = 0; i < kSmallAppend; ++i)
-        if (i < n) acc[i] = fmaf(xs[i][w][j], rr, acc[i]);
+    for (int i = 0; i < n; ++i) {
+      float acc = 0.0f;
+#pragma unroll 8
+      for (int j = 0; j < D; ++j) acc = fmaf(xs[i][w][j], RT[j * D + ch], acc);
+      rot[i][w][ch] = f2bf(acc);
     }
-#pragma unroll
-    for (int i = 0; i < kSmallAppend; ++i)
-      if (i < n) rot[i][w][ch] = f2bf(acc[i]);
   }
   __syncthreads();
 
@@ -357,8 +355,7 @@ cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_append_small<<<cs.n * L.n_kv, 256, smem, s>>>(L, layer, cs, k, v, evict_only);
-  return cudaGetLastError();
+  return launch_pdl(k_append_small, dim3(cs.n * L.n_kv), dim3(256), smem, s, 0, L, layer, cs, k, v, evict_only);
 }
 
 cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,

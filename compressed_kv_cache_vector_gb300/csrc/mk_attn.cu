@@ -1,8 +1,7 @@
 // PackedAttention: decode attention straight from the packed pages, with
-// dense sink and window tokens, online softmax, scatter accumulation of the
-// rotated values by their channel indices, and the un-rotation by R_v.  The
-// same kernel with dense items only and no rotation is the uncompressed
-// reference.
+// dense sink and window tokens, online softmax, the rotated values
+// accumulated by their channel indices, and the un-rotation by R_v.  The same
+// kernel with dense items only and no rotation is the uncompressed reference.
 //
 // Method: "MosaicKV：...阅读笔记" (zhongzhuzhou.org), Eq. (1) (dense
 // attention), Eq. (13) (attention on the kept tokens' compressed vectors),
@@ -11,14 +10,23 @@
 // attention on packed vectors with positions rebuilt on the fly, inverse
 // rotation merged into the query).
 //
-// GB300 structure: one thread-block cluster of C <= 16 CTAs per (sequence,
-// kv head).  Each CTA takes a contiguous share of the work items (dense
-// chunks of 16 tokens, then packed page groups of TG tokens); each warp
-// double-buffers its items into shared memory with cp.async.  The split-T
-// log-sum-exp merge and the un-rotation go through distributed shared
-// memory: CTA `rank` merges and un-rotates output channels
-// [rank*128/C, (rank+1)*128/C).  No global partials, no counters, no waits
-// other than cluster barriers.
+// GB300 structure.
+//  * Work items of one (sequence, kv head): dense chunks of 16 tokens (sinks,
+//    window), then 16-token groups of the selected / always-attended pages.
+//    They are split over Q clusters of C CTAs (8 warps each); every warp
+//    double-buffers its items into shared memory with cp.async.
+//  * Per group the warp rebuilds the positions: it zero-fills a 16 x 128 bf16
+//    K tile and V tile and scatters the kept values by their channel indices
+//    (lanes 0-15 keys, lanes 16-31 values).  Logits S^T[16 tok x 8 heads] and
+//    the value sum O'^T[128 x 8 heads] then run on the tensor cores
+//    (mma.sync m16n8k16, bf16 in, fp32 accumulate).  The fp32 operands q' and
+//    p are split into bf16 hi + lo parts (two MMAs), so the products keep
+//    ~16 significant bits: the rounding stays far below the 5e-3 tolerance.
+//  * The split-T log-sum-exp merge: warps -> CTA in shared memory, CTAs ->
+//    cluster through distributed shared memory (CTA `rank` owns output
+//    channels [rank*128/C, (rank+1)*128/C)), clusters -> unit through the
+//    workspace when Q > 1: the last cluster to arrive (atomic counter, no
+//    waiting) merges and un-rotates.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -33,9 +41,10 @@ namespace mk {
 
 namespace {
 constexpr int kWarps = 8;
-constexpr int kDC = 16;                     // dense chunk (tokens)
-constexpr int kKRow = D + 8;                // padded K row (bf16) in a staged dense chunk: 272 bytes
-constexpr int kDenseStage = kDC * (kKRow + D) * 2;
+constexpr int kTG = 16;                      // tokens per group (one MMA tile)
+constexpr int kRow = D + 8;                  // padded bf16 row: 272 bytes, ldmatrix conflict-free
+constexpr int kTile = kTG * kRow;            // one 16-row tile (bf16 elements)
+constexpr int kDenseStage = 2 * kTile * 2;   // staged dense chunk: K tile + V tile (bytes)
 constexpr float kScaleLog2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
 __device__ __forceinline__ int always_block(const UnitDesc& ud, int nblk, int i) {
@@ -49,86 +58,76 @@ __device__ __forceinline__ int always_block(const UnitDesc& ud, int nblk, int i)
   return -1;
 }
 
-template <int G>
-__device__ __forceinline__ void load_q(const float* qs, int c, float (&qv)[G]) {
-  if constexpr (G % 4 == 0) {
-#pragma unroll
-    for (int h = 0; h < G; h += 4) {
-      const float4 t = *reinterpret_cast<const float4*>(qs + c * G + h);
-      qv[h] = t.x; qv[h + 1] = t.y; qv[h + 2] = t.z; qv[h + 3] = t.w;
-    }
-  } else {
-#pragma unroll
-    for (int h = 0; h < G; ++h) qv[h] = qs[c * G + h];
-  }
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// fp32 -> (hi, lo) bf16 pair with hi + lo ~ x to ~16 bits.
+__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+}
+__device__ __forceinline__ uint32_t pack2(uint16_t lo16, uint16_t hi16) {
+  return (uint32_t)lo16 | ((uint32_t)hi16 << 16);
 }
 
-template <int G>
-__device__ __forceinline__ void fma_vec(float* a, const float (&p)[G], float v) {
-  if constexpr (G % 4 == 0) {
-#pragma unroll
-    for (int h = 0; h < G; h += 4) {
-      float4 t = *reinterpret_cast<float4*>(a + h);
-      t.x = fmaf(p[h], v, t.x); t.y = fmaf(p[h + 1], v, t.y);
-      t.z = fmaf(p[h + 2], v, t.z); t.w = fmaf(p[h + 3], v, t.w);
-      *reinterpret_cast<float4*>(a + h) = t;
-    }
-  } else {
-#pragma unroll
-    for (int h = 0; h < G; ++h) a[h] = fmaf(p[h], v, a[h]);
-  }
-}
-
-// One work item of a warp: a dense chunk or one TG-token group of a page.
 struct Task {
-  int kind;      // 0 none, 1 dense, 2 sparse group, 3 skipped (bad block id)
-  int item;      // item index in this unit's list
+  int kind;      // 0 none, 1 dense chunk, 2 packed group, 3 skipped (bad block id)
+  int item;
   int j0, nd;    // dense: first dense token and count
   int b, r, tg, n_live;
 };
 
-struct UnitInfo {
-  int n_sink, win_lo, n_dense, n_dch, nblk, n_mid, ns, n_items;
-};
-
-size_t smem_for(const Layout& L, int tg, int nst, int nc) {
-  const int G = L.G;
-  const size_t sb = (size_t)((std::max(6 * tg * L.r_max, kDenseStage) + 15) / 16 * 16);
-  return (size_t)D * G * 4                         // q'
-         + (size_t)kWarps * nc * D * G * 4         // per-warp accumulators
-         + (size_t)kWarps * 32 * G * 4             // per-token softmax weights
-         + (size_t)kWarps * nst * sb               // stages
-         + (size_t)kWarps * G * 2 * 4              // per-warp (m, l)
-         + 16 * ((G * 2 * 4 + 15) / 16)            // CTA (m, l)
-         + (size_t)2 * G * D * 4;                  // CTA acc, merged o'
+size_t smem_for(const Layout& L, int nst) {
+  const size_t sb = (size_t)((std::max(6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16);
+  const size_t per_warp = nst * sb + (size_t)kDenseStage + 2 * 8 * kTG * 2;  // stages, K/V tiles, P hi/lo
+  return (size_t)kWarps * per_warp
+         + (size_t)L.G * D * 4          // q' (fp32) for building the B fragments
+         + (size_t)kWarps * 8 * 2 * 4   // per-warp (m, l) for 8 head slots
+         + 8 * 2 * 4                    // CTA (m, l)
+         + (size_t)2 * L.G * D * 4      // CTA acc, merged o'
+         + 16;                          // flags
 }
 }  // namespace
 
-// Shared-memory plan of the attention kernel; fills the attn_* fields of the
-// layout and returns the dynamic shared memory size (0 if nothing fits).
-size_t attn_plan(Layout& L, int r_min) {
-  const int nc = r_min >= 32 ? 2 : (r_min >= 16 ? 3 : 1);
-  const int tgs[2] = {32, 16};
-  for (int nst = 2; nst >= 1; --nst)
-    for (int ti = 0; ti < 2; ++ti) {
-      const int tg = tgs[ti];
-      if (tg > L.B) continue;
-      const size_t s = smem_for(L, tg, nst, nc);
-      if (s <= 227 * 1024) {
-        L.attn_tg = tg;
-        L.attn_nst = nst;
-        L.attn_nc = nc;
-        L.attn_sb = (int)((std::max(6 * tg * L.r_max, kDenseStage) + 15) / 16 * 16);
-        return s;
-      }
+// Shared-memory plan; fills attn_nst / attn_sb and returns the dynamic shared
+// memory size (0 if nothing fits).
+size_t attn_plan(Layout& L, int /*r_min*/) {
+  for (int nst = 2; nst >= 1; --nst) {
+    const size_t s = smem_for(L, nst);
+    if (s <= 227 * 1024) {
+      L.attn_tg = kTG;
+      L.attn_nst = nst;
+      L.attn_nc = 1;
+      L.attn_sb = (int)((std::max(6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16);
+      return s;
     }
+  }
   return 0;
 }
 
-size_t attn_smem_bytes(const Layout& L, int) { return smem_for(L, L.attn_tg, L.attn_nst, L.attn_nc); }
+size_t attn_smem_bytes(const Layout& L, int) { return smem_for(L, L.attn_nst); }
 
 template <int G, bool DENSE>
-__global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs cs, const int32_t* __restrict__ ids,
+__global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs cs, int Q,
+                                                 const int32_t* __restrict__ ids,
                                                  const int32_t* __restrict__ n_sel_in,
                                                  const uint16_t* __restrict__ q_in, const uint16_t* __restrict__ Kd,
                                                  const uint16_t* __restrict__ Vd, int64_t t_stride,
@@ -136,104 +135,121 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
-  const int NC = L.attn_nc, NST = L.attn_nst, TG = L.attn_tg, SB = L.attn_sb;
+  const int NST = L.attn_nst, SB = L.attn_sb;
 
   extern __shared__ __align__(16) unsigned char smem[];
-  float* qs = reinterpret_cast<float*>(smem);                       // [D][G]
-  float* accw = qs + D * G;                                         // [kWarps][NC][D][G]
-  float* ptok = accw + kWarps * NC * D * G;                         // [kWarps][32][G]
-  unsigned char* stages = reinterpret_cast<unsigned char*>(ptok + kWarps * 32 * G);  // [kWarps][NST][SB]
-  float* mlw = reinterpret_cast<float*>(stages + (size_t)kWarps * NST * SB);         // [kWarps][G][2]
-  float* cl_ml = mlw + kWarps * G * 2;                              // [G][2] (padded to 16 B)
-  float* cl_acc = cl_ml + 4 * ((G * 2 + 3) / 4);                    // [G][D]
-  float* ofull = cl_acc + G * D;                                    // [G][D]
+  const size_t per_warp = (size_t)NST * SB + kDenseStage + 2 * 8 * kTG * 2;
+  unsigned char* warp_area = smem;                                             // [kWarps][per_warp]
+  float* qs = reinterpret_cast<float*>(smem + kWarps * per_warp);              // [G][D]
+  float* mlw = qs + G * D;                                                     // [kWarps][8][2]
+  float* cl_ml = mlw + kWarps * 16;                                            // [8][2]
+  float* cl_acc = cl_ml + 16;                                                  // [G][D]
+  float* ofull = cl_acc + G * D;                                               // [G][D]
+  int* flag = reinterpret_cast<int*>(ofull + G * D);
   __shared__ UnitDesc ud;
   __shared__ int s_abort, s_ns;
 
-  const int unit_call = blockIdx.x / C;
+  const int per_unit = Q * C;
+  const int unit_call = blockIdx.x / per_unit;
+  const int kq = blockIdx.x - unit_call * per_unit;   // CTA index within the unit: q*C + rank
+  const int qi = kq / C;
   const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
   const int seq = cs.seq[ci];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tig = lane & 3;
   const int64_t u = DENSE ? 0 : unit_index(L, layer, seq, kvh);
   const int64_t slot = (int64_t)seq * L.n_kv + kvh;
 
+  if (!DENSE && rank == 0 && qi == 0) {   // R_v is static: warm L2 before the wait
+    const char* rv = unit_base(L, u) + L.off_rv;
+    for (int i = tid; i < D * D * 4 / 128; i += blockDim.x) prefetch_l2(rv + (size_t)i * 128);
+  }
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     s_abort = has_error(L);
-    if (!DENSE) {
-      ud = L.desc[u];
-      s_ns = n_sel_in[(int64_t)ci * L.n_kv + kvh];
-    } else {
-      s_ns = 0;
-    }
+    if (!DENSE) ud = L.desc[u];
+    s_ns = DENSE ? 0 : n_sel_in[(int64_t)ci * L.n_kv + kvh];
   }
   __syncthreads();
-  // Every CTA of the cluster must reach the cluster barriers below, so an
-  // abort only skips the work, never the barriers.
+  // Every CTA must reach the cluster barriers below: an abort only empties the work.
   bool skip = s_abort != 0;
 
   const int S = L.S, W = L.W, B = L.B;
-  UnitInfo ui{};
+  int n_sink = 0, win_lo = 0, n_dense, nblk = 0, n_mid = 0, ns = s_ns, n_always = 0;
   if (DENSE) {
-    ui.n_dense = cs.T_old[ci];
+    n_dense = cs.T_old[ci];
   } else {
     const int T = ud.T;
-    ui.n_sink = min(S, T);
-    ui.n_mid = n_mid_tokens(L, T);
-    ui.win_lo = S + ui.n_mid;
-    ui.n_dense = ui.n_sink + max(0, T - ui.win_lo);
-    ui.nblk = n_mid_blocks(L, T);
-    ui.ns = s_ns;
-    if (ui.ns < 0 || ui.ns > L.k_max) {
-      if (tid == 0) set_error(L, ERR_BAD_NSEL, (int32_t)u, ui.ns);
+    n_sink = min(S, T);
+    n_mid = n_mid_tokens(L, T);
+    win_lo = S + n_mid;
+    n_dense = n_sink + max(0, T - win_lo);
+    nblk = n_mid_blocks(L, T);
+    n_always = nblk - n_scored_blocks(ud, nblk);
+    if (ns < 0 || ns > L.k_max) {
+      if (tid == 0) set_error(L, ERR_BAD_NSEL, (int32_t)u, ns);
       skip = true;
-      ui.ns = 0;
+      ns = 0;
     }
   }
-  ui.n_dch = (ui.n_dense + kDC - 1) / kDC;
-  const int n_always = DENSE ? 0 : ui.nblk - n_scored_blocks(ud, ui.nblk);
-  ui.n_items = skip ? 0 : ui.n_dch + ui.ns + n_always;
-  const int per = (ui.n_items + C - 1) / C;
-  const int i0 = rank * per, i1 = min(ui.n_items, i0 + per);
+  const int n_dch = (n_dense + kTG - 1) / kTG;
+  const int n_items = skip ? 0 : n_dch + ns + n_always;
+  const int per = (n_items + per_unit - 1) / per_unit;
+  const int i0 = kq * per, i1 = min(n_items, i0 + per);
 
   for (int i = tid; i < G * D; i += blockDim.x) {
-    const int h = i / D, c = i % D;
     float v = 0.0f;
     if (!skip) {
-      if (DENSE) v = bf2f(q_in[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G + h) * D + c]);
-      else v = L.qrot[(slot * G + h) * D + c];
+      if (DENSE) v = bf2f(q_in[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D + i]);
+      else v = L.qrot[slot * G * D + i];
     }
-    qs[c * G + h] = v;
+    qs[i] = v;
   }
-  for (int i = tid; i < kWarps * NC * D * G; i += blockDim.x) accw[i] = 0.0f;
   __syncthreads();
+
+  // q'^T B fragments (k = channel, n = head), hi and lo parts: 8 k-chunks.
+  uint32_t bqh[8][2], bql[8][2];
+#pragma unroll
+  for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint16_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
+      if (g < G) {
+        const int c = kc * 16 + half * 8 + 2 * tig;
+        split_bf16(qs[g * D + c], h0, l0);
+        split_bf16(qs[g * D + c + 1], h1, l1);
+      }
+      bqh[kc][half] = pack2(h0, h1);
+      bql[kc][half] = pack2(l0, l1);
+    }
 
   const char* base = DENSE ? nullptr : unit_base(L, u);
   const int32_t* my_ids = DENSE ? nullptr : ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
-  float* acc = accw + warp * NC * D * G;
-  float* pt = ptok + warp * 32 * G;
-  unsigned char* stg = stages + (size_t)warp * NST * SB;
-  float m[G], l[G], racc[4][G];
+  unsigned char* my_area = warp_area + (size_t)warp * per_warp;
+  uint16_t* tiles = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB);           // K tile, V tile
+  uint16_t* ps = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB + kDenseStage);  // [2][8][16]
+
+  float o[8][4];  // O'^T fragments: m-tile mt, rows = channels, cols = heads
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.0f;
+  for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) racc[i][h] = 0.0f;
-  }
+    for (int k = 0; k < 4; ++k) o[mt][k] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2*tig, 2*tig+1
 
   auto make_task = [&](int it, int tg) -> Task {
     Task t{};
     if (it >= i1) return t;
     t.item = it;
-    if (it < ui.n_dch) {
+    if (it < n_dch) {
       t.kind = 1;
-      t.j0 = it * kDC;
-      t.nd = min(kDC, ui.n_dense - t.j0);
+      t.j0 = it * kTG;
+      t.nd = min(kTG, n_dense - t.j0);
       return t;
     }
-    const int pi = it - ui.n_dch;
-    const int b = pi < ui.ns ? __ldg(my_ids + pi) : always_block(ud, ui.nblk, pi - ui.ns);
-    if (b < 0 || b >= ui.nblk) {
+    const int pi = it - n_dch;
+    const int b = pi < ns ? __ldg(my_ids + pi) : always_block(ud, nblk, pi - ns);
+    if (b < 0 || b >= nblk) {
       if (lane == 0) set_error(L, ERR_BAD_BLOCK, (int32_t)u, b);
       t.kind = 3;
       return t;
@@ -242,24 +258,23 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
     t.b = b;
     t.r = ud.r[seg_of_block(ud, b)];
     t.tg = tg;
-    t.n_live = min(B, ui.n_mid - b * B);
+    t.n_live = min(B, n_mid - b * B);
     return t;
   };
   auto advance = [&](const Task& t) -> Task {
-    if (t.kind == 2 && t.tg + TG < t.n_live) return make_task(t.item, t.tg + TG);
+    if (t.kind == 2 && t.tg + kTG < t.n_live) return make_task(t.item, t.tg + kTG);
     return make_task(t.item + kWarps, 0);
   };
-  // Dense rows of token j of this unit (sinks, then the window ring).
   auto dense_rows = [&](int j, const uint16_t*& kr, const uint16_t*& vr) {
     if (DENSE) {
       const int64_t off = (((int64_t)ci * L.n_kv + kvh) * t_stride + j) * D;
       kr = Kd + off;
       vr = Vd + off;
-    } else if (j < ui.n_sink) {
+    } else if (j < n_sink) {
       kr = reinterpret_cast<const uint16_t*>(base + L.off_sink_k) + (int64_t)j * D;
       vr = reinterpret_cast<const uint16_t*>(base + L.off_sink_v) + (int64_t)j * D;
     } else {
-      const int p = ui.win_lo + (j - ui.n_sink);
+      const int p = win_lo + (j - n_sink);
       const int64_t sl = (int64_t)((p - S) % W) * D;
       kr = reinterpret_cast<const uint16_t*>(base + L.off_win_k) + sl;
       vr = reinterpret_cast<const uint16_t*>(base + L.off_win_v) + sl;
@@ -267,19 +282,19 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
   };
   auto issue = [&](const Task& t, unsigned char* dst) {
     if (t.kind == 1) {
-      // K rows padded to 272 bytes, then V rows of 256 bytes.
+      // K tile then V tile, rows padded to 272 bytes.
       for (int i = lane; i < t.nd * 16; i += 32) {
         const int row = i >> 4, part = i & 15;
         const uint16_t *kr, *vr;
         dense_rows(t.j0 + row, kr, vr);
-        cp_async16(dst + row * kKRow * 2 + part * 16, kr + part * 8);
-        cp_async16(dst + kDC * kKRow * 2 + row * D * 2 + part * 16, vr + part * 8);
+        cp_async16(dst + row * kRow * 2 + part * 16, kr + part * 8);
+        cp_async16(dst + kTile * 2 + row * kRow * 2 + part * 16, vr + part * 8);
       }
     } else if (t.kind == 2) {
-      // This group's rows of the page's four sub-arrays.  B is a multiple of
-      // TG, so whole groups stay inside the page; sizes and offsets are
-      // multiples of 16 bytes.
-      const int Br = B * t.r, gr = TG * t.r;
+      // This group's rows of the page's four sub-arrays (B is a multiple of
+      // 16, so a whole group stays inside the page; sizes and offsets are
+      // multiples of 16 bytes).
+      const int Br = B * t.r, gr = kTG * t.r;
       const char* page = base + L.off_pages + (int64_t)t.b * L.page_stride;
       const char* src[4] = {page + 2 * t.tg * t.r, page + 2 * Br + t.tg * t.r, page + 3 * Br + 2 * t.tg * t.r,
                             page + 5 * Br + t.tg * t.r};
@@ -292,163 +307,145 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
       }
     }
   };
-  // Online-softmax update of this warp's state (log2 domain).
-  auto softmax_update = [&](const float (&s)[G], bool valid, float (&p)[G], float (&alpha)[G]) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float sh = valid ? s[h] : -INFINITY;
-      const float mn = fmaxf(m[h], warp_max(sh));
-      alpha[h] = exp2f(m[h] - mn);
-      p[h] = valid ? exp2f(sh - mn) : 0.0f;
-      l[h] = l[h] * alpha[h] + warp_sum(p[h]);
-      m[h] = mn;
-    }
-  };
-  auto rescale = [&](const float (&alpha)[G]) {
-    for (int k = 0; k < NC; ++k)
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int h = 0; h < G; ++h) acc[(k * D + 4 * lane + i) * G + h] *= alpha[h];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int h = 0; h < G; ++h) racc[i][h] *= alpha[h];
-  };
 
   Task cur = make_task(i0 + warp, 0);
   int st = 0;
-  issue(cur, stg);
+  issue(cur, my_area);
   cp_async_commit();
   while (cur.kind != 0) {
     const Task nxt = advance(cur);
     if (NST == 2) {
-      issue(nxt, stg + (size_t)(st ^ 1) * SB);
+      issue(nxt, my_area + (size_t)(st ^ 1) * SB);
       cp_async_commit();
       asm volatile("cp.async.wait_group 1;\n" ::: "memory");
     } else {
       cp_async_wait_all();
     }
     __syncwarp();
-    const unsigned char* buf = stg + (size_t)st * SB;
-    if (cur.kind == 1) {
-      // Dense chunk.  K: lane = token, 8 channels per 16-byte load (rows
-      // padded so the 8 lanes of a phase hit distinct banks).  V: lanes own
-      // channels 4*lane .. 4*lane+3 and accumulate in registers.
-      const uint16_t* Ks = reinterpret_cast<const uint16_t*>(buf);
-      const uint16_t* Vs = reinterpret_cast<const uint16_t*>(buf + kDC * kKRow * 2);
-      const bool valid = lane < cur.nd;
-      float s[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) s[h] = 0.0f;
-      if (valid) {
-#pragma unroll 2
-        for (int c8 = 0; c8 < D; c8 += 8) {
-          const uint4 kk = *reinterpret_cast<const uint4*>(Ks + lane * kKRow + c8);
-          const float kf[8] = {bf2f(kk.x & 0xffff), bf2f(kk.x >> 16), bf2f(kk.y & 0xffff), bf2f(kk.y >> 16),
-                               bf2f(kk.z & 0xffff), bf2f(kk.z >> 16), bf2f(kk.w & 0xffff), bf2f(kk.w >> 16)};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float qv[G];
-            load_q<G>(qs, c8 + i, qv);
-#pragma unroll
-            for (int h = 0; h < G; ++h) s[h] = fmaf(qv[h], kf[i], s[h]);
+    const unsigned char* buf = my_area + (size_t)st * SB;
+    if (cur.kind == 1 || cur.kind == 2) {
+      const uint16_t* Kt;
+      const uint16_t* Vt;
+      int ntok;
+      if (cur.kind == 1) {
+        Kt = reinterpret_cast<const uint16_t*>(buf);
+        Vt = Kt + kTile;
+        ntok = cur.nd;
+        if (ntok < kTG) {
+          // rows past the chunk hold stale bytes: zero them (0 * NaN would poison P.V)
+          uint16_t* kb = const_cast<uint16_t*>(Kt);
+          for (int i = lane; i < (kTG - ntok) * 16; i += 32) {
+            const int row = ntok + (i >> 4), part = i & 15;
+            *reinterpret_cast<uint4*>(kb + row * kRow + part * 8) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(kb + kTile + row * kRow + part * 8) = make_uint4(0, 0, 0, 0);
           }
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) s[h] *= kScaleLog2;
-      float p[G], alpha[G];
-      softmax_update(s, valid, p, alpha);
-      rescale(alpha);
-#pragma unroll
-      for (int h = 0; h < G; ++h) pt[lane * G + h] = p[h];
-      __syncwarp();
-      for (int t = 0; t < cur.nd; ++t) {
-        float pp[G];
-        load_q<G>(pt, t, pp);
-        const uint2 v4 = *reinterpret_cast<const uint2*>(Vs + t * D + 4 * lane);
-        const float vf[4] = {bf2f(v4.x & 0xffff), bf2f(v4.x >> 16), bf2f(v4.y & 0xffff), bf2f(v4.y >> 16)};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int h = 0; h < G; ++h) racc[i][h] = fmaf(pp[h], vf[i], racc[i][h]);
-      }
-    } else if (cur.kind == 2) {
-      const int r = cur.r, gr = TG * r;
-      const uint16_t* Kv = reinterpret_cast<const uint16_t*>(buf);
-      const uint8_t* Ki = buf + 2 * gr;
-      const uint16_t* Vv = reinterpret_cast<const uint16_t*>(buf + 3 * gr);
-      const uint8_t* Vi = buf + 5 * gr;
-      const int ntok = min(TG, cur.n_live - cur.tg);
-      const bool valid = lane < ntok;
-      float s[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) s[h] = 0.0f;
-      if (valid) {
-        const int row = lane * r;
-        if ((r & 1) == 0) {
-          const uint16_t* ki2 = reinterpret_cast<const uint16_t*>(Ki + row);
-          const uint32_t* kv2 = reinterpret_cast<const uint32_t*>(Kv + row);
-#pragma unroll 2
-          for (int jj = 0; jj < (r >> 1); ++jj) {
-            const uint32_t ip = ki2[jj], vp = kv2[jj];
-            float q0[G], q1[G];
-            load_q<G>(qs, ip & 0xff, q0);
-            load_q<G>(qs, ip >> 8, q1);
-            const float v0 = bf2f(vp & 0xffff), v1 = bf2f(vp >> 16);
-#pragma unroll
-            for (int h = 0; h < G; ++h) s[h] = fmaf(q1[h], v1, fmaf(q0[h], v0, s[h]));
-          }
-        } else {
-          for (int jj = 0; jj < r; ++jj) {
-            float qv[G];
-            load_q<G>(qs, Ki[row + jj], qv);
-            const float kv = bf2f(Kv[row + jj]);
-#pragma unroll
-            for (int h = 0; h < G; ++h) s[h] = fmaf(qv[h], kv, s[h]);
-          }
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) s[h] *= kScaleLog2;
-      float p[G], alpha[G];
-      softmax_update(s, valid, p, alpha);
-      rescale(alpha);
-#pragma unroll
-      for (int h = 0; h < G; ++h) pt[lane * G + h] = p[h];
-      __syncwarp();
-      if (NC > 1) {
-        // Flattened element stream: element e = t*r + j of this group.  The
-        // 32 elements of one instruction span at most NC consecutive tokens,
-        // each writing its own accumulator copy (t mod NC), so no two lanes
-        // of an instruction touch the same address.
-        const int total = ntok * r;
-        int t = lane / r, j = lane - t * r, k = t % NC;
-        for (int e = lane; e < total; e += 32) {
-          float pp[G];
-          load_q<G>(pt, t, pp);
-          fma_vec<G>(acc + (k * D + Vi[e]) * G, pp, bf2f(Vv[e]));
-          j += 32;
-          while (j >= r) {
-            j -= r;
-            ++t;
-            if (++k == NC) k = 0;
-          }
+          __syncwarp();
         }
       } else {
-        for (int t = 0; t < ntok; ++t) {
-          float pp[G];
-          load_q<G>(pt, t, pp);
-          for (int jj = lane; jj < r; jj += 32) fma_vec<G>(acc + Vi[t * r + jj] * G, pp, bf2f(Vv[t * r + jj]));
-          __syncwarp();
+        // Rebuild positions: zero both tiles, scatter kept values by index.
+        uint4* z = reinterpret_cast<uint4*>(tiles);
+#pragma unroll
+        for (int i = lane; i < kDenseStage / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        const int r = cur.r, gr = kTG * r;
+        ntok = min(kTG, cur.n_live - cur.tg);
+        const int t = lane & 15;
+        const bool is_v = lane >= 16;
+        if (t < ntok) {
+          const uint16_t* val = reinterpret_cast<const uint16_t*>(buf + (is_v ? 3 * gr : 0)) + t * r;
+          const uint8_t* idx = buf + (is_v ? 5 * gr : 2 * gr) + t * r;
+          uint16_t* row = tiles + (is_v ? kTile : 0) + t * kRow;
+          if ((r & 1) == 0) {
+            const uint16_t* i2 = reinterpret_cast<const uint16_t*>(idx);
+            const uint32_t* v2 = reinterpret_cast<const uint32_t*>(val);
+#pragma unroll 4
+            for (int jj = 0; jj < (r >> 1); ++jj) {
+              const uint32_t ip = i2[jj], vp = v2[jj];
+              row[ip & 0xff] = (uint16_t)(vp & 0xffff);
+              row[ip >> 8] = (uint16_t)(vp >> 16);
+            }
+          } else {
+            for (int jj = 0; jj < r; ++jj) row[idx[jj]] = val[jj];
+          }
+        }
+        __syncwarp();
+        Kt = tiles;
+        Vt = tiles + kTile;
+      }
+
+      // Logits S^T[token][head] = sum_c K[token][c] q'[head][c] (hi + lo parts).
+      float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      {
+        const int mi = lane >> 3, ri = lane & 7;
+        const uint16_t* arow = Kt + (ri + (mi & 1) * 8) * kRow + (mi >> 1) * 8;
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc) {
+          uint32_t a[4];
+          ldsm_x4(a, arow + kc * 16);
+          mma_bf16(s, a, bqh[kc][0], bqh[kc][1]);
+          mma_bf16(s, a, bql[kc][0], bql[kc][1]);
+        }
+      }
+      // Online softmax over this group's tokens (g, g+8) for heads 2tig, 2tig+1.
+      const bool v_lo = g < ntok, v_hi = g + 8 < ntok;
+      const float s00 = v_lo ? s[0] * kScaleLog2 : -INFINITY, s01 = v_lo ? s[1] * kScaleLog2 : -INFINITY;
+      const float s10 = v_hi ? s[2] * kScaleLog2 : -INFINITY, s11 = v_hi ? s[3] * kScaleLog2 : -INFINITY;
+      float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, off));
+      }
+      const float mn0 = fmaxf(m0, x0), mn1 = fmaxf(m1, x1);
+      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+      const float p00 = exp2f(s00 - mn0), p01 = exp2f(s01 - mn1);
+      const float p10 = exp2f(s10 - mn0), p11 = exp2f(s11 - mn1);
+      float y0 = p00 + p10, y1 = p01 + p11;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        y0 += __shfl_xor_sync(FULL, y0, off);
+        y1 += __shfl_xor_sync(FULL, y1, off);
+      }
+      l0 = l0 * a0 + y0;
+      l1 = l1 * a1 + y1;
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= a0;
+        o[mt][1] *= a1;
+        o[mt][2] *= a0;
+        o[mt][3] *= a1;
+      }
+      // P (hi, lo) to shared memory as [head][token], read back as B fragments.
+      {
+        uint16_t h, lw;
+        const int h0 = 2 * tig, h1 = 2 * tig + 1;
+        split_bf16(p00, h, lw); ps[h0 * kTG + g] = h; ps[128 + h0 * kTG + g] = lw;
+        split_bf16(p01, h, lw); ps[h1 * kTG + g] = h; ps[128 + h1 * kTG + g] = lw;
+        split_bf16(p10, h, lw); ps[h0 * kTG + g + 8] = h; ps[128 + h0 * kTG + g + 8] = lw;
+        split_bf16(p11, h, lw); ps[h1 * kTG + g + 8] = h; ps[128 + h1 * kTG + g + 8] = lw;
+      }
+      __syncwarp();
+      const uint32_t* ps32 = reinterpret_cast<const uint32_t*>(ps);
+      const uint32_t pbh0 = ps32[(g * kTG + 2 * tig) >> 1], pbh1 = ps32[(g * kTG + 2 * tig + 8) >> 1];
+      const uint32_t pbl0 = ps32[(128 + g * kTG + 2 * tig) >> 1], pbl1 = ps32[(128 + g * kTG + 2 * tig + 8) >> 1];
+      // O'^T[channel][head] += sum_token V[token][channel] P[token][head].
+      {
+        const int mi = lane >> 3, ri = lane & 7;
+        const uint16_t* vrow = Vt + (ri + (mi >> 1) * 8) * kRow + (mi & 1) * 8;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_t(a, vrow + mt * 16);
+          mma_bf16(o[mt], a, pbh0, pbh1);
+          mma_bf16(o[mt], a, pbl0, pbl1);
         }
       }
     }
     __syncwarp();
     if (NST == 1) {
-      // single stage: fetch the next item only once this one is consumed
-      issue(nxt, stg);
+      issue(nxt, my_area);
       cp_async_commit();
     }
     cur = nxt;
@@ -457,73 +454,126 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
   cp_async_wait_all();
   __syncwarp();
 
-  // Fold the accumulator copies and the register (dense) accumulators into copy 0.
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const int c = 4 * lane + i;
-      float a = acc[c * G + h] + racc[i][h];
-      for (int k = 1; k < NC; ++k) a += acc[(k * D + c) * G + h];
-      acc[c * G + h] = a;
+  // ---- merge: warps -> CTA ------------------------------------------------
+  if (g == 0) {
+    mlw[(warp * 8 + 2 * tig) * 2] = m0;
+    mlw[(warp * 8 + 2 * tig) * 2 + 1] = l0;
+    mlw[(warp * 8 + 2 * tig + 1) * 2] = m1;
+    mlw[(warp * 8 + 2 * tig + 1) * 2 + 1] = l1;
+  }
+  __syncthreads();
+  float* dump = reinterpret_cast<float*>(warp_area);  // [kWarps][G][D], main loop is over
+  {
+    float e0 = 0.0f, e1 = 0.0f;
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+    float M0 = -INFINITY, M1 = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) {
+      M0 = fmaxf(M0, mlw[(w * 8 + h0) * 2]);
+      M1 = fmaxf(M1, mlw[(w * 8 + h1) * 2]);
     }
-  if (lane == 0) {
+    if (m0 != -INFINITY) e0 = exp2f(m0 - M0);
+    if (m1 != -INFINITY) e1 = exp2f(m1 - M1);
+    float* dw = dump + (size_t)warp * G * D;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      mlw[(warp * G + h) * 2] = m[h];
-      mlw[(warp * G + h) * 2 + 1] = l[h];
+    for (int mt = 0; mt < 8; ++mt) {
+      const int c = mt * 16 + g;
+      if (h0 < G) {
+        dw[h0 * D + c] = o[mt][0] * e0;
+        dw[h0 * D + c + 8] = o[mt][2] * e0;
+      }
+      if (h1 < G) {
+        dw[h1 * D + c] = o[mt][1] * e1;
+        dw[h1 * D + c + 8] = o[mt][3] * e1;
+      }
     }
   }
   __syncthreads();
-  // CTA partial: (m, l, acc) merged over the warps.
   for (int i = tid; i < G * D; i += blockDim.x) {
-    const int h = i / D, c = i % D;
+    float a = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) a += dump[(size_t)w * G * D + i];
+    cl_acc[i] = a;
+  }
+  if (tid < G) {
     float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mlw[(w * G + h) * 2]);
-    float a = 0.0f, ls = 0.0f;
-    if (M != -INFINITY) {
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mlw[(w * 8 + tid) * 2]);
+    float ls = 0.0f;
+    if (M != -INFINITY)
       for (int w = 0; w < kWarps; ++w) {
-        const float mw = mlw[(w * G + h) * 2];
-        if (mw == -INFINITY) continue;
-        const float e = exp2f(mw - M);
-        a = fmaf(accw[(w * NC * D + c) * G + h], e, a);
-        ls = fmaf(mlw[(w * G + h) * 2 + 1], e, ls);
+        const float mw = mlw[(w * 8 + tid) * 2];
+        if (mw != -INFINITY) ls += mlw[(w * 8 + tid) * 2 + 1] * exp2f(mw - M);
       }
-    }
-    cl_acc[h * D + c] = a;
-    if (c == 0) {
-      cl_ml[h * 2] = M;
-      cl_ml[h * 2 + 1] = ls;
-    }
+    cl_ml[tid * 2] = M;
+    cl_ml[tid * 2 + 1] = ls;
   }
   cluster.sync();
 
-  // Merge the cluster's partials for this CTA's channel slice and broadcast
-  // the normalised o' slice to every CTA of the cluster.
-  const int w = D / C;
-  const int c_lo = rank * w;
+  // ---- merge: CTAs -> cluster, for this CTA's channel slice ---------------
+  const int w = D / C, c_lo = rank * w;
+  float* part_acc = L.part_acc + slot * MK_MAX_SPLITS * G * D;
+  float* part_ml = L.part_ml + slot * MK_MAX_SPLITS * G * 2;
   for (int i = tid; i < G * w; i += blockDim.x) {
     const int h = i / w, c = c_lo + (i - h * w);
     float M = -INFINITY;
     for (int r2 = 0; r2 < C; ++r2) M = fmaxf(M, cluster.map_shared_rank(cl_ml, r2)[h * 2]);
-    float o = 0.0f, ls = 0.0f;
-    if (M != -INFINITY) {
+    float a = 0.0f, ls = 0.0f;
+    if (M != -INFINITY)
       for (int r2 = 0; r2 < C; ++r2) {
         const float* ml = cluster.map_shared_rank(cl_ml, r2);
         const float mr = ml[h * 2];
         if (mr == -INFINITY) continue;
         const float e = exp2f(mr - M);
-        o = fmaf(cluster.map_shared_rank(cl_acc, r2)[h * D + c], e, o);
+        a = fmaf(cluster.map_shared_rank(cl_acc, r2)[h * D + c], e, a);
         ls = fmaf(ml[h * 2 + 1], e, ls);
       }
+    if (Q == 1) {
+      const float v = ls > 0.0f ? a / ls : 0.0f;
+      for (int r2 = 0; r2 < C; ++r2) cluster.map_shared_rank(ofull, r2)[h * D + c] = v;
+    } else {
+      part_acc[((size_t)qi * G + h) * D + c] = a;
+      if (i - h * w == 0 && rank == 0) {
+        part_ml[((size_t)qi * G + h) * 2] = M;
+        part_ml[((size_t)qi * G + h) * 2 + 1] = ls;
+      }
     }
-    const float v = ls > 0.0f ? o / ls : 0.0f;
-    for (int r2 = 0; r2 < C; ++r2) cluster.map_shared_rank(ofull, r2)[h * D + c] = v;
+  }
+  if (Q > 1) {
+    // ---- merge: clusters -> unit (last cluster to arrive) -----------------
+    __threadfence();
+    cluster.sync();
+    if (rank == 0 && tid == 0) {
+      const int prev = atomicAdd(&L.counters[slot], 1);
+      *flag = (prev == Q - 1);
+      if (prev == Q - 1) L.counters[slot] = 0;
+    }
+    cluster.sync();
+    const int last = *cluster.map_shared_rank(flag, 0);
+    if (!last) {
+      cluster.sync();  // same barrier count in every CTA of the cluster
+      return;
+    }
+    __threadfence();
+    for (int i = tid; i < G * w; i += blockDim.x) {
+      const int h = i / w, c = c_lo + (i - h * w);
+      float M = -INFINITY;
+      for (int q2 = 0; q2 < Q; ++q2) M = fmaxf(M, __ldcg(part_ml + ((size_t)q2 * G + h) * 2));
+      float a = 0.0f, ls = 0.0f;
+      if (M != -INFINITY)
+        for (int q2 = 0; q2 < Q; ++q2) {
+          const float mq = __ldcg(part_ml + ((size_t)q2 * G + h) * 2);
+          if (mq == -INFINITY) continue;
+          const float e = exp2f(mq - M);
+          a = fmaf(__ldcg(part_acc + ((size_t)q2 * G + h) * D + c), e, a);
+          ls = fmaf(__ldcg(part_ml + ((size_t)q2 * G + h) * 2 + 1), e, ls);
+        }
+      const float v = ls > 0.0f ? a / ls : 0.0f;
+      for (int r2 = 0; r2 < C; ++r2) cluster.map_shared_rank(ofull, r2)[h * D + c] = v;
+    }
   }
   cluster.sync();
   if (s_abort) return;
 
-  // Output channels [c_lo, c_lo + w): out_j = sum_c o'_c R_v[c][j].
+  // ---- output channels [c_lo, c_lo + w): out_j = sum_c o'_c R_v[c][j] ------
   uint16_t* orow = out + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D;
   if (DENSE) {
     for (int i = tid; i < G * w; i += blockDim.x) {
@@ -532,7 +582,8 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
     }
     return;
   }
-  float* rvs = reinterpret_cast<float*>(stages);  // [128][w]: staged R_v columns
+  float* rvs = reinterpret_cast<float*>(warp_area);   // [128][w] staged R_v columns
+  float* red = rvs + D * w;                           // [parts][G*w]
   const float* Rv = reinterpret_cast<const float*>(base + L.off_rv);
   const int w4 = w / 4;
   for (int i = tid; i < D * w4; i += blockDim.x) {
@@ -542,32 +593,84 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
-  // Each output (h, j) is split over `parts` threads, combined through smem.
   const int outs = G * w;
   const int parts = max(1, (int)blockDim.x / outs);
   const int cper = D / parts;
-  float* red = accw;  // free now: [parts][outs]
   for (int i = tid; i < outs * parts; i += blockDim.x) {
-    const int o = i % outs, pidx = i / outs;
-    const int h = o / w, jl = o - h * w;
+    const int oo = i % outs, pidx = i / outs;
+    const int h = oo / w, jl = oo - h * w;
     float a = 0.0f;
     for (int c = pidx * cper; c < (pidx + 1) * cper; ++c) a = fmaf(ofull[h * D + c], rvs[c * w + jl], a);
-    red[pidx * outs + o] = a;
+    red[pidx * outs + oo] = a;
   }
   __syncthreads();
-  for (int o = tid; o < outs; o += blockDim.x) {
+  for (int oo = tid; oo < outs; oo += blockDim.x) {
     float a = 0.0f;
-    for (int pidx = 0; pidx < parts; ++pidx) a += red[pidx * outs + o];
-    const int h = o / w, jl = o - h * w;
+    for (int pidx = 0; pidx < parts; ++pidx) a += red[pidx * outs + oo];
+    const int h = oo / w, jl = oo - h * w;
     orow[h * D + c_lo + jl] = f2bf(a);
   }
 }
 
 namespace {
+// Cluster size C and clusters per unit Q: every cluster resident at once
+// (checked against cudaOccupancyMaxActiveClusters), as many CTAs as the SMs
+// allow, preferring larger clusters when the CTA count is within 90%.
+template <int G, bool DENSE>
+void choose_grid(int units, int max_items, size_t smem, int& C, int& Q) {
+  static int max_active[17];
+  static size_t for_smem = 0;
+  if (for_smem != smem) {
+    for (int c = 1; c <= 16; c *= 2) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(c, 1, 1);
+      cfg.blockDim = dim3(256, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = c;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_attn<G, DENSE>, &cfg);
+      if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      max_active[c] = n;
+      if (std::getenv("MK_LOG"))
+        std::fprintf(stderr, "[mosaickv] attention G=%d dense=%d smem=%zu: cluster %d -> %d resident\n", G,
+                     (int)DENSE, smem, c, n);
+    }
+    for_smem = smem;
+  }
+  int best = 0;
+  for (int c = 1; c <= 16; c *= 2) {
+    if (max_active[c] < units) continue;
+    int q = std::min(MK_MAX_SPLITS, max_active[c] / units);
+    q = std::min(q, std::max(1, max_items / (2 * c)));
+    best = std::max(best, units * q * c);
+  }
+  C = 1;
+  Q = 1;
+  for (int c = 16; c >= 1; c /= 2) {
+    if (max_active[c] < units) continue;
+    int q = std::min(MK_MAX_SPLITS, max_active[c] / units);
+    q = std::min(q, std::max(1, max_items / (2 * c)));
+    if ((int64_t)units * q * c * 10 >= (int64_t)best * 9) {
+      C = c;
+      Q = q;
+      break;
+    }
+  }
+}
+
 template <int G, bool DENSE>
 cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                        const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
-                       int cluster, size_t smem, cudaStream_t s) {
+                       int max_items, size_t smem, cudaStream_t s) {
   static size_t set_bytes = 0;
   if (smem > set_bytes) {
     cudaError_t e = cudaFuncSetAttribute(k_attn<G, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -576,76 +679,39 @@ cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int
     if (e != cudaSuccess) return e;
     set_bytes = smem;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // Halve the cluster until one cluster of it can be resident (checked once
-  // per cluster size and shared-memory size).
-  static int verified[17] = {0};
-  static size_t verified_smem = 0;
-  if (verified_smem != smem) {
-    for (int i = 0; i < 17; ++i) verified[i] = 0;
-    verified_smem = smem;
-  }
-  while (cluster > 1) {
-    if (verified[cluster] == 0) {
-      cfg.gridDim = dim3(cluster, 1, 1);
-      attr[0].val.clusterDim.x = cluster;
-      int n = 0;
-      const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_attn<G, DENSE>, &cfg);
-      if (e != cudaSuccess) (void)cudaGetLastError();
-      verified[cluster] = (e == cudaSuccess && n > 0) ? 1 : -1;
-      if (std::getenv("MK_LOG"))
-        std::fprintf(stderr, "[mosaickv] attention G=%d dense=%d smem=%zu cluster=%d: max active clusters %d (%s)\n",
-                     G, (int)DENSE, smem, cluster, n, cudaGetErrorString(e));
-    }
-    if (verified[cluster] == 1) break;
-    cluster /= 2;
-  }
-  cfg.gridDim = dim3(cluster * cs.n * L.n_kv, 1, 1);
-  attr[0].val.clusterDim.x = cluster;
-  return cudaLaunchKernelEx(&cfg, k_attn<G, DENSE>, L, layer, cs, ids, n_sel, q, K, V, t_stride, out);
+  const int units = cs.n * L.n_kv;
+  int C = 1, Q = 1;
+  choose_grid<G, DENSE>(units, max_items, smem, C, Q);
+  if (std::getenv("MK_LOG"))
+    std::fprintf(stderr, "[mosaickv] attention launch: %d units x Q=%d clusters x C=%d CTAs\n", units, Q, C);
+  return launch_pdl(k_attn<G, DENSE>, dim3(units * Q * C), dim3(256), smem, s, C, L, layer, cs, Q, ids, n_sel, q,
+                    K, V, t_stride, out);
 }
 
 template <bool DENSE>
 cudaError_t launch_attn_g(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                           const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
-                          int cluster, cudaStream_t s) {
+                          int max_items, cudaStream_t s) {
   const size_t smem = attn_smem_bytes(L, 0);
   if (smem == 0 || smem > 227 * 1024) return cudaErrorInvalidConfiguration;
   switch (L.G) {
-    case 1: return launch_one<1, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, cluster, smem, s);
-    case 2: return launch_one<2, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, cluster, smem, s);
-    case 4: return launch_one<4, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, cluster, smem, s);
-    case 8: return launch_one<8, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, cluster, smem, s);
+    case 1: return launch_one<1, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+    case 2: return launch_one<2, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+    case 4: return launch_one<4, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+    case 8: return launch_one<8, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }
 }  // namespace
 
-// Cluster size per (sequence, kv head): a power of two <= 16 (so that 128
-// output channels split evenly) giving at most about one CTA per SM.
-int attn_cluster_size(int n_units) {
-  int c = 1;
-  while (c < 16 && (int64_t)n_units * c * 2 <= 152) c *= 2;
-  return c;
-}
-
 cudaError_t launch_decode_attn(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids,
-                               const int32_t* n_sel, uint16_t* out, int cluster, cudaStream_t s) {
-  return launch_attn_g<false>(L, layer, cs, ids, n_sel, nullptr, nullptr, nullptr, 0, out, cluster, s);
+                               const int32_t* n_sel, uint16_t* out, int max_items, cudaStream_t s) {
+  return launch_attn_g<false>(L, layer, cs, ids, n_sel, nullptr, nullptr, nullptr, 0, out, max_items, s);
 }
 
 cudaError_t launch_dense_attn(const Layout& L, const CallSeqs& cs, const uint16_t* q, const uint16_t* K,
-                              const uint16_t* V, int64_t t_stride, uint16_t* out, int cluster, cudaStream_t s) {
-  return launch_attn_g<true>(L, 0, cs, nullptr, nullptr, q, K, V, t_stride, out, cluster, s);
+                              const uint16_t* V, int64_t t_stride, uint16_t* out, int max_items, cudaStream_t s) {
+  return launch_attn_g<true>(L, 0, cs, nullptr, nullptr, q, K, V, t_stride, out, max_items, s);
 }
 
 }  // namespace mk

@@ -56,7 +56,7 @@ struct Layout {
   float* scores;                // [max_seqs][n_kv][nblk_cap]
   float* part_acc;              // [max_seqs][n_kv][MK_MAX_SPLITS][G][128]
   float* part_ml;               // [max_seqs][n_kv][MK_MAX_SPLITS][G][2]
-  int32_t* counters;            // [max_seqs][n_kv]
+  int32_t* counters;            // [2][max_seqs][n_kv]: attention merge, selection top-k
 };
 
 // Per-call sequence list, passed by value.
@@ -165,8 +165,44 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
 }
+// Programmatic dependent launch: a kernel launched with the
+// programmatic-serialization attribute may start while the previous kernel
+// in the stream finishes.  It must call pdl_wait() before touching anything
+// the previous kernel writes; it calls pdl_trigger() right after its own wait,
+// so that whatever a kernel reads before its wait was complete two launches
+// earlier.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 __device__ __forceinline__ char* unit_base(const Layout& L, int64_t u) {
   return L.units + u * L.unit_stride;
+}
+#endif
+
+#ifdef __CUDACC__
+// Launch with programmatic stream serialization (and an optional cluster size).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster > 0) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 #endif
 
@@ -179,13 +215,14 @@ cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, c
 cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,
                                 int32_t* ids, int32_t* n_sel, float* scores_out, int max_nblk,
                                 cudaStream_t s);
+// max_items: the largest number of attention work items (16-token dense
+// chunks + selected/always pages) of any (sequence, kv head) in the call.
 cudaError_t launch_decode_attn(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids,
-                               const int32_t* n_sel, uint16_t* out, int cluster, cudaStream_t s);
+                               const int32_t* n_sel, uint16_t* out, int max_items, cudaStream_t s);
 cudaError_t launch_dense_attn(const Layout& L, const CallSeqs& cs, const uint16_t* q,
                               const uint16_t* K, const uint16_t* V, int64_t t_stride,
-                              uint16_t* out, int cluster, cudaStream_t s);
+                              uint16_t* out, int max_items, cudaStream_t s);
 size_t attn_plan(Layout& L, int r_min);
-int attn_cluster_size(int n_units);
 cudaError_t launch_gram(const uint16_t* x, int64_t n_rows, int64_t row_stride, float* gram,
                         cudaStream_t s);
 size_t attn_smem_bytes(const Layout& L, int r_max);

@@ -2,14 +2,36 @@
 // from its per-channel min/max keys, keep the top-k blocks.
 //
 // Method: "MosaicKV：...阅读笔记" (zhongzhuzhou.org), Eq. (12) (block score
-// from the compressed keys, with q' the rotated query) and the description
+// from the compressed keys with the rotated query q') and the description
 // of Quest's per-block min/max bound; "MosaicKV: Serving Long-Context LLM
 // with Dynamic Two-D KV Cache Compression" (paperlayer.ai), sec. 4.2 stage 2
 // (top-k token blocks before each decode attention layer) and sec. 5.3
 // (inverse rotation merged into the query).
+//
+// GB300 structure: one kernel, P CTAs per (sequence, kv head).
+//  * Each CTA stages R_k^T (cp.async) and forms q' for the group's heads.
+//  * Scoring is a dense contraction: for block b and head h,
+//      sum_j max(q'_hj mn_bj, q'_hj mx_bj) = [mn_b | mx_b] . [min(q'_h,0) | max(q'_h,0)]
+//    over K = 256.  Meta tiles of 16 blocks are staged with cp.async and
+//    multiplied on the tensor cores (mma.sync m16n8k16).  The fp32 operand is
+//    split exactly into three bf16 parts (24 = 3 x 8 significant bits) and the
+//    meta values are bf16, so every product is exact and the accumulation is
+//    fp32: the scores keep fp32 accuracy.
+//  * The last CTA of each (sequence, kv head) to finish (atomic counter, no
+//    waiting) runs the radix top-k over the unit's scores in shared memory.
+#include <algorithm>
+
 #include "mk_internal.cuh"
 
 namespace mk {
+
+namespace {
+constexpr int kSelWarps = 8;
+constexpr int kMT = 16;                       // blocks per MMA tile
+constexpr int kMetaRow = 2 * D + 8;           // padded bf16 row (528 bytes): ldmatrix conflict-free
+constexpr int kMetaTile = kMT * kMetaRow * 2; // bytes per staged tile
+constexpr int kSelSmem = kSelWarps * 2 * kMetaTile;  // double-buffered tiles (also holds R_k^T and keys)
+static_assert(kSelSmem >= D * D * 4, "R_k^T staging fits in the tile area");
 
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -17,146 +39,252 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// grid (chunks, n_seqs * n_kv); 256 threads.
-template <int G>
-__global__ void __launch_bounds__(256) k_score(Layout L, int layer, CallSeqs cs, const uint16_t* __restrict__ q,
-                                               float* __restrict__ scores_out) {
-  const int ci = blockIdx.y / L.n_kv, kvh = blockIdx.y - ci * L.n_kv;
-  const int seq = cs.seq[ci];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t u = unit_index(L, layer, seq, kvh);
-  __shared__ float qs[G][D];
-  __shared__ __align__(16) float qr[D][G];
-  __shared__ int s_abort, s_T;
-  if (tid == 0) {
-    s_abort = has_error(L);
-    s_T = L.desc[u].T;
-  }
-  for (int i = tid; i < G * D; i += blockDim.x) {
-    const int h = i / D, c = i % D;
-    qs[h][c] = bf2f(q[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G + h) * D + c]);
-  }
-  __syncthreads();
-  if (s_abort) return;
-  const char* base = unit_base(L, u);
-  extern __shared__ __align__(16) float Rs[];   // R_k^T [128][128]
-  {
-    const float4* src = reinterpret_cast<const float4*>(base + L.off_rkt);
-    for (int i = tid; i < D * D / 4; i += blockDim.x) cp_async16(reinterpret_cast<float4*>(Rs) + i, src + i);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
-  }
-  if (tid < D) {
-    float acc[G];
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Exact three-way split of an fp32 value into bf16 parts (x = p0 + p1 + p2
+// for normal x: each part takes the next 8 significant bits).
+__device__ __forceinline__ void split3(float x, uint16_t (&p)[3]) {
+  float r = x;
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-    for (int j = 0; j < D; ++j) {
-      const float rr = Rs[j * D + tid];
-#pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][j], rr, acc[h]);
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      qr[tid][h] = acc[h];
-      if (blockIdx.x == 0) L.qrot[(((int64_t)seq * L.n_kv + kvh) * G + h) * D + tid] = acc[h];
-    }
-  }
-  __syncthreads();
-  float qreg[4][G];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int h = 0; h < G; ++h) qreg[i][h] = qr[4 * lane + i][h];
-
-  const int nblk = n_mid_blocks(L, s_T);
-  const uint16_t* meta = reinterpret_cast<const uint16_t*>(base + L.off_meta);
-  float* sc = L.scores + ((int64_t)seq * L.n_kv + kvh) * L.nblk_cap;
-  float* so = scores_out ? scores_out + ((int64_t)ci * L.n_kv + kvh) * L.nblk_cap : nullptr;
-  const float inv_sqrt_d = 0.08838834764831845f;
-  for (int b = blockIdx.x * 8 + warp; b < nblk; b += gridDim.x * 8) {
-    const uint2 mn4 = __ldg(reinterpret_cast<const uint2*>(meta + (int64_t)b * 2 * D) + lane);
-    const uint2 mx4 = __ldg(reinterpret_cast<const uint2*>(meta + (int64_t)b * 2 * D + D) + lane);
-    const float mn[4] = {bf2f(mn4.x & 0xffff), bf2f(mn4.x >> 16), bf2f(mn4.y & 0xffff), bf2f(mn4.y >> 16)};
-    const float mx[4] = {bf2f(mx4.x & 0xffff), bf2f(mx4.x >> 16), bf2f(mx4.y & 0xffff), bf2f(mx4.y >> 16)};
-    float best = -INFINITY;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float s = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) s = fmaf(qreg[i][h], qreg[i][h] >= 0.0f ? mx[i] : mn[i], s);
-      s = warp_sum(s);
-      best = fmaxf(best, s);
-    }
-    best *= inv_sqrt_d;
-    if (lane == 0) {
-      sc[b] = best;
-      if (so) so[b] = best;
-    }
+  for (int i = 0; i < 3; ++i) {
+    const __nv_bfloat16 h = __float2bfloat16_rz(r);
+    p[i] = __bfloat16_as_ushort(h);
+    r -= __bfloat162float(h);
   }
 }
 
-// Block-wide exclusive scan of 0/1 flags over 1024 threads; returns the
-// prefix and writes the total to *total.
-__device__ __forceinline__ int block_flag_scan(bool f, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned bal = __ballot_sync(FULL, f);
-  const int in_warp = __popc(bal & ((1u << lane) - 1u));
+// Block-wide exclusive scan of per-thread counts; total in *total.
+__device__ __forceinline__ int block_count_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int ex_w = warp_excl_scan(v, lane);
   __syncthreads();
-  if (lane == 0) warp_tot[warp] = __popc(bal);
+  if (lane == 31) warp_tot[warp] = ex_w + v;
   __syncthreads();
   if (warp == 0) {
-    const int v = warp_tot[lane];
-    const int ex = warp_excl_scan(v, lane);
-    warp_tot[lane] = ex;
-    if (lane == 31) warp_tot[32] = ex + v;
+    const int t = lane < nw ? warp_tot[lane] : 0;
+    const int ex = warp_excl_scan(t, lane);
+    if (lane < nw) warp_tot[lane] = ex;
+    if (lane == 31) warp_tot[32] = ex + t;
   }
   __syncthreads();
   *total = warp_tot[32];
-  return warp_tot[warp] + in_warp;
+  return warp_tot[warp] + ex_w;
 }
+}  // namespace
 
-// One CTA (1024 threads) per (sequence, kv head): k largest scores among the
-// scored segments' blocks, ties to the lower id, written in ascending order.
-__global__ void __launch_bounds__(1024) k_topk(Layout L, int layer, CallSeqs cs, int32_t* __restrict__ ids,
-                                               int32_t* __restrict__ n_sel) {
-  const int ci = blockIdx.x / L.n_kv, kvh = blockIdx.x - ci * L.n_kv;
-  const int seq = cs.seq[ci];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t u = unit_index(L, layer, seq, kvh);
+// grid: P CTAs per (sequence, kv head) of the call; 256 threads.
+template <int G>
+__global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs cs, int P,
+                                                   const uint16_t* __restrict__ q, int32_t* __restrict__ ids,
+                                                   int32_t* __restrict__ n_sel, float* __restrict__ scores_out) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ float qs[G][D];
+  __shared__ float qr[2][G][D];
   __shared__ UnitDesc ud;
   __shared__ unsigned hist[256];
   __shared__ int warp_tot[33];
   __shared__ uint32_t s_prefix;
-  __shared__ int s_remaining, s_abort;
-  if (tid == 0) {
-    ud = L.desc[u];
-    s_abort = has_error(L);
+  __shared__ int s_rem, s_abort, s_last;
+
+  const int unit_call = blockIdx.x / P, part = blockIdx.x - unit_call * P;
+  const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
+  const int seq = cs.seq[ci];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tig = lane & 3;
+  const int64_t u = unit_index(L, layer, seq, kvh);
+  const int64_t slot = (int64_t)seq * L.n_kv + kvh;
+  for (int i = tid; i < G * D; i += blockDim.x)
+    qs[i / D][i % D] = bf2f(q[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D + i]);
+  const char* base = unit_base(L, u);
+  {
+    const float4* src = reinterpret_cast<const float4*>(base + L.off_rkt);
+    for (int i = tid; i < D * D / 4; i += blockDim.x) cp_async16(reinterpret_cast<float4*>(smem) + i, src + i);
+    cp_async_commit();
+    cp_async_wait_all();
   }
   __syncthreads();
+
+  // q'_h[c] = sum_j q_h[j] R_k[c][j]: thread (c, half of j), halves added.
+  {
+    const float* Rs = reinterpret_cast<const float*>(smem);
+    const int c = tid & (D - 1), half = tid >> 7;
+    float acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+    for (int j = half * 64; j < half * 64 + 64; ++j) {
+      const float rr = Rs[j * D + c];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][j], rr, acc[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) qr[half][h][c] = acc[h];
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += blockDim.x) {
+    const int h = i / D, c = i % D;
+    const float v = qr[0][h][c] + qr[1][h][c];
+    qr[0][h][c] = v;
+  }
+  __syncthreads();
+
+  // B fragments of [min(q',0) | max(q',0)] (k = 0..255, n = head), 3 exact parts.
+  uint32_t bq[3][16][2];
+#pragma unroll
+  for (int kc = 0; kc < 16; ++kc)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint16_t e0[3] = {0, 0, 0}, e1[3] = {0, 0, 0};
+      if (g < G) {
+        const int k = kc * 16 + hf * 8 + 2 * tig;
+        const float x0 = k < D ? fminf(qr[0][g][k], 0.0f) : fmaxf(qr[0][g][k - D], 0.0f);
+        const float x1 = (k + 1) < D ? fminf(qr[0][g][k + 1], 0.0f) : fmaxf(qr[0][g][k + 1 - D], 0.0f);
+        split3(x0, e0);
+        split3(x1, e1);
+      }
+#pragma unroll
+      for (int s = 0; s < 3; ++s) bq[s][kc][hf] = (uint32_t)e0[s] | ((uint32_t)e1[s] << 16);
+    }
+  // Everything above used only q and R_k.  From here on the kernel reads
+  // what the append kernel wrote (lengths, block keys).
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) {
+    s_abort = has_error(L);
+    ud = L.desc[u];
+  }
+  if (part == 0)
+    for (int i = tid; i < G * D; i += blockDim.x) L.qrot[slot * G * D + i] = qr[0][i / D][i % D];
+  __syncthreads();  // also: the R_k^T area becomes the tile stages
   if (s_abort) return;
+
   const int nblk = n_mid_blocks(L, ud.T);
+  const int ntiles = (nblk + kMT - 1) / kMT;
+  const int tper = (ntiles + P - 1) / P;
+  const int t0 = part * tper, t1 = min(ntiles, t0 + tper);
+  const uint16_t* meta = reinterpret_cast<const uint16_t*>(base + L.off_meta);
+  float* sc = L.scores + slot * L.nblk_cap;
+  float* so = scores_out ? scores_out + ((int64_t)ci * L.n_kv + kvh) * L.nblk_cap : nullptr;
+  unsigned char* stg = smem + (size_t)warp * 2 * kMetaTile;
+  auto issue = [&](int t, unsigned char* dst) {
+    if (t >= t1) return;
+    for (int i = lane; i < kMT * 32; i += 32) {
+      const int row = i >> 5, prt = i & 31;
+      const int b = t * kMT + row;
+      if (b < nblk) cp_async16(dst + row * kMetaRow * 2 + prt * 16, meta + (int64_t)b * 2 * D + prt * 8);
+    }
+  };
+  const float inv_sqrt_d = 0.08838834764831845f;
+  int st = 0;
+  int t = t0 + warp;
+  issue(t, stg);
+  cp_async_commit();
+  for (; t < t1; t += kSelWarps) {
+    issue(t + kSelWarps, stg + (size_t)(st ^ 1) * kMetaTile);
+    cp_async_commit();
+    asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+    __syncwarp();
+    const uint16_t* tile = reinterpret_cast<const uint16_t*>(stg + (size_t)st * kMetaTile);
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int mi = lane >> 3, ri = lane & 7;
+    const uint16_t* arow = tile + (ri + (mi & 1) * 8) * kMetaRow + (mi >> 1) * 8;
+#pragma unroll
+    for (int kc = 0; kc < 16; ++kc) {
+      uint32_t a[4];
+      ldsm_x4(a, arow + kc * 16);
+      mma_bf16(s, a, bq[0][kc][0], bq[0][kc][1]);
+      mma_bf16(s, a, bq[1][kc][0], bq[1][kc][1]);
+      mma_bf16(s, a, bq[2][kc][0], bq[2][kc][1]);
+    }
+    // rows: blocks g, g+8; columns: heads 2tig, 2tig+1 -> max over the group's heads
+    const bool h0 = 2 * tig < G, h1 = 2 * tig + 1 < G;
+    float b_lo = fmaxf(h0 ? s[0] : -INFINITY, h1 ? s[1] : -INFINITY);
+    float b_hi = fmaxf(h0 ? s[2] : -INFINITY, h1 ? s[3] : -INFINITY);
+    b_lo = fmaxf(b_lo, __shfl_xor_sync(FULL, b_lo, 1));
+    b_hi = fmaxf(b_hi, __shfl_xor_sync(FULL, b_hi, 1));
+    b_lo = fmaxf(b_lo, __shfl_xor_sync(FULL, b_lo, 2));
+    b_hi = fmaxf(b_hi, __shfl_xor_sync(FULL, b_hi, 2));
+    if (tig == 0) {
+      const int b0 = t * kMT + g, b1 = b0 + 8;
+      if (b0 < nblk) {
+        sc[b0] = b_lo * inv_sqrt_d;
+        if (so) so[b0] = b_lo * inv_sqrt_d;
+      }
+      if (b1 < nblk) {
+        sc[b1] = b_hi * inv_sqrt_d;
+        if (so) so[b1] = b_hi * inv_sqrt_d;
+      }
+    }
+    __syncwarp();
+    st ^= 1;
+  }
+  cp_async_wait_all();
+
+  // ---- the last CTA of this (sequence, kv head) selects the top-k ---------
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&L.counters[L.max_seqs * L.n_kv + slot], 1);
+    s_last = (prev == P - 1);
+    if (prev == P - 1) L.counters[L.max_seqs * L.n_kv + slot] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
   const int n_cand = n_scored_blocks(ud, nblk);
   const int k = n_select(L, n_cand);
-  const float* sc = L.scores + ((int64_t)seq * L.n_kv + kvh) * L.nblk_cap;
   int32_t* out = ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
+  const bool all = k >= n_cand;
+  // Thread t owns blocks [t*R, t*R + R); its keys sit at t*(R+1) + i in shared
+  // memory (odd stride: conflict-free).  Key 0 marks a block that is not a
+  // candidate (an always-attended segment or past the end); real scores never
+  // map to 0, and since k <= #candidates the top k never reach key 0.
+  const int nth = blockDim.x;
+  const int R = (nblk + nth - 1) / nth;
+  const int RS = R | 1;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+  const bool in_smem = (size_t)RS * nth * 4 <= (size_t)kSelSmem;
+  auto key_at = [&](int i) -> uint32_t {  // i-th key of this thread
+    const int b = tid * R + i;
+    if (b >= nblk) return 0u;
+    if (in_smem) return keys[tid * RS + i];
+    return ud.always[seg_of_block(ud, b)] ? 0u : ordered_key(__ldcg(sc + b));
+  };
+  if (in_smem) {
+    for (int i = 0; i < R; ++i) {
+      const int b = tid * R + i;
+      uint32_t key = 0u;
+      if (b < nblk && !ud.always[seg_of_block(ud, b)]) key = ordered_key(__ldcg(sc + b));
+      keys[tid * RS + i] = key;
+    }
+  }
+  __syncthreads();
 
   uint32_t prefix = 0, mask = 0;
   int need = 0;
-  const bool all = k >= n_cand;
   if (!all) {
-    if (tid == 0) s_remaining = k;
+    if (tid == 0) s_rem = k;
     for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) hist[tid] = 0;
+      for (int i = tid; i < 256; i += nth) hist[i] = 0;
       __syncthreads();
-      for (int b = tid; b < nblk; b += blockDim.x) {
-        if (ud.always[seg_of_block(ud, b)]) continue;
-        const uint32_t key = ordered_key(sc[b]);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      for (int i = 0; i < R; ++i) {
+        const uint32_t key = key_at(i);
+        if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
       if (warp == 0) {
-        const int rem = s_remaining;
+        const int rem = s_rem;
         int cnt = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) cnt += (int)hist[255 - (8 * lane + i)];
@@ -167,42 +295,48 @@ __global__ void __launch_bounds__(1024) k_topk(Layout L, int layer, CallSeqs cs,
           int acc = ex;
           for (int i = 0; i < 8; ++i) {
             const int dgt = 255 - (8 * lane + i);
-            const int hcount = (int)hist[dgt];
-            if (acc + hcount >= rem) {
+            const int hc = (int)hist[dgt];
+            if (acc + hc >= rem) {
               s_prefix = (uint32_t)dgt;
-              s_remaining = rem - acc;
+              s_rem = rem - acc;
               break;
             }
-            acc += hcount;
+            acc += hc;
           }
         }
       }
       __syncthreads();
       prefix |= s_prefix << shift;
       mask |= 255u << shift;
-      __syncthreads();
     }
-    need = s_remaining;
+    need = s_rem;  // ties (key == prefix) to take, lowest block ids first
   }
-
-  int run_sel = 0, run_tie = 0;
-  for (int b0 = 0; b0 < nblk; b0 += blockDim.x) {
-    const int b = b0 + tid;
-    bool cand = false;
-    uint32_t key = 0;
-    if (b < nblk) {
-      cand = !ud.always[seg_of_block(ud, b)];
-      if (cand && !all) key = ordered_key(sc[b]);
+  // Ordered compaction: counts per thread range, two block scans, then write.
+  int n_tie = 0, n_gt = 0;
+  for (int i = 0; i < R; ++i) {
+    const uint32_t key = key_at(i);
+    if (key == 0u) continue;
+    if (all || key > prefix) ++n_gt;
+    else if (key == prefix) ++n_tie;
+  }
+  int tie_tot;
+  const int tie_ex = block_count_scan(n_tie, warp_tot, &tie_tot);
+  const int take_ties = all ? 0 : max(0, min(n_tie, need - tie_ex));
+  int sel_tot;
+  int pos = block_count_scan(n_gt + take_ties, warp_tot, &sel_tot);
+  int ties_left = take_ties;
+  for (int i = 0; i < R; ++i) {
+    const uint32_t key = key_at(i);
+    if (key == 0u) continue;
+    bool sel = all || key > prefix;
+    if (!sel && key == prefix && ties_left > 0) {
+      sel = true;
+      --ties_left;
     }
-    const bool is_eq = cand && !all && key == prefix;
-    int tie_tot;
-    const int tie_ex = block_flag_scan(is_eq, warp_tot, &tie_tot) + run_tie;
-    const bool sel = cand && (all || key > prefix || (is_eq && tie_ex < need));
-    int sel_tot;
-    const int pos = block_flag_scan(sel, warp_tot, &sel_tot) + run_sel;
-    if (sel && pos < L.k_max) out[pos] = b;
-    run_tie += tie_tot;
-    run_sel += sel_tot;
+    if (sel) {
+      if (pos < L.k_max) out[pos] = tid * R + i;
+      ++pos;
+    }
   }
   if (tid == 0) n_sel[(int64_t)ci * L.n_kv + kvh] = k;
 }
@@ -211,34 +345,29 @@ cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, 
                                 int32_t* ids, int32_t* n_sel, float* scores_out, int max_nblk,
                                 cudaStream_t s) {
   const int units = cs.n * L.n_kv;
-  int chunks = (2 * 152 + units - 1) / units;
-  const int max_chunks = (max_nblk + 7) / 8;
-  if (chunks > max_chunks) chunks = max_chunks;
-  if (chunks < 1) chunks = 1;
-  dim3 grid(chunks, units);
-  const int smem = D * D * (int)sizeof(float);
-#define MK_SCORE_CASE(GG)                                                                                  \
-  case GG: {                                                                                               \
-    static bool set = false;                                                                               \
-    if (!set) {                                                                                            \
-      cudaError_t e = cudaFuncSetAttribute(k_score<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
-      if (e != cudaSuccess) return e;                                                                      \
-      set = true;                                                                                          \
-    }                                                                                                      \
-    k_score<GG><<<grid, 256, smem, s>>>(L, layer, cs, q, scores_out);                                      \
-    break;                                                                                                 \
+  const int tiles = (max_nblk + kMT - 1) / kMT;
+  int P = std::max(1, 152 / units);
+  P = std::min(P, std::max(1, (tiles + kSelWarps - 1) / kSelWarps));
+  const dim3 grid(units * P);
+#define MK_SEL_CASE(GG)                                                                                      \
+  case GG: {                                                                                                 \
+    static bool set = false;                                                                                 \
+    if (!set) {                                                                                              \
+      cudaError_t e = cudaFuncSetAttribute(k_select<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem); \
+      if (e != cudaSuccess) return e;                                                                        \
+      set = true;                                                                                            \
+    }                                                                                                        \
+    return launch_pdl(k_select<GG>, grid, dim3(256), kSelSmem, s, 0, L, layer, cs, P, q, ids, n_sel,        \
+                      scores_out);                                                                           \
   }
   switch (L.G) {
-    MK_SCORE_CASE(1)
-    MK_SCORE_CASE(2)
-    MK_SCORE_CASE(4)
-    MK_SCORE_CASE(8)
+    MK_SEL_CASE(1)
+    MK_SEL_CASE(2)
+    MK_SEL_CASE(4)
+    MK_SEL_CASE(8)
     default: return cudaErrorInvalidValue;
   }
-#undef MK_SCORE_CASE
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  k_topk<<<units, 1024, 0, s>>>(L, layer, cs, ids, n_sel);
+#undef MK_SEL_CASE
   return cudaGetLastError();
 }
 

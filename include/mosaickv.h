@@ -20,7 +20,14 @@
  *    found by a kernel (capacity overrun, bad block id) set a sticky device
  *    error word, make later kernels of the context return early, and are read
  *    with mk_poll_error.  No call aborts, throws or traps.
- *  - One context must be used by one host thread at a time.
+ *  - One context must be used by one host thread at a time, and its calls
+ *    must be ordered on the device (one stream, or events between streams).
+ *  - The decode kernels use programmatic dependent launch: each may start its
+ *    prologue while the previous kernel in the stream finishes.  Before its
+ *    wait point a kernel reads only the rotations and, for mk_block_select,
+ *    the query; so the query must be complete when the stream's previous
+ *    kernel finishes (true whenever it is written before the preceding
+ *    mk_append_compress, or by any kernel that does not itself trigger early).
  *  - Positions: a sequence holds tokens 0..T-1.  Sink tokens [0, S) and the
  *    recent window [T-W, T) are stored uncompressed (rotated bf16); the
  *    middle [S, T-W) is cut into blocks of B tokens from position S.
