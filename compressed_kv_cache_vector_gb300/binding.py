@@ -68,6 +68,7 @@ _SIGS = {
     "mk_seq_length": [c_vp, c_i32, c_i32, ctypes.POINTER(c_i32)],
     "mk_layout": [c_vp, c_i32, c_i32, c_i32, ctypes.POINTER(MkLayoutInfo)],
     "mk_record_event": [c_vp, c_vp],
+    "mk_dense_decode_attn_noalloc": [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_vp],
 }
 
 _lib = None
@@ -252,6 +253,16 @@ class MosaicKV:
                 L["nblk_cap"], L["page_stride"]),
             "layout": L,
         }
+
+
+def dense_attn_noalloc(n_q_heads, n_kv_heads, T, q, K, V, out, stream=None):
+    """Uncompressed decode attention with no context and no workspace: the
+    library's static scratch array stands in for it (for callers that cannot
+    allocate device memory where they run attention)."""
+    _check("mk_dense_decode_attn_noalloc", load().mk_dense_decode_attn_noalloc(
+        n_q_heads, n_kv_heads, len(T), _i32(T), _ptr(q), _ptr(K), _ptr(V), K.shape[2], _ptr(out),
+        _stream(stream)))
+    return out
 
 
 def record_event(ev, stream=None):

@@ -181,6 +181,30 @@ mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T,
                                const void* q, const void* K, const void* V, int64_t t_stride,
                                void* out, mk_stream stream);
 
+/* Allocation-free variant of mk_dense_decode_attn.  The paper has no
+ * counterpart to this call; it exists for callers that cannot allocate
+ * device memory at the point where they run attention (a plugin inside a host
+ * framework whose enqueue step forbids allocation, a serving runtime with a
+ * fixed memory plan, a process whose allocator belongs to someone else) and
+ * therefore cannot provide a context's workspace.  It takes only inputs and
+ * outputs and needs no context: q [n_seqs][n_q_heads][128], K, V
+ * [n_seqs][n_kv_heads][t_stride][128] (bf16, device), T host int32
+ * [n_seqs] with 1 <= T[i] <= t_stride, out [n_seqs][n_q_heads][128] bf16.
+ * Its scratch (split-T partials, counters, error word) is one static device
+ * array of MK_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds
+ * until the process exits (about 4.3 MB).  Calls with
+ * n_seqs * n_q_heads > MK_NOALLOC_MAX_QUERY_HEADS return MK_ENOMEM before
+ * anything is launched.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  Every call shares the
+ * array and clears what must start at zero; calls that overlap on the GPU
+ * (different streams without ordering) race on it and give wrong results. */
+#define MK_NOALLOC_SCRATCH_BYTES 4456448
+#define MK_NOALLOC_MAX_QUERY_HEADS 128
+mk_status mk_dense_decode_attn_noalloc(int32_t n_q_heads, int32_t n_kv_heads, int32_t n_seqs,
+                                       const int32_t* T, const void* q, const void* K, const void* V,
+                                       int64_t t_stride, void* out, mk_stream stream);
+
 /* Set-up helper, not on the decode path: gram = X^T X (fp32 accumulation)
  * for X: device bf16 rows of 128 values, row i at x + i*row_stride elements.
  * gram: device fp32 [128][128], overwritten. */
