@@ -79,6 +79,7 @@ Plan make_plan(const mk_config* c) {
   L.r_max = r_max;
   L.nblk_cap = mk::n_mid_blocks(L, c->max_tokens);
   L.k_max = std::max(1, mk::n_select(L, L.nblk_cap));
+  L.scores_stride = (std::max(1, L.nblk_cap) + 3) & ~3;
   L.page_stride = (int64_t)6 * L.B * r_max;
   const int64_t D = MK_HEAD_DIM;
   int64_t off = 0;
@@ -98,7 +99,7 @@ Plan make_plan(const mk_config* c) {
   const int64_t slots = (int64_t)c->max_seqs * c->n_kv_heads;
   int64_t w = 0;
   w = align_up(w + slots * L.G * D * 4);                       // qrot
-  w = align_up(w + slots * (int64_t)std::max(1, L.nblk_cap) * 4);  // scores
+  w = align_up(w + slots * (int64_t)L.scores_stride * 4);      // scores
   w = align_up(w + slots * MK_MAX_SPLITS * L.G * D * 4);       // part_acc
   w = align_up(w + slots * MK_MAX_SPLITS * L.G * 2 * 4);       // part_ml
   w = align_up(w + slots * 4 * 2);                             // counters: attention, selection
@@ -118,7 +119,7 @@ void bind_pointers(Plan& p, void* arena, void* ws) {
   char* w = static_cast<char*>(ws);
   int64_t o = 0;
   L.qrot = reinterpret_cast<float*>(w + o); o = align_up(o + slots * L.G * D * 4);
-  L.scores = reinterpret_cast<float*>(w + o); o = align_up(o + slots * (int64_t)std::max(1, L.nblk_cap) * 4);
+  L.scores = reinterpret_cast<float*>(w + o); o = align_up(o + slots * (int64_t)L.scores_stride * 4);
   L.part_acc = reinterpret_cast<float*>(w + o); o = align_up(o + slots * MK_MAX_SPLITS * L.G * D * 4);
   L.part_ml = reinterpret_cast<float*>(w + o); o = align_up(o + slots * MK_MAX_SPLITS * L.G * 2 * 4);
   L.counters = reinterpret_cast<int32_t*>(w + o);
@@ -419,7 +420,8 @@ mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T, co
 }
 
 mk_status mk_gram(const void* x, int64_t n_rows, int64_t row_stride, float* gram, mk_stream stream) {
-  if (!x || !gram || n_rows < 1 || row_stride < MK_HEAD_DIM) return MK_EINVAL;
+  if (!x || !gram || n_rows < 1 || row_stride < MK_HEAD_DIM || row_stride % 8 || ((uintptr_t)x & 15))
+    return MK_EINVAL;
   return cuda_status(mk::launch_gram(static_cast<const uint16_t*>(x), n_rows, row_stride, gram,
                                      (cudaStream_t)stream));
 }

@@ -11,40 +11,37 @@
 // rotation merged into the query).
 //
 // GB300 structure.
-//  * Work items of one (sequence, kv head): dense chunks of 16 tokens (sinks,
+//  * Work items of one (sequence, kv head): dense chunks of 8 tokens (sinks,
 //    window), then 16-token groups of the selected / always-attended pages.
-//    They are split over Q clusters of C CTAs (8 warps each); every warp
-//    double-buffers its items into shared memory with cp.async.
-//  * Per group the warp rebuilds the positions: it zero-fills a 16 x 128 bf16
-//    K tile and V tile and scatters the kept values by their channel indices
-//    (lanes 0-15 keys, lanes 16-31 values).  Logits S^T[16 tok x 8 heads] and
-//    the value sum O'^T[128 x 8 heads] then run on the tensor cores
-//    (mma.sync m16n8k16, bf16 in, fp32 accumulate).  The fp32 operands q' and
-//    p are split into bf16 hi + lo parts (two MMAs), so the products keep
-//    ~16 significant bits: the rounding stays far below the 5e-3 tolerance.
-//  * The split-T log-sum-exp merge: warps -> CTA in shared memory, CTAs ->
-//    cluster through distributed shared memory (CTA `rank` owns output
-//    channels [rank*128/C, (rank+1)*128/C)), clusters -> unit through the
-//    workspace when Q > 1: the last cluster to arrive (atomic counter, no
-//    waiting) merges and un-rotates.
+//    P CTAs (8 warps, two CTAs per SM) share them; each warp double-buffers
+//    its items into shared memory with cp.async.
+//  * Per group the warp rebuilds positions in one 16 x 128 bf16 tile: it
+//    zero-fills it and scatters the kept key values by their channel indices
+//    (two lanes per token), computes the logits S^T[16 tok x 8 heads] on the
+//    tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), then does the
+//    same for the values and accumulates O'^T[128 x 8 heads].  The fp32
+//    operands q' and p are split into bf16 hi + lo parts (two MMAs), keeping
+//    ~16 significant bits, far below the 5e-3 tolerance.
+//  * Split-T merge: warps -> CTA in shared memory, CTA partials (m, l, acc)
+//    -> workspace; the last CTA of the unit to arrive (atomic counter, no
+//    waiting) stages all partials with one cp.async burst, merges them
+//    (log-sum-exp), un-rotates (out = o' R_v) and stores bf16.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 
-#include <cooperative_groups.h>
-
 #include "mk_internal.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace mk {
 
 namespace {
 constexpr int kWarps = 8;
-constexpr int kTG = 16;                      // tokens per group (one MMA tile)
+constexpr int kTG = 16;                      // tokens per packed group (one MMA tile)
+constexpr int kDC = 8;                       // tokens per dense chunk
 constexpr int kRow = D + 8;                  // padded bf16 row: 272 bytes, ldmatrix conflict-free
-constexpr int kTile = kTG * kRow;            // one 16-row tile (bf16 elements)
-constexpr int kDenseStage = 2 * kTile * 2;   // staged dense chunk: K tile + V tile (bytes)
+constexpr int kTileBytes = kTG * kRow * 2;   // 16-row tile
+constexpr int kDenseStage = 2 * kDC * kRow * 2;  // staged dense chunk: 8 K rows + 8 V rows
+constexpr int kPsBytes = 2 * 8 * kTG * 2;    // P hi/lo as [8 heads][16 tokens]
 constexpr float kScaleLog2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
 __device__ __forceinline__ int always_block(const UnitDesc& ud, int nblk, int i) {
@@ -88,6 +85,24 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo16, uint16_t hi16) {
   return (uint32_t)lo16 | ((uint32_t)hi16 << 16);
 }
 
+// Rebuild one token's dense row from its packed (values, indices): the row is
+// zero already.  Lanes t and t + 16 share token t and split its elements.
+__device__ __forceinline__ void scatter_row(uint16_t* row, const uint16_t* val, const uint8_t* idx, int r,
+                                            int lane) {
+  const int h2 = (r >> 1) & ~1;
+  const int j0 = lane < 16 ? 0 : h2, j1 = lane < 16 ? h2 : r;
+  if ((r & 1) == 0) {
+    for (int jj = j0; jj < j1; jj += 2) {
+      const uint32_t ip = *reinterpret_cast<const uint16_t*>(idx + jj);
+      const uint32_t vp = *reinterpret_cast<const uint32_t*>(val + jj);
+      row[ip & 0xff] = (uint16_t)(vp & 0xffff);
+      row[ip >> 8] = (uint16_t)(vp >> 16);
+    }
+  } else {
+    for (int jj = j0; jj < j1; ++jj) row[idx[jj]] = val[jj];
+  }
+}
+
 struct Task {
   int kind;      // 0 none, 1 dense chunk, 2 packed group, 3 skipped (bad block id)
   int item;
@@ -95,15 +110,10 @@ struct Task {
   int b, r, tg, n_live;
 };
 
+int stage_bytes(const Layout& L) { return (std::max(6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16; }
+size_t per_warp_bytes(const Layout& L, int nst) { return (size_t)nst * stage_bytes(L) + kTileBytes + kPsBytes; }
 size_t smem_for(const Layout& L, int nst) {
-  const size_t sb = (size_t)((std::max(6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16);
-  const size_t per_warp = nst * sb + (size_t)kDenseStage + 2 * 8 * kTG * 2;  // stages, K/V tiles, P hi/lo
-  return (size_t)kWarps * per_warp
-         + (size_t)L.G * D * 4          // q' (fp32) for building the B fragments
-         + (size_t)kWarps * 8 * 2 * 4   // per-warp (m, l) for 8 head slots
-         + 8 * 2 * 4                    // CTA (m, l)
-         + (size_t)2 * L.G * D * 4      // CTA acc, merged o'
-         + 16;                          // flags
+  return (size_t)kWarps * per_warp_bytes(L, nst) + (size_t)kWarps * 8 * 2 * 4 + kRow * 2 + 64;
 }
 }  // namespace
 
@@ -116,7 +126,7 @@ size_t attn_plan(Layout& L, int /*r_min*/) {
       L.attn_tg = kTG;
       L.attn_nst = nst;
       L.attn_nc = 1;
-      L.attn_sb = (int)((std::max(6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16);
+      L.attn_sb = stage_bytes(L);
       return s;
     }
   }
@@ -125,34 +135,32 @@ size_t attn_plan(Layout& L, int /*r_min*/) {
 
 size_t attn_smem_bytes(const Layout& L, int) { return smem_for(L, L.attn_nst); }
 
+// Largest number of CTAs per unit whose partials the merging CTA can stage
+// (next to the merged o' and the un-rotation halves).
+int attn_max_parts(const Layout& L) {
+  const int64_t avail = (int64_t)kWarps * per_warp_bytes(L, L.attn_nst) - (int64_t)3 * L.G * D * 4 - 64;  // o', halves
+  return (int)std::max<int64_t>(1, std::min<int64_t>(MK_MAX_SPLITS, avail / ((int64_t)L.G * (D + 2) * 4)));
+}
+
 template <int G, bool DENSE>
-__global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs cs, int Q,
+__global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs cs, int P,
                                                  const int32_t* __restrict__ ids,
                                                  const int32_t* __restrict__ n_sel_in,
                                                  const uint16_t* __restrict__ q_in, const uint16_t* __restrict__ Kd,
                                                  const uint16_t* __restrict__ Vd, int64_t t_stride,
                                                  uint16_t* __restrict__ out) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = (int)cluster.num_blocks();
-  const int rank = (int)cluster.block_rank();
   const int NST = L.attn_nst, SB = L.attn_sb;
-
   extern __shared__ __align__(16) unsigned char smem[];
-  const size_t per_warp = (size_t)NST * SB + kDenseStage + 2 * 8 * kTG * 2;
-  unsigned char* warp_area = smem;                                             // [kWarps][per_warp]
-  float* qs = reinterpret_cast<float*>(smem + kWarps * per_warp);              // [G][D]
-  float* mlw = qs + G * D;                                                     // [kWarps][8][2]
-  float* cl_ml = mlw + kWarps * 16;                                            // [8][2]
-  float* cl_acc = cl_ml + 16;                                                  // [G][D]
-  float* ofull = cl_acc + G * D;                                               // [G][D]
-  int* flag = reinterpret_cast<int*>(ofull + G * D);
+  const size_t pwb = (size_t)NST * SB + kTileBytes + kPsBytes;
+  unsigned char* warp_area = smem;                                       // [kWarps][pwb]
+  float* mlw = reinterpret_cast<float*>(smem + kWarps * pwb);            // [kWarps][8][2]
+  uint16_t* zrow = reinterpret_cast<uint16_t*>(mlw + kWarps * 16);      // one zero row (272 B)
   __shared__ UnitDesc ud;
-  __shared__ int s_abort, s_ns;
+  __shared__ int s_abort, s_ns, s_last;
+  __shared__ float s_m[8], s_l[8];
 
-  const int per_unit = Q * C;
-  const int unit_call = blockIdx.x / per_unit;
-  const int kq = blockIdx.x - unit_call * per_unit;   // CTA index within the unit: q*C + rank
-  const int qi = kq / C;
+  const int unit_call = blockIdx.x / P;
+  const int part = blockIdx.x - unit_call * P;
   const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
   const int seq = cs.seq[ci];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -160,10 +168,11 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
   const int64_t u = DENSE ? 0 : unit_index(L, layer, seq, kvh);
   const int64_t slot = (int64_t)seq * L.n_kv + kvh;
 
-  if (!DENSE && rank == 0 && qi == 0) {   // R_v is static: warm L2 before the wait
+  if (!DENSE && part == 0) {  // R_v is static: warm L2 for the final un-rotation
     const char* rv = unit_base(L, u) + L.off_rv;
     for (int i = tid; i < D * D * 4 / 128; i += blockDim.x) prefetch_l2(rv + (size_t)i * 128);
   }
+  for (int i = tid; i < kRow / 8; i += blockDim.x) reinterpret_cast<uint4*>(zrow)[i] = make_uint4(0, 0, 0, 0);
   pdl_wait();
   pdl_trigger();
   if (tid == 0) {
@@ -172,7 +181,6 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
     s_ns = DENSE ? 0 : n_sel_in[(int64_t)ci * L.n_kv + kvh];
   }
   __syncthreads();
-  // Every CTA must reach the cluster barriers below: an abort only empties the work.
   bool skip = s_abort != 0;
 
   const int S = L.S, W = L.W, B = L.B;
@@ -193,49 +201,16 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
       ns = 0;
     }
   }
-  const int n_dch = (n_dense + kTG - 1) / kTG;
+  const int n_dch = (n_dense + kDC - 1) / kDC;
   const int n_items = skip ? 0 : n_dch + ns + n_always;
-  const int per = (n_items + per_unit - 1) / per_unit;
-  const int i0 = kq * per, i1 = min(n_items, i0 + per);
-
-  for (int i = tid; i < G * D; i += blockDim.x) {
-    float v = 0.0f;
-    if (!skip) {
-      if (DENSE) v = bf2f(q_in[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D + i]);
-      else v = L.qrot[slot * G * D + i];
-    }
-    qs[i] = v;
-  }
-  __syncthreads();
-
-  // q'^T B fragments (k = channel, n = head), hi and lo parts: 8 k-chunks.
-  uint32_t bqh[8][2], bql[8][2];
-#pragma unroll
-  for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint16_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
-      if (g < G) {
-        const int c = kc * 16 + half * 8 + 2 * tig;
-        split_bf16(qs[g * D + c], h0, l0);
-        split_bf16(qs[g * D + c + 1], h1, l1);
-      }
-      bqh[kc][half] = pack2(h0, h1);
-      bql[kc][half] = pack2(l0, l1);
-    }
+  const int per = (n_items + P - 1) / P;
+  const int i0 = part * per, i1 = min(n_items, i0 + per);
 
   const char* base = DENSE ? nullptr : unit_base(L, u);
   const int32_t* my_ids = DENSE ? nullptr : ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
-  unsigned char* my_area = warp_area + (size_t)warp * per_warp;
-  uint16_t* tiles = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB);           // K tile, V tile
-  uint16_t* ps = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB + kDenseStage);  // [2][8][16]
-
-  float o[8][4];  // O'^T fragments: m-tile mt, rows = channels, cols = heads
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) o[mt][k] = 0.0f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2*tig, 2*tig+1
+  unsigned char* my_area = warp_area + (size_t)warp * pwb;
+  uint16_t* tile = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB);
+  uint16_t* ps = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB + kTileBytes);
 
   auto make_task = [&](int it, int tg) -> Task {
     Task t{};
@@ -243,8 +218,8 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
     t.item = it;
     if (it < n_dch) {
       t.kind = 1;
-      t.j0 = it * kTG;
-      t.nd = min(kTG, n_dense - t.j0);
+      t.j0 = it * kDC;
+      t.nd = min(kDC, n_dense - t.j0);
       return t;
     }
     const int pi = it - n_dch;
@@ -282,13 +257,13 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
   };
   auto issue = [&](const Task& t, unsigned char* dst) {
     if (t.kind == 1) {
-      // K tile then V tile, rows padded to 272 bytes.
+      // 8 K rows then 8 V rows, padded to 272 bytes.
       for (int i = lane; i < t.nd * 16; i += 32) {
-        const int row = i >> 4, part = i & 15;
+        const int row = i >> 4, prt = i & 15;
         const uint16_t *kr, *vr;
         dense_rows(t.j0 + row, kr, vr);
-        cp_async16(dst + row * kRow * 2 + part * 16, kr + part * 8);
-        cp_async16(dst + kTile * 2 + row * kRow * 2 + part * 16, vr + part * 8);
+        cp_async16(dst + row * kRow * 2 + prt * 16, kr + prt * 8);
+        cp_async16(dst + (kDC + row) * kRow * 2 + prt * 16, vr + prt * 8);
       }
     } else if (t.kind == 2) {
       // This group's rows of the page's four sub-arrays (B is a multiple of
@@ -308,10 +283,49 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
     }
   };
 
+  // Start the first item's copies before reading q'.
   Task cur = make_task(i0 + warp, 0);
   int st = 0;
   issue(cur, my_area);
   cp_async_commit();
+
+  // q'^T B fragments (k = channel, n = head), hi and lo parts: 8 k-chunks.
+  uint32_t bqh[8][2], bql[8][2];
+  {
+    const float* qrot = L.qrot + slot * G * D;
+    const uint16_t* qin = DENSE ? q_in + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D : nullptr;
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint16_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
+        if (g < G && !skip) {
+          const int c = kc * 16 + hf * 8 + 2 * tig;
+          float x0, x1;
+          if (DENSE) {
+            x0 = bf2f(qin[g * D + c]);
+            x1 = bf2f(qin[g * D + c + 1]);
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(qrot + g * D + c);
+            x0 = v.x;
+            x1 = v.y;
+          }
+          split_bf16(x0, h0, l0);
+          split_bf16(x1, h1, l1);
+        }
+        bqh[kc][hf] = pack2(h0, h1);
+        bql[kc][hf] = pack2(l0, l1);
+      }
+  }
+
+  float o[8][4];  // O'^T fragments: m-tile mt, rows = channels, cols = heads
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[mt][k] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2*tig, 2*tig+1
+
+  const int mi = lane >> 3, ri = lane & 7;
   while (cur.kind != 0) {
     const Task nxt = advance(cur);
     if (NST == 2) {
@@ -324,69 +338,37 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
     __syncwarp();
     const unsigned char* buf = my_area + (size_t)st * SB;
     if (cur.kind == 1 || cur.kind == 2) {
-      const uint16_t* Kt;
-      const uint16_t* Vt;
       int ntok;
+      const uint16_t* arow_k;   // this lane's ldmatrix row address for the key tile
       if (cur.kind == 1) {
-        Kt = reinterpret_cast<const uint16_t*>(buf);
-        Vt = Kt + kTile;
         ntok = cur.nd;
-        if (ntok < kTG) {
-          // rows past the chunk hold stale bytes: zero them (0 * NaN would poison P.V)
-          uint16_t* kb = const_cast<uint16_t*>(Kt);
-          for (int i = lane; i < (kTG - ntok) * 16; i += 32) {
-            const int row = ntok + (i >> 4), part = i & 15;
-            *reinterpret_cast<uint4*>(kb + row * kRow + part * 8) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(kb + kTile + row * kRow + part * 8) = make_uint4(0, 0, 0, 0);
-          }
-          __syncwarp();
-        }
+        const int row = ri + (mi & 1) * 8;
+        const uint16_t* kb = reinterpret_cast<const uint16_t*>(buf);
+        arow_k = (row < ntok ? kb + row * kRow : zrow) + (mi >> 1) * 8;
       } else {
-        // Rebuild positions: zero both tiles, scatter kept values by index.
-        uint4* z = reinterpret_cast<uint4*>(tiles);
-#pragma unroll
-        for (int i = lane; i < kDenseStage / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
-        __syncwarp();
-        const int r = cur.r, gr = kTG * r;
         ntok = min(kTG, cur.n_live - cur.tg);
-        const int t = lane & 15;
-        const bool is_v = lane >= 16;
-        if (t < ntok) {
-          const uint16_t* val = reinterpret_cast<const uint16_t*>(buf + (is_v ? 3 * gr : 0)) + t * r;
-          const uint8_t* idx = buf + (is_v ? 5 * gr : 2 * gr) + t * r;
-          uint16_t* row = tiles + (is_v ? kTile : 0) + t * kRow;
-          if ((r & 1) == 0) {
-            const uint16_t* i2 = reinterpret_cast<const uint16_t*>(idx);
-            const uint32_t* v2 = reinterpret_cast<const uint32_t*>(val);
-#pragma unroll 4
-            for (int jj = 0; jj < (r >> 1); ++jj) {
-              const uint32_t ip = i2[jj], vp = v2[jj];
-              row[ip & 0xff] = (uint16_t)(vp & 0xffff);
-              row[ip >> 8] = (uint16_t)(vp >> 16);
-            }
-          } else {
-            for (int jj = 0; jj < r; ++jj) row[idx[jj]] = val[jj];
-          }
-        }
+        // Rebuild key positions: zero the tile, scatter by channel index.
+        uint4* z = reinterpret_cast<uint4*>(tile);
+        for (int i = lane; i < kTileBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
         __syncwarp();
-        Kt = tiles;
-        Vt = tiles + kTile;
+        const int r = cur.r, t = lane & 15;
+        if (t < ntok)
+          scatter_row(tile + t * kRow, reinterpret_cast<const uint16_t*>(buf) + t * r, buf + 2 * kTG * r + t * r, r,
+                      lane);
+        __syncwarp();
+        arow_k = tile + (ri + (mi & 1) * 8) * kRow + (mi >> 1) * 8;
       }
 
       // Logits S^T[token][head] = sum_c K[token][c] q'[head][c] (hi + lo parts).
       float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      {
-        const int mi = lane >> 3, ri = lane & 7;
-        const uint16_t* arow = Kt + (ri + (mi & 1) * 8) * kRow + (mi >> 1) * 8;
 #pragma unroll
-        for (int kc = 0; kc < 8; ++kc) {
-          uint32_t a[4];
-          ldsm_x4(a, arow + kc * 16);
-          mma_bf16(s, a, bqh[kc][0], bqh[kc][1]);
-          mma_bf16(s, a, bql[kc][0], bql[kc][1]);
-        }
+      for (int kc = 0; kc < 8; ++kc) {
+        uint32_t a[4];
+        ldsm_x4(a, arow_k + kc * 16);
+        mma_bf16(s, a, bqh[kc][0], bqh[kc][1]);
+        mma_bf16(s, a, bql[kc][0], bql[kc][1]);
       }
-      // Online softmax over this group's tokens (g, g+8) for heads 2tig, 2tig+1.
+      // Online softmax over this item's tokens (g, g+8) for heads 2tig, 2tig+1.
       const bool v_lo = g < ntok, v_hi = g + 8 < ntok;
       const float s00 = v_lo ? s[0] * kScaleLog2 : -INFINITY, s01 = v_lo ? s[1] * kScaleLog2 : -INFINITY;
       const float s10 = v_hi ? s[2] * kScaleLog2 : -INFINITY, s11 = v_hi ? s[3] * kScaleLog2 : -INFINITY;
@@ -426,21 +408,35 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
         split_bf16(p10, h, lw); ps[h0 * kTG + g + 8] = h; ps[128 + h0 * kTG + g + 8] = lw;
         split_bf16(p11, h, lw); ps[h1 * kTG + g + 8] = h; ps[128 + h1 * kTG + g + 8] = lw;
       }
-      __syncwarp();
+      // Value tile: dense rows in the stage, or rebuilt in the (now free) tile.
+      const int vrow = ri + (mi >> 1) * 8;  // ldmatrix.trans rows are tokens
+      const uint16_t* vrow_base;
+      if (cur.kind == 1) {
+        const uint16_t* vb = reinterpret_cast<const uint16_t*>(buf) + kDC * kRow;
+        vrow_base = (vrow < ntok ? vb + vrow * kRow : zrow) + (mi & 1) * 8;
+        __syncwarp();
+      } else {
+        __syncwarp();  // the key tile's ldmatrix reads are done
+        uint4* z = reinterpret_cast<uint4*>(tile);
+        for (int i = lane; i < kTileBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+        __syncwarp();
+        const int r = cur.r, t = lane & 15, gr = kTG * r;
+        if (t < ntok)
+          scatter_row(tile + t * kRow, reinterpret_cast<const uint16_t*>(buf + 3 * gr) + t * r, buf + 5 * gr + t * r,
+                      r, lane);
+        __syncwarp();
+        vrow_base = tile + vrow * kRow + (mi & 1) * 8;
+      }
       const uint32_t* ps32 = reinterpret_cast<const uint32_t*>(ps);
       const uint32_t pbh0 = ps32[(g * kTG + 2 * tig) >> 1], pbh1 = ps32[(g * kTG + 2 * tig + 8) >> 1];
       const uint32_t pbl0 = ps32[(128 + g * kTG + 2 * tig) >> 1], pbl1 = ps32[(128 + g * kTG + 2 * tig + 8) >> 1];
       // O'^T[channel][head] += sum_token V[token][channel] P[token][head].
-      {
-        const int mi = lane >> 3, ri = lane & 7;
-        const uint16_t* vrow = Vt + (ri + (mi >> 1) * 8) * kRow + (mi & 1) * 8;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          uint32_t a[4];
-          ldsm_x4_t(a, vrow + mt * 16);
-          mma_bf16(o[mt], a, pbh0, pbh1);
-          mma_bf16(o[mt], a, pbl0, pbl1);
-        }
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_t(a, vrow_base + mt * 16);
+        mma_bf16(o[mt], a, pbh0, pbh1);
+        mma_bf16(o[mt], a, pbl0, pbl1);
       }
     }
     __syncwarp();
@@ -454,7 +450,7 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
   cp_async_wait_all();
   __syncwarp();
 
-  // ---- merge: warps -> CTA ------------------------------------------------
+  // ---- warps -> CTA partial ------------------------------------------------
   if (g == 0) {
     mlw[(warp * 8 + 2 * tig) * 2] = m0;
     mlw[(warp * 8 + 2 * tig) * 2 + 1] = l0;
@@ -462,7 +458,7 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
     mlw[(warp * 8 + 2 * tig + 1) * 2 + 1] = l1;
   }
   __syncthreads();
-  float* dump = reinterpret_cast<float*>(warp_area);  // [kWarps][G][D], main loop is over
+  float* dump = reinterpret_cast<float*>(warp_area);  // [kWarps][G][D] (main loop is over)
   {
     float e0 = 0.0f, e1 = 0.0f;
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
@@ -487,13 +483,6 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
       }
     }
   }
-  __syncthreads();
-  for (int i = tid; i < G * D; i += blockDim.x) {
-    float a = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) a += dump[(size_t)w * G * D + i];
-    cl_acc[i] = a;
-  }
   if (tid < G) {
     float M = -INFINITY;
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mlw[(w * 8 + tid) * 2]);
@@ -503,189 +492,135 @@ __global__ void __launch_bounds__(256, 1) k_attn(Layout L, int layer, CallSeqs c
         const float mw = mlw[(w * 8 + tid) * 2];
         if (mw != -INFINITY) ls += mlw[(w * 8 + tid) * 2 + 1] * exp2f(mw - M);
       }
-    cl_ml[tid * 2] = M;
-    cl_ml[tid * 2 + 1] = ls;
+    s_m[tid] = M;
+    s_l[tid] = ls;
   }
-  cluster.sync();
+  __syncthreads();
+  float* pacc = L.part_acc + slot * MK_MAX_SPLITS * G * D;   // [part][G][D]
+  float* pml = L.part_ml + slot * MK_MAX_SPLITS * G * 2;     // [part][G][2]
+  for (int i = tid; i < G * D; i += blockDim.x) {
+    float a = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) a += dump[(size_t)w * G * D + i];
+    pacc[(size_t)part * G * D + i] = a;
+  }
+  if (tid < G) {
+    pml[(part * G + tid) * 2] = s_m[tid];
+    pml[(part * G + tid) * 2 + 1] = s_l[tid];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&L.counters[slot], 1);
+    s_last = (prev == P - 1);
+    if (prev == P - 1) L.counters[slot] = 0;
+  }
+  __syncthreads();
+  if (!s_last || s_abort) return;
+  __threadfence();
 
-  // ---- merge: CTAs -> cluster, for this CTA's channel slice ---------------
-  const int w = D / C, c_lo = rank * w;
-  float* part_acc = L.part_acc + slot * MK_MAX_SPLITS * G * D;
-  float* part_ml = L.part_ml + slot * MK_MAX_SPLITS * G * 2;
-  for (int i = tid; i < G * w; i += blockDim.x) {
-    const int h = i / w, c = c_lo + (i - h * w);
-    float M = -INFINITY;
-    for (int r2 = 0; r2 < C; ++r2) M = fmaxf(M, cluster.map_shared_rank(cl_ml, r2)[h * 2]);
-    float a = 0.0f, ls = 0.0f;
-    if (M != -INFINITY)
-      for (int r2 = 0; r2 < C; ++r2) {
-        const float* ml = cluster.map_shared_rank(cl_ml, r2);
-        const float mr = ml[h * 2];
-        if (mr == -INFINITY) continue;
-        const float e = exp2f(mr - M);
-        a = fmaf(cluster.map_shared_rank(cl_acc, r2)[h * D + c], e, a);
-        ls = fmaf(ml[h * 2 + 1], e, ls);
-      }
-    if (Q == 1) {
-      const float v = ls > 0.0f ? a / ls : 0.0f;
-      for (int r2 = 0; r2 < C; ++r2) cluster.map_shared_rank(ofull, r2)[h * D + c] = v;
-    } else {
-      part_acc[((size_t)qi * G + h) * D + c] = a;
-      if (i - h * w == 0 && rank == 0) {
-        part_ml[((size_t)qi * G + h) * 2] = M;
-        part_ml[((size_t)qi * G + h) * 2 + 1] = ls;
-      }
-    }
-  }
-  if (Q > 1) {
-    // ---- merge: clusters -> unit (last cluster to arrive) -----------------
-    __threadfence();
-    cluster.sync();
-    if (rank == 0 && tid == 0) {
-      const int prev = atomicAdd(&L.counters[slot], 1);
-      *flag = (prev == Q - 1);
-      if (prev == Q - 1) L.counters[slot] = 0;
-    }
-    cluster.sync();
-    const int last = *cluster.map_shared_rank(flag, 0);
-    if (!last) {
-      cluster.sync();  // same barrier count in every CTA of the cluster
-      return;
-    }
-    __threadfence();
-    for (int i = tid; i < G * w; i += blockDim.x) {
-      const int h = i / w, c = c_lo + (i - h * w);
-      float M = -INFINITY;
-      for (int q2 = 0; q2 < Q; ++q2) M = fmaxf(M, __ldcg(part_ml + ((size_t)q2 * G + h) * 2));
-      float a = 0.0f, ls = 0.0f;
-      if (M != -INFINITY)
-        for (int q2 = 0; q2 < Q; ++q2) {
-          const float mq = __ldcg(part_ml + ((size_t)q2 * G + h) * 2);
-          if (mq == -INFINITY) continue;
-          const float e = exp2f(mq - M);
-          a = fmaf(__ldcg(part_acc + ((size_t)q2 * G + h) * D + c), e, a);
-          ls = fmaf(__ldcg(part_ml + ((size_t)q2 * G + h) * 2 + 1), e, ls);
-        }
-      const float v = ls > 0.0f ? a / ls : 0.0f;
-      for (int r2 = 0; r2 < C; ++r2) cluster.map_shared_rank(ofull, r2)[h * D + c] = v;
-    }
-  }
-  cluster.sync();
-  if (s_abort) return;
-
-  // ---- output channels [c_lo, c_lo + w): out_j = sum_c o'_c R_v[c][j] ------
-  uint16_t* orow = out + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D;
-  if (DENSE) {
-    for (int i = tid; i < G * w; i += blockDim.x) {
-      const int h = i / w, j = c_lo + (i - h * w);
-      orow[h * D + j] = f2bf(ofull[h * D + j]);
-    }
-    return;
-  }
-  float* rvs = reinterpret_cast<float*>(warp_area);   // [128][w] staged R_v columns
-  float* red = rvs + D * w;                           // [parts][G*w]
-  const float* Rv = reinterpret_cast<const float*>(base + L.off_rv);
-  const int w4 = w / 4;
-  for (int i = tid; i < D * w4; i += blockDim.x) {
-    const int c = i / w4, q4 = i - c * w4;
-    cp_async16(rvs + c * w + 4 * q4, Rv + (size_t)c * D + c_lo + 4 * q4);
-  }
+  // ---- the last CTA: merge the P partials, un-rotate, store ----------------
+  float* ofull = reinterpret_cast<float*>(warp_area);       // [G][D]
+  float* red = ofull + G * D;                                // [2][G][D]
+  float* sacc = red + 2 * G * D;                             // [P][G][D]
+  float* sml = sacc + (size_t)P * G * D;                     // [P][G][2]
+  for (int i = tid; i < P * G * D / 4; i += blockDim.x) cp_async16(sacc + 4 * i, pacc + 4 * i);
+  for (int i = tid; i < (P * G * 2 + 3) / 4; i += blockDim.x) cp_async16(sml + 4 * i, pml + 4 * i);
   cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
-  const int outs = G * w;
-  const int parts = max(1, (int)blockDim.x / outs);
-  const int cper = D / parts;
-  for (int i = tid; i < outs * parts; i += blockDim.x) {
-    const int oo = i % outs, pidx = i / outs;
-    const int h = oo / w, jl = oo - h * w;
-    float a = 0.0f;
-    for (int c = pidx * cper; c < (pidx + 1) * cper; ++c) a = fmaf(ofull[h * D + c], rvs[c * w + jl], a);
-    red[pidx * outs + oo] = a;
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int p = 0; p < P; ++p) M = fmaxf(M, sml[(p * G + tid) * 2]);
+    float ls = 0.0f;
+    if (M != -INFINITY)
+      for (int p = 0; p < P; ++p) {
+        const float mp = sml[(p * G + tid) * 2];
+        if (mp != -INFINITY) ls += sml[(p * G + tid) * 2 + 1] * exp2f(mp - M);
+      }
+    s_m[tid] = M;
+    s_l[tid] = ls;
   }
   __syncthreads();
-  for (int oo = tid; oo < outs; oo += blockDim.x) {
+  for (int i = tid; i < G * D; i += blockDim.x) {
+    const int h = i / D;
+    const float M = s_m[h], ls = s_l[h];
     float a = 0.0f;
-    for (int pidx = 0; pidx < parts; ++pidx) a += red[pidx * outs + oo];
-    const int h = oo / w, jl = oo - h * w;
-    orow[h * D + c_lo + jl] = f2bf(a);
+    if (M != -INFINITY && ls > 0.0f) {
+      for (int p = 0; p < P; ++p) {
+        const float mp = sml[(p * G + h) * 2];
+        if (mp != -INFINITY) a = fmaf(sacc[(size_t)p * G * D + i], exp2f(mp - M), a);
+      }
+      a /= ls;
+    }
+    ofull[i] = a;
   }
+  __syncthreads();
+  uint16_t* orow = out + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D;
+  if (DENSE) {
+    for (int i = tid; i < G * D; i += blockDim.x) orow[i] = f2bf(ofull[i]);
+    return;
+  }
+  // out[h][j] = sum_c o'[h][c] R_v[c][j]: R_v staged over the partials (one
+  // cp.async burst) when it fits, then thread (j, half of c), halves summed.
+  const float* Rv = reinterpret_cast<const float*>(base + L.off_rv);
+  const bool rv_smem = (size_t)(3 * G * D) * 4 + (size_t)D * D * 4 <= (size_t)kWarps * pwb;
+  if (rv_smem) {
+    for (int i = tid; i < D * D / 4; i += blockDim.x) cp_async16(sacc + 4 * i, Rv + 4 * i);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+  }
+  const float* Rsrc = rv_smem ? sacc : Rv;
+  {
+    const int j = tid & (D - 1), half = tid >> 7;
+    float acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+    const float* Rc = Rsrc + (size_t)half * 64 * D + j;
+#pragma unroll 16
+    for (int c = 0; c < 64; ++c) {
+      const float rr = Rc[(size_t)c * D];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = fmaf(ofull[h * D + half * 64 + c], rr, acc[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) red[(half * G + h) * D + j] = acc[h];
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += blockDim.x) orow[i] = f2bf(red[i] + red[G * D + i]);
 }
 
 namespace {
-// Cluster size C and clusters per unit Q: every cluster resident at once
-// (checked against cudaOccupancyMaxActiveClusters), as many CTAs as the SMs
-// allow, preferring larger clusters when the CTA count is within 90%.
-template <int G, bool DENSE>
-void choose_grid(int units, int max_items, size_t smem, int& C, int& Q) {
-  static int max_active[17];
-  static size_t for_smem = 0;
-  if (for_smem != smem) {
-    for (int c = 1; c <= 16; c *= 2) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(c, 1, 1);
-      cfg.blockDim = dim3(256, 1, 1);
-      cfg.dynamicSmemBytes = smem;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = c;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_attn<G, DENSE>, &cfg);
-      if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        n = 0;
-      }
-      max_active[c] = n;
-      if (std::getenv("MK_LOG"))
-        std::fprintf(stderr, "[mosaickv] attention G=%d dense=%d smem=%zu: cluster %d -> %d resident\n", G,
-                     (int)DENSE, smem, c, n);
-    }
-    for_smem = smem;
-  }
-  int best = 0;
-  for (int c = 1; c <= 16; c *= 2) {
-    if (max_active[c] < units) continue;
-    int q = std::min(MK_MAX_SPLITS, max_active[c] / units);
-    q = std::min(q, std::max(1, max_items / (2 * c)));
-    best = std::max(best, units * q * c);
-  }
-  C = 1;
-  Q = 1;
-  for (int c = 16; c >= 1; c /= 2) {
-    if (max_active[c] < units) continue;
-    int q = std::min(MK_MAX_SPLITS, max_active[c] / units);
-    q = std::min(q, std::max(1, max_items / (2 * c)));
-    if ((int64_t)units * q * c * 10 >= (int64_t)best * 9) {
-      C = c;
-      Q = q;
-      break;
-    }
-  }
-}
-
 template <int G, bool DENSE>
 cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                        const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
                        int max_items, size_t smem, cudaStream_t s) {
   static size_t set_bytes = 0;
+  static int occ = 1, sms = 0;
   if (smem > set_bytes) {
     cudaError_t e = cudaFuncSetAttribute(k_attn<G, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_attn<G, DENSE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
     set_bytes = smem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn<G, DENSE>, 256, smem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 1;
+    }
+    occ = std::max(1, n);
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+                                                  cudaSuccess)
+      sms = v;
   }
   const int units = cs.n * L.n_kv;
-  int C = 1, Q = 1;
-  choose_grid<G, DENSE>(units, max_items, smem, C, Q);
+  int P = std::max(1, (std::max(sms, 1) * occ) / units);
+  P = std::min(P, std::max(1, max_items / 2));
+  P = std::min(P, attn_max_parts(L));
   if (std::getenv("MK_LOG"))
-    std::fprintf(stderr, "[mosaickv] attention launch: %d units x Q=%d clusters x C=%d CTAs\n", units, Q, C);
-  return launch_pdl(k_attn<G, DENSE>, dim3(units * Q * C), dim3(256), smem, s, C, L, layer, cs, Q, ids, n_sel, q,
-                    K, V, t_stride, out);
+    std::fprintf(stderr, "[mosaickv] attention: %d units x %d CTAs (%d per SM), %zu B smem\n", units, P, occ, smem);
+  return launch_pdl(k_attn<G, DENSE>, dim3(units * P), dim3(256), smem, s, 0, L, layer, cs, P, ids, n_sel, q, K, V,
+                    t_stride, out);
 }
 
 template <bool DENSE>

@@ -53,7 +53,8 @@ struct Layout {
   int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, accumulator copies, stage bytes
   // workspace
   float* qrot;                  // [max_seqs][n_kv][G][128]
-  float* scores;                // [max_seqs][n_kv][nblk_cap]
+  float* scores;                // [max_seqs][n_kv][scores_stride]
+  int32_t scores_stride;        // nblk_cap rounded up to a multiple of 4
   float* part_acc;              // [max_seqs][n_kv][MK_MAX_SPLITS][G][128]
   float* part_ml;               // [max_seqs][n_kv][MK_MAX_SPLITS][G][2]
   int32_t* counters;            // [2][max_seqs][n_kv]: attention merge, selection top-k

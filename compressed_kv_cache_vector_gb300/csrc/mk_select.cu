@@ -64,23 +64,13 @@ __device__ __forceinline__ void split3(float x, uint16_t (&p)[3]) {
   }
 }
 
-// Block-wide exclusive scan of per-thread counts; total in *total.
-__device__ __forceinline__ int block_count_scan(int v, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int ex_w = warp_excl_scan(v, lane);
-  __syncthreads();
-  if (lane == 31) warp_tot[warp] = ex_w + v;
-  __syncthreads();
-  if (warp == 0) {
-    const int t = lane < nw ? warp_tot[lane] : 0;
-    const int ex = warp_excl_scan(t, lane);
-    if (lane < nw) warp_tot[lane] = ex;
-    if (lane == 31) warp_tot[32] = ex + t;
-  }
-  __syncthreads();
-  *total = warp_tot[32];
-  return warp_tot[warp] + ex_w;
+// Ties (keys equal to the threshold) held by warps 0..w-1.
+__device__ __forceinline__ int tie_before(const int* warp_tot, int w) {
+  int t = 0;
+  for (int i = 0; i < w; ++i) t += warp_tot[8 + i];
+  return t;
 }
+
 }  // namespace
 
 // grid: P CTAs per (sequence, kv head) of the call; 256 threads.
@@ -94,8 +84,8 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   __shared__ UnitDesc ud;
   __shared__ unsigned hist[256];
   __shared__ int warp_tot[33];
-  __shared__ uint32_t s_prefix;
   __shared__ int s_rem, s_abort, s_last;
+  __shared__ uint32_t s_lo, s_hi;
 
   const int unit_call = blockIdx.x / P, part = blockIdx.x - unit_call * P;
   const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
@@ -173,7 +163,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const int tper = (ntiles + P - 1) / P;
   const int t0 = part * tper, t1 = min(ntiles, t0 + tper);
   const uint16_t* meta = reinterpret_cast<const uint16_t*>(base + L.off_meta);
-  float* sc = L.scores + slot * L.nblk_cap;
+  float* sc = L.scores + slot * L.scores_stride;
   float* so = scores_out ? scores_out + ((int64_t)ci * L.n_kv + kvh) * L.nblk_cap : nullptr;
   unsigned char* stg = smem + (size_t)warp * 2 * kMetaTile;
   auto issue = [&](int t, unsigned char* dst) {
@@ -246,41 +236,72 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const int k = n_select(L, n_cand);
   int32_t* out = ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
   const bool all = k >= n_cand;
-  // Thread t owns blocks [t*R, t*R + R); its keys sit at t*(R+1) + i in shared
-  // memory (odd stride: conflict-free).  Key 0 marks a block that is not a
-  // candidate (an always-attended segment or past the end); real scores never
-  // map to 0, and since k <= #candidates the top k never reach key 0.
-  const int nth = blockDim.x;
-  const int R = (nblk + nth - 1) / nth;
-  const int RS = R | 1;
+  const int nth = blockDim.x, nw = nth >> 5;
+  // Keys in shared memory: one cp.async burst of the unit's scores, then
+  // converted in place (0 marks a block that is not a candidate: an
+  // always-attended segment; real scores never map to 0, and k <= #candidates
+  // keeps the top k away from it).
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-  const bool in_smem = (size_t)RS * nth * 4 <= (size_t)kSelSmem;
-  auto key_at = [&](int i) -> uint32_t {  // i-th key of this thread
-    const int b = tid * R + i;
-    if (b >= nblk) return 0u;
-    if (in_smem) return keys[tid * RS + i];
+  const bool in_smem = (size_t)nblk * 4 <= (size_t)kSelSmem;
+  if (in_smem) {
+    for (int i = tid; i < (nblk + 3) / 4; i += nth) cp_async16(keys + 4 * i, sc + 4 * i);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    for (int b = tid; b < nblk; b += nth) {
+      const float f = __uint_as_float(keys[b]);
+      keys[b] = ud.always[seg_of_block(ud, b)] ? 0u : ordered_key(f);
+    }
+    __syncthreads();
+  }
+  auto key_of = [&](int b) -> uint32_t {
+    if (in_smem) return keys[b];
     return ud.always[seg_of_block(ud, b)] ? 0u : ordered_key(__ldcg(sc + b));
   };
-  if (in_smem) {
-    for (int i = 0; i < R; ++i) {
-      const int b = tid * R + i;
-      uint32_t key = 0u;
-      if (b < nblk && !ud.always[seg_of_block(ud, b)]) key = ordered_key(__ldcg(sc + b));
-      keys[tid * RS + i] = key;
-    }
-  }
-  __syncthreads();
 
-  uint32_t prefix = 0, mask = 0;
-  int need = 0;
+  // Threshold search: the k-th largest candidate key lies in [lo, hi]; each
+  // pass counts the keys of that range in <= 256 bins of power-of-two width
+  // (spread over the data's own range, so few threads share a bin) and keeps
+  // the bin holding the k-th key, until the range is a single key value.
+  uint32_t prefix = 0;  // the threshold key once the search ends
+  int need = 0;         // how many keys equal to it are taken (lowest ids first)
   if (!all) {
-    if (tid == 0) s_rem = k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int b = tid; b < nblk; b += nth) {
+      const uint32_t key = key_of(b);
+      if (key != 0u) {
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+      }
+    }
+    kmin = __reduce_min_sync(FULL, kmin);
+    kmax = __reduce_max_sync(FULL, kmax);
+    if (lane == 0) {
+      hist[warp] = kmin;
+      hist[32 + warp] = kmax;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t a = 0xffffffffu, b = 0u;
+      for (int w = 0; w < nw; ++w) {
+        a = min(a, hist[w]);
+        b = max(b, hist[32 + w]);
+      }
+      s_lo = a;
+      s_hi = b;
+      s_rem = k;
+    }
+    __syncthreads();
+    for (int pass = 0; pass < 40; ++pass) {
+      const uint32_t lo = s_lo, hi = s_hi;
+      if (lo == hi) break;
+      const uint32_t span = hi - lo;  // >= 1
+      const int sh = max(0, 32 - __clz(span) - 8);  // bins of width 2^sh: (span >> sh) < 256
       for (int i = tid; i < 256; i += nth) hist[i] = 0;
       __syncthreads();
-      for (int i = 0; i < R; ++i) {
-        const uint32_t key = key_at(i);
-        if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      for (int b = tid; b < nblk; b += nth) {
+        const uint32_t key = key_of(b);
+        if (key != 0u && key >= lo && key <= hi) atomicAdd(&hist[(key - lo) >> sh], 1u);
       }
       __syncthreads();
       if (warp == 0) {
@@ -294,10 +315,13 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
         if (lane == src) {
           int acc = ex;
           for (int i = 0; i < 8; ++i) {
-            const int dgt = 255 - (8 * lane + i);
-            const int hc = (int)hist[dgt];
+            const int bin = 255 - (8 * lane + i);
+            const int hc = (int)hist[bin];
             if (acc + hc >= rem) {
-              s_prefix = (uint32_t)dgt;
+              const uint32_t blo = lo + ((uint32_t)bin << sh);
+              const uint64_t bhi = (uint64_t)blo + ((1ull << sh) - 1ull);
+              s_lo = blo;
+              s_hi = bhi < (uint64_t)hi ? (uint32_t)bhi : hi;
               s_rem = rem - acc;
               break;
             }
@@ -306,37 +330,46 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
         }
       }
       __syncthreads();
-      prefix |= s_prefix << shift;
-      mask |= 255u << shift;
     }
-    need = s_rem;  // ties (key == prefix) to take, lowest block ids first
+    prefix = s_lo;
+    need = s_rem;
   }
-  // Ordered compaction: counts per thread range, two block scans, then write.
-  int n_tie = 0, n_gt = 0;
-  for (int i = 0; i < R; ++i) {
-    const uint32_t key = key_at(i);
-    if (key == 0u) continue;
-    if (all || key > prefix) ++n_gt;
-    else if (key == prefix) ++n_tie;
+
+  // Ordered compaction: warp w owns blocks [w*RW, (w+1)*RW), walked 32 at a
+  // time with ballots; one block-wide scan gives each warp its offsets.
+  const int RW = ((nblk + nw - 1) / nw + 31) & ~31;
+  const int wb0 = warp * RW, wb1 = min(nblk, wb0 + RW);
+  int w_gt = 0, w_eq = 0;
+  for (int b0 = wb0; b0 < wb1; b0 += 32) {
+    const int b = b0 + lane;
+    const uint32_t key = b < wb1 ? key_of(b) : 0u;
+    w_gt += __popc(__ballot_sync(FULL, key != 0u && (all || key > prefix)));
+    w_eq += __popc(__ballot_sync(FULL, key != 0u && !all && key == prefix));
   }
-  int tie_tot;
-  const int tie_ex = block_count_scan(n_tie, warp_tot, &tie_tot);
-  const int take_ties = all ? 0 : max(0, min(n_tie, need - tie_ex));
-  int sel_tot;
-  int pos = block_count_scan(n_gt + take_ties, warp_tot, &sel_tot);
-  int ties_left = take_ties;
-  for (int i = 0; i < R; ++i) {
-    const uint32_t key = key_at(i);
-    if (key == 0u) continue;
-    bool sel = all || key > prefix;
-    if (!sel && key == prefix && ties_left > 0) {
-      sel = true;
-      --ties_left;
+  if (lane == 0) {
+    warp_tot[warp] = w_gt;
+    warp_tot[8 + warp] = w_eq;
+  }
+  __syncthreads();
+  int sel_off = 0, tie_off = 0;
+  for (int w = 0; w < warp; ++w) tie_off += warp_tot[8 + w];
+  for (int w = 0; w < warp; ++w) sel_off += warp_tot[w] + max(0, min(warp_tot[8 + w], need - tie_before(warp_tot, w)));
+  for (int b0 = wb0; b0 < wb1; b0 += 32) {
+    const int b = b0 + lane;
+    const uint32_t key = b < wb1 ? key_of(b) : 0u;
+    const unsigned gt = __ballot_sync(FULL, key != 0u && (all || key > prefix));
+    const unsigned eq = __ballot_sync(FULL, key != 0u && !all && key == prefix);
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int tie_rank = tie_off + __popc(eq & lt_mask);
+    const bool take_tie = ((eq >> lane) & 1u) && tie_rank < need;
+    const unsigned tk = __ballot_sync(FULL, take_tie);
+    const unsigned sel = gt | tk;
+    if ((sel >> lane) & 1u) {
+      const int pos = sel_off + __popc(sel & lt_mask);
+      if (pos < L.k_max) out[pos] = b;
     }
-    if (sel) {
-      if (pos < L.k_max) out[pos] = tid * R + i;
-      ++pos;
-    }
+    sel_off += __popc(sel);
+    tie_off += __popc(eq);
   }
   if (tid == 0) n_sel[(int64_t)ci * L.n_kv + kvh] = k;
 }

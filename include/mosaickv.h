@@ -206,7 +206,8 @@ mk_status mk_dense_decode_attn_noalloc(int32_t n_q_heads, int32_t n_kv_heads, in
                                        int64_t t_stride, void* out, mk_stream stream);
 
 /* Set-up helper, not on the decode path: gram = X^T X (fp32 accumulation)
- * for X: device bf16 rows of 128 values, row i at x + i*row_stride elements.
+ * for X: device bf16 rows of 128 values, row i at x + i*row_stride elements
+ * (x 16-byte aligned, row_stride a multiple of 8).
  * gram: device fp32 [128][128], overwritten. */
 mk_status mk_gram(const void* x, int64_t n_rows, int64_t row_stride, float* gram, mk_stream stream);
 
