@@ -79,7 +79,7 @@ Plan make_plan(const mk_config* c) {
   L.r_max = r_max;
   L.nblk_cap = mk::n_mid_blocks(L, c->max_tokens);
   L.k_max = std::max(1, mk::n_select(L, L.nblk_cap));
-  L.scores_stride = (std::max(1, L.nblk_cap) + 3) & ~3;
+  L.keys_stride = (std::max(1, L.nblk_cap) + 3) & ~3;
   L.page_stride = (int64_t)6 * L.B * r_max;
   const int64_t D = MK_HEAD_DIM;
   int64_t off = 0;
@@ -99,7 +99,8 @@ Plan make_plan(const mk_config* c) {
   const int64_t slots = (int64_t)c->max_seqs * c->n_kv_heads;
   int64_t w = 0;
   w = align_up(w + slots * L.G * D * 4);                       // qrot
-  w = align_up(w + slots * (int64_t)L.scores_stride * 4);      // scores
+  w = align_up(w + slots * (int64_t)L.keys_stride * 4);        // block keys
+  w = align_up(w + slots * (int64_t)mk::kKeyBins * 4);         // coarse key histograms
   w = align_up(w + slots * MK_MAX_SPLITS * L.G * D * 4);       // part_acc
   w = align_up(w + slots * MK_MAX_SPLITS * L.G * 2 * 4);       // part_ml
   w = align_up(w + slots * 4 * 2);                             // counters: attention, selection
@@ -119,7 +120,8 @@ void bind_pointers(Plan& p, void* arena, void* ws) {
   char* w = static_cast<char*>(ws);
   int64_t o = 0;
   L.qrot = reinterpret_cast<float*>(w + o); o = align_up(o + slots * L.G * D * 4);
-  L.scores = reinterpret_cast<float*>(w + o); o = align_up(o + slots * (int64_t)L.scores_stride * 4);
+  L.keys = reinterpret_cast<uint32_t*>(w + o); o = align_up(o + slots * (int64_t)L.keys_stride * 4);
+  L.khist = reinterpret_cast<uint32_t*>(w + o); o = align_up(o + slots * (int64_t)mk::kKeyBins * 4);
   L.part_acc = reinterpret_cast<float*>(w + o); o = align_up(o + slots * MK_MAX_SPLITS * L.G * D * 4);
   L.part_ml = reinterpret_cast<float*>(w + o); o = align_up(o + slots * MK_MAX_SPLITS * L.G * 2 * 4);
   L.counters = reinterpret_cast<int32_t*>(w + o);
@@ -225,6 +227,7 @@ mk_status mk_create(const mk_config* cfg, void* arena, size_t arena_bytes, void*
   int r_min = MK_HEAD_DIM;
   for (int i = 0; i < cfg->n_segments; ++i) r_min = std::min(r_min, (int)cfg->seg[i].r);
   if (mk::attn_plan(p.L, r_min) == 0) return MK_ENOTSUP;
+  if (!mk::select_plan_ok(p.L)) return MK_ENOTSUP;
   bind_pointers(p, arena, workspace);
   mk_ctx* ctx = new (std::nothrow) mk_ctx();
   if (!ctx) return MK_ENOMEM;
@@ -240,6 +243,8 @@ mk_status mk_create(const mk_config* cfg, void* arena, size_t arena_bytes, void*
   ctx->rot_set.assign(ls * cfg->n_kv_heads, 0);
   cudaError_t e = cudaMemset(arena, 0, (size_t)p.units_off);
   if (e == cudaSuccess) e = cudaMemset(ctx->L.counters, 0, sizeof(int32_t) * 2 * cfg->max_seqs * cfg->n_kv_heads);
+  if (e == cudaSuccess)
+    e = cudaMemset(ctx->L.khist, 0, sizeof(uint32_t) * mk::kKeyBins * cfg->max_seqs * cfg->n_kv_heads);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     delete ctx;

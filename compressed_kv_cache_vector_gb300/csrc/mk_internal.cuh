@@ -14,6 +14,7 @@ constexpr int D = MK_HEAD_DIM;
 constexpr int kDenseChunk = 16;        // tokens per dense work item in attention
 constexpr int kTileTokens = 64;        // tokens per bulk-append tile
 constexpr int kSmallAppend = 16;       // largest per-sequence append handled by the decode kernel
+constexpr int kKeyBins = 4096;         // coarse key histogram of the block selection (top 12 key bits)
 constexpr uint32_t FULL = 0xffffffffu;
 
 // Device error codes (detail word); the status word holds MK_EDEVICE.
@@ -53,8 +54,9 @@ struct Layout {
   int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, accumulator copies, stage bytes
   // workspace
   float* qrot;                  // [max_seqs][n_kv][G][128]
-  float* scores;                // [max_seqs][n_kv][scores_stride]
-  int32_t scores_stride;        // nblk_cap rounded up to a multiple of 4
+  uint32_t* keys;               // [max_seqs][n_kv][keys_stride]: ordered block-score keys, 0 = not a candidate
+  int32_t keys_stride;          // nblk_cap rounded up to a multiple of 4
+  uint32_t* khist;              // [max_seqs][n_kv][kKeyBins]: key counts by top 12 bits (zero between calls)
   float* part_acc;              // [max_seqs][n_kv][MK_MAX_SPLITS][G][128]
   float* part_ml;               // [max_seqs][n_kv][MK_MAX_SPLITS][G][2]
   int32_t* counters;            // [2][max_seqs][n_kv]: attention merge, selection top-k
@@ -213,6 +215,8 @@ cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, 
                                 const uint16_t* v, int evict_only, cudaStream_t s);
 cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
                                const uint16_t* v, int total_tiles, cudaStream_t s);
+// Whether the block selection can handle the context's largest block count.
+bool select_plan_ok(const Layout& L);
 cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,
                                 int32_t* ids, int32_t* n_sel, float* scores_out, int max_nblk,
                                 cudaStream_t s);

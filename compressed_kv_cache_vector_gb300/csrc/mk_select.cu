@@ -17,8 +17,18 @@
 //    split exactly into three bf16 parts (24 = 3 x 8 significant bits) and the
 //    meta values are bf16, so every product is exact and the accumulation is
 //    fp32: the scores keep fp32 accuracy.
+//  * Each score is written as an order-preserving 32-bit key (0 for blocks of
+//    always-attended segments, which are not candidates) and counted in a
+//    4096-bin histogram of the keys' top 12 bits, kept in shared memory and
+//    added to the unit's histogram in global memory when the CTA is done.
 //  * The last CTA of each (sequence, kv head) to finish (atomic counter, no
-//    waiting) runs the radix top-k over the unit's scores in shared memory.
+//    waiting) selects the top k: the histogram gives the coarse bin of the
+//    k-th largest key; keys above it are taken outright, keys inside it are
+//    gathered into a short list that two 1024-bin passes resolve to the exact
+//    threshold; the ids are then written in ascending order from per-thread
+//    bit masks and one block scan.  Every loop does the same work on every
+//    thread (no per-key serial chains), because a single CTA of 8 warps runs
+//    it and its time is latency, not bandwidth.
 #include <algorithm>
 
 #include "mk_internal.cuh"
@@ -30,8 +40,20 @@ constexpr int kSelWarps = 8;
 constexpr int kMT = 16;                       // blocks per MMA tile
 constexpr int kMetaRow = 2 * D + 8;           // padded bf16 row (528 bytes): ldmatrix conflict-free
 constexpr int kMetaTile = kMT * kMetaRow * 2; // bytes per staged tile
-constexpr int kSelSmem = kSelWarps * 2 * kMetaTile;  // double-buffered tiles (also holds R_k^T and keys)
+constexpr int kSelSmem = kSelWarps * 2 * kMetaTile;  // double-buffered tiles (also holds R_k^T)
+constexpr int kSelSmemMax = 192 * 1024;              // dynamic shared memory cap (top-k key staging)
+constexpr int kFineBins = 1024;
 static_assert(kSelSmem >= D * D * 4, "R_k^T staging fits in the tile area");
+
+// Top-k plan for nblk keys: each thread owns CPT 16-byte chunks (4 keys),
+// CPT a multiple of 8; the keys are staged in shared memory when they fit
+// beside the two per-thread mask arrays (else read from global memory).
+__host__ __device__ inline int topk_cpt(int nblk) {
+  const int nch = (nblk + 3) >> 2;
+  return ((nch + 255) / 256 + 7) & ~7;
+}
+__host__ __device__ inline int64_t topk_mask_bytes(int cpt) { return (int64_t)256 * cpt; }
+__host__ __device__ inline int64_t topk_stage_bytes(int cpt) { return (int64_t)256 * cpt * 16; }
 
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -64,11 +86,65 @@ __device__ __forceinline__ void split3(float x, uint16_t (&p)[3]) {
   }
 }
 
-// Ties (keys equal to the threshold) held by warps 0..w-1.
-__device__ __forceinline__ int tie_before(const int* warp_tot, int w) {
-  int t = 0;
-  for (int i = 0; i < w; ++i) t += warp_tot[8 + i];
-  return t;
+// Exclusive prefix sums of two per-thread counts over the CTA (256 threads).
+__device__ __forceinline__ int2 block_excl_scan2(int a, int b, int2* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int xa = a, xb = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ya = __shfl_up_sync(FULL, xa, o), yb = __shfl_up_sync(FULL, xb, o);
+    if (lane >= o) {
+      xa += ya;
+      xb += yb;
+    }
+  }
+  if (lane == 31) wsum[warp] = make_int2(xa, xb);
+  __syncthreads();
+  int pa = 0, pb = 0;
+  for (int w = 0; w < warp; ++w) {
+    pa += wsum[w].x;
+    pb += wsum[w].y;
+  }
+  __syncthreads();
+  return make_int2(pa + xa - a, pb + xb - b);
+}
+
+// Histogram h of NB bins, bin index increasing with the key: find the bin
+// holding the rem-th largest key.  Thread t reads the t-th slice of NB/256
+// bins from the top; the thread whose slice holds it writes the bin and the
+// rank of the key inside the bin.  Ends with a barrier.
+template <int NB>
+__device__ __forceinline__ void find_bin(const uint32_t* h, int rem, int2* wsum, int* s_bin, int* s_rem) {
+  constexpr int PER = NB / 256;
+  static_assert(PER % 4 == 0, "slices of whole 16-byte words");
+  const int t = threadIdx.x;
+  const uint4* hv = reinterpret_cast<const uint4*>(h + NB - PER * (t + 1));
+  uint32_t v[PER];
+#pragma unroll
+  for (int i = 0; i < PER / 4; ++i) {
+    const uint4 x = hv[i];
+    v[4 * i] = x.x;
+    v[4 * i + 1] = x.y;
+    v[4 * i + 2] = x.z;
+    v[4 * i + 3] = x.w;
+  }
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) c += (int)v[i];
+  const int ex = block_excl_scan2(c, 0, wsum).x;
+  if (ex < rem && ex + c >= rem) {
+    int acc = ex;
+#pragma unroll
+    for (int i = PER - 1; i >= 0; --i) {
+      const int hb = (int)v[i];
+      if (acc < rem && acc + hb >= rem) {
+        *s_bin = NB - PER * (t + 1) + i;
+        *s_rem = rem - acc;
+      }
+      acc += hb;
+    }
+  }
+  __syncthreads();
 }
 
 }  // namespace
@@ -77,15 +153,16 @@ __device__ __forceinline__ int tie_before(const int* warp_tot, int w) {
 template <int G>
 __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs cs, int P,
                                                    const uint16_t* __restrict__ q, int32_t* __restrict__ ids,
-                                                   int32_t* __restrict__ n_sel, float* __restrict__ scores_out) {
+                                                   int32_t* __restrict__ n_sel, float* __restrict__ scores_out,
+                                                   int dyn_bytes) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ float qs[G][D];
   __shared__ float qr[2][G][D];
   __shared__ UnitDesc ud;
-  __shared__ unsigned hist[256];
-  __shared__ int warp_tot[33];
-  __shared__ int s_rem, s_abort, s_last;
-  __shared__ uint32_t s_lo, s_hi;
+  __shared__ __align__(16) uint32_t hc[kKeyBins];   // coarse key histogram
+  __shared__ __align__(16) uint32_t hf[kFineBins];  // fine histogram of the threshold search
+  __shared__ int2 wsum[kSelWarps];
+  __shared__ int s_abort, s_last, s_bin, s_rem, s_len;
 
   const int unit_call = blockIdx.x / P, part = blockIdx.x - unit_call * P;
   const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
@@ -96,6 +173,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const int64_t slot = (int64_t)seq * L.n_kv + kvh;
   for (int i = tid; i < G * D; i += blockDim.x)
     qs[i / D][i % D] = bf2f(q[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D + i]);
+  for (int i = tid; i < kKeyBins / 4; i += blockDim.x) reinterpret_cast<uint4*>(hc)[i] = make_uint4(0, 0, 0, 0);
   const char* base = unit_base(L, u);
   {
     const float4* src = reinterpret_cast<const float4*>(base + L.off_rkt);
@@ -133,17 +211,17 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
 #pragma unroll
   for (int kc = 0; kc < 16; ++kc)
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
+    for (int hf2 = 0; hf2 < 2; ++hf2) {
       uint16_t e0[3] = {0, 0, 0}, e1[3] = {0, 0, 0};
       if (g < G) {
-        const int k = kc * 16 + hf * 8 + 2 * tig;
+        const int k = kc * 16 + hf2 * 8 + 2 * tig;
         const float x0 = k < D ? fminf(qr[0][g][k], 0.0f) : fmaxf(qr[0][g][k - D], 0.0f);
         const float x1 = (k + 1) < D ? fminf(qr[0][g][k + 1], 0.0f) : fmaxf(qr[0][g][k + 1 - D], 0.0f);
         split3(x0, e0);
         split3(x1, e1);
       }
 #pragma unroll
-      for (int s = 0; s < 3; ++s) bq[s][kc][hf] = (uint32_t)e0[s] | ((uint32_t)e1[s] << 16);
+      for (int s = 0; s < 3; ++s) bq[s][kc][hf2] = (uint32_t)e0[s] | ((uint32_t)e1[s] << 16);
     }
   // Everything above used only q and R_k.  From here on the kernel reads
   // what the append kernel wrote (lengths, block keys).
@@ -163,7 +241,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const int tper = (ntiles + P - 1) / P;
   const int t0 = part * tper, t1 = min(ntiles, t0 + tper);
   const uint16_t* meta = reinterpret_cast<const uint16_t*>(base + L.off_meta);
-  float* sc = L.scores + slot * L.scores_stride;
+  uint32_t* kw = L.keys + slot * L.keys_stride;
   float* so = scores_out ? scores_out + ((int64_t)ci * L.n_kv + kvh) * L.nblk_cap : nullptr;
   unsigned char* stg = smem + (size_t)warp * 2 * kMetaTile;
   auto issue = [&](int t, unsigned char* dst) {
@@ -173,6 +251,13 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
       const int b = t * kMT + row;
       if (b < nblk) cp_async16(dst + row * kMetaRow * 2 + prt * 16, meta + (int64_t)b * 2 * D + prt * 8);
     }
+  };
+  // Write block b's score: the user's fp32 copy, the key, the histogram count.
+  auto emit = [&](int b, float sc) {
+    if (so) so[b] = sc;
+    const uint32_t key = ud.always[seg_of_block(ud, b)] ? 0u : ordered_key(sc);
+    kw[b] = key;
+    if (key) atomicAdd(&hc[key >> 20], 1u);
   };
   const float inv_sqrt_d = 0.08838834764831845f;
   int st = 0;
@@ -206,19 +291,23 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     b_hi = fmaxf(b_hi, __shfl_xor_sync(FULL, b_hi, 2));
     if (tig == 0) {
       const int b0 = t * kMT + g, b1 = b0 + 8;
-      if (b0 < nblk) {
-        sc[b0] = b_lo * inv_sqrt_d;
-        if (so) so[b0] = b_lo * inv_sqrt_d;
-      }
-      if (b1 < nblk) {
-        sc[b1] = b_hi * inv_sqrt_d;
-        if (so) so[b1] = b_hi * inv_sqrt_d;
-      }
+      if (b0 < nblk) emit(b0, b_lo * inv_sqrt_d);
+      if (b1 < nblk) emit(b1, b_hi * inv_sqrt_d);
     }
     __syncwarp();
     st ^= 1;
   }
   cp_async_wait_all();
+  __syncthreads();
+  // Add this CTA's histogram to the unit's.
+  uint32_t* gh = L.khist + slot * kKeyBins;
+  for (int i = tid; i < kKeyBins / 4; i += blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(hc)[i];
+    if (v.x) atomicAdd(gh + 4 * i, v.x);
+    if (v.y) atomicAdd(gh + 4 * i + 1, v.y);
+    if (v.z) atomicAdd(gh + 4 * i + 2, v.z);
+    if (v.w) atomicAdd(gh + 4 * i + 3, v.w);
+  }
 
   // ---- the last CTA of this (sequence, kv head) selects the top-k ---------
   __threadfence();
@@ -235,143 +324,207 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const int n_cand = n_scored_blocks(ud, nblk);
   const int k = n_select(L, n_cand);
   int32_t* out = ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
-  const bool all = k >= n_cand;
-  const int nth = blockDim.x, nw = nth >> 5;
-  // Keys in shared memory: one cp.async burst of the unit's scores, then
-  // converted in place (0 marks a block that is not a candidate: an
-  // always-attended segment; real scores never map to 0, and k <= #candidates
-  // keeps the top k away from it).
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-  const bool in_smem = (size_t)nblk * 4 <= (size_t)kSelSmem;
-  if (in_smem) {
-    for (int i = tid; i < (nblk + 3) / 4; i += nth) cp_async16(keys + 4 * i, sc + 4 * i);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
-    for (int b = tid; b < nblk; b += nth) {
-      const float f = __uint_as_float(keys[b]);
-      keys[b] = ud.always[seg_of_block(ud, b)] ? 0u : ordered_key(f);
+  const bool all = k >= n_cand;  // every candidate is taken
+  const int nch = (nblk + 3) >> 2;
+  const int CPT = topk_cpt(nblk), NG = CPT >> 3;
+  const bool staged = topk_stage_bytes(CPT) + topk_mask_bytes(CPT) <= (int64_t)dyn_bytes;
+  uint4* ks = reinterpret_cast<uint4*>(smem);
+  uint32_t* m_above = reinterpret_cast<uint32_t*>(smem + (staged ? topk_stage_bytes(CPT) : 0));
+  uint32_t* m_in = m_above + NG * 256;
+  uint32_t* list = m_in + NG * 256;
+  const int list_cap = (int)((dyn_bytes - (reinterpret_cast<unsigned char*>(list) - smem)) / 4);
+
+  // The unit's histogram (then cleared for the next call) and its keys.
+  for (int i = tid; i < kKeyBins / 4; i += blockDim.x) cp_async16(hc + 4 * i, gh + 4 * i);
+  cp_async_commit();
+  if (staged) {
+    // chunk c at c ^ ((c / CPT) & 7): the 8 threads of a quarter warp reading
+    // their j-th chunks hit 8 different 16-byte bank groups.
+    for (int c = tid; c < 256 * CPT; c += blockDim.x) {
+      uint4* dst = ks + (c ^ ((c / CPT) & 7));
+      if (c < nch) cp_async16(dst, kw + 4 * c);
+      else *dst = make_uint4(0, 0, 0, 0);
     }
-    __syncthreads();
   }
-  auto key_of = [&](int b) -> uint32_t {
-    if (in_smem) return keys[b];
-    return ud.always[seg_of_block(ud, b)] ? 0u : ordered_key(__ldcg(sc + b));
+  cp_async_commit();
+  asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+  __syncthreads();
+  for (int i = tid; i < kKeyBins / 4; i += blockDim.x) reinterpret_cast<uint4*>(gh)[i] = make_uint4(0, 0, 0, 0);
+  // Undecided range [lo, hi]: the coarse bin of the k-th largest key.
+  uint32_t lo = 1u, hi = 0xffffffffu;
+  int rem = 0;
+  if (!all) {
+    find_bin<kKeyBins>(hc, k, wsum, &s_bin, &s_rem);
+    lo = max(1u, (uint32_t)s_bin << 20);
+    hi = ((uint32_t)s_bin << 20) | 0xfffffu;
+    rem = s_rem;
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  if (staged && tid == 0 && (nblk & 3)) {  // key slots past nblk in the last chunk
+    const int c = nch - 1;
+    uint32_t* last = reinterpret_cast<uint32_t*>(ks + (c ^ ((c / CPT) & 7)));
+    for (int e = nblk & 3; e < 4; ++e) last[e] = 0u;
+  }
+  __syncthreads();
+  // Thread tid's j-th chunk: keys tid*CPT*4 + 4j .. +3.
+  auto chunk = [&](int j) -> uint4 {
+    if (staged) return ks[tid * CPT + (j ^ (tid & 7))];
+    const int c = tid * CPT + j;
+    if (c >= nch) return make_uint4(0, 0, 0, 0);
+    uint4 v = __ldcg(reinterpret_cast<const uint4*>(kw) + c);
+    const int e0 = 4 * c;
+    if (e0 + 1 >= nblk) v.y = 0u;
+    if (e0 + 2 >= nblk) v.z = 0u;
+    if (e0 + 3 >= nblk) v.w = 0u;
+    return v;
+  };
+  auto key_at = [&](int i) -> uint32_t {  // i: key index within this thread's range
+    const uint4 v = chunk(i >> 2);
+    const int qq = i & 3;
+    return qq == 0 ? v.x : qq == 1 ? v.y : qq == 2 ? v.z : v.w;
   };
 
-  // Threshold search: the k-th largest candidate key lies in [lo, hi]; each
-  // pass counts the keys of that range in <= 256 bins of power-of-two width
-  // (spread over the data's own range, so few threads share a bin) and keeps
-  // the bin holding the k-th key, until the range is a single key value.
-  uint32_t prefix = 0;  // the threshold key once the search ends
-  int need = 0;         // how many keys equal to it are taken (lowest ids first)
-  if (!all) {
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-    for (int b = tid; b < nblk; b += nth) {
-      const uint32_t key = key_of(b);
-      if (key != 0u) {
-        kmin = min(kmin, key);
-        kmax = max(kmax, key);
-      }
-    }
-    kmin = __reduce_min_sync(FULL, kmin);
-    kmax = __reduce_max_sync(FULL, kmax);
-    if (lane == 0) {
-      hist[warp] = kmin;
-      hist[32 + warp] = kmax;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t a = 0xffffffffu, b = 0u;
-      for (int w = 0; w < nw; ++w) {
-        a = min(a, hist[w]);
-        b = max(b, hist[32 + w]);
-      }
-      s_lo = a;
-      s_hi = b;
-      s_rem = k;
-    }
-    __syncthreads();
-    for (int pass = 0; pass < 40; ++pass) {
-      const uint32_t lo = s_lo, hi = s_hi;
-      if (lo == hi) break;
-      const uint32_t span = hi - lo;  // >= 1
-      const int sh = max(0, 32 - __clz(span) - 8);  // bins of width 2^sh: (span >> sh) < 256
-      for (int i = tid; i < 256; i += nth) hist[i] = 0;
-      __syncthreads();
-      for (int b = tid; b < nblk; b += nth) {
-        const uint32_t key = key_of(b);
-        if (key != 0u && key >= lo && key <= hi) atomicAdd(&hist[(key - lo) >> sh], 1u);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        const int rem = s_rem;
-        int cnt = 0;
+  // Pass 1: per 32 keys, masks of the keys above the range (taken) and inside it.
+  const bool top_bin = !all && hi == 0xffffffffu;  // nothing lies above the top bin
+  const uint32_t above_from = all ? 1u : hi + 1u;
+  int n_above = 0, n_in = 0;
+  for (int gi = 0; gi < NG; ++gi) {
+    uint32_t ab = 0, ib = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cnt += (int)hist[255 - (8 * lane + i)];
-        const int ex = warp_excl_scan(cnt, lane);
-        const unsigned hit = __ballot_sync(FULL, ex + cnt >= rem);
-        const int src = __ffs(hit) - 1;
-        if (lane == src) {
-          int acc = ex;
-          for (int i = 0; i < 8; ++i) {
-            const int bin = 255 - (8 * lane + i);
-            const int hc = (int)hist[bin];
-            if (acc + hc >= rem) {
-              const uint32_t blo = lo + ((uint32_t)bin << sh);
-              const uint64_t bhi = (uint64_t)blo + ((1ull << sh) - 1ull);
-              s_lo = blo;
-              s_hi = bhi < (uint64_t)hi ? (uint32_t)bhi : hi;
-              s_rem = rem - acc;
-              break;
+    for (int jj = 0; jj < 8; ++jj) {
+      const uint4 v = chunk(gi * 8 + jj);
+      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        if (!top_bin && e[qq] >= above_from) ab |= 1u << (jj * 4 + qq);
+        if (!all && e[qq] - lo <= hi - lo) ib |= 1u << (jj * 4 + qq);
+      }
+    }
+    m_above[gi * 256 + tid] = ab;
+    m_in[gi * 256 + tid] = ib;
+    n_above += __popc(ab);
+    n_in += __popc(ib);
+  }
+
+  // Threshold: the rem-th largest key inside [lo, hi], found by two passes of
+  // kFineBins bins (the range spans at most 2^20 keys).
+  uint32_t thr = 0;
+  int need = 0;
+  if (!all) {
+    const int off0 = block_excl_scan2(n_in, 0, wsum).x;
+    if (tid == blockDim.x - 1) s_len = off0 + n_in;
+    __syncthreads();
+    const int len = s_len;
+    const bool listed = len <= list_cap;
+    if (listed) {
+      int off = off0;
+      for (int gi = 0; gi < NG; ++gi) {
+        const uint32_t ib = m_in[gi * 256 + tid];
+        if (ib) {
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const uint4 v = chunk(gi * 8 + jj);
+            const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const int bb = jj * 4 + qq;
+              if ((ib >> bb) & 1u) list[off + __popc(ib & ((1u << bb) - 1u))] = e[qq];
             }
-            acc += hc;
+          }
+        }
+        off += __popc(ib);
+      }
+    }
+    for (int pass = 0; pass < 2 && lo != hi; ++pass) {
+      const int sh = max(0, 32 - __clz(hi - lo) - 10);  // (hi - lo) >> sh < kFineBins
+      for (int i = tid; i < kFineBins; i += blockDim.x) hf[i] = 0;
+      __syncthreads();
+      if (listed) {
+        for (int i = tid; i < len; i += blockDim.x) {
+          const uint32_t key = list[i];
+          if (key - lo <= hi - lo) atomicAdd(&hf[(key - lo) >> sh], 1u);
+        }
+      } else {
+        for (int gi = 0; gi < NG; ++gi) {
+          uint32_t m = m_in[gi * 256 + tid];
+          while (m) {
+            const int bb = __ffs(m) - 1;
+            m &= m - 1;
+            const uint32_t key = key_at(gi * 32 + bb);
+            if (key - lo <= hi - lo) atomicAdd(&hf[(key - lo) >> sh], 1u);
           }
         }
       }
       __syncthreads();
+      find_bin<kFineBins>(hf, rem, wsum, &s_bin, &s_rem);
+      const uint32_t nlo = lo + ((uint32_t)s_bin << sh);
+      const uint64_t nhi = (uint64_t)nlo + ((1ull << sh) - 1ull);
+      hi = nhi < (uint64_t)hi ? (uint32_t)nhi : hi;
+      lo = nlo;
+      rem = s_rem;
     }
-    prefix = s_lo;
-    need = s_rem;
+    thr = lo;
+    need = rem;  // keys equal to thr that are taken, lowest block ids first
   }
 
-  // Ordered compaction: warp w owns blocks [w*RW, (w+1)*RW), walked 32 at a
-  // time with ballots; one block-wide scan gives each warp its offsets.
-  const int RW = ((nblk + nw - 1) / nw + 31) & ~31;
-  const int wb0 = warp * RW, wb1 = min(nblk, wb0 + RW);
-  int w_gt = 0, w_eq = 0;
-  for (int b0 = wb0; b0 < wb1; b0 += 32) {
-    const int b = b0 + lane;
-    const uint32_t key = b < wb1 ? key_of(b) : 0u;
-    w_gt += __popc(__ballot_sync(FULL, key != 0u && (all || key > prefix)));
-    w_eq += __popc(__ballot_sync(FULL, key != 0u && !all && key == prefix));
-  }
-  if (lane == 0) {
-    warp_tot[warp] = w_gt;
-    warp_tot[8 + warp] = w_eq;
-  }
-  __syncthreads();
-  int sel_off = 0, tie_off = 0;
-  for (int w = 0; w < warp; ++w) tie_off += warp_tot[8 + w];
-  for (int w = 0; w < warp; ++w) sel_off += warp_tot[w] + max(0, min(warp_tot[8 + w], need - tie_before(warp_tot, w)));
-  for (int b0 = wb0; b0 < wb1; b0 += 32) {
-    const int b = b0 + lane;
-    const uint32_t key = b < wb1 ? key_of(b) : 0u;
-    const unsigned gt = __ballot_sync(FULL, key != 0u && (all || key > prefix));
-    const unsigned eq = __ballot_sync(FULL, key != 0u && !all && key == prefix);
-    const unsigned lt_mask = (1u << lane) - 1u;
-    const int tie_rank = tie_off + __popc(eq & lt_mask);
-    const bool take_tie = ((eq >> lane) & 1u) && tie_rank < need;
-    const unsigned tk = __ballot_sync(FULL, take_tie);
-    const unsigned sel = gt | tk;
-    if ((sel >> lane) & 1u) {
-      const int pos = sel_off + __popc(sel & lt_mask);
-      if (pos < L.k_max) out[pos] = b;
+  // Pass 2: the undecided keys above thr join the taken ones; the ones equal
+  // to it are the ties.
+  int n_gt = n_above, n_eq = 0;
+  if (!all)
+    for (int gi = 0; gi < NG; ++gi) {
+      const uint32_t ib = m_in[gi * 256 + tid];
+      uint32_t gm = 0, em = 0;
+      if (ib) {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const uint4 v = chunk(gi * 8 + jj);
+          const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            if (e[qq] > thr) gm |= 1u << (jj * 4 + qq);
+            if (e[qq] == thr) em |= 1u << (jj * 4 + qq);
+          }
+        }
+        gm &= ib;
+        em &= ib;
+      }
+      m_above[gi * 256 + tid] |= gm;
+      m_in[gi * 256 + tid] = em;
+      n_gt += __popc(gm);
+      n_eq += __popc(em);
     }
-    sel_off += __popc(sel);
-    tie_off += __popc(eq);
+  const int2 ex = block_excl_scan2(n_gt, n_eq, wsum);
+
+  // Ordered output: thread tid's ids follow those of threads 0..tid-1.
+  int take_eq = all ? 0 : max(0, min(n_eq, need - ex.y));
+  int pos = ex.x + min(ex.y, need);
+  const int kbase = tid * CPT * 4;
+  for (int gi = 0; gi < NG; ++gi) {
+    uint32_t sel = m_above[gi * 256 + tid];
+    if (!all) {
+      uint32_t em = m_in[gi * 256 + tid];
+      while (take_eq > 0 && em) {
+        sel |= em & (0u - em);
+        em &= em - 1;
+        --take_eq;
+      }
+    }
+    if (sel) {
+#pragma unroll
+      for (int bb = 0; bb < 32; ++bb) {
+        const int p = pos + __popc(sel & ((1u << bb) - 1u));
+        if (((sel >> bb) & 1u) && p < L.k_max) out[p] = kbase + gi * 32 + bb;
+      }
+    }
+    pos += __popc(sel);
   }
   if (tid == 0) n_sel[(int64_t)ci * L.n_kv + kvh] = k;
+}
+
+bool select_plan_ok(const Layout& L) {
+  // Without staged keys the selection still needs its two mask arrays.
+  return topk_mask_bytes(topk_cpt(std::max(1, L.nblk_cap))) <= (int64_t)kSelSmem;
 }
 
 cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,
@@ -382,16 +535,21 @@ cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, 
   int P = std::max(1, 152 / units);
   P = std::min(P, std::max(1, (tiles + kSelWarps - 1) / kSelWarps));
   const dim3 grid(units * P);
+  // Dynamic shared memory: the meta tile stages, or the top-k's keys, masks
+  // and list for the context's largest block count, whichever is larger.
+  const int cpt = topk_cpt(L.nblk_cap);
+  const int64_t want = topk_stage_bytes(cpt) + topk_mask_bytes(cpt) + (int64_t)4 * L.nblk_cap;
+  const int dyn = (int)std::max<int64_t>(kSelSmem, std::min<int64_t>(kSelSmemMax, want));
 #define MK_SEL_CASE(GG)                                                                                      \
   case GG: {                                                                                                 \
-    static bool set = false;                                                                                 \
-    if (!set) {                                                                                              \
-      cudaError_t e = cudaFuncSetAttribute(k_select<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem); \
+    static int set = 0;                                                                                      \
+    if (set < dyn) {                                                                                         \
+      cudaError_t e = cudaFuncSetAttribute(k_select<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);  \
       if (e != cudaSuccess) return e;                                                                        \
-      set = true;                                                                                            \
+      set = dyn;                                                                                             \
     }                                                                                                        \
-    return launch_pdl(k_select<GG>, grid, dim3(256), kSelSmem, s, 0, L, layer, cs, P, q, ids, n_sel,        \
-                      scores_out);                                                                           \
+    return launch_pdl(k_select<GG>, grid, dim3(256), dyn, s, 0, L, layer, cs, P, q, ids, n_sel, scores_out, \
+                      dyn);                                                                                  \
   }
   switch (L.G) {
     MK_SEL_CASE(1)

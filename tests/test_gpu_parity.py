@@ -153,6 +153,54 @@ def test_block_select_scores_and_ids(G, topk_fixed, retain):
     assert near_ties <= 1
 
 
+@pytest.mark.parametrize("T,retain,segments", [
+    (480_000, 100, [(0, 32, 0)]),                # ~30K blocks: keys staged, in-bin list too long
+    (720_000, 50, [(0, 32, 0)]),                 # ~45K blocks: keys read from global memory
+    (200_000, 100, [(0, 32, 0), (500, 16, 1)]),  # always-attended second half: not candidates
+])
+def test_block_select_all_ties_large(T, retain, segments):
+    """Every token carries the same key, so every candidate block has the same
+    score and the top-k is the k lowest candidate ids (ties go to the lower id)."""
+    from compressed_kv_cache_vector_gb300 import synth
+    from tests.harness import signed_permutation
+    S, W, B, G = 4, 64, 16, 4
+    st = O.Strategy(S, W, B, list(segments), 0, retain)
+    cfg = make_config(G, 1, 1, 1, T + 1, S, W, B, segments, 0, retain)
+    mk = MosaicKV(cfg, "cuda")
+    Rk, Rv = signed_permutation(31), signed_permutation(37)
+    mk.set_rotation(0, 0, 0, Rk.astype(np.float32), Rv.astype(np.float32))
+    rows = synth.lowrank_outlier(64, D, 0.9, 123, device="cuda")
+    k_row, v_row = rows[5:6], rows[9:10]
+    mk.append(0, [0], [T], k_row.expand(T, D).reshape(T, 1, D).contiguous(),
+              v_row.expand(T, D).reshape(T, 1, D).contiguous())
+    q = synth.query(1, G, D, 77, device="cuda")
+    scores = torch.full((1, 1, mk.nblk_cap), float("nan"), dtype=torch.float32, device="cuda")
+    ids, n_sel = mk.block_select(0, [0], q, scores=scores)
+    torch.cuda.synchronize()
+    assert mk.poll_error()[0] == 0
+    # The oracle's score of one such block, from a short cache of the same tokens.
+    Ts = S + W + 3 * B
+    oc = O.OracleCache(O.Strategy(S, W, B, [(0, 32, 0)], 0, retain), Ts)
+    oc.set_rotation(Rk, Rv)
+    oc.append(synth.bf16_values(k_row.expand(Ts, D)), synth.bf16_values(v_row.expand(Ts, D)))
+    qs = q[0].cpu().to(torch.float64).numpy()
+    _, grp = oc.scores(qs)
+    mn, mx = oc.meta()
+    tol = score_tolerance(oc.rotate_query(qs), mn, mx)
+    assert np.all(grp == grp[0])
+    # The long cache's candidates and k, from the oracle's segment rules.
+    nb = O.n_middle_blocks(T, st)
+    firsts = O.segment_first_blocks(T, st)
+    cand = np.array([b for b in range(nb) if not st.segments[O.block_segment(b, firsts)][2]], dtype=np.int64)
+    k = O.n_select(len(cand), st)
+    got_s = scores[0, 0, :nb].cpu().numpy().astype(np.float64)
+    assert np.all(got_s[cand] == got_s[cand[0]])
+    assert abs(got_s[cand[0]] - grp[0]) <= tol[0]
+    assert int(n_sel[0, 0]) == k
+    want = O.topk_blocks(np.full(nb, grp[0]), cand, k)
+    assert np.array_equal(ids[0, 0, :k].cpu().numpy(), want)
+
+
 @pytest.mark.parametrize("case", [
     Case(n_q=4, n_kv=2, seq_lens=[2048, 700], rot="eigh", steps=[1] * 5 + [40], seed=11),
     Case(n_q=8, n_kv=1, seq_lens=[5000], rot="eigh", block=64, window=256, segments=[(0, 38, 0)],
