@@ -17,11 +17,19 @@
 //    its items into shared memory with cp.async.
 //  * Per group the warp rebuilds positions in one 16 x 128 bf16 tile: it
 //    zero-fills it and scatters the kept key values by their channel indices
-//    (two lanes per token), computes the logits S^T[16 tok x 8 heads] on the
-//    tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate), then does the
-//    same for the values and accumulates O'^T[128 x 8 heads].  The fp32
+//    (two lanes per token).  The logits are computed transposed,
+//    S[head][token] = q' K^T on the tensor cores (mma.sync m16n8k16, bf16 in,
+//    fp32 accumulate; q' is the A operand, the key tile the B operand), which
+//    leaves each lane holding the softmax weights of one head for four tokens
+//    in exactly the B-operand layout of the value product: P never leaves the
+//    registers.  The same tile is then rebuilt with the values and
+//    O'^T[128 x 8 heads] += V^T P accumulates on the tensor cores.  The fp32
 //    operands q' and p are split into bf16 hi + lo parts (two MMAs), keeping
 //    ~16 significant bits, far below the 5e-3 tolerance.
+//  * Online softmax with a lazily raised running max: the accumulators are
+//    rescaled only when a group's max exceeds the running one by more than
+//    2^8 (weights stay <= 2^8, exact in the hi + lo split), so most groups
+//    skip the rescale.
 //  * Split-T merge: warps -> CTA in shared memory, CTA partials (m, l, acc)
 //    -> workspace; the last CTA of the unit to arrive (atomic counter, no
 //    waiting) stages all partials with one cp.async burst, merges them
@@ -35,13 +43,13 @@
 namespace mk {
 
 namespace {
-constexpr int kWarps = 8;
+constexpr int kMaxWarps = 12;                // one CTA per SM, 8 or 12 warps (shared memory decides)
 constexpr int kTG = 16;                      // tokens per packed group (one MMA tile)
 constexpr int kDC = 8;                       // tokens per dense chunk
 constexpr int kRow = D + 8;                  // padded bf16 row: 272 bytes, ldmatrix conflict-free
 constexpr int kTileBytes = kTG * kRow * 2;   // 16-row tile
 constexpr int kDenseStage = 2 * kDC * kRow * 2;  // staged dense chunk: 8 K rows + 8 V rows
-constexpr int kPsBytes = 2 * 8 * kTG * 2;    // P hi/lo as [8 heads][16 tokens]
+constexpr float kLazy = 8.0f;                // log2 headroom before the running max is raised
 constexpr float kScaleLog2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
 __device__ __forceinline__ int always_block(const UnitDesc& ud, int nblk, int i) {
@@ -75,14 +83,21 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// fp32 -> (hi, lo) bf16 pair with hi + lo ~ x to ~16 bits.
-__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(x);
-  hi = __bfloat16_as_ushort(h);
-  lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+// Same with rows 8-15 of A zero: A = (a0 = rows 0-7 k 0-7, a2 = rows 0-7 k 8-15).
+__device__ __forceinline__ void mma_bf16_top(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%6,%5,%6}, {%7,%8}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack2(uint16_t lo16, uint16_t hi16) {
-  return (uint32_t)lo16 | ((uint32_t)hi16 << 16);
+// (x0, x1) -> packed bf16x2 hi parts and lo parts (x ~ hi + lo to ~16 bits).
+__device__ __forceinline__ void split2_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // Rebuild one token's dense row from its packed (values, indices): the row is
@@ -111,21 +126,25 @@ struct Task {
 };
 
 int stage_bytes(const Layout& L) { return (std::max(6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16; }
-size_t per_warp_bytes(const Layout& L, int nst) { return (size_t)nst * stage_bytes(L) + kTileBytes + kPsBytes; }
-size_t smem_for(const Layout& L, int nst) {
-  return (size_t)kWarps * per_warp_bytes(L, nst) + (size_t)kWarps * 8 * 2 * 4 + kRow * 2 + 64;
+// Per warp: the stages, then one tile (keys, then values).
+size_t per_warp_bytes(const Layout& L, int nst) { return (size_t)nst * stage_bytes(L) + kTileBytes; }
+size_t smem_for(const Layout& L, int nst, int nw) {
+  return (size_t)nw * per_warp_bytes(L, nst) + (size_t)nw * 8 * 2 * 4 + kRow * 2 + 64;
 }
 }  // namespace
 
 // Shared-memory plan; fills attn_nst / attn_sb and returns the dynamic shared
 // memory size (0 if nothing fits).
 size_t attn_plan(Layout& L, int /*r_min*/) {
-  for (int nst = 2; nst >= 1; --nst) {
-    const size_t s = smem_for(L, nst);
+  // Double-buffered stages first (they hide the copy latency), then as many
+  // warps as fit.
+  const int plans[4][2] = {{2, 12}, {2, 8}, {1, 12}, {1, 8}};
+  for (const auto& pl : plans) {
+    const size_t s = smem_for(L, pl[0], pl[1]);
     if (s <= 227 * 1024) {
       L.attn_tg = kTG;
-      L.attn_nst = nst;
-      L.attn_nc = 1;
+      L.attn_nst = pl[0];
+      L.attn_nc = pl[1];  // warps per CTA
       L.attn_sb = stage_bytes(L);
       return s;
     }
@@ -133,25 +152,27 @@ size_t attn_plan(Layout& L, int /*r_min*/) {
   return 0;
 }
 
-size_t attn_smem_bytes(const Layout& L, int) { return smem_for(L, L.attn_nst); }
+size_t attn_smem_bytes(const Layout& L, int) { return smem_for(L, L.attn_nst, L.attn_nc); }
 
 // Largest number of CTAs per unit whose partials the merging CTA can stage
 // (next to the merged o' and the un-rotation halves).
 int attn_max_parts(const Layout& L) {
-  const int64_t avail = (int64_t)kWarps * per_warp_bytes(L, L.attn_nst) - (int64_t)3 * L.G * D * 4 - 64;  // o', halves
+  const int64_t avail = (int64_t)L.attn_nc * per_warp_bytes(L, L.attn_nst) -
+                        (int64_t)(1 + L.attn_nc / 4) * L.G * D * 4 - 64;  // o', slices
   return (int)std::max<int64_t>(1, std::min<int64_t>(MK_MAX_SPLITS, avail / ((int64_t)L.G * (D + 2) * 4)));
 }
 
 template <int G, bool DENSE>
-__global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs cs, int P,
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer, CallSeqs cs, int P,
                                                  const int32_t* __restrict__ ids,
                                                  const int32_t* __restrict__ n_sel_in,
                                                  const uint16_t* __restrict__ q_in, const uint16_t* __restrict__ Kd,
                                                  const uint16_t* __restrict__ Vd, int64_t t_stride,
                                                  uint16_t* __restrict__ out) {
   const int NST = L.attn_nst, SB = L.attn_sb;
+  const int kWarps = blockDim.x >> 5, kSlices = blockDim.x >> 7;
   extern __shared__ __align__(16) unsigned char smem[];
-  const size_t pwb = (size_t)NST * SB + kTileBytes + kPsBytes;
+  const size_t pwb = (size_t)NST * SB + kTileBytes;
   unsigned char* warp_area = smem;                                       // [kWarps][pwb]
   float* mlw = reinterpret_cast<float*>(smem + kWarps * pwb);            // [kWarps][8][2]
   uint16_t* zrow = reinterpret_cast<uint16_t*>(mlw + kWarps * 16);      // one zero row (272 B)
@@ -210,7 +231,6 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
   const int32_t* my_ids = DENSE ? nullptr : ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
   unsigned char* my_area = warp_area + (size_t)warp * pwb;
   uint16_t* tile = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB);
-  uint16_t* ps = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB + kTileBytes);
 
   auto make_task = [&](int it, int tg) -> Task {
     Task t{};
@@ -289,8 +309,9 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
   issue(cur, my_area);
   cp_async_commit();
 
-  // q'^T B fragments (k = channel, n = head), hi and lo parts: 8 k-chunks.
-  uint32_t bqh[8][2], bql[8][2];
+  // q' as the A operand (rows = heads g < G, k = channel), hi and lo parts:
+  // per 16-channel chunk a lane holds rows g (a0, a2); rows g + 8 are zero.
+  uint32_t aqh[8][2], aql[8][2];
   {
     const float* qrot = L.qrot + slot * G * D;
     const uint16_t* qin = DENSE ? q_in + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D : nullptr;
@@ -298,10 +319,9 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
     for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint16_t h0 = 0, l0 = 0, h1 = 0, l1 = 0;
+        float x0 = 0.0f, x1 = 0.0f;
         if (g < G && !skip) {
           const int c = kc * 16 + hf * 8 + 2 * tig;
-          float x0, x1;
           if (DENSE) {
             x0 = bf2f(qin[g * D + c]);
             x1 = bf2f(qin[g * D + c + 1]);
@@ -310,26 +330,25 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
             x0 = v.x;
             x1 = v.y;
           }
-          split_bf16(x0, h0, l0);
-          split_bf16(x1, h1, l1);
         }
-        bqh[kc][hf] = pack2(h0, h1);
-        bql[kc][hf] = pack2(l0, l1);
+        split2_bf16(x0, x1, aqh[kc][hf], aql[kc][hf]);
       }
   }
 
-  float o[8][4];  // O'^T fragments: m-tile mt, rows = channels, cols = heads
+  float o[8][4];  // O'^T fragments: m-tile mt, rows = channels, cols = heads 2tig, 2tig+1
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int k = 0; k < 4; ++k) o[mt][k] = 0.0f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2*tig, 2*tig+1
+  float m_run = -INFINITY, l_run = 0.0f;  // head g: running max (log2 units) and sum
+  const bool head_ok = g < G;
 
   const int mi = lane >> 3, ri = lane & 7;
+  const int ktok = ri + (mi >> 1) * 8, kch = (mi & 1) * 8;  // ldmatrix rows for the key B fragments
+  const int vtok = ri + (mi >> 1) * 8, vch = (mi & 1) * 8;  // ldmatrix.trans rows for the value A fragments
   while (cur.kind != 0) {
-    const Task nxt = advance(cur);
     if (NST == 2) {
-      issue(nxt, my_area + (size_t)(st ^ 1) * SB);
+      issue(advance(cur), my_area + (size_t)(st ^ 1) * SB);  // recomputed at the end: fewer live registers
       cp_async_commit();
       asm volatile("cp.async.wait_group 1;\n" ::: "memory");
     } else {
@@ -339,16 +358,16 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
     const unsigned char* buf = my_area + (size_t)st * SB;
     if (cur.kind == 1 || cur.kind == 2) {
       int ntok;
-      const uint16_t* arow_k;   // this lane's ldmatrix row address for the key tile
+      const uint16_t* krow;  // this lane's ldmatrix row of the key tile
       if (cur.kind == 1) {
         ntok = cur.nd;
-        const int row = ri + (mi & 1) * 8;
         const uint16_t* kb = reinterpret_cast<const uint16_t*>(buf);
-        arow_k = (row < ntok ? kb + row * kRow : zrow) + (mi >> 1) * 8;
+        krow = (ktok < ntok ? kb + ktok * kRow : zrow) + kch;
       } else {
         ntok = min(kTG, cur.n_live - cur.tg);
         // Rebuild key positions: zero the tile, scatter by channel index.
         uint4* z = reinterpret_cast<uint4*>(tile);
+#pragma unroll
         for (int i = lane; i < kTileBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
         __syncwarp();
         const int r = cur.r, t = lane & 15;
@@ -356,68 +375,65 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
           scatter_row(tile + t * kRow, reinterpret_cast<const uint16_t*>(buf) + t * r, buf + 2 * kTG * r + t * r, r,
                       lane);
         __syncwarp();
-        arow_k = tile + (ri + (mi & 1) * 8) * kRow + (mi >> 1) * 8;
+        krow = tile + ktok * kRow + kch;
       }
 
-      // Logits S^T[token][head] = sum_c K[token][c] q'[head][c] (hi + lo parts).
-      float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // S[head][token] = sum_c q'[head][c] K[token][c]: tokens 0-7 (s0), 8-15 (s1).
+      float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int kc = 0; kc < 8; ++kc) {
-        uint32_t a[4];
-        ldsm_x4(a, arow_k + kc * 16);
-        mma_bf16(s, a, bqh[kc][0], bqh[kc][1]);
-        mma_bf16(s, a, bql[kc][0], bql[kc][1]);
+        uint32_t b[4];
+        ldsm_x4(b, krow + kc * 16);
+        mma_bf16_top(s0, aqh[kc][0], aqh[kc][1], b[0], b[1]);
+        mma_bf16_top(s0, aql[kc][0], aql[kc][1], b[0], b[1]);
+        mma_bf16_top(s1, aqh[kc][0], aqh[kc][1], b[2], b[3]);
+        mma_bf16_top(s1, aql[kc][0], aql[kc][1], b[2], b[3]);
       }
-      // Online softmax over this item's tokens (g, g+8) for heads 2tig, 2tig+1.
-      const bool v_lo = g < ntok, v_hi = g + 8 < ntok;
-      const float s00 = v_lo ? s[0] * kScaleLog2 : -INFINITY, s01 = v_lo ? s[1] * kScaleLog2 : -INFINITY;
-      const float s10 = v_hi ? s[2] * kScaleLog2 : -INFINITY, s11 = v_hi ? s[3] * kScaleLog2 : -INFINITY;
-      float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
+      // Online softmax for head g over tokens 2tig, 2tig+1, 8+2tig, 9+2tig
+      // (the four lanes of a quad hold the group's 16 tokens).
+      const int t0 = 2 * tig;
+      float v0 = (head_ok && t0 < ntok) ? s0[0] * kScaleLog2 : -INFINITY;
+      float v1 = (head_ok && t0 + 1 < ntok) ? s0[1] * kScaleLog2 : -INFINITY;
+      float v2 = (head_ok && t0 + 8 < ntok) ? s1[0] * kScaleLog2 : -INFINITY;
+      float v3 = (head_ok && t0 + 9 < ntok) ? s1[1] * kScaleLog2 : -INFINITY;
+      float x = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
+      x = fmaxf(x, __shfl_xor_sync(FULL, x, 1));
+      x = fmaxf(x, __shfl_xor_sync(FULL, x, 2));
+      const bool raise = x > m_run + kLazy;  // false for an all-masked group (x = -inf)
+      const float m_new = raise ? x : m_run;
+      const float a = raise ? exp2f(m_run - m_new) : 1.0f;
+      const float p0 = exp2f(v0 - m_new), p1 = exp2f(v1 - m_new);
+      const float p2 = exp2f(v2 - m_new), p3 = exp2f(v3 - m_new);
+      float y = (p0 + p1) + (p2 + p3);
+      y += __shfl_xor_sync(FULL, y, 1);
+      y += __shfl_xor_sync(FULL, y, 2);
+      l_run = l_run * a + y;
+      m_run = m_new;
+      if (__any_sync(FULL, raise)) {
+        // o columns are heads 2tig, 2tig+1: their factors live in quads 2tig, 2tig+1.
+        const float a0 = __shfl_sync(FULL, a, (2 * tig) << 2), a1 = __shfl_sync(FULL, a, (2 * tig + 1) << 2);
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, off));
-        x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, off));
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= a0;
+          o[mt][1] *= a1;
+          o[mt][2] *= a0;
+          o[mt][3] *= a1;
+        }
       }
-      const float mn0 = fmaxf(m0, x0), mn1 = fmaxf(m1, x1);
-      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
-      const float p00 = exp2f(s00 - mn0), p01 = exp2f(s01 - mn1);
-      const float p10 = exp2f(s10 - mn0), p11 = exp2f(s11 - mn1);
-      float y0 = p00 + p10, y1 = p01 + p11;
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        y0 += __shfl_xor_sync(FULL, y0, off);
-        y1 += __shfl_xor_sync(FULL, y1, off);
-      }
-      l0 = l0 * a0 + y0;
-      l1 = l1 * a1 + y1;
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= a0;
-        o[mt][1] *= a1;
-        o[mt][2] *= a0;
-        o[mt][3] *= a1;
-      }
-      // P (hi, lo) to shared memory as [head][token], read back as B fragments.
-      {
-        uint16_t h, lw;
-        const int h0 = 2 * tig, h1 = 2 * tig + 1;
-        split_bf16(p00, h, lw); ps[h0 * kTG + g] = h; ps[128 + h0 * kTG + g] = lw;
-        split_bf16(p01, h, lw); ps[h1 * kTG + g] = h; ps[128 + h1 * kTG + g] = lw;
-        split_bf16(p10, h, lw); ps[h0 * kTG + g + 8] = h; ps[128 + h0 * kTG + g + 8] = lw;
-        split_bf16(p11, h, lw); ps[h1 * kTG + g + 8] = h; ps[128 + h1 * kTG + g + 8] = lw;
-      }
+      // P as the B operand of the value product: k = token, n = head g.
+      uint32_t pbh0, pbl0, pbh1, pbl1;
+      split2_bf16(p0, p1, pbh0, pbl0);
+      split2_bf16(p2, p3, pbh1, pbl1);
+
       // Value tile: dense rows in the stage, or rebuilt in the (now free) tile.
-      const int vrow = ri + (mi >> 1) * 8;  // ldmatrix.trans rows are tokens
-      const uint16_t* vrow_base;
+      const uint16_t* vrow;
       if (cur.kind == 1) {
         const uint16_t* vb = reinterpret_cast<const uint16_t*>(buf) + kDC * kRow;
-        vrow_base = (vrow < ntok ? vb + vrow * kRow : zrow) + (mi & 1) * 8;
-        __syncwarp();
+        vrow = (vtok < ntok ? vb + vtok * kRow : zrow) + vch;
       } else {
         __syncwarp();  // the key tile's ldmatrix reads are done
         uint4* z = reinterpret_cast<uint4*>(tile);
+#pragma unroll
         for (int i = lane; i < kTileBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
         __syncwarp();
         const int r = cur.r, t = lane & 15, gr = kTG * r;
@@ -425,50 +441,45 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
           scatter_row(tile + t * kRow, reinterpret_cast<const uint16_t*>(buf + 3 * gr) + t * r, buf + 5 * gr + t * r,
                       r, lane);
         __syncwarp();
-        vrow_base = tile + vrow * kRow + (mi & 1) * 8;
+        vrow = tile + vtok * kRow + vch;
       }
-      const uint32_t* ps32 = reinterpret_cast<const uint32_t*>(ps);
-      const uint32_t pbh0 = ps32[(g * kTG + 2 * tig) >> 1], pbh1 = ps32[(g * kTG + 2 * tig + 8) >> 1];
-      const uint32_t pbl0 = ps32[(128 + g * kTG + 2 * tig) >> 1], pbl1 = ps32[(128 + g * kTG + 2 * tig + 8) >> 1];
       // O'^T[channel][head] += sum_token V[token][channel] P[token][head].
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        uint32_t a[4];
-        ldsm_x4_t(a, vrow_base + mt * 16);
-        mma_bf16(o[mt], a, pbh0, pbh1);
-        mma_bf16(o[mt], a, pbl0, pbl1);
+        uint32_t av[4];
+        ldsm_x4_t(av, vrow + mt * 16);
+        mma_bf16(o[mt], av, pbh0, pbh1);
+        mma_bf16(o[mt], av, pbl0, pbl1);
       }
     }
     __syncwarp();
+    cur = advance(cur);
     if (NST == 1) {
-      issue(nxt, my_area);
+      issue(cur, my_area);
       cp_async_commit();
     }
-    cur = nxt;
     st ^= (NST - 1);
   }
   cp_async_wait_all();
   __syncwarp();
 
   // ---- warps -> CTA partial ------------------------------------------------
-  if (g == 0) {
-    mlw[(warp * 8 + 2 * tig) * 2] = m0;
-    mlw[(warp * 8 + 2 * tig) * 2 + 1] = l0;
-    mlw[(warp * 8 + 2 * tig + 1) * 2] = m1;
-    mlw[(warp * 8 + 2 * tig + 1) * 2 + 1] = l1;
+  if (tig == 0) {
+    mlw[(warp * 8 + g) * 2] = m_run;
+    mlw[(warp * 8 + g) * 2 + 1] = l_run;
   }
   __syncthreads();
   float* dump = reinterpret_cast<float*>(warp_area);  // [kWarps][G][D] (main loop is over)
   {
-    float e0 = 0.0f, e1 = 0.0f;
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
     float M0 = -INFINITY, M1 = -INFINITY;
     for (int w = 0; w < kWarps; ++w) {
       M0 = fmaxf(M0, mlw[(w * 8 + h0) * 2]);
       M1 = fmaxf(M1, mlw[(w * 8 + h1) * 2]);
     }
-    if (m0 != -INFINITY) e0 = exp2f(m0 - M0);
-    if (m1 != -INFINITY) e1 = exp2f(m1 - M1);
+    const float mw0 = mlw[(warp * 8 + h0) * 2], mw1 = mlw[(warp * 8 + h1) * 2];
+    const float e0 = mw0 != -INFINITY ? exp2f(mw0 - M0) : 0.0f;
+    const float e1 = mw1 != -INFINITY ? exp2f(mw1 - M1) : 0.0f;
     float* dw = dump + (size_t)warp * G * D;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
@@ -521,8 +532,8 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
 
   // ---- the last CTA: merge the P partials, un-rotate, store ----------------
   float* ofull = reinterpret_cast<float*>(warp_area);       // [G][D]
-  float* red = ofull + G * D;                                // [2][G][D]
-  float* sacc = red + 2 * G * D;                             // [P][G][D]
+  float* red = ofull + G * D;                                // [kSlices][G][D]
+  float* sacc = red + kSlices * G * D;                       // [P][G][D]
   float* sml = sacc + (size_t)P * G * D;                     // [P][G][2]
   for (int i = tid; i < P * G * D / 4; i += blockDim.x) cp_async16(sacc + 4 * i, pacc + 4 * i);
   for (int i = tid; i < (P * G * 2 + 3) / 4; i += blockDim.x) cp_async16(sml + 4 * i, pml + 4 * i);
@@ -564,7 +575,7 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
   // out[h][j] = sum_c o'[h][c] R_v[c][j]: R_v staged over the partials (one
   // cp.async burst) when it fits, then thread (j, half of c), halves summed.
   const float* Rv = reinterpret_cast<const float*>(base + L.off_rv);
-  const bool rv_smem = (size_t)(3 * G * D) * 4 + (size_t)D * D * 4 <= (size_t)kWarps * pwb;
+  const bool rv_smem = (size_t)((1 + kSlices) * G * D) * 4 + (size_t)D * D * 4 <= (size_t)kWarps * pwb;
   if (rv_smem) {
     for (int i = tid; i < D * D / 4; i += blockDim.x) cp_async16(sacc + 4 * i, Rv + 4 * i);
     cp_async_commit();
@@ -573,22 +584,28 @@ __global__ void __launch_bounds__(256, 2) k_attn(Layout L, int layer, CallSeqs c
   }
   const float* Rsrc = rv_smem ? sacc : Rv;
   {
-    const int j = tid & (D - 1), half = tid >> 7;
+    // thread (j, slice of c), slices summed
+    const int kC = (D + kSlices - 1) / kSlices;
+    const int j = tid & (D - 1), sl = tid >> 7;
+    const int c0 = sl * kC, c1 = min(D, c0 + kC);
     float acc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-    const float* Rc = Rsrc + (size_t)half * 64 * D + j;
-#pragma unroll 16
-    for (int c = 0; c < 64; ++c) {
-      const float rr = Rc[(size_t)c * D];
+#pragma unroll 4
+    for (int c = c0; c < c1; ++c) {
+      const float rr = Rsrc[(size_t)c * D + j];
 #pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = fmaf(ofull[h * D + half * 64 + c], rr, acc[h]);
+      for (int h = 0; h < G; ++h) acc[h] = fmaf(ofull[h * D + c], rr, acc[h]);
     }
 #pragma unroll
-    for (int h = 0; h < G; ++h) red[(half * G + h) * D + j] = acc[h];
+    for (int h = 0; h < G; ++h) red[(sl * G + h) * D + j] = acc[h];
   }
   __syncthreads();
-  for (int i = tid; i < G * D; i += blockDim.x) orow[i] = f2bf(red[i] + red[G * D + i]);
+  for (int i = tid; i < G * D; i += blockDim.x) {
+    float a = 0.0f;
+    for (int sl = 0; sl < kSlices; ++sl) a += red[sl * G * D + i];
+    orow[i] = f2bf(a);
+  }
 }
 
 namespace {
@@ -603,7 +620,7 @@ cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int
     if (e != cudaSuccess) return e;
     set_bytes = smem;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn<G, DENSE>, 256, smem) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn<G, DENSE>, L.attn_nc * 32, smem) != cudaSuccess) {
       (void)cudaGetLastError();
       n = 1;
     }
@@ -619,7 +636,7 @@ cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int
   P = std::min(P, attn_max_parts(L));
   if (std::getenv("MK_LOG"))
     std::fprintf(stderr, "[mosaickv] attention: %d units x %d CTAs (%d per SM), %zu B smem\n", units, P, occ, smem);
-  return launch_pdl(k_attn<G, DENSE>, dim3(units * P), dim3(256), smem, s, 0, L, layer, cs, P, ids, n_sel, q, K, V,
+  return launch_pdl(k_attn<G, DENSE>, dim3(units * P), dim3(L.attn_nc * 32), smem, s, 0, L, layer, cs, P, ids, n_sel, q, K, V,
                     t_stride, out);
 }
 

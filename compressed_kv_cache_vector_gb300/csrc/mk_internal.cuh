@@ -51,7 +51,7 @@ struct Layout {
   int32_t S, W, B, n_kv, G, max_seqs, nblk_cap, cap_tokens, n_layers, k_max;
   int32_t topk_fixed, retain_permille, r_max;
   int32_t attn_tg;              // attention: tokens per staged page group (32 or 16)
-  int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, accumulator copies, stage bytes
+  int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, warps per CTA, stage bytes
   // workspace
   float* qrot;                  // [max_seqs][n_kv][G][128]
   uint32_t* keys;               // [max_seqs][n_kv][keys_stride]: ordered block-score keys, 0 = not a candidate
