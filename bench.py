@@ -156,7 +156,7 @@ def oracle_sample(wl, steps=None, seconds=15.0):
     from compressed_kv_cache_vector_gb300 import synth
     from oracle import mosaickv_oracle as O
     T0 = wl.seq_lens[0]
-    n_extra = (steps or 64) + 1
+    n_extra = (steps or 4096) + 1
     sd = synth.seed_for(wl.name, 0, 0, 0)
     K = synth.bf16_values(synth.lowrank_outlier(T0 + n_extra, D, wl.decay, sd))
     V = synth.bf16_values(synth.lowrank_outlier(T0 + n_extra, D, wl.decay, sd + 1))
