@@ -13,19 +13,26 @@
 // GB300 structure.
 //  * Work items of one (sequence, kv head): dense chunks of 8 tokens (sinks,
 //    window), then 16-token groups of the selected / always-attended pages.
-//    P CTAs (8 warps, two CTAs per SM) share them; each warp double-buffers
+//    P CTAs (one per SM, 8 or 12 warps) share them; each warp double-buffers
 //    its items into shared memory with cp.async.
-//  * Per group the warp rebuilds positions in one 16 x 128 bf16 tile: it
-//    zero-fills it and scatters the kept key values by their channel indices
-//    (two lanes per token).  The logits are computed transposed,
-//    S[head][token] = q' K^T on the tensor cores (mma.sync m16n8k16, bf16 in,
-//    fp32 accumulate; q' is the A operand, the key tile the B operand), which
-//    leaves each lane holding the softmax weights of one head for four tokens
-//    in exactly the B-operand layout of the value product: P never leaves the
-//    registers.  The same tile is then rebuilt with the values and
-//    O'^T[128 x 8 heads] += V^T P accumulates on the tensor cores.  The fp32
-//    operands q' and p are split into bf16 hi + lo parts (two MMAs), keeping
-//    ~16 significant bits, far below the 5e-3 tolerance.
+//  * Per group the warp rebuilds positions in a 16 x 128 bf16 key tile and a
+//    value tile: it zero-fills them and scatters the kept values by their
+//    channel indices, lanes taking consecutive packed elements (coalesced
+//    loads, few bank conflicts).  Kept channels are stored ascending, so a
+//    token's last index is its highest channel; only the 16-channel chunks up
+//    to the group's highest one are zeroed, loaded and multiplied (in the
+//    rotated basis the kept channels gather in the leading ones).
+//  * The logits are computed as S[head][token] = q' K^T on the tensor cores
+//    (mma.sync m16n8k16, bf16 in, fp32 accumulate; q' is the A operand, the
+//    key tile the B operand), which leaves each lane holding the softmax
+//    weights of one head for four tokens in exactly the B-operand layout of
+//    the value product: P never leaves the registers.  Then
+//    O'^T[128 x 8] += V^T P accumulates on the tensor cores.  The fp32
+//    operands q' and p are split into bf16 hi + lo parts (~16 significant
+//    bits, far below the 5e-3 tolerance): q' hi in A rows 0-7 and lo in rows
+//    8-15, so one MMA per 16 channels yields both partial logits; with G <= 4
+//    heads, P hi fills B columns 0-3 and P lo columns 4-7, so one MMA per 16
+//    channels accumulates both (the columns are added once at the end).
 //  * Online softmax with a lazily raised running max: the accumulators are
 //    rescaled only when a group's max exceeds the running one by more than
 //    2^8 (weights stay <= 2^8, exact in the hi + lo split), so most groups
@@ -83,14 +90,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// Same with rows 8-15 of A zero: A = (a0 = rows 0-7 k 0-7, a2 = rows 0-7 k 8-15).
-__device__ __forceinline__ void mma_bf16_top(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%6,%5,%6}, {%7,%8}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
-}
 // (x0, x1) -> packed bf16x2 hi parts and lo parts (x ~ hi + lo to ~16 bits).
 __device__ __forceinline__ void split2_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -100,21 +99,20 @@ __device__ __forceinline__ void split2_bf16(float x0, float x1, uint32_t& hi, ui
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// Rebuild one token's dense row from its packed (values, indices): the row is
-// zero already.  Lanes t and t + 16 share token t and split its elements.
-__device__ __forceinline__ void scatter_row(uint16_t* row, const uint16_t* val, const uint8_t* idx, int r,
-                                            int lane) {
-  const int h2 = (r >> 1) & ~1;
-  const int j0 = lane < 16 ? 0 : h2, j1 = lane < 16 ? h2 : r;
-  if ((r & 1) == 0) {
-    for (int jj = j0; jj < j1; jj += 2) {
-      const uint32_t ip = *reinterpret_cast<const uint16_t*>(idx + jj);
-      const uint32_t vp = *reinterpret_cast<const uint32_t*>(val + jj);
-      row[ip & 0xff] = (uint16_t)(vp & 0xffff);
-      row[ip >> 8] = (uint16_t)(vp >> 16);
-    }
-  } else {
-    for (int jj = j0; jj < j1; ++jj) row[idx[jj]] = val[jj];
+// Rebuild a group's dense rows from its packed (values, indices): the rows
+// are zero already.  Element e = t * r + j (token t, rank j) is the e-th
+// entry of both packed arrays; lane l takes the pairs (e, e + 1) with
+// e = 2 l + 64 i, so each load of the warp reads one contiguous 128-byte
+// (values) or 64-byte (indices) run.  t = floor(e / r) = umulhi(2e, rm) with
+// rm = ceil(2^31 / r) (exact for e < 2^20).
+__device__ __forceinline__ void scatter_flat(uint16_t* tile, const uint16_t* val, const uint8_t* idx, int n_el,
+                                             uint32_t rm, int lane) {
+  for (int e = 2 * lane; e < n_el; e += 64) {
+    const uint32_t vp = *reinterpret_cast<const uint32_t*>(val + e);
+    const uint32_t ip = *reinterpret_cast<const uint16_t*>(idx + e);
+    const int t0 = (int)__umulhi(2u * (uint32_t)e, rm), t1 = (int)__umulhi(2u * (uint32_t)e + 2u, rm);
+    tile[t0 * kRow + (ip & 0xff)] = (uint16_t)(vp & 0xffff);
+    if (e + 1 < n_el) tile[t1 * kRow + (ip >> 8)] = (uint16_t)(vp >> 16);
   }
 }
 
@@ -126,8 +124,8 @@ struct Task {
 };
 
 int stage_bytes(const Layout& L) { return (std::max(6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16; }
-// Per warp: the stages, then one tile (keys, then values).
-size_t per_warp_bytes(const Layout& L, int nst) { return (size_t)nst * stage_bytes(L) + kTileBytes; }
+// Per warp: the stages, then the key tile and the value tile.
+size_t per_warp_bytes(const Layout& L, int nst) { return (size_t)nst * stage_bytes(L) + 2 * kTileBytes; }
 size_t smem_for(const Layout& L, int nst, int nw) {
   return (size_t)nw * per_warp_bytes(L, nst) + (size_t)nw * 8 * 2 * 4 + kRow * 2 + 64;
 }
@@ -172,7 +170,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   const int NST = L.attn_nst, SB = L.attn_sb;
   const int kWarps = blockDim.x >> 5, kSlices = blockDim.x >> 7;
   extern __shared__ __align__(16) unsigned char smem[];
-  const size_t pwb = (size_t)NST * SB + kTileBytes;
+  const size_t pwb = (size_t)NST * SB + 2 * kTileBytes;
   unsigned char* warp_area = smem;                                       // [kWarps][pwb]
   float* mlw = reinterpret_cast<float*>(smem + kWarps * pwb);            // [kWarps][8][2]
   uint16_t* zrow = reinterpret_cast<uint16_t*>(mlw + kWarps * 16);      // one zero row (272 B)
@@ -230,7 +228,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   const char* base = DENSE ? nullptr : unit_base(L, u);
   const int32_t* my_ids = DENSE ? nullptr : ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
   unsigned char* my_area = warp_area + (size_t)warp * pwb;
-  uint16_t* tile = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB);
+  uint16_t* tk = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB);  // dense key tile
+  uint16_t* tv = tk + kTG * kRow;                                           // dense value tile
 
   auto make_task = [&](int it, int tg) -> Task {
     Task t{};
@@ -257,7 +256,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     return t;
   };
   auto advance = [&](const Task& t) -> Task {
-    if (t.kind == 2 && t.tg + kTG < t.n_live) return make_task(t.item, t.tg + kTG);
+    if (t.kind == 2 && t.tg + kTG < t.n_live) {
+      Task n = t;
+      n.tg += kTG;
+      return n;
+    }
     return make_task(t.item + kWarps, 0);
   };
   auto dense_rows = [&](int j, const uint16_t*& kr, const uint16_t*& vr) {
@@ -289,16 +292,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
       // This group's rows of the page's four sub-arrays (B is a multiple of
       // 16, so a whole group stays inside the page; sizes and offsets are
       // multiples of 16 bytes).
-      const int Br = B * t.r, gr = kTG * t.r;
+      // The stage holds them back to back: [K val 2gr][K idx gr][V val 2gr][V idx gr]
+      // bytes, chunk c of the stage comes from page + off_q + 16 c.
+      const int Br = B * t.r, gr = kTG * t.r, tr = t.tg * t.r;
       const char* page = base + L.off_pages + (int64_t)t.b * L.page_stride;
-      const char* src[4] = {page + 2 * t.tg * t.r, page + 2 * Br + t.tg * t.r, page + 3 * Br + 2 * t.tg * t.r,
-                            page + 5 * Br + t.tg * t.r};
-      const int len[4] = {2 * gr, gr, 2 * gr, gr};
-      int off = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        for (int i = lane * 16; i < len[q]; i += 32 * 16) cp_async16(dst + off + i, src[q] + i);
-        off += len[q];
+      const int c1 = gr >> 3, c2 = c1 + (gr >> 4), c3 = c2 + (gr >> 3), c4 = c3 + (gr >> 4);
+      const int o0 = 2 * tr, o1 = 2 * Br + tr - 16 * c1, o2 = 3 * Br + 2 * tr - 16 * c2, o3 = 5 * Br + tr - 16 * c3;
+      for (int c = lane; c < c4; c += 32) {
+        const int o = c < c1 ? o0 : c < c2 ? o1 : c < c3 ? o2 : o3;
+        cp_async16(dst + 16 * c, page + o + 16 * c);
       }
     }
   };
@@ -309,9 +311,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   issue(cur, my_area);
   cp_async_commit();
 
-  // q' as the A operand (rows = heads g < G, k = channel), hi and lo parts:
-  // per 16-channel chunk a lane holds rows g (a0, a2); rows g + 8 are zero.
-  uint32_t aqh[8][2], aql[8][2];
+  // q' as the A operand of the logits (k = channel): row g holds the bf16 hi
+  // part and row g + 8 the lo part of head hq = g % G (rows repeat when
+  // G < 8), so one MMA gives both partial sums in the same lane.
+  const int hq = g % G;
+  uint32_t aq[8][4];
   {
     const float* qrot = L.qrot + slot * G * D;
     const uint16_t* qin = DENSE ? q_in + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D : nullptr;
@@ -320,28 +324,30 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float x0 = 0.0f, x1 = 0.0f;
-        if (g < G && !skip) {
+        if (!skip) {
           const int c = kc * 16 + hf * 8 + 2 * tig;
           if (DENSE) {
-            x0 = bf2f(qin[g * D + c]);
-            x1 = bf2f(qin[g * D + c + 1]);
+            x0 = bf2f(qin[hq * D + c]);
+            x1 = bf2f(qin[hq * D + c + 1]);
           } else {
-            const float2 v = *reinterpret_cast<const float2*>(qrot + g * D + c);
+            const float2 v = *reinterpret_cast<const float2*>(qrot + hq * D + c);
             x0 = v.x;
             x1 = v.y;
           }
         }
-        split2_bf16(x0, x1, aqh[kc][hf], aql[kc][hf]);
+        split2_bf16(x0, x1, aq[kc][2 * hf], aq[kc][2 * hf + 1]);
       }
   }
 
-  float o[8][4];  // O'^T fragments: m-tile mt, rows = channels, cols = heads 2tig, 2tig+1
+  // O'^T fragments, m-tile mt: rows = channels mt*16 + g (+8), columns 2tig,
+  // 2tig+1.  With G <= 4, column n holds the hi part (n < 4) or the lo part
+  // (n >= 4) of head n % G; with G = 8, column n is head n.
+  float o[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int k = 0; k < 4; ++k) o[mt][k] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f;  // head g: running max (log2 units) and sum
-  const bool head_ok = g < G;
+  float m_run = -INFINITY, l_run = 0.0f;  // head hq: running max (log2 units) and sum
 
   const int mi = lane >> 3, ri = lane & 7;
   const int ktok = ri + (mi >> 1) * 8, kch = (mi & 1) * 8;  // ldmatrix rows for the key B fragments
@@ -357,45 +363,69 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     __syncwarp();
     const unsigned char* buf = my_area + (size_t)st * SB;
     if (cur.kind == 1 || cur.kind == 2) {
-      int ntok;
-      const uint16_t* krow;  // this lane's ldmatrix row of the key tile
+      int ntok, nck_k = 8, nck_v = 8;  // 16-channel chunks that can hold a nonzero
+      const uint16_t *krow, *vrow;      // this lane's ldmatrix rows
       if (cur.kind == 1) {
         ntok = cur.nd;
         const uint16_t* kb = reinterpret_cast<const uint16_t*>(buf);
+        const uint16_t* vb = kb + kDC * kRow;
         krow = (ktok < ntok ? kb + ktok * kRow : zrow) + kch;
+        vrow = (vtok < ntok ? vb + vtok * kRow : zrow) + vch;
       } else {
         ntok = min(kTG, cur.n_live - cur.tg);
-        // Rebuild key positions: zero the tile, scatter by channel index.
-        uint4* z = reinterpret_cast<uint4*>(tile);
+        const int r = cur.r, gr = kTG * r;
+        const uint16_t* kval = reinterpret_cast<const uint16_t*>(buf);
+        const uint8_t* kidx = buf + 2 * gr;
+        const uint16_t* vval = reinterpret_cast<const uint16_t*>(buf + 3 * gr);
+        const uint8_t* vidx = buf + 5 * gr;
+        // Kept channels are stored in ascending order, so a token's last
+        // index is its highest channel: the group's rows are zero from the
+        // chunk after the largest one on.
+        const int tt = lane & 15;
+        uint32_t hk = 0, hv = 0;
+        if (tt < ntok) {
+          hk = kidx[tt * r + r - 1];
+          hv = vidx[tt * r + r - 1];
+        }
+        nck_k = (int)(__reduce_max_sync(FULL, hk) >> 4) + 1;
+        nck_v = (int)(__reduce_max_sync(FULL, hv) >> 4) + 1;
+        // Zero those chunks of all 16 rows (lane: row tt, 16-byte half lane >> 4).
+        uint4* zk = reinterpret_cast<uint4*>(tk + tt * kRow) + (lane >> 4);
+        uint4* zv = reinterpret_cast<uint4*>(tv + tt * kRow) + (lane >> 4);
 #pragma unroll
-        for (int i = lane; i < kTileBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 8; ++c) {
+          if (c < nck_k) zk[2 * c] = make_uint4(0, 0, 0, 0);
+          if (c < nck_v) zv[2 * c] = make_uint4(0, 0, 0, 0);
+        }
         __syncwarp();
-        const int r = cur.r, t = lane & 15;
-        if (t < ntok)
-          scatter_row(tile + t * kRow, reinterpret_cast<const uint16_t*>(buf) + t * r, buf + 2 * kTG * r + t * r, r,
-                      lane);
+        const int n_el = ntok * r;
+        const uint32_t rm = (0x80000000u + (uint32_t)r - 1u) / (uint32_t)r;
+        scatter_flat(tk, kval, kidx, n_el, rm, lane);
+        scatter_flat(tv, vval, vidx, n_el, rm, lane);
         __syncwarp();
-        krow = tile + ktok * kRow + kch;
+        krow = tk + ktok * kRow + kch;
+        vrow = tv + vtok * kRow + vch;
       }
 
-      // S[head][token] = sum_c q'[head][c] K[token][c]: tokens 0-7 (s0), 8-15 (s1).
+      // S[head][token] = sum_c q'[head][c] K[token][c] over the nonzero
+      // chunks: tokens 0-7 (s0), 8-15 (s1); c0/c1 hi part, c2/c3 lo part.
       float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int kc = 0; kc < 8; ++kc) {
-        uint32_t b[4];
-        ldsm_x4(b, krow + kc * 16);
-        mma_bf16_top(s0, aqh[kc][0], aqh[kc][1], b[0], b[1]);
-        mma_bf16_top(s0, aql[kc][0], aql[kc][1], b[0], b[1]);
-        mma_bf16_top(s1, aqh[kc][0], aqh[kc][1], b[2], b[3]);
-        mma_bf16_top(s1, aql[kc][0], aql[kc][1], b[2], b[3]);
+        if (kc < nck_k) {
+          uint32_t b[4];
+          ldsm_x4(b, krow + kc * 16);
+          mma_bf16(s0, aq[kc], b[0], b[1]);
+          mma_bf16(s1, aq[kc], b[2], b[3]);
+        }
       }
-      // Online softmax for head g over tokens 2tig, 2tig+1, 8+2tig, 9+2tig
+      // Online softmax for head hq over tokens 2tig, 2tig+1, 8+2tig, 9+2tig
       // (the four lanes of a quad hold the group's 16 tokens).
       const int t0 = 2 * tig;
-      float v0 = (head_ok && t0 < ntok) ? s0[0] * kScaleLog2 : -INFINITY;
-      float v1 = (head_ok && t0 + 1 < ntok) ? s0[1] * kScaleLog2 : -INFINITY;
-      float v2 = (head_ok && t0 + 8 < ntok) ? s1[0] * kScaleLog2 : -INFINITY;
-      float v3 = (head_ok && t0 + 9 < ntok) ? s1[1] * kScaleLog2 : -INFINITY;
+      const float v0 = t0 < ntok ? (s0[0] + s0[2]) * kScaleLog2 : -INFINITY;
+      const float v1 = t0 + 1 < ntok ? (s0[1] + s0[3]) * kScaleLog2 : -INFINITY;
+      const float v2 = t0 + 8 < ntok ? (s1[0] + s1[2]) * kScaleLog2 : -INFINITY;
+      const float v3 = t0 + 9 < ntok ? (s1[1] + s1[3]) * kScaleLog2 : -INFINITY;
       float x = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
       x = fmaxf(x, __shfl_xor_sync(FULL, x, 1));
       x = fmaxf(x, __shfl_xor_sync(FULL, x, 2));
@@ -410,7 +440,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
       l_run = l_run * a + y;
       m_run = m_new;
       if (__any_sync(FULL, raise)) {
-        // o columns are heads 2tig, 2tig+1: their factors live in quads 2tig, 2tig+1.
+        // Column n's head is n % G, whose factor quad n (g = n) holds.
         const float a0 = __shfl_sync(FULL, a, (2 * tig) << 2), a1 = __shfl_sync(FULL, a, (2 * tig + 1) << 2);
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
@@ -420,36 +450,32 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
           o[mt][3] *= a1;
         }
       }
-      // P as the B operand of the value product: k = token, n = head g.
-      uint32_t pbh0, pbl0, pbh1, pbl1;
-      split2_bf16(p0, p1, pbh0, pbl0);
-      split2_bf16(p2, p3, pbh1, pbl1);
-
-      // Value tile: dense rows in the stage, or rebuilt in the (now free) tile.
-      const uint16_t* vrow;
-      if (cur.kind == 1) {
-        const uint16_t* vb = reinterpret_cast<const uint16_t*>(buf) + kDC * kRow;
-        vrow = (vtok < ntok ? vb + vtok * kRow : zrow) + vch;
+      // P as the B operand of the value product: k = token, n = column g.
+      uint32_t ph0, pl0, ph1, pl1;
+      split2_bf16(p0, p1, ph0, pl0);
+      split2_bf16(p2, p3, ph1, pl1);
+      // O'^T[channel][column] += sum_token V[token][channel] P[token][column].
+      if (G <= 4) {
+        const bool lo = g >= 4;
+        const uint32_t pb0 = lo ? pl0 : ph0, pb1 = lo ? pl1 : ph1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          if (mt < nck_v) {
+            uint32_t av[4];
+            ldsm_x4_t(av, vrow + mt * 16);
+            mma_bf16(o[mt], av, pb0, pb1);
+          }
+        }
       } else {
-        __syncwarp();  // the key tile's ldmatrix reads are done
-        uint4* z = reinterpret_cast<uint4*>(tile);
 #pragma unroll
-        for (int i = lane; i < kTileBytes / 16; i += 32) z[i] = make_uint4(0, 0, 0, 0);
-        __syncwarp();
-        const int r = cur.r, t = lane & 15, gr = kTG * r;
-        if (t < ntok)
-          scatter_row(tile + t * kRow, reinterpret_cast<const uint16_t*>(buf + 3 * gr) + t * r, buf + 5 * gr + t * r,
-                      r, lane);
-        __syncwarp();
-        vrow = tile + vtok * kRow + vch;
-      }
-      // O'^T[channel][head] += sum_token V[token][channel] P[token][head].
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        uint32_t av[4];
-        ldsm_x4_t(av, vrow + mt * 16);
-        mma_bf16(o[mt], av, pbh0, pbh1);
-        mma_bf16(o[mt], av, pbl0, pbl1);
+        for (int mt = 0; mt < 8; ++mt) {
+          if (mt < nck_v) {
+            uint32_t av[4];
+            ldsm_x4_t(av, vrow + mt * 16);
+            mma_bf16(o[mt], av, ph0, ph1);
+            mma_bf16(o[mt], av, pl0, pl1);
+          }
+        }
       }
     }
     __syncwarp();
@@ -462,6 +488,16 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   }
   cp_async_wait_all();
   __syncwarp();
+  if (G <= 4) {
+    // Fold the lo columns (lanes tig + 2) into the hi ones.
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[mt][k] += __shfl_xor_sync(FULL, o[mt][k], 2);
+  }
+  // This lane's columns now hold heads 2tig, 2tig+1 (valid below G, and for
+  // G <= 4 only in lanes tig < 2).
+  const bool col_ok0 = 2 * tig < G && (G == 8 || tig < 2), col_ok1 = 2 * tig + 1 < G && (G == 8 || tig < 2);
 
   // ---- warps -> CTA partial ------------------------------------------------
   if (tig == 0) {
@@ -484,11 +520,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       const int c = mt * 16 + g;
-      if (h0 < G) {
+      if (col_ok0) {
         dw[h0 * D + c] = o[mt][0] * e0;
         dw[h0 * D + c + 8] = o[mt][2] * e0;
       }
-      if (h1 < G) {
+      if (col_ok1) {
         dw[h1 * D + c] = o[mt][1] * e1;
         dw[h1 * D + c + 8] = o[mt][3] * e1;
       }
