@@ -56,6 +56,7 @@ constexpr int kDC = 8;                       // tokens per dense chunk
 constexpr int kRow = D + 8;                  // padded bf16 row: 272 bytes, ldmatrix conflict-free
 constexpr int kTileBytes = kTG * kRow * 2;   // 16-row tile
 constexpr int kDenseStage = 2 * kDC * kRow * 2;  // staged dense chunk: 8 K rows + 8 V rows
+constexpr int kIdsCap = 256;                 // block ids a CTA caches in shared memory
 constexpr float kLazy = 8.0f;                // log2 headroom before the running max is raised
 constexpr float kScaleLog2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
@@ -99,20 +100,29 @@ __device__ __forceinline__ void split2_bf16(float x0, float x1, uint32_t& hi, ui
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// Rebuild a group's dense rows from its packed (values, indices): the rows
-// are zero already.  Element e = t * r + j (token t, rank j) is the e-th
-// entry of both packed arrays; lane l takes the pairs (e, e + 1) with
-// e = 2 l + 64 i, so each load of the warp reads one contiguous 128-byte
+// Rebuild a group's dense key and value rows from their packed (values,
+// indices): the rows are zero already.  Element e = t * r + j (token t, rank
+// j) is the e-th entry of the packed arrays; lane l takes the pairs (e, e + 1)
+// with e = 2 l + 64 i, so each load of the warp reads one contiguous 128-byte
 // (values) or 64-byte (indices) run.  t = floor(e / r) = umulhi(2e, rm) with
-// rm = ceil(2^31 / r) (exact for e < 2^20).
-__device__ __forceinline__ void scatter_flat(uint16_t* tile, const uint16_t* val, const uint8_t* idx, int n_el,
-                                             uint32_t rm, int lane) {
+// rm = ceil(2^31 / r) (exact for e < 2^20).  Keys and values share e, so their
+// loads and stores interleave.
+__device__ __forceinline__ void scatter_kv(uint16_t* tk, uint16_t* tv, const uint16_t* kval, const uint8_t* kidx,
+                                           const uint16_t* vval, const uint8_t* vidx, int n_el, uint32_t rm,
+                                           int lane) {
+#pragma unroll 2
   for (int e = 2 * lane; e < n_el; e += 64) {
-    const uint32_t vp = *reinterpret_cast<const uint32_t*>(val + e);
-    const uint32_t ip = *reinterpret_cast<const uint16_t*>(idx + e);
-    const int t0 = (int)__umulhi(2u * (uint32_t)e, rm), t1 = (int)__umulhi(2u * (uint32_t)e + 2u, rm);
-    tile[t0 * kRow + (ip & 0xff)] = (uint16_t)(vp & 0xffff);
-    if (e + 1 < n_el) tile[t1 * kRow + (ip >> 8)] = (uint16_t)(vp >> 16);
+    const uint32_t kp = *reinterpret_cast<const uint32_t*>(kval + e);
+    const uint32_t vp = *reinterpret_cast<const uint32_t*>(vval + e);
+    const uint32_t ki = *reinterpret_cast<const uint16_t*>(kidx + e);
+    const uint32_t vi = *reinterpret_cast<const uint16_t*>(vidx + e);
+    const int r0 = (int)__umulhi(2u * (uint32_t)e, rm) * kRow, r1 = (int)__umulhi(2u * (uint32_t)e + 2u, rm) * kRow;
+    tk[r0 + (ki & 0xff)] = (uint16_t)(kp & 0xffff);
+    tv[r0 + (vi & 0xff)] = (uint16_t)(vp & 0xffff);
+    if (e + 1 < n_el) {
+      tk[r1 + (ki >> 8)] = (uint16_t)(kp >> 16);
+      tv[r1 + (vi >> 8)] = (uint16_t)(vp >> 16);
+    }
   }
 }
 
@@ -139,7 +149,7 @@ size_t attn_plan(Layout& L, int /*r_min*/) {
   const int plans[4][2] = {{2, 12}, {2, 8}, {1, 12}, {1, 8}};
   for (const auto& pl : plans) {
     const size_t s = smem_for(L, pl[0], pl[1]);
-    if (s <= 227 * 1024) {
+    if (s <= 225 * 1024) {  // leaves room for the static shared memory
       L.attn_tg = kTG;
       L.attn_nst = pl[0];
       L.attn_nc = pl[1];  // warps per CTA
@@ -153,10 +163,10 @@ size_t attn_plan(Layout& L, int /*r_min*/) {
 size_t attn_smem_bytes(const Layout& L, int) { return smem_for(L, L.attn_nst, L.attn_nc); }
 
 // Largest number of CTAs per unit whose partials the merging CTA can stage
-// (next to the merged o' and the un-rotation halves).
+// (next to the merged o', the un-rotation slices and R_v).
 int attn_max_parts(const Layout& L) {
   const int64_t avail = (int64_t)L.attn_nc * per_warp_bytes(L, L.attn_nst) -
-                        (int64_t)(1 + L.attn_nc / 4) * L.G * D * 4 - 64;  // o', slices
+                        (int64_t)(1 + L.attn_nc / 4) * L.G * D * 4 - (int64_t)D * D * 4 - 64;  // o', slices, R_v
   return (int)std::max<int64_t>(1, std::min<int64_t>(MK_MAX_SPLITS, avail / ((int64_t)L.G * (D + 2) * 4)));
 }
 
@@ -177,6 +187,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   __shared__ UnitDesc ud;
   __shared__ int s_abort, s_ns, s_last;
   __shared__ float s_m[8], s_l[8];
+  __shared__ int32_t s_ids[kIdsCap];  // this CTA's selected block ids (its j-th item: ids[part + j P])
 
   const int unit_call = blockIdx.x / P;
   const int part = blockIdx.x - unit_call * P;
@@ -186,6 +197,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   const int g = lane >> 2, tig = lane & 3;
   const int64_t u = DENSE ? 0 : unit_index(L, layer, seq, kvh);
   const int64_t slot = (int64_t)seq * L.n_kv + kvh;
+  const int32_t* my_ids = DENSE ? nullptr : ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
 
   if (!DENSE && part == 0) {  // R_v is static: warm L2 for the final un-rotation
     const char* rv = unit_base(L, u) + L.off_rv;
@@ -194,10 +206,34 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   for (int i = tid; i < kRow / 8; i += blockDim.x) reinterpret_cast<uint4*>(zrow)[i] = make_uint4(0, 0, 0, 0);
   pdl_wait();
   pdl_trigger();
+  // One round of independent loads (L2 path: the previous kernel wrote them):
+  // state, selection count, this CTA's block ids, q'.
   if (tid == 0) {
     s_abort = has_error(L);
     if (!DENSE) ud = L.desc[u];
-    s_ns = DENSE ? 0 : n_sel_in[(int64_t)ci * L.n_kv + kvh];
+    s_ns = DENSE ? 0 : __ldcg(n_sel_in + (int64_t)ci * L.n_kv + kvh);
+  }
+  if (!DENSE)
+    for (int j = tid; j < kIdsCap && part + j * P < L.k_max; j += blockDim.x) s_ids[j] = __ldcg(my_ids + part + j * P);
+  // q' as the A operand of the logits (k = channel): row g holds the bf16 hi
+  // part and row g + 8 the lo part of head hq = g % G (rows repeat when
+  // G < 8), so one MMA gives both partial sums in the same lane.
+  const int hq = g % G;
+  float2 qx[8][2];
+  {
+    const float* qrot = L.qrot + slot * G * D;
+    const uint16_t* qin = DENSE ? q_in + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D : nullptr;
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c = kc * 16 + hf * 8 + 2 * tig;
+        if (DENSE) {
+          qx[kc][hf] = make_float2(bf2f(qin[hq * D + c]), bf2f(qin[hq * D + c + 1]));
+        } else {
+          qx[kc][hf] = __ldcg(reinterpret_cast<const float2*>(qrot + hq * D + c));
+        }
+      }
   }
   __syncthreads();
   bool skip = s_abort != 0;
@@ -220,29 +256,38 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
       ns = 0;
     }
   }
+  uint32_t aq[8][4];
+#pragma unroll
+  for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const float2 x = skip ? make_float2(0.0f, 0.0f) : qx[kc][hf];
+      split2_bf16(x.x, x.y, aq[kc][2 * hf], aq[kc][2 * hf + 1]);
+    }
+  // Items of the unit: the selected pages, the always-attended pages, then
+  // the dense chunks.  CTA `part` takes items part, part + P, ...; its warps
+  // take its j-th items round robin (j = warp, warp + kWarps, ...).
   const int n_dch = (n_dense + kDC - 1) / kDC;
-  const int n_items = skip ? 0 : n_dch + ns + n_always;
-  const int per = (n_items + P - 1) / P;
-  const int i0 = part * per, i1 = min(n_items, i0 + per);
+  const int n_items = skip ? 0 : ns + n_always + n_dch;
+  const int n_mine = n_items > part ? (n_items - part + P - 1) / P : 0;
 
   const char* base = DENSE ? nullptr : unit_base(L, u);
-  const int32_t* my_ids = DENSE ? nullptr : ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
   unsigned char* my_area = warp_area + (size_t)warp * pwb;
   uint16_t* tk = reinterpret_cast<uint16_t*>(my_area + (size_t)NST * SB);  // dense key tile
   uint16_t* tv = tk + kTG * kRow;                                           // dense value tile
 
-  auto make_task = [&](int it, int tg) -> Task {
+  auto make_task = [&](int j, int tg) -> Task {
     Task t{};
-    if (it >= i1) return t;
-    t.item = it;
-    if (it < n_dch) {
+    if (j >= n_mine) return t;
+    t.item = j;
+    const int it = part + j * P;
+    if (it >= ns + n_always) {
       t.kind = 1;
-      t.j0 = it * kDC;
+      t.j0 = (it - ns - n_always) * kDC;
       t.nd = min(kDC, n_dense - t.j0);
       return t;
     }
-    const int pi = it - n_dch;
-    const int b = pi < ns ? __ldg(my_ids + pi) : always_block(ud, nblk, pi - ns);
+    const int b = it < ns ? (j < kIdsCap ? s_ids[j] : __ldcg(my_ids + it)) : always_block(ud, nblk, it - ns);
     if (b < 0 || b >= nblk) {
       if (lane == 0) set_error(L, ERR_BAD_BLOCK, (int32_t)u, b);
       t.kind = 3;
@@ -291,9 +336,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     } else if (t.kind == 2) {
       // This group's rows of the page's four sub-arrays (B is a multiple of
       // 16, so a whole group stays inside the page; sizes and offsets are
-      // multiples of 16 bytes).
-      // The stage holds them back to back: [K val 2gr][K idx gr][V val 2gr][V idx gr]
-      // bytes, chunk c of the stage comes from page + off_q + 16 c.
+      // multiples of 16 bytes).  The stage holds them back to back,
+      // [K val 2gr][K idx gr][V val 2gr][V idx gr] bytes: chunk c of the
+      // stage comes from page + o_q + 16 c.
       const int Br = B * t.r, gr = kTG * t.r, tr = t.tg * t.r;
       const char* page = base + L.off_pages + (int64_t)t.b * L.page_stride;
       const int c1 = gr >> 3, c2 = c1 + (gr >> 4), c3 = c2 + (gr >> 3), c4 = c3 + (gr >> 4);
@@ -305,39 +350,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     }
   };
 
-  // Start the first item's copies before reading q'.
-  Task cur = make_task(i0 + warp, 0);
+  Task cur = make_task(warp, 0);
   int st = 0;
   issue(cur, my_area);
   cp_async_commit();
-
-  // q' as the A operand of the logits (k = channel): row g holds the bf16 hi
-  // part and row g + 8 the lo part of head hq = g % G (rows repeat when
-  // G < 8), so one MMA gives both partial sums in the same lane.
-  const int hq = g % G;
-  uint32_t aq[8][4];
-  {
-    const float* qrot = L.qrot + slot * G * D;
-    const uint16_t* qin = DENSE ? q_in + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D : nullptr;
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float x0 = 0.0f, x1 = 0.0f;
-        if (!skip) {
-          const int c = kc * 16 + hf * 8 + 2 * tig;
-          if (DENSE) {
-            x0 = bf2f(qin[hq * D + c]);
-            x1 = bf2f(qin[hq * D + c + 1]);
-          } else {
-            const float2 v = *reinterpret_cast<const float2*>(qrot + hq * D + c);
-            x0 = v.x;
-            x1 = v.y;
-          }
-        }
-        split2_bf16(x0, x1, aq[kc][2 * hf], aq[kc][2 * hf + 1]);
-      }
-  }
 
   // O'^T fragments, m-tile mt: rows = channels mt*16 + g (+8), columns 2tig,
   // 2tig+1.  With G <= 4, column n holds the hi part (n < 4) or the lo part
@@ -400,8 +416,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
         __syncwarp();
         const int n_el = ntok * r;
         const uint32_t rm = (0x80000000u + (uint32_t)r - 1u) / (uint32_t)r;
-        scatter_flat(tk, kval, kidx, n_el, rm, lane);
-        scatter_flat(tv, vval, vidx, n_el, rm, lane);
+        scatter_kv(tk, tv, kval, kidx, vval, vidx, n_el, rm, lane);
         __syncwarp();
         krow = tk + ktok * kRow + kch;
         vrow = tv + vtok * kRow + vch;
@@ -567,10 +582,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   __threadfence();
 
   // ---- the last CTA: merge the P partials, un-rotate, store ----------------
-  float* ofull = reinterpret_cast<float*>(warp_area);       // [G][D]
-  float* red = ofull + G * D;                                // [kSlices][G][D]
-  float* sacc = red + kSlices * G * D;                       // [P][G][D]
-  float* sml = sacc + (size_t)P * G * D;                     // [P][G][2]
+  // Shared memory: o' [G][D] | slice sums [kSlices][G][D] | R_v [D][D] |
+  // partials [P][G][D] | (m, l) [P][G][2]; R_v and the partials arrive in one
+  // cp.async burst (R_v sits in L2: part 0 prefetched it).
+  float* ofull = reinterpret_cast<float*>(warp_area);
+  float* red = ofull + G * D;
+  float* rvs = red + kSlices * G * D;
+  float* sacc = rvs + (DENSE ? 0 : D * D);
+  float* sml = sacc + (size_t)P * G * D;
+  if (!DENSE) {
+    const float* Rv = reinterpret_cast<const float*>(base + L.off_rv);
+    for (int i = tid; i < D * D / 4; i += blockDim.x) cp_async16(rvs + 4 * i, Rv + 4 * i);
+  }
   for (int i = tid; i < P * G * D / 4; i += blockDim.x) cp_async16(sacc + 4 * i, pacc + 4 * i);
   for (int i = tid; i < (P * G * 2 + 3) / 4; i += blockDim.x) cp_async16(sml + 4 * i, pml + 4 * i);
   cp_async_commit();
@@ -608,19 +631,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     for (int i = tid; i < G * D; i += blockDim.x) orow[i] = f2bf(ofull[i]);
     return;
   }
-  // out[h][j] = sum_c o'[h][c] R_v[c][j]: R_v staged over the partials (one
-  // cp.async burst) when it fits, then thread (j, half of c), halves summed.
-  const float* Rv = reinterpret_cast<const float*>(base + L.off_rv);
-  const bool rv_smem = (size_t)((1 + kSlices) * G * D) * 4 + (size_t)D * D * 4 <= (size_t)kWarps * pwb;
-  if (rv_smem) {
-    for (int i = tid; i < D * D / 4; i += blockDim.x) cp_async16(sacc + 4 * i, Rv + 4 * i);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
-  }
-  const float* Rsrc = rv_smem ? sacc : Rv;
+  // out[h][j] = sum_c o'[h][c] R_v[c][j]: thread (j, slice of c), slices summed.
   {
-    // thread (j, slice of c), slices summed
     const int kC = (D + kSlices - 1) / kSlices;
     const int j = tid & (D - 1), sl = tid >> 7;
     const int c0 = sl * kC, c1 = min(D, c0 + kC);
@@ -629,7 +641,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     for (int h = 0; h < G; ++h) acc[h] = 0.0f;
 #pragma unroll 4
     for (int c = c0; c < c1; ++c) {
-      const float rr = Rsrc[(size_t)c * D + j];
+      const float rr = rvs[c * D + j];
 #pragma unroll
       for (int h = 0; h < G; ++h) acc[h] = fmaf(ofull[h * D + c], rr, acc[h]);
     }
