@@ -135,7 +135,9 @@ struct Task {
 
 int stage_bytes(const Layout& L) { return (std::max(6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16; }
 // Per warp: the stages, then the key tile and the value tile.
-size_t per_warp_bytes(const Layout& L, int nst) { return (size_t)nst * stage_bytes(L) + 2 * kTileBytes; }
+size_t per_warp_bytes(const Layout& L, int nst) {
+  return (size_t)nst * stage_bytes(L) + 2 * kTileBytes + ((size_t)nst * 8 + 15) / 16 * 16;  // + stage barriers
+}
 size_t smem_for(const Layout& L, int nst, int nw) {
   return (size_t)nw * per_warp_bytes(L, nst) + (size_t)nw * 8 * 2 * 4 + kRow * 2 + 64;
 }
@@ -146,8 +148,16 @@ size_t smem_for(const Layout& L, int nst, int nw) {
 size_t attn_plan(Layout& L, int /*r_min*/) {
   // Double-buffered stages first (they hide the copy latency), then as many
   // warps as fit.
-  const int plans[4][2] = {{2, 12}, {2, 8}, {1, 12}, {1, 8}};
+  int plans[8][2] = {{2, 12}, {2, 10}, {2, 8}, {2, 6}, {2, 4}, {0, 0}, {0, 0}, {0, 0}};
+  if (const char* e = std::getenv("MK_ATTN_PLAN")) {  // tuning override: "stages,warps"
+    int a = 0, b = 0;
+    if (std::sscanf(e, "%d,%d", &a, &b) == 2 && a >= 2 && b >= 4 && b <= kMaxWarps) {
+      plans[0][0] = a;
+      plans[0][1] = b;
+    }
+  }
   for (const auto& pl : plans) {
+    if (pl[0] == 0) break;
     const size_t s = smem_for(L, pl[0], pl[1]);
     if (s <= 225 * 1024) {  // leaves room for the static shared memory
       L.attn_tg = kTG;
@@ -180,14 +190,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   const int NST = L.attn_nst, SB = L.attn_sb;
   const int kWarps = blockDim.x >> 5, kSlices = blockDim.x >> 7;
   extern __shared__ __align__(16) unsigned char smem[];
-  const size_t pwb = (size_t)NST * SB + 2 * kTileBytes;
+  const size_t pwb = (size_t)NST * SB + 2 * kTileBytes + ((size_t)NST * 8 + 15) / 16 * 16;
   unsigned char* warp_area = smem;                                       // [kWarps][pwb]
   float* mlw = reinterpret_cast<float*>(smem + kWarps * pwb);            // [kWarps][8][2]
   uint16_t* zrow = reinterpret_cast<uint16_t*>(mlw + kWarps * 16);      // one zero row (272 B)
   __shared__ UnitDesc ud;
   __shared__ int s_abort, s_ns, s_last;
   __shared__ float s_m[8], s_l[8];
-  __shared__ int32_t s_ids[kIdsCap];  // this CTA's selected block ids (its j-th item: ids[part + j P])
+  __shared__ int32_t s_ids[kIdsCap];
+  __shared__ uint64_t s_bar;          // the merging CTA's staging barrier  // this CTA's selected block ids (its j-th item: ids[part + j P])
 
   const int unit_call = blockIdx.x / P;
   const int part = blockIdx.x - unit_call * P;
@@ -301,6 +312,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     return t;
   };
   auto advance = [&](const Task& t) -> Task {
+    if (t.kind == 0) return t;
     if (t.kind == 2 && t.tg + kTG < t.n_live) {
       Task n = t;
       n.tg += kTG;
@@ -323,37 +335,63 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
       vr = reinterpret_cast<const uint16_t*>(base + L.off_win_v) + sl;
     }
   };
-  auto issue = [&](const Task& t, unsigned char* dst) {
+  // Bulk copies of a task into stage sidx; its barrier expects the bytes.
+  uint64_t* bars = reinterpret_cast<uint64_t*>(my_area + (size_t)NST * SB + 2 * kTileBytes);
+  auto issue = [&](const Task& t, int sidx) {
+    unsigned char* dst = my_area + (size_t)sidx * SB;
     if (t.kind == 1) {
-      // 8 K rows then 8 V rows, padded to 272 bytes.
-      for (int i = lane; i < t.nd * 16; i += 32) {
-        const int row = i >> 4, prt = i & 15;
+      // nd K rows then nd V rows, 256 bytes each, into rows padded to 272 bytes.
+      if (lane == 0) {
+        fence_proxy_async();
+        mbar_expect_tx(&bars[sidx], 2u * (unsigned)t.nd * D * 2);
+      }
+      __syncwarp();
+      if (lane < 2 * t.nd) {
+        const int row = lane >> 1, isv = lane & 1;
         const uint16_t *kr, *vr;
         dense_rows(t.j0 + row, kr, vr);
-        cp_async16(dst + row * kRow * 2 + prt * 16, kr + prt * 8);
-        cp_async16(dst + (kDC + row) * kRow * 2 + prt * 16, vr + prt * 8);
+        bulk_g2s(dst + (isv * kDC + row) * kRow * 2, isv ? vr : kr, D * 2, &bars[sidx]);
       }
     } else if (t.kind == 2) {
       // This group's rows of the page's four sub-arrays (B is a multiple of
       // 16, so a whole group stays inside the page; sizes and offsets are
-      // multiples of 16 bytes).  The stage holds them back to back,
-      // [K val 2gr][K idx gr][V val 2gr][V idx gr] bytes: chunk c of the
-      // stage comes from page + o_q + 16 c.
-      const int Br = B * t.r, gr = kTG * t.r, tr = t.tg * t.r;
-      const char* page = base + L.off_pages + (int64_t)t.b * L.page_stride;
-      const int c1 = gr >> 3, c2 = c1 + (gr >> 4), c3 = c2 + (gr >> 3), c4 = c3 + (gr >> 4);
-      const int o0 = 2 * tr, o1 = 2 * Br + tr - 16 * c1, o2 = 3 * Br + 2 * tr - 16 * c2, o3 = 5 * Br + tr - 16 * c3;
-      for (int c = lane; c < c4; c += 32) {
-        const int o = c < c1 ? o0 : c < c2 ? o1 : c < c3 ? o2 : o3;
-        cp_async16(dst + 16 * c, page + o + 16 * c);
+      // multiples of 16 bytes), back to back in the stage:
+      // [K val 2gr][K idx gr][V val 2gr][V idx gr] bytes; lane q copies run q.
+      if (lane == 0) {
+        fence_proxy_async();
+        mbar_expect_tx(&bars[sidx], 6u * kTG * (unsigned)t.r);
+      }
+      __syncwarp();
+      if (lane < 4) {
+        const int Br = B * t.r, gr = kTG * t.r, tr = t.tg * t.r;
+        const char* page = base + L.off_pages + (int64_t)t.b * L.page_stride;
+        const int soff = lane == 0 ? 2 * tr : lane == 1 ? 2 * Br + tr : lane == 2 ? 3 * Br + 2 * tr : 5 * Br + tr;
+        const int doff = lane == 0 ? 0 : lane == 1 ? 2 * gr : lane == 2 ? 3 * gr : 5 * gr;
+        bulk_g2s(dst + doff, page + soff, (lane & 1) ? gr : 2 * gr, &bars[sidx]);
       }
     }
   };
+  auto has_copy = [](const Task& t) { return t.kind == 1 || t.kind == 2; };
 
-  Task cur = make_task(warp, 0);
+  if (lane == 0) {
+    for (int i = 0; i < NST; ++i) mbar_init(&bars[i], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  // Ring of NST stages: the task being consumed sits in stage st, the next
+  // NST - 1 tasks are in flight.  ph: parity of each stage's next phase;
+  // pend: stages with copies in flight.
+  Task cur = make_task(warp, 0), ahead = cur;
   int st = 0;
-  issue(cur, my_area);
-  cp_async_commit();
+  uint32_t ph = 0, pend = 0;
+  bool broken = false;
+  issue(cur, 0);
+  if (has_copy(cur)) pend |= 1u;
+  for (int i = 1; i < NST - 1; ++i) {
+    ahead = advance(ahead);
+    issue(ahead, i);
+    if (has_copy(ahead)) pend |= 1u << i;
+  }
 
   // O'^T fragments, m-tile mt: rows = channels mt*16 + g (+8), columns 2tig,
   // 2tig+1.  With G <= 4, column n holds the hi part (n < 4) or the lo part
@@ -369,14 +407,21 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   const int ktok = ri + (mi >> 1) * 8, kch = (mi & 1) * 8;  // ldmatrix rows for the key B fragments
   const int vtok = ri + (mi >> 1) * 8, vch = (mi & 1) * 8;  // ldmatrix.trans rows for the value A fragments
   while (cur.kind != 0) {
-    if (NST == 2) {
-      issue(advance(cur), my_area + (size_t)(st ^ 1) * SB);  // recomputed at the end: fewer live registers
-      cp_async_commit();
-      asm volatile("cp.async.wait_group 1;\n" ::: "memory");
-    } else {
-      cp_async_wait_all();
+    {
+      const int sn = st + NST - 1 < NST ? st + NST - 1 : st - 1;  // (st + NST - 1) mod NST
+      ahead = advance(ahead);
+      issue(ahead, sn);
+      if (has_copy(ahead)) pend |= 1u << sn;
     }
-    __syncwarp();
+    if (has_copy(cur)) {
+      if (!mbar_wait(&bars[st], (ph >> st) & 1u)) {
+        if (lane == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, st, (int32_t)MK_ETIMEOUT);
+        broken = true;
+        break;
+      }
+      ph ^= 1u << st;
+      pend &= ~(1u << st);
+    }
     const unsigned char* buf = my_area + (size_t)st * SB;
     if (cur.kind == 1 || cur.kind == 2) {
       int ntok, nck_k = 8, nck_v = 8;  // 16-channel chunks that can hold a nonzero
@@ -495,13 +540,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     }
     __syncwarp();
     cur = advance(cur);
-    if (NST == 1) {
-      issue(cur, my_area);
-      cp_async_commit();
-    }
-    st ^= (NST - 1);
+    st = st + 1 < NST ? st + 1 : 0;
   }
-  cp_async_wait_all();
+  if (broken) {
+    // Let the copies still in flight land before the stages are reused.
+    for (int i = 0; i < NST; ++i)
+      if ((pend >> i) & 1u) (void)mbar_wait(&bars[i], (ph >> i) & 1u);
+  }
   __syncwarp();
   if (G <= 4) {
     // Fold the lo columns (lanes tig + 2) into the hi ones.
@@ -515,6 +560,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   const bool col_ok0 = 2 * tig < G && (G == 8 || tig < 2), col_ok1 = 2 * tig + 1 < G && (G == 8 || tig < 2);
 
   // ---- warps -> CTA partial ------------------------------------------------
+  if (!DENSE && warp == 0) {  // the merging CTA stages R_v soon: bring it back into L2
+    const char* rv = base + L.off_rv;
+    for (int i = lane; i < D * D * 4 / 128; i += 32) prefetch_l2(rv + (size_t)i * 128);
+  }
   if (tig == 0) {
     mlw[(warp * 8 + g) * 2] = m_run;
     mlw[(warp * 8 + g) * 2 + 1] = l_run;
@@ -590,15 +639,27 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   float* rvs = red + kSlices * G * D;
   float* sacc = rvs + (DENSE ? 0 : D * D);
   float* sml = sacc + (size_t)P * G * D;
-  if (!DENSE) {
-    const float* Rv = reinterpret_cast<const float*>(base + L.off_rv);
-    for (int i = tid; i < D * D / 4; i += blockDim.x) cp_async16(rvs + 4 * i, Rv + 4 * i);
+  {
+    const unsigned b_rv = DENSE ? 0u : (unsigned)(D * D * 4), b_acc = (unsigned)(P * G * D * 4);
+    const unsigned b_ml = ((unsigned)(P * G * 2 * 4) + 15u) & ~15u;
+    if (tid == 0) {
+      mbar_init(&s_bar, 1);
+      mbar_init_fence();
+      fence_proxy_async_all();  // shared area written by the main loop, partials by the generic proxy
+      mbar_expect_tx(&s_bar, b_rv + b_acc + b_ml);
+      if (!DENSE) bulk_g2s(rvs, base + L.off_rv, b_rv, &s_bar);
+      bulk_g2s(sacc, pacc, b_acc, &s_bar);
+      bulk_g2s(sml, pml, b_ml, &s_bar);
+    }
+    __syncthreads();
+    if (!mbar_wait(&s_bar, 0)) {
+      if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -1, (int32_t)MK_ETIMEOUT);
+      (void)mbar_wait(&s_bar, 0);
+      return;
+    }
   }
-  for (int i = tid; i < P * G * D / 4; i += blockDim.x) cp_async16(sacc + 4 * i, pacc + 4 * i);
-  for (int i = tid; i < (P * G * 2 + 3) / 4; i += blockDim.x) cp_async16(sml + 4 * i, pml + 4 * i);
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
+  // Per (partial, head) weight exp2(m_p - M) / l, computed once; written over
+  // the m entries.
   if (tid < G) {
     float M = -INFINITY;
     for (int p = 0; p < P; ++p) M = fmaxf(M, sml[(p * G + tid) * 2]);
@@ -608,21 +669,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
         const float mp = sml[(p * G + tid) * 2];
         if (mp != -INFINITY) ls += sml[(p * G + tid) * 2 + 1] * exp2f(mp - M);
       }
-    s_m[tid] = M;
-    s_l[tid] = ls;
+    const float inv = (M != -INFINITY && ls > 0.0f) ? 1.0f / ls : 0.0f;
+    for (int p = 0; p < P; ++p) {
+      const float mp = sml[(p * G + tid) * 2];
+      sml[(p * G + tid) * 2] = (mp != -INFINITY && inv != 0.0f) ? exp2f(mp - M) * inv : 0.0f;
+    }
   }
   __syncthreads();
   for (int i = tid; i < G * D; i += blockDim.x) {
     const int h = i / D;
-    const float M = s_m[h], ls = s_l[h];
     float a = 0.0f;
-    if (M != -INFINITY && ls > 0.0f) {
-      for (int p = 0; p < P; ++p) {
-        const float mp = sml[(p * G + h) * 2];
-        if (mp != -INFINITY) a = fmaf(sacc[(size_t)p * G * D + i], exp2f(mp - M), a);
-      }
-      a /= ls;
-    }
+    for (int p = 0; p < P; ++p) a = fmaf(sacc[(size_t)p * G * D + i], sml[(p * G + h) * 2], a);
     ofull[i] = a;
   }
   __syncthreads();

@@ -24,6 +24,7 @@ enum DevErr : int32_t {
   ERR_BAD_BLOCK = 2,   // selected block id out of range
   ERR_BAD_NSEL = 3,    // n_sel larger than the ids row
   ERR_NO_ROTATION = 4,
+  ERR_COPY_WAIT = 5,   // a bulk copy did not complete within the wait bound (status MK_ETIMEOUT)
 };
 
 // Per (layer, seq, kv head) state kept on the device (64 bytes).
@@ -148,8 +149,9 @@ __device__ __forceinline__ int warp_excl_scan(int v, int lane) {
   }
   return x - v;
 }
-__device__ __forceinline__ void set_error(const Layout& L, int32_t detail, int32_t unit, int32_t aux) {
-  if (atomicCAS(&L.err[0], 0, (int32_t)MK_EDEVICE) == 0) {
+__device__ __forceinline__ void set_error(const Layout& L, int32_t detail, int32_t unit, int32_t aux,
+                                          int32_t status = (int32_t)MK_EDEVICE) {
+  if (atomicCAS(&L.err[0], 0, status) == 0) {
     L.err[1] = detail;
     L.err[2] = unit;
     L.err[3] = aux;
@@ -167,6 +169,57 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+// Bulk (TMA) global -> shared copies completing on an mbarrier.  One request
+// moves a whole contiguous run (16-byte aligned addresses, size a multiple of
+// 16), so a single SM keeps far more bytes in flight than with 16-byte
+// cp.async requests.
+__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Makes initialised barriers visible to the asynchronous (bulk copy) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// Orders this thread's earlier shared-memory accesses before later bulk
+// copies into the same bytes.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+// Same for every state space: global data this CTA (or, through an acquired
+// counter, another CTA) wrote becomes visible to later bulk copies.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;\n" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete: false once
+// 20 ms have passed (far above any real copy time).
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > 20000000ull) return false;
+  return true;
 }
 // Programmatic dependent launch: a kernel launched with the
 // programmatic-serialization attribute may start while the previous kernel

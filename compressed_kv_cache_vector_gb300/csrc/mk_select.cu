@@ -22,10 +22,11 @@
 //    4096-bin histogram of the keys' top 12 bits, kept in shared memory and
 //    added to the unit's histogram in global memory when the CTA is done.
 //  * The last CTA of each (sequence, kv head) to finish (atomic counter, no
-//    waiting) selects the top k: the histogram gives the coarse bin of the
-//    k-th largest key; keys above it are taken outright, keys inside it are
-//    gathered into a short list that two 1024-bin passes resolve to the exact
-//    threshold; the ids are then written in ascending order from per-thread
+//    waiting) selects the top k.  It stages the histogram and all keys with
+//    one bulk copy each (a single SM moves them far faster that way than with
+//    16-byte requests); the histogram gives the coarse bin of the k-th
+//    largest key, two 1024-bin passes over the keys inside it give the exact
+//    threshold, and the ids are written in ascending order from per-thread
 //    bit masks and one block scan.  Every loop does the same work on every
 //    thread (no per-key serial chains), because a single CTA of 8 warps runs
 //    it and its time is latency, not bandwidth.
@@ -53,7 +54,6 @@ __host__ __device__ inline int topk_cpt(int nblk) {
   return ((nch + 255) / 256 + 7) & ~7;
 }
 __host__ __device__ inline int64_t topk_mask_bytes(int cpt) { return (int64_t)256 * cpt; }
-__host__ __device__ inline int64_t topk_stage_bytes(int cpt) { return (int64_t)256 * cpt * 16; }
 
 __device__ __forceinline__ uint32_t ordered_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   __shared__ __align__(16) uint32_t hc[kKeyBins];   // coarse key histogram
   __shared__ __align__(16) uint32_t hf[kFineBins];  // fine histogram of the threshold search
   __shared__ int2 wsum[kSelWarps];
-  __shared__ int s_abort, s_last, s_bin, s_rem, s_len;
+  __shared__ int s_abort, s_last, s_bin, s_rem;
+  __shared__ uint64_t s_bar;  // top-k staging barrier
 
   const int unit_call = blockIdx.x / P, part = blockIdx.x - unit_call * P;
   const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
@@ -327,133 +328,64 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const bool all = k >= n_cand;  // every candidate is taken
   const int nch = (nblk + 3) >> 2;
   const int CPT = topk_cpt(nblk), NG = CPT >> 3;
-  const bool staged = topk_stage_bytes(CPT) + topk_mask_bytes(CPT) <= (int64_t)dyn_bytes;
+  const int64_t kbytes = (int64_t)nch * 16;
+  const bool staged = kbytes + topk_mask_bytes(CPT) <= (int64_t)dyn_bytes;
   uint4* ks = reinterpret_cast<uint4*>(smem);
-  uint32_t* m_above = reinterpret_cast<uint32_t*>(smem + (staged ? topk_stage_bytes(CPT) : 0));
-  uint32_t* m_in = m_above + NG * 256;
-  uint32_t* list = m_in + NG * 256;
-  const int list_cap = (int)((dyn_bytes - (reinterpret_cast<unsigned char*>(list) - smem)) / 4);
+  uint32_t* m_gt = reinterpret_cast<uint32_t*>(smem + (staged ? kbytes : 0));
+  uint32_t* m_eq = m_gt + NG * 256;
 
-  // The unit's histogram (then cleared for the next call) and its keys.
-  for (int i = tid; i < kKeyBins / 4; i += blockDim.x) cp_async16(hc + 4 * i, gh + 4 * i);
-  cp_async_commit();
-  if (staged) {
-    // chunk c at c ^ ((c / CPT) & 7): the 8 threads of a quarter warp reading
-    // their j-th chunks hit 8 different 16-byte bank groups.
-    for (int c = tid; c < 256 * CPT; c += blockDim.x) {
-      uint4* dst = ks + (c ^ ((c / CPT) & 7));
-      if (c < nch) cp_async16(dst, kw + 4 * c);
-      else *dst = make_uint4(0, 0, 0, 0);
-    }
+  // The unit's coarse histogram and its keys, one bulk copy each (the scoring
+  // CTAs' writes were acquired through the counter).
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    mbar_init_fence();
+    fence_proxy_async_all();
+    mbar_expect_tx(&s_bar, (unsigned)(kKeyBins * 4 + (staged ? kbytes : 0)));
+    bulk_g2s(hc, gh, kKeyBins * 4, &s_bar);
+    if (staged) bulk_g2s(ks, kw, (unsigned)kbytes, &s_bar);
   }
-  cp_async_commit();
-  asm volatile("cp.async.wait_group 1;\n" ::: "memory");
   __syncthreads();
+  if (!mbar_wait(&s_bar, 0)) {
+    if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -2, (int32_t)MK_ETIMEOUT);
+    (void)mbar_wait(&s_bar, 0);
+    return;
+  }
   for (int i = tid; i < kKeyBins / 4; i += blockDim.x) reinterpret_cast<uint4*>(gh)[i] = make_uint4(0, 0, 0, 0);
-  // Undecided range [lo, hi]: the coarse bin of the k-th largest key.
-  uint32_t lo = 1u, hi = 0xffffffffu;
-  int rem = 0;
-  if (!all) {
-    find_bin<kKeyBins>(hc, k, wsum, &s_bin, &s_rem);
-    lo = max(1u, (uint32_t)s_bin << 20);
-    hi = ((uint32_t)s_bin << 20) | 0xfffffu;
-    rem = s_rem;
-  }
-  cp_async_wait_all();
-  __syncthreads();
-  if (staged && tid == 0 && (nblk & 3)) {  // key slots past nblk in the last chunk
-    const int c = nch - 1;
-    uint32_t* last = reinterpret_cast<uint32_t*>(ks + (c ^ ((c / CPT) & 7)));
-    for (int e = nblk & 3; e < 4; ++e) last[e] = 0u;
-  }
-  __syncthreads();
-  // Thread tid's j-th chunk: keys tid*CPT*4 + 4j .. +3.
-  auto chunk = [&](int j) -> uint4 {
-    if (staged) return ks[tid * CPT + (j ^ (tid & 7))];
-    const int c = tid * CPT + j;
+  // Thread tid owns chunks tid * CPT .. + CPT - 1 (4 keys each, keys past
+  // nblk read as 0).  Within each group of 8 chunks it visits chunk
+  // jj ^ (tid & 7) at step jj, so the 8 threads of a quarter warp read 8
+  // different 16-byte bank groups.
+  auto chunk = [&](int lc) -> uint4 {
+    const int c = tid * CPT + lc;
     if (c >= nch) return make_uint4(0, 0, 0, 0);
-    uint4 v = __ldcg(reinterpret_cast<const uint4*>(kw) + c);
+    uint4 v = staged ? ks[c] : __ldcg(reinterpret_cast<const uint4*>(kw) + c);
     const int e0 = 4 * c;
     if (e0 + 1 >= nblk) v.y = 0u;
     if (e0 + 2 >= nblk) v.z = 0u;
     if (e0 + 3 >= nblk) v.w = 0u;
     return v;
   };
-  auto key_at = [&](int i) -> uint32_t {  // i: key index within this thread's range
-    const uint4 v = chunk(i >> 2);
-    const int qq = i & 3;
-    return qq == 0 ? v.x : qq == 1 ? v.y : qq == 2 ? v.z : v.w;
-  };
 
-  // Pass 1: per 32 keys, masks of the keys above the range (taken) and inside it.
-  const bool top_bin = !all && hi == 0xffffffffu;  // nothing lies above the top bin
-  const uint32_t above_from = all ? 1u : hi + 1u;
-  int n_above = 0, n_in = 0;
-  for (int gi = 0; gi < NG; ++gi) {
-    uint32_t ab = 0, ib = 0;
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const uint4 v = chunk(gi * 8 + jj);
-      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-        if (!top_bin && e[qq] >= above_from) ab |= 1u << (jj * 4 + qq);
-        if (!all && e[qq] - lo <= hi - lo) ib |= 1u << (jj * 4 + qq);
-      }
-    }
-    m_above[gi * 256 + tid] = ab;
-    m_in[gi * 256 + tid] = ib;
-    n_above += __popc(ab);
-    n_in += __popc(ib);
-  }
-
-  // Threshold: the rem-th largest key inside [lo, hi], found by two passes of
-  // kFineBins bins (the range spans at most 2^20 keys).
+  // Threshold: the coarse bin of the k-th largest key, then two passes of
+  // kFineBins bins over the keys inside it (the bin spans 2^20 key values).
   uint32_t thr = 0;
   int need = 0;
   if (!all) {
-    const int off0 = block_excl_scan2(n_in, 0, wsum).x;
-    if (tid == blockDim.x - 1) s_len = off0 + n_in;
-    __syncthreads();
-    const int len = s_len;
-    const bool listed = len <= list_cap;
-    if (listed) {
-      int off = off0;
-      for (int gi = 0; gi < NG; ++gi) {
-        const uint32_t ib = m_in[gi * 256 + tid];
-        if (ib) {
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const uint4 v = chunk(gi * 8 + jj);
-            const uint32_t e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              const int bb = jj * 4 + qq;
-              if ((ib >> bb) & 1u) list[off + __popc(ib & ((1u << bb) - 1u))] = e[qq];
-            }
-          }
-        }
-        off += __popc(ib);
-      }
-    }
+    find_bin<kKeyBins>(hc, k, wsum, &s_bin, &s_rem);
+    uint32_t lo = max(1u, (uint32_t)s_bin << 20), hi = ((uint32_t)s_bin << 20) | 0xfffffu;
+    int rem = s_rem;
     for (int pass = 0; pass < 2 && lo != hi; ++pass) {
       const int sh = max(0, 32 - __clz(hi - lo) - 10);  // (hi - lo) >> sh < kFineBins
       for (int i = tid; i < kFineBins; i += blockDim.x) hf[i] = 0;
       __syncthreads();
-      if (listed) {
-        for (int i = tid; i < len; i += blockDim.x) {
-          const uint32_t key = list[i];
-          if (key - lo <= hi - lo) atomicAdd(&hf[(key - lo) >> sh], 1u);
-        }
-      } else {
-        for (int gi = 0; gi < NG; ++gi) {
-          uint32_t m = m_in[gi * 256 + tid];
-          while (m) {
-            const int bb = __ffs(m) - 1;
-            m &= m - 1;
-            const uint32_t key = key_at(gi * 32 + bb);
-            if (key - lo <= hi - lo) atomicAdd(&hf[(key - lo) >> sh], 1u);
-          }
+      for (int gi = 0; gi < NG; ++gi) {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const uint4 v = chunk(gi * 8 + (jj ^ (tid & 7)));
+          const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (e[q] - lo <= hi - lo) atomicAdd(&hf[(e[q] - lo) >> sh], 1u);
         }
       }
       __syncthreads();
@@ -468,32 +400,28 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     need = rem;  // keys equal to thr that are taken, lowest block ids first
   }
 
-  // Pass 2: the undecided keys above thr join the taken ones; the ones equal
-  // to it are the ties.
-  int n_gt = n_above, n_eq = 0;
-  if (!all)
-    for (int gi = 0; gi < NG; ++gi) {
-      const uint32_t ib = m_in[gi * 256 + tid];
-      uint32_t gm = 0, em = 0;
-      if (ib) {
+  // Per 32 keys: masks of the keys above thr (all candidates when every one
+  // is taken) and of the ties.
+  int n_gt = 0, n_eq = 0;
+  for (int gi = 0; gi < NG; ++gi) {
+    uint32_t gm = 0, em = 0;
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const uint4 v = chunk(gi * 8 + jj);
-          const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+    for (int jj = 0; jj < 8; ++jj) {
+      const int lj = jj ^ (tid & 7);
+      const uint4 v = chunk(gi * 8 + lj);
+      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            if (e[qq] > thr) gm |= 1u << (jj * 4 + qq);
-            if (e[qq] == thr) em |= 1u << (jj * 4 + qq);
-          }
-        }
-        gm &= ib;
-        em &= ib;
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t bit = 1u << (lj * 4 + q);
+        if (all ? e[q] != 0u : e[q] > thr) gm |= bit;
+        else if (!all && e[q] == thr) em |= bit;
       }
-      m_above[gi * 256 + tid] |= gm;
-      m_in[gi * 256 + tid] = em;
-      n_gt += __popc(gm);
-      n_eq += __popc(em);
     }
+    m_gt[gi * 256 + tid] = gm;
+    m_eq[gi * 256 + tid] = em;
+    n_gt += __popc(gm);
+    n_eq += __popc(em);
+  }
   const int2 ex = block_excl_scan2(n_gt, n_eq, wsum);
 
   // Ordered output: thread tid's ids follow those of threads 0..tid-1.
@@ -501,14 +429,12 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   int pos = ex.x + min(ex.y, need);
   const int kbase = tid * CPT * 4;
   for (int gi = 0; gi < NG; ++gi) {
-    uint32_t sel = m_above[gi * 256 + tid];
-    if (!all) {
-      uint32_t em = m_in[gi * 256 + tid];
-      while (take_eq > 0 && em) {
-        sel |= em & (0u - em);
-        em &= em - 1;
-        --take_eq;
-      }
+    uint32_t sel = m_gt[gi * 256 + tid];
+    uint32_t em = m_eq[gi * 256 + tid];
+    while (take_eq > 0 && em) {
+      sel |= em & (0u - em);
+      em &= em - 1;
+      --take_eq;
     }
     if (sel) {
 #pragma unroll
@@ -535,10 +461,10 @@ cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, 
   int P = std::max(1, 152 / units);
   P = std::min(P, std::max(1, (tiles + kSelWarps - 1) / kSelWarps));
   const dim3 grid(units * P);
-  // Dynamic shared memory: the meta tile stages, or the top-k's keys, masks
-  // and list for the context's largest block count, whichever is larger.
+  // Dynamic shared memory: the meta tile stages, or the top-k's keys and
+  // masks for the context's largest block count, whichever is larger.
   const int cpt = topk_cpt(L.nblk_cap);
-  const int64_t want = topk_stage_bytes(cpt) + topk_mask_bytes(cpt) + (int64_t)4 * L.nblk_cap;
+  const int64_t want = (int64_t)16 * ((L.nblk_cap + 3) / 4) + topk_mask_bytes(cpt);
   const int dyn = (int)std::max<int64_t>(kSelSmem, std::min<int64_t>(kSelSmemMax, want));
 #define MK_SEL_CASE(GG)                                                                                      \
   case GG: {                                                                                                 \
