@@ -148,10 +148,12 @@ size_t smem_for(const Layout& L, int nst, int nw) {
 size_t attn_plan(Layout& L, int /*r_min*/) {
   // Double-buffered stages first (they hide the copy latency), then as many
   // warps as fit.
-  int plans[8][2] = {{2, 12}, {2, 10}, {2, 8}, {2, 6}, {2, 4}, {0, 0}, {0, 0}, {0, 0}};
+  // Warps per CTA are a multiple of 4: the merge's un-rotation splits the
+  // channels into blockDim.x / 128 slices of 128 threads.
+  int plans[8][2] = {{2, 12}, {2, 8}, {2, 4}, {0, 0}, {0, 0}, {0, 0}, {0, 0}, {0, 0}};
   if (const char* e = std::getenv("MK_ATTN_PLAN")) {  // tuning override: "stages,warps"
     int a = 0, b = 0;
-    if (std::sscanf(e, "%d,%d", &a, &b) == 2 && a >= 2 && b >= 4 && b <= kMaxWarps) {
+    if (std::sscanf(e, "%d,%d", &a, &b) == 2 && a >= 2 && b >= 4 && b <= kMaxWarps && b % 4 == 0) {
       plans[0][0] = a;
       plans[0][1] = b;
     }

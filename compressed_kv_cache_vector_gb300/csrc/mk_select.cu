@@ -147,6 +147,194 @@ __device__ __forceinline__ void find_bin(const uint32_t* h, int rem, int2* wsum,
   __syncthreads();
 }
 
+// Top-k over the staged keys for nch <= 256 * kRoundsMax chunks of 4 keys:
+// thread tid takes chunks j * 256 + tid (round j), so the block's key order
+// is (j, tid) and every load of a round is conflict free.  The code runs once
+// per launch on its SM, where each instruction not yet in the instruction
+// cache costs a fetch, so every pass is a short loop.  sc: 1024 words of
+// shared scratch.
+//  * Threshold: the coarse bin of the histogram brackets it; counting passes
+//    (interpolated in count space, with a bisection step whenever one shrank
+//    the bracket by less than half) narrow the bracket until it holds at most
+//    256 keys, which are then ranked exactly.
+//  * Output: per round, a block's key above the threshold goes to position
+//    (keys above it before it) + min(ties before it, need); a tie is taken
+//    when fewer than `need` ties precede it.  The counts before a key come
+//    from per-round per-warp totals and a warp scan of packed counts.
+constexpr int kRoundsMax = 16;
+constexpr int SC_CNT = 0, SC_G = 16, SC_GN = 272, SC_THR = 273, SC_WT = 280, SC_BT = 280 + 8 * kRoundsMax;
+static_assert(SC_BT + 8 * kRoundsMax <= 1024, "scratch");
+__device__ void topk_loop(const uint4* ks, int nch, int nblk, int k, bool all, const uint32_t* hc, uint32_t* sc,
+                          int2* wsum, int* s_bin, int* s_rem, int32_t* out, int k_max) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rounds = (nch + 255) >> 8;
+  // This thread's chunk of round j, keys past nblk zero.
+  auto chunk = [&](int j) -> uint4 {
+    const int c = j * 256 + tid;
+    uint4 v = c < nch ? ks[c] : make_uint4(0, 0, 0, 0);
+    if (4 * c + 1 >= nblk) v.y = 0u;
+    if (4 * c + 2 >= nblk) v.z = 0u;
+    if (4 * c + 3 >= nblk) v.w = 0u;
+    return v;
+  };
+  int par = 0;
+  // Block-wide number of keys >= x (one barrier; the two count slots alternate).
+  auto cge = [&](uint64_t x) -> int {
+    int c = 0;
+    if (x <= 0xffffffffull) {
+      const uint32_t xx = (uint32_t)x;
+#pragma unroll 1
+      for (int j = 0; j < rounds; ++j) {
+        const uint4 v = chunk(j);
+        c += (v.x >= xx) + (v.y >= xx) + (v.z >= xx) + (v.w >= xx);
+      }
+    }
+    c = (int)__reduce_add_sync(FULL, (unsigned)c);
+    if (lane == 0) sc[SC_CNT + par * 8 + warp] = (uint32_t)c;
+    __syncthreads();
+    int t = 0;
+#pragma unroll 1
+    for (int w = 0; w < 8; ++w) t += (int)sc[SC_CNT + par * 8 + w];
+    par ^= 1;
+    return t;
+  };
+
+  uint32_t thr = 1u;  // every candidate (key >= 1) when all are taken
+  int need = 0;
+  if (!all) {
+    find_bin<kKeyBins>(hc, k, wsum, s_bin, s_rem);
+    const uint64_t b = (uint64_t)*s_bin;
+    uint64_t lo = b << 20 ? b << 20 : 1ull, hi = (b << 20) | 0xfffffull;
+    int c_hi = k - *s_rem;             // keys above hi
+    int c_lo = c_hi + (int)hc[b];      // keys >= lo
+    bool bisect = false;
+    while (lo < hi && c_lo - c_hi > 256) {
+      uint64_t x;
+      if (bisect) {
+        x = lo + (hi - lo + 1) / 2;
+      } else {
+        // cge falls from c_lo at lo to c_hi at hi + 1; aim where it crosses k
+        // (fp32: the step only needs to be roughly right).
+        const float f = __fdividef((float)(k - c_hi), (float)(c_lo - c_hi));
+        const uint64_t d = (uint64_t)(f * (float)(hi + 1 - lo));
+        x = hi + 1 - d;
+        x = x < lo + 1 ? lo + 1 : (x > hi ? hi : x);
+      }
+      const uint64_t w0 = hi - lo;
+      const int c = cge(x);
+      if (c >= k) {
+        lo = x;
+        c_lo = c;
+      } else {
+        hi = x - 1;
+        c_hi = c;
+      }
+      bisect = !bisect && (hi - lo) > w0 / 2;
+    }
+    if (lo < hi) {
+      // At most 256 keys lie in [lo, hi]: gather and rank them.
+      if (tid == 0) sc[SC_GN] = 0u;
+      __syncthreads();
+#pragma unroll 1
+      for (int j = 0; j < rounds; ++j) {
+        const uint4 v = chunk(j);
+        const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (e[q] >= lo && e[q] <= hi) sc[SC_G + atomicAdd(&sc[SC_GN], 1u)] = e[q];
+      }
+      __syncthreads();
+      const int m = (int)sc[SC_GN];
+      const int want = k - c_hi;  // rank of the threshold among them (1 = largest)
+      if (tid < m) {
+        const uint32_t key = sc[SC_G + tid];
+        int gt = 0, eq = 0;
+#pragma unroll 4
+        for (int i = 0; i < m; ++i) {
+          const uint32_t o = sc[SC_G + i];
+          gt += o > key;
+          eq += o == key;
+        }
+        if (gt < want && gt + eq >= want) sc[SC_THR] = key;
+      }
+      __syncthreads();
+      lo = sc[SC_THR];
+    }
+    thr = (uint32_t)lo;
+    need = k - cge((uint64_t)thr + 1);  // ties to take
+  }
+
+  // Keys above thr (all candidates when every one is taken) and ties of one
+  // chunk, as 4-bit masks.
+  auto masks = [&](int j, uint32_t& gm, uint32_t& em) {
+    const uint4 v = chunk(j);
+    const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+    gm = 0u;
+    em = 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      gm |= (all ? e[q] != 0u : e[q] > thr) ? 1u << q : 0u;
+      em |= (!all && e[q] == thr) ? 1u << q : 0u;
+    }
+  };
+  // Per round: warp totals of (above, ties), packed as above | ties << 16.
+#pragma unroll 1
+  for (int j = 0; j < rounds; ++j) {
+    uint32_t gm, em;
+    masks(j, gm, em);
+    const unsigned t = __reduce_add_sync(FULL, (unsigned)__popc(gm) | ((unsigned)__popc(em) << 16));
+    if (lane == 0) sc[SC_WT + j * 8 + warp] = t;
+  }
+  __syncthreads();
+  // Base of (round j, warp w) = exclusive scan of the totals in (j, w) order
+  // (at most 128 of them: threads 0-127, warp scans, then earlier warps' sums).
+  uint32_t wv = 0u, winc = 0u;
+  if (warp < 4) {
+    wv = tid < rounds * 8 ? sc[SC_WT + tid] : 0u;
+    winc = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(FULL, winc, o);
+      if (lane >= o) winc += y;
+    }
+    if (lane == 31) sc[SC_CNT + warp] = winc;  // the count slots are free now
+  }
+  __syncthreads();
+  if (tid < rounds * 8) {
+    uint32_t add = 0u;
+#pragma unroll 1
+    for (int w = 0; w < warp; ++w) add += sc[SC_CNT + w];
+    sc[SC_BT + tid] = add + winc - wv;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int j = 0; j < rounds; ++j) {
+    uint32_t gm, em;
+    masks(j, gm, em);
+    const uint32_t own = (uint32_t)__popc(gm) | ((uint32_t)__popc(em) << 16);
+    uint32_t inc = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const uint32_t before = sc[SC_BT + j * 8 + warp] + inc - own;
+    const int g_before = (int)(before & 0xffffu), e_before = (int)(before >> 16);
+    // ties this chunk takes: those still below `need`
+    const int take_eq = max(0, min(__popc(em), need - e_before));
+    uint32_t tm = em;
+    while (__popc(tm) > take_eq) tm &= ~(1u << (31 - __clz(tm)));  // keep the lowest ids
+    const uint32_t take = gm | tm;
+    const int p0 = g_before + min(e_before, need);
+    const int c = j * 256 + tid;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int p = p0 + __popc(take & ((1u << q) - 1u));
+      if (((take >> q) & 1u) && p < k_max) out[p] = 4 * c + q;
+    }
+  }
+}
+
 }  // namespace
 
 // grid: P CTAs per (sequence, kv head) of the call; 256 threads.
@@ -351,7 +539,12 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     return;
   }
   for (int i = tid; i < kKeyBins / 4; i += blockDim.x) reinterpret_cast<uint4*>(gh)[i] = make_uint4(0, 0, 0, 0);
-  // Thread tid owns chunks tid * CPT .. + CPT - 1 (4 keys each, keys past
+  if (staged && nch <= 256 * kRoundsMax) {
+    topk_loop(ks, nch, nblk, k, all, hc, hf, wsum, &s_bin, &s_rem, out, L.k_max);
+    if (tid == 0) n_sel[(int64_t)ci * L.n_kv + kvh] = k;
+    return;
+  }
+  // Larger block counts: thread tid owns chunks tid * CPT .. + CPT - 1 (4 keys each, keys past
   // nblk read as 0).  Within each group of 8 chunks it visits chunk
   // jj ^ (tid & 7) at step jj, so the 8 threads of a quarter warp read 8
   // different 16-byte bank groups.
