@@ -202,6 +202,7 @@ def build_gpu(wl, dev, rank, capacity_extra):
                               wl.segments, wl.topk_fixed, wl.retain_permille)
     mk = binding.MosaicKV(cfg, dev)
     seqs = list(range(wl.n_seqs))
+    prefill_ms = mk.prefill_ms = []
     gram = torch.empty(D, D, dtype=torch.float32, device=dev)
     for l in range(wl.n_layers):
         ks, vs = [], []
@@ -219,9 +220,16 @@ def build_gpu(wl, dev, rank, capacity_extra):
             ks.append(torch.stack(kh, 1))
             vs.append(torch.stack(vh, 1))
             del kh, vh
-        mk.append(l, seqs, list(wl.seq_lens), torch.cat(ks).contiguous(), torch.cat(vs).contiguous())
+        kcat, vcat = torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
         del ks, vs
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        binding.record_event(e0)
+        mk.append(l, seqs, list(wl.seq_lens), kcat, vcat)   # bulk prefill of the layer
+        binding.record_event(e1)
+        torch.cuda.synchronize()
+        prefill_ms.append(e0.elapsed_time(e1))
+        del kcat, vcat
     st, detail = mk.poll_error()
     if st != 0:
         raise RuntimeError(f"device error during cache build: {st}/{detail}")
@@ -459,6 +467,15 @@ def main():
                             timing="CUDA graph of one full step, replayed; CUDA events on the stream"),
                 hbm_gbs=gbs, alg_bytes_per_step=step_bytes, roofline=roofline, phases=phases,
                 cpu_baseline=cpu, e2e=e2e, gpu_launches=4 * L * a.steps, clocks=clk)
+    if mk.prefill_ms:
+        pm = sorted(mk.prefill_ms)[len(mk.prefill_ms) // 2]
+        ntok = sum(wl.seq_lens) * wl.n_kv_heads
+        line["prefill"] = {
+            "kernel": "k_append_bulk (128-token tiles: tcgen05 rotation GEMM, top-r, pack, block min/max)",
+            "ms_per_layer_median": pm, "vectors_per_s": 2 * ntok / (pm * 1e-3),
+            "tensor_tflops": 2 * ntok * 3 * 2 * D * D / (pm * 1e-3) / 1e12,
+            "hbm_read_gbs": 2 * ntok * D * 2 / (pm * 1e-3) / 1e9,
+            "how": "CUDA events around the bulk mk_append_compress of each layer while building the cache"}
     if dense:
         line["dense_reference"] = dense
     print(json.dumps(line), flush=True)

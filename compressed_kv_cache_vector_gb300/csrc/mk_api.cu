@@ -86,6 +86,8 @@ Plan make_plan(const mk_config* c) {
   L.off_rkt = off; off += D * D * 4;
   L.off_rvt = off; off += D * D * 4;
   L.off_rv = off; off += D * D * 4;
+  L.off_rkp = off; off += 3 * D * D * 2;
+  L.off_rvp = off; off += 3 * D * D * 2;
   L.off_sink_k = off; off = align_up(off + std::max<int64_t>(1, L.S) * D * 2);
   L.off_sink_v = off; off = align_up(off + std::max<int64_t>(1, L.S) * D * 2);
   L.off_win_k = off; off = align_up(off + (int64_t)L.W * D * 2);
@@ -268,12 +270,37 @@ mk_status mk_set_rotation(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_he
   const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq;
   if (ctx->T[ls] != 0) return MK_ESTATE;
   const int D = MK_HEAD_DIM;
-  std::vector<float> buf((size_t)3 * D * D);
+  // R_k^T, R_v^T, R_v (fp32), then R_k and R_v each split exactly into three
+  // bf16 parts (x = p0 + p1 + p2: 8 significant bits each, truncated) in the
+  // tensor cores' K-major operand layout (B operand of k' = k R^T: row = output
+  // channel, K = input channel), contiguous after them in the unit.
+  std::vector<float> buf((size_t)3 * D * D + (size_t)3 * D * D);  // 3 fp32 matrices + 6 bf16 parts
+  uint16_t* parts = reinterpret_cast<uint16_t*>(buf.data() + (size_t)3 * D * D);
+  auto split3 = [](float x, uint16_t p[3]) {
+    float r = x;
+    for (int i = 0; i < 3; ++i) {
+      uint32_t b;
+      std::memcpy(&b, &r, 4);
+      p[i] = (uint16_t)(b >> 16);
+      const uint32_t hb = b & 0xffff0000u;
+      float h;
+      std::memcpy(&h, &hb, 4);
+      r -= h;
+    }
+  };
   for (int i = 0; i < D; ++i)
     for (int j = 0; j < D; ++j) {
       buf[(size_t)j * D + i] = Rk[(size_t)i * D + j];                 // R_k^T
       buf[(size_t)D * D + (size_t)j * D + i] = Rv[(size_t)i * D + j];  // R_v^T
       buf[(size_t)2 * D * D + (size_t)i * D + j] = Rv[(size_t)i * D + j];
+      const int off = mk::umma_kmajor_offset(i, j) / 2;  // element (row i, k j), in bf16 units
+      uint16_t pk[3], pv[3];
+      split3(Rk[(size_t)i * D + j], pk);
+      split3(Rv[(size_t)i * D + j], pv);
+      for (int q = 0; q < 3; ++q) {
+        parts[(size_t)q * D * D + off] = pk[q];
+        parts[(size_t)(3 + q) * D * D + off] = pv[q];
+      }
     }
   const int64_t u = mk::unit_index(ctx->L, layer, seq, kv_head);
   char* dst = ctx->L.units + u * ctx->L.unit_stride + ctx->L.off_rkt;
@@ -303,6 +330,8 @@ mk_status mk_append_compress(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const i
   }
   if (total == 0) return MK_OK;
   if (!k || !v || total > INT32_MAX) return MK_EINVAL;
+  // The bulk path reads 16-byte vectors of k and v.
+  if (max_new > mk::kSmallAppend && (((uintptr_t)k | (uintptr_t)v) & 15u) != 0) return MK_EINVAL;
   cudaStream_t s = (cudaStream_t)stream;
   CallSeqs* cs = new (std::nothrow) CallSeqs();
   if (!cs) return MK_ENOMEM;

@@ -213,19 +213,37 @@ __global__ void __launch_bounds__(256) k_append_small(Layout L, int layer, CallS
   if (tid == 0) L.desc[u].T = T_new;
 }
 
-// Bulk append of new tokens (prefill): tiles of up to 64 positions aligned so
-// that every middle block lies in one tile; grid (tiles, kv heads).  The
-// length was already advanced by the eviction pass that precedes it.
+// Bulk append of new tokens (prefill): tiles of up to 128 positions aligned so
+// that every middle block sits in one tile, one CTA per (tile, kv head).
+// The rotation of the tile is a dense GEMM on the 5th-generation tensor
+// cores: D[128 tok x 128 ch] = X[128 x 128] R^T with X the tile's bf16 keys
+// (values) and R split exactly into three bf16 parts (pre-split in the unit
+// at mk_set_rotation), 24 tcgen05.mma (3 parts x 8 k-steps of 16) per
+// tensor accumulating in fp32 in tensor memory.  Every product is exact and
+// the sum is fp32, as in the per-token path.  The epilogue rounds the
+// accumulators to bf16 rows in shared memory, where one warp per token does
+// the top-r selection and packing, and the block min/max follow.
+namespace {
+constexpr int kRotRow = D + 8;                                  // padded bf16 row of the rotated tile
+constexpr int kBulkXBytes = kTileTokens * D * 2;                // 32 KB tensor-core A tile
+constexpr int kBulkRBytes = 3 * D * D * 2;                      // 96 KB: the three parts of R
+constexpr int kBulkRotBytes = 2 * kTileTokens * kRotRow * 2;    // rotated K and V rows
+constexpr int kBulkSmem = kBulkXBytes + kBulkRBytes + kBulkRotBytes + kTileTokens * 32;
+constexpr uint32_t kBulkIdesc = umma_idesc_bf16(128, 128);
+}  // namespace
+
 __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSeqs cs,
                                                      const uint16_t* __restrict__ kin,
                                                      const uint16_t* __restrict__ vin) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  float* Rs = reinterpret_cast<float*>(smem);                          // [128][128]
-  float* xs = Rs + D * D;                                              // [64][128]
-  uint16_t* rot = reinterpret_cast<uint16_t*>(xs + kTileTokens * D);   // [2][64][128]
-  uint8_t* keepk = reinterpret_cast<uint8_t*>(rot + 2 * kTileTokens * D);  // [64][32] nibbles
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* Xs = smem;                                     // A: tile rows, K-major core matrices
+  unsigned char* Rp = smem + kBulkXBytes;                       // B: three parts of R
+  uint16_t* rot = reinterpret_cast<uint16_t*>(Rp + kBulkRBytes);  // [2][128][kRotRow]
+  uint8_t* keepk = reinterpret_cast<uint8_t*>(rot + 2 * kTileTokens * kRotRow);  // [128][32] nibbles
   __shared__ UnitDesc ud;
-  __shared__ int s_ci, s_abort;
+  __shared__ int s_ci, s_abort, s_fail;
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t bar_copy, bar_mma;
 
   const int tile = blockIdx.x, kvh = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -237,7 +255,11 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
     }
     s_ci = lo;
     s_abort = has_error(L);
+    s_fail = 0;
     ud = L.desc[unit_index(L, layer, cs.seq[lo], kvh)];
+    mbar_init(&bar_copy, 1);
+    mbar_init(&bar_mma, 1);
+    mbar_init_fence();
   }
   __syncthreads();
   if (s_abort) return;
@@ -254,42 +276,90 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
   if (nt <= 0) return;
   char* base = unit_base(L, u);
   const int64_t in_stride = (int64_t)L.n_kv * D;
+  const int64_t row0 = cs.row_off[ci] + (lo - T_old);
+
+  if (warp == 0) tmem_alloc(&s_tmem, 256);  // K accumulators in columns 0-127, V in 128-255
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tmem = s_tmem;
 
   for (int w = 0; w < 2; ++w) {
+    // R parts: one bulk copy (contiguous, already in operand layout).
+    if (tid == 0) {
+      fence_proxy_async();
+      mbar_expect_tx(&bar_copy, kBulkRBytes);
+      bulk_g2s(Rp, base + (w == 0 ? L.off_rkp : L.off_rvp), kBulkRBytes, &bar_copy);
+    }
+    // X: the tile's rows, 16 bytes (8 channels) per load, into core matrices;
+    // rows past the tile's tokens are zero.
+    const uint16_t* src = (w == 0 ? kin : vin) + (int64_t)kvh * D;
+    for (int i = tid; i < kTileTokens * (D / 8); i += blockDim.x) {
+      const int t = i >> 4, c8 = i & 15;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < nt) v = *reinterpret_cast<const uint4*>(src + (row0 + t) * in_stride + c8 * 8);
+      *reinterpret_cast<uint4*>(Xs + umma_kmajor_offset(t, c8 * 8)) = v;
+    }
+    fence_proxy_async();
     __syncthreads();
-    const float4* RT = reinterpret_cast<const float4*>(base + (w == 0 ? L.off_rkt : L.off_rvt));
-    for (int i = tid; i < D * D / 4; i += blockDim.x) reinterpret_cast<float4*>(Rs)[i] = __ldg(RT + i);
-    const uint16_t* src = (w == 0 ? kin : vin);
-    for (int i = tid; i < nt * D; i += blockDim.x) {
-      const int t = i / D, c = i % D;
-      xs[t * D + c] = bf2f(src[(int64_t)(cs.row_off[ci] + (lo - T_old) + t) * in_stride + (int64_t)kvh * D + c]);
+    if (!mbar_wait(&bar_copy, (unsigned)w)) {
+      if (tid == 0) s_fail = 1;
     }
     __syncthreads();
-    const int ch = tid & 127, th = tid >> 7;
-    float acc[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-    for (int jj = 0; jj < D; jj += 4) {
-      const float r0 = Rs[(jj + 0) * D + ch], r1 = Rs[(jj + 1) * D + ch];
-      const float r2 = Rs[(jj + 2) * D + ch], r3 = Rs[(jj + 3) * D + ch];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float4 x = *reinterpret_cast<const float4*>(xs + (th * 32 + i) * D + jj);
-        float a = acc[i];
-        a = fmaf(x.x, r0, a);
-        a = fmaf(x.y, r1, a);
-        a = fmaf(x.z, r2, a);
-        a = fmaf(x.w, r3, a);
-        acc[i] = a;
-      }
+    if (s_fail) break;
+    if (tid == 0) {
+      tmem_fence_after_sync();
+      for (int p = 0; p < 3; ++p)
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_bf16(tmem + (uint32_t)(w * 128), umma_desc(Xs + kk * 256, 128, 2048),
+                    umma_desc(Rp + p * D * D * 2 + kk * 256, 128, 2048), kBulkIdesc, p > 0 || kk > 0);
+      umma_commit(&bar_mma);
     }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int t = th * 32 + i;
-      if (t < nt) rot[(w * kTileTokens + t) * D + ch] = f2bf(acc[i]);
+    // The next tensor's X and R overwrite the operands: wait for the MMAs.
+    if (!mbar_wait(&bar_mma, (unsigned)w)) {
+      if (tid == 0) s_fail = 1;
     }
+    tmem_fence_after_sync();
+    __syncthreads();
+    if (s_fail) break;
   }
+  if (s_fail) {
+    // A copy or the MMAs did not complete in time: report it, give the
+    // hardware another bounded wait, free the tensor memory and stop.
+    if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -3, (int32_t)MK_ETIMEOUT);
+    (void)mbar_wait(&bar_copy, 0);
+    (void)mbar_wait(&bar_mma, 0);
+    tmem_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+    return;
+  }
+
+  // Epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (tokens), columns of
+  // half w / 4, rounds to bf16 and stores the rows.
+  {
+    const int q = warp & 3, h = warp >> 2;
+    const int t = 32 * q + lane;
+    for (int w = 0; w < 2; ++w)
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        const int col = h * 64 + c * 32;
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(w * 128 + col), v);
+        uint4* dst = reinterpret_cast<uint4*>(rot + ((size_t)w * kTileTokens + t) * kRotRow + col);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            pk[e] = (uint32_t)f2bf(__uint_as_float(v[8 * g + 2 * e])) |
+                    ((uint32_t)f2bf(__uint_as_float(v[8 * g + 2 * e + 1])) << 16);
+          dst[g] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+  }
+  tmem_fence_before_sync();
   __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
 
   uint16_t* sink_k = reinterpret_cast<uint16_t*>(base + L.off_sink_k);
   uint16_t* sink_v = reinterpret_cast<uint16_t*>(base + L.off_sink_v);
@@ -297,8 +367,8 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
   uint16_t* win_v = reinterpret_cast<uint16_t*>(base + L.off_win_v);
   for (int t = warp; t < nt; t += 8) {
     const int p = lo + t;
-    const uint16_t* rk = rot + t * D;
-    const uint16_t* rv = rot + (kTileTokens + t) * D;
+    const uint16_t* rk = rot + (size_t)t * kRotRow;
+    const uint16_t* rv = rot + (size_t)(kTileTokens + t) * kRotRow;
     if (p < S || p >= T_new - W) {
       uint16_t* dk = p < S ? sink_k + (int64_t)p * D : win_k + (int64_t)((p - S) % W) * D;
       uint16_t* dv = p < S ? sink_v + (int64_t)p * D : win_v + (int64_t)((p - S) % W) * D;
@@ -330,7 +400,7 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
       for (int p = st; p < en; ++p) {
         const int t = p - lo;
         const bool kept = (keepk[t * 32 + (c >> 2)] >> (c & 3)) & 1;
-        const float kt = kept ? bf2f(rot[t * D + c]) : 0.0f;
+        const float kt = kept ? bf2f(rot[(size_t)t * kRotRow + c]) : 0.0f;
         if (!have) { mn = kt; mx = kt; have = true; }
         else { mn = fminf(mn, kt); mx = fmaxf(mx, kt); }
       }
@@ -360,16 +430,14 @@ cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, 
 
 cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
                                const uint16_t* v, int total_tiles, cudaStream_t s) {
-  const size_t smem = (size_t)D * D * 4 + (size_t)kTileTokens * D * 4 + 2 * (size_t)kTileTokens * D * 2 +
-                      (size_t)kTileTokens * 32;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_append_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_append_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(total_tiles, L.n_kv);
-  k_append_bulk<<<grid, 256, smem, s>>>(L, layer, cs, k, v);
+  k_append_bulk<<<grid, 256, kBulkSmem, s>>>(L, layer, cs, k, v);
   return cudaGetLastError();
 }
 

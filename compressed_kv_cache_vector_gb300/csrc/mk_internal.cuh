@@ -12,7 +12,7 @@ namespace mk {
 
 constexpr int D = MK_HEAD_DIM;
 constexpr int kDenseChunk = 16;        // tokens per dense work item in attention
-constexpr int kTileTokens = 64;        // tokens per bulk-append tile
+constexpr int kTileTokens = 128;       // tokens per bulk-append tile (one 128-row tensor-core tile)
 constexpr int kSmallAppend = 16;       // largest per-sequence append handled by the decode kernel
 constexpr int kKeyBins = 4096;         // coarse key histogram of the block selection (top 12 key bits)
 constexpr uint32_t FULL = 0xffffffffu;
@@ -47,6 +47,7 @@ struct Layout {
   char* units;                  // first unit region
   int64_t unit_stride;
   int64_t off_rkt, off_rvt, off_rv, off_sink_k, off_sink_v, off_win_k, off_win_v;
+  int64_t off_rkp, off_rvp;     // R_k, R_v as three bf16 parts each, tensor-core operand layout
   int64_t off_meta, off_pages;
   int64_t page_stride;
   int32_t S, W, B, n_kv, G, max_seqs, nblk_cap, cap_tokens, n_layers, k_max;
@@ -109,8 +110,8 @@ __host__ __device__ inline int n_select(const Layout& L, int n_scored) {
   if (k > n_scored) k = n_scored;
   return (int)k;
 }
-// Bulk-append tiles: [T_old, f), [f, f+64), ... with f the first position
-// S + 64j (or S) past T_old, so that every middle block sits in one tile.
+// Bulk-append tiles: [T_old, f), [f, f+128), ... with f the first position
+// S + 128j (or S) past T_old, so that every middle block sits in one tile.
 __host__ __device__ inline int tile_first_boundary(int T_old, int S) {
   if (T_old < S) return S;
   return S + ((T_old - S) / kTileTokens + 1) * kTileTokens;
@@ -207,6 +208,63 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
       : "memory");
   return ok != 0;
 }
+// ---- 5th-generation tensor cores (tcgen05), single CTA --------------------
+// Shared-memory matrix descriptor, K-major operand without swizzle: 8-row x
+// 16-byte core matrices stored contiguously (128 bytes each); lbo = bytes
+// between core matrices adjacent along K, sbo = bytes between 8-row groups.
+__device__ __forceinline__ uint64_t umma_desc(const void* p, unsigned lbo, unsigned sbo) {
+  uint64_t d = (uint64_t)((smem_u32(p) >> 4) & 0x3fffu);
+  d |= (uint64_t)((lbo >> 4) & 0x3fffu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3fffu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version of tcgen05; base offset 0, no swizzle
+  return d;
+}
+// Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier when every MMA issued so far by this thread is done.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+// Whole warp: allocate ncols (power of two >= 32) TMEM columns, address to *dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, unsigned ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, unsigned ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Whole warp: 32 consecutive fp32 columns of this warp's 32 TMEM lanes
+// (lane quarter = warp % 4), one lane per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+// Byte offset of element (row, k) of a 128-column bf16 matrix in the K-major
+// core-matrix layout above (lbo = 128, sbo = 2048).
+__host__ __device__ constexpr int umma_kmajor_offset(int row, int k) {
+  return ((row >> 3) * 16 + (k >> 3)) * 128 + (row & 7) * 16 + (k & 7) * 2;
+}
+
 // Bounded wait for the phase with the given parity to complete: false once
 // 20 ms have passed (far above any real copy time).
 __device__ __forceinline__ uint64_t global_ns() {

@@ -138,11 +138,13 @@ mk_status mk_set_rotation(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_he
  * token leaving the window: per-vector top-r channels by magnitude, ties to
  * the lower channel, stored in ascending channel order ([N] Eq. (9),
  * Algorithm 1; [S] sec. 4.2, 5.1), plus the block's min/max keys.
- * k, v: device bf16 [sum(n_new)][n_kv_heads][128], sequences in call order.
+ * k, v: device bf16 [sum(n_new)][n_kv_heads][128], sequences in call order,
+ * 16-byte aligned when any n_new[i] exceeds 16 (the bulk path, whose rotation
+ * of 128-token tiles runs as a tensor-core GEMM, reads 16-byte vectors).
  * The first append of a sequence is its prefill: it fixes the strategy
  * segments.  seq_ids/n_new are host arrays; n_new[i] >= 0.
  * Errors: MK_ENOMEM if a sequence would pass max_tokens; MK_ESTATE if a
- * rotation is missing; MK_EINVAL for bad ids or duplicates. */
+ * rotation is missing; MK_EINVAL for bad ids, duplicates or misaligned k, v. */
 mk_status mk_append_compress(mk_ctx* ctx, int32_t layer, int32_t n_seqs,
                              const int32_t* seq_ids, const int32_t* n_new,
                              const void* k, const void* v, mk_stream stream);
