@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dense-ref", action="store_true", help="also time the uncompressed reference kernel")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling runs)")
+    ap.add_argument("--separate", action="store_true",
+                    help="append and block selection as two launches (default: mk_append_select, one launch)")
     return ap.parse_args()
 
 
@@ -293,10 +295,15 @@ def main():
         for l in range(L):
             if instrument:
                 binding.record_event(ev[l][0])
-            mk.append(l, seqs, [1] * n_seq, k_in[l], v_in[l])
-            if instrument:
-                binding.record_event(ev[l][1])
-            mk.block_select(l, seqs, q_in[l], *sel[l])
+            if a.separate:
+                mk.append(l, seqs, [1] * n_seq, k_in[l], v_in[l])
+                if instrument:
+                    binding.record_event(ev[l][1])
+                mk.block_select(l, seqs, q_in[l], *sel[l])
+            else:
+                mk.append_select(l, seqs, k_in[l], v_in[l], q_in[l], *sel[l])
+                if instrument:
+                    binding.record_event(ev[l][1])
             if instrument:
                 binding.record_event(ev[l][2])
             mk.decode_attn(l, seqs, *sel[l], out=outs[l])
@@ -400,14 +407,19 @@ def main():
             roofline["traffic"] = tr["bytes_per_launch"]
     except Exception:
         pass
-    phases = {
-        "append_ms": app_avg, "select_ms": sel_avg, "attn_ms": attn_avg,
-        "append_gbs": per["append"] / (app_avg * 1e-3) / 1e9,
-        "select_gbs": per["select"] / (sel_avg * 1e-3) / 1e9,
-        "attn_gbs": achieved,
-        "step_span_ms": statistics.mean(span_ms),
-        "alg_bytes_per_layer": per,
-    }
+    if a.separate:
+        phases = {
+            "append_ms": app_avg, "select_ms": sel_avg, "attn_ms": attn_avg,
+            "append_gbs": per["append"] / (app_avg * 1e-3) / 1e9,
+            "select_gbs": per["select"] / (sel_avg * 1e-3) / 1e9,
+        }
+    else:
+        phases = {
+            "append_select_ms": app_avg + sel_avg, "attn_ms": attn_avg,
+            "append_select_gbs": (per["append"] + per["select"]) / ((app_avg + sel_avg) * 1e-3) / 1e9,
+        }
+    phases.update({"attn_gbs": achieved, "step_span_ms": statistics.mean(span_ms), "alg_bytes_per_layer": per,
+                   "launches_per_layer": 3 if a.separate else 2})
 
     # end to end through the public API with host buffers (eager calls)
     e2e = None
@@ -425,8 +437,11 @@ def main():
                 dk[l].copy_(hk[l], non_blocking=True)
                 dv[l].copy_(hv[l], non_blocking=True)
                 dq[l].copy_(hq[l], non_blocking=True)
-                mk.append(l, seqs, [1] * n_seq, dk[l], dv[l])
-                mk.block_select(l, seqs, dq[l], *sel[l])
+                if a.separate:
+                    mk.append(l, seqs, [1] * n_seq, dk[l], dv[l])
+                    mk.block_select(l, seqs, dq[l], *sel[l])
+                else:
+                    mk.append_select(l, seqs, dk[l], dv[l], dq[l], *sel[l])
                 mk.decode_attn(l, seqs, *sel[l], out=outs[l])
                 ho[l].copy_(outs[l], non_blocking=True)
 
@@ -464,9 +479,11 @@ def main():
     line = dict(base, value=value, ms_per_step=ms,
                 config=dict(wcfg, l2="step reads ~%.2f GB across layers, far above the 129 MB L2" %
                             (step_bytes / 1e9),
-                            timing="CUDA graph of one full step, replayed; CUDA events on the stream"),
+                            timing="CUDA graph of one full step, replayed; CUDA events on the stream",
+                            calls=("mk_append_compress + mk_block_select + mk_decode_attn" if a.separate else
+                                   "mk_append_select + mk_decode_attn") + " per layer"),
                 hbm_gbs=gbs, alg_bytes_per_step=step_bytes, roofline=roofline, phases=phases,
-                cpu_baseline=cpu, e2e=e2e, gpu_launches=4 * L * a.steps, clocks=clk)
+                cpu_baseline=cpu, e2e=e2e, gpu_launches=(3 if a.separate else 2) * L * a.steps, clocks=clk)
     if mk.prefill_ms:
         pm = sorted(mk.prefill_ms)[len(mk.prefill_ms) // 2]
         ntok = sum(wl.seq_lens) * wl.n_kv_heads

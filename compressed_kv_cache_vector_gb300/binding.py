@@ -59,6 +59,7 @@ _SIGS = {
     "mk_set_rotation": [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp],
     "mk_append_compress": [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp],
     "mk_block_select": [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp],
+    "mk_append_select": [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp],
     "mk_decode_attn": [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp],
     "mk_dense_decode_attn": [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_vp],
     "mk_gram": [c_vp, c_i64, c_i64, c_vp, c_vp],
@@ -191,6 +192,15 @@ class MosaicKV:
         _check("mk_block_select", self.lib.mk_block_select(
             self.h, layer, len(seq_ids), _i32(seq_ids), _ptr(q), _ptr(ids), _ptr(n_sel), _ptr(scores),
             _stream(stream)))
+        return ids, n_sel
+
+    def append_select(self, layer, seq_ids, k, v, q, ids=None, n_sel=None, scores=None, stream=None):
+        """One new token per sequence (k, v: [n_seqs, n_kv, 128] bf16) appended, then blocks selected for q."""
+        if ids is None:
+            ids, n_sel = self.alloc_select(len(seq_ids))
+        _check("mk_append_select", self.lib.mk_append_select(
+            self.h, layer, len(seq_ids), _i32(seq_ids), _ptr(k), _ptr(v), _ptr(q), _ptr(ids), _ptr(n_sel),
+            _ptr(scores), _stream(stream)))
         return ids, n_sel
 
     def decode_attn(self, layer, seq_ids, ids, n_sel, out=None, stream=None):

@@ -398,6 +398,42 @@ mk_status mk_block_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int3
   return MK_OK;
 }
 
+mk_status mk_append_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids, const void* k,
+                           const void* v, const void* q, int32_t* ids, int32_t* n_sel, float* scores,
+                           mk_stream stream) {
+  mk_status st = check_seqs(ctx, layer, n_seqs, seq_ids);
+  if (st != MK_OK) return st;
+  if (!k || !v || !q || !ids || !n_sel) return MK_EINVAL;
+  int max_nblk = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq_ids[i];
+    if (ctx->T[ls] == 0) return MK_ESTATE;  // the prefill comes first
+    if ((int64_t)ctx->T[ls] + 1 > ctx->cfg.max_tokens) return MK_ENOMEM;
+    for (int h = 0; h < ctx->cfg.n_kv_heads; ++h)
+      if (!ctx->rot_set[ls * ctx->cfg.n_kv_heads + h]) return MK_ESTATE;
+    max_nblk = std::max(max_nblk, mk::n_mid_blocks(ctx->L, ctx->T[ls] + 1));
+  }
+  CallSeqs* cs = new (std::nothrow) CallSeqs();
+  if (!cs) return MK_ENOMEM;
+  cs->n = n_seqs;
+  for (int i = 0; i < n_seqs; ++i) {
+    const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq_ids[i];
+    cs->seq[i] = seq_ids[i];
+    cs->n_new[i] = 1;
+    cs->row_off[i] = i;
+    cs->T_old[i] = ctx->T[ls];
+  }
+  cudaError_t e = mk::launch_block_select(ctx->L, layer, *cs, static_cast<const uint16_t*>(q), ids, n_sel, scores,
+                                          std::max(1, max_nblk), (cudaStream_t)stream,
+                                          static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v));
+  delete cs;
+  if (e != cudaSuccess) return MK_ECUDA;
+  for (int i = 0; i < n_seqs; ++i) ctx->T[(size_t)layer * ctx->cfg.max_seqs + seq_ids[i]] += 1;
+  ctx->sel_layer = layer;
+  ctx->sel_seqs.assign(seq_ids, seq_ids + n_seqs);
+  return MK_OK;
+}
+
 mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids, const int32_t* ids,
                          const int32_t* n_sel, void* out, mk_stream stream) {
   mk_status st = check_seqs(ctx, layer, n_seqs, seq_ids);

@@ -1,0 +1,176 @@
+// Per-vector compression and the decode-path append body, shared by the
+// append kernels and the fused append + block-selection kernel.
+//
+// Method: "MosaicKV：...阅读笔记" (zhongzhuzhou.org), Eq. (7)/(8) (rotation of
+// each new token), Eq. (9) and Algorithm 1 (per-vector top-r); "MosaicKV:
+// Serving Long-Context LLM with Dynamic Two-D KV Cache Compression"
+// (paperlayer.ai), sec. 4.2 stage 1 and sec. 5.1 (packed contiguous storage).
+#pragma once
+
+#include "mk_internal.cuh"
+
+namespace mk {
+
+// Per-vector top-r of 128 bf16 magnitudes held 4 per lane (channels
+// 4*lane .. 4*lane+3).  Keeps the r largest magnitudes, ties to the lower
+// channel.  Returns this lane's keep bits; rank0 receives the packed position
+// (ascending channel order) of the lane's first kept channel.
+//
+// The r-th largest magnitude t is found by a bitwise search from the most
+// significant bit (the largest t with #{m >= t} >= r); all m > t are kept and
+// the r - #{m > t} lowest channels with m == t.
+__device__ __forceinline__ unsigned warp_topr(const uint32_t m[4], int r, int lane, int& rank0) {
+  uint32_t t = 0;
+#pragma unroll
+  for (int bit = 14; bit >= 0; --bit) {
+    const uint32_t cand = t | (1u << bit);
+    const unsigned c = (unsigned)(m[0] >= cand) + (unsigned)(m[1] >= cand) +
+                       (unsigned)(m[2] >= cand) + (unsigned)(m[3] >= cand);
+    if ((int)__reduce_add_sync(FULL, c) >= r) t = cand;
+  }
+  const unsigned gt = (unsigned)(m[0] > t) + (unsigned)(m[1] > t) + (unsigned)(m[2] > t) + (unsigned)(m[3] > t);
+  const unsigned eq = (unsigned)(m[0] == t) + (unsigned)(m[1] == t) + (unsigned)(m[2] == t) + (unsigned)(m[3] == t);
+  const int need = r - (int)__reduce_add_sync(FULL, gt);
+  int run = warp_excl_scan((int)eq, lane);
+  unsigned keep = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (m[i] > t) {
+      keep |= 1u << i;
+    } else if (m[i] == t) {
+      if (run < need) keep |= 1u << i;
+      ++run;
+    }
+  }
+  rank0 = warp_excl_scan(__popc(keep), lane);
+  return keep;
+}
+
+// Compresses one rotated vector (128 bf16 words at `row`) of middle position
+// `pos` into its page; for a key also folds it into the block's min/max.
+// Called by one full warp.  Returns this lane's keep bits.
+__device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc& ud, char* base, int pos,
+                                                 const uint16_t* row, int is_v, int lane,
+                                                 bool update_meta) {
+  const int m = pos - L.S;
+  const int b = m / L.B;
+  const int t = m - b * L.B;
+  const int r = ud.r[seg_of_block(ud, b)];
+  char* page = base + L.off_pages + (int64_t)b * L.page_stride;
+  const int Br = L.B * r;
+  uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? 3 * Br : 0));
+  uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? 5 * Br : 2 * Br));
+  const uint2 raw = *reinterpret_cast<const uint2*>(row + 4 * lane);
+  uint16_t v[4] = {(uint16_t)(raw.x & 0xffff), (uint16_t)(raw.x >> 16), (uint16_t)(raw.y & 0xffff),
+                   (uint16_t)(raw.y >> 16)};
+  uint32_t mag[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) mag[i] = v[i] & 0x7fffu;
+  int rank;
+  const unsigned keep = warp_topr(mag, r, lane, rank);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (keep >> i & 1u) {
+      val[t * r + rank] = v[i];
+      idx[t * r + rank] = (uint8_t)(4 * lane + i);
+      ++rank;
+    }
+  }
+  if (update_meta) {
+    uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta) + (int64_t)b * 2 * D;
+    uint2 omn = make_uint2(0, 0), omx = make_uint2(0, 0);
+    if (t != 0) {
+      omn = *reinterpret_cast<const uint2*>(meta + 4 * lane);
+      omx = *reinterpret_cast<const uint2*>(meta + D + 4 * lane);
+    }
+    const uint16_t pmn[4] = {(uint16_t)(omn.x & 0xffff), (uint16_t)(omn.x >> 16), (uint16_t)(omn.y & 0xffff),
+                             (uint16_t)(omn.y >> 16)};
+    const uint16_t pmx[4] = {(uint16_t)(omx.x & 0xffff), (uint16_t)(omx.x >> 16), (uint16_t)(omx.y & 0xffff),
+                             (uint16_t)(omx.y >> 16)};
+    uint16_t nmn[4], nmx[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float kt = (keep >> i & 1u) ? bf2f(v[i]) : 0.0f;
+      float lo = kt, hi = kt;
+      if (t != 0) {
+        lo = fminf(bf2f(pmn[i]), kt);
+        hi = fmaxf(bf2f(pmx[i]), kt);
+      }
+      nmn[i] = f2bf(lo);
+      nmx[i] = f2bf(hi);
+    }
+    *reinterpret_cast<uint2*>(meta + 4 * lane) =
+        make_uint2((uint32_t)nmn[0] | ((uint32_t)nmn[1] << 16), (uint32_t)nmn[2] | ((uint32_t)nmn[3] << 16));
+    *reinterpret_cast<uint2*>(meta + D + 4 * lane) =
+        make_uint2((uint32_t)nmx[0] | ((uint32_t)nmx[1] << 16), (uint32_t)nmx[2] | ((uint32_t)nmx[3] << 16));
+  }
+  return keep;
+}
+
+// Decode-path append of n new tokens to one (sequence, kv head) by one CTA of
+// 256 threads: evicts the window tokens that leave it into the middle
+// (select, pack, block min/max), then rotates the first n_rot (0 or n, at
+// most kSmallAppend) new tokens (k' = k R_k^T, v' = v R_v^T with
+// Rs = [R_k^T | R_v^T] in shared memory, possibly still arriving by
+// cp.async) and stores them.  kin/vin point at the unit's first new row;
+// xs: n_rot*2*128 floats and rot: n_rot*2*128 bf16 of shared scratch.
+// Leaves the device length to the caller.  Ends with a barrier.
+__device__ __forceinline__ void append_small_body(const Layout& L, const UnitDesc& ud, char* base, int T_old, int n,
+                                                  int n_rot, const uint16_t* kin, const uint16_t* vin,
+                                                  int64_t in_stride, const float* Rs, float* xs, uint16_t* rot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T_new = T_old + n;
+  const int S = L.S, W = L.W;
+  uint16_t* win_k = reinterpret_cast<uint16_t*>(base + L.off_win_k);
+  uint16_t* win_v = reinterpret_cast<uint16_t*>(base + L.off_win_v);
+
+  // Phase A: window tokens that leave the window, in position order.
+  const int e_lo = max(S, T_old - W), e_hi = min(T_old, T_new - W);
+  if (warp < 2) {
+    for (int e = e_lo; e < e_hi; ++e) {
+      const int slot = (e - S) % W;
+      const uint16_t* row = (warp == 0 ? win_k : win_v) + (int64_t)slot * D;
+      compress_vec(L, ud, base, e, row, warp, lane, warp == 0);
+    }
+  }
+  __syncthreads();
+
+  // Phase B: rotate the new tokens (k' = k R_k^T, v' = v R_v^T).
+  for (int i = tid; i < n_rot * 2 * D; i += blockDim.x) {
+    const int t = i / (2 * D), w = (i / D) & 1, c = i % D;
+    const uint16_t* src = (w == 0 ? kin : vin) + (int64_t)t * in_stride;
+    xs[(t * 2 + w) * D + c] = bf2f(src[c]);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  {
+    // thread (w, ch): channel ch of the rotated key (w = 0) or value (w = 1)
+    const int w = tid >> 7, ch = tid & 127;
+    const float* RT = Rs + w * D * D;
+    for (int i = 0; i < n_rot; ++i) {
+      float acc = 0.0f;
+#pragma unroll 8
+      for (int j = 0; j < D; ++j) acc = fmaf(xs[(i * 2 + w) * D + j], RT[j * D + ch], acc);
+      rot[(i * 2 + w) * D + ch] = f2bf(acc);
+    }
+  }
+  __syncthreads();
+
+  // Route: sinks and window dense, the rest compressed in position order.
+  uint16_t* sink_k = reinterpret_cast<uint16_t*>(base + L.off_sink_k);
+  uint16_t* sink_v = reinterpret_cast<uint16_t*>(base + L.off_sink_v);
+  for (int i = 0; i < n_rot; ++i) {
+    const int p = T_old + i;
+    if (p < S || p >= T_new - W) {
+      uint16_t* dk = p < S ? sink_k + (int64_t)p * D : win_k + (int64_t)((p - S) % W) * D;
+      uint16_t* dv = p < S ? sink_v + (int64_t)p * D : win_v + (int64_t)((p - S) % W) * D;
+      if (tid < D) dk[tid] = rot[(i * 2) * D + tid];
+      else dv[tid - D] = rot[(i * 2 + 1) * D + tid - D];
+    } else if (warp < 2) {
+      compress_vec(L, ud, base, p, rot + (i * 2 + warp) * D, warp, lane, warp == 0);
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace mk

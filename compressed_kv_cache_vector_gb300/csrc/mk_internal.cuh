@@ -328,9 +328,11 @@ cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, c
                                const uint16_t* v, int total_tiles, cudaStream_t s);
 // Whether the block selection can handle the context's largest block count.
 bool select_plan_ok(const Layout& L);
+// kin/vin non-null: append one new token per sequence first (fused decode
+// append, see k_select).
 cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,
                                 int32_t* ids, int32_t* n_sel, float* scores_out, int max_nblk,
-                                cudaStream_t s);
+                                cudaStream_t s, const uint16_t* kin = nullptr, const uint16_t* vin = nullptr);
 // max_items: the largest number of attention work items (16-token dense
 // chunks + selected/always pages) of any (sequence, kv head) in the call.
 cudaError_t launch_decode_attn(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids,

@@ -32,7 +32,7 @@
 //    it and its time is latency, not bandwidth.
 #include <algorithm>
 
-#include "mk_internal.cuh"
+#include "mk_append_body.cuh"
 
 namespace mk {
 
@@ -44,7 +44,7 @@ constexpr int kMetaTile = kMT * kMetaRow * 2; // bytes per staged tile
 constexpr int kSelSmem = kSelWarps * 2 * kMetaTile;  // double-buffered tiles (also holds R_k^T)
 constexpr int kSelSmemMax = 192 * 1024;              // dynamic shared memory cap (top-k key staging)
 constexpr int kFineBins = 1024;
-static_assert(kSelSmem >= D * D * 4, "R_k^T staging fits in the tile area");
+static_assert(kSelSmem >= 2 * D * D * 4 + 2 * D * 4 + 2 * D * 2, "R_k^T, R_v^T and the append scratch fit in the tile area");
 
 // Top-k plan for nblk keys: each thread owns CPT 16-byte chunks (4 keys),
 // CPT a multiple of 8; the keys are staged in shared memory when they fit
@@ -162,7 +162,7 @@ __device__ __forceinline__ void find_bin(const uint32_t* h, int rem, int2* wsum,
 //    when fewer than `need` ties precede it.  The counts before a key come
 //    from per-round per-warp totals and a warp scan of packed counts.
 constexpr int kRoundsMax = 16;
-constexpr int SC_CNT = 0, SC_G = 16, SC_GN = 272, SC_THR = 273, SC_WT = 280, SC_BT = 280 + 8 * kRoundsMax;
+constexpr int SC_CNT = 0, SC_G = 16, SC_GN = 276, SC_THR = 277, SC_WT = 280, SC_BT = 280 + 8 * kRoundsMax;  // SC_G: 256 keys + 4 pad
 static_assert(SC_BT + 8 * kRoundsMax <= 1024, "scratch");
 __device__ void topk_loop(const uint4* ks, int nch, int nblk, int k, bool all, const uint32_t* hc, uint32_t* sc,
                           int2* wsum, int* s_bin, int* s_rem, int32_t* out, int k_max) {
@@ -183,7 +183,7 @@ __device__ void topk_loop(const uint4* ks, int nch, int nblk, int k, bool all, c
     int c = 0;
     if (x <= 0xffffffffull) {
       const uint32_t xx = (uint32_t)x;
-#pragma unroll 1
+#pragma unroll 4
       for (int j = 0; j < rounds; ++j) {
         const uint4 v = chunk(j);
         c += (v.x >= xx) + (v.y >= xx) + (v.z >= xx) + (v.w >= xx);
@@ -192,11 +192,10 @@ __device__ void topk_loop(const uint4* ks, int nch, int nblk, int k, bool all, c
     c = (int)__reduce_add_sync(FULL, (unsigned)c);
     if (lane == 0) sc[SC_CNT + par * 8 + warp] = (uint32_t)c;
     __syncthreads();
-    int t = 0;
-#pragma unroll 1
-    for (int w = 0; w < 8; ++w) t += (int)sc[SC_CNT + par * 8 + w];
+    const uint4 c0 = *reinterpret_cast<const uint4*>(sc + SC_CNT + par * 8);
+    const uint4 c1 = *reinterpret_cast<const uint4*>(sc + SC_CNT + par * 8 + 4);
     par ^= 1;
-    return t;
+    return (int)((c0.x + c0.y) + (c0.z + c0.w) + (c1.x + c1.y) + (c1.z + c1.w));
   };
 
   uint32_t thr = 1u;  // every candidate (key >= 1) when all are taken
@@ -208,7 +207,7 @@ __device__ void topk_loop(const uint4* ks, int nch, int nblk, int k, bool all, c
     int c_hi = k - *s_rem;             // keys above hi
     int c_lo = c_hi + (int)hc[b];      // keys >= lo
     bool bisect = false;
-    while (lo < hi && c_lo - c_hi > 256) {
+    while (lo < hi && c_lo - c_hi > 64) {
       uint64_t x;
       if (bisect) {
         x = lo + (hi - lo + 1) / 2;
@@ -232,7 +231,7 @@ __device__ void topk_loop(const uint4* ks, int nch, int nblk, int k, bool all, c
       bisect = !bisect && (hi - lo) > w0 / 2;
     }
     if (lo < hi) {
-      // At most 256 keys lie in [lo, hi]: gather and rank them.
+      // At most 64 keys lie in [lo, hi]: gather and rank them.
       if (tid == 0) sc[SC_GN] = 0u;
       __syncthreads();
 #pragma unroll 1
@@ -240,20 +239,30 @@ __device__ void topk_loop(const uint4* ks, int nch, int nblk, int k, bool all, c
         const uint4 v = chunk(j);
         const uint32_t e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (e[q] >= lo && e[q] <= hi) sc[SC_G + atomicAdd(&sc[SC_GN], 1u)] = e[q];
+        for (int q = 0; q < 4; ++q) {
+          const bool in = e[q] >= lo && e[q] <= hi;
+          const unsigned bal = __ballot_sync(FULL, in);
+          if (bal) {
+            unsigned pos = 0u;
+            if (lane == 0) pos = atomicAdd(&sc[SC_GN], (unsigned)__popc(bal));
+            pos = __shfl_sync(FULL, pos, 0) + (unsigned)__popc(bal & ((1u << lane) - 1u));
+            if (in) sc[SC_G + pos] = e[q];
+          }
+        }
       }
       __syncthreads();
       const int m = (int)sc[SC_GN];
+      if (tid < 3) sc[SC_G + m + tid] = 0u;  // pad to whole 16-byte words (0 is never a candidate key)
+      __syncthreads();
       const int want = k - c_hi;  // rank of the threshold among them (1 = largest)
       if (tid < m) {
         const uint32_t key = sc[SC_G + tid];
         int gt = 0, eq = 0;
-#pragma unroll 4
-        for (int i = 0; i < m; ++i) {
-          const uint32_t o = sc[SC_G + i];
-          gt += o > key;
-          eq += o == key;
+#pragma unroll 2
+        for (int i = 0; i < m; i += 4) {
+          const uint4 o = *reinterpret_cast<const uint4*>(sc + SC_G + i);
+          gt += (o.x > key) + (o.y > key) + (o.z > key) + (o.w > key);
+          eq += (o.x == key) + (o.y == key) + (o.z == key) + (o.w == key);
         }
         if (gt < want && gt + eq >= want) sc[SC_THR] = key;
       }
@@ -278,7 +287,7 @@ __device__ void topk_loop(const uint4* ks, int nch, int nblk, int k, bool all, c
     }
   };
   // Per round: warp totals of (above, ties), packed as above | ties << 16.
-#pragma unroll 1
+#pragma unroll 4
   for (int j = 0; j < rounds; ++j) {
     uint32_t gm, em;
     masks(j, gm, em);
@@ -338,11 +347,18 @@ __device__ void topk_loop(const uint4* ks, int nch, int nblk, int k, bool all, c
 }  // namespace
 
 // grid: P CTAs per (sequence, kv head) of the call; 256 threads.
-template <int G>
+// With APPEND, the kernel first appends one new token per sequence (the
+// decode step's append, fused): CTA 0 of each unit evicts the window token
+// that leaves the window, rotates and stores the new one, and scores the
+// unit's last tiles afterwards (the evicted token lands in the last block);
+// the last CTA of the unit advances the device length.  kin/vin:
+// [n_seqs][n_kv][128] bf16.
+template <int G, bool APPEND>
 __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs cs, int P,
                                                    const uint16_t* __restrict__ q, int32_t* __restrict__ ids,
                                                    int32_t* __restrict__ n_sel, float* __restrict__ scores_out,
-                                                   int dyn_bytes) {
+                                                   int dyn_bytes, const uint16_t* __restrict__ kin,
+                                                   const uint16_t* __restrict__ vin) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ float qs[G][D];
   __shared__ float qr[2][G][D];
@@ -365,8 +381,10 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   for (int i = tid; i < kKeyBins / 4; i += blockDim.x) reinterpret_cast<uint4*>(hc)[i] = make_uint4(0, 0, 0, 0);
   const char* base = unit_base(L, u);
   {
+    // R_k^T (and, for the appending CTA, R_v^T right after it in the unit).
+    const int nmat = (APPEND && part == 0) ? 2 : 1;
     const float4* src = reinterpret_cast<const float4*>(base + L.off_rkt);
-    for (int i = tid; i < D * D / 4; i += blockDim.x) cp_async16(reinterpret_cast<float4*>(smem) + i, src + i);
+    for (int i = tid; i < nmat * D * D / 4; i += blockDim.x) cp_async16(reinterpret_cast<float4*>(smem) + i, src + i);
     cp_async_commit();
     cp_async_wait_all();
   }
@@ -425,10 +443,30 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   __syncthreads();  // also: the R_k^T area becomes the tile stages
   if (s_abort) return;
 
-  const int nblk = n_mid_blocks(L, ud.T);
+  int T_cur = ud.T;
+  if (APPEND) {
+    const int n = cs.n_new[ci];
+    if (T_cur + n > L.cap_tokens) {
+      if (part == 0 && tid == 0) set_error(L, ERR_CAPACITY, (int32_t)u, T_cur + n);
+      return;
+    }
+    if (part == 0) {
+      const int64_t in_stride = (int64_t)L.n_kv * D;
+      const int64_t row0 = (int64_t)cs.row_off[ci] * in_stride + (int64_t)kvh * D;
+      float* xs = reinterpret_cast<float*>(smem + 2 * D * D * 4);
+      uint16_t* rot = reinterpret_cast<uint16_t*>(xs + n * 2 * D);
+      append_small_body(L, ud, const_cast<char*>(base), T_cur, n, n, kin + row0, vin + row0, in_stride,
+                        reinterpret_cast<const float*>(smem), xs, rot);
+      __threadfence();  // the updated block min/max before this CTA's own tiles are read
+    }
+    T_cur += n;
+  }
+  const int nblk = n_mid_blocks(L, T_cur);
   const int ntiles = (nblk + kMT - 1) / kMT;
   const int tper = (ntiles + P - 1) / P;
-  const int t0 = part * tper, t1 = min(ntiles, t0 + tper);
+  // With APPEND, CTA 0 takes the last tiles (after its own append).
+  const int t1 = APPEND ? max(0, ntiles - part * tper) : min(ntiles, part * tper + tper);
+  const int t0 = APPEND ? max(0, t1 - tper) : part * tper;
   const uint16_t* meta = reinterpret_cast<const uint16_t*>(base + L.off_meta);
   uint32_t* kw = L.keys + slot * L.keys_stride;
   float* so = scores_out ? scores_out + ((int64_t)ci * L.n_kv + kvh) * L.nblk_cap : nullptr;
@@ -508,6 +546,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   }
   __syncthreads();
   if (!s_last) return;
+  if (APPEND && tid == 0) L.desc[u].T = T_cur;  // every CTA of the unit has read the old length
   __threadfence();
 
   const int n_cand = n_scored_blocks(ud, nblk);
@@ -648,27 +687,30 @@ bool select_plan_ok(const Layout& L) {
 
 cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,
                                 int32_t* ids, int32_t* n_sel, float* scores_out, int max_nblk,
-                                cudaStream_t s) {
+                                cudaStream_t s, const uint16_t* kin, const uint16_t* vin) {
   const int units = cs.n * L.n_kv;
   const int tiles = (max_nblk + kMT - 1) / kMT;
   int P = std::max(1, 152 / units);
   P = std::min(P, std::max(1, (tiles + kSelWarps - 1) / kSelWarps));
   const dim3 grid(units * P);
   // Dynamic shared memory: the meta tile stages, or the top-k's keys and
-  // masks for the context's largest block count, whichever is larger.
+  // masks for the context's largest block count, whichever is larger (the
+  // tile stages also hold R_k^T and R_v^T plus the append scratch).
   const int cpt = topk_cpt(L.nblk_cap);
   const int64_t want = (int64_t)16 * ((L.nblk_cap + 3) / 4) + topk_mask_bytes(cpt);
   const int dyn = (int)std::max<int64_t>(kSelSmem, std::min<int64_t>(kSelSmemMax, want));
-#define MK_SEL_CASE(GG)                                                                                      \
-  case GG: {                                                                                                 \
-    static int set = 0;                                                                                      \
-    if (set < dyn) {                                                                                         \
-      cudaError_t e = cudaFuncSetAttribute(k_select<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);  \
-      if (e != cudaSuccess) return e;                                                                        \
-      set = dyn;                                                                                             \
-    }                                                                                                        \
-    return launch_pdl(k_select<GG>, grid, dim3(256), dyn, s, 0, L, layer, cs, P, q, ids, n_sel, scores_out, \
-                      dyn);                                                                                  \
+  const bool append = kin != nullptr;
+#define MK_SEL_CASE(GG)                                                                                       \
+  case GG: {                                                                                                  \
+    static int set[2] = {0, 0};                                                                               \
+    auto kern = append ? k_select<GG, true> : k_select<GG, false>;                                             \
+    if (set[append] < dyn) {                                                                                  \
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);           \
+      if (e != cudaSuccess) return e;                                                                         \
+      set[append] = dyn;                                                                                      \
+    }                                                                                                         \
+    return launch_pdl(kern, grid, dim3(256), dyn, s, 0, L, layer, cs, P, q, ids, n_sel, scores_out, dyn, kin, \
+                      vin);                                                                                   \
   }
   switch (L.G) {
     MK_SEL_CASE(1)

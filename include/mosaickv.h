@@ -149,6 +149,20 @@ mk_status mk_append_compress(mk_ctx* ctx, int32_t layer, int32_t n_seqs,
                              const int32_t* seq_ids, const int32_t* n_new,
                              const void* k, const void* v, mk_stream stream);
 
+/* The decode step's append and block selection in one launch: appends one
+ * new token to each listed sequence (as mk_append_compress with n_new = 1)
+ * and then selects its blocks for the query q (as mk_block_select), with the
+ * same results as those two calls in a row.  k, v: device bf16
+ * [n_seqs][n_kv_heads][128] (one row per sequence, in call order); q, ids,
+ * n_sel, scores as for mk_block_select.  Every sequence must hold its prefill
+ * already.  One kernel does both: the append of each (sequence, kv head) runs
+ * in the CTA that scores the blocks its evicted token can change.  This is
+ * not a step of the pages' method, only a fusion of two of its steps.
+ * Errors: those of the two calls it replaces. */
+mk_status mk_append_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
+                           const void* k, const void* v, const void* q, int32_t* ids,
+                           int32_t* n_sel, float* scores, mk_stream stream);
+
 /* Scores every middle block of each (sequence, kv head) from its min/max
  * keys and the rotated query q' = q R_k^T:
  *   s_b = max_h (1/sqrt(d)) sum_j max(q'_hj mn_bj, q'_hj mx_bj)

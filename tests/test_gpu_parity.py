@@ -324,3 +324,66 @@ def test_repeatable_bytes():
         out = p.mk.decode_attn(0, [0], ids, n_sel)
         outs.append(bits(out))
     assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("case", [
+    Case(n_q=8, n_kv=2, seq_lens=[3000, 700], rot="eigh", oracle_units=[], seed=21),
+    Case(n_q=4, n_kv=1, seq_lens=[4000, 1200, 300], rot="eigh", block=16, window=128,
+         segments=[(0, 32, 0), (350, 64, 1), (650, 32, 0)], oracle_units=[], seed=22),
+    Case(n_q=4, n_kv=2, seq_lens=[40, 70], rot="eigh", window=64, oracle_units=[], seed=23),
+], ids=["gqa4-2seq", "serving-segments", "filling-window"])
+def test_append_select_equals_separate_calls(case):
+    """The fused decode append + block selection gives the ids, the stored
+    state and the attention output of the two calls it replaces, step after
+    step (evicted tokens cross block boundaries and fill partial blocks)."""
+    n_steps = 40
+    case.steps = [1] * n_steps
+    a, b = Pair(case), Pair(case)
+    seqs = list(range(len(case.seq_lens)))
+    for step in range(n_steps):
+        rows = [torch.stack([a.K[(0, s, h)][a.T[s]] for h in range(case.n_kv)]) for s in seqs]
+        k = torch.stack(rows).contiguous()
+        v = torch.stack([torch.stack([a.V[(0, s, h)][a.T[s]] for h in range(case.n_kv)]) for s in seqs]).contiguous()
+        q = a.query(100 + step)
+        a.mk.append(0, seqs, [1] * len(seqs), k, v)
+        ids_a, ns_a = a.mk.block_select(0, seqs, q)
+        ids_b, ns_b = b.mk.append_select(0, seqs, k, v, q)
+        out_a = a.mk.decode_attn(0, seqs, ids_a, ns_a)
+        out_b = b.mk.decode_attn(0, seqs, ids_b, ns_b)
+        torch.cuda.synchronize()
+        for s in seqs:
+            a.T[s] += 1
+        ns = ns_a.cpu().numpy()
+        assert np.array_equal(ns, ns_b.cpu().numpy()), step
+        ia, ib = ids_a.cpu().numpy(), ids_b.cpu().numpy()
+        for s in seqs:
+            for h in range(case.n_kv):
+                assert np.array_equal(ia[s, h, :ns[s, h]], ib[s, h, :ns[s, h]]), (step, s, h)
+        assert np.array_equal(bits(out_a), bits(out_b)), step
+    assert a.mk.poll_error() == (0, 0) and b.mk.poll_error() == (0, 0)
+    a.mk.sync_state()
+    b.mk.sync_state()
+    for s in seqs:
+        T = a.mk.seq_length(0, s)
+        assert T == b.mk.seq_length(0, s) == case.seq_lens[s] + n_steps
+        for h in range(case.n_kv):
+            va, vb = a.mk.unit_views(0, s, h), b.mk.unit_views(0, s, h)
+            L = va["layout"]
+            S, W, B = case.n_sink, case.window, case.block
+            n_sink = min(S, T)
+            if n_sink:
+                assert np.array_equal(bits(va["sink_k"])[:n_sink], bits(vb["sink_k"])[:n_sink])
+            for p in range(max(S, T - W), T):
+                sl = (p - S) % W
+                assert np.array_equal(bits(va["win_k"])[sl], bits(vb["win_k"])[sl]), p
+                assert np.array_equal(bits(va["win_v"])[sl], bits(vb["win_v"])[sl]), p
+            mid = max(0, T - S - W)
+            nb = (mid + B - 1) // B
+            assert np.array_equal(bits(va["meta"])[:nb], bits(vb["meta"])[:nb])
+            pa, pb = va["pages"].cpu().numpy(), vb["pages"].cpu().numpy()
+            for blk in range(nb):
+                seg = [i for i, f in enumerate(L["seg_first_block"]) if blk >= f][-1]
+                r = case.segments[seg][1]
+                n_live = min(B, mid - blk * B)
+                for g, w_ in zip(page_rows(pa[blk], B, r, n_live), page_rows(pb[blk], B, r, n_live)):
+                    assert np.array_equal(g, w_), (s, h, blk)
