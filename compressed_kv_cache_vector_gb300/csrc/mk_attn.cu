@@ -177,8 +177,9 @@ size_t attn_smem_bytes(const Layout& L, int) { return smem_for(L, L.attn_nst, L.
 // Largest number of CTAs per unit whose partials the merging CTA can stage
 // (next to the merged o', the un-rotation slices and R_v).
 int attn_max_parts(const Layout& L) {
-  const int64_t avail = (int64_t)L.attn_nc * per_warp_bytes(L, L.attn_nst) -
-                        (int64_t)(1 + L.attn_nc / 4) * L.G * D * 4 - (int64_t)D * D * 4 - 64;  // o', slices, R_v
+  const int64_t dump = ((int64_t)L.attn_nc * L.G * D * 4 + 15) / 16 * 16;
+  const int64_t avail = (int64_t)L.attn_nc * per_warp_bytes(L, L.attn_nst) - dump - (int64_t)D * D * 4 -
+                        (int64_t)(1 + L.attn_nc / 4) * L.G * D * 4 - 64;  // dump, R_v, o', slices
   return (int)std::max<int64_t>(1, std::min<int64_t>(MK_MAX_SPLITS, avail / ((int64_t)L.G * (D + 2) * 4)));
 }
 
@@ -196,11 +197,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   unsigned char* warp_area = smem;                                       // [kWarps][pwb]
   float* mlw = reinterpret_cast<float*>(smem + kWarps * pwb);            // [kWarps][8][2]
   uint16_t* zrow = reinterpret_cast<uint16_t*>(mlw + kWarps * 16);      // one zero row (272 B)
-  __shared__ UnitDesc ud;
+  __shared__ __align__(16) UnitDesc ud;
   __shared__ int s_abort, s_ns, s_last;
   __shared__ float s_m[8], s_l[8];
   __shared__ int32_t s_ids[kIdsCap];
-  __shared__ uint64_t s_bar;          // the merging CTA's staging barrier  // this CTA's selected block ids (its j-th item: ids[part + j P])
+  __shared__ uint64_t s_bar, s_bar2;  // R_v staging (every CTA), partials staging (the merging CTA)  // this CTA's selected block ids (its j-th item: ids[part + j P])
 
   const int unit_call = blockIdx.x / P;
   const int part = blockIdx.x - unit_call * P;
@@ -217,14 +218,34 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     for (int i = tid; i < D * D * 4 / 128; i += blockDim.x) prefetch_l2(rv + (size_t)i * 128);
   }
   for (int i = tid; i < kRow / 8; i += blockDim.x) reinterpret_cast<uint4*>(zrow)[i] = make_uint4(0, 0, 0, 0);
+  // Barriers before the wait point (their init fence stays off the critical path).
+  unsigned char* const my_area0 = warp_area + (size_t)warp * pwb;
+  uint64_t* const bars0 = reinterpret_cast<uint64_t*>(my_area0 + (size_t)NST * SB + 2 * kTileBytes);
+  if (lane == 0) {
+    for (int i = 0; i < NST; ++i) mbar_init(&bars0[i], 1);
+    if (tid == 0) {
+      mbar_init(&s_bar, 1);
+      mbar_init(&s_bar2, 1);
+    }
+    mbar_init_fence();
+  }
   pdl_wait();
   pdl_trigger();
   // One round of independent loads (L2 path: the previous kernel wrote them):
   // state, selection count, this CTA's block ids, q'.
   if (tid == 0) {
-    s_abort = has_error(L);
-    if (!DENSE) ud = L.desc[u];
-    s_ns = DENSE ? 0 : __ldcg(n_sel_in + (int64_t)ci * L.n_kv + kvh);
+    // all three loads in flight before the first use
+    const int32_t err = __ldcg(L.err);
+    uint4 dd[4] = {};
+    if (!DENSE)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dd[i] = __ldcg(reinterpret_cast<const uint4*>(L.desc + u) + i);
+    const int32_t ns0 = DENSE ? 0 : __ldcg(n_sel_in + (int64_t)ci * L.n_kv + kvh);
+    s_abort = err;
+    if (!DENSE)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(&ud)[i] = dd[i];
+    s_ns = ns0;
   }
   if (!DENSE)
     for (int j = tid; j < kIdsCap && part + j * P < L.k_max; j += blockDim.x) s_ids[j] = __ldcg(my_ids + part + j * P);
@@ -375,11 +396,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   };
   auto has_copy = [](const Task& t) { return t.kind == 1 || t.kind == 2; };
 
-  if (lane == 0) {
-    for (int i = 0; i < NST; ++i) mbar_init(&bars[i], 1);
-    mbar_init_fence();
-  }
-  __syncwarp();
   // Ring of NST stages: the task being consumed sits in stage st, the next
   // NST - 1 tasks are in flight.  ph: parity of each stage's next phase;
   // pend: stages with copies in flight.
@@ -562,23 +578,31 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   const bool col_ok0 = 2 * tig < G && (G == 8 || tig < 2), col_ok1 = 2 * tig + 1 < G && (G == 8 || tig < 2);
 
   // ---- warps -> CTA partial ------------------------------------------------
-  if (!DENSE && warp == 0) {  // the merging CTA stages R_v soon: bring it back into L2
-    const char* rv = base + L.off_rv;
-    for (int i = lane; i < D * D * 4 / 128; i += 32) prefetch_l2(rv + (size_t)i * 128);
-  }
   if (tig == 0) {
     mlw[(warp * 8 + g) * 2] = m_run;
     mlw[(warp * 8 + g) * 2 + 1] = l_run;
   }
   __syncthreads();
+  // Every CTA stages R_v above the dump area now (the merging CTA, which is
+  // not known yet, then has it at hand); a CTA that turns out not to merge
+  // waits for the copy before it exits.
+  const size_t dump_bytes = ((size_t)kWarps * G * D * 4 + 15) / 16 * 16;
+  float* rvs = reinterpret_cast<float*>(warp_area + dump_bytes);
+  if (!DENSE && tid == 0) {
+    fence_proxy_async();  // the stages and tiles were written by the main loop
+    mbar_expect_tx(&s_bar, (unsigned)(D * D * 4));
+    bulk_g2s(rvs, base + L.off_rv, (unsigned)(D * D * 4), &s_bar);
+  }
   float* dump = reinterpret_cast<float*>(warp_area);  // [kWarps][G][D] (main loop is over)
   {
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
     float M0 = -INFINITY, M1 = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) {
-      M0 = fmaxf(M0, mlw[(w * 8 + h0) * 2]);
-      M1 = fmaxf(M1, mlw[(w * 8 + h1) * 2]);
-    }
+#pragma unroll
+    for (int w = 0; w < kMaxWarps; ++w)
+      if (w < kWarps) {
+        M0 = fmaxf(M0, mlw[(w * 8 + h0) * 2]);
+        M1 = fmaxf(M1, mlw[(w * 8 + h1) * 2]);
+      }
     const float mw0 = mlw[(warp * 8 + h0) * 2], mw1 = mlw[(warp * 8 + h1) * 2];
     const float e0 = mw0 != -INFINITY ? exp2f(mw0 - M0) : 0.0f;
     const float e1 = mw1 != -INFINITY ? exp2f(mw1 - M1) : 0.0f;
@@ -596,17 +620,16 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
       }
     }
   }
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mlw[(w * 8 + tid) * 2]);
-    float ls = 0.0f;
-    if (M != -INFINITY)
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = mlw[(w * 8 + tid) * 2];
-        if (mw != -INFINITY) ls += mlw[(w * 8 + tid) * 2 + 1] * exp2f(mw - M);
-      }
-    s_m[tid] = M;
-    s_l[tid] = ls;
+  for (int h = warp; h < G; h += kWarps) {
+    // warp h: head h's (m, l) over the CTA's warps, lanes = warps
+    const float mw = lane < kWarps ? mlw[(lane * 8 + h) * 2] : -INFINITY;
+    const float lw = lane < kWarps ? mlw[(lane * 8 + h) * 2 + 1] : 0.0f;
+    const float M = warp_max(mw);
+    const float ls = warp_sum(mw != -INFINITY ? lw * exp2f(mw - M) : 0.0f);
+    if (lane == 0) {
+      s_m[h] = M;
+      s_l[h] = ls;
+    }
   }
   __syncthreads();
   float* pacc = L.part_acc + slot * MK_MAX_SPLITS * G * D;   // [part][G][D]
@@ -614,7 +637,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   for (int i = tid; i < G * D; i += blockDim.x) {
     float a = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) a += dump[(size_t)w * G * D + i];
+    for (int w = 0; w < kMaxWarps; ++w)
+      if (w < kWarps) a += dump[(size_t)w * G * D + i];
     pacc[(size_t)part * G * D + i] = a;
   }
   if (tid < G) {
@@ -629,52 +653,58 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     if (prev == P - 1) L.counters[slot] = 0;
   }
   __syncthreads();
-  if (!s_last || s_abort) return;
+  if (!s_last || s_abort) {
+    if (!DENSE) (void)mbar_wait(&s_bar, 0);  // no bulk copy may still be landing in this CTA's memory
+    return;
+  }
   __threadfence();
 
   // ---- the last CTA: merge the P partials, un-rotate, store ----------------
-  // Shared memory: o' [G][D] | slice sums [kSlices][G][D] | R_v [D][D] |
-  // partials [P][G][D] | (m, l) [P][G][2]; R_v and the partials arrive in one
-  // cp.async burst (R_v sits in L2: part 0 prefetched it).
-  float* ofull = reinterpret_cast<float*>(warp_area);
+  // Shared memory: dump [kWarps][G][D] | R_v [D][D] (already staged) | o' [G][D]
+  // | slice sums [kSlices][G][D] | partials [P][G][D] | (m, l) [P][G][2].
+  float* ofull = rvs + (DENSE ? 0 : D * D);
   float* red = ofull + G * D;
-  float* rvs = red + kSlices * G * D;
-  float* sacc = rvs + (DENSE ? 0 : D * D);
+  float* sacc = red + kSlices * G * D;
   float* sml = sacc + (size_t)P * G * D;
   {
-    const unsigned b_rv = DENSE ? 0u : (unsigned)(D * D * 4), b_acc = (unsigned)(P * G * D * 4);
-    const unsigned b_ml = ((unsigned)(P * G * 2 * 4) + 15u) & ~15u;
+    const unsigned b_acc = (unsigned)(P * G * D * 4), b_ml = ((unsigned)(P * G * 2 * 4) + 15u) & ~15u;
     if (tid == 0) {
-      mbar_init(&s_bar, 1);
-      mbar_init_fence();
-      fence_proxy_async_all();  // shared area written by the main loop, partials by the generic proxy
-      mbar_expect_tx(&s_bar, b_rv + b_acc + b_ml);
-      if (!DENSE) bulk_g2s(rvs, base + L.off_rv, b_rv, &s_bar);
-      bulk_g2s(sacc, pacc, b_acc, &s_bar);
-      bulk_g2s(sml, pml, b_ml, &s_bar);
+      fence_proxy_async_all();  // partials written through the generic proxy
+      mbar_expect_tx(&s_bar2, b_acc + b_ml);
+      bulk_g2s(sacc, pacc, b_acc, &s_bar2);
+      bulk_g2s(sml, pml, b_ml, &s_bar2);
     }
-    __syncthreads();
-    if (!mbar_wait(&s_bar, 0)) {
+    const bool ok = mbar_wait(&s_bar2, 0) && (DENSE || mbar_wait(&s_bar, 0));
+    if (!ok) {
       if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -1, (int32_t)MK_ETIMEOUT);
-      (void)mbar_wait(&s_bar, 0);
+      (void)mbar_wait(&s_bar2, 0);
+      if (!DENSE) (void)mbar_wait(&s_bar, 0);
       return;
     }
   }
   // Per (partial, head) weight exp2(m_p - M) / l, computed once; written over
   // the m entries.
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int p = 0; p < P; ++p) M = fmaxf(M, sml[(p * G + tid) * 2]);
-    float ls = 0.0f;
-    if (M != -INFINITY)
-      for (int p = 0; p < P; ++p) {
-        const float mp = sml[(p * G + tid) * 2];
-        if (mp != -INFINITY) ls += sml[(p * G + tid) * 2 + 1] * exp2f(mp - M);
-      }
+  for (int h = warp; h < G; h += kWarps) {
+    // warp h: head h over the partials, lanes p, p + 32 (P <= 64)
+    float mp[2], lp[2];
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int p = lane + 32 * k2;
+      mp[k2] = p < P ? sml[(p * G + h) * 2] : -INFINITY;
+      lp[k2] = p < P ? sml[(p * G + h) * 2 + 1] : 0.0f;
+    }
+    const float M = warp_max(fmaxf(mp[0], mp[1]));
+    float part_l = 0.0f;
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2)
+      if (mp[k2] != -INFINITY) part_l += lp[k2] * exp2f(mp[k2] - M);
+    const float ls = warp_sum(part_l);
     const float inv = (M != -INFINITY && ls > 0.0f) ? 1.0f / ls : 0.0f;
-    for (int p = 0; p < P; ++p) {
-      const float mp = sml[(p * G + tid) * 2];
-      sml[(p * G + tid) * 2] = (mp != -INFINITY && inv != 0.0f) ? exp2f(mp - M) * inv : 0.0f;
+    __syncwarp();
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int p = lane + 32 * k2;
+      if (p < P) sml[(p * G + h) * 2] = (mp[k2] != -INFINITY && inv != 0.0f) ? exp2f(mp[k2] - M) * inv : 0.0f;
     }
   }
   __syncthreads();
