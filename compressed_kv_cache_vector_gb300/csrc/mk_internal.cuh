@@ -328,6 +328,11 @@ cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, c
                                const uint16_t* v, int total_tiles, cudaStream_t s);
 // Whether the block selection can handle the context's largest block count.
 bool select_plan_ok(const Layout& L);
+bool topk_plan_ok(const Layout& L);
+// The top-k kernel behind the scoring kernel (append: the scoring kernel
+// appended cs.n_new tokens; the top-k kernel then advances the lengths).
+cudaError_t launch_topk(const Layout& L, int layer, const CallSeqs& cs, int32_t* ids, int32_t* n_sel, bool append,
+                        cudaStream_t s);
 // kin/vin non-null: append one new token per sequence first (fused decode
 // append, see k_select).
 cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,

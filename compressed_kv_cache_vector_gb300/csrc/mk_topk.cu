@@ -1,0 +1,332 @@
+// Top-k block selection over the block-score keys of each (sequence, kv
+// head): the k largest scores, ties to the lower block id, ids ascending.
+//
+// Method: "MosaicKV：...阅读笔记" (zhongzhuzhou.org), Eq. (12) (the k blocks
+// with the largest bound are attended); "MosaicKV: Serving Long-Context LLM
+// with Dynamic Two-D KV Cache Compression" (paperlayer.ai), sec. 4.2 stage 2
+// (top-k token blocks before each decode attention layer).
+//
+// GB300 structure: one CTA of 1024 threads per (sequence, kv head), launched
+// right behind the scoring kernel (programmatic dependent launch).  The
+// scoring kernel leaves, per unit, an order-preserving 32-bit key per block
+// (0 = not a candidate) and a 4096-bin histogram of the keys' top 12 bits.
+//  * One bulk copy each stages the histogram and the keys; thread t takes
+//    the 16-byte chunks j * 1024 + t (round j), so every read of a round is
+//    conflict free and the block's key order is (j, t).
+//  * Threshold: the histogram's coarse bin brackets the k-th key; counting
+//    passes (interpolated in count space, a bisection step whenever one
+//    shrank the bracket by less than half) narrow it to at most 64 keys,
+//    which are ranked exactly.
+//  * Output: a key above the threshold goes to position (keys above it
+//    before it) + min(ties before it, need); a tie is taken while fewer than
+//    `need` ties precede it.  The counts before a key come from per-round
+//    per-warp totals (one block scan) and warp scans.
+// This code runs once per launch on its SM, so the passes are short loops
+// (instructions not yet in the instruction cache cost a fetch each).
+#include <algorithm>
+
+#include "mk_internal.cuh"
+
+namespace mk {
+
+namespace {
+constexpr int kTkThreads = 1024, kTkWarps = kTkThreads / 32;
+constexpr int kTkRoundsMax = 32;                              // nch <= 32768: nblk <= 131072
+constexpr int kTkGather = 64;                                 // keys ranked exactly at the end
+constexpr int kTkSmemMax = 200 * 1024;                        // keys staged when they fit
+
+// Exclusive prefix sums of two per-thread counts over the 1024 threads.
+__device__ __forceinline__ int2 block_excl_scan2_1024(int a, int b, int2* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int xa = a, xb = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ya = __shfl_up_sync(FULL, xa, o), yb = __shfl_up_sync(FULL, xb, o);
+    if (lane >= o) {
+      xa += ya;
+      xb += yb;
+    }
+  }
+  if (lane == 31) wsum[warp] = make_int2(xa, xb);
+  __syncthreads();
+  if (warp == 0) {
+    const int2 w = wsum[lane];
+    int sa = w.x, sb = w.y;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ya = __shfl_up_sync(FULL, sa, o), yb = __shfl_up_sync(FULL, sb, o);
+      if (lane >= o) {
+        sa += ya;
+        sb += yb;
+      }
+    }
+    wsum[lane] = make_int2(sa - w.x, sb - w.y);
+  }
+  __syncthreads();
+  const int2 base = wsum[warp];
+  __syncthreads();  // wsum may be reused right after
+  return make_int2(base.x + xa - a, base.y + xb - b);
+}
+}  // namespace
+
+// grid: one CTA per (sequence, kv head) of the call; 1024 threads.  With
+// APPEND the scoring kernel appended cs.n_new[ci] tokens first: the length
+// it read is advanced here, after every scoring CTA has read it.
+template <bool APPEND>
+__global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, CallSeqs cs, int32_t* __restrict__ ids,
+                                                        int32_t* __restrict__ n_sel, int dyn_bytes) {
+  extern __shared__ __align__(16) unsigned char smem[];   // staged keys
+  __shared__ __align__(16) uint32_t hc[kKeyBins];
+  __shared__ __align__(16) int cnt[2][kTkWarps];
+  __shared__ __align__(16) uint32_t gl[kTkGather + 4];
+  __shared__ __align__(16) int2 wtab[kTkThreads];          // per (round, warp): totals, then their bases
+  __shared__ int2 wsum[kTkWarps];
+  __shared__ __align__(16) UnitDesc ud;
+  __shared__ int s_abort, s_bin, s_rem, s_gn;
+  __shared__ uint32_t s_thr;
+  __shared__ __align__(8) uint64_t bar;
+
+  const int ci = blockIdx.x / L.n_kv, kvh = blockIdx.x - ci * L.n_kv;
+  const int seq = cs.seq[ci];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t u = unit_index(L, layer, seq, kvh);
+  const int64_t slot = (int64_t)seq * L.n_kv + kvh;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) {
+    const int32_t err = __ldcg(L.err);
+    uint4 dd[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dd[i] = __ldcg(reinterpret_cast<const uint4*>(L.desc + u) + i);
+    s_abort = err;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(&ud)[i] = dd[i];
+  }
+  __syncthreads();
+  if (s_abort) return;
+  const int T_cur = ud.T + (APPEND ? cs.n_new[ci] : 0);
+  const int nblk = n_mid_blocks(L, T_cur);
+  const int n_cand = n_scored_blocks(ud, nblk);
+  const int k = n_select(L, n_cand);
+  const bool all = k >= n_cand;  // every candidate is taken
+  const int nch = (nblk + 3) >> 2;
+  const int rounds = (nch + kTkThreads - 1) / kTkThreads;
+  uint32_t* kw = L.keys + slot * L.keys_stride;
+  uint32_t* gh = L.khist + slot * kKeyBins;
+  int32_t* out = ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
+  const bool staged = (int64_t)nch * 16 <= (int64_t)dyn_bytes;
+  const uint4* ks = reinterpret_cast<const uint4*>(smem);
+
+  // The histogram and the keys, one bulk copy each.
+  if (tid == 0) {
+    fence_proxy_async_all();
+    const unsigned kb = staged ? (unsigned)nch * 16u : 0u;
+    mbar_expect_tx(&bar, kKeyBins * 4u + kb);
+    bulk_g2s(hc, gh, kKeyBins * 4, &bar);
+    if (kb) bulk_g2s(smem, kw, kb, &bar);
+  }
+  if (!mbar_wait(&bar, 0)) {
+    if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -2, (int32_t)MK_ETIMEOUT);
+    (void)mbar_wait(&bar, 0);
+    return;
+  }
+  // Clear the unit's histogram for the next call (the copy has landed);
+  // advance the length after the fused append.
+  reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);
+  if (APPEND && tid == 0) L.desc[u].T = T_cur;
+
+  // This thread's chunk of round j, keys past nblk zero.
+  auto chunk = [&](int j) -> uint4 {
+    const int c = j * kTkThreads + tid;
+    if (c >= nch) return make_uint4(0, 0, 0, 0);
+    uint4 v = staged ? ks[c] : __ldcg(reinterpret_cast<const uint4*>(kw) + c);
+    if (4 * c + 1 >= nblk) v.y = 0u;
+    if (4 * c + 2 >= nblk) v.z = 0u;
+    if (4 * c + 3 >= nblk) v.w = 0u;
+    return v;
+  };
+  int par = 0;
+  // Block-wide number of keys >= x (one barrier; the two count slots alternate).
+  auto cge = [&](uint64_t x) -> int {
+    int c = 0;
+    if (x <= 0xffffffffull) {
+      const uint32_t xx = (uint32_t)x;
+#pragma unroll 1
+      for (int j = 0; j < rounds; ++j) {
+        const uint4 v = chunk(j);
+        c += (v.x >= xx) + (v.y >= xx) + (v.z >= xx) + (v.w >= xx);
+      }
+    }
+    c = (int)__reduce_add_sync(FULL, (unsigned)c);
+    if (lane == 0) cnt[par][warp] = c;
+    __syncthreads();
+    const int t = (lane < kTkWarps) ? cnt[par][lane] : 0;
+    par ^= 1;
+    return (int)__reduce_add_sync(FULL, (unsigned)t);
+  };
+
+  uint32_t thr = 1u;  // every candidate (key >= 1) when all are taken
+  int need = 0;
+  if (!all) {
+    // Coarse bin of the k-th largest key: thread t holds bins 4095 - 4t - 3 .. 4095 - 4t.
+    {
+      const uint4 h4 = reinterpret_cast<const uint4*>(hc)[kKeyBins / 4 - 1 - tid];
+      const int c = (int)(h4.x + h4.y + h4.z + h4.w);
+      const int ex = block_excl_scan2_1024(c, 0, wsum).x;  // keys in higher bins
+      if (ex < k && ex + c >= k) {
+        const uint32_t hv[4] = {h4.w, h4.z, h4.y, h4.x};  // descending bin order
+        int acc = ex;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (acc < k && acc + (int)hv[i] >= k) {
+            s_bin = kKeyBins - 1 - 4 * tid - i;
+            s_rem = k - acc;
+          }
+          acc += (int)hv[i];
+        }
+      }
+      __syncthreads();
+    }
+    const uint64_t b = (uint64_t)s_bin;
+    uint64_t lo = b << 20 ? b << 20 : 1ull, hi = (b << 20) | 0xfffffull;
+    int c_hi = k - s_rem;           // keys above hi
+    int c_lo = c_hi + (int)hc[b];   // keys >= lo
+    bool bisect = false;
+    while (lo < hi && c_lo - c_hi > kTkGather) {
+      uint64_t x;
+      if (bisect) {
+        x = lo + (hi - lo + 1) / 2;
+      } else {
+        // cge falls from c_lo at lo to c_hi at hi + 1; aim where it crosses k
+        // (fp32: the step only needs to be roughly right).
+        const float f = __fdividef((float)(k - c_hi), (float)(c_lo - c_hi));
+        const uint64_t d = (uint64_t)(f * (float)(hi + 1 - lo));
+        x = hi + 1 - d;
+        x = x < lo + 1 ? lo + 1 : (x > hi ? hi : x);
+      }
+      const uint64_t w0 = hi - lo;
+      const int c = cge(x);
+      if (c >= k) {
+        lo = x;
+        c_lo = c;
+      } else {
+        hi = x - 1;
+        c_hi = c;
+      }
+      bisect = !bisect && (hi - lo) > w0 / 2;
+    }
+    if (lo < hi) {
+      // At most kTkGather keys lie in [lo, hi]: gather and rank them.
+      if (tid == 0) s_gn = 0;
+      __syncthreads();
+#pragma unroll 1
+      for (int j = 0; j < rounds; ++j) {
+        const uint4 v = chunk(j);
+        const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (e[q] >= lo && e[q] <= hi) gl[atomicAdd(&s_gn, 1)] = e[q];
+      }
+      __syncthreads();
+      const int m = s_gn;
+      if (tid < 3) gl[m + tid] = 0u;  // pad to whole 16-byte words (0 is never a candidate key)
+      __syncthreads();
+      const int want = k - c_hi;      // rank of the threshold among them (1 = largest)
+      if (tid < m) {
+        const uint32_t key = gl[tid];
+        int gt = 0, eq = 0;
+        for (int i = 0; i < m; i += 4) {
+          const uint4 o = *reinterpret_cast<const uint4*>(gl + i);
+          gt += (o.x > key) + (o.y > key) + (o.z > key) + (o.w > key);
+          eq += (o.x == key) + (o.y == key) + (o.z == key) + (o.w == key);
+        }
+        if (gt < want && gt + eq >= want) s_thr = key;
+      }
+      __syncthreads();
+      lo = s_thr;
+    }
+    thr = (uint32_t)lo;
+    need = k - cge((uint64_t)thr + 1);  // ties to take
+  }
+
+  // Keys above thr (all candidates when every one is taken) and ties of one
+  // chunk, as 4-bit masks.
+  auto masks = [&](int j, uint32_t& gm, uint32_t& em) {
+    const uint4 v = chunk(j);
+    const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+    gm = 0u;
+    em = 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      gm |= (all ? e[q] != 0u : e[q] > thr) ? 1u << q : 0u;
+      em |= (!all && e[q] == thr) ? 1u << q : 0u;
+    }
+  };
+  // Per (round, warp): totals of (above, ties); then their exclusive scan in
+  // (round, warp) order, one entry per thread.
+#pragma unroll 1
+  for (int j = 0; j < rounds; ++j) {
+    uint32_t gm, em;
+    masks(j, gm, em);
+    const int tg = (int)__reduce_add_sync(FULL, (unsigned)__popc(gm));
+    const int te = (int)__reduce_add_sync(FULL, (unsigned)__popc(em));
+    if (lane == 0) wtab[j * kTkWarps + warp] = make_int2(tg, te);
+  }
+  __syncthreads();
+  {
+    const int2 v = tid < rounds * kTkWarps ? wtab[tid] : make_int2(0, 0);
+    const int2 ex = block_excl_scan2_1024(v.x, v.y, wsum);
+    wtab[tid] = ex;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int j = 0; j < rounds; ++j) {
+    uint32_t gm, em;
+    masks(j, gm, em);
+    const int og = __popc(gm), oe = __popc(em);
+    int ig = og, ie = oe;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yg = __shfl_up_sync(FULL, ig, o), ye = __shfl_up_sync(FULL, ie, o);
+      if (lane >= o) {
+        ig += yg;
+        ie += ye;
+      }
+    }
+    const int2 base = wtab[j * kTkWarps + warp];
+    const int g_before = base.x + ig - og, e_before = base.y + ie - oe;
+    const int take_eq = max(0, min(oe, need - e_before));  // ties still below `need`
+    uint32_t tm = em;
+    while (__popc(tm) > take_eq) tm &= ~(1u << (31 - __clz(tm)));  // keep the lowest ids
+    const uint32_t take = gm | tm;
+    const int p0 = g_before + min(e_before, need);
+    const int c = j * kTkThreads + tid;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int p = p0 + __popc(take & ((1u << q) - 1u));
+      if (((take >> q) & 1u) && p < L.k_max) out[p] = 4 * c + q;
+    }
+  }
+  if (tid == 0) n_sel[(int64_t)ci * L.n_kv + kvh] = k;
+}
+
+bool topk_plan_ok(const Layout& L) { return (L.nblk_cap + 3) / 4 <= kTkThreads * kTkRoundsMax; }
+
+cudaError_t launch_topk(const Layout& L, int layer, const CallSeqs& cs, int32_t* ids, int32_t* n_sel, bool append,
+                        cudaStream_t s) {
+  const int dyn = (int)std::min<int64_t>(kTkSmemMax, (int64_t)16 * ((L.nblk_cap + 3) / 4));
+  static int set[2] = {-1, -1};
+  auto kern = append ? k_topk<true> : k_topk<false>;
+  if (set[append] < dyn) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    if (e != cudaSuccess) return e;
+    set[append] = dyn;
+  }
+  return launch_pdl(kern, dim3(cs.n * L.n_kv), dim3(kTkThreads), dyn, s, 0, L, layer, cs, ids, n_sel, dyn);
+}
+
+}  // namespace mk
