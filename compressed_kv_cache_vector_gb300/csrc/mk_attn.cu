@@ -100,6 +100,19 @@ __device__ __forceinline__ void split2_bf16(float x0, float x1, uint32_t& hi, ui
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  unsigned short v;
+  asm("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;\n" ::"r"(a), "h"((unsigned short)v) : "memory");
+}
 // Rebuild a group's dense key and value rows from their packed (values,
 // indices): the rows are zero already.  Element e = t * r + j (token t, rank
 // j) is the e-th entry of the packed arrays; lane l takes the pairs (e, e + 1)
@@ -107,21 +120,37 @@ __device__ __forceinline__ void split2_bf16(float x0, float x1, uint32_t& hi, ui
 // (values) or 64-byte (indices) run.  t = floor(e / r) = umulhi(2e, rm) with
 // rm = ceil(2^31 / r) (exact for e < 2^20).  Keys and values share e, so their
 // loads and stores interleave.
-__device__ __forceinline__ void scatter_kv(uint16_t* tk, uint16_t* tv, const uint16_t* kval, const uint8_t* kidx,
-                                           const uint16_t* vval, const uint8_t* vidx, int n_el, uint32_t rm,
-                                           int lane) {
-#pragma unroll 2
-  for (int e = 2 * lane; e < n_el; e += 64) {
-    const uint32_t kp = *reinterpret_cast<const uint32_t*>(kval + e);
-    const uint32_t vp = *reinterpret_cast<const uint32_t*>(vval + e);
-    const uint32_t ki = *reinterpret_cast<const uint16_t*>(kidx + e);
-    const uint32_t vi = *reinterpret_cast<const uint16_t*>(vidx + e);
-    const int r0 = (int)__umulhi(2u * (uint32_t)e, rm) * kRow, r1 = (int)__umulhi(2u * (uint32_t)e + 2u, rm) * kRow;
-    tk[r0 + (ki & 0xff)] = (uint16_t)(kp & 0xffff);
-    tv[r0 + (vi & 0xff)] = (uint16_t)(vp & 0xffff);
+// Addresses are shared-window bytes: tk, tv (tiles), kv/ki/vv/vi (packed
+// values and indices); two pairs per lane per step, loads first.
+__device__ __forceinline__ void scatter_kv(uint32_t tk, uint32_t tv, uint32_t kv, uint32_t ki, uint32_t vv,
+                                           uint32_t vi, int n_el, uint32_t rm, int lane) {
+  for (int e = 2 * lane; e < n_el; e += 128) {
+    const int e2 = e + 64;
+    const bool has2 = e2 < n_el;
+    const uint32_t kp = lds_u32(kv + 2 * e), vp = lds_u32(vv + 2 * e);
+    const uint32_t kx = lds_u16(ki + e), vx = lds_u16(vi + e);
+    uint32_t kp2 = 0, vp2 = 0, kx2 = 0, vx2 = 0;
+    if (has2) {
+      kp2 = lds_u32(kv + 2 * e2);
+      vp2 = lds_u32(vv + 2 * e2);
+      kx2 = lds_u16(ki + e2);
+      vx2 = lds_u16(vi + e2);
+    }
+    const uint32_t r0 = __umulhi(2u * (uint32_t)e, rm) * (kRow * 2), r1 = __umulhi(2u * (uint32_t)e + 2u, rm) * (kRow * 2);
+    sts_u16(tk + r0 + 2 * (kx & 0xff), kp);
+    sts_u16(tv + r0 + 2 * (vx & 0xff), vp);
     if (e + 1 < n_el) {
-      tk[r1 + (ki >> 8)] = (uint16_t)(kp >> 16);
-      tv[r1 + (vi >> 8)] = (uint16_t)(vp >> 16);
+      sts_u16(tk + r1 + 2 * (kx >> 8), kp >> 16);
+      sts_u16(tv + r1 + 2 * (vx >> 8), vp >> 16);
+    }
+    if (has2) {
+      const uint32_t q0 = __umulhi(2u * (uint32_t)e2, rm) * (kRow * 2), q1 = __umulhi(2u * (uint32_t)e2 + 2u, rm) * (kRow * 2);
+      sts_u16(tk + q0 + 2 * (kx2 & 0xff), kp2);
+      sts_u16(tv + q0 + 2 * (vx2 & 0xff), vp2);
+      if (e2 + 1 < n_el) {
+        sts_u16(tk + q1 + 2 * (kx2 >> 8), kp2 >> 16);
+        sts_u16(tv + q1 + 2 * (vx2 >> 8), vp2 >> 16);
+      }
     }
   }
 }
@@ -479,7 +508,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
         __syncwarp();
         const int n_el = ntok * r;
         const uint32_t rm = (0x80000000u + (uint32_t)r - 1u) / (uint32_t)r;
-        scatter_kv(tk, tv, kval, kidx, vval, vidx, n_el, rm, lane);
+        scatter_kv(smem_u32(tk), smem_u32(tv), smem_u32(kval), smem_u32(kidx), smem_u32(vval), smem_u32(vidx), n_el,
+                   rm, lane);
         __syncwarp();
         krow = tk + ktok * kRow + kch;
         vrow = tv + vtok * kRow + vch;
