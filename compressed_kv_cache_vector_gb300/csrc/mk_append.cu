@@ -232,9 +232,7 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
       reinterpret_cast<uint2*>(dk)[lane] = reinterpret_cast<const uint2*>(rk)[lane];
       reinterpret_cast<uint2*>(dv)[lane] = reinterpret_cast<const uint2*>(rv)[lane];
     } else {
-      const unsigned kk = compress_vec(L, ud, base, p, rk, 0, lane, false);
-      compress_vec(L, ud, base, p, rv, 1, lane, false);
-      keepk[t * 32 + lane] = (uint8_t)kk;
+      keepk[t * 32 + lane] = (uint8_t)compress_kv(L, ud, base, p, rk, rv, lane);
     }
   }
   __syncthreads();

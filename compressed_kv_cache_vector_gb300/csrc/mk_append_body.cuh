@@ -107,6 +107,102 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   return keep;
 }
 
+// The same for a token's key and value at once (same r): both searches share
+// each warp reduction (counts packed as key | value << 16), which halves the
+// dependent reductions per vector.
+__device__ __forceinline__ void warp_topr2(const uint32_t mk[4], const uint32_t mv[4], int r, int lane,
+                                           unsigned& keep_k, unsigned& keep_v, int& rank_k, int& rank_v) {
+  uint32_t tk = 0, tv = 0;
+#pragma unroll
+  for (int bit = 14; bit >= 0; --bit) {
+    const uint32_t ck = tk | (1u << bit), cv = tv | (1u << bit);
+    const unsigned c = ((unsigned)(mk[0] >= ck) + (unsigned)(mk[1] >= ck) + (unsigned)(mk[2] >= ck) +
+                        (unsigned)(mk[3] >= ck)) |
+                       (((unsigned)(mv[0] >= cv) + (unsigned)(mv[1] >= cv) + (unsigned)(mv[2] >= cv) +
+                         (unsigned)(mv[3] >= cv))
+                        << 16);
+    const unsigned sum = __reduce_add_sync(FULL, c);
+    if ((int)(sum & 0xffffu) >= r) tk = ck;
+    if ((int)(sum >> 16) >= r) tv = cv;
+  }
+  unsigned gt = 0, eq = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    gt += (unsigned)(mk[i] > tk) | ((unsigned)(mv[i] > tv) << 16);
+    eq += (unsigned)(mk[i] == tk) | ((unsigned)(mv[i] == tv) << 16);
+  }
+  const unsigned gsum = __reduce_add_sync(FULL, gt);
+  const int need_k = r - (int)(gsum & 0xffffu), need_v = r - (int)(gsum >> 16);
+  const int run0 = warp_excl_scan((int)eq, lane);
+  int run_k = run0 & 0xffff, run_v = run0 >> 16;
+  keep_k = 0;
+  keep_v = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (mk[i] > tk) {
+      keep_k |= 1u << i;
+    } else if (mk[i] == tk) {
+      if (run_k < need_k) keep_k |= 1u << i;
+      ++run_k;
+    }
+    if (mv[i] > tv) {
+      keep_v |= 1u << i;
+    } else if (mv[i] == tv) {
+      if (run_v < need_v) keep_v |= 1u << i;
+      ++run_v;
+    }
+  }
+  const int rk0 = warp_excl_scan(__popc(keep_k) | (__popc(keep_v) << 16), lane);
+  rank_k = rk0 & 0xffff;
+  rank_v = rk0 >> 16;
+}
+
+// Compresses a token's rotated key and value (128 bf16 words each at rk, rv)
+// of middle position `pos` into its page (no block min/max: the caller
+// folds those).  Called by one full warp.  Returns the key's keep bits.
+__device__ __forceinline__ unsigned compress_kv(const Layout& L, const UnitDesc& ud, char* base, int pos,
+                                                const uint16_t* rk, const uint16_t* rv, int lane) {
+  const int m = pos - L.S;
+  const int b = m / L.B;
+  const int t = m - b * L.B;
+  const int r = ud.r[seg_of_block(ud, b)];
+  char* page = base + L.off_pages + (int64_t)b * L.page_stride;
+  const int Br = L.B * r;
+  const uint2 rawk = *reinterpret_cast<const uint2*>(rk + 4 * lane);
+  const uint2 rawv = *reinterpret_cast<const uint2*>(rv + 4 * lane);
+  const uint16_t vk[4] = {(uint16_t)(rawk.x & 0xffff), (uint16_t)(rawk.x >> 16), (uint16_t)(rawk.y & 0xffff),
+                          (uint16_t)(rawk.y >> 16)};
+  const uint16_t vv[4] = {(uint16_t)(rawv.x & 0xffff), (uint16_t)(rawv.x >> 16), (uint16_t)(rawv.y & 0xffff),
+                          (uint16_t)(rawv.y >> 16)};
+  uint32_t mk[4], mv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    mk[i] = vk[i] & 0x7fffu;
+    mv[i] = vv[i] & 0x7fffu;
+  }
+  unsigned keep_k, keep_v;
+  int rank_k, rank_v;
+  warp_topr2(mk, mv, r, lane, keep_k, keep_v, rank_k, rank_v);
+  uint16_t* valk = reinterpret_cast<uint16_t*>(page);
+  uint8_t* idxk = reinterpret_cast<uint8_t*>(page + 2 * Br);
+  uint16_t* valv = reinterpret_cast<uint16_t*>(page + 3 * Br);
+  uint8_t* idxv = reinterpret_cast<uint8_t*>(page + 5 * Br);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (keep_k >> i & 1u) {
+      valk[t * r + rank_k] = vk[i];
+      idxk[t * r + rank_k] = (uint8_t)(4 * lane + i);
+      ++rank_k;
+    }
+    if (keep_v >> i & 1u) {
+      valv[t * r + rank_v] = vv[i];
+      idxv[t * r + rank_v] = (uint8_t)(4 * lane + i);
+      ++rank_v;
+    }
+  }
+  return keep_k;
+}
+
 // Decode-path append of n new tokens to one (sequence, kv head) by one CTA of
 // 256 threads: evicts the window tokens that leave it into the middle
 // (select, pack, block min/max), then rotates the first n_rot (0 or n, at
