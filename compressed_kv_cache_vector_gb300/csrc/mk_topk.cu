@@ -13,10 +13,11 @@
 //  * One bulk copy each stages the histogram and the keys; thread t takes
 //    the 16-byte chunks j * 1024 + t (round j), so every read of a round is
 //    conflict free and the block's key order is (j, t).
-//  * Threshold: the histogram's coarse bin brackets the k-th key; counting
-//    passes (interpolated in count space, a bisection step whenever one
-//    shrank the bracket by less than half) narrow it to at most 64 keys,
-//    which are ranked exactly.
+//  * Threshold: the histogram's coarse bin holds the k-th key.  Two passes
+//    over the keys of that bin histogram their next 10 bits and then their
+//    last 10 bits (1024 bins each, atomics aggregated per warp over equal
+//    bins), and a block scan of each picks the bin that holds the k-th key:
+//    the threshold key and the number of its ties to take come out exact.
 //  * Output: a key above the threshold goes to position (keys above it
 //    before it) + min(ties before it, need); a tie is taken while fewer than
 //    `need` ties precede it.  The counts before a key come from per-round
@@ -32,7 +33,6 @@ namespace mk {
 namespace {
 constexpr int kTkThreads = 1024, kTkWarps = kTkThreads / 32;
 constexpr int kTkRoundsMax = 32;                              // nch <= 32768: nblk <= 131072
-constexpr int kTkGather = 64;                                 // keys ranked exactly at the end
 constexpr int kTkSmemMax = 200 * 1024;                        // keys staged when they fit
 
 // Exclusive prefix sums of two per-thread counts over the 1024 threads.
@@ -77,13 +77,11 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
                                                         int32_t* __restrict__ n_sel, int dyn_bytes) {
   extern __shared__ __align__(16) unsigned char smem[];   // staged keys
   __shared__ __align__(16) uint32_t hc[kKeyBins];
-  __shared__ __align__(16) int cnt[2][kTkWarps];
-  __shared__ __align__(16) uint32_t gl[kTkGather + 4];
+  __shared__ __align__(16) uint32_t fh[2][1024];           // fine histograms
   __shared__ __align__(16) int2 wtab[kTkThreads];          // per (round, warp): totals, then their bases
   __shared__ int2 wsum[kTkWarps];
   __shared__ __align__(16) UnitDesc ud;
-  __shared__ int s_abort, s_bin, s_rem, s_gn;
-  __shared__ uint32_t s_thr;
+  __shared__ int s_abort, s_bin, s_rem;
   __shared__ __align__(8) uint64_t bar;
 
   const int ci = blockIdx.x / L.n_kv, kvh = blockIdx.x - ci * L.n_kv;
@@ -91,23 +89,19 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t u = unit_index(L, layer, seq, kvh);
   const int64_t slot = (int64_t)seq * L.n_kv + kvh;
+  // The unit's descriptor was last written two or more launches back (by
+  // the append or by this kernel in an earlier call), never by the scoring
+  // kernel this launch waits on, so it is read before the wait point.
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_init_fence();
-  }
-  pdl_wait();
-  pdl_trigger();
-  if (tid == 0) {
-    const int32_t err = __ldcg(L.err);
     uint4 dd[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) dd[i] = __ldcg(reinterpret_cast<const uint4*>(L.desc + u) + i);
-    s_abort = err;
 #pragma unroll
     for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(&ud)[i] = dd[i];
   }
   __syncthreads();
-  if (s_abort) return;
   const int T_cur = ud.T + (APPEND ? cs.n_new[ci] : 0);
   const int nblk = n_mid_blocks(L, T_cur);
   const int n_cand = n_scored_blocks(ud, nblk);
@@ -120,20 +114,29 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
   int32_t* out = ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
   const bool staged = (int64_t)nch * 16 <= (int64_t)dyn_bytes;
   const uint4* ks = reinterpret_cast<const uint4*>(smem);
+  pdl_wait();
+  pdl_trigger();
 
-  // The histogram and the keys, one bulk copy each.
+  // The histogram and the keys, one bulk copy each, in flight while the
+  // error word is read.
   if (tid == 0) {
     fence_proxy_async_all();
     const unsigned kb = staged ? (unsigned)nch * 16u : 0u;
     mbar_expect_tx(&bar, kKeyBins * 4u + kb);
     bulk_g2s(hc, gh, kKeyBins * 4, &bar);
     if (kb) bulk_g2s(smem, kw, kb, &bar);
+    s_abort = __ldcg(L.err);
   }
-  if (!mbar_wait(&bar, 0)) {
+  fh[0][tid] = 0u;
+  fh[1][tid] = 0u;
+  const bool landed = mbar_wait(&bar, 0);
+  if (!landed) {
     if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -2, (int32_t)MK_ETIMEOUT);
     (void)mbar_wait(&bar, 0);
     return;
   }
+  __syncthreads();
+  if (s_abort) return;
   // Clear the unit's histogram for the next call (the copy has landed);
   // advance the length after the fused append.
   reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);
@@ -149,28 +152,40 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
     if (4 * c + 3 >= nblk) v.w = 0u;
     return v;
   };
-  int par = 0;
-  // Block-wide number of keys >= x (one barrier; the two count slots alternate).
-  auto cge = [&](uint64_t x) -> int {
-    int c = 0;
-    if (x <= 0xffffffffull) {
-      const uint32_t xx = (uint32_t)x;
+  // Histogram into h, by bits [shift, shift + 10), of the keys whose bits
+  // from shift + 10 up equal pre (0 is never a candidate).  Lanes with equal
+  // bins add once, so equal keys cost one atomic per warp.
+  auto fine_pass = [&](uint32_t* h, uint32_t pre, int shift) {
 #pragma unroll 1
-      for (int j = 0; j < rounds; ++j) {
-        const uint4 v = chunk(j);
-        c += (v.x >= xx) + (v.y >= xx) + (v.z >= xx) + (v.w >= xx);
+    for (int j = 0; j < rounds; ++j) {
+      const uint4 v = chunk(j);
+      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const bool in = e[q] != 0u && (e[q] >> (shift + 10)) == pre;
+        if (__any_sync(FULL, in)) {
+          const uint32_t bin = in ? (e[q] >> shift) & 1023u : 0xffffffffu;
+          const unsigned grp = __match_any_sync(FULL, bin);
+          if (in && lane == __ffs(grp) - 1) atomicAdd(&h[bin], (uint32_t)__popc(grp));
+        }
       }
     }
-    c = (int)__reduce_add_sync(FULL, (unsigned)c);
-    if (lane == 0) cnt[par][warp] = c;
     __syncthreads();
-    const int t = (lane < kTkWarps) ? cnt[par][lane] : 0;
-    par ^= 1;
-    return (int)__reduce_add_sync(FULL, (unsigned)t);
+  };
+  // The bin of h (descending) that holds the rem-th largest of its keys:
+  // s_bin, and s_rem = its rank inside that bin.
+  auto fine_find = [&](const uint32_t* h, int rem) {
+    const int c = (int)h[1023 - tid];
+    const int ex = block_excl_scan2_1024(c, 0, wsum).x;  // keys in higher bins
+    if (ex < rem && ex + c >= rem) {
+      s_bin = 1023 - tid;
+      s_rem = rem - ex;
+    }
+    __syncthreads();
   };
 
   uint32_t thr = 1u;  // every candidate (key >= 1) when all are taken
-  int need = 0;
+  int need = 0;       // keys equal to thr to take
   if (!all) {
     // Coarse bin of the k-th largest key: thread t holds bins 4095 - 4t - 3 .. 4095 - 4t.
     {
@@ -191,66 +206,16 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
       }
       __syncthreads();
     }
-    const uint64_t b = (uint64_t)s_bin;
-    uint64_t lo = b << 20 ? b << 20 : 1ull, hi = (b << 20) | 0xfffffull;
-    int c_hi = k - s_rem;           // keys above hi
-    int c_lo = c_hi + (int)hc[b];   // keys >= lo
-    bool bisect = false;
-    while (lo < hi && c_lo - c_hi > kTkGather) {
-      uint64_t x;
-      if (bisect) {
-        x = lo + (hi - lo + 1) / 2;
-      } else {
-        // cge falls from c_lo at lo to c_hi at hi + 1; aim where it crosses k
-        // (fp32: the step only needs to be roughly right).
-        const float f = __fdividef((float)(k - c_hi), (float)(c_lo - c_hi));
-        const uint64_t d = (uint64_t)(f * (float)(hi + 1 - lo));
-        x = hi + 1 - d;
-        x = x < lo + 1 ? lo + 1 : (x > hi ? hi : x);
-      }
-      const uint64_t w0 = hi - lo;
-      const int c = cge(x);
-      if (c >= k) {
-        lo = x;
-        c_lo = c;
-      } else {
-        hi = x - 1;
-        c_hi = c;
-      }
-      bisect = !bisect && (hi - lo) > w0 / 2;
-    }
-    if (lo < hi) {
-      // At most kTkGather keys lie in [lo, hi]: gather and rank them.
-      if (tid == 0) s_gn = 0;
-      __syncthreads();
-#pragma unroll 1
-      for (int j = 0; j < rounds; ++j) {
-        const uint4 v = chunk(j);
-        const uint32_t e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (e[q] >= lo && e[q] <= hi) gl[atomicAdd(&s_gn, 1)] = e[q];
-      }
-      __syncthreads();
-      const int m = s_gn;
-      if (tid < 3) gl[m + tid] = 0u;  // pad to whole 16-byte words (0 is never a candidate key)
-      __syncthreads();
-      const int want = k - c_hi;      // rank of the threshold among them (1 = largest)
-      if (tid < m) {
-        const uint32_t key = gl[tid];
-        int gt = 0, eq = 0;
-        for (int i = 0; i < m; i += 4) {
-          const uint4 o = *reinterpret_cast<const uint4*>(gl + i);
-          gt += (o.x > key) + (o.y > key) + (o.z > key) + (o.w > key);
-          eq += (o.x == key) + (o.y == key) + (o.z == key) + (o.w == key);
-        }
-        if (gt < want && gt + eq >= want) s_thr = key;
-      }
-      __syncthreads();
-      lo = s_thr;
-    }
-    thr = (uint32_t)lo;
-    need = k - cge((uint64_t)thr + 1);  // ties to take
+    const uint32_t b = (uint32_t)s_bin;
+    const int rem0 = s_rem;
+    fine_pass(fh[0], b, 10);
+    fine_find(fh[0], rem0);
+    const uint32_t ba = (uint32_t)s_bin;
+    const int rem1 = s_rem;
+    fine_pass(fh[1], (b << 10) | ba, 0);
+    fine_find(fh[1], rem1);
+    thr = (b << 20) | (ba << 10) | (uint32_t)s_bin;
+    need = s_rem;
   }
 
   // Keys above thr (all candidates when every one is taken) and ties of one
