@@ -61,6 +61,13 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? 3 * Br : 0));
   uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? 5 * Br : 2 * Br));
   const uint2 raw = *reinterpret_cast<const uint2*>(row + 4 * lane);
+  // The block's min/max are loaded with the row, ahead of the search.
+  uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta) + (int64_t)b * 2 * D;
+  uint2 omn = make_uint2(0, 0), omx = make_uint2(0, 0);
+  if (update_meta && t != 0) {
+    omn = *reinterpret_cast<const uint2*>(meta + 4 * lane);
+    omx = *reinterpret_cast<const uint2*>(meta + D + 4 * lane);
+  }
   uint16_t v[4] = {(uint16_t)(raw.x & 0xffff), (uint16_t)(raw.x >> 16), (uint16_t)(raw.y & 0xffff),
                    (uint16_t)(raw.y >> 16)};
   uint32_t mag[4];
@@ -77,12 +84,6 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
     }
   }
   if (update_meta) {
-    uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta) + (int64_t)b * 2 * D;
-    uint2 omn = make_uint2(0, 0), omx = make_uint2(0, 0);
-    if (t != 0) {
-      omn = *reinterpret_cast<const uint2*>(meta + 4 * lane);
-      omx = *reinterpret_cast<const uint2*>(meta + D + 4 * lane);
-    }
     const uint16_t pmn[4] = {(uint16_t)(omn.x & 0xffff), (uint16_t)(omn.x >> 16), (uint16_t)(omn.y & 0xffff),
                              (uint16_t)(omn.y >> 16)};
     const uint16_t pmx[4] = {(uint16_t)(omx.x & 0xffff), (uint16_t)(omx.x >> 16), (uint16_t)(omx.y & 0xffff),
@@ -267,6 +268,44 @@ __device__ __forceinline__ void append_small_body(const Layout& L, const UnitDes
     }
   }
   __syncthreads();
+}
+
+// The decode step's append of one token to a unit whose window is full
+// (T_old >= S + W, W > 0), for the fused append + selection: the token at
+// T_old - W leaves the window into the middle and the new token takes its
+// window slot.  Warps 0 and 1 compress the leaving key (with the block
+// min/max) and value while warps 2-5 rotate the new token; only the window
+// write waits for both.  Same arithmetic as append_small_body with n = 1.
+// Called by all 256 threads; Rs = [R_k^T | R_v^T] in shared memory,
+// xs: 2*128 floats of shared scratch.  Shared memory is not touched after
+// the one barrier inside, so the caller may reuse it at once.
+__device__ __forceinline__ void append_one_body(const Layout& L, const UnitDesc& ud, char* base, int T_old,
+                                                const uint16_t* kin, const uint16_t* vin, const float* Rs,
+                                                float* xs) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int e = T_old - L.W;
+  const int slot = (e - L.S) % L.W;
+  uint16_t* win_k = reinterpret_cast<uint16_t*>(base + L.off_win_k) + (int64_t)slot * D;
+  uint16_t* win_v = reinterpret_cast<uint16_t*>(base + L.off_win_v) + (int64_t)slot * D;
+  const int ch = tid - 64;  // warps 2-5: channel of k' and v'
+  float ak = 0.0f, av = 0.0f;
+  if (warp < 2) {
+    compress_vec(L, ud, base, e, warp == 0 ? win_k : win_v, warp, lane, warp == 0);
+  } else if (warp < 6) {
+    xs[ch] = bf2f(kin[ch]);
+    xs[D + ch] = bf2f(vin[ch]);
+    asm volatile("bar.sync 1, 128;\n" ::: "memory");
+#pragma unroll 8
+    for (int j = 0; j < D; ++j) {
+      ak = fmaf(xs[j], Rs[j * D + ch], ak);
+      av = fmaf(xs[D + j], Rs[D * D + j * D + ch], av);
+    }
+  }
+  __syncthreads();  // the leaving rows were read, and shared memory is free
+  if (warp >= 2 && warp < 6) {
+    win_k[ch] = f2bf(ak);
+    win_v[ch] = f2bf(av);
+  }
 }
 
 }  // namespace mk

@@ -37,10 +37,11 @@
 //    rescaled only when a group's max exceeds the running one by more than
 //    2^8 (weights stay <= 2^8, exact in the hi + lo split), so most groups
 //    skip the rescale.
-//  * Split-T merge: warps -> CTA in shared memory, CTA partials (m, l, acc)
-//    -> workspace; the last CTA of the unit to arrive (atomic counter, no
-//    waiting) stages all partials with one cp.async burst, merges them
-//    (log-sum-exp), un-rotates (out = o' R_v) and stores bf16.
+//  * Split-T merge: warps -> CTA in shared memory; each CTA un-rotates its
+//    partial (o'_p R_v, with R_v staged by a bulk copy) and writes (m, l,
+//    acc) to the workspace; the last CTA of the unit to arrive (atomic
+//    counter, no waiting) stages all partials with one bulk copy, merges
+//    them (log-sum-exp weights) and stores bf16.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -177,8 +178,8 @@ size_t smem_for(const Layout& L, int nst, int nw) {
 size_t attn_plan(Layout& L, int /*r_min*/) {
   // Double-buffered stages first (they hide the copy latency), then as many
   // warps as fit.
-  // Warps per CTA are a multiple of 4: the merge's un-rotation splits the
-  // channels into blockDim.x / 128 slices of 128 threads.
+  // Warps per CTA are a multiple of 4, an equal share for each of the SM's
+  // four sub-partitions.
   int plans[8][2] = {{2, 12}, {2, 8}, {2, 4}, {0, 0}, {0, 0}, {0, 0}, {0, 0}, {0, 0}};
   if (const char* e = std::getenv("MK_ATTN_PLAN")) {  // tuning override: "stages,warps"
     int a = 0, b = 0;
@@ -204,11 +205,11 @@ size_t attn_plan(Layout& L, int /*r_min*/) {
 size_t attn_smem_bytes(const Layout& L, int) { return smem_for(L, L.attn_nst, L.attn_nc); }
 
 // Largest number of CTAs per unit whose partials the merging CTA can stage
-// (next to the merged o', the un-rotation slices and R_v).
+// (next to the warps' dump, R_v and the CTA's o').
 int attn_max_parts(const Layout& L) {
   const int64_t dump = ((int64_t)L.attn_nc * L.G * D * 4 + 15) / 16 * 16;
   const int64_t avail = (int64_t)L.attn_nc * per_warp_bytes(L, L.attn_nst) - dump - (int64_t)D * D * 4 -
-                        (int64_t)(1 + L.attn_nc / 4) * L.G * D * 4 - 64;  // dump, R_v, o', slices
+                        (int64_t)L.G * D * 4 - 64;  // dump, R_v, o'
   return (int)std::max<int64_t>(1, std::min<int64_t>(MK_MAX_SPLITS, avail / ((int64_t)L.G * (D + 2) * 4)));
 }
 
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
                                                  const uint16_t* __restrict__ Vd, int64_t t_stride,
                                                  uint16_t* __restrict__ out) {
   const int NST = L.attn_nst, SB = L.attn_sb;
-  const int kWarps = blockDim.x >> 5, kSlices = blockDim.x >> 7;
+  const int kWarps = blockDim.x >> 5;
   extern __shared__ __align__(16) unsigned char smem[];
   const size_t pwb = (size_t)NST * SB + 2 * kTileBytes + ((size_t)NST * 8 + 15) / 16 * 16;
   unsigned char* warp_area = smem;                                       // [kWarps][pwb]
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   const int64_t slot = (int64_t)seq * L.n_kv + kvh;
   const int32_t* my_ids = DENSE ? nullptr : ids + ((int64_t)ci * L.n_kv + kvh) * L.k_max;
 
-  if (!DENSE && part == 0) {  // R_v is static: warm L2 for the final un-rotation
+  if (!DENSE && part == 0) {  // R_v is static: warm L2 for the partials' un-rotation
     const char* rv = unit_base(L, u) + L.off_rv;
     for (int i = tid; i < D * D * 4 / 128; i += blockDim.x) prefetch_l2(rv + (size_t)i * 128);
   }
@@ -258,10 +259,39 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     }
     mbar_init_fence();
   }
+  // q' as the A operand of the logits (k = channel): row g holds the bf16 hi
+  // part and row g + 8 the lo part of head hq = g % G (rows repeat when
+  // G < 8), so one MMA gives both partial sums in the same lane.  The
+  // selection kernel wrote q' two launches back (the top-k kernel runs in
+  // between and leaves it alone), so it is read before the wait point; the
+  // caller's q of the dense reference is read after it.
+  const int hq = g % G;
+  uint32_t aq[8][4];
+  auto load_q = [&]() {
+    const float* qrot = L.qrot + slot * G * D;
+    const uint16_t* qin = DENSE ? q_in + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D : nullptr;
+    float2 qx[8][2];
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c = kc * 16 + hf * 8 + 2 * tig;
+        if (DENSE) {
+          qx[kc][hf] = make_float2(bf2f(qin[hq * D + c]), bf2f(qin[hq * D + c + 1]));
+        } else {
+          qx[kc][hf] = __ldcg(reinterpret_cast<const float2*>(qrot + hq * D + c));
+        }
+      }
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) split2_bf16(qx[kc][hf].x, qx[kc][hf].y, aq[kc][2 * hf], aq[kc][2 * hf + 1]);
+  };
+  if (!DENSE) load_q();
   pdl_wait();
   pdl_trigger();
   // One round of independent loads (L2 path: the previous kernel wrote them):
-  // state, selection count, this CTA's block ids, q'.
+  // state, selection count, this CTA's block ids.
   if (tid == 0) {
     // all three loads in flight before the first use
     const int32_t err = __ldcg(L.err);
@@ -278,26 +308,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   }
   if (!DENSE)
     for (int j = tid; j < kIdsCap && part + j * P < L.k_max; j += blockDim.x) s_ids[j] = __ldcg(my_ids + part + j * P);
-  // q' as the A operand of the logits (k = channel): row g holds the bf16 hi
-  // part and row g + 8 the lo part of head hq = g % G (rows repeat when
-  // G < 8), so one MMA gives both partial sums in the same lane.
-  const int hq = g % G;
-  float2 qx[8][2];
-  {
-    const float* qrot = L.qrot + slot * G * D;
-    const uint16_t* qin = DENSE ? q_in + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D : nullptr;
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int c = kc * 16 + hf * 8 + 2 * tig;
-        if (DENSE) {
-          qx[kc][hf] = make_float2(bf2f(qin[hq * D + c]), bf2f(qin[hq * D + c + 1]));
-        } else {
-          qx[kc][hf] = __ldcg(reinterpret_cast<const float2*>(qrot + hq * D + c));
-        }
-      }
-  }
+  if (DENSE) load_q();
   __syncthreads();
   bool skip = s_abort != 0;
 
@@ -319,14 +330,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
       ns = 0;
     }
   }
-  uint32_t aq[8][4];
-#pragma unroll
-  for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const float2 x = skip ? make_float2(0.0f, 0.0f) : qx[kc][hf];
-      split2_bf16(x.x, x.y, aq[kc][2 * hf], aq[kc][2 * hf + 1]);
-    }
   // Items of the unit: the selected pages, the always-attended pages, then
   // the dense chunks.  CTA `part` takes items part, part + P, ...; its warps
   // take its j-th items round robin (j = warp, warp + kWarps, ...).
@@ -613,9 +616,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     mlw[(warp * 8 + g) * 2 + 1] = l_run;
   }
   __syncthreads();
-  // Every CTA stages R_v above the dump area now (the merging CTA, which is
-  // not known yet, then has it at hand); a CTA that turns out not to merge
-  // waits for the copy before it exits.
+  // Every CTA stages R_v above the dump area now, for the un-rotation of its
+  // partial after the cross-warp sums.
   const size_t dump_bytes = ((size_t)kWarps * G * D * 4 + 15) / 16 * 16;
   float* rvs = reinterpret_cast<float*>(warp_area + dump_bytes);
   if (!DENSE && tid == 0) {
@@ -662,14 +664,80 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     }
   }
   __syncthreads();
+  // The CTA's partial: o' summed over its warps, then (MosaicKV) un-rotated
+  // here, out_p = o'_p R_v, so that the merge is a weighted sum of rows that
+  // are already in the output basis (the un-rotation is linear).
+  // Shared memory above the dump: R_v [D][D] | o' [D][G] | partials
+  // [P][G][D] | (m, l) [P][G][2] (merging CTA).
   float* pacc = L.part_acc + slot * MK_MAX_SPLITS * G * D;   // [part][G][D]
   float* pml = L.part_ml + slot * MK_MAX_SPLITS * G * 2;     // [part][G][2]
+  float* ofull = rvs + (DENSE ? 0 : D * D);
+  float* sacc = ofull + G * D;
+  float* sml = sacc + (size_t)P * G * D;
   for (int i = tid; i < G * D; i += blockDim.x) {
     float a = 0.0f;
 #pragma unroll
     for (int w = 0; w < kMaxWarps; ++w)
       if (w < kWarps) a += dump[(size_t)w * G * D + i];
-    pacc[(size_t)part * G * D + i] = a;
+    if (DENSE)
+      pacc[(size_t)part * G * D + i] = a;
+    else
+      ofull[(i % D) * G + i / D] = a;  // [channel][head]: one vector load per channel below
+  }
+  if (!DENSE) {
+    if (!mbar_wait(&s_bar, 0)) {
+      if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -3, (int32_t)MK_ETIMEOUT);
+      (void)mbar_wait(&s_bar, 0);
+    }
+    __syncthreads();
+    // out_p[h][j] = sum_c o'_p[h][c] R_v[c][j]: lane = four columns j, warp =
+    // slice of c; the slice sums go over the dump area (read above) and are
+    // added in slice order.
+    {
+      float* slc = dump;  // [kWarps][G][D]
+      const int kC = (D + kWarps - 1) / kWarps;
+      const int c0 = warp * kC, c1 = min(D, c0 + kC);
+      float acc[G][4];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.0f;
+#pragma unroll 4
+      for (int c = c0; c < c1; ++c) {
+        const float4 rr = *reinterpret_cast<const float4*>(rvs + c * D + 4 * lane);
+        float oc[G];
+        if constexpr (G % 4 == 0) {
+#pragma unroll
+          for (int h = 0; h < G; h += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(ofull + c * G + h);
+            oc[h] = t.x;
+            oc[h + 1] = t.y;
+            oc[h + 2] = t.z;
+            oc[h + 3] = t.w;
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < G; ++h) oc[h] = ofull[c * G + h];
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          acc[h][0] = fmaf(oc[h], rr.x, acc[h][0]);
+          acc[h][1] = fmaf(oc[h], rr.y, acc[h][1]);
+          acc[h][2] = fmaf(oc[h], rr.z, acc[h][2]);
+          acc[h][3] = fmaf(oc[h], rr.w, acc[h][3]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        *reinterpret_cast<float4*>(slc + ((size_t)warp * G + h) * D + 4 * lane) =
+            make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+      __syncthreads();
+      for (int i = tid; i < G * D; i += blockDim.x) {
+        float a = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kMaxWarps; ++w)
+          if (w < kWarps) a += slc[(size_t)w * G * D + i];
+        pacc[(size_t)part * G * D + i] = a;
+      }
+    }
   }
   if (tid < G) {
     pml[(part * G + tid) * 2] = s_m[tid];
@@ -683,19 +751,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     if (prev == P - 1) L.counters[slot] = 0;
   }
   __syncthreads();
-  if (!s_last || s_abort) {
-    if (!DENSE) (void)mbar_wait(&s_bar, 0);  // no bulk copy may still be landing in this CTA's memory
-    return;
-  }
+  if (!s_last || s_abort) return;
   __threadfence();
 
-  // ---- the last CTA: merge the P partials, un-rotate, store ----------------
-  // Shared memory: dump [kWarps][G][D] | R_v [D][D] (already staged) | o' [G][D]
-  // | slice sums [kSlices][G][D] | partials [P][G][D] | (m, l) [P][G][2].
-  float* ofull = rvs + (DENSE ? 0 : D * D);
-  float* red = ofull + G * D;
-  float* sacc = red + kSlices * G * D;
-  float* sml = sacc + (size_t)P * G * D;
+  // ---- the last CTA: merge the P partials and store -------------------------
   {
     const unsigned b_acc = (unsigned)(P * G * D * 4), b_ml = ((unsigned)(P * G * 2 * 4) + 15u) & ~15u;
     if (tid == 0) {
@@ -704,11 +763,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
       bulk_g2s(sacc, pacc, b_acc, &s_bar2);
       bulk_g2s(sml, pml, b_ml, &s_bar2);
     }
-    const bool ok = mbar_wait(&s_bar2, 0) && (DENSE || mbar_wait(&s_bar, 0));
-    if (!ok) {
+    if (!mbar_wait(&s_bar2, 0)) {
       if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -1, (int32_t)MK_ETIMEOUT);
       (void)mbar_wait(&s_bar2, 0);
-      if (!DENSE) (void)mbar_wait(&s_bar, 0);
       return;
     }
   }
@@ -738,39 +795,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
     }
   }
   __syncthreads();
+  uint16_t* orow = out + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D;
   for (int i = tid; i < G * D; i += blockDim.x) {
     const int h = i / D;
     float a = 0.0f;
+#pragma unroll 8
     for (int p = 0; p < P; ++p) a = fmaf(sacc[(size_t)p * G * D + i], sml[(p * G + h) * 2], a);
-    ofull[i] = a;
-  }
-  __syncthreads();
-  uint16_t* orow = out + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D;
-  if (DENSE) {
-    for (int i = tid; i < G * D; i += blockDim.x) orow[i] = f2bf(ofull[i]);
-    return;
-  }
-  // out[h][j] = sum_c o'[h][c] R_v[c][j]: thread (j, slice of c), slices summed.
-  {
-    const int kC = (D + kSlices - 1) / kSlices;
-    const int j = tid & (D - 1), sl = tid >> 7;
-    const int c0 = sl * kC, c1 = min(D, c0 + kC);
-    float acc[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-#pragma unroll 4
-    for (int c = c0; c < c1; ++c) {
-      const float rr = rvs[c * D + j];
-#pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = fmaf(ofull[h * D + c], rr, acc[h]);
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) red[(sl * G + h) * D + j] = acc[h];
-  }
-  __syncthreads();
-  for (int i = tid; i < G * D; i += blockDim.x) {
-    float a = 0.0f;
-    for (int sl = 0; sl < kSlices; ++sl) a += red[sl * G * D + i];
     orow[i] = f2bf(a);
   }
 }

@@ -176,8 +176,12 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
       const int64_t row0 = (int64_t)cs.row_off[ci] * in_stride + (int64_t)kvh * D;
       float* xs = reinterpret_cast<float*>(smem + 2 * D * D * 4);
       uint16_t* rot = reinterpret_cast<uint16_t*>(xs + n * 2 * D);
-      append_small_body(L, ud, const_cast<char*>(base), T_cur, n, n, kin + row0, vin + row0, in_stride,
-                        reinterpret_cast<const float*>(smem), xs, rot);
+      if (n == 1 && L.W > 0 && T_cur >= L.S + L.W)
+        append_one_body(L, ud, const_cast<char*>(base), T_cur, kin + row0, vin + row0,
+                        reinterpret_cast<const float*>(smem), xs);
+      else
+        append_small_body(L, ud, const_cast<char*>(base), T_cur, n, n, kin + row0, vin + row0, in_stride,
+                          reinterpret_cast<const float*>(smem), xs, rot);
       __threadfence();  // the updated block min/max before this CTA's own tiles are read
     }
     T_cur += n;

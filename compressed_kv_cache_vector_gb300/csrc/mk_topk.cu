@@ -153,8 +153,9 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
     return v;
   };
   // Histogram into h, by bits [shift, shift + 10), of the keys whose bits
-  // from shift + 10 up equal pre (0 is never a candidate).  Lanes with equal
-  // bins add once, so equal keys cost one atomic per warp.
+  // from shift + 10 up equal pre (0 is never a candidate).  When all of a
+  // warp's keys in range share one bin they add once, so runs of equal keys
+  // do not serialise on one address.
   auto fine_pass = [&](uint32_t* h, uint32_t pre, int shift) {
 #pragma unroll 1
     for (int j = 0; j < rounds; ++j) {
@@ -163,10 +164,16 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const bool in = e[q] != 0u && (e[q] >> (shift + 10)) == pre;
-        if (__any_sync(FULL, in)) {
-          const uint32_t bin = in ? (e[q] >> shift) & 1023u : 0xffffffffu;
-          const unsigned grp = __match_any_sync(FULL, bin);
-          if (in && lane == __ffs(grp) - 1) atomicAdd(&h[bin], (uint32_t)__popc(grp));
+        const unsigned act = __ballot_sync(FULL, in);
+        if (act) {
+          const uint32_t bin = (e[q] >> shift) & 1023u;
+          const uint32_t bmin = __reduce_min_sync(FULL, in ? bin : 1023u);
+          const uint32_t bmax = __reduce_max_sync(FULL, in ? bin : 0u);
+          if (bmin == bmax) {
+            if (lane == __ffs(act) - 1) atomicAdd(&h[bin], (uint32_t)__popc(act));
+          } else if (in) {
+            atomicAdd(&h[bin], 1u);
+          }
         }
       }
     }
