@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   __shared__ UnitDesc ud;
   __shared__ __align__(16) uint32_t hc[kKeyBins];   // coarse key histogram
   __shared__ int s_abort;
+  __shared__ __align__(8) uint64_t s_rbar;
 
   const int unit_call = blockIdx.x / P, part = blockIdx.x - unit_call * P;
   const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
@@ -97,19 +98,25 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const int g = lane >> 2, tig = lane & 3;
   const int64_t u = unit_index(L, layer, seq, kvh);
   const int64_t slot = (int64_t)seq * L.n_kv + kvh;
+  const char* base = unit_base(L, u);
+  // R_k^T (and, for the appending CTA, R_v^T right after it in the unit) by
+  // one bulk copy, in flight while q is converted and the histogram cleared.
+  const unsigned r_bytes = (unsigned)((APPEND && part == 0) ? 2 : 1) * D * D * 4;
+  if (tid == 0) {
+    mbar_init(&s_rbar, 1);
+    mbar_init_fence();
+    mbar_expect_tx(&s_rbar, r_bytes);
+    bulk_g2s(smem, base + L.off_rkt, r_bytes, &s_rbar);
+  }
   for (int i = tid; i < G * D; i += blockDim.x)
     qs[i / D][i % D] = bf2f(q[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D + i]);
   for (int i = tid; i < kKeyBins / 4; i += blockDim.x) reinterpret_cast<uint4*>(hc)[i] = make_uint4(0, 0, 0, 0);
-  const char* base = unit_base(L, u);
-  {
-    // R_k^T (and, for the appending CTA, R_v^T right after it in the unit).
-    const int nmat = (APPEND && part == 0) ? 2 : 1;
-    const float4* src = reinterpret_cast<const float4*>(base + L.off_rkt);
-    for (int i = tid; i < nmat * D * D / 4; i += blockDim.x) cp_async16(reinterpret_cast<float4*>(smem) + i, src + i);
-    cp_async_commit();
-    cp_async_wait_all();
+  __syncthreads();  // the barrier's initialisation is visible before anyone waits on it
+  if (!mbar_wait(&s_rbar, 0)) {
+    if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -4, (int32_t)MK_ETIMEOUT);
+    (void)mbar_wait(&s_rbar, 0);
+    return;
   }
-  __syncthreads();
 
   // q'_h[c] = sum_j q_h[j] R_k[c][j]: thread (c, half of j), halves added.
   {
