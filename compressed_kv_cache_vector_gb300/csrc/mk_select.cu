@@ -57,14 +57,16 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 // Exact three-way split of an fp32 value into bf16 parts (x = p0 + p1 + p2
-// for normal x: each part takes the next 8 significant bits).
+// for normal x: each part takes the next 8 significant bits).  A part is the
+// remainder truncated to its upper 16 bits (bf16 rounded toward zero), and
+// the subtraction that leaves the next remainder is exact.
 __device__ __forceinline__ void split3(float x, uint16_t (&p)[3]) {
   float r = x;
 #pragma unroll
   for (int i = 0; i < 3; ++i) {
-    const __nv_bfloat16 h = __float2bfloat16_rz(r);
-    p[i] = __bfloat16_as_ushort(h);
-    r -= __bfloat162float(h);
+    const uint32_t b = __float_as_uint(r) & 0xffff0000u;
+    p[i] = (uint16_t)(b >> 16);
+    r -= __uint_as_float(b);
   }
 }
 
@@ -84,12 +86,13 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
                                                    int dyn_bytes, const uint16_t* __restrict__ kin,
                                                    const uint16_t* __restrict__ vin) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ float qs[G][D];
+  __shared__ __align__(16) float qs[D][G];  // q, channel-major: one vector load per channel
   __shared__ float qr[2][G][D];
   __shared__ UnitDesc ud;
   __shared__ __align__(16) uint32_t hc[kKeyBins];   // coarse key histogram
   __shared__ int s_abort;
   __shared__ __align__(8) uint64_t s_rbar;
+  __shared__ uint32_t bqs[3][16][2][32];            // B fragments, staged once
 
   const int unit_call = blockIdx.x / P, part = blockIdx.x - unit_call * P;
   const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     bulk_g2s(smem, base + L.off_rkt, r_bytes, &s_rbar);
   }
   for (int i = tid; i < G * D; i += blockDim.x)
-    qs[i / D][i % D] = bf2f(q[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D + i]);
+    qs[i % D][i / D] = bf2f(q[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D + i]);
   for (int i = tid; i < kKeyBins / 4; i += blockDim.x) reinterpret_cast<uint4*>(hc)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();  // the barrier's initialisation is visible before anyone waits on it
   if (!mbar_wait(&s_rbar, 0)) {
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     for (int j = half * 64; j < half * 64 + 64; ++j) {
       const float rr = Rs[j * D + c];
 #pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][j], rr, acc[h]);
+      for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[j][h], rr, acc[h]);
     }
 #pragma unroll
     for (int h = 0; h < G; ++h) qr[half][h][c] = acc[h];
@@ -141,23 +144,30 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   }
   __syncthreads();
 
-  // B fragments of [min(q',0) | max(q',0)] (k = 0..255, n = head), 3 exact parts.
+  // B fragments of [min(q',0) | max(q',0)] (k = 0..255, n = head), 3 exact
+  // parts: built once per (chunk, half, lane) by a short loop into shared
+  // memory, then loaded into the registers of every warp.
+  for (int i = tid; i < 16 * 2 * 32; i += blockDim.x) {
+    const int ln = i & 31, hf2 = (i >> 5) & 1, kc = i >> 6;
+    const int n = ln >> 2, k = kc * 16 + hf2 * 8 + 2 * (ln & 3);
+    uint16_t e0[3] = {0, 0, 0}, e1[3] = {0, 0, 0};
+    if (n < G) {
+      const float x0 = k < D ? fminf(qr[0][n][k], 0.0f) : fmaxf(qr[0][n][k - D], 0.0f);
+      const float x1 = (k + 1) < D ? fminf(qr[0][n][k + 1], 0.0f) : fmaxf(qr[0][n][k + 1 - D], 0.0f);
+      split3(x0, e0);
+      split3(x1, e1);
+    }
+#pragma unroll
+    for (int s = 0; s < 3; ++s) bqs[s][kc][hf2][ln] = (uint32_t)e0[s] | ((uint32_t)e1[s] << 16);
+  }
+  __syncthreads();
   uint32_t bq[3][16][2];
 #pragma unroll
-  for (int kc = 0; kc < 16; ++kc)
+  for (int s = 0; s < 3; ++s)
 #pragma unroll
-    for (int hf2 = 0; hf2 < 2; ++hf2) {
-      uint16_t e0[3] = {0, 0, 0}, e1[3] = {0, 0, 0};
-      if (g < G) {
-        const int k = kc * 16 + hf2 * 8 + 2 * tig;
-        const float x0 = k < D ? fminf(qr[0][g][k], 0.0f) : fmaxf(qr[0][g][k - D], 0.0f);
-        const float x1 = (k + 1) < D ? fminf(qr[0][g][k + 1], 0.0f) : fmaxf(qr[0][g][k + 1 - D], 0.0f);
-        split3(x0, e0);
-        split3(x1, e1);
-      }
+    for (int kc = 0; kc < 16; ++kc)
 #pragma unroll
-      for (int s = 0; s < 3; ++s) bq[s][kc][hf2] = (uint32_t)e0[s] | ((uint32_t)e1[s] << 16);
-    }
+      for (int hf2 = 0; hf2 < 2; ++hf2) bq[s][kc][hf2] = bqs[s][kc][hf2][lane];
   // Everything above used only q and R_k.  From here on the kernel reads
   // what the append kernel wrote (lengths, block keys).
   pdl_wait();
