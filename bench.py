@@ -34,6 +34,12 @@ UNIT = "context tokens/s"
 D = 128
 
 
+# Kernels each layer of a decode step launches: the fused path runs k_select
+# (append + scoring), k_topk and k_attn; the separate path adds k_append_small
+# in front of the same three.
+LAUNCHES_PER_LAYER = {False: 3, True: 4}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,7 +425,7 @@ def main():
             "append_select_gbs": (per["append"] + per["select"]) / ((app_avg + sel_avg) * 1e-3) / 1e9,
         }
     phases.update({"attn_gbs": achieved, "step_span_ms": statistics.mean(span_ms), "alg_bytes_per_layer": per,
-                   "launches_per_layer": 3 if a.separate else 2})
+                   "launches_per_layer": LAUNCHES_PER_LAYER[a.separate]})
 
     # end to end through the public API with host buffers (eager calls)
     e2e = None
@@ -483,7 +489,7 @@ def main():
                             calls=("mk_append_compress + mk_block_select + mk_decode_attn" if a.separate else
                                    "mk_append_select + mk_decode_attn") + " per layer"),
                 hbm_gbs=gbs, alg_bytes_per_step=step_bytes, roofline=roofline, phases=phases,
-                cpu_baseline=cpu, e2e=e2e, gpu_launches=(3 if a.separate else 2) * L * a.steps, clocks=clk)
+                cpu_baseline=cpu, e2e=e2e, gpu_launches=LAUNCHES_PER_LAYER[a.separate] * L * a.steps, clocks=clk)
     if mk.prefill_ms:
         pm = sorted(mk.prefill_ms)[len(mk.prefill_ms) // 2]
         ntok = sum(wl.seq_lens) * wl.n_kv_heads
