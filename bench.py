@@ -40,6 +40,22 @@ D = 128
 LAUNCHES_PER_LAYER = {False: 3, True: 4}
 
 
+def max_over_ranks(x, dist, device):
+    """The largest of the ranks' x (the job's time is its slowest rank's); x itself on one rank."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(units_per_rank, world, ms):
+    """Whole-job throughput under weak scaling: every rank processes the same number of units (context
+    tokens x layers) in one step, and the step takes ms on the slowest rank."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -369,10 +385,7 @@ def main():
     if st != 0:
         raise RuntimeError(f"device error word set during the run: {st}/{detail}")
     ms = total_ms / a.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
 
     # algorithmic bytes at the mean length of the timed steps
     T_mid = [t + a.warmup + a.steps / 2 for t in T_start]
@@ -384,7 +397,7 @@ def main():
             per[k_] += b[k_] * Hkv
     step_bytes = sum(per.values()) * L
     ctx_tokens = sum(T_mid) * L * world
-    value = ctx_tokens / (ms * 1e-3)
+    value = weak_value(sum(T_mid) * L, world, ms)
     gbs = step_bytes * world / (ms * 1e-3) / 1e9
 
     peaks = {}
@@ -459,10 +472,7 @@ def main():
             e2e_step()
         torch.cuda.synchronize()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / a.steps
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
         h2d = sum(t.numel() * 2 for t in hk + hv + hq)
         d2h = sum(t.numel() * 2 for t in ho)
         e2e = {"value": ctx_tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
