@@ -43,6 +43,15 @@ class MkConfig(ctypes.Structure):
                 ("n_segments", c_i32), ("seg", MkSegment * MK_MAX_SEGMENTS)]
 
 
+class MkAlg2Params(ctypes.Structure):
+    _fields_ = [("outlier_abs", ctypes.c_double), ("outlier_ratio_max", ctypes.c_double),
+                ("alpha", ctypes.c_double), ("r_min", c_i32), ("r_max", c_i32), ("hist_bins", c_i32)]
+
+
+class MkSegStats(ctypes.Structure):
+    _fields_ = [("variance", ctypes.c_double), ("outlier_ratio", ctypes.c_double), ("entropy", ctypes.c_double)]
+
+
 class MkLayoutInfo(ctypes.Structure):
     _fields_ = [("rkt", c_i64), ("rvt", c_i64), ("rv", c_i64), ("sink_k", c_i64), ("sink_v", c_i64),
                 ("win_k", c_i64), ("win_v", c_i64), ("meta", c_i64), ("pages", c_i64),
@@ -70,6 +79,11 @@ _SIGS = {
     "mk_layout": [c_vp, c_i32, c_i32, c_i32, ctypes.POINTER(MkLayoutInfo)],
     "mk_record_event": [c_vp, c_vp],
     "mk_dense_decode_attn_noalloc": [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_vp],
+    "mk_cov_update": [c_vp, c_vp, c_i64, c_i64, c_i32],
+    "mk_rotation_from_cov": [c_vp, c_i32, c_vp, c_vp],
+    "mk_choose_r": [c_vp, c_i32, ctypes.c_double, ctypes.POINTER(c_i32)],
+    "mk_alg2_segment_r": [c_vp, c_i64, c_i64, c_i32, ctypes.c_double, ctypes.POINTER(MkAlg2Params),
+                          ctypes.POINTER(MkSegStats), ctypes.POINTER(c_i32)],
 }
 
 _lib = None
@@ -292,10 +306,59 @@ def gram(x, n_rows, row_stride, out=None, stream=None):
 
 
 def rotation_from_gram(G):
-    """Host eigensolve of a Gram matrix (float64): rows of R are the
-    eigenvectors by descending eigenvalue, so k' = k R^T."""
+    """Host eigensolve of a Gram matrix (the library's native Jacobi, fp64):
+    rows of R are the eigenvectors by descending eigenvalue, so k' = k R^T."""
     Gd = np.asarray(G, dtype=np.float64)
-    Gd = 0.5 * (Gd + Gd.T)
-    lam, vecs = np.linalg.eigh(Gd)
-    order = np.argsort(-lam, kind="stable")
-    return np.ascontiguousarray(vecs[:, order].T, dtype=np.float32)
+    R, _ = rotation_from_cov(0.5 * (Gd + Gd.T))
+    return R
+
+
+# ---- host-side strategy generation (host arrays; no GPU) ----------------------
+
+def _np_ptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _bf16_words(x):
+    """A 2-D array of bf16 words (uint16) from a uint16 array or a CPU bf16 tensor."""
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return np.ascontiguousarray(x, dtype=np.uint16)
+
+
+def cov_update(G, x):
+    """G += X^T X in fp64 (G: d x d float64, updated in place; x: n x d bf16 rows)."""
+    w = _bf16_words(x)
+    assert G.dtype == np.float64 and G.flags.c_contiguous and G.shape == (w.shape[1], w.shape[1])
+    _check("mk_cov_update", load().mk_cov_update(_np_ptr(G), _np_ptr(w), w.shape[0], w.shape[1], w.shape[1]))
+    return G
+
+
+def rotation_from_cov(G):
+    """Native Jacobi eigen-decomposition: (R float32 d x d, rows = eigenvectors; lambda descending)."""
+    Gd = np.ascontiguousarray(G, dtype=np.float64)
+    d = Gd.shape[0]
+    R = np.empty((d, d), dtype=np.float32)
+    lam = np.empty(d, dtype=np.float64)
+    _check("mk_rotation_from_cov", load().mk_rotation_from_cov(_np_ptr(Gd), d, _np_ptr(R), _np_ptr(lam)))
+    return R, lam
+
+
+def choose_r(lam, loss_max):
+    """Smallest r whose discarded energy is at most loss_max."""
+    l = np.ascontiguousarray(lam, dtype=np.float64)
+    r = c_i32(0)
+    _check("mk_choose_r", load().mk_choose_r(_np_ptr(l), l.shape[0], float(loss_max), ctypes.byref(r)))
+    return r.value
+
+
+def alg2_segment_r(seg, budget, outlier_abs, outlier_ratio_max, alpha, r_min, r_max, hist_bins):
+    """Algorithm 2 on one rotated segment: (r, {variance, outlier_ratio, entropy})."""
+    w = _bf16_words(seg)
+    p = MkAlg2Params(outlier_abs, outlier_ratio_max, alpha, r_min, r_max, hist_bins)
+    st = MkSegStats()
+    r = c_i32(0)
+    _check("mk_alg2_segment_r", load().mk_alg2_segment_r(_np_ptr(w), w.shape[0], w.shape[1], w.shape[1],
+                                                         float(budget), ctypes.byref(p), ctypes.byref(st),
+                                                         ctypes.byref(r)))
+    return r.value, {"variance": st.variance, "outlier_ratio": st.outlier_ratio, "entropy": st.entropy}

@@ -227,6 +227,61 @@ mk_status mk_dense_decode_attn_noalloc(int32_t n_q_heads, int32_t n_kv_heads, in
  * gram: device fp32 [128][128], overwritten. */
 mk_status mk_gram(const void* x, int64_t n_rows, int64_t row_stride, float* gram, mk_stream stream);
 
+/* ---- Host-side strategy generation (host memory only; no device, no context) ----
+ * The CPU part of the method: the covariance a head accumulates, the
+ * rotation from its eigenvectors ([N] Eq. (4), (6)), the channel count that
+ * keeps the discarded energy under a loss threshold ([N] Eq. (5); [S] sec.
+ * 5.5, channel parameters chosen under a loss threshold), and the per-segment
+ * channel count of [N] Algorithm 2 (Eq. (10)-(11)).  All arithmetic is fp64.
+ * These calls touch no GPU and may run on any thread, concurrently with the
+ * decode calls. */
+
+/* G += sum over the n rows x of x^T x.  G: d x d row-major doubles (the
+ * caller's accumulator, updated in place); x: n rows of d bf16 words, row i
+ * at x + i * row_stride words.  MK_EINVAL: null pointer, d < 1 or n < 0. */
+mk_status mk_cov_update(double* G, const void* x, int64_t n, int64_t row_stride, int32_t d);
+
+/* Eigen-decomposition of the symmetric d x d matrix G (row-major doubles) by
+ * cyclic Jacobi rotations: lambda[i] in descending order, R (d x d floats,
+ * row-major) with row i the unit eigenvector of lambda[i], so R is the
+ * rotation mk_set_rotation takes (k' = k R^T).  Eigenvectors are unique up to
+ * sign (and, for repeated eigenvalues, up to a rotation of their subspace).
+ * MK_EINVAL: null pointer, d < 1, or G not symmetric (relative 1e-12);
+ * MK_ETIMEOUT: no convergence within 100 sweeps (R and lambda still hold the
+ * last iterate). */
+mk_status mk_rotation_from_cov(const double* G, int32_t d, float* R, double* lambda);
+
+/* Smallest r in [1, d] whose discarded energy sum_{i>=r} lambda_i /
+ * sum_i lambda_i (lambda descending, [N] Eq. (5): 1 - Energy(r)) is at most
+ * loss_max.  A zero spectrum gives r = 1; eigenvalues down to -1e-9 lambda_0
+ * (roundoff) count as zero.  MK_EINVAL: null pointer, d < 1, loss_max < 0, a
+ * lambda below -1e-9 lambda_0, or lambda not descending (same tolerance). */
+mk_status mk_choose_r(const double* lambda, int32_t d, double loss_max, int32_t* r);
+
+/* [N] Algorithm 2 for one rotated segment of s vectors of d channels. */
+typedef struct mk_alg2_params {
+  double outlier_abs;       /* |x| above this counts as an outlier element */
+  double outlier_ratio_max; /* above this outlier ratio the segment is compressed harder */
+  double alpha;             /* strength of the adjustment */
+  int32_t r_min, r_max;     /* clamp of the result */
+  int32_t hist_bins;        /* bins of the magnitude histogram (entropy) */
+} mk_alg2_params;
+typedef struct mk_seg_stats {
+  double variance;      /* mean over channels of the channel's population variance */
+  double outlier_ratio; /* #{|x| > outlier_abs} / (s d) */
+  double entropy;       /* -sum p ln p over the magnitude histogram (natural log) */
+} mk_seg_stats;
+/* seg: s rows of d bf16 words (row stride row_stride words), already
+ * rotated; budget: the segment's element budget R_budget.  With
+ * u = outlier_ratio, r = budget/s * (1 - alpha u) if u > outlier_ratio_max,
+ * else budget/s * (1 + alpha (1 - u)); clamped to [r_min, r_max] and rounded
+ * down.  The histogram has hist_bins equal bins over [0, max |x|] (a value
+ * equal to the maximum goes to the last bin; all-zero data fill bin 0).
+ * stats may be NULL.  MK_EINVAL: null seg or r, s < 1, d < 1, hist_bins < 1,
+ * r_min < 1, r_max < r_min, budget < 0. */
+mk_status mk_alg2_segment_r(const void* seg, int64_t s, int64_t row_stride, int32_t d, double budget,
+                            const mk_alg2_params* params, mk_seg_stats* stats, int32_t* r);
+
 /* Waits for the device and reads the sticky error word: MK_OK, MK_EDEVICE or
  * MK_ETIMEOUT; *detail (optional) receives the kernel's detail code. */
 mk_status mk_poll_error(mk_ctx* ctx, int32_t* detail);
