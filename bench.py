@@ -84,7 +84,8 @@ def unit_bytes(wl, T, firsts):
     segs = wl.segments
     bounds = list(firsts) + [nblk]
     scored, always_bytes, r_scored = 0, 0, segs[0][1]
-    for i, (_, r, always) in enumerate(segs):
+    for i, sg in enumerate(segs):
+        r, always = sg[1], sg[2]
         lo, hi = min(bounds[i], nblk), min(bounds[i + 1] if i + 1 < len(segs) else nblk, nblk)
         n = max(0, hi - lo)
         if always:
@@ -108,7 +109,8 @@ def segment_firsts(wl, T0):
     S, W, B = wl.n_sink, wl.window, wl.block
     nb0 = (max(0, T0 - S - W) + B - 1) // B
     out, prev = [], 0
-    for i, (beg, _, _) in enumerate(wl.segments):
+    for i, sg in enumerate(wl.segments):
+        beg = sg[0]
         b = 0 if i == 0 else min(max((max(0, beg * T0 // 1000 - S) + B - 1) // B, prev), nb0)
         out.append(b)
         prev = b

@@ -33,7 +33,7 @@ class MosaicKVError(RuntimeError):
 
 
 class MkSegment(ctypes.Structure):
-    _fields_ = [("begin_permille", c_i32), ("r", c_i32), ("always", c_i32), ("reserved", c_i32)]
+    _fields_ = [("begin_permille", c_i32), ("r", c_i32), ("always", c_i32), ("keep_channels", c_i32)]
 
 
 class MkConfig(ctypes.Structure):
@@ -141,8 +141,10 @@ def make_config(n_q_heads, n_kv_heads, n_layers, max_seqs, max_tokens, n_sink, w
     c.n_sink, c.window, c.block = n_sink, window, block
     c.topk_fixed, c.retain_permille = topk_fixed, retain_permille
     c.n_segments = len(segments)
-    for i, (b, r, a) in enumerate(segments):
-        c.seg[i].begin_permille, c.seg[i].r, c.seg[i].always, c.seg[i].reserved = b, r, a, 0
+    for i, sg in enumerate(segments):
+        b, r, a = sg[:3]
+        keep = sg[3] if len(sg) > 3 else 0
+        c.seg[i].begin_permille, c.seg[i].r, c.seg[i].always, c.seg[i].keep_channels = b, r, a, keep
     return c
 
 

@@ -52,7 +52,8 @@ mk_status check_config(const mk_config* c) {
   int prev = 0;
   for (int i = 0; i < c->n_segments; ++i) {
     const mk_segment& s = c->seg[i];
-    if (s.r < 1 || s.r > MK_HEAD_DIM || (s.always != 0 && s.always != 1) || s.reserved != 0) return MK_EINVAL;
+    if (s.r < 1 || s.r > MK_HEAD_DIM || (s.always != 0 && s.always != 1)) return MK_EINVAL;
+    if (s.keep_channels != 0 && (s.keep_channels < s.r || s.keep_channels > MK_HEAD_DIM)) return MK_EINVAL;
     if (s.begin_permille < 0 || s.begin_permille > 1000) return MK_EINVAL;
     if (i == 0 && s.begin_permille != 0) return MK_EINVAL;
     if (s.begin_permille < prev) return MK_EINVAL;
@@ -159,7 +160,12 @@ UnitDesc host_desc(const mk_ctx* ctx, int layer, int seq) {
   for (int s = 0; s < MK_MAX_SEGMENTS; ++s) {
     d.first_block[s] = ctx->firsts[i * MK_MAX_SEGMENTS + s];
     d.r[s] = s < ctx->cfg.n_segments ? ctx->cfg.seg[s].r : 0;
-    d.always[s] = s < ctx->cfg.n_segments ? ctx->cfg.seg[s].always : 0;
+    if (s < ctx->cfg.n_segments) {
+      const mk_segment& g = ctx->cfg.seg[s];
+      d.sflags[s] = mk::seg_flags(g.always != 0, g.keep_channels ? g.keep_channels : MK_HEAD_DIM);
+    } else {
+      d.sflags[s] = mk::seg_flags(false, MK_HEAD_DIM);
+    }
   }
   return d;
 }

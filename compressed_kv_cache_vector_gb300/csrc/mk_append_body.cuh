@@ -55,7 +55,8 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   const int m = pos - L.S;
   const int b = m / L.B;
   const int t = m - b * L.B;
-  const int r = ud.r[seg_of_block(ud, b)];
+  const int sg = seg_of_block(ud, b);
+  const int r = ud.r[sg], keep = seg_keep(ud, sg);
   char* page = base + L.off_pages + (int64_t)b * L.page_stride;
   const int Br = L.B * r;
   uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? 3 * Br : 0));
@@ -70,14 +71,16 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   }
   uint16_t v[4] = {(uint16_t)(raw.x & 0xffff), (uint16_t)(raw.x >> 16), (uint16_t)(raw.y & 0xffff),
                    (uint16_t)(raw.y >> 16)};
+  // Channels from `keep` on are truncated: magnitude 0, and with r <= keep
+  // the ties at 0 go to lower channels, so they are never taken.
   uint32_t mag[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) mag[i] = v[i] & 0x7fffu;
+  for (int i = 0; i < 4; ++i) mag[i] = 4 * lane + i < keep ? v[i] & 0x7fffu : 0u;
   int rank;
-  const unsigned keep = warp_topr(mag, r, lane, rank);
+  const unsigned kbits = warp_topr(mag, r, lane, rank);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    if (keep >> i & 1u) {
+    if (kbits >> i & 1u) {
       val[t * r + rank] = v[i];
       idx[t * r + rank] = (uint8_t)(4 * lane + i);
       ++rank;
@@ -91,7 +94,7 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
     uint16_t nmn[4], nmx[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float kt = (keep >> i & 1u) ? bf2f(v[i]) : 0.0f;
+      const float kt = (kbits >> i & 1u) ? bf2f(v[i]) : 0.0f;
       float lo = kt, hi = kt;
       if (t != 0) {
         lo = fminf(bf2f(pmn[i]), kt);
@@ -105,7 +108,7 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
     *reinterpret_cast<uint2*>(meta + D + 4 * lane) =
         make_uint2((uint32_t)nmx[0] | ((uint32_t)nmx[1] << 16), (uint32_t)nmx[2] | ((uint32_t)nmx[3] << 16));
   }
-  return keep;
+  return kbits;
 }
 
 // The same for a token's key and value at once (same r): both searches share
@@ -166,7 +169,8 @@ __device__ __forceinline__ unsigned compress_kv(const Layout& L, const UnitDesc&
   const int m = pos - L.S;
   const int b = m / L.B;
   const int t = m - b * L.B;
-  const int r = ud.r[seg_of_block(ud, b)];
+  const int sg = seg_of_block(ud, b);
+  const int r = ud.r[sg], keep = seg_keep(ud, sg);
   char* page = base + L.off_pages + (int64_t)b * L.page_stride;
   const int Br = L.B * r;
   const uint2 rawk = *reinterpret_cast<const uint2*>(rk + 4 * lane);
@@ -177,9 +181,10 @@ __device__ __forceinline__ unsigned compress_kv(const Layout& L, const UnitDesc&
                           (uint16_t)(rawv.y >> 16)};
   uint32_t mk[4], mv[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    mk[i] = vk[i] & 0x7fffu;
-    mv[i] = vv[i] & 0x7fffu;
+  for (int i = 0; i < 4; ++i) {  // channels from `keep` on are truncated (see compress_vec)
+    const bool live = 4 * lane + i < keep;
+    mk[i] = live ? vk[i] & 0x7fffu : 0u;
+    mv[i] = live ? vv[i] & 0x7fffu : 0u;
   }
   unsigned keep_k, keep_v;
   int rank_k, rank_v;

@@ -63,7 +63,7 @@ constexpr float kScaleLog2 = 0.08838834764831845f * 1.4426950408889634f;  // log
 
 __device__ __forceinline__ int always_block(const UnitDesc& ud, int nblk, int i) {
   for (int s = 0; s < ud.n_seg; ++s) {
-    if (!ud.always[s]) continue;
+    if (!seg_always(ud, s)) continue;
     const int lo = min(ud.first_block[s], nblk);
     const int hi = (s + 1 < ud.n_seg) ? min(ud.first_block[s + 1], nblk) : nblk;
     if (i < hi - lo) return lo + i;

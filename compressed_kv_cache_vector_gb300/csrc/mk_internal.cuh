@@ -35,9 +35,13 @@ struct UnitDesc {
   int32_t rot_set;
   int32_t first_block[MK_MAX_SEGMENTS];
   int32_t r[MK_MAX_SEGMENTS];
-  int32_t always[MK_MAX_SEGMENTS];
+  int32_t sflags[MK_MAX_SEGMENTS];  // per segment: bit 0 always attended; bits 8-15 channels eligible for the top-r
 };
 static_assert(sizeof(UnitDesc) == 64, "UnitDesc is 64 bytes");
+
+__host__ __device__ inline int32_t seg_flags(bool always, int keep) { return (always ? 1 : 0) | (keep << 8); }
+__host__ __device__ inline bool seg_always(const UnitDesc& u, int s) { return (u.sflags[s] & 1) != 0; }
+__host__ __device__ inline int seg_keep(const UnitDesc& u, int s) { return (u.sflags[s] >> 8) & 0xff; }
 
 // Everything a kernel needs to find data in the arena and workspace.
 struct Layout {
@@ -98,7 +102,7 @@ __host__ __device__ inline int n_scored_blocks(const UnitDesc& u, int nblk) {
     int hi = (i + 1 < u.n_seg) ? u.first_block[i + 1] : nblk;
     if (hi > nblk) hi = nblk;
     if (lo > nblk) lo = nblk;
-    if (!u.always[i] && hi > lo) n += hi - lo;
+    if (!seg_always(u, i) && hi > lo) n += hi - lo;
   }
   return n;
 }

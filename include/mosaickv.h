@@ -71,7 +71,11 @@ typedef struct mk_segment {
   int32_t begin_permille; /* 0..1000 */
   int32_t r;              /* channels kept per vector, 1..128 */
   int32_t always;         /* 1: attended in full, never scored; 0: top-k */
-  int32_t reserved;       /* must be 0 */
+  int32_t keep_channels;  /* 0 (= 128) or r..128: the per-vector top-r of the
+                             compressed middle picks among the first
+                             keep_channels rotated channels only, the bottom
+                             ones being truncated ([S] sec. 5.2 truncates the
+                             bottom 25%: 96).  Sinks and window stay whole. */
 } mk_segment;
 
 typedef struct mk_config {

@@ -110,18 +110,22 @@ def energy(R, X, r):
 # --------------------------------------------------------------------------
 # Channel selection: [N] Eq. (9) / Algorithm 1 and the global-mask contrast
 # --------------------------------------------------------------------------
-def topr_select(X, r):
+def topr_select(X, r, keep=None):
     """Per-vector top-r by magnitude ([N] Eq. (9), Algorithm 1).
 
     X: [n, d] bf16-exact values.  Order channels by |x| descending, ties to
     the lower channel (a stable sort keeps channel order among equals), keep
-    the first r, and return them in ascending channel order.
+    the first r, and return them in ascending channel order.  With `keep`,
+    only the first `keep` channels are candidates: the bottom ones are
+    truncated ([S] sec. 5.2).
     Returns (idx uint8 [n, r], vals float64 [n, r]).
     """
     X = np.asarray(X, dtype=np.float64)
     if X.ndim == 1:
         X = X[None, :]
-    order = np.argsort(-np.abs(X), axis=1, kind="stable")[:, :r]
+    keep = X.shape[1] if keep is None else keep
+    assert r <= keep
+    order = np.argsort(-np.abs(X[:, :keep]), axis=1, kind="stable")[:, :r]
     idx = np.sort(order, axis=1)
     vals = np.take_along_axis(X, idx, axis=1)
     return idx.astype(np.uint8), vals
@@ -155,9 +159,15 @@ class Strategy:
     n_sink: int
     window: int
     block: int
-    segments: list            # [(begin_permille, r, always)]
+    segments: list            # [(begin_permille, r, always[, keep_channels])]
     topk_fixed: int = 0
     retain_permille: int = 0
+
+    def __post_init__(self):
+        # keep_channels: the first channels eligible for the top-r; 0 or
+        # absent means all of them ([S] sec. 5.2 truncates the bottom 25%).
+        self.segments = [(sg[0], sg[1], sg[2], (sg[3] if len(sg) > 3 and sg[3] else D_HEAD))
+                         for sg in self.segments]
 
 
 def n_middle_blocks(T, st: Strategy):
@@ -170,7 +180,8 @@ def segment_first_blocks(T0, st: Strategy):
     nb0 = n_middle_blocks(T0, st)
     firsts = []
     prev = 0
-    for i, (begin, _r, _a) in enumerate(st.segments):
+    for i, sg in enumerate(st.segments):
+        begin = sg[0]
         if i == 0:
             b = 0
         else:
@@ -275,7 +286,7 @@ class OracleCache:
         self.Vr = np.zeros((capacity, d), dtype=dt)
         self.Kt = np.zeros((capacity, d), dtype=dt)     # zero-filled compressed (middle rows)
         self.Vt = np.zeros((capacity, d), dtype=dt)
-        rmax = max(r for _, r, _ in st.segments)
+        rmax = max(sg[1] for sg in st.segments)
         self.kidx = np.zeros((capacity, rmax), dtype=np.uint8)
         self.vidx = np.zeros((capacity, rmax), dtype=np.uint8)
         self.kval = np.zeros((capacity, rmax), dtype=dt)
@@ -301,6 +312,9 @@ class OracleCache:
 
     def always_of_block(self, b):
         return bool(self.st.segments[block_segment(b, self.firsts)][2])
+
+    def keep_of_block(self, b):
+        return self.st.segments[block_segment(b, self.firsts)][3]
 
     def n_blocks(self):
         return n_middle_blocks(self.T, self.st)
@@ -345,10 +359,10 @@ class OracleCache:
         blocks = (pos - S) // B
         for b in np.unique(blocks):
             sel = pos[blocks == b]
-            r = self.r_of_block(int(b))
+            r, keep = self.r_of_block(int(b)), self.keep_of_block(int(b))
             for src, dst_idx, dst_val, dense in ((self.Kr, self.kidx, self.kval, self.Kt),
                                                 (self.Vr, self.vidx, self.vval, self.Vt)):
-                idx, vals = topr_select(src[sel].astype(np.float64), r)
+                idx, vals = topr_select(src[sel].astype(np.float64), r, keep)
                 dst_idx[sel, :r] = idx
                 dst_idx[sel, r:] = 0
                 dst_val[sel, :r] = vals

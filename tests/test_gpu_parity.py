@@ -85,6 +85,23 @@ def test_append_storage_multisegment_r128_block64():
         _check_storage(p, u)
 
 
+def test_append_storage_truncated_bottom_channels():
+    # [S] sec. 5.2: the bottom rotated channels are truncated before the
+    # per-vector top-r (here the first 96 of 128 are eligible).
+    case = Case(n_q=4, n_kv=2, seq_lens=[1500, 400], rot="perm", window=64,
+                segments=[(0, 38, 0, 96), (500, 64, 1, 96)], steps=[1] * 30 + [7], seed=21)
+    p = Pair(case)
+    for u in p.units:
+        _check_storage(p, u)
+    p.run_steps()
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    for u in p.units:
+        _check_storage(p, u)
+        oc = p.orc[u]
+        assert int(oc.kidx[:oc.T].max()) < 96 and int(oc.vidx[:oc.T].max()) < 96
+
+
 def test_append_from_empty_through_sinks_and_window():
     # Starts below S+W; single-token appends walk through sinks, window, middle.
     case = Case(n_q=2, n_kv=1, seq_lens=[2], rot="perm", n_sink=4, window=16, block=16,
@@ -211,9 +228,11 @@ def test_block_select_all_ties_large(T, retain, segments):
          segments=[(0, 32, 0)], seed=14),
     Case(n_q=4, n_kv=1, seq_lens=[40], rot="eigh", window=64, seed=15),          # empty middle
     Case(n_q=2, n_kv=1, seq_lens=[3], rot="eigh", n_sink=4, window=8, seed=16),  # T < S
+    Case(n_q=4, n_kv=2, seq_lens=[3000], rot="eigh", block=32, segments=[(0, 38, 0, 96)], steps=[1, 1, 2],
+         seed=18),                                                                 # bottom 25% truncated
     Case(n_q=4, n_kv=1, seq_lens=[1500], rot="eigh", segments=[(0, 128, 0)], topk_fixed=10 ** 6,
          retain_permille=0, seed=17),                                              # r = d, all blocks
-], ids=["gqa4-2seq", "b64-5pct", "serving-segments", "single-head-c1", "empty-middle", "below-sinks",
+], ids=["gqa4-2seq", "b64-5pct", "serving-segments", "single-head-c1", "empty-middle", "below-sinks", "truncated-96",
         "r128-allblocks"])
 def test_decode_attention_matches_oracle(case):
     p = Pair(case)

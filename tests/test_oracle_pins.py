@@ -106,6 +106,26 @@ def test_topr_d128_against_python_sort():
     assert np.array_equal(idx, np.tile(np.arange(38), (4, 1)))
 
 
+def test_topr_truncated_bottom_channels_brute_force():
+    # [S] sec. 5.2: only the first `keep` channels are candidates.  Brute
+    # force over the truncated vector, and (an independent form) the top-r of
+    # the vector whose bottom channels are zeroed, which agrees whenever the
+    # candidates hold at least r nonzero magnitudes.
+    rng = np.random.default_rng(22)
+    for _ in range(300):
+        d = int(rng.integers(3, 10))
+        keep = int(rng.integers(1, d + 1))
+        r = int(rng.integers(1, keep + 1))
+        x = rng.integers(-3, 4, size=d).astype(np.float64)
+        idx, vals = O.topr_select(x, r, keep)
+        want = _brute_topr(x[:keep], r)
+        assert list(idx[0]) == want and np.array_equal(vals[0], x[want])
+        if np.count_nonzero(x[:keep]) >= r:
+            z = x.copy()
+            z[keep:] = 0.0
+            assert list(O.topr_select(z, r)[0][0]) == want
+
+
 # ---------------------------------------------------------- rotation ----
 def _gen(T, decay, seed, outliers=True):
     x = synth.lowrank_outlier(T, 128, decay, seed, n_outlier_channels=4 if outliers else 0)
