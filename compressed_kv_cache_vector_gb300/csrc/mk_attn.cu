@@ -51,13 +51,14 @@
 namespace mk {
 
 namespace {
-constexpr int kMaxWarps = 12;                // one CTA per SM, 8 or 12 warps (shared memory decides)
+constexpr int kMaxWarps = 16;                // one CTA per SM, 4 to 16 warps (shared memory decides)
 constexpr int kTG = 16;                      // tokens per packed group (one MMA tile)
 constexpr int kDC = 8;                       // tokens per dense chunk
 constexpr int kRow = D + 8;                  // padded bf16 row: 272 bytes, ldmatrix conflict-free
 constexpr int kTileBytes = kTG * kRow * 2;   // 16-row tile
 constexpr int kDenseStage = 2 * kDC * kRow * 2;  // staged dense chunk: 8 K rows + 8 V rows
 constexpr int kIdsCap = 256;                 // block ids a CTA caches in shared memory
+constexpr int kLongSelTokens = 32768;        // selected tokens per unit from which 16 warps pay off
 constexpr float kLazy = 8.0f;                // log2 headroom before the running max is raised
 constexpr float kScaleLog2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
@@ -180,10 +181,25 @@ size_t attn_plan(Layout& L, int /*r_min*/) {
   // warps as fit.
   // Warps per CTA are a multiple of 4, an equal share for each of the SM's
   // four sub-partitions.
+  // Long selections (many 16-token groups per warp) are bound by the main
+  // loop's densify work: 16 warps with one stage each (the next copy goes out
+  // as soon as a stage is consumed) beat 12 warps with two.  Short ones are
+  // bound by each warp's latency chain: two stages, 12 warps (which also get
+  // more registers).
+  const bool long_sel = (int64_t)L.k_max * L.B >= kLongSelTokens;
   int plans[8][2] = {{2, 12}, {2, 8}, {2, 4}, {0, 0}, {0, 0}, {0, 0}, {0, 0}, {0, 0}};
+  if (long_sel) {
+    const int lp[4][2] = {{1, 16}, {2, 12}, {2, 8}, {2, 4}};
+    for (int i = 0; i < 4; ++i) {
+      plans[i][0] = lp[i][0];
+      plans[i][1] = lp[i][1];
+    }
+  }
   if (const char* e = std::getenv("MK_ATTN_PLAN")) {  // tuning override: "stages,warps"
     int a = 0, b = 0;
-    if (std::sscanf(e, "%d,%d", &a, &b) == 2 && a >= 2 && b >= 4 && b <= kMaxWarps && b % 4 == 0) {
+    // one stage goes with 16 warps, two or more with at most 12
+    if (std::sscanf(e, "%d,%d", &a, &b) == 2 && b >= 4 && b <= kMaxWarps && b % 4 == 0 &&
+        ((b > 12 && a == 1) || (b <= 12 && a >= 2))) {
       plans[0][0] = a;
       plans[0][1] = b;
     }
@@ -213,8 +229,8 @@ int attn_max_parts(const Layout& L) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(MK_MAX_SPLITS, avail / ((int64_t)L.G * (D + 2) * 4)));
 }
 
-template <int G, bool DENSE>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer, CallSeqs cs, int P,
+template <int G, bool DENSE, int MAXW>
+__global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, CallSeqs cs, int P,
                                                  const int32_t* __restrict__ ids,
                                                  const int32_t* __restrict__ n_sel_in,
                                                  const uint16_t* __restrict__ q_in, const uint16_t* __restrict__ Kd,
@@ -429,8 +445,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   auto has_copy = [](const Task& t) { return t.kind == 1 || t.kind == 2; };
 
   // Ring of NST stages: the task being consumed sits in stage st, the next
-  // NST - 1 tasks are in flight.  ph: parity of each stage's next phase;
-  // pend: stages with copies in flight.
+  // NST - 1 tasks are in flight.  With one stage, the next task's copy goes
+  // out as soon as the current one's stage is consumed (after the scatter of
+  // a packed group, after the value product of a dense chunk).  ph: parity of
+  // each stage's next phase; pend: stages with copies in flight.
   Task cur = make_task(warp, 0), ahead = cur;
   int st = 0;
   uint32_t ph = 0, pend = 0;
@@ -456,8 +474,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
   const int mi = lane >> 3, ri = lane & 7;
   const int ktok = ri + (mi >> 1) * 8, kch = (mi & 1) * 8;  // ldmatrix rows for the key B fragments
   const int vtok = ri + (mi >> 1) * 8, vch = (mi & 1) * 8;  // ldmatrix.trans rows for the value A fragments
+  // The 16-warp plan has one stage (kOneStage); the 12-warp plans two or more.
+  constexpr bool kOneStage = MAXW > 12;
   while (cur.kind != 0) {
-    {
+    bool next_out = !kOneStage;
+    auto issue_next = [&]() {  // one stage: the next task into the consumed stage
+      if (!kOneStage || next_out) return;
+      __syncwarp();
+      ahead = advance(cur);
+      issue(ahead, st);
+      if (has_copy(ahead)) pend |= 1u << st;
+      next_out = true;
+    };
+    if (!kOneStage) {
       const int sn = st + NST - 1 < NST ? st + NST - 1 : st - 1;  // (st + NST - 1) mod NST
       ahead = advance(ahead);
       issue(ahead, sn);
@@ -514,6 +543,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
         scatter_kv(smem_u32(tk), smem_u32(tv), smem_u32(kval), smem_u32(kidx), smem_u32(vval), smem_u32(vidx), n_el,
                    rm, lane);
         __syncwarp();
+        issue_next();  // the packed group now lives in the tiles
         krow = tk + ktok * kRow + kch;
         vrow = tv + vtok * kRow + vch;
       }
@@ -589,6 +619,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
         }
       }
     }
+    issue_next();  // dense chunk, skipped item: after every use of the stage
     __syncwarp();
     cur = advance(cur);
     st = st + 1 < NST ? st + 1 : 0;
@@ -806,18 +837,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) k_attn(Layout L, int layer,
 }
 
 namespace {
-template <int G, bool DENSE>
+template <int G, bool DENSE, int MAXW>
 cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                        const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
                        int max_items, size_t smem, cudaStream_t s) {
   static size_t set_bytes = 0;
   static int occ = 1, sms = 0;
   if (smem > set_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn<G, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_attn<G, DENSE, MAXW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     set_bytes = smem;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn<G, DENSE>, L.attn_nc * 32, smem) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn<G, DENSE, MAXW>, L.attn_nc * 32, smem) != cudaSuccess) {
       (void)cudaGetLastError();
       n = 1;
     }
@@ -833,7 +864,7 @@ cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int
   P = std::min(P, attn_max_parts(L));
   if (std::getenv("MK_LOG"))
     std::fprintf(stderr, "[mosaickv] attention: %d units x %d CTAs (%d per SM), %zu B smem\n", units, P, occ, smem);
-  return launch_pdl(k_attn<G, DENSE>, dim3(units * P), dim3(L.attn_nc * 32), smem, s, 0, L, layer, cs, P, ids, n_sel, q, K, V,
+  return launch_pdl(k_attn<G, DENSE, MAXW>, dim3(units * P), dim3(L.attn_nc * 32), smem, s, 0, L, layer, cs, P, ids, n_sel, q, K, V,
                     t_stride, out);
 }
 
@@ -843,11 +874,20 @@ cudaError_t launch_attn_g(const Layout& L, int layer, const CallSeqs& cs, const 
                           int max_items, cudaStream_t s) {
   const size_t smem = attn_smem_bytes(L, 0);
   if (smem == 0 || smem > 227 * 1024) return cudaErrorInvalidConfiguration;
+  const bool wide = L.attn_nc > 12;  // launch bounds of 16 warps (at most 128 registers)
   switch (L.G) {
-    case 1: return launch_one<1, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
-    case 2: return launch_one<2, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
-    case 4: return launch_one<4, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
-    case 8: return launch_one<8, DENSE>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+    case 1:
+      return wide ? launch_one<1, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s)
+                  : launch_one<1, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+    case 2:
+      return wide ? launch_one<2, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s)
+                  : launch_one<2, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+    case 4:
+      return wide ? launch_one<4, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s)
+                  : launch_one<4, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+    case 8:
+      return wide ? launch_one<8, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s)
+                  : launch_one<8, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }

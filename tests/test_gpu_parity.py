@@ -230,9 +230,11 @@ def test_block_select_all_ties_large(T, retain, segments):
     Case(n_q=2, n_kv=1, seq_lens=[3], rot="eigh", n_sink=4, window=8, seed=16),  # T < S
     Case(n_q=4, n_kv=2, seq_lens=[3000], rot="eigh", block=32, segments=[(0, 38, 0, 96)], steps=[1, 1, 2],
          seed=18),                                                                 # bottom 25% truncated
+    Case(n_q=4, n_kv=1, seq_lens=[42000], rot="eigh", block=64, window=128, topk_fixed=600, retain_permille=0,
+         steps=[1, 1], seed=19),                                                   # long selection: 16-warp plan
     Case(n_q=4, n_kv=1, seq_lens=[1500], rot="eigh", segments=[(0, 128, 0)], topk_fixed=10 ** 6,
          retain_permille=0, seed=17),                                              # r = d, all blocks
-], ids=["gqa4-2seq", "b64-5pct", "serving-segments", "single-head-c1", "empty-middle", "below-sinks", "truncated-96",
+], ids=["gqa4-2seq", "b64-5pct", "serving-segments", "single-head-c1", "empty-middle", "below-sinks", "truncated-96", "long-16warps",
         "r128-allblocks"])
 def test_decode_attention_matches_oracle(case):
     p = Pair(case)
