@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
       if (has_copy(ahead)) pend |= 1u << sn;
     }
     if (has_copy(cur)) {
-      if (!mbar_wait(&bars[st], (ph >> st) & 1u)) {
+      if (!mbar_wait_warp(&bars[st], (ph >> st) & 1u)) {
         if (lane == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, st, (int32_t)MK_ETIMEOUT);
         broken = true;
         break;

@@ -283,6 +283,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
     if (global_ns() - t0 > 20000000ull) return false;
   return true;
 }
+// The same for a full warp whose lanes then branch together on the result:
+// if any lane gave up, all report failure (a lane that saw the phase
+// complete finds it complete again in the caller's drain).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, unsigned parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
+}
 // Programmatic dependent launch: a kernel launched with the
 // programmatic-serialization attribute may start while the previous kernel
 // in the stream finishes.  It must call pdl_wait() before touching anything

@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   __shared__ __align__(16) uint32_t hc[kKeyBins];   // coarse key histogram
   __shared__ int s_abort;
   __shared__ __align__(8) uint64_t s_rbar;
+  __shared__ __align__(8) uint64_t s_tbar[kSelWarps][2];  // each warp's two meta-tile stages
   __shared__ uint32_t bqs[3][16][2][32];            // B fragments, staged once
 
   const int unit_call = blockIdx.x / P, part = blockIdx.x - unit_call * P;
@@ -107,6 +108,10 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const unsigned r_bytes = (unsigned)((APPEND && part == 0) ? 2 : 1) * D * D * 4;
   if (tid == 0) {
     mbar_init(&s_rbar, 1);
+    for (int w = 0; w < kSelWarps; ++w) {
+      mbar_init(&s_tbar[w][0], 1);
+      mbar_init(&s_tbar[w][1], 1);
+    }
     mbar_init_fence();
     mbar_expect_tx(&s_rbar, r_bytes);
     bulk_g2s(smem, base + L.off_rkt, r_bytes, &s_rbar);
@@ -199,7 +204,8 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
       else
         append_small_body(L, ud, const_cast<char*>(base), T_cur, n, n, kin + row0, vin + row0, in_stride,
                           reinterpret_cast<const float*>(smem), xs, rot);
-      __threadfence();  // the updated block min/max before this CTA's own tiles are read
+      __threadfence();          // the updated block min/max before this CTA's own tiles are read,
+      fence_proxy_async_all();  // which the bulk copies (async proxy) do
     }
     T_cur += n;
   }
@@ -221,13 +227,22 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   uint32_t* kw = L.keys + slot * L.keys_stride;
   float* so = scores_out ? scores_out + ((int64_t)ci * L.n_kv + kvh) * L.nblk_cap : nullptr;
   unsigned char* stg = smem + (size_t)warp * 2 * kMetaTile;
-  auto issue = [&](int t, unsigned char* dst) {
+  // Tile t (16 blocks) into stage sidx: one 512-byte bulk copy per block row
+  // (rows padded to kMetaRow for conflict-free ldmatrix), on the stage's
+  // barrier; rows past the last block are not loaded (and not scored).
+  uint32_t tph = 0, tpend = 0;  // per stage: phase parity, copy in flight
+  auto issue = [&](int t, int sidx) {
     if (t >= t1) return;
-    for (int i = lane; i < kMT * 32; i += 32) {
-      const int row = i >> 5, prt = i & 31;
-      const int b = t * kMT + row;
-      if (b < nblk) cp_async16(dst + row * kMetaRow * 2 + prt * 16, meta + (int64_t)b * 2 * D + prt * 8);
+    unsigned char* dst = stg + (size_t)sidx * kMetaTile;
+    const int nrow = min(kMT, nblk - t * kMT);
+    if (lane == 0) {
+      fence_proxy_async();  // the stage was last read by ldmatrix
+      mbar_expect_tx(&s_tbar[warp][sidx], (unsigned)nrow * 2u * D * 2u);
     }
+    __syncwarp();
+    if (lane < nrow)
+      bulk_g2s(dst + lane * kMetaRow * 2, meta + (int64_t)(t * kMT + lane) * 2 * D, 2 * D * 2, &s_tbar[warp][sidx]);
+    tpend |= 1u << sidx;
   };
   // Write block b's score: the user's fp32 copy, the key, the histogram count.
   auto emit = [&](int b, float sc) {
@@ -239,13 +254,15 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const float inv_sqrt_d = 0.08838834764831845f;
   int st = 0;
   int t = t0 + warp;
-  issue(t, stg);
-  cp_async_commit();
+  issue(t, 0);
   for (; t < t1; t += kSelWarps) {
-    issue(t + kSelWarps, stg + (size_t)(st ^ 1) * kMetaTile);
-    cp_async_commit();
-    asm volatile("cp.async.wait_group 1;\n" ::: "memory");
-    __syncwarp();
+    issue(t + kSelWarps, st ^ 1);
+    if (!mbar_wait_warp(&s_tbar[warp][st], (tph >> st) & 1u)) {
+      if (lane == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -5, (int32_t)MK_ETIMEOUT);
+      break;
+    }
+    tph ^= 1u << st;
+    tpend &= ~(1u << st);
     const uint16_t* tile = reinterpret_cast<const uint16_t*>(stg + (size_t)st * kMetaTile);
     float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const int mi = lane >> 3, ri = lane & 7;
@@ -274,7 +291,9 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     __syncwarp();
     st ^= 1;
   }
-  cp_async_wait_all();
+  // Only after a timed-out wait can copies still be landing: let them.
+  for (int i = 0; i < 2; ++i)
+    if ((tpend >> i) & 1u) (void)mbar_wait(&s_tbar[warp][i], (tph >> i) & 1u);
   __syncthreads();
   // Add this CTA's histogram to the unit's (the top-k kernel reads it).
   uint32_t* gh = L.khist + slot * kKeyBins;
