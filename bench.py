@@ -38,6 +38,9 @@ D = 128
 # (append + scoring), k_topk and k_attn; the separate path adds k_append_small
 # in front of the same three.
 LAUNCHES_PER_LAYER = {False: 3, True: 4}
+# Untimed steps between the warm-up and the timed region while the clock
+# sampler starts (each appends one token per layer, so capacity allows them).
+CLOCK_SOAK_STEPS = 200
 
 
 def max_over_ranks(x, dist, device):
@@ -132,7 +135,7 @@ class Clocks:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -302,7 +305,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     from compressed_kv_cache_vector_gb300 import binding, synth
-    extra = 4 * (a.warmup + a.steps) + 32
+    extra = 4 * (a.warmup + a.steps) + 32 + CLOCK_SOAK_STEPS
     mk = build_gpu(wl, dev, rank, extra)
     L, n_seq, Hq, Hkv = wl.n_layers, wl.n_seqs, wl.n_q_heads, wl.n_kv_heads
     seqs = list(range(n_seq))
@@ -354,13 +357,24 @@ def main():
     mk.sync_state()
     T_start = [mk.seq_length(0, si) for si in seqs]
 
+    # Clocks: nvidia-smi every 20 ms from the start of the warm-up (its own
+    # start-up takes longer than the short timed region) to the end of the
+    # timed regions; every sample is taken under the same load.
+    clocks = Clocks(local)
+    clocks.start()
     for _ in range(a.warmup):
         graph.replay()
+    # A few more untimed steps (at most CLOCK_SOAK_STEPS, about 0.2 s) so that
+    # the sampler's first readings fall under this load, not before it.
+    t_soak = time.perf_counter() + 0.2
+    n_soak = 0
+    while n_soak < CLOCK_SOAK_STEPS and time.perf_counter() < t_soak:
+        graph.replay()
+        torch.cuda.synchronize()
+        n_soak += 1
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    clocks = Clocks(local)
-    clocks.start()
     # Timed region A: K steps back to back (the reported value).
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -390,7 +404,7 @@ def main():
     ms = max_over_ranks(ms, dist, dev)
 
     # algorithmic bytes at the mean length of the timed steps
-    T_mid = [t + a.warmup + a.steps / 2 for t in T_start]
+    T_mid = [t + a.warmup + n_soak + a.steps / 2 for t in T_start]
     firsts = [segment_firsts(wl, T0) for T0 in wl.seq_lens]
     per = {"append": 0, "select": 0, "attn": 0}
     for si, T in enumerate(T_mid):
@@ -505,6 +519,7 @@ def main():
                 config=dict(wcfg, l2="step reads ~%.2f GB across layers, far above the 129 MB L2" %
                             (step_bytes / 1e9),
                             timing="CUDA graph of one full step, replayed; CUDA events on the stream",
+                            untimed_soak_steps=n_soak,
                             calls=("mk_append_compress + mk_block_select + mk_decode_attn" if a.separate else
                                    "mk_append_select + mk_decode_attn") + " per layer"),
                 hbm_gbs=gbs, alg_bytes_per_step=step_bytes, roofline=roofline, phases=phases,
