@@ -71,6 +71,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dense-ref", action="store_true", help="also time the uncompressed reference kernel")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling runs)")
+    ap.add_argument("--meta-channels", type=int, default=0,
+                    help="variant: channel-compressed per-block keys keeping this many channels")
     ap.add_argument("--separate", action="store_true",
                     help="append and block selection as two launches (default: mk_append_select, one launch)")
     return ap.parse_args()
@@ -101,10 +103,12 @@ def unit_bytes(wl, T, firsts):
     else:
         k = min(max(1, (wl.retain_permille * scored + 999) // 1000), scored) if scored else 0
     dense = min(S, T) + (T - (S + mid))
-    sel = nblk * 2 * D * 2 + G * D * 2 + D * D * 4
+    mc = getattr(wl, "meta_channels", 0)
+    key_row = (5 * mc + 15) // 16 * 16 if mc else 2 * D * 2   # a block's key as the scoring reads it
+    sel = nblk * key_row + G * D * 2 + D * D * 4
     attn = k * 6 * B * r_scored + always_bytes + dense * 2 * D * 2 + D * D * 4 + G * D * (4 + 2)
     r_new = segs[-1][1]
-    app = 2 * D * 2 + 2 * D * D * 4 + 2 * D * 2 + 2 * D * 2 + 6 * r_new + 2 * 2 * D * 2
+    app = 2 * D * 2 + 2 * D * D * 4 + 2 * D * 2 + 2 * D * 2 + 6 * r_new + 2 * 2 * D * 2 + (key_row if mc else 0)
     return {"append": app, "select": sel, "attn": attn}
 
 
@@ -228,7 +232,7 @@ def build_gpu(wl, dev, rank, capacity_extra):
     build()
     cfg = binding.make_config(wl.n_q_heads, wl.n_kv_heads, wl.n_layers, wl.n_seqs,
                               max(wl.seq_lens) + capacity_extra, wl.n_sink, wl.window, wl.block,
-                              wl.segments, wl.topk_fixed, wl.retain_permille)
+                              wl.segments, wl.topk_fixed, wl.retain_permille, wl.meta_channels)
     mk = binding.MosaicKV(cfg, dev)
     seqs = list(range(wl.n_seqs))
     prefill_ms = mk.prefill_ms = []
@@ -273,6 +277,9 @@ def main():
     if a.layers:
         wl.n_layers = a.layers
         wl.name += f"-{a.layers}layer"
+    if a.meta_channels:
+        wl.meta_channels = a.meta_channels
+        wl.name += f"-keys{a.meta_channels}ch"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

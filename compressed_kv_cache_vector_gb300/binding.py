@@ -40,7 +40,7 @@ class MkConfig(ctypes.Structure):
     _fields_ = [("head_dim", c_i32), ("n_q_heads", c_i32), ("n_kv_heads", c_i32), ("n_layers", c_i32),
                 ("max_seqs", c_i32), ("max_tokens", c_i32), ("n_sink", c_i32), ("window", c_i32),
                 ("block", c_i32), ("topk_fixed", c_i32), ("retain_permille", c_i32),
-                ("n_segments", c_i32), ("seg", MkSegment * MK_MAX_SEGMENTS)]
+                ("n_segments", c_i32), ("seg", MkSegment * MK_MAX_SEGMENTS), ("meta_channels", c_i32)]
 
 
 class MkAlg2Params(ctypes.Structure):
@@ -56,7 +56,8 @@ class MkLayoutInfo(ctypes.Structure):
     _fields_ = [("rkt", c_i64), ("rvt", c_i64), ("rv", c_i64), ("sink_k", c_i64), ("sink_v", c_i64),
                 ("win_k", c_i64), ("win_v", c_i64), ("meta", c_i64), ("pages", c_i64),
                 ("page_stride", c_i64), ("nblk_cap", c_i32), ("T", c_i32),
-                ("seg_first_block", c_i32 * MK_MAX_SEGMENTS), ("n_segments", c_i32), ("reserved", c_i32)]
+                ("seg_first_block", c_i32 * MK_MAX_SEGMENTS), ("n_segments", c_i32), ("reserved", c_i32),
+                ("cmeta", c_i64), ("cmeta_row", c_i32), ("meta_channels", c_i32)]
 
 
 _SIGS = {
@@ -133,13 +134,14 @@ def _stream(stream=None):
 
 
 def make_config(n_q_heads, n_kv_heads, n_layers, max_seqs, max_tokens, n_sink, window, block,
-                segments, topk_fixed=0, retain_permille=0) -> MkConfig:
+                segments, topk_fixed=0, retain_permille=0, meta_channels=0) -> MkConfig:
     c = MkConfig()
     c.head_dim = MK_HEAD_DIM
     c.n_q_heads, c.n_kv_heads, c.n_layers = n_q_heads, n_kv_heads, n_layers
     c.max_seqs, c.max_tokens = max_seqs, max_tokens
     c.n_sink, c.window, c.block = n_sink, window, block
     c.topk_fixed, c.retain_permille = topk_fixed, retain_permille
+    c.meta_channels = meta_channels
     c.n_segments = len(segments)
     for i, sg in enumerate(segments):
         b, r, a = sg[:3]
@@ -277,6 +279,8 @@ class MosaicKV:
             "meta": words(L["meta"], L["nblk_cap"] * 2 * D).view(L["nblk_cap"], 2, D),
             "pages": a[L["pages"]:L["pages"] + L["nblk_cap"] * L["page_stride"]].view(
                 L["nblk_cap"], L["page_stride"]),
+            "cmeta": (a[L["cmeta"]:L["cmeta"] + L["nblk_cap"] * L["cmeta_row"]].view(L["nblk_cap"], L["cmeta_row"])
+                      if L["meta_channels"] else None),
             "layout": L,
         }
 

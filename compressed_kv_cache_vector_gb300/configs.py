@@ -28,6 +28,7 @@ class Workload:
     segments: list          # [(begin_permille, r, always)]
     topk_fixed: int = 0     # > 0: select exactly this many blocks
     retain_permille: int = 0
+    meta_channels: int = 0        # > 0: channel-compressed per-block keys (a variant; 0 in every listed workload)
     decay: float = 0.92
     append_per_step: int = 1
     description: str = ""

@@ -49,6 +49,7 @@ mk_status check_config(const mk_config* c) {
   if (c->topk_fixed < 0 || c->retain_permille < 0 || c->retain_permille > 1000) return MK_EINVAL;
   if (c->topk_fixed == 0 && c->retain_permille == 0) return MK_EINVAL;
   if (c->n_segments < 1 || c->n_segments > MK_MAX_SEGMENTS) return MK_EINVAL;
+  if (c->meta_channels < 0 || c->meta_channels > MK_MAX_META_CHANNELS) return MK_EINVAL;
   int prev = 0;
   for (int i = 0; i < c->n_segments; ++i) {
     const mk_segment& s = c->seg[i];
@@ -95,6 +96,9 @@ Plan make_plan(const mk_config* c) {
   L.off_win_v = off; off = align_up(off + (int64_t)L.W * D * 2);
   L.off_meta = off; off = align_up(off + (int64_t)std::max(1, L.nblk_cap) * 2 * D * 2);
   L.off_pages = off; off = align_up(off + (int64_t)std::max(1, L.nblk_cap) * L.page_stride);
+  L.meta_c = c->meta_channels;
+  L.cmeta_row = L.meta_c > 0 ? (5 * L.meta_c + 15) / 16 * 16 : 0;
+  L.off_cmeta = off; off = align_up(off + (int64_t)std::max(1, L.nblk_cap) * L.cmeta_row);
   L.unit_stride = off;
   p.n_units = (int64_t)c->n_layers * c->max_seqs * c->n_kv_heads;
   p.units_off = align_up(kAlign + p.n_units * (int64_t)sizeof(UnitDesc));
@@ -563,6 +567,9 @@ mk_status mk_layout(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, mk
   out->T = ctx->T[ls];
   for (int s = 0; s < MK_MAX_SEGMENTS; ++s) out->seg_first_block[s] = ctx->firsts[ls * MK_MAX_SEGMENTS + s];
   out->n_segments = ctx->cfg.n_segments;
+  out->cmeta = base + L.off_cmeta;
+  out->cmeta_row = L.cmeta_row;
+  out->meta_channels = L.meta_c;
   return MK_OK;
 }
 

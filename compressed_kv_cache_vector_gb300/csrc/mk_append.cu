@@ -261,6 +261,25 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
       }
       meta[(int64_t)b * 2 * D + c] = f2bf(mn);
       meta[(int64_t)b * 2 * D + D + c] = f2bf(mx);
+      if (L.meta_c > 0) {  // the rows for the compressed keys, over the (now free) A tile
+        uint16_t* bm = reinterpret_cast<uint16_t*>(Xs) + (b - b0) * 2 * D;
+        bm[c] = f2bf(mn);
+        bm[D + c] = f2bf(mx);
+      }
+    }
+  }
+  if (L.meta_c > 0 && mlo < mhi) {
+    __syncthreads();
+    const int b0 = (mlo - S) / B, b1 = (mhi - 1 - S) / B;
+    for (int b = b0 + warp; b <= b1; b += 8) {
+      const uint16_t* bm = reinterpret_cast<const uint16_t*>(Xs) + (b - b0) * 2 * D;
+      uint16_t mn[4], mx[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mn[i] = bm[4 * lane + i];
+        mx[i] = bm[D + 4 * lane + i];
+      }
+      compress_key_row(L, base, b, mn, mx, lane);
     }
   }
 }

@@ -46,6 +46,34 @@ __device__ __forceinline__ unsigned warp_topr(const uint32_t m[4], int r, int la
   return keep;
 }
 
+// Channel-compressed key of block b ([S] sec. 5.2: the per-block keys are
+// channel-compressed like the vectors): from the block's min/max row (four
+// channels per lane, 4*lane .. 4*lane+3), keep the L.meta_c channels with the
+// largest bound magnitude max(|min|, |max|), ties to the lower channel, and
+// store them in ascending channel order as [min x m][max x m][channel x m].
+// Called by one full warp.
+__device__ __forceinline__ void compress_key_row(const Layout& L, char* base, int b, const uint16_t mn[4],
+                                                 const uint16_t mx[4], int lane) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = max((uint32_t)(mn[i] & 0x7fffu), (uint32_t)(mx[i] & 0x7fffu));
+  int rank;
+  const unsigned kb = warp_topr(w, L.meta_c, lane, rank);
+  char* row = base + L.off_cmeta + (int64_t)b * L.cmeta_row;
+  uint16_t* cmn = reinterpret_cast<uint16_t*>(row);
+  uint16_t* cmx = cmn + L.meta_c;
+  uint8_t* cch = reinterpret_cast<uint8_t*>(cmx + L.meta_c);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (kb >> i & 1u) {
+      cmn[rank] = mn[i];
+      cmx[rank] = mx[i];
+      cch[rank] = (uint8_t)(4 * lane + i);
+      ++rank;
+    }
+  }
+}
+
 // Compresses one rotated vector (128 bf16 words at `row`) of middle position
 // `pos` into its page; for a key also folds it into the block's min/max.
 // Called by one full warp.  Returns this lane's keep bits.
@@ -107,6 +135,7 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
         make_uint2((uint32_t)nmn[0] | ((uint32_t)nmn[1] << 16), (uint32_t)nmn[2] | ((uint32_t)nmn[3] << 16));
     *reinterpret_cast<uint2*>(meta + D + 4 * lane) =
         make_uint2((uint32_t)nmx[0] | ((uint32_t)nmx[1] << 16), (uint32_t)nmx[2] | ((uint32_t)nmx[3] << 16));
+    if (L.meta_c > 0) compress_key_row(L, base, b, nmn, nmx, lane);
   }
   return kbits;
 }

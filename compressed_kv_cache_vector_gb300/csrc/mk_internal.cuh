@@ -53,6 +53,8 @@ struct Layout {
   int64_t off_rkt, off_rvt, off_rv, off_sink_k, off_sink_v, off_win_k, off_win_v;
   int64_t off_rkp, off_rvp;     // R_k, R_v as three bf16 parts each, tensor-core operand layout
   int64_t off_meta, off_pages;
+  int64_t off_cmeta;            // compressed per-block keys (meta_c > 0): [nblk_cap][cmeta_row] bytes
+  int32_t meta_c, cmeta_row;    // channels a compressed key keeps (0 = none), bytes per row
   int64_t page_stride;
   int32_t S, W, B, n_kv, G, max_seqs, nblk_cap, cap_tokens, n_layers, k_max;
   int32_t topk_fixed, retain_permille, r_max;

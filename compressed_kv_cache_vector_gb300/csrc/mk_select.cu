@@ -231,17 +231,33 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   // (rows padded to kMetaRow for conflict-free ldmatrix), on the stage's
   // barrier; rows past the last block are not loaded (and not scored).
   uint32_t tph = 0, tpend = 0;  // per stage: phase parity, copy in flight
+  // With channel-compressed keys (L.meta_c > 0) a stage holds the tile's
+  // compressed rows (one bulk copy), rebuilt into one dense tile after it.
+  const bool cmp = L.meta_c > 0;
+  const int mc = L.meta_c;
+  const char* cmeta = base + L.off_cmeta;
+  auto cstage = [&](int sidx) { return stg + kMetaTile + (size_t)sidx * kMT * L.cmeta_row; };
   auto issue = [&](int t, int sidx) {
     if (t >= t1) return;
-    unsigned char* dst = stg + (size_t)sidx * kMetaTile;
     const int nrow = min(kMT, nblk - t * kMT);
-    if (lane == 0) {
-      fence_proxy_async();  // the stage was last read by ldmatrix
-      mbar_expect_tx(&s_tbar[warp][sidx], (unsigned)nrow * 2u * D * 2u);
+    if (cmp) {
+      if (lane == 0) {
+        fence_proxy_async();  // the stage was last read by the rebuild
+        mbar_expect_tx(&s_tbar[warp][sidx], (unsigned)(nrow * L.cmeta_row));
+        bulk_g2s(cstage(sidx), cmeta + (int64_t)t * kMT * L.cmeta_row, (unsigned)(nrow * L.cmeta_row),
+                 &s_tbar[warp][sidx]);
+      }
+      __syncwarp();
+    } else {
+      unsigned char* dst = stg + (size_t)sidx * kMetaTile;
+      if (lane == 0) {
+        fence_proxy_async();  // the stage was last read by ldmatrix
+        mbar_expect_tx(&s_tbar[warp][sidx], (unsigned)nrow * 2u * D * 2u);
+      }
+      __syncwarp();
+      if (lane < nrow)
+        bulk_g2s(dst + lane * kMetaRow * 2, meta + (int64_t)(t * kMT + lane) * 2 * D, 2 * D * 2, &s_tbar[warp][sidx]);
     }
-    __syncwarp();
-    if (lane < nrow)
-      bulk_g2s(dst + lane * kMetaRow * 2, meta + (int64_t)(t * kMT + lane) * 2 * D, 2 * D * 2, &s_tbar[warp][sidx]);
     tpend |= 1u << sidx;
   };
   // Write block b's score: the user's fp32 copy, the key, the histogram count.
@@ -264,6 +280,26 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     tph ^= 1u << st;
     tpend &= ~(1u << st);
     const uint16_t* tile = reinterpret_cast<const uint16_t*>(stg + (size_t)st * kMetaTile);
+    if (cmp) {
+      // Zero-filled dense rows [min | max] from the compressed ones: the
+      // dropped channels count as zero in the score.
+      uint16_t* dt = reinterpret_cast<uint16_t*>(stg);
+      for (int i = lane; i < kMT * 32; i += 32)
+        *reinterpret_cast<uint4*>(dt + (i >> 5) * kMetaRow + (i & 31) * 8) = make_uint4(0, 0, 0, 0);
+      __syncwarp();
+      const int nrow = min(kMT, nblk - t * kMT);
+      const unsigned char* cs = cstage(st);
+      for (int e = lane; e < nrow * mc; e += 32) {
+        const int row = e / mc, i = e - row * mc;
+        const unsigned char* crow = cs + row * L.cmeta_row;
+        const uint16_t* cv = reinterpret_cast<const uint16_t*>(crow);
+        const int ch = crow[4 * mc + i];
+        dt[row * kMetaRow + ch] = cv[i];
+        dt[row * kMetaRow + D + ch] = cv[mc + i];
+      }
+      __syncwarp();
+      tile = dt;
+    }
     float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const int mi = lane >> 3, ri = lane & 7;
     const uint16_t* arow = tile + (ri + (mi & 1) * 8) * kMetaRow + (mi >> 1) * 8;

@@ -47,6 +47,7 @@ extern "C" {
 #define MK_MAX_GROUP 8       /* query heads per kv head (GQA group) */
 #define MK_MAX_CALL_SEQS 256 /* sequences per call */
 #define MK_MAX_SPLITS 64     /* split-T work items per (sequence, kv head) */
+#define MK_MAX_META_CHANNELS 48 /* channels a compressed per-block key may keep */
 
 typedef enum mk_status {
   MK_OK = 0,
@@ -92,6 +93,13 @@ typedef struct mk_config {
   int32_t retain_permille; /* else keep ceil(retain*n/1000), clamped to [1, n] */
   int32_t n_segments;      /* 1..MK_MAX_SEGMENTS */
   mk_segment seg[MK_MAX_SEGMENTS];
+  int32_t meta_channels;   /* 0: full per-block keys (min and max over all 128
+                              channels).  1..MK_MAX_META_CHANNELS: the keys are
+                              channel-compressed too ([S] sec. 5.2): each block
+                              keeps the meta_channels channels with the largest
+                              bound magnitude max(|min|, |max|), ties to the
+                              lower channel, and the scores use those only (the
+                              others count as zero). */
 } mk_config;
 
 /* Byte offsets of one (layer, sequence, kv head) inside the arena, for tests
@@ -110,6 +118,12 @@ typedef struct mk_layout_info {
   int32_t seg_first_block[MK_MAX_SEGMENTS];
   int32_t n_segments;
   int32_t reserved;
+  int64_t cmeta;             /* compressed per-block keys (meta_channels > 0):
+                                [nblk_cap] rows of cmeta_row bytes, each
+                                [min bf16 x m][max bf16 x m][channel u8 x m],
+                                m = meta_channels, channels ascending */
+  int32_t cmeta_row;
+  int32_t meta_channels;
 } mk_layout_info;
 
 /* Sizes of the caller-owned buffers for a configuration. */

@@ -162,12 +162,31 @@ class Strategy:
     segments: list            # [(begin_permille, r, always[, keep_channels])]
     topk_fixed: int = 0
     retain_permille: int = 0
+    meta_channels: int = 0    # > 0: channel-compressed per-block keys ([S] sec. 5.2)
 
     def __post_init__(self):
         # keep_channels: the first channels eligible for the top-r; 0 or
         # absent means all of them ([S] sec. 5.2 truncates the bottom 25%).
         self.segments = [(sg[0], sg[1], sg[2], (sg[3] if len(sg) > 3 and sg[3] else D_HEAD))
                          for sg in self.segments]
+
+
+def compress_key_rows(mn, mx, m):
+    """Channel-compressed per-block keys ([S] sec. 5.2: prefill encoding
+    channel-compresses the per-block keys as it does the vectors): in each
+    block keep the m channels with the largest bound magnitude
+    max(|min|, |max|), ties to the lower channel, in ascending channel order.
+    Returns (idx [nb, m], min values, max values)."""
+    mn = np.asarray(mn, dtype=np.float64)
+    mx = np.asarray(mx, dtype=np.float64)
+    w = np.maximum(np.abs(mn), np.abs(mx))
+    idx = np.sort(np.argsort(-w, axis=1, kind="stable")[:, :m], axis=1)
+    return idx, np.take_along_axis(mn, idx, axis=1), np.take_along_axis(mx, idx, axis=1)
+
+
+def zero_filled_keys(idx, cmn, cmx, d=D_HEAD):
+    """Dense min/max rows of compressed keys: the dropped channels are zero."""
+    return densify(idx, cmn, d), densify(idx, cmx, d)
 
 
 def n_middle_blocks(T, st: Strategy):
@@ -421,9 +440,17 @@ class OracleCache:
         nb = self.n_blocks_mid()
         return np.array([b for b in range(nb) if self.always_of_block(b)], dtype=np.int64)
 
+    def score_keys(self):
+        """The per-block keys the scores use: the min/max rows, or with
+        channel-compressed keys their zero-filled dense form."""
+        mn, mx = self.meta()
+        if self.st.meta_channels:
+            mn, mx = zero_filled_keys(*compress_key_rows(mn, mx, self.st.meta_channels), self.d)
+        return mn, mx
+
     def scores(self, q):
         """Group scores over every middle block (always-blocks included)."""
-        mn, mx = self.meta()
+        mn, mx = self.score_keys()
         per, grp = block_scores(self.rotate_query(q), mn, mx)
         return per, grp
 

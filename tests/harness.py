@@ -43,6 +43,7 @@ class Case:
     seed: int = 0
     n_layers: int = 1
     oracle_units: list = None                     # [(layer, seq, kvh)]; None = all
+    meta_channels: int = 0                        # > 0: channel-compressed per-block keys
 
     @property
     def G(self):
@@ -50,7 +51,7 @@ class Case:
 
     def strategy(self):
         return O.Strategy(self.n_sink, self.window, self.block, list(self.segments),
-                          self.topk_fixed, self.retain_permille)
+                          self.topk_fixed, self.retain_permille, self.meta_channels)
 
 
 class Pair:
@@ -63,7 +64,7 @@ class Pair:
         self.T_total = [t + extra for t in case.seq_lens]
         cfg = make_config(case.n_q, case.n_kv, case.n_layers, len(case.seq_lens), max(self.T_total) + 1,
                           case.n_sink, case.window, case.block, case.segments, case.topk_fixed,
-                          case.retain_permille)
+                          case.retain_permille, case.meta_channels)
         self.mk = MosaicKV(cfg, device)
         self.K, self.V, self.R = {}, {}, {}
         units = case.oracle_units

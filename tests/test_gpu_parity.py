@@ -51,6 +51,13 @@ def _check_storage(p: Pair, unit):
     meta = bits(views["meta"])[:nb]
     assert np.array_equal(meta[:, 0], O.bf16_bits(mn))
     assert np.array_equal(meta[:, 1], O.bf16_bits(mx))
+    if p.c.meta_channels:
+        m = p.c.meta_channels
+        idx, cmn, cmx = O.compress_key_rows(mn, mx, m)
+        rows = views["cmeta"].cpu().numpy()[:nb]
+        assert np.array_equal(rows[:, :2 * m].copy().view(np.uint16), O.bf16_bits(cmn))
+        assert np.array_equal(rows[:, 2 * m:4 * m].copy().view(np.uint16), O.bf16_bits(cmx))
+        assert np.array_equal(rows[:, 4 * m:5 * m], idx.astype(np.uint8))
     pages = views["pages"].cpu().numpy()
     for b in range(nb):
         r = oc.r_of_block(b)
@@ -102,6 +109,20 @@ def test_append_storage_truncated_bottom_channels():
         assert int(oc.kidx[:oc.T].max()) < 96 and int(oc.vidx[:oc.T].max()) < 96
 
 
+def test_append_storage_compressed_block_keys():
+    # [S] sec. 5.2: the per-block keys are channel-compressed too (here 24 of 128).
+    case = Case(n_q=4, n_kv=2, seq_lens=[1300, 333], rot="perm", block=32, window=64, meta_channels=24,
+                steps=[1] * 40 + [9, 1], seed=23)
+    p = Pair(case)
+    for u in p.units:
+        _check_storage(p, u)
+    p.run_steps()
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    for u in p.units:
+        _check_storage(p, u)
+
+
 def test_append_from_empty_through_sinks_and_window():
     # Starts below S+W; single-token appends walk through sinks, window, middle.
     case = Case(n_q=2, n_kv=1, seq_lens=[2], rot="perm", n_sink=4, window=16, block=16,
@@ -135,10 +156,11 @@ def test_rotation_within_fp32_accumulation_bound():
     assert flips <= 0.05 * total
 
 
-@pytest.mark.parametrize("G,topk_fixed,retain", [(4, 0, 100), (1, 64, 0), (8, 0, 300)])
-def test_block_select_scores_and_ids(G, topk_fixed, retain):
+@pytest.mark.parametrize("G,topk_fixed,retain,meta_c", [(4, 0, 100, 0), (1, 64, 0, 0), (8, 0, 300, 0),
+                                                       (4, 0, 100, 32), (2, 0, 100, 48)])
+def test_block_select_scores_and_ids(G, topk_fixed, retain, meta_c):
     case = Case(n_q=G * 2, n_kv=2, seq_lens=[4096, 2500], rot="perm", topk_fixed=topk_fixed,
-                retain_permille=retain, steps=[1, 1, 3], seed=5 + G)
+                retain_permille=retain, steps=[1, 1, 3], seed=5 + G, meta_channels=meta_c)
     p = Pair(case)
     p.run_steps()
     q = p.query(1)
@@ -153,7 +175,7 @@ def test_block_select_scores_and_ids(G, topk_fixed, retain):
         per, grp = oc.scores(qs)
         nb = oc.n_blocks_mid()
         got_s = scores[s, h, :nb].astype(np.float64)
-        mn, mx = oc.meta()
+        mn, mx = oc.score_keys()
         tol = score_tolerance(oc.rotate_query(qs), mn, mx)
         assert np.all(np.abs(got_s - grp) <= tol)
         cand = oc.candidates()
@@ -230,11 +252,13 @@ def test_block_select_all_ties_large(T, retain, segments):
     Case(n_q=2, n_kv=1, seq_lens=[3], rot="eigh", n_sink=4, window=8, seed=16),  # T < S
     Case(n_q=4, n_kv=2, seq_lens=[3000], rot="eigh", block=32, segments=[(0, 38, 0, 96)], steps=[1, 1, 2],
          seed=18),                                                                 # bottom 25% truncated
+    Case(n_q=4, n_kv=2, seq_lens=[3000], rot="eigh", block=32, meta_channels=32, steps=[1, 1, 2],
+         seed=20),                                                                 # compressed block keys
     Case(n_q=4, n_kv=1, seq_lens=[42000], rot="eigh", block=64, window=128, topk_fixed=600, retain_permille=0,
          steps=[1, 1], seed=19),                                                   # long selection: 16-warp plan
     Case(n_q=4, n_kv=1, seq_lens=[1500], rot="eigh", segments=[(0, 128, 0)], topk_fixed=10 ** 6,
          retain_permille=0, seed=17),                                              # r = d, all blocks
-], ids=["gqa4-2seq", "b64-5pct", "serving-segments", "single-head-c1", "empty-middle", "below-sinks", "truncated-96", "long-16warps",
+], ids=["gqa4-2seq", "b64-5pct", "serving-segments", "single-head-c1", "empty-middle", "below-sinks", "truncated-96", "keys-32ch", "long-16warps",
         "r128-allblocks"])
 def test_decode_attention_matches_oracle(case):
     p = Pair(case)
@@ -352,7 +376,8 @@ def test_repeatable_bytes():
     Case(n_q=4, n_kv=1, seq_lens=[4000, 1200, 300], rot="eigh", block=16, window=128,
          segments=[(0, 32, 0), (350, 64, 1), (650, 32, 0)], oracle_units=[], seed=22),
     Case(n_q=4, n_kv=2, seq_lens=[40, 70], rot="eigh", window=64, oracle_units=[], seed=23),
-], ids=["gqa4-2seq", "serving-segments", "filling-window"])
+    Case(n_q=4, n_kv=2, seq_lens=[2500, 900], rot="eigh", block=32, meta_channels=24, oracle_units=[], seed=24),
+], ids=["gqa4-2seq", "serving-segments", "filling-window", "keys-24ch"])
 def test_append_select_equals_separate_calls(case):
     """The fused decode append + block selection gives the ids, the stored
     state and the attention output of the two calls it replaces, step after

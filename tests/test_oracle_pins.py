@@ -126,6 +126,30 @@ def test_topr_truncated_bottom_channels_brute_force():
             assert list(O.topr_select(z, r)[0][0]) == want
 
 
+def test_compressed_block_keys_brute_force_and_full_width():
+    # [S] sec. 5.2: per block, the m channels with the largest max(|min|, |max|),
+    # ties to the lower channel, ascending; brute force over small rows.
+    rng = np.random.default_rng(24)
+    for _ in range(200):
+        d = int(rng.integers(2, 9))
+        m = int(rng.integers(1, d + 1))
+        mn = rng.integers(-3, 1, size=(3, d)).astype(np.float64)
+        mx = mn + rng.integers(0, 4, size=(3, d))
+        idx, cmn, cmx = O.compress_key_rows(mn, mx, m)
+        for r in range(3):
+            w = np.maximum(np.abs(mn[r]), np.abs(mx[r]))
+            want = sorted(sorted(range(d), key=lambda c: (-w[c], c))[:m])
+            assert list(idx[r]) == want
+            assert np.array_equal(cmn[r], mn[r, want]) and np.array_equal(cmx[r], mx[r, want])
+    # Keeping every channel gives back the full keys, so the scores are unchanged.
+    mn = rng.standard_normal((5, 128))
+    mx = mn + rng.random((5, 128))
+    fmn, fmx = O.zero_filled_keys(*O.compress_key_rows(mn, mx, 128))
+    assert np.array_equal(fmn, mn) and np.array_equal(fmx, mx)
+    q = rng.standard_normal((2, 128))
+    assert np.array_equal(O.block_scores(q, fmn, fmx)[1], O.block_scores(q, mn, mx)[1])
+
+
 # ---------------------------------------------------------- rotation ----
 def _gen(T, decay, seed, outliers=True):
     x = synth.lowrank_outlier(T, 128, decay, seed, n_outlier_channels=4 if outliers else 0)
