@@ -18,9 +18,10 @@ Sources (cited by page title and equation/section):
   [S] "MosaicKV: Serving Long-Context LLM with Dynamic Two-D KV Cache
       Compression" (paperlayer.ai summary of arXiv 2607.00760v1):
       sec. 4.2-4.3 (two-stage compression, per-segment strategy),
-      sec. 5.1 (packed format), sec. 5.3 (PackedAttention), sec. 6.3.
+      sec. 5.1 (packed format), sec. 5.2 (encoding variants), sec. 5.3
+      (PackedAttention), sec. 6.3.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * segments: sinks [0, S), recent window [T-W, T), middle [S, T-W) cut into
     blocks of B tokens from S; the last block may be partial;
   * per-vector top-r: magnitude descending, ties to the lower channel; the
@@ -34,7 +35,12 @@ Readings where the pages are silent (each is listed in the design doc):
   * strategy segments start at the first block boundary at or after
     begin_permille/1000 of the prefill length; the last one is open-ended;
   * decode append: the new token enters the window; the window's oldest
-    token, once more than W are held, moves into the middle.
+    token, once more than W are held, moves into the middle;
+  * sec. 5.2 variants (off by default): "bottom channels truncated" = the
+    per-vector top-r picks among the first keep_channels rotated channels
+    only; "per-block keys channel-compressed" = each block keeps the m
+    channels with the largest max(|min|, |max|), ties to the lower channel,
+    and the scores use them with the other channels zero.
 
 Parity status: every public function is pinned by tests/test_oracle_pins.py
 (worked example, brute force, closed forms, library routines, invariants).

@@ -17,7 +17,7 @@ Sources (cited by page title and equation/section):
       Compression" (paperlayer.ai summary): sec. 5.5 (incremental covariance,
       channel parameters under a loss threshold).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * the covariance is the uncentred second moment sum x^T x ([N] Eq. (4)
     rotates by the eigenvectors of K^T K);
   * the loss of keeping r channels is the discarded energy 1 - Energy(r);
