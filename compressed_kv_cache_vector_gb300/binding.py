@@ -85,6 +85,9 @@ _SIGS = {
     "mk_choose_r": [c_vp, c_i32, ctypes.c_double, ctypes.POINTER(c_i32)],
     "mk_alg2_segment_r": [c_vp, c_i64, c_i64, c_i32, ctypes.c_double, ctypes.POINTER(MkAlg2Params),
                           ctypes.POINTER(MkSegStats), ctypes.POINTER(c_i32)],
+    "mk_host_pack_blocks": [c_vp, c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_i64, c_i32, c_vp, c_vp,
+                            c_vp],
+    "mk_swap_segment": [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp],
 }
 
 _lib = None
@@ -237,6 +240,17 @@ class MosaicKV:
             self.h, len(T), _i32(T), _ptr(q), _ptr(K), _ptr(V), K.shape[2], _ptr(out), _stream(stream)))
         return out
 
+    def swap_segment(self, layer, seq, kvh, segment, r, keep_channels, pages, meta, cmeta=None, stream=None):
+        """Replace a closed segment's pages and keys with host-packed ones (host_pack_blocks), under r from
+        then on.  The host arrays must live until the stream has run the copies."""
+        pg = np.ascontiguousarray(pages, dtype=np.uint8)
+        mt = np.ascontiguousarray(meta, dtype=np.uint16)
+        cm = None if cmeta is None else np.ascontiguousarray(cmeta, dtype=np.uint8)
+        self._swap_keep = (pg, mt, cm)   # kept alive until the next swap
+        _check("mk_swap_segment", self.lib.mk_swap_segment(
+            self.h, layer, seq, kvh, segment, r, keep_channels, _np_ptr(pg), _np_ptr(mt),
+            _np_ptr(cm) if cm is not None else ctypes.c_void_p(0), _stream(stream)))
+
     def poll_error(self):
         d = c_i32()
         st = self.lib.mk_poll_error(self.h, ctypes.byref(d))
@@ -368,3 +382,20 @@ def alg2_segment_r(seg, budget, outlier_abs, outlier_ratio_max, alpha, r_min, r_
                                                          float(budget), ctypes.byref(p), ctypes.byref(st),
                                                          ctypes.byref(r)))
     return r.value, {"variance": st.variance, "outlier_ratio": st.outlier_ratio, "entropy": st.entropy}
+
+
+def host_pack_blocks(Rk, Rv, k, v, block, r, keep_channels, page_stride, meta_channels=0):
+    """Exact host re-compression of complete blocks (raw bf16 rows k, v: n_blocks * block rows of 128):
+    (pages uint8 [n, page_stride], meta uint16 [n, 2, 128], compressed keys uint8 [n, row] or None)."""
+    kw, vw = _bf16_words(k), _bf16_words(v)
+    n = kw.shape[0] // block
+    Rk32 = np.ascontiguousarray(Rk, dtype=np.float32)
+    Rv32 = np.ascontiguousarray(Rv, dtype=np.float32)
+    pages = np.empty((n, page_stride), dtype=np.uint8)
+    meta = np.empty((n, 2, MK_HEAD_DIM), dtype=np.uint16)
+    crow = (5 * meta_channels + 15) // 16 * 16 if meta_channels else 0
+    cmeta = np.empty((n, crow), dtype=np.uint8) if meta_channels else None
+    _check("mk_host_pack_blocks", load().mk_host_pack_blocks(
+        _np_ptr(Rk32), _np_ptr(Rv32), _np_ptr(kw), _np_ptr(vw), kw.shape[1], n, block, r, keep_channels, page_stride,
+        meta_channels, _np_ptr(pages), _np_ptr(meta), _np_ptr(cmeta) if cmeta is not None else ctypes.c_void_p(0)))
+    return pages, meta, cmeta

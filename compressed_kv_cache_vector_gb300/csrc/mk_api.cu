@@ -583,3 +583,35 @@ mk_status mk_record_event(void* event, mk_stream stream) {
 }
 
 }  // extern "C"
+
+mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, int32_t segment, int32_t r,
+                          int32_t keep_channels, const void* pages, const void* meta, const void* cmeta,
+                          mk_stream stream) {
+  if (!ctx || !pages || !meta) return MK_EINVAL;
+  const mk_config& c = ctx->cfg;
+  const Layout& L = ctx->L;
+  if (layer < 0 || layer >= c.n_layers || seq < 0 || seq >= c.max_seqs || kv_head < 0 || kv_head >= c.n_kv_heads)
+    return MK_EINVAL;
+  if (segment < 0 || segment >= c.n_segments) return MK_EINVAL;
+  if (r < 1 || r > L.r_max) return MK_EINVAL;  // the pages hold at most r_max entries per token
+  if (keep_channels != 0 && (keep_channels < r || keep_channels > MK_HEAD_DIM)) return MK_EINVAL;
+  if (L.meta_c > 0 && !cmeta) return MK_EINVAL;
+  const size_t ls = (size_t)layer * c.max_seqs + seq;
+  if (ctx->T0[ls] == 0 || segment == c.n_segments - 1) return MK_ESTATE;
+  const int fb = ctx->firsts[ls * MK_MAX_SEGMENTS + segment], lb = ctx->firsts[ls * MK_MAX_SEGMENTS + segment + 1];
+  const int n = lb - fb;
+  if (n <= 0) return MK_ESTATE;
+  const int64_t u = mk::unit_index(L, layer, seq, kv_head);
+  char* base = L.units + u * L.unit_stride;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(base + L.off_pages + (int64_t)fb * L.page_stride, pages,
+                                  (size_t)n * (size_t)L.page_stride, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(base + L.off_meta + (int64_t)fb * 2 * MK_HEAD_DIM * 2, meta,
+                        (size_t)n * 2 * MK_HEAD_DIM * 2, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && L.meta_c > 0)
+    e = cudaMemcpyAsync(base + L.off_cmeta + (int64_t)fb * L.cmeta_row, cmeta, (size_t)n * (size_t)L.cmeta_row,
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = mk::launch_set_segment(L, u, segment, r, keep_channels ? keep_channels : MK_HEAD_DIM, s);
+  return cuda_status(e);
+}

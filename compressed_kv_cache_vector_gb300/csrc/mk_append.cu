@@ -284,6 +284,20 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
   }
 }
 
+// A segment's channel count and truncation after a swap of its pages
+// (double-buffered re-compression); the flags keep the always bit.
+__global__ void k_set_segment(Layout L, int64_t u, int seg, int r, int keep) {
+  if (threadIdx.x == 0) {
+    L.desc[u].r[seg] = r;
+    L.desc[u].sflags[seg] = (L.desc[u].sflags[seg] & 1) | (keep << 8);
+  }
+}
+
+cudaError_t launch_set_segment(const Layout& L, int64_t u, int seg, int r, int keep, cudaStream_t s) {
+  k_set_segment<<<1, 32, 0, s>>>(L, u, seg, r, keep);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_init_desc(const Layout& L, int layer, int seq, const UnitDesc& d, cudaStream_t s) {
   k_init_desc<<<1, 32 * ((L.n_kv + 31) / 32), 0, s>>>(L, layer, seq, d);
   return cudaGetLastError();

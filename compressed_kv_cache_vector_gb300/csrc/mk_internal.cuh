@@ -334,6 +334,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Kernel launchers (defined in the .cu files); they return cudaGetLastError().
 cudaError_t launch_init_desc(const Layout& L, int layer, int seq, const UnitDesc& d, cudaStream_t s);
+cudaError_t launch_set_segment(const Layout& L, int64_t u, int seg, int r, int keep, cudaStream_t s);
 cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
                                 const uint16_t* v, int evict_only, cudaStream_t s);
 cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,

@@ -1,7 +1,9 @@
 // Host-side strategy generation: the covariance a head accumulates, the
 // rotation from its eigenvectors, the channel count under a loss threshold,
-// and the per-segment channel count of Algorithm 2.  Host code only (fp64);
-// no device memory, no context.
+// and the per-segment channel count of Algorithm 2; and the host side of the
+// double-buffered compression (sec. 5.4 of the paperlayer summary): exact
+// re-compression of complete blocks into the arena's formats.  Host code only
+// (fp64); no device memory, no context.
 //
 // Method: "MosaicKV：...阅读笔记" (zhongzhuzhou.org): Eq. (4) and (6) (the
 // rotation R from the eigenvectors of K^T K, eigenvalues descending), Eq. (5)
@@ -202,6 +204,116 @@ extern "C" mk_status mk_alg2_segment_r(const void* seg, int64_t s, int64_t row_s
     stats->variance = variance;
     stats->outlier_ratio = outlier_ratio;
     stats->entropy = entropy;
+  }
+  return MK_OK;
+}
+
+// ---- Host re-compression of complete blocks ([S] sec. 5.4: the CPU side of
+// the double-buffered compression).  Same formats as the device path; the
+// rotation is exact fp64 rounded once to bf16.
+namespace {
+
+// Nearest bf16 value to x, ties to even (8 significant bits; below the
+// smallest normal the spacing stays 2^-133); zero comes back as +0.
+double bf16_round(double x) {
+  if (x == 0.0) return 0.0;
+  int e = 0;
+  (void)std::frexp(x, &e);
+  if (e < -125) e = -125;
+  const double ulp = std::ldexp(1.0, e - 8);
+  return std::nearbyint(x / ulp) * ulp + 0.0;
+}
+
+inline uint16_t bf16_bits(double y) {
+  const float f = (float)y;  // exact: y is a bf16 value
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  return (uint16_t)(u >> 16);
+}
+
+// Channels [0, keep) of y ordered by magnitude descending (ties to the lower
+// channel); the first r, in ascending channel order.
+void top_r(const double* y, int keep, int r, int* out) {
+  std::vector<int> c((size_t)keep);
+  std::iota(c.begin(), c.end(), 0);
+  std::stable_sort(c.begin(), c.end(), [&](int a, int b) { return std::fabs(y[a]) > std::fabs(y[b]); });
+  std::sort(c.begin(), c.begin() + r);
+  std::copy(c.begin(), c.begin() + r, out);
+}
+
+}  // namespace
+
+extern "C" mk_status mk_host_pack_blocks(const float* R_k, const float* R_v, const void* k, const void* v,
+                                         int64_t row_stride, int32_t n_blocks, int32_t block, int32_t r,
+                                         int32_t keep_channels, int64_t page_stride, int32_t meta_channels,
+                                         void* pages, void* meta, void* cmeta) {
+  constexpr int D = MK_HEAD_DIM;
+  if (!R_k || !R_v || !k || !v || !pages || !meta || n_blocks < 0 || row_stride < D) return MK_EINVAL;
+  if (block != 16 && block != 32 && block != 64) return MK_EINVAL;
+  if (r < 1 || r > D || (keep_channels != 0 && (keep_channels < r || keep_channels > D))) return MK_EINVAL;
+  if (page_stride < (int64_t)6 * block * r) return MK_EINVAL;
+  if (meta_channels < 0 || meta_channels > MK_MAX_META_CHANNELS || (meta_channels > 0 && !cmeta)) return MK_EINVAL;
+  const int keep = keep_channels ? keep_channels : D;
+  const int64_t crow = meta_channels > 0 ? (5 * meta_channels + 15) / 16 * 16 : 0;
+  std::memset(pages, 0, (size_t)n_blocks * (size_t)page_stride);
+  if (crow) std::memset(cmeta, 0, (size_t)n_blocks * (size_t)crow);
+  const int Br = block * r;
+  std::vector<double> x(D), y(D), zk(D);
+  std::vector<int> kept((size_t)r);
+  for (int32_t b = 0; b < n_blocks; ++b) {
+    unsigned char* page = static_cast<unsigned char*>(pages) + (int64_t)b * page_stride;
+    double mn[D], mx[D];
+    for (int t = 0; t < block; ++t) {
+      const int64_t row = (int64_t)b * block + t;
+      for (int w = 0; w < 2; ++w) {
+        const uint16_t* src = row_ptr(w == 0 ? k : v, row, row_stride);
+        const float* R = w == 0 ? R_k : R_v;
+        for (int j = 0; j < D; ++j) x[j] = bf16_to_double(src[j]);
+        for (int c = 0; c < D; ++c) {
+          double acc = 0.0;
+          for (int j = 0; j < D; ++j) acc += x[j] * (double)R[(size_t)c * D + j];
+          y[c] = bf16_round(acc);
+        }
+        top_r(y.data(), keep, r, kept.data());
+        uint16_t* val = reinterpret_cast<uint16_t*>(page + (w == 0 ? 0 : 3 * Br));
+        uint8_t* idx = page + (w == 0 ? 2 * Br : 5 * Br);
+        for (int i = 0; i < r; ++i) {
+          val[t * r + i] = bf16_bits(y[kept[i]]);
+          idx[t * r + i] = (uint8_t)kept[i];
+        }
+        if (w == 0) {
+          // min/max over the block of the zero-filled compressed key
+          std::fill(zk.begin(), zk.end(), 0.0);
+          for (int i = 0; i < r; ++i) zk[kept[i]] = y[kept[i]];
+          for (int c = 0; c < D; ++c) {
+            mn[c] = t == 0 ? zk[c] : std::min(mn[c], zk[c]);
+            mx[c] = t == 0 ? zk[c] : std::max(mx[c], zk[c]);
+          }
+        }
+      }
+    }
+    uint16_t* mrow = static_cast<uint16_t*>(meta) + (int64_t)b * 2 * D;
+    for (int c = 0; c < D; ++c) {
+      mn[c] += 0.0;  // a zero bound is +0
+      mx[c] += 0.0;
+      mrow[c] = bf16_bits(mn[c]);
+      mrow[D + c] = bf16_bits(mx[c]);
+    }
+    if (crow) {
+      double wgt[D];
+      for (int c = 0; c < D; ++c) wgt[c] = std::max(std::fabs(mn[c]), std::fabs(mx[c]));
+      std::vector<int> ck((size_t)meta_channels);
+      top_r(wgt, D, meta_channels, ck.data());
+      unsigned char* cr = static_cast<unsigned char*>(cmeta) + (int64_t)b * crow;
+      uint16_t* cmn = reinterpret_cast<uint16_t*>(cr);
+      uint16_t* cmx = cmn + meta_channels;
+      uint8_t* cch = reinterpret_cast<uint8_t*>(cmx + meta_channels);
+      for (int i = 0; i < meta_channels; ++i) {
+        cmn[i] = bf16_bits(mn[ck[i]]);
+        cmx[i] = bf16_bits(mx[ck[i]]);
+        cch[i] = (uint8_t)ck[i];
+      }
+    }
   }
   return MK_OK;
 }

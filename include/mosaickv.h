@@ -300,6 +300,45 @@ typedef struct mk_seg_stats {
 mk_status mk_alg2_segment_r(const void* seg, int64_t s, int64_t row_stride, int32_t d, double budget,
                             const mk_alg2_params* params, mk_seg_stats* stats, int32_t* r);
 
+/* ---- Double-buffered re-compression of a closed segment ([S] sec. 5.4) ----
+ * While decoding goes on with the GPU's compression of a segment, the CPU
+ * re-compresses the segment's tokens exactly (fp64 rotation, rounded once to
+ * bf16), possibly under a new strategy (channel count r, truncation), and the
+ * result replaces the GPU's version in the arena, stream-ordered and without
+ * blocking the host.  Here a segment keeps the head's rotation; per-segment
+ * rotations are not supported. */
+
+/* Packs n_blocks complete blocks of `block` tokens on the host, in the
+ * arena's formats.  k, v: the blocks' raw (unrotated) bf16 rows, row i at
+ * k + i * row_stride words; R_k, R_v: the head's rotations (as given to
+ * mk_set_rotation).  Each token is rotated in fp64 (k' = k R^T) and rounded
+ * to nearest-even bf16; its top-r over the first keep_channels channels
+ * (0 = all) is kept as in mk_append_compress.  Outputs, all host memory:
+ * pages (n_blocks x page_stride bytes: [K values B*r bf16][K indices B*r
+ * u8][V values][V indices], the rest zero), meta (n_blocks x 2 x 128 bf16:
+ * per-channel min and max of the zero-filled compressed keys), and, with
+ * meta_channels > 0, cmeta (n_blocks rows of ((5 meta_channels + 15) / 16) *
+ * 16 bytes, the compressed block keys).  MK_EINVAL: a null pointer, block not
+ * 16, 32 or 64, r outside [1, 128], keep_channels outside {0} u [r, 128],
+ * page_stride < 6 * block * r, meta_channels outside [0, 48]. */
+mk_status mk_host_pack_blocks(const float* R_k, const float* R_v, const void* k, const void* v, int64_t row_stride,
+                              int32_t n_blocks, int32_t block, int32_t r, int32_t keep_channels, int64_t page_stride,
+                              int32_t meta_channels, void* pages, void* meta, void* cmeta);
+
+/* Replaces strategy segment `segment` of one (layer, sequence, kv head) with
+ * pages, meta (and cmeta) packed by mk_host_pack_blocks for all of its blocks
+ * (mk_layout gives the segment's first blocks), under channel count r and
+ * truncation keep_channels from then on.  The segment must be closed: not the
+ * last one, which still receives appends.  r may not exceed the largest r of
+ * the configuration (the page capacity).  Host copies and a descriptor update
+ * are enqueued on `stream`; the host buffers must stay valid until they run
+ * (pinned memory makes the copies asynchronous).  MK_EINVAL: bad ids, a null
+ * buffer, r or keep_channels out of range; MK_ESTATE: the sequence has no
+ * prefill yet, or the segment is the last or empty. */
+mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, int32_t segment, int32_t r,
+                          int32_t keep_channels, const void* pages, const void* meta, const void* cmeta,
+                          mk_stream stream);
+
 /* Waits for the device and reads the sticky error word: MK_OK, MK_EDEVICE or
  * MK_ETIMEOUT; *detail (optional) receives the kernel's detail code. */
 mk_status mk_poll_error(mk_ctx* ctx, int32_t* detail);

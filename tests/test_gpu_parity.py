@@ -284,6 +284,72 @@ def test_decode_attention_matches_oracle(case):
     print("worst relative L2", worst)
 
 
+def test_swap_closed_segment_with_host_repack():
+    """[S] sec. 5.4: the CPU re-compresses a closed segment exactly, here under
+    a new strategy (r 32 -> 20, bottom 32 channels truncated), and the result
+    replaces the GPU's version while decoding goes on.  The cache then equals,
+    byte for byte, the oracle built with the new strategy from the start, and
+    attention follows it."""
+    import dataclasses
+    from compressed_kv_cache_vector_gb300 import binding
+    case = Case(n_q=4, n_kv=2, seq_lens=[3000, 1800], rot="perm", block=32, window=64,
+                segments=[(0, 32, 0), (600, 32, 0)], steps=[1] * 7, seed=31)
+    p = Pair(case)
+    for n in case.steps[:6]:
+        p.step(n)
+    S, B = case.n_sink, case.block
+    for (l, s, h) in p.units:
+        lay = p.mk.layout(l, s, h)
+        fb = lay["seg_first_block"]
+        rows = slice(S + fb[0] * B, S + fb[1] * B)
+        Rk, Rv = p.R[(l, s, h)]
+        pages, meta, _ = binding.host_pack_blocks(Rk, Rv, p.K[(l, s, h)][rows].cpu(), p.V[(l, s, h)][rows].cpu(),
+                                                  B, 20, 96, lay["page_stride"])
+        p.mk.swap_segment(l, s, h, 0, 20, 96, pages, meta)
+        torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    # The oracle of the new strategy, fed the same tokens.
+    case2 = dataclasses.replace(case, segments=[(0, 20, 0, 96), (600, 32, 0)])
+    ref = Pair(case2)
+    for n in case2.steps[:6]:
+        ref.step(n)
+    p.c, p.orc = case2, ref.orc
+    for u in p.units:
+        _check_storage(p, u)
+    # Decoding goes on (the open segment is untouched; p.step also advances
+    # the oracle, now ref's), then attention.
+    p.step(case.steps[6])
+    for u in p.units:
+        _check_storage(p, u)
+    q = p.query(5)
+    ids, n_sel = p.mk.block_select(0, [0, 1], q)
+    out = p.mk.decode_attn(0, [0, 1], ids, n_sel)
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    out = out.cpu().to(torch.float64).numpy()
+    ids, n_sel = ids.cpu().numpy(), n_sel.cpu().numpy()
+    G = case.G
+    for (l, s, h), oc in ref.orc.items():
+        qs = q[s, h * G:(h + 1) * G].cpu().to(torch.float64).numpy()
+        want = oc.attention(qs, ids[s, h, :n_sel[s, h]])
+        for g in range(G):
+            assert rel_l2(out[s, h * G + g], want[g]) <= ATOL_REL
+
+
+def test_swap_segment_refuses_open_or_bad_segments():
+    from compressed_kv_cache_vector_gb300 import binding
+    case = Case(n_q=4, n_kv=1, seq_lens=[2000], rot="perm", block=32, segments=[(0, 32, 0), (600, 32, 0)], seed=32)
+    p = Pair(case)
+    lay = p.mk.layout(0, 0, 0)
+    pages = np.zeros((1, lay["page_stride"]), dtype=np.uint8)
+    meta = np.zeros((1, 2, 128), dtype=np.uint16)
+    for seg, r, keep in ((1, 20, 0), (0, 40, 0), (0, 20, 10), (2, 20, 0)):
+        with pytest.raises(binding.MosaicKVError):
+            p.mk.swap_segment(0, 0, 0, seg, r, keep, pages, meta)   # open segment, r above r_max, keep < r, no such
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+
+
 def test_dense_reference_attention():
     torch.manual_seed(0)
     n, Hkv, G, T = 2, 2, 4, 3000
