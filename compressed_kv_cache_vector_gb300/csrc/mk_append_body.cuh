@@ -79,7 +79,7 @@ __device__ __forceinline__ void compress_key_row(const Layout& L, char* base, in
 // Called by one full warp.  Returns this lane's keep bits.
 __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc& ud, char* base, int pos,
                                                  const uint16_t* row, int is_v, int lane,
-                                                 bool update_meta) {
+                                                 bool update_meta, uint2* meta_out = nullptr) {
   const int m = pos - L.S;
   const int b = m / L.B;
   const int t = m - b * L.B;
@@ -135,6 +135,12 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
         make_uint2((uint32_t)nmn[0] | ((uint32_t)nmn[1] << 16), (uint32_t)nmn[2] | ((uint32_t)nmn[3] << 16));
     *reinterpret_cast<uint2*>(meta + D + 4 * lane) =
         make_uint2((uint32_t)nmx[0] | ((uint32_t)nmx[1] << 16), (uint32_t)nmx[2] | ((uint32_t)nmx[3] << 16));
+    if (meta_out) {  // this lane's four channels of the new min and max rows
+      meta_out[0] =
+          make_uint2((uint32_t)nmn[0] | ((uint32_t)nmn[1] << 16), (uint32_t)nmn[2] | ((uint32_t)nmn[3] << 16));
+      meta_out[1] =
+          make_uint2((uint32_t)nmx[0] | ((uint32_t)nmx[1] << 16), (uint32_t)nmx[2] | ((uint32_t)nmx[3] << 16));
+    }
     if (L.meta_c > 0) compress_key_row(L, base, b, nmn, nmx, lane);
   }
   return kbits;
@@ -312,10 +318,13 @@ __device__ __forceinline__ void append_small_body(const Layout& L, const UnitDes
 // write waits for both.  Same arithmetic as append_small_body with n = 1.
 // Called by all 256 threads; Rs = [R_k^T | R_v^T] in shared memory,
 // xs: 2*128 floats of shared scratch.  Shared memory is not touched after
-// the one barrier inside, so the caller may reuse it at once.
+// the one barrier inside, so the caller may reuse it at once.  Optional:
+// warp 6 waits on `lbar` (a copy the caller started) before that barrier,
+// and warp 0 returns its lane's part of the block's new min/max rows in
+// meta_out[0..1].
 __device__ __forceinline__ void append_one_body(const Layout& L, const UnitDesc& ud, char* base, int T_old,
                                                 const uint16_t* kin, const uint16_t* vin, const float* Rs,
-                                                float* xs) {
+                                                float* xs, uint64_t* lbar = nullptr, uint2* meta_out = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e = T_old - L.W;
   const int slot = (e - L.S) % L.W;
@@ -324,8 +333,13 @@ __device__ __forceinline__ void append_one_body(const Layout& L, const UnitDesc&
   const int ch = tid - 64;  // warps 2-5: channel of k' and v'
   float ak = 0.0f, av = 0.0f;
   if (warp < 2) {
-    compress_vec(L, ud, base, e, warp == 0 ? win_k : win_v, warp, lane, warp == 0);
-  } else if (warp < 6) {
+    compress_vec(L, ud, base, e, warp == 0 ? win_k : win_v, warp, lane, warp == 0, warp == 0 ? meta_out : nullptr);
+  } else if (warp == 6 && lbar) {
+    if (!mbar_wait(lbar, 0)) {
+      if (lane == 0) set_error(L, ERR_COPY_WAIT, -1, -6, (int32_t)MK_ETIMEOUT);
+      (void)mbar_wait(lbar, 0);
+    }
+  } else if (warp >= 2 && warp < 6) {
     xs[ch] = bf2f(kin[ch]);
     xs[D + ch] = bf2f(vin[ch]);
     asm volatile("bar.sync 1, 128;\n" ::: "memory");

@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   __shared__ int s_abort;
   __shared__ __align__(8) uint64_t s_rbar;
   __shared__ __align__(8) uint64_t s_tbar[kSelWarps][2];  // each warp's two meta-tile stages
-  __shared__ uint32_t bqs[3][16][2][32];            // B fragments, staged once
+  __shared__ __align__(16) uint32_t bqs[3][16][2][32];  // B fragments, staged once (then: the early last tile)
+  __shared__ __align__(8) uint64_t s_lbar;            // the early last tile's copy
 
   const int unit_call = blockIdx.x / P, part = blockIdx.x - unit_call * P;
   const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   const unsigned r_bytes = (unsigned)((APPEND && part == 0) ? 2 : 1) * D * D * 4;
   if (tid == 0) {
     mbar_init(&s_rbar, 1);
+    mbar_init(&s_lbar, 1);
     for (int w = 0; w < kSelWarps; ++w) {
       mbar_init(&s_tbar[w][0], 1);
       mbar_init(&s_tbar[w][1], 1);
@@ -187,6 +189,12 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   if (s_abort) return;
 
   int T_cur = ud.T;
+  // The appending CTA's last tile, staged early (see below): its index, rows,
+  // and warp 0's part of the leaving token's new min/max row.
+  bool early = false;
+  int tl = 0;
+  uint2 mrow[2] = {make_uint2(0, 0), make_uint2(0, 0)};
+  uint16_t* lt = reinterpret_cast<uint16_t*>(&bqs[0][0][0][0]);
   if (APPEND) {
     const int n = cs.n_new[ci];
     if (T_cur + n > L.cap_tokens) {
@@ -198,14 +206,45 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
       const int64_t row0 = (int64_t)cs.row_off[ci] * in_stride + (int64_t)kvh * D;
       float* xs = reinterpret_cast<float*>(smem + 2 * D * D * 4);
       uint16_t* rot = reinterpret_cast<uint16_t*>(xs + n * 2 * D);
-      if (n == 1 && L.W > 0 && T_cur >= L.S + L.W)
+      const bool one = n == 1 && L.W > 0 && T_cur >= L.S + L.W;
+      // With full keys and other CTAs to share the rest, warp 6 stages the
+      // unit's last tile (which holds the leaving token's block) while the
+      // append runs; warp 0 then patches that block's row with the new
+      // min/max it computed, instead of reading back what it wrote.
+      early = one && P > 1 && L.meta_c == 0;
+      if (early) {
+        const int nb_new = n_mid_blocks(L, T_cur + 1);
+        tl = (nb_new - 1) / kMT;
+        const int nrow = nb_new - tl * kMT;
+        if (warp == 6) {
+          if (lane == 0) {
+            fence_proxy_async();  // the area was last read as the B fragments
+            mbar_expect_tx(&s_lbar, (unsigned)nrow * 2u * D * 2u);
+          }
+          __syncwarp();
+          const uint16_t* meta0 = reinterpret_cast<const uint16_t*>(base + L.off_meta);
+          if (lane < nrow)
+            bulk_g2s(lt + lane * kMetaRow, meta0 + (int64_t)(tl * kMT + lane) * 2 * D, 2 * D * 2, &s_lbar);
+        }
+      }
+      if (one)
         append_one_body(L, ud, const_cast<char*>(base), T_cur, kin + row0, vin + row0,
-                        reinterpret_cast<const float*>(smem), xs);
+                        reinterpret_cast<const float*>(smem), xs, early ? &s_lbar : nullptr, mrow);
       else
         append_small_body(L, ud, const_cast<char*>(base), T_cur, n, n, kin + row0, vin + row0, in_stride,
                           reinterpret_cast<const float*>(smem), xs, rot);
-      __threadfence();          // the updated block min/max before this CTA's own tiles are read,
-      fence_proxy_async_all();  // which the bulk copies (async proxy) do
+      if (early) {
+        if (warp == 0) {  // the copy landed before the append's barrier
+          const int be = (T_cur - L.W - L.S) / L.B;
+          uint16_t* rowp = lt + (be - tl * kMT) * kMetaRow;
+          *reinterpret_cast<uint2*>(rowp + 4 * lane) = mrow[0];
+          *reinterpret_cast<uint2*>(rowp + D + 4 * lane) = mrow[1];
+          __syncwarp();
+        }
+      } else {
+        __threadfence();          // the updated block min/max before this CTA's own tiles are read,
+        fence_proxy_async_all();  // which the bulk copies (async proxy) do
+      }
     }
     T_cur += n;
   }
@@ -223,6 +262,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     t0 = min(ntiles, part * tper);
     t1 = min(ntiles, t0 + tper);
   }
+  if (early) t1 = t0;  // the last tile is already staged (scored below by warp 0)
   const uint16_t* meta = reinterpret_cast<const uint16_t*>(base + L.off_meta);
   uint32_t* kw = L.keys + slot * L.keys_stride;
   float* so = scores_out ? scores_out + ((int64_t)ci * L.n_kv + kvh) * L.nblk_cap : nullptr;
@@ -268,6 +308,34 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     if (key) atomicAdd(&hc[key >> 20], 1u);
   };
   const float inv_sqrt_d = 0.08838834764831845f;
+  // Scores of tile t (16 dense [min | max] rows) into keys, histogram, scores.
+  auto score_tile = [&](const uint16_t* tile, int t) {
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int mi = lane >> 3, ri = lane & 7;
+    const uint16_t* arow = tile + (ri + (mi & 1) * 8) * kMetaRow + (mi >> 1) * 8;
+#pragma unroll
+    for (int kc = 0; kc < 16; ++kc) {
+      uint32_t a[4];
+      ldsm_x4(a, arow + kc * 16);
+      mma_bf16(s, a, bq[0][kc][0], bq[0][kc][1]);
+      mma_bf16(s, a, bq[1][kc][0], bq[1][kc][1]);
+      mma_bf16(s, a, bq[2][kc][0], bq[2][kc][1]);
+    }
+    // rows: blocks g, g+8; columns: heads 2tig, 2tig+1 -> max over the group's heads
+    const bool h0 = 2 * tig < G, h1 = 2 * tig + 1 < G;
+    float b_lo = fmaxf(h0 ? s[0] : -INFINITY, h1 ? s[1] : -INFINITY);
+    float b_hi = fmaxf(h0 ? s[2] : -INFINITY, h1 ? s[3] : -INFINITY);
+    b_lo = fmaxf(b_lo, __shfl_xor_sync(FULL, b_lo, 1));
+    b_hi = fmaxf(b_hi, __shfl_xor_sync(FULL, b_hi, 1));
+    b_lo = fmaxf(b_lo, __shfl_xor_sync(FULL, b_lo, 2));
+    b_hi = fmaxf(b_hi, __shfl_xor_sync(FULL, b_hi, 2));
+    if (tig == 0) {
+      const int b0 = t * kMT + g, b1 = b0 + 8;
+      if (b0 < nblk) emit(b0, b_lo * inv_sqrt_d);
+      if (b1 < nblk) emit(b1, b_hi * inv_sqrt_d);
+    }
+  };
+  if (early && warp == 0) score_tile(lt, tl);
   int st = 0;
   int t = t0 + warp;
   issue(t, 0);
@@ -300,30 +368,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
       __syncwarp();
       tile = dt;
     }
-    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const int mi = lane >> 3, ri = lane & 7;
-    const uint16_t* arow = tile + (ri + (mi & 1) * 8) * kMetaRow + (mi >> 1) * 8;
-#pragma unroll
-    for (int kc = 0; kc < 16; ++kc) {
-      uint32_t a[4];
-      ldsm_x4(a, arow + kc * 16);
-      mma_bf16(s, a, bq[0][kc][0], bq[0][kc][1]);
-      mma_bf16(s, a, bq[1][kc][0], bq[1][kc][1]);
-      mma_bf16(s, a, bq[2][kc][0], bq[2][kc][1]);
-    }
-    // rows: blocks g, g+8; columns: heads 2tig, 2tig+1 -> max over the group's heads
-    const bool h0 = 2 * tig < G, h1 = 2 * tig + 1 < G;
-    float b_lo = fmaxf(h0 ? s[0] : -INFINITY, h1 ? s[1] : -INFINITY);
-    float b_hi = fmaxf(h0 ? s[2] : -INFINITY, h1 ? s[3] : -INFINITY);
-    b_lo = fmaxf(b_lo, __shfl_xor_sync(FULL, b_lo, 1));
-    b_hi = fmaxf(b_hi, __shfl_xor_sync(FULL, b_hi, 1));
-    b_lo = fmaxf(b_lo, __shfl_xor_sync(FULL, b_lo, 2));
-    b_hi = fmaxf(b_hi, __shfl_xor_sync(FULL, b_hi, 2));
-    if (tig == 0) {
-      const int b0 = t * kMT + g, b1 = b0 + 8;
-      if (b0 < nblk) emit(b0, b_lo * inv_sqrt_d);
-      if (b1 < nblk) emit(b1, b_hi * inv_sqrt_d);
-    }
+    score_tile(tile, t);
     __syncwarp();
     st ^= 1;
   }
