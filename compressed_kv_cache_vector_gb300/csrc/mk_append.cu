@@ -222,7 +222,8 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
   uint16_t* sink_v = reinterpret_cast<uint16_t*>(base + L.off_sink_v);
   uint16_t* win_k = reinterpret_cast<uint16_t*>(base + L.off_win_k);
   uint16_t* win_v = reinterpret_cast<uint16_t*>(base + L.off_win_v);
-  for (int t = warp; t < nt; t += 8) {
+  // One token: dense (sink or window) or compressed.
+  auto one_token = [&](int t) {
     const int p = lo + t;
     const uint16_t* rk = rot + (size_t)t * kRotRow;
     const uint16_t* rv = rot + (size_t)(kTileTokens + t) * kRotRow;
@@ -233,6 +234,22 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
       reinterpret_cast<uint2*>(dv)[lane] = reinterpret_cast<const uint2*>(rv)[lane];
     } else {
       keepk[t * 32 + lane] = (uint8_t)compress_kv(L, ud, base, p, rk, rv, lane);
+    }
+  };
+  // Warp w takes tokens w, w + 8, ...; two middle tokens at a time share their
+  // top-r searches' reductions (four searches per chain).
+  const auto middle = [&](int t) { const int p = lo + t; return p >= S && p < T_new - W; };
+  for (int t = warp; t < nt; t += 16) {
+    const int t2 = t + 8;
+    if (t2 < nt && middle(t) && middle(t2)) {
+      unsigned ka, kb;
+      compress_kv2(L, ud, base, lo + t, lo + t2, rot + (size_t)t * kRotRow, rot + (size_t)(kTileTokens + t) * kRotRow,
+                   rot + (size_t)t2 * kRotRow, rot + (size_t)(kTileTokens + t2) * kRotRow, lane, ka, kb);
+      keepk[t * 32 + lane] = (uint8_t)ka;
+      keepk[t2 * 32 + lane] = (uint8_t)kb;
+    } else {
+      one_token(t);
+      if (t2 < nt) one_token(t2);
     }
   }
   __syncthreads();

@@ -244,6 +244,114 @@ __device__ __forceinline__ unsigned compress_kv(const Layout& L, const UnitDesc&
   return keep_k;
 }
 
+// Four such searches at once (two tokens' keys and values, each with its own
+// r <= 128): every warp reduction carries four 8-bit counts (a lane adds at
+// most 4 to each, so no field overflows into the next).
+__device__ __forceinline__ void warp_topr4(const uint32_t m[4][4], const int r[4], int lane, unsigned keep[4],
+                                           int rank[4]) {
+  uint32_t t[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int bit = 14; bit >= 0; --bit) {
+    unsigned c = 0;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint32_t cand = t[v] | (1u << bit);
+      const unsigned n = (unsigned)(m[v][0] >= cand) + (unsigned)(m[v][1] >= cand) + (unsigned)(m[v][2] >= cand) +
+                         (unsigned)(m[v][3] >= cand);
+      c |= n << (8 * v);
+    }
+    const unsigned sum = __reduce_add_sync(FULL, c);
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      if ((int)((sum >> (8 * v)) & 0xffu) >= r[v]) t[v] |= 1u << bit;
+  }
+  unsigned gt = 0, eq = 0;
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      gt += (unsigned)(m[v][i] > t[v]) << (8 * v);
+      eq += (unsigned)(m[v][i] == t[v]) << (8 * v);
+    }
+  const unsigned gsum = __reduce_add_sync(FULL, gt);
+  const unsigned run0 = (unsigned)warp_excl_scan((int)eq, lane);
+  unsigned pc = 0;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int need = r[v] - (int)((gsum >> (8 * v)) & 0xffu);
+    int run = (int)((run0 >> (8 * v)) & 0xffu);
+    unsigned k = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (m[v][i] > t[v]) {
+        k |= 1u << i;
+      } else if (m[v][i] == t[v]) {
+        if (run < need) k |= 1u << i;
+        ++run;
+      }
+    }
+    keep[v] = k;
+    pc |= (unsigned)__popc(k) << (8 * v);
+  }
+  const unsigned rk0 = (unsigned)warp_excl_scan((int)pc, lane);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) rank[v] = (int)((rk0 >> (8 * v)) & 0xffu);
+}
+
+// compress_kv for two middle tokens at once (positions pa, pb; rotated rows
+// at rka/rva and rkb/rvb): their four top-r searches share each reduction.
+// Returns each token's key keep bits.
+__device__ __forceinline__ void compress_kv2(const Layout& L, const UnitDesc& ud, char* base, int pa, int pb,
+                                             const uint16_t* rka, const uint16_t* rva, const uint16_t* rkb,
+                                             const uint16_t* rvb, int lane, unsigned& keep_a, unsigned& keep_b) {
+  const int pos[2] = {pa, pb};
+  const uint16_t* rows[4] = {rka, rva, rkb, rvb};
+  int rr[4], kp[2], bb[2], tt[2];
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const int m = pos[w] - L.S;
+    bb[w] = m / L.B;
+    tt[w] = m - bb[w] * L.B;
+    const int sg = seg_of_block(ud, bb[w]);
+    rr[2 * w] = rr[2 * w + 1] = ud.r[sg];
+    kp[w] = seg_keep(ud, sg);
+  }
+  uint16_t vals[4][4];
+  uint32_t mag[4][4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(rows[v] + 4 * lane);
+    vals[v][0] = (uint16_t)(raw.x & 0xffff);
+    vals[v][1] = (uint16_t)(raw.x >> 16);
+    vals[v][2] = (uint16_t)(raw.y & 0xffff);
+    vals[v][3] = (uint16_t)(raw.y >> 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mag[v][i] = 4 * lane + i < kp[v >> 1] ? vals[v][i] & 0x7fffu : 0u;  // truncated: 0
+  }
+  unsigned keep[4];
+  int rank[4];
+  warp_topr4(mag, rr, lane, keep, rank);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int w = v >> 1, isv = v & 1, r = rr[v];
+    char* page = base + L.off_pages + (int64_t)bb[w] * L.page_stride;
+    const int Br = L.B * r;
+    uint16_t* val = reinterpret_cast<uint16_t*>(page + (isv ? 3 * Br : 0));
+    uint8_t* idx = reinterpret_cast<uint8_t*>(page + (isv ? 5 * Br : 2 * Br));
+    int rk = rank[v];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (keep[v] >> i & 1u) {
+        val[tt[w] * r + rk] = vals[v][i];
+        idx[tt[w] * r + rk] = (uint8_t)(4 * lane + i);
+        ++rk;
+      }
+    }
+  }
+  keep_a = keep[0];
+  keep_b = keep[2];
+}
+
 // Decode-path append of n new tokens to one (sequence, kv head) by one CTA of
 // 256 threads: evicts the window tokens that leave it into the middle
 // (select, pack, block min/max), then rotates the first n_rot (0 or n, at
