@@ -52,6 +52,8 @@ def test_sizes_follow_the_layout(lib):
     dict(block=24), dict(n_q_heads=24), dict(segments=[(100, 38, 0)]), dict(segments=[(0, 0, 0)]),
     dict(segments=[(0, 129, 0)]), dict(retain_permille=0), dict(window=0),
     dict(segments=[(0, 32, 0), (500, 64, 1), (400, 32, 0)]),
+    dict(segments=[(0, 38, 0, 30)]), dict(segments=[(0, 38, 0, 129)]),   # truncation below r, above d
+    dict(meta_channels=-1), dict(meta_channels=49),                      # compressed keys out of range
 ])
 def test_bad_configs_rejected(lib, bad):
     with pytest.raises(K.MosaicKVError) as e:
@@ -64,3 +66,13 @@ def test_head_dim_must_be_128(lib):
     c.head_dim = 64
     sz = ctypes.c_size_t()
     assert lib.mk_arena_bytes(ctypes.byref(c), ctypes.byref(sz)) == 1
+
+
+def test_variant_options_change_the_arena(lib):
+    a0, _, _ = K.sizes(_cfg())
+    a_trunc, _, _ = K.sizes(_cfg(segments=[(0, 38, 0, 96)]))
+    assert a_trunc == a0                                   # truncation only changes which channels are kept
+    a_keys, _, _ = K.sizes(_cfg(meta_channels=32))
+    nblk = (131072 + 64 - 4 - 256 + 31) // 32
+    # one compressed key row per block and head: 5 * 32 = 160 bytes
+    assert 8 * nblk * 160 <= a_keys - a0 <= 8 * (nblk * 160 + 256)
