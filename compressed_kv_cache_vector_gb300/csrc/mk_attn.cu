@@ -11,10 +11,12 @@
 // rotation merged into the query).
 //
 // GB300 structure.
-//  * Work items of one (sequence, kv head): dense chunks of 8 tokens (sinks,
-//    window), then 16-token groups of the selected / always-attended pages.
-//    P CTAs (one per SM, 8 or 12 warps) share them; each warp double-buffers
-//    its items into shared memory with cp.async.
+//  * Work items of one (sequence, kv head): the selected and always-attended
+//    pages (16-token groups), then dense chunks of 8 tokens (sinks, window).
+//    P CTAs (one per SM) share them.  Short selections use 12 warps, each
+//    double-buffering its items into shared memory by bulk copies; long ones
+//    16 warps with one stage each, the next copy issued as soon as the stage
+//    is consumed.
 //  * Per group the warp rebuilds positions in a 16 x 128 bf16 key tile and a
 //    value tile: it zero-fills them and scatters the kept values by their
 //    channel indices, lanes taking consecutive packed elements (coalesced
