@@ -9,11 +9,16 @@
 // (inverse rotation merged into the query).
 //
 // GB300 structure: P CTAs per (sequence, kv head).
-//  * Each CTA stages R_k^T (cp.async) and forms q' for the group's heads.
+//  * Each CTA stages R_k^T by one bulk copy and forms q' for the group's
+//    heads before the wait point (this prologue runs between the previous
+//    layer's attention and the scoring: the two kernels' CTAs do not fit on
+//    one SM together).
 //  * Scoring is a dense contraction: for block b and head h,
 //      sum_j max(q'_hj mn_bj, q'_hj mx_bj) = [mn_b | mx_b] . [min(q'_h,0) | max(q'_h,0)]
-//    over K = 256.  Meta tiles of 16 blocks are staged with cp.async and
-//    multiplied on the tensor cores (mma.sync m16n8k16).  The fp32 operand is
+//    over K = 256.  Meta tiles of 16 blocks are staged by bulk copies (one
+//    per block row, double-buffered per warp) and multiplied on the tensor
+//    cores (mma.sync m16n8k16).  With channel-compressed keys the staged rows
+//    are rebuilt into the same dense tile, dropped channels zero.  The fp32 operand is
 //    split exactly into three bf16 parts (24 = 3 x 8 significant bits) and the
 //    meta values are bf16, so every product is exact and the accumulation is
 //    fp32: the scores keep fp32 accuracy.
@@ -23,6 +28,8 @@
 //    added to the unit's histogram in global memory when the CTA is done.
 //  * The top k of each (sequence, kv head) follow in a second kernel
 //    (mk_topk.cu) launched right behind this one.
+//  * With APPEND, CTA 0 of each unit first appends the step's new token (see
+//    k_select) and scores the unit's last tile.
 #include <algorithm>
 
 #include "mk_append_body.cuh"
