@@ -350,10 +350,13 @@ def test_swap_segment_refuses_open_or_bad_segments():
     assert p.mk.poll_error() == (0, 0)
 
 
-def test_dense_reference_attention():
+@pytest.mark.parametrize("topk_fixed,retain", [(0, 100), (2100, 0)], ids=["12-warp-plan", "16-warp-plan"])
+def test_dense_reference_attention(topk_fixed, retain):
+    # The second configuration's longest selection (2100 blocks of 16 tokens)
+    # picks the 16-warp, one-stage plan for the context, the reference too.
     torch.manual_seed(0)
     n, Hkv, G, T = 2, 2, 4, 3000
-    cfg = make_config(Hkv * G, Hkv, 1, n, 4096, 4, 64, 16, [(0, 32, 0)], 0, 100)
+    cfg = make_config(Hkv * G, Hkv, 1, n, 40000, 4, 64, 16, [(0, 32, 0)], topk_fixed, retain)
     mk = MosaicKV(cfg)
     K = torch.randn(n, Hkv, T, 128, device="cuda").to(torch.bfloat16)
     V = torch.randn(n, Hkv, T, 128, device="cuda").to(torch.bfloat16)
