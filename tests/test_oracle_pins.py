@@ -299,6 +299,154 @@ def test_topk_brute_force_with_ties():
 
 
 # ------------------------------------------------------ attention ------
+def _hand_attention_case():
+    """Two query heads over three tokens, with every value worked out by hand.
+
+    [N] Eq. (1): o = softmax(q k^T / sqrt(d)) V with d = 128.  Head 0 is
+    sqrt(128) e_0, so its logits are the tokens' channel-0 entries, chosen as
+    0, ln 2, ln 3: the weights are 1/6, 2/6, 3/6.  Head 1 is 2 sqrt(128) e_1
+    over channel-1 entries 0, 0, ln 2 / 2: logits 0, 0, ln 2, weights 1/4,
+    1/4, 2/4.  V's rows are 6 e_0, 3 e_1 and 2 e_2 + e_3, so
+      head 0: o = (1, 1, 1, 1/2, 0, ...)
+      head 1: o = (3/2, 3/4, 1, 1/2, 0, ...).
+    """
+    d = 128
+    q = np.zeros((2, d))
+    q[0, 0] = math.sqrt(d)
+    q[1, 1] = 2 * math.sqrt(d)
+    K = np.zeros((3, d))
+    K[:, 0] = [0.0, math.log(2), math.log(3)]
+    K[:, 1] = [0.0, 0.0, math.log(2) / 2]
+    V = np.zeros((3, d))
+    V[0, 0], V[1, 1], V[2, 2], V[2, 3] = 6.0, 3.0, 2.0, 1.0
+    want = np.zeros((2, d))
+    want[0, :4] = [1.0, 1.0, 1.0, 0.5]
+    want[1, :4] = [1.5, 0.75, 1.0, 0.5]
+    return q, K, V, want
+
+
+def _sdpa(q, K, V):
+    """torch's scaled_dot_product_attention in float64 (default scale 1/sqrt(E), E = q's last dim)."""
+    t = lambda x: torch.as_tensor(np.asarray(x, dtype=np.float64))[None, None]
+    return torch.nn.functional.scaled_dot_product_attention(t(q), t(K), t(V))[0, 0].numpy()
+
+
+def _softmax_pins_hold(fn):
+    """The two pins of softmax_attention, as a predicate (used on planted mistakes too)."""
+    q, K, V, want = _hand_attention_case()
+    if not np.allclose(fn(q, K, V), want, rtol=0, atol=1e-14):
+        return False
+    rng = np.random.default_rng(81)
+    for G, T in ((1, 1), (4, 7), (8, 300)):
+        q = rng.standard_normal((G, 128))
+        K = rng.standard_normal((T, 128)) * 3.0
+        V = rng.standard_normal((T, 128))
+        ref = _sdpa(q, K, V)
+        if not np.allclose(fn(q, K, V), ref, rtol=0, atol=1e-12 * np.abs(ref).max()):
+            return False
+    return True
+
+
+def test_softmax_attention_hand_case_and_library_routine():
+    # [N] Eq. (1)/(13): a hand-computed case with exact weights, and torch's
+    # scaled_dot_product_attention in float64 on random inputs.
+    assert _softmax_pins_hold(O.softmax_attention)
+    assert _softmax_pins_hold(O.dense_attention)
+    # No tokens: the output is zero (a state the kernels see with T = 0).
+    assert not O.softmax_attention(np.ones((2, 128)), np.zeros((0, 128)), np.zeros((0, 128))).any()
+
+
+def test_softmax_pins_catch_planted_mistakes():
+    def scaled(c):
+        def f(q, K, V):
+            lg = q @ K.T * c
+            p = np.exp(lg - lg.max(axis=1, keepdims=True))
+            return (p / p.sum(axis=1, keepdims=True)) @ V
+        return f
+
+    def wrong_axis(q, K, V):
+        lg = q @ K.T / math.sqrt(128)
+        p = np.exp(lg - lg.max(axis=0, keepdims=True))
+        return (p / p.sum(axis=0, keepdims=True)) @ V
+
+    def unnormalised(q, K, V):
+        lg = q @ K.T / math.sqrt(128)
+        return np.exp(lg - lg.max(axis=1, keepdims=True)) @ V
+
+    assert _softmax_pins_hold(scaled(1 / math.sqrt(128)))          # the right form passes
+    for bad in (scaled(1 / 128), scaled(1 / math.sqrt(38)), scaled(1.0), wrong_axis, unnormalised):
+        assert not _softmax_pins_hold(bad)
+
+
+def test_densify_hand_case_and_planted_mistake():
+    # Zero-filled k~ from (index, value) pairs, d = 4 worked by hand.
+    idx = np.array([[0, 2], [1, 3], [0, 1]], dtype=np.uint8)
+    vals = np.array([[1.5, -2.0], [3.0, 0.25], [0.0, 7.0]])
+    want = np.array([[1.5, 0.0, -2.0, 0.0], [0.0, 3.0, 0.0, 0.25], [0.0, 7.0, 0.0, 0.0]])
+    assert np.array_equal(O.densify(idx, vals, 4), want)
+    # A densify that ignored the indices (values into the first r channels) fails it.
+    wrong = np.zeros((3, 4))
+    wrong[:, :2] = vals
+    assert not np.array_equal(wrong, want)
+
+
+def test_compressed_rows_are_brute_force_top_r_of_rotated_rows():
+    # At r < d the zero-filled rows the attention reads (Kt, Vt) hold, for each
+    # middle token, exactly its r largest-magnitude rotated channels (a Python
+    # sort, ties to the lower channel) and zero elsewhere.
+    st = O.Strategy(4, 32, 16, [(0, 38, 0), (500, 17, 0)], 0, 100)
+    c, _, _ = _cache(900, st, 70)
+    for t in range(4, 4 + c.n_mid, 7):
+        r = c.r_of_block((t - 4) // 16)
+        for rows, dense in ((c.Kr, c.Kt), (c.Vr, c.Vt)):
+            x = rows[t].astype(np.float64)
+            keep = sorted(sorted(range(128), key=lambda j: (-abs(x[j]), j))[:r])
+            z = np.zeros(128)
+            z[keep] = x[keep]
+            assert np.array_equal(dense[t].astype(np.float64), z)
+
+
+def test_compressed_attention_by_explicit_sums_over_packed_pairs():
+    # [N] Eq. (13)-(14) at r < d, restated with scalar loops over the packed
+    # (index, value) pairs of each page (no zero-filled rows), math.exp for the
+    # softmax and an explicit un-rotation; the pages' bytes are pinned by hand
+    # in test_page_byte_layout.
+    st = O.Strategy(4, 24, 16, [(0, 38, 0)], topk_fixed=3)
+    c, _, _ = _cache(170, st, 71, G=2)
+    q = np.random.default_rng(72).standard_normal((2, 128))
+    ids, _ = c.select(q)
+    qr = q @ c.Rk.T
+    toks = []                                   # (key pairs, value pairs) per attended token
+    for p in list(c.sink_positions()) + list(c.window_positions()):
+        toks.append((list(enumerate(c.Kr[p].astype(np.float64))), list(enumerate(c.Vr[p].astype(np.float64)))))
+    for b in ids:
+        lo, hi = c.block_tokens(int(b))
+        kv, ki, vv, vi = _page_rows(c.page_bytes(int(b)), 16, 38, hi - lo)
+        for t in range(hi - lo):
+            toks.append((list(zip(ki[t].tolist(), O.bits_to_value(kv[t]).tolist())),
+                         list(zip(vi[t].tolist(), O.bits_to_value(vv[t]).tolist()))))
+    got = np.zeros((2, 128))
+    for h in range(2):
+        logits = [sum(qr[h, j] * x for j, x in kp) / math.sqrt(128) for kp, _ in toks]
+        m = max(logits)
+        w = [math.exp(l - m) for l in logits]
+        acc = [0.0] * 128
+        for wi, (_, vp) in zip(w, toks):
+            for j, x in vp:
+                acc[j] += wi * x
+        o = [a / sum(w) for a in acc]
+        for j in range(128):
+            got[h, j] = sum(o[i] * c.Rv[i, j] for i in range(128))
+    want = c.attention(q, ids)
+    assert np.allclose(want, got, rtol=0, atol=1e-12 * np.abs(got).max())
+
+
+def _page_rows(pg, B, r, n):
+    Br = B * r
+    return (pg[:2 * Br].view(np.uint16).reshape(B, r)[:n], pg[2 * Br:3 * Br].reshape(B, r)[:n],
+            pg[3 * Br:5 * Br].view(np.uint16).reshape(B, r)[:n], pg[5 * Br:].reshape(B, r)[:n])
+
+
 @pytest.mark.parametrize("G", [1, 4])
 def test_full_channels_all_blocks_equals_dense_attention(G):
     st = O.Strategy(4, 40, 16, [(0, 128, 0)], topk_fixed=10 ** 6)
@@ -307,7 +455,7 @@ def test_full_channels_all_blocks_equals_dense_attention(G):
     ids, _ = c.select(q)
     assert len(ids) == c.n_blocks_mid()
     got = c.attention(q, ids)
-    want = O.dense_attention(q, K, V)
+    want = _sdpa(q, K, V)                       # [N] Eq. (1) by the library routine
     assert np.allclose(got, want, rtol=0, atol=1e-12 * np.abs(want).max())
 
 
