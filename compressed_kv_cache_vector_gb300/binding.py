@@ -80,6 +80,7 @@ _SIGS = {
     "mk_layout": [c_vp, c_i32, c_i32, c_i32, ctypes.POINTER(MkLayoutInfo)],
     "mk_record_event": [c_vp, c_vp],
     "mk_dense_decode_attn_noalloc": [c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_vp],
+    "mk_noalloc_poll_error": [ctypes.POINTER(c_i32)],
     "mk_cov_update": [c_vp, c_vp, c_i64, c_i64, c_i32],
     "mk_rotation_from_cov": [c_vp, c_i32, c_vp, c_vp],
     "mk_choose_r": [c_vp, c_i32, ctypes.c_double, ctypes.POINTER(c_i32)],
@@ -307,6 +308,14 @@ def dense_attn_noalloc(n_q_heads, n_kv_heads, T, q, K, V, out, stream=None):
         n_q_heads, n_kv_heads, len(T), _i32(T), _ptr(q), _ptr(K), _ptr(V), K.shape[2], _ptr(out),
         _stream(stream)))
     return out
+
+
+def noalloc_poll_error():
+    """(status, detail) of the allocation-free call's device-side error word on
+    the current device (waits for the device; clears the word)."""
+    d = c_i32(0)
+    st = load().mk_noalloc_poll_error(ctypes.byref(d))
+    return st, d.value
 
 
 def record_event(ev, stream=None):

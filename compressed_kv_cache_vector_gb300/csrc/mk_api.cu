@@ -5,7 +5,10 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "mk_internal.cuh"
@@ -190,6 +193,48 @@ mk_status check_seqs(const mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int
 inline mk_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MK_OK : MK_ECUDA; }
 
 }  // namespace
+
+namespace mk {
+
+cudaError_t kernel_smem_attr(const void* fn, int bytes, int threads, int* occ, int* sms) {
+  struct Entry {
+    int attr_bytes = -1;             // limit set on this device
+    int occ_bytes = -1, occ_threads = 0, occ = 1, sms = 0;
+  };
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, Entry> seen;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry& en = seen[{fn, dev}];
+  if (en.attr_bytes < bytes) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    en.attr_bytes = bytes;
+  }
+  if ((occ || sms) && (en.occ_bytes != bytes || en.occ_threads != threads)) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, (size_t)bytes) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 1;
+    }
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      v = 0;
+    }
+    en.occ = n > 0 ? n : 1;
+    en.sms = v;
+    en.occ_bytes = bytes;
+    en.occ_threads = threads;
+  }
+  if (occ) *occ = en.occ;
+  if (sms) *sms = en.sms;
+  return cudaSuccess;
+}
+
+}  // namespace mk
 
 extern "C" {
 
@@ -478,6 +523,7 @@ mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32
 mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T, const void* q, const void* K,
                                const void* V, int64_t t_stride, void* out, mk_stream stream) {
   if (!ctx || !T || !q || !K || !V || !out) return MK_EINVAL;
+  if (((uintptr_t)q | (uintptr_t)K | (uintptr_t)V | (uintptr_t)out) & 15) return MK_EINVAL;  // bulk-copied rows
   if (n_seqs < 1 || n_seqs > ctx->cfg.max_seqs || t_stride < 1) return MK_EINVAL;
   CallSeqs* cs = new (std::nothrow) CallSeqs();
   if (!cs) return MK_ENOMEM;

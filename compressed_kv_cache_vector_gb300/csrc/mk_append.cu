@@ -323,24 +323,16 @@ cudaError_t launch_init_desc(const Layout& L, int layer, int seq, const UnitDesc
 cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
                                 const uint16_t* v, int evict_only, cudaStream_t s) {
   const size_t smem = evict_only ? 0 : (size_t)2 * D * D * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_append_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         2 * D * D * (int)sizeof(float));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = kernel_smem_attr((const void*)k_append_small, 2 * D * D * (int)sizeof(float), 256, nullptr,
+                                   nullptr);
+  if (e != cudaSuccess) return e;
   return launch_pdl(k_append_small, dim3(cs.n * L.n_kv), dim3(256), smem, s, 0, L, layer, cs, k, v, evict_only);
 }
 
 cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
                                const uint16_t* v, int total_tiles, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_append_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = kernel_smem_attr((const void*)k_append_bulk, kBulkSmem, 256, nullptr, nullptr);
+  if (e != cudaSuccess) return e;
   dim3 grid(total_tiles, L.n_kv);
   k_append_bulk<<<grid, 256, kBulkSmem, s>>>(L, layer, cs, k, v);
   return cudaGetLastError();

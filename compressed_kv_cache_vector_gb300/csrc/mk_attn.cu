@@ -843,23 +843,9 @@ template <int G, bool DENSE, int MAXW>
 cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                        const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
                        int max_items, size_t smem, cudaStream_t s) {
-  static size_t set_bytes = 0;
-  static int occ = 1, sms = 0;
-  if (smem > set_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn<G, DENSE, MAXW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    set_bytes = smem;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn<G, DENSE, MAXW>, L.attn_nc * 32, smem) != cudaSuccess) {
-      (void)cudaGetLastError();
-      n = 1;
-    }
-    occ = std::max(1, n);
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
-                                                  cudaSuccess)
-      sms = v;
-  }
+  int occ = 1, sms = 0;
+  cudaError_t e = kernel_smem_attr((const void*)k_attn<G, DENSE, MAXW>, (int)smem, L.attn_nc * 32, &occ, &sms);
+  if (e != cudaSuccess) return e;
   const int units = cs.n * L.n_kv;
   int P = std::max(1, (std::max(sms, 1) * occ) / units);
   P = std::min(P, std::max(1, max_items / 2));

@@ -332,6 +332,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 #endif
 
+// Raises a kernel's dynamic shared memory limit to `bytes` on the current
+// device (cudaFuncSetAttribute acts on one device only), once per (kernel,
+// device) and size, under a lock, and reports the kernel's resident blocks per
+// SM at that size with `threads` threads (occ) and the device's SM count (sms).
+// Defined in mk_api.cu.
+cudaError_t kernel_smem_attr(const void* fn, int bytes, int threads, int* occ, int* sms);
+
 // Kernel launchers (defined in the .cu files); they return cudaGetLastError().
 cudaError_t launch_init_desc(const Layout& L, int layer, int seq, const UnitDesc& d, cudaStream_t s);
 cudaError_t launch_set_segment(const Layout& L, int64_t u, int seg, int r, int keep, cudaStream_t s);

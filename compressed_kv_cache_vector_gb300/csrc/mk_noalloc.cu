@@ -47,6 +47,8 @@ extern "C" mk_status mk_dense_decode_attn_noalloc(int32_t n_q_heads, int32_t n_k
                                                   const int32_t* T, const void* q, const void* K, const void* V,
                                                   int64_t t_stride, void* out, mk_stream stream) {
   if (!T || !q || !K || !V || !out) return MK_EINVAL;
+  // K and V rows arrive by bulk copies, which need 16-byte aligned sources.
+  if (((uintptr_t)q | (uintptr_t)K | (uintptr_t)V | (uintptr_t)out) & 15) return MK_EINVAL;
   if (n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads) return MK_EINVAL;
   const int G = n_q_heads / n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return MK_EINVAL;
@@ -90,12 +92,28 @@ extern "C" mk_status mk_dense_decode_attn_noalloc(int32_t n_q_heads, int32_t n_k
     cs.seq[i] = i;
     cs.T_old[i] = T[i];
   }
-  // Everything that must start at zero: the error word and the counters
-  // (a previous call may have left them set if it failed part-way).
+  // What must start at zero: the arrival counters (a previous call that
+  // failed part-way may have left them set).  The error word before them is
+  // kept: a device-side failure stays recorded until mk_noalloc_poll_error
+  // reads and clears it, and meanwhile every call leaves its output alone.
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)off_acc, s);
+  cudaError_t e = cudaMemsetAsync(scratch + off_cnt, 0, (size_t)(off_acc - off_cnt), s);
   if (e == cudaSuccess)
     e = mk::launch_dense_attn(L, cs, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(K),
                               static_cast<const uint16_t*>(V), t_stride, static_cast<uint16_t*>(out), max_items, s);
   return e == cudaSuccess ? MK_OK : MK_ECUDA;
+}
+
+extern "C" mk_status mk_noalloc_poll_error(int32_t* detail) {
+  unsigned char* scratch = nullptr;
+  mk_status st = scratch_for_current_device(&scratch);
+  if (st != MK_OK) return st;
+  int32_t w[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(w, scratch, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && w[0] != 0) e = cudaMemset(scratch, 0, sizeof(w));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return MK_ECUDA;
+  if (detail) *detail = w[1];
+  return w[0] == 0 ? MK_OK : (mk_status)w[0];
 }

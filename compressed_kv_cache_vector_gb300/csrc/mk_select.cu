@@ -410,14 +410,10 @@ cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, 
   const bool append = kin != nullptr;
 #define MK_SEL_CASE(GG)                                                                                       \
   case GG: {                                                                                                  \
-    static int set[2] = {0, 0};                                                                               \
     auto kern = append ? k_select<GG, true> : k_select<GG, false>;                                             \
-    if (set[append] < dyn) {                                                                                  \
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);           \
-      if (e != cudaSuccess) return e;                                                                         \
-      set[append] = dyn;                                                                                      \
-    }                                                                                                         \
-    cudaError_t e = launch_pdl(kern, grid, dim3(256), dyn, s, 0, L, layer, cs, P, q, ids, n_sel, scores_out,   \
+    cudaError_t e = kernel_smem_attr((const void*)kern, dyn, 256, nullptr, nullptr);                           \
+    if (e != cudaSuccess) return e;                                                                            \
+    e = launch_pdl(kern, grid, dim3(256), dyn, s, 0, L, layer, cs, P, q, ids, n_sel, scores_out,   \
                                dyn, kin, vin);                                                                 \
     if (e != cudaSuccess) return e;                                                                            \
     return launch_topk(L, layer, cs, ids, n_sel, append, s);                                                   \

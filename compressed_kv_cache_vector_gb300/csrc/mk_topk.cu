@@ -291,13 +291,9 @@ bool topk_plan_ok(const Layout& L) { return (L.nblk_cap + 3) / 4 <= kTkThreads *
 cudaError_t launch_topk(const Layout& L, int layer, const CallSeqs& cs, int32_t* ids, int32_t* n_sel, bool append,
                         cudaStream_t s) {
   const int dyn = (int)std::min<int64_t>(kTkSmemMax, (int64_t)16 * ((L.nblk_cap + 3) / 4));
-  static int set[2] = {-1, -1};
   auto kern = append ? k_topk<true> : k_topk<false>;
-  if (set[append] < dyn) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-    if (e != cudaSuccess) return e;
-    set[append] = dyn;
-  }
+  cudaError_t e = kernel_smem_attr((const void*)kern, dyn, kTkThreads, nullptr, nullptr);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(cs.n * L.n_kv), dim3(kTkThreads), dyn, s, 0, L, layer, cs, ids, n_sel, dyn);
 }
 

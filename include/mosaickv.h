@@ -210,7 +210,8 @@ mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32
  * reference ([N] Eq. (1)): out = softmax(q K^T / sqrt(d)) V over
  * K, V: device bf16 [n_seqs][n_kv_heads][t_stride][128], the first T[i]
  * tokens of sequence i (T: host int32, 1 <= T[i] <= t_stride).  Uses the
- * context's workspace and its head counts. */
+ * context's workspace and its head counts.  q, K, V and out must be 16-byte
+ * aligned (K and V rows move by bulk copies): MK_EINVAL otherwise. */
 mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T,
                                const void* q, const void* K, const void* V, int64_t t_stride,
                                void* out, mk_stream stream);
@@ -223,7 +224,8 @@ mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T,
  * therefore cannot provide a context's workspace.  It takes only inputs and
  * outputs and needs no context: q [n_seqs][n_q_heads][128], K, V
  * [n_seqs][n_kv_heads][t_stride][128] (bf16, device), T host int32
- * [n_seqs] with 1 <= T[i] <= t_stride, out [n_seqs][n_q_heads][128] bf16.
+ * [n_seqs] with 1 <= T[i] <= t_stride, out [n_seqs][n_q_heads][128] bf16;
+ * q, K, V and out 16-byte aligned (MK_EINVAL otherwise, before any launch).
  * Its scratch (split-T partials, counters, error word) is one static device
  * array of MK_NOALLOC_SCRATCH_BYTES that every GPU loading this library holds
  * until the process exits (about 4.3 MB).  Calls with
@@ -232,12 +234,22 @@ mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T,
  * array's device address (cudaGetSymbolAddress, with that device current);
  * make that first call before any stream capture.  Every call shares the
  * array and clears what must start at zero; calls that overlap on the GPU
- * (different streams without ordering) race on it and give wrong results. */
+ * (different streams without ordering) race on it and give wrong results.
+ * The return value covers host-side checks and the launch only.  A failure
+ * found on the device (a bounded wait for a copy that ran out) is recorded in
+ * the array's error word, which calls do not clear: from then on every call
+ * on that device leaves its output untouched until mk_noalloc_poll_error
+ * reports and clears the failure. */
 #define MK_NOALLOC_SCRATCH_BYTES 4456448
 #define MK_NOALLOC_MAX_QUERY_HEADS 128
 mk_status mk_dense_decode_attn_noalloc(int32_t n_q_heads, int32_t n_kv_heads, int32_t n_seqs,
                                        const int32_t* T, const void* q, const void* K, const void* V,
                                        int64_t t_stride, void* out, mk_stream stream);
+/* Device-side status of mk_dense_decode_attn_noalloc on the current device:
+ * waits for the whole device, then returns MK_OK, or MK_ETIMEOUT / MK_EDEVICE
+ * with the kernel's detail code in *detail (optional), and clears the error
+ * word so later calls run again.  Allocates nothing; no context needed. */
+mk_status mk_noalloc_poll_error(int32_t* detail);
 
 /* Set-up helper, not on the decode path: gram = X^T X (fp32 accumulation)
  * for X: device bf16 rows of 128 values, row i at x + i*row_stride elements

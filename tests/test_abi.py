@@ -76,3 +76,14 @@ def test_variant_options_change_the_arena(lib):
     nblk = (131072 + 64 - 4 - 256 + 31) // 32
     # one compressed key row per block and head: 5 * 32 = 160 bytes
     assert 8 * nblk * 160 <= a_keys - a0 <= 8 * (nblk * 160 + 256)
+
+
+def test_noalloc_refuses_misaligned_pointers_before_any_launch(lib):
+    # The pointers are never dereferenced: the 16-byte check comes first.
+    T = (ctypes.c_int32 * 1)(64)
+    good, odd = 1 << 20, (1 << 20) + 2
+    for q, k, v, o in ((odd, good, good, good), (good, odd, good, good), (good, good, odd, good),
+                       (good, good, good, odd)):
+        st = lib.mk_dense_decode_attn_noalloc(4, 1, 1, T, ctypes.c_void_p(q), ctypes.c_void_p(k),
+                                              ctypes.c_void_p(v), 64, ctypes.c_void_p(o), None)
+        assert st == 1
