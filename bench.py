@@ -170,32 +170,30 @@ class Clocks:
 # ----------------------------------------------------------------------------
 # CPU oracle sample (cpu_baseline and the reference arm)
 # ----------------------------------------------------------------------------
-def blas_threads():
+def _host_ram_bytes():
     try:
-        from threadpoolctl import threadpool_info
-        n = [p.get("num_threads", 1) for p in threadpool_info() if p.get("user_api") == "blas"]
-        if n:
-            return max(n)
-    except Exception:
-        pass
-    return os.cpu_count() or 1
+        return os.sysconf("SC_PHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        return 64 << 30
 
 
-def oracle_sample(wl, steps=None, seconds=15.0):
-    """Times the oracle's decode step on one (layer 0, seq 0, kv head 0) unit
-    of the workload and scales it to the full step (all layers, sequences and
-    kv heads): returns (context tokens/s, description, seconds timed)."""
-    import torch
+def _oracle_unit(job):
+    """One worker process: builds one (layer, sequence, kv head) unit of the
+    workload in the fp64 oracle (prefill), then times its decode steps (append
+    one token, select, attend) for `seconds`, or exactly `steps` of them.
+    Returns (seconds per decode step, steps timed)."""
+    wl, (layer, seq, kvh), steps, seconds = job
     from compressed_kv_cache_vector_gb300 import synth
     from oracle import mosaickv_oracle as O
-    T0 = wl.seq_lens[0]
-    n_extra = (steps or 4096) + 1
-    sd = synth.seed_for(wl.name, 0, 0, 0)
+    T0 = wl.seq_lens[seq]
+    n_extra = (steps if steps is not None else 4096) + 1
+    sd = synth.seed_for(wl.name, 0, layer, seq, kvh)
     K = synth.bf16_values(synth.lowrank_outlier(T0 + n_extra, D, wl.decay, sd))
     V = synth.bf16_values(synth.lowrank_outlier(T0 + n_extra, D, wl.decay, sd + 1))
     Rk, _ = O.rotation_from_keys(K[:T0])
     Rv, _ = O.rotation_from_keys(V[:T0])
-    st = O.Strategy(wl.n_sink, wl.window, wl.block, list(wl.segments), wl.topk_fixed, wl.retain_permille)
+    st = O.Strategy(wl.n_sink, wl.window, wl.block, list(wl.segments), wl.topk_fixed, wl.retain_permille,
+                    wl.meta_channels)
     oc = O.OracleCache(st, T0 + n_extra)
     oc.set_rotation(Rk, Rv)
     oc.append(K[:T0], V[:T0])
@@ -213,13 +211,43 @@ def oracle_sample(wl, steps=None, seconds=15.0):
             break
         if steps is None and (t_total >= seconds or n >= n_extra - 1):
             break
-    per_unit = t_total / n
-    units = wl.n_layers * wl.n_seqs * wl.n_kv_heads
-    full_step = per_unit * units
+    return t_total / n, n
+
+
+def oracle_sample(wl, steps=None, seconds=15.0):
+    """Times the oracle's decode step on a sample of the workload's units, one
+    single-threaded process per host core (spawned, never forked), each on its
+    own (layer, sequence, kv head) unit, all at once.  The full step's time is
+    extrapolated: every unit's mean step time, over the units the cores share.
+    Returns (context tokens/s, description, seconds of the longest worker,
+    processes used)."""
+    import multiprocessing as mpr
+    units = [(l, s, h) for l in range(wl.n_layers) for s in range(wl.n_seqs) for h in range(wl.n_kv_heads)]
+    cores = os.cpu_count() or 1
+    per_worker = 3600 * (max(wl.seq_lens) + 4096)         # oracle arrays of one unit, bytes
+    n_proc = max(1, min(cores, len(units), int(0.5 * _host_ram_bytes() // per_worker)))
+    pick = [units[(i * len(units)) // n_proc] for i in range(n_proc)]
+    env_keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in env_keys}
+    for k in env_keys:
+        os.environ[k] = "1"                              # one thread per worker process
+    try:
+        with mpr.get_context("spawn").Pool(n_proc) as pool:
+            res = pool.map(_oracle_unit, [(wl, u, steps, seconds) for u in pick])
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    mean_step = sum(r[0] for r in res) / len(res)
+    full_step = mean_step * len(units) / n_proc         # the cores share the units
     ctx = sum(wl.seq_lens) * wl.n_layers
-    desc = (f"{n} decode steps of one (layer, sequence, kv head) unit at T={T0} (fp64 numpy oracle), "
-            f"scaled by {units} units to one full step")
-    return ctx / full_step, desc, t_total
+    n_steps = sum(r[1] for r in res)
+    desc = (f"{n_proc} single-threaded processes in parallel, each timing decode steps of its own "
+            f"(layer, sequence, kv head) unit (fp64 numpy oracle; {n_steps} steps in all); the full step "
+            f"of {len(units)} units extrapolated as mean step time x {len(units)} / {n_proc}")
+    return ctx / full_step, desc, max(r[0] * r[1] for r in res), n_proc
 
 
 # ----------------------------------------------------------------------------
@@ -269,8 +297,35 @@ def build_gpu(wl, dev, rank, capacity_extra):
     return mk
 
 
+def _free_port():
+    import socket
+    so = socket.socket()
+    so.bind(("127.0.0.1", 0))
+    port = so.getsockname()[1]
+    so.close()
+    return port
+
+
+def launch_ranks(a):
+    """--gpus N outside a launcher: run this script as N ranks under
+    torch.distributed.run (one process per GPU, rendezvous on 127.0.0.1) and
+    return its exit code.  Our arm needs N visible GPUs; it exits with an error
+    instead of running fewer ranks than asked."""
+    if a.impl == "ours":
+        import torch
+        have = torch.cuda.device_count()
+        if have < a.gpus:
+            print(f"bench.py: --gpus {a.gpus} asked, {have} GPU(s) visible", file=sys.stderr)
+            return 2
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={a.gpus}",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     a = parse()
+    if a.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(a))
     import torch
     from compressed_kv_cache_vector_gb300 import configs
     wl = configs.get(a.config)
@@ -299,10 +354,12 @@ def main():
     if a.impl == "reference":
         if rank != 0:
             return
-        cpu_v, desc, secs = oracle_sample(wl, steps=a.warmup + a.steps)
+        cpu_v, desc, secs, n_proc = oracle_sample(wl, steps=a.warmup + a.steps)
         line = dict(base, impl="reference", value=cpu_v, n_gpus=world,
-                    ms_per_step=1e3 * sum(wl.seq_lens) * wl.n_layers / cpu_v, config=wcfg,
-                    cpu_baseline={"value": cpu_v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                    ms_per_step=1e3 * sum(wl.seq_lens) * wl.n_layers / cpu_v,
+                    ms_per_step_kind=f"extrapolated: sampled units' mean step time x units / {n_proc} processes",
+                    config=wcfg,
+                    cpu_baseline={"value": cpu_v, "unit": UNIT, "cores": n_proc, "kind": "oracle",
                                   "sample": desc},
                     e2e={"value": cpu_v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                     dtype="f64")
@@ -361,6 +418,15 @@ def main():
     with torch.cuda.graph(graph_ev, stream=s):
         step(True)
     torch.cuda.synchronize()
+    # A third capture: only the layers' attention launches, back to back (each
+    # over its layer's cache and selection, as left by the step), for the
+    # dominant kernel's average launch duration without event nodes between
+    # kernels.
+    graph_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_attn, stream=s):
+        for l in range(L):
+            mk.decode_attn(l, seqs, *sel[l], out=outs[l])
+    torch.cuda.synchronize()
     mk.sync_state()
     T_start = [mk.seq_length(0, si) for si in seqs]
 
@@ -402,6 +468,14 @@ def main():
             app_ms.append(ev[l][0].elapsed_time(ev[l][1]))
             sel_ms.append(ev[l][1].elapsed_time(ev[l][2]))
             attn_ms.append(ev[l][2].elapsed_time(ev[l][3]))
+    # Timed region C: the attention-only graph, K times.
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(a.steps):
+        graph_attn.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    attn_only_ms = e0.elapsed_time(e1) / (a.steps * L)
     clk = clocks.stop()
     mk.sync_state()
     st, detail = mk.poll_error()
@@ -435,11 +509,13 @@ def main():
     attn_avg = statistics.mean(attn_ms)
     sel_avg = statistics.mean(sel_ms)
     app_avg = statistics.mean(app_ms)
-    achieved = per["attn"] / (attn_avg * 1e-3) / 1e9
+    achieved = per["attn"] / (attn_only_ms * 1e-3) / 1e9
     roofline = {"kernel": "k_attn (packed sparse attention + split-T combine + un-rotation)",
                 "bound": "hbm", "achieved": achieved, "peak": peak, "peak_source": peak_src,
                 "unit": "GB/s", "frac": achieved / peak, "traffic": None,
-                "alg_bytes_per_launch": per["attn"], "avg_launch_ms": attn_avg}
+                "alg_bytes_per_launch": per["attn"], "avg_launch_ms": attn_only_ms,
+                "avg_launch_ms_how": f"CUDA events around {a.steps} replays of a graph of the {L} layers' "
+                                     "attention launches back to back, divided by the launches"}
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             tr = json.load(f).get(wl.name, {}).get("k_attn")
@@ -460,8 +536,12 @@ def main():
             "append_select_ms": app_avg + sel_avg, "attn_ms": attn_avg,
             "append_select_gbs": (per["append"] + per["select"]) / ((app_avg + sel_avg) * 1e-3) / 1e9,
         }
-    phases.update({"attn_gbs": achieved, "step_span_ms": statistics.mean(span_ms), "alg_bytes_per_layer": per,
-                   "launches_per_layer": LAUNCHES_PER_LAYER[a.separate]})
+    phases.update({"attn_gbs_instrumented": per["attn"] / (attn_avg * 1e-3) / 1e9,
+                   "step_span_ms": statistics.mean(span_ms), "alg_bytes_per_layer": per,
+                   "launches_per_layer": LAUNCHES_PER_LAYER[a.separate],
+                   "how": "instrumented graph: event-record nodes between the kernels, so a kernel cannot start "
+                          "its prologue under the previous one (programmatic dependent launch overlap is lost); "
+                          "each phase is timed alone and the phases add up to more than the step"})
 
     # end to end through the public API with host buffers (eager calls): each
     # step copies all layers' new k, v and q from one pinned host buffer in
@@ -516,19 +596,20 @@ def main():
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
-        cpu_v, desc, secs = oracle_sample(wl, seconds=a.cpu_seconds)
-        cpu = {"value": cpu_v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc,
+        cpu_v, desc, secs, n_proc = oracle_sample(wl, seconds=a.cpu_seconds)
+        cpu = {"value": cpu_v, "unit": UNIT, "cores": n_proc, "kind": "oracle", "sample": desc,
                "seconds": secs}
 
     if rank != 0:
         return
     line = dict(base, value=value, ms_per_step=ms,
-                config=dict(wcfg, l2="step reads ~%.2f GB across layers, far above the 129 MB L2" %
-                            (step_bytes / 1e9),
-                            timing="CUDA graph of one full step, replayed; CUDA events on the stream",
-                            untimed_soak_steps=n_soak,
-                            calls=("mk_append_compress + mk_block_select + mk_decode_attn" if a.separate else
-                                   "mk_append_select + mk_decode_attn") + " per layer"),
+                config=wcfg,
+                timing={"l2": "step reads ~%.2f GB across layers, far above the 129 MB L2, so no flush" %
+                              (step_bytes / 1e9),
+                        "how": "CUDA graph of one full step, replayed; CUDA events on the stream",
+                        "untimed_soak_steps": n_soak,
+                        "calls": ("mk_append_compress + mk_block_select + mk_decode_attn" if a.separate else
+                                  "mk_append_select + mk_decode_attn") + " per layer"},
                 hbm_gbs=gbs, alg_bytes_per_step=step_bytes, roofline=roofline, phases=phases,
                 cpu_baseline=cpu, e2e=e2e, gpu_launches=LAUNCHES_PER_LAYER[a.separate] * L * a.steps, clocks=clk)
     if mk.prefill_ms:

@@ -156,3 +156,40 @@ def score_tolerance(qr, mn, mx):
     """Bound on |fp32 score - exact score|: 128-term fp32 sums of exact products."""
     terms = np.abs(qr)[:, None, :] * np.maximum(np.abs(mn), np.abs(mx))[None, :, :]
     return (terms.sum(axis=2).max(axis=0) / math.sqrt(D)) * (D + 2) * 2.0 ** -24 + 1e-30
+
+
+def check_storage(p: Pair, unit):
+    """Sinks, window ring, meta and pages bit-exact against the oracle."""
+    oc = p.orc[unit]
+    l, s, h = unit
+    views = p.mk.unit_views(l, s, h)
+    S, W, B = p.c.n_sink, p.c.window, p.c.block
+    sp = oc.sink_positions()
+    if len(sp):
+        assert np.array_equal(bits(views["sink_k"])[: len(sp)], O.bf16_bits(oc.Kr[sp]))
+        assert np.array_equal(bits(views["sink_v"])[: len(sp)], O.bf16_bits(oc.Vr[sp]))
+    wk, wv = bits(views["win_k"]), bits(views["win_v"])
+    for pos in oc.window_positions():
+        slot = (pos - S) % W
+        assert np.array_equal(wk[slot], O.bf16_bits(oc.Kr[pos])), pos
+        assert np.array_equal(wv[slot], O.bf16_bits(oc.Vr[pos])), pos
+    nb = oc.n_blocks_mid()
+    mn, mx = oc.meta()
+    meta = bits(views["meta"])[:nb]
+    assert np.array_equal(meta[:, 0], O.bf16_bits(mn))
+    assert np.array_equal(meta[:, 1], O.bf16_bits(mx))
+    if p.c.meta_channels:
+        m = p.c.meta_channels
+        idx, cmn, cmx = O.compress_key_rows(mn, mx, m)
+        rows = views["cmeta"].cpu().numpy()[:nb]
+        assert np.array_equal(rows[:, :2 * m].copy().view(np.uint16), O.bf16_bits(cmn))
+        assert np.array_equal(rows[:, 2 * m:4 * m].copy().view(np.uint16), O.bf16_bits(cmx))
+        assert np.array_equal(rows[:, 4 * m:5 * m], idx.astype(np.uint8))
+    pages = views["pages"].cpu().numpy()
+    for b in range(nb):
+        r = oc.r_of_block(b)
+        lo, hi = oc.block_tokens(b)
+        got = page_rows(pages[b], B, r, hi - lo)
+        want = page_rows(oc.page_bytes(b), B, r, hi - lo)
+        for g, w_, name in zip(got, want, ("kval", "kidx", "vval", "vidx")):
+            assert np.array_equal(g, w_), (b, name)
