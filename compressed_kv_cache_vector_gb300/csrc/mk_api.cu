@@ -26,8 +26,7 @@ struct mk_ctx {
   std::vector<int32_t> T0;           // prefill length, 0 = not started
   std::vector<int32_t> firsts;       // [layers][max_seqs][MK_MAX_SEGMENTS]
   std::vector<uint8_t> rot_set;      // [layers][max_seqs][n_kv]
-  int sel_layer = -1;                // last mk_block_select: layer and sequence list
-  std::vector<int32_t> sel_seqs;
+  std::vector<std::vector<int32_t>> sel_seqs;  // per layer: sequence list of its last selection
 };
 
 namespace {
@@ -108,7 +107,7 @@ Plan make_plan(const mk_config* c) {
   p.arena_bytes = p.units_off + p.n_units * L.unit_stride;
   const int64_t slots = (int64_t)c->max_seqs * c->n_kv_heads;
   int64_t w = 0;
-  w = align_up(w + slots * L.G * D * 4);                       // qrot
+  w = align_up(w + (int64_t)c->n_layers * slots * L.G * D * 4);  // qrot, per layer
   w = align_up(w + slots * (int64_t)L.keys_stride * 4);        // block keys
   w = align_up(w + slots * (int64_t)mk::kKeyBins * 4);         // coarse key histograms
   w = align_up(w + slots * MK_MAX_SPLITS * L.G * D * 4);       // part_acc
@@ -129,7 +128,7 @@ void bind_pointers(Plan& p, void* arena, void* ws) {
   const int64_t slots = (int64_t)L.max_seqs * L.n_kv;
   char* w = static_cast<char*>(ws);
   int64_t o = 0;
-  L.qrot = reinterpret_cast<float*>(w + o); o = align_up(o + slots * L.G * D * 4);
+  L.qrot = reinterpret_cast<float*>(w + o); o = align_up(o + (int64_t)L.n_layers * slots * L.G * D * 4);
   L.keys = reinterpret_cast<uint32_t*>(w + o); o = align_up(o + slots * (int64_t)L.keys_stride * 4);
   L.khist = reinterpret_cast<uint32_t*>(w + o); o = align_up(o + slots * (int64_t)mk::kKeyBins * 4);
   L.part_acc = reinterpret_cast<float*>(w + o); o = align_up(o + slots * MK_MAX_SPLITS * L.G * D * 4);
@@ -298,6 +297,7 @@ mk_status mk_create(const mk_config* cfg, void* arena, size_t arena_bytes, void*
   ctx->T0.assign(ls, 0);
   ctx->firsts.assign(ls * MK_MAX_SEGMENTS, 0);
   ctx->rot_set.assign(ls * cfg->n_kv_heads, 0);
+  ctx->sel_seqs.assign(cfg->n_layers, std::vector<int32_t>());
   cudaError_t e = cudaMemset(arena, 0, (size_t)p.units_off);
   if (e == cudaSuccess) e = cudaMemset(ctx->L.counters, 0, sizeof(int32_t) * 2 * cfg->max_seqs * cfg->n_kv_heads);
   if (e == cudaSuccess)
@@ -448,8 +448,7 @@ mk_status mk_block_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int3
                                           std::max(1, max_nblk), (cudaStream_t)stream);
   delete cs;
   if (e != cudaSuccess) return MK_ECUDA;
-  ctx->sel_layer = layer;
-  ctx->sel_seqs.assign(seq_ids, seq_ids + n_seqs);
+  ctx->sel_seqs[layer].assign(seq_ids, seq_ids + n_seqs);
   return MK_OK;
 }
 
@@ -484,8 +483,7 @@ mk_status mk_append_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int
   delete cs;
   if (e != cudaSuccess) return MK_ECUDA;
   for (int i = 0; i < n_seqs; ++i) ctx->T[(size_t)layer * ctx->cfg.max_seqs + seq_ids[i]] += 1;
-  ctx->sel_layer = layer;
-  ctx->sel_seqs.assign(seq_ids, seq_ids + n_seqs);
+  ctx->sel_seqs[layer].assign(seq_ids, seq_ids + n_seqs);
   return MK_OK;
 }
 
@@ -494,9 +492,8 @@ mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32
   mk_status st = check_seqs(ctx, layer, n_seqs, seq_ids);
   if (st != MK_OK) return st;
   if (!ids || !n_sel || !out) return MK_EINVAL;
-  if (ctx->sel_layer != layer || (int)ctx->sel_seqs.size() != n_seqs ||
-      !std::equal(ctx->sel_seqs.begin(), ctx->sel_seqs.end(), seq_ids))
-    return MK_ESTATE;
+  const std::vector<int32_t>& last = ctx->sel_seqs[layer];
+  if ((int)last.size() != n_seqs || !std::equal(last.begin(), last.end(), seq_ids)) return MK_ESTATE;
   CallSeqs* cs = new (std::nothrow) CallSeqs();
   if (!cs) return MK_ENOMEM;
   cs->n = n_seqs;

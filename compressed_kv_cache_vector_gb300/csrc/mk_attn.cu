@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
   const int hq = g % G;
   uint32_t aq[8][4];
   auto load_q = [&]() {
-    const float* qrot = L.qrot + slot * G * D;
+    const float* qrot = qrot_of(L, layer, slot);
     const uint16_t* qin = DENSE ? q_in + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D : nullptr;
     float2 qx[8][2];
 #pragma unroll

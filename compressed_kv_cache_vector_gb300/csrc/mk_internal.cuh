@@ -61,7 +61,7 @@ struct Layout {
   int32_t attn_tg;              // attention: tokens per staged page group (32 or 16)
   int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, warps per CTA, stage bytes
   // workspace
-  float* qrot;                  // [max_seqs][n_kv][G][128]
+  float* qrot;                  // [n_layers][max_seqs][n_kv][G][128]: q' of each layer's last selection
   uint32_t* keys;               // [max_seqs][n_kv][keys_stride]: ordered block-score keys, 0 = not a candidate
   int32_t keys_stride;          // nblk_cap rounded up to a multiple of 4
   uint32_t* khist;              // [max_seqs][n_kv][kKeyBins]: key counts by top 12 bits (zero between calls)
@@ -82,6 +82,10 @@ struct CallSeqs {
 
 __host__ __device__ inline int64_t unit_index(const Layout& L, int layer, int seq, int kvh) {
   return ((int64_t)layer * L.max_seqs + seq) * L.n_kv + kvh;
+}
+// q' of (layer, sequence slot), written by the selection, read by attention.
+__host__ __device__ inline float* qrot_of(const Layout& L, int layer, int64_t slot) {
+  return L.qrot + ((int64_t)layer * L.max_seqs * L.n_kv + slot) * L.G * 128;
 }
 __host__ __device__ inline int n_mid_tokens(const Layout& L, int T) {
   int m = T - L.W - L.S;

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     ud = L.desc[u];
   }
   if (part == 0)
-    for (int i = tid; i < G * D; i += blockDim.x) L.qrot[slot * G * D + i] = qr[0][i / D][i % D];
+    for (int i = tid; i < G * D; i += blockDim.x) qrot_of(L, layer, slot)[i] = qr[0][i / D][i % D];
   __syncthreads();  // also: the R_k^T area becomes the tile stages
   if (s_abort) return;
 

@@ -199,9 +199,10 @@ mk_status mk_block_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int3
 /* PackedAttention ([N] Eq. (13), (14); [S] sec. 5.3): for each query head,
  * softmax attention of q' over the sink tokens, the window, the tokens of the
  * selected blocks and of the always-attended segments, read straight from the
- * packed pages; then output = o' R_v.  Must follow mk_block_select for the
- * same layer and sequence list (it reads that call's q' from the workspace).
- * ids/n_sel: as written by mk_block_select.  out: device bf16
+ * packed pages; then output = o' R_v.  Uses the q' of the last
+ * mk_block_select (or mk_append_select) of the same layer, kept in the
+ * workspace per layer, whose sequence list must equal this call's: MK_ESTATE
+ * otherwise.  ids/n_sel: as written by that call.  out: device bf16
  * [n_seqs][n_q_heads][128]. */
 mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32_t* seq_ids,
                          const int32_t* ids, const int32_t* n_sel, void* out, mk_stream stream);
