@@ -10,7 +10,10 @@ and a few (sequence, kv head) units are followed by the fp64 oracle:
     window 256, 10% of blocks), rotations exact in bf16 (signed permutations)
     so that every stored byte can be compared;
   * one kv head of the 1M-token layer (T = 1048576, block 64, window 512, 5% of
-    blocks) with rotations from the eigenvectors of K^T K;
+    blocks), with a signed permutation and with rotations from the
+    eigenvectors of K^T K (there the scores are checked on the block keys the
+    kernel stored, since a general rotation may round a stored value one bf16
+    step away from the oracle's);
   * the serving mix: 64 sequences of log-uniform lengths 8K..128K, the middle
     30% kept at r = 64 and attended in full, the rest r = 32 with 10% of blocks.
 
@@ -26,7 +29,7 @@ import torch
 
 from compressed_kv_cache_vector_gb300 import configs, synth
 from oracle import mosaickv_oracle as O
-from tests.harness import Case, Pair, check_storage, rel_l2, score_tolerance
+from tests.harness import Case, Pair, bits, check_storage, rel_l2, score_tolerance
 
 pytestmark = pytest.mark.gpu
 ATOL_REL = 5e-3
@@ -36,6 +39,7 @@ def _fused_steps(p: Pair, n_steps: int):
     """n_steps decode steps through mk_append_select + mk_decode_attn, each
     checked against the oracle units; returns the number of near-ties met."""
     c = p.c
+    exact = c.rot != "eigh"
     G = c.G
     seqs = list(range(len(c.seq_lens)))
     scores = torch.empty(len(seqs), c.n_kv, p.mk.nblk_cap, dtype=torch.float32, device="cuda")
@@ -63,13 +67,21 @@ def _fused_steps(p: Pair, n_steps: int):
             assert ns_h[s, h] == k_, (step, s, h)
             got_ids = ids_h[s, h, :k_]
             if len(cand):
-                _, grp = oc.scores(qs)
-                mn, mx = oc.score_keys()
+                nb = oc.n_blocks_mid()
+                if exact:
+                    mn, mx = oc.score_keys()
+                else:
+                    # A general rotation rounds a stored value one bf16 step
+                    # away from the oracle's now and then, so the kernel's
+                    # block keys are scored as stored.
+                    meta = O.bits_to_value(bits(p.mk.unit_views(l, s, h)["meta"])[:nb])
+                    mn, mx = meta[:, 0], meta[:, 1]
+                grp = O.block_scores(oc.rotate_query(qs), mn, mx)[1]
                 tol = score_tolerance(oc.rotate_query(qs), mn, mx)
-                got_s = sc_h[s, h, :oc.n_blocks_mid()].astype(np.float64)
+                got_s = sc_h[s, h, :nb].astype(np.float64)
                 assert np.all(np.abs(got_s[cand] - grp[cand]) <= tol[cand]), (step, s, h)
                 assert np.array_equal(got_ids, O.topk_blocks(got_s, cand, k_)), (step, s, h)
-                want_ids, _ = oc.select(qs)
+                want_ids = O.topk_blocks(grp, cand, k_)
                 if not np.array_equal(got_ids, want_ids):
                     srt = np.sort(grp[cand])[::-1]
                     assert k_ < len(cand) and srt[k_ - 1] - srt[k_] <= 2 * tol.max(), (step, s, h)
@@ -100,12 +112,15 @@ def test_128k_layer_fused_decode_steps():
     assert p.mk.seq_length(0, 0) == 131072 + 3
 
 
-def test_1m_layer_one_kv_head_fused_decode_steps():
+@pytest.mark.parametrize("rot", ["perm", "eigh"])
+def test_1m_layer_one_kv_head_fused_decode_steps(rot):
     wl = configs.get("c4")
-    case = _case_from(wl, n_q=wl.group, n_kv=1, rot="eigh", steps=[1, 1], seed=401)
+    case = _case_from(wl, n_q=wl.group, n_kv=1, rot=rot, steps=[1, 1], seed=401)
     p = Pair(case)                                  # T = 1048576, 16376 middle blocks, k = 819
     assert p.mk.nblk_cap >= 16376
     assert _fused_steps(p, 2) <= 1
+    if rot == "perm":
+        check_storage(p, p.units[0])
 
 
 def test_serving_mix_64_sequences_fused_decode_steps():
