@@ -70,6 +70,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dense-ref", action="store_true", help="also time the uncompressed reference kernel")
+    ap.add_argument("--no-quest", action="store_true", help="skip the Quest comparator (uncompressed pages)")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling runs)")
     ap.add_argument("--meta-channels", type=int, default=0,
                     help="variant: channel-compressed per-block keys keeping this many channels")
@@ -253,15 +254,21 @@ def oracle_sample(wl, steps=None, seconds=15.0):
 # ----------------------------------------------------------------------------
 # GPU workload
 # ----------------------------------------------------------------------------
-def build_gpu(wl, dev, rank, capacity_extra):
+def build_gpu(wl, dev, rank, capacity_extra, quest=False):
+    """The workload's cache on the GPU, built by bulk prefill of every layer.
+    quest=True builds the Quest comparator instead: uncompressed pages
+    (every channel kept), identity rotations, the same segments and blocks."""
     import torch
     from compressed_kv_cache_vector_gb300 import binding, synth
     from compressed_kv_cache_vector_gb300.build import build
     build()
+    segments = [(sg[0], D, sg[2]) for sg in wl.segments] if quest else wl.segments
     cfg = binding.make_config(wl.n_q_heads, wl.n_kv_heads, wl.n_layers, wl.n_seqs,
                               max(wl.seq_lens) + capacity_extra, wl.n_sink, wl.window, wl.block,
-                              wl.segments, wl.topk_fixed, wl.retain_permille, wl.meta_channels)
+                              segments, wl.topk_fixed, wl.retain_permille, 0 if quest else wl.meta_channels,
+                              1 if quest else 0)
     mk = binding.MosaicKV(cfg, dev)
+    eye = np.eye(D, dtype=np.float32)
     seqs = list(range(wl.n_seqs))
     prefill_ms = mk.prefill_ms = []
     gram = torch.empty(D, D, dtype=torch.float32, device=dev)
@@ -273,9 +280,12 @@ def build_gpu(wl, dev, rank, capacity_extra):
                 sd = synth.seed_for(wl.name, rank, l, s, h)
                 k = synth.lowrank_outlier(T, D, wl.decay, sd, device=dev)
                 v = synth.lowrank_outlier(T, D, wl.decay, sd + 1, device=dev)
-                Rk = binding.rotation_from_gram(binding.gram(k, T, D, gram).cpu().numpy())
-                Rv = binding.rotation_from_gram(binding.gram(v, T, D, gram).cpu().numpy())
-                mk.set_rotation(l, s, h, Rk, Rv)
+                if quest:
+                    mk.set_rotation(l, s, h, eye, eye)
+                else:
+                    Rk = binding.rotation_from_gram(binding.gram(k, T, D, gram).cpu().numpy())
+                    Rv = binding.rotation_from_gram(binding.gram(v, T, D, gram).cpu().numpy())
+                    mk.set_rotation(l, s, h, Rk, Rv)
                 kh.append(k)
                 vh.append(v)
             ks.append(torch.stack(kh, 1))
@@ -427,6 +437,13 @@ def main():
         for l in range(L):
             mk.decode_attn(l, seqs, *sel[l], out=outs[l])
     torch.cuda.synchronize()
+    graph_sel = None
+    if not a.separate:   # and only the selection calls (append + block selection), back to back
+        graph_sel = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_sel, stream=s):
+            for l in range(L):
+                mk.append_select(l, seqs, k_in[l], v_in[l], q_in[l], *sel[l])
+        torch.cuda.synchronize()
     mk.sync_state()
     T_start = [mk.seq_length(0, si) for si in seqs]
 
@@ -476,6 +493,8 @@ def main():
     e1.record()
     torch.cuda.synchronize()
     attn_only_ms = e0.elapsed_time(e1) / (a.steps * L)
+    # Timed region D: the selection-only graph, K times.
+    sel_only_ms = time_graph(graph_sel, a.steps) / L if graph_sel is not None else None
     clk = clocks.stop()
     mk.sync_state()
     st, detail = mk.poll_error()
@@ -536,7 +555,9 @@ def main():
             "append_select_ms": app_avg + sel_avg, "attn_ms": attn_avg,
             "append_select_gbs": (per["append"] + per["select"]) / ((app_avg + sel_avg) * 1e-3) / 1e9,
         }
-    phases.update({"attn_gbs_instrumented": per["attn"] / (attn_avg * 1e-3) / 1e9,
+    phases.update({"graphs_ms_per_layer": {"step": ms / L, "append_select_only": sel_only_ms,
+                                           "attn_only": attn_only_ms},
+                   "attn_gbs_instrumented": per["attn"] / (attn_avg * 1e-3) / 1e9,
                    "step_span_ms": statistics.mean(span_ms), "alg_bytes_per_layer": per,
                    "launches_per_layer": LAUNCHES_PER_LAYER[a.separate],
                    "how": "instrumented graph: event-record nodes between the kernels, so a kernel cannot start "
@@ -593,6 +614,14 @@ def main():
     dense = None
     if a.dense_ref and rank == 0:
         dense = dense_reference(mk, wl, dev)
+    quest = None
+    if not a.no_quest and rank == 0 and not a.separate:
+        del graph, graph_ev, graph_attn, graph_sel
+        quest = quest_reference(wl, dev, rank, a.steps)
+        quest["attn_ratio_quest_over_ours"] = quest["attn_ms_per_layer"] / attn_only_ms
+        if sel_only_ms:
+            quest["select_ratio_quest_over_ours"] = quest["select_ms_per_layer"] / sel_only_ms
+        quest["step_ratio_quest_over_ours"] = quest["step_ms_per_layer"] / (ms / L)
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
@@ -623,7 +652,91 @@ def main():
             "how": "CUDA events around the bulk mk_append_compress of each layer while building the cache"}
     if dense:
         line["dense_reference"] = dense
+    if quest:
+        line["quest_reference"] = quest
     print(json.dumps(line), flush=True)
+
+
+def time_graph(graph, reps):
+    """ms per replay of a captured graph: CUDA events around `reps` replays on
+    the current stream, after one untimed replay."""
+    import torch
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def capture_layer_graphs(mk, L, seqs, k_in, v_in, q_in, sel, outs, stream):
+    """Three graphs over L layers: the whole decode step (append + selection,
+    attention), the selection calls alone, the attention calls alone."""
+    import torch
+    graphs = {}
+    for name in ("step", "select", "attn"):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(L):
+                if name != "attn":
+                    mk.append_select(l, seqs, k_in[l], v_in[l], q_in[l], *sel[l])
+                if name != "select":
+                    mk.decode_attn(l, seqs, *sel[l], out=outs[l])
+        torch.cuda.synchronize()
+        graphs[name] = g
+    return graphs
+
+
+def quest_reference(wl, dev, rank, steps):
+    """The Quest comparator ([S] sec. 6.1, 6.3) on the same workload shape:
+    uncompressed pages, identity rotations, the same block selection kernels
+    and the same attention kernel reading whole rows.  Built for as few
+    layers as make one pass over their selected pages larger than the L2
+    (so no layer is read from L2 on its next turn)."""
+    import copy
+    import torch
+    from compressed_kv_cache_vector_gb300 import synth
+    qw = copy.deepcopy(wl)
+    B = wl.block
+    nblk = max(1, (max(wl.seq_lens) - wl.n_sink - wl.window) // B)
+    k = max(1, (wl.retain_permille * nblk + 999) // 1000) if not wl.topk_fixed else wl.topk_fixed
+    sel_bytes = k * B * 4 * D * wl.n_kv_heads * wl.n_seqs
+    qw.n_layers = int(min(wl.n_layers, max(1, math.ceil(3 * 129e6 / sel_bytes))))
+    qw.meta_channels = 0
+    reps = max(4, steps)
+    mk = build_gpu(qw, dev, rank, 4 * reps + 16, quest=True)
+    L, n_seq = qw.n_layers, qw.n_seqs
+    seqs = list(range(n_seq))
+    g = torch.Generator(device=dev)
+    g.manual_seed(4321 + rank)
+    k_in = [torch.randn(n_seq, qw.n_kv_heads, D, generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+    v_in = [torch.randn(n_seq, qw.n_kv_heads, D, generator=g, device=dev).to(torch.bfloat16) for _ in range(L)]
+    q_in = [synth.query(n_seq, qw.n_q_heads, D, synth.seed_for(wl.name, "q", rank, l), device=dev) for l in range(L)]
+    sel = [mk.alloc_select(n_seq) for _ in range(L)]
+    outs = [torch.empty(n_seq, qw.n_q_heads, D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for l in range(L):
+            mk.append_select(l, seqs, k_in[l], v_in[l], q_in[l], *sel[l])
+            mk.decode_attn(l, seqs, *sel[l], out=outs[l])
+    torch.cuda.synchronize()
+    graphs = capture_layer_graphs(mk, L, seqs, k_in, v_in, q_in, sel, outs, s)
+    res = {name: time_graph(gr, reps) / L for name, gr in graphs.items()}
+    st, detail = mk.poll_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the Quest comparator: {st}/{detail}")
+    out = {"layers": L, "step_ms_per_layer": res["step"], "select_ms_per_layer": res["select"],
+           "attn_ms_per_layer": res["attn"], "selected_page_bytes_per_layer": sel_bytes,
+           "how": "uncompressed pages (every channel, no rotation), same selection and attention kernels; "
+                  "graphs of the layers' calls, CUDA events around replays"}
+    mk.close()
+    del mk
+    torch.cuda.empty_cache()
+    return out
 
 
 def dense_reference(mk, wl, dev, reps=10):

@@ -40,7 +40,8 @@ class MkConfig(ctypes.Structure):
     _fields_ = [("head_dim", c_i32), ("n_q_heads", c_i32), ("n_kv_heads", c_i32), ("n_layers", c_i32),
                 ("max_seqs", c_i32), ("max_tokens", c_i32), ("n_sink", c_i32), ("window", c_i32),
                 ("block", c_i32), ("topk_fixed", c_i32), ("retain_permille", c_i32),
-                ("n_segments", c_i32), ("seg", MkSegment * MK_MAX_SEGMENTS), ("meta_channels", c_i32)]
+                ("n_segments", c_i32), ("seg", MkSegment * MK_MAX_SEGMENTS), ("meta_channels", c_i32),
+                ("page_format", c_i32)]
 
 
 class MkAlg2Params(ctypes.Structure):
@@ -138,7 +139,7 @@ def _stream(stream=None):
 
 
 def make_config(n_q_heads, n_kv_heads, n_layers, max_seqs, max_tokens, n_sink, window, block,
-                segments, topk_fixed=0, retain_permille=0, meta_channels=0) -> MkConfig:
+                segments, topk_fixed=0, retain_permille=0, meta_channels=0, page_format=0) -> MkConfig:
     c = MkConfig()
     c.head_dim = MK_HEAD_DIM
     c.n_q_heads, c.n_kv_heads, c.n_layers = n_q_heads, n_kv_heads, n_layers
@@ -146,6 +147,7 @@ def make_config(n_q_heads, n_kv_heads, n_layers, max_seqs, max_tokens, n_sink, w
     c.n_sink, c.window, c.block = n_sink, window, block
     c.topk_fixed, c.retain_permille = topk_fixed, retain_permille
     c.meta_channels = meta_channels
+    c.page_format = page_format
     c.n_segments = len(segments)
     for i, sg in enumerate(segments):
         b, r, a = sg[:3]

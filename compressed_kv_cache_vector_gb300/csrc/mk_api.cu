@@ -61,7 +61,10 @@ mk_status check_config(const mk_config* c) {
     if (i == 0 && s.begin_permille != 0) return MK_EINVAL;
     if (s.begin_permille < prev) return MK_EINVAL;
     prev = s.begin_permille;
+    if (c->page_format == MK_PAGES_DENSE && (s.r != MK_HEAD_DIM || s.keep_channels != 0)) return MK_EINVAL;
   }
+  if (c->page_format != MK_PAGES_PACKED && c->page_format != MK_PAGES_DENSE) return MK_EINVAL;
+  if (c->page_format == MK_PAGES_DENSE && c->meta_channels != 0) return MK_EINVAL;
   return MK_OK;
 }
 
@@ -84,7 +87,9 @@ Plan make_plan(const mk_config* c) {
   L.nblk_cap = mk::n_mid_blocks(L, c->max_tokens);
   L.k_max = std::max(1, mk::n_select(L, L.nblk_cap));
   L.keys_stride = (std::max(1, L.nblk_cap) + 3) & ~3;
-  L.page_stride = (int64_t)6 * L.B * r_max;
+  L.dense_pages = c->page_format == MK_PAGES_DENSE ? 1 : 0;
+  // packed: 6 r bytes per token (K and V values and indices); dense: 2 x 256
+  L.page_stride = L.dense_pages ? (int64_t)4 * L.B * MK_HEAD_DIM : (int64_t)6 * L.B * r_max;
   const int64_t D = MK_HEAD_DIM;
   int64_t off = 0;
   L.off_rkt = off; off += D * D * 4;
@@ -633,6 +638,7 @@ mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_he
   if (!ctx || !pages || !meta) return MK_EINVAL;
   const mk_config& c = ctx->cfg;
   const Layout& L = ctx->L;
+  if (L.dense_pages) return MK_ENOTSUP;  // uncompressed pages have nothing to re-compress
   if (layer < 0 || layer >= c.n_layers || seq < 0 || seq >= c.max_seqs || kv_head < 0 || kv_head >= c.n_kv_heads)
     return MK_EINVAL;
   if (segment < 0 || segment >= c.n_segments) return MK_EINVAL;

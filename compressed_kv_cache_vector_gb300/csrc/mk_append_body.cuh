@@ -11,6 +11,16 @@
 
 namespace mk {
 
+// Uncompressed pages (the Quest comparator): token slot t of block b holds
+// the whole rotated key row at [t] and value row at [B + t] of 128 bf16 words.
+// A lane stores its four channels (4*lane .. 4*lane+3).
+__device__ __forceinline__ void store_dense_row(const Layout& L, char* base, int b, int t, int is_v,
+                                                uint2 four, int lane) {
+  uint16_t* row = reinterpret_cast<uint16_t*>(base + L.off_pages + (int64_t)b * L.page_stride) +
+                  (int64_t)(is_v * L.B + t) * D;
+  reinterpret_cast<uint2*>(row)[lane] = four;
+}
+
 // Per-vector top-r of 128 bf16 magnitudes held 4 per lane (channels
 // 4*lane .. 4*lane+3).  Keeps the r largest magnitudes, ties to the lower
 // channel.  Returns this lane's keep bits; rank0 receives the packed position
@@ -105,13 +115,18 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
 #pragma unroll
   for (int i = 0; i < 4; ++i) mag[i] = 4 * lane + i < keep ? v[i] & 0x7fffu : 0u;
   int rank;
-  const unsigned kbits = warp_topr(mag, r, lane, rank);
+  unsigned kbits = 0xfu;
+  if (L.dense_pages) {
+    store_dense_row(L, base, b, t, is_v, raw, lane);
+  } else {
+    kbits = warp_topr(mag, r, lane, rank);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (kbits >> i & 1u) {
-      val[t * r + rank] = v[i];
-      idx[t * r + rank] = (uint8_t)(4 * lane + i);
-      ++rank;
+    for (int i = 0; i < 4; ++i) {
+      if (kbits >> i & 1u) {
+        val[t * r + rank] = v[i];
+        idx[t * r + rank] = (uint8_t)(4 * lane + i);
+        ++rank;
+      }
     }
   }
   if (update_meta) {
@@ -221,6 +236,11 @@ __device__ __forceinline__ unsigned compress_kv(const Layout& L, const UnitDesc&
     mk[i] = live ? vk[i] & 0x7fffu : 0u;
     mv[i] = live ? vv[i] & 0x7fffu : 0u;
   }
+  if (L.dense_pages) {
+    store_dense_row(L, base, b, t, 0, rawk, lane);
+    store_dense_row(L, base, b, t, 1, rawv, lane);
+    return 0xfu;
+  }
   unsigned keep_k, keep_v;
   int rank_k, rank_v;
   warp_topr2(mk, mv, r, lane, keep_k, keep_v, rank_k, rank_v);
@@ -327,6 +347,16 @@ __device__ __forceinline__ void compress_kv2(const Layout& L, const UnitDesc& ud
     vals[v][3] = (uint16_t)(raw.y >> 16);
 #pragma unroll
     for (int i = 0; i < 4; ++i) mag[v][i] = 4 * lane + i < kp[v >> 1] ? vals[v][i] & 0x7fffu : 0u;  // truncated: 0
+  }
+  if (L.dense_pages) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      store_dense_row(L, base, bb[v >> 1], tt[v >> 1], v & 1,
+                      make_uint2((uint32_t)vals[v][0] | ((uint32_t)vals[v][1] << 16),
+                                 (uint32_t)vals[v][2] | ((uint32_t)vals[v][3] << 16)),
+                      lane);
+    keep_a = keep_b = 0xfu;
+    return;
   }
   unsigned keep[4];
   int rank[4];

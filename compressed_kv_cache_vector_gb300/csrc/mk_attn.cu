@@ -161,12 +161,15 @@ __device__ __forceinline__ void scatter_kv(uint32_t tk, uint32_t tv, uint32_t kv
 
 struct Task {
   int kind;      // 0 none, 1 dense chunk, 2 packed group, 3 skipped (bad block id)
+                 // (kind 1 with b >= 0: rows j0.. of an uncompressed page, the Quest comparator)
   int item;
   int j0, nd;    // dense: first dense token and count
   int b, r, tg, n_live;
 };
 
-int stage_bytes(const Layout& L) { return (std::max(6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16; }
+int stage_bytes(const Layout& L) {
+  return (std::max(L.dense_pages ? 0 : 6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16;
+}
 // Per warp: the stages, then the key tile and the value tile.
 size_t per_warp_bytes(const Layout& L, int nst) {
   return (size_t)nst * stage_bytes(L) + 2 * kTileBytes + ((size_t)nst * 8 + 15) / 16 * 16;  // + stage barriers
@@ -367,6 +370,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
     const int it = part + j * P;
     if (it >= ns + n_always) {
       t.kind = 1;
+      t.b = -1;
       t.j0 = (it - ns - n_always) * kDC;
       t.nd = min(kDC, n_dense - t.j0);
       return t;
@@ -377,11 +381,17 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
       t.kind = 3;
       return t;
     }
-    t.kind = 2;
     t.b = b;
+    t.n_live = min(B, n_mid - b * B);
+    if (!DENSE && L.dense_pages) {  // whole rows: staged like the dense chunks
+      t.kind = 1;
+      t.j0 = tg;
+      t.nd = min(kDC, t.n_live - tg);
+      return t;
+    }
+    t.kind = 2;
     t.r = ud.r[seg_of_block(ud, b)];
     t.tg = tg;
-    t.n_live = min(B, n_mid - b * B);
     return t;
   };
   auto advance = [&](const Task& t) -> Task {
@@ -389,6 +399,12 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
     if (t.kind == 2 && t.tg + kTG < t.n_live) {
       Task n = t;
       n.tg += kTG;
+      return n;
+    }
+    if (t.kind == 1 && t.b >= 0 && t.j0 + kDC < t.n_live) {
+      Task n = t;
+      n.j0 += kDC;
+      n.nd = min(kDC, t.n_live - n.j0);
       return n;
     }
     return make_task(t.item + kWarps, 0);
@@ -422,7 +438,13 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
       if (lane < 2 * t.nd) {
         const int row = lane >> 1, isv = lane & 1;
         const uint16_t *kr, *vr;
-        dense_rows(t.j0 + row, kr, vr);
+        if (t.b >= 0) {
+          kr = reinterpret_cast<const uint16_t*>(base + L.off_pages + (int64_t)t.b * L.page_stride) +
+               (int64_t)(t.j0 + row) * D;
+          vr = kr + (int64_t)B * D;
+        } else {
+          dense_rows(t.j0 + row, kr, vr);
+        }
         bulk_g2s(dst + (isv * kDC + row) * kRow * 2, isv ? vr : kr, D * 2, &bars[sidx]);
       }
     } else if (t.kind == 2) {

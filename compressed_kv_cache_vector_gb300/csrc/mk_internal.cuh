@@ -58,6 +58,7 @@ struct Layout {
   int64_t page_stride;
   int32_t S, W, B, n_kv, G, max_seqs, nblk_cap, cap_tokens, n_layers, k_max;
   int32_t topk_fixed, retain_permille, r_max;
+  int32_t dense_pages;          // 1: uncompressed middle pages [K B x 128][V B x 128] (Quest comparator)
   int32_t attn_tg;              // attention: tokens per staged page group (32 or 16)
   int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, warps per CTA, stage bytes
   // workspace

@@ -100,7 +100,20 @@ typedef struct mk_config {
                               bound magnitude max(|min|, |max|), ties to the
                               lower channel, and the scores use those only (the
                               others count as zero). */
+  int32_t page_format;     /* MK_PAGES_PACKED (0): the method's per-vector top-r
+                              pages.  MK_PAGES_DENSE (1): the Quest comparator
+                              ([S] sec. 6.1 baselines, sec. 6.3): middle blocks
+                              keep every channel (page = [K bf16 B x 128][V bf16
+                              B x 128]) and only the token-block selection
+                              applies; every segment must then have r = 128,
+                              keep_channels 0, and meta_channels must be 0.
+                              Block min/max, scores, top-k and attention are the
+                              same calls; with an identity rotation this is
+                              Quest's page selection on the raw keys. */
 } mk_config;
+
+#define MK_PAGES_PACKED 0
+#define MK_PAGES_DENSE 1
 
 /* Byte offsets of one (layer, sequence, kv head) inside the arena, for tests
  * and tools.  Pages: block b lives at pages + b*page_stride and holds

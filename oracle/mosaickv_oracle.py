@@ -485,6 +485,50 @@ class OracleCache:
         return o @ self.Rv
 
 
+def quest_decode(q, K, V, st: Strategy, T0=None):
+    """The Quest comparator: token-block selection alone on the uncompressed cache.
+
+    Quest is the block-selection baseline the pages compare against ([S]
+    sec. 6.1 baselines, sec. 6.3 "over Quest"; [N] describes its per-block
+    min/max keys).  With the same segment layout as the method: sink tokens
+    [0, S) and the window [T-W, T) are always attended; the middle [S, T-W)
+    is cut into blocks of B tokens from S.  Each block keeps the elementwise
+    min and max of its raw keys; a block's score is
+    max over the group's heads of (1/sqrt(d)) sum_j max(q_j mn_j, q_j mx_j);
+    the k best blocks of the scored segments are kept (ties to the lower
+    block id; segments marked always are attended whole), and each head
+    attends, softmax(q K^T / sqrt(d)) V, over the raw rows of sinks, window,
+    kept and always-attended blocks.  Every channel is kept.
+    q: [G, d]; K, V: [T, d] (float64 values); T0: the length at which the
+    segment boundaries were fixed (default T).  Returns (ids, out [G, d]).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    T, d = K.shape
+    S, W, B = st.n_sink, st.window, st.block
+    mid = max(0, T - S - W)
+    nb = (mid + B - 1) // B
+    firsts = segment_first_blocks(T if T0 is None else T0, st)
+    always = [bool(st.segments[block_segment(b, firsts)][2]) for b in range(nb)]
+    scores = np.empty(nb)
+    for b in range(nb):
+        rows = K[S + b * B:S + min((b + 1) * B, mid)]
+        mn, mx = rows.min(axis=0), rows.max(axis=0)
+        scores[b] = max(sum(max(q[h, j] * mn[j], q[h, j] * mx[j]) for j in range(d))
+                        for h in range(q.shape[0])) / math.sqrt(d)
+    cand = [b for b in range(nb) if not always[b]]
+    k = n_select(len(cand), st)
+    ids = sorted(sorted(cand, key=lambda b: (-scores[b], b))[:k])
+    keep = list(range(min(S, T))) + list(range(S + mid, T))
+    for b in sorted(ids + [b for b in range(nb) if always[b]]):
+        keep += list(range(S + b * B, S + min((b + 1) * B, mid)))
+    logits = q @ K[keep].T / math.sqrt(d)
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    return np.array(ids, dtype=np.int64), p @ V[keep]
+
+
 def speedup_bound(alpha, beta):
     """[N] Eq. (15): T d / (s_sel r) = 1 / (alpha beta)."""
     return 1.0 / (alpha * beta)

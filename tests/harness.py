@@ -44,6 +44,7 @@ class Case:
     n_layers: int = 1
     oracle_units: list = None                     # [(layer, seq, kvh)]; None = all
     meta_channels: int = 0                        # > 0: channel-compressed per-block keys
+    page_format: int = 0                          # 1: uncompressed pages (the Quest comparator)
 
     @property
     def G(self):
@@ -64,7 +65,7 @@ class Pair:
         self.T_total = [t + extra for t in case.seq_lens]
         cfg = make_config(case.n_q, case.n_kv, case.n_layers, len(case.seq_lens), max(self.T_total) + 1,
                           case.n_sink, case.window, case.block, case.segments, case.topk_fixed,
-                          case.retain_permille, case.meta_channels)
+                          case.retain_permille, case.meta_channels, case.page_format)
         self.mk = MosaicKV(cfg, device)
         self.K, self.V, self.R = {}, {}, {}
         units = case.oracle_units

@@ -87,3 +87,18 @@ def test_noalloc_refuses_misaligned_pointers_before_any_launch(lib):
         st = lib.mk_dense_decode_attn_noalloc(4, 1, 1, T, ctypes.c_void_p(q), ctypes.c_void_p(k),
                                               ctypes.c_void_p(v), 64, ctypes.c_void_p(o), None)
         assert st == 1
+
+
+def test_quest_comparator_config_rules(lib):
+    # Uncompressed pages keep every channel: r = 128, no truncation, no
+    # compressed block keys; the pages are 2 x B x 128 bf16.
+    ok = _cfg(segments=[(0, 128, 0)], page_format=1)
+    a, _, _ = K.sizes(ok)
+    nblk = (131072 + 64 - 4 - 256 + 31) // 32
+    assert a > 8 * nblk * 4 * 32 * 128
+    for bad in (dict(segments=[(0, 38, 0)]), dict(segments=[(0, 128, 0)], meta_channels=16),
+                dict(segments=[(0, 128, 0, 96)]), dict(segments=[(0, 128, 0)], page_format=2)):
+        bad.setdefault("page_format", 1)
+        with pytest.raises(K.MosaicKVError) as e:
+            K.sizes(_cfg(**bad))
+        assert e.value.status == 1

@@ -500,3 +500,29 @@ def test_pins_catch_planted_mistakes():
     exact = np.array([O.block_max_exact(qr, c.Kt[slice(*c.block_tokens(b))])
                       for b in range(c.n_blocks_mid())])
     assert np.any(wrong_s < exact - 1e-9)
+
+
+# ------------------------------------------------------ Quest comparator ----
+@pytest.mark.parametrize("segments,G,topk", [([(0, 128, 0)], 4, 0), ([(0, 128, 0), (400, 128, 1)], 1, 0),
+                                            ([(0, 128, 0)], 8, 5)])
+def test_quest_equals_the_method_with_every_channel_and_no_rotation(segments, G, topk):
+    # Quest keeps every channel and does not rotate: the method's oracle with
+    # r = d and R = I computes the same block keys, scores, ids and output.
+    st = O.Strategy(4, 40, 16, segments, topk, 0 if topk else 100)
+    K = _gen(1500, 0.9, 90)
+    V = _gen(1500, 0.9, 91)
+    c = O.OracleCache(st, 1508)
+    c.set_rotation(np.eye(128), np.eye(128))
+    c.append(K[:1400], V[:1400])
+    for t in range(1400, 1500, 20):
+        c.append(K[t:t + 20], V[t:t + 20])
+    q = O.bf16_round(np.random.default_rng(92).standard_normal((G, 128)))
+    ids, out = O.quest_decode(q, K, V, st, T0=1400)
+    want_ids, _ = c.select(q)
+    assert np.array_equal(ids, want_ids)
+    assert np.allclose(out, c.attention(q, want_ids), rtol=0, atol=1e-12)
+    # and with every block kept it is dense attention, [N] Eq. (1)
+    st_all = O.Strategy(4, 40, 16, [(0, 128, 0)], 10 ** 6)
+    _, out_all = O.quest_decode(q, K, V, st_all)
+    ref = _sdpa(q, K, V)
+    assert np.allclose(out_all, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
