@@ -502,7 +502,7 @@ mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32
   CallSeqs* cs = new (std::nothrow) CallSeqs();
   if (!cs) return MK_ENOMEM;
   cs->n = n_seqs;
-  int max_items = 1;
+  int32_t items[MK_MAX_CALL_SEQS];
   for (int i = 0; i < n_seqs; ++i) {
     cs->seq[i] = seq_ids[i];
     const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq_ids[i];
@@ -512,11 +512,10 @@ mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32
     const int scored = mk::n_scored_blocks(d, nblk);
     const int dense = std::min(ctx->L.S, T) + std::max(0, T - (ctx->L.S + mk::n_mid_tokens(ctx->L, T)));
     const int groups = (ctx->L.B + mk::kDenseChunk - 1) / mk::kDenseChunk;
-    const int items = (dense + mk::kDenseChunk - 1) / mk::kDenseChunk +
-                      (mk::n_select(ctx->L, scored) + (nblk - scored)) * groups;
-    max_items = std::max(max_items, items);
+    items[i] = (dense + mk::kDenseChunk - 1) / mk::kDenseChunk +
+               (mk::n_select(ctx->L, scored) + (nblk - scored)) * groups;
   }
-  cudaError_t e = mk::launch_decode_attn(ctx->L, layer, *cs, ids, n_sel, static_cast<uint16_t*>(out), max_items,
+  cudaError_t e = mk::launch_decode_attn(ctx->L, layer, *cs, ids, n_sel, static_cast<uint16_t*>(out), items,
                                          (cudaStream_t)stream);
   delete cs;
   return cuda_status(e);
@@ -530,7 +529,7 @@ mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T, co
   CallSeqs* cs = new (std::nothrow) CallSeqs();
   if (!cs) return MK_ENOMEM;
   cs->n = n_seqs;
-  int max_items = 1;
+  int32_t items[MK_MAX_CALL_SEQS];
   for (int i = 0; i < n_seqs; ++i) {
     if (T[i] < 1 || T[i] > t_stride) {
       delete cs;
@@ -538,11 +537,11 @@ mk_status mk_dense_decode_attn(mk_ctx* ctx, int32_t n_seqs, const int32_t* T, co
     }
     cs->seq[i] = i;
     cs->T_old[i] = T[i];
-    max_items = std::max(max_items, (T[i] + mk::kDenseChunk - 1) / mk::kDenseChunk);
+    items[i] = (T[i] + mk::kDenseChunk - 1) / mk::kDenseChunk;
   }
   cudaError_t e = mk::launch_dense_attn(ctx->L, *cs, static_cast<const uint16_t*>(q),
                                         static_cast<const uint16_t*>(K), static_cast<const uint16_t*>(V), t_stride,
-                                        static_cast<uint16_t*>(out), max_items, (cudaStream_t)stream);
+                                        static_cast<uint16_t*>(out), items, (cudaStream_t)stream);
   delete cs;
   return cuda_status(e);
 }

@@ -45,6 +45,7 @@
 //    counter, no waiting) stages all partials with one bulk copy, merges
 //    them (log-sum-exp weights) and stores bf16.
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 
@@ -235,7 +236,7 @@ int attn_max_parts(const Layout& L) {
 }
 
 template <int G, bool DENSE, int MAXW>
-__global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, CallSeqs cs, int P,
+__global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, CallSeqs cs, AttnSplit split,
                                                  const int32_t* __restrict__ ids,
                                                  const int32_t* __restrict__ n_sel_in,
                                                  const uint16_t* __restrict__ q_in, const uint16_t* __restrict__ Kd,
@@ -254,9 +255,19 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
   __shared__ int32_t s_ids[kIdsCap];
   __shared__ uint64_t s_bar, s_bar2;  // R_v staging (every CTA), partials staging (the merging CTA)  // this CTA's selected block ids (its j-th item: ids[part + j P])
 
-  const int unit_call = blockIdx.x / P;
-  const int part = blockIdx.x - unit_call * P;
-  const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
+  // This CTA's sequence (the last with off <= blockIdx.x), kv head and part.
+  int ci = 0;
+  {
+    int hi = cs.n - 1;
+    const int bid = (int)blockIdx.x;
+    while (ci < hi) {
+      const int mid = (ci + hi + 1) >> 1;
+      if (split.off[mid] <= bid) ci = mid; else hi = mid - 1;
+    }
+  }
+  const int P = (split.off[ci + 1] - split.off[ci]) / L.n_kv;
+  const int local = (int)blockIdx.x - split.off[ci];
+  const int kvh = local / P, part = local - kvh * P;
   const int seq = cs.seq[ci];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tig = lane & 3;
@@ -864,53 +875,71 @@ namespace {
 template <int G, bool DENSE, int MAXW>
 cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                        const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
-                       int max_items, size_t smem, cudaStream_t s) {
+                       const int32_t* items, size_t smem, cudaStream_t s) {
   int occ = 1, sms = 0;
   cudaError_t e = kernel_smem_attr((const void*)k_attn<G, DENSE, MAXW>, (int)smem, L.attn_nc * 32, &occ, &sms);
   if (e != cudaSuccess) return e;
+  // CTAs per (sequence, kv head) in proportion to its items: one wave of
+  // CTAs when the units fit on the SMs; with more units than CTA slots (many
+  // sequences), about four CTAs' worth of work per slot, so long sequences
+  // split and the SMs finish together.
+  const int slots = std::max(1, std::max(sms, 1) * occ);
   const int units = cs.n * L.n_kv;
-  int P = std::max(1, (std::max(sms, 1) * occ) / units);
-  P = std::min(P, std::max(1, max_items / 2));
-  P = std::min(P, attn_max_parts(L));
+  int64_t work = 0;
+  for (int i = 0; i < cs.n; ++i) work += (int64_t)std::max(1, items[i]) * L.n_kv;
+  const double per_cta = (double)work / ((double)slots * (units > slots ? 4 : 1));
+  const int cap = attn_max_parts(L);
+  AttnSplit split;
+  split.off[0] = 0;
+  int p_min = 1 << 30, p_max = 0;
+  for (int i = 0; i < cs.n; ++i) {
+    const int it = std::max(1, items[i]);
+    int P = (int)std::floor((double)it / per_cta);
+    P = std::max(1, std::min(P, std::min(cap, std::max(1, it / 2))));
+    p_min = std::min(p_min, P);
+    p_max = std::max(p_max, P);
+    split.off[i + 1] = split.off[i] + P * L.n_kv;
+  }
   if (std::getenv("MK_LOG"))
-    std::fprintf(stderr, "[mosaickv] attention: %d units x %d CTAs (%d per SM), %zu B smem\n", units, P, occ, smem);
-  return launch_pdl(k_attn<G, DENSE, MAXW>, dim3(units * P), dim3(L.attn_nc * 32), smem, s, 0, L, layer, cs, P, ids, n_sel, q, K, V,
-                    t_stride, out);
+    std::fprintf(stderr, "[mosaickv] attention: %d units, %d to %d CTAs each, %d CTAs (%d per SM), %zu B smem\n",
+                 units, p_min, p_max, split.off[cs.n], occ, smem);
+  return launch_pdl(k_attn<G, DENSE, MAXW>, dim3(split.off[cs.n]), dim3(L.attn_nc * 32), smem, s, 0, L, layer, cs,
+                    split, ids, n_sel, q, K, V, t_stride, out);
 }
 
 template <bool DENSE>
 cudaError_t launch_attn_g(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                           const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
-                          int max_items, cudaStream_t s) {
+                          const int32_t* items, cudaStream_t s) {
   const size_t smem = attn_smem_bytes(L, 0);
   if (smem == 0 || smem > 227 * 1024) return cudaErrorInvalidConfiguration;
   const bool wide = L.attn_nc > 12;  // launch bounds of 16 warps (at most 128 registers)
   switch (L.G) {
     case 1:
-      return wide ? launch_one<1, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s)
-                  : launch_one<1, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+      return wide ? launch_one<1, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s)
+                  : launch_one<1, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s);
     case 2:
-      return wide ? launch_one<2, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s)
-                  : launch_one<2, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+      return wide ? launch_one<2, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s)
+                  : launch_one<2, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s);
     case 4:
-      return wide ? launch_one<4, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s)
-                  : launch_one<4, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+      return wide ? launch_one<4, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s)
+                  : launch_one<4, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s);
     case 8:
-      return wide ? launch_one<8, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s)
-                  : launch_one<8, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, max_items, smem, s);
+      return wide ? launch_one<8, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s)
+                  : launch_one<8, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }
 }  // namespace
 
 cudaError_t launch_decode_attn(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids,
-                               const int32_t* n_sel, uint16_t* out, int max_items, cudaStream_t s) {
-  return launch_attn_g<false>(L, layer, cs, ids, n_sel, nullptr, nullptr, nullptr, 0, out, max_items, s);
+                               const int32_t* n_sel, uint16_t* out, const int32_t* items, cudaStream_t s) {
+  return launch_attn_g<false>(L, layer, cs, ids, n_sel, nullptr, nullptr, nullptr, 0, out, items, s);
 }
 
 cudaError_t launch_dense_attn(const Layout& L, const CallSeqs& cs, const uint16_t* q, const uint16_t* K,
-                              const uint16_t* V, int64_t t_stride, uint16_t* out, int max_items, cudaStream_t s) {
-  return launch_attn_g<true>(L, 0, cs, nullptr, nullptr, q, K, V, t_stride, out, max_items, s);
+                              const uint16_t* V, int64_t t_stride, uint16_t* out, const int32_t* items, cudaStream_t s) {
+  return launch_attn_g<true>(L, 0, cs, nullptr, nullptr, q, K, V, t_stride, out, items, s);
 }
 
 }  // namespace mk

@@ -363,13 +363,20 @@ cudaError_t launch_topk(const Layout& L, int layer, const CallSeqs& cs, int32_t*
 cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,
                                 int32_t* ids, int32_t* n_sel, float* scores_out, int max_nblk,
                                 cudaStream_t s, const uint16_t* kin = nullptr, const uint16_t* vin = nullptr);
-// max_items: the largest number of attention work items (16-token dense
-// chunks + selected/always pages) of any (sequence, kv head) in the call.
+// items[i]: the attention work of each (sequence i, kv head) of the call, in
+// items of up to kDenseChunk tokens (dense chunks, page groups), host array.
+// A sequence gets CTAs per kv head in proportion to its items.
 cudaError_t launch_decode_attn(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids,
-                               const int32_t* n_sel, uint16_t* out, int max_items, cudaStream_t s);
+                               const int32_t* n_sel, uint16_t* out, const int32_t* items, cudaStream_t s);
 cudaError_t launch_dense_attn(const Layout& L, const CallSeqs& cs, const uint16_t* q,
                               const uint16_t* K, const uint16_t* V, int64_t t_stride,
-                              uint16_t* out, int max_items, cudaStream_t s);
+                              uint16_t* out, const int32_t* items, cudaStream_t s);
+
+// Attention CTAs of a call: sequence i (call order) owns CTAs off[i] ..
+// off[i + 1] - 1, n_kv x P_i of them (kv head major, then part).
+struct AttnSplit {
+  int32_t off[MK_MAX_CALL_SEQS + 1];
+};
 size_t attn_plan(Layout& L, int r_min);
 cudaError_t launch_gram(const uint16_t* x, int64_t n_rows, int64_t row_stride, float* gram,
                         cudaStream_t s);

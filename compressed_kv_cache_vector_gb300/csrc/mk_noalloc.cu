@@ -53,10 +53,10 @@ extern "C" mk_status mk_dense_decode_attn_noalloc(int32_t n_q_heads, int32_t n_k
   const int G = n_q_heads / n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return MK_EINVAL;
   if (n_seqs < 1 || n_seqs > MK_MAX_CALL_SEQS || t_stride < 1) return MK_EINVAL;
-  int max_items = 1;
+  int32_t items[MK_MAX_CALL_SEQS];
   for (int i = 0; i < n_seqs; ++i) {
     if (T[i] < 1 || T[i] > t_stride) return MK_EINVAL;
-    max_items = std::max(max_items, (T[i] + mk::kDenseChunk - 1) / mk::kDenseChunk);
+    items[i] = (T[i] + mk::kDenseChunk - 1) / mk::kDenseChunk;
   }
   // Size limit: n_seqs * n_q_heads <= MK_NOALLOC_MAX_QUERY_HEADS.
   if ((int64_t)n_seqs * n_q_heads > MK_NOALLOC_MAX_QUERY_HEADS) return MK_ENOMEM;
@@ -100,7 +100,7 @@ extern "C" mk_status mk_dense_decode_attn_noalloc(int32_t n_q_heads, int32_t n_k
   cudaError_t e = cudaMemsetAsync(scratch + off_cnt, 0, (size_t)(off_acc - off_cnt), s);
   if (e == cudaSuccess)
     e = mk::launch_dense_attn(L, cs, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(K),
-                              static_cast<const uint16_t*>(V), t_stride, static_cast<uint16_t*>(out), max_items, s);
+                              static_cast<const uint16_t*>(V), t_stride, static_cast<uint16_t*>(out), items, s);
   return e == cudaSuccess ? MK_OK : MK_ECUDA;
 }
 
