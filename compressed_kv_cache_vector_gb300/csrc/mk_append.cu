@@ -71,138 +71,192 @@ __global__ void __launch_bounds__(256) k_append_small(Layout L, int layer, CallS
 }
 
 // Bulk append of new tokens (prefill): tiles of up to 128 positions aligned so
-// that every middle block sits in one tile, one CTA per (tile, kv head).
-// The rotation of the tile is a dense GEMM on the 5th-generation tensor
-// cores: D[128 tok x 128 ch] = X[128 x 128] R^T with X the tile's bf16 keys
-// (values) and R split exactly into three bf16 parts (pre-split in the unit
-// at mk_set_rotation), 24 tcgen05.mma (3 parts x 8 k-steps of 16) per
-// tensor accumulating in fp32 in tensor memory.  Every product is exact and
-// the sum is fp32, as in the per-token path.  The epilogue rounds the
-// accumulators to bf16 rows in shared memory, where one warp per token does
-// the top-r selection and packing, and the block min/max follow.
+// that every middle block sits in one tile.  A work item is one tensor (keys
+// or values) of one tile of one kv head; the kernel is persistent: each CTA
+// takes a contiguous run of items ordered by (tensor, kv head, tile), so it
+// loads that head's rotation once and streams its tiles.
+//  * The rotation of a tile is a dense GEMM on the 5th-generation tensor
+//    cores: D[128 tok x 128 ch] = X[128 x 128] R^T with X the tile's bf16 rows
+//    and R split exactly into three bf16 parts (pre-split in the unit at
+//    mk_set_rotation, one 96 KB bulk copy), 24 tcgen05.mma (3 parts x 8
+//    k-steps of 16) accumulating in fp32 in tensor memory.  Every product is
+//    exact and the sum is fp32, as in the per-token path.
+//  * Pipeline: the next item's rows arrive by 16-byte cp.async copies into
+//    the other operand buffer while the current item is compressed; its MMAs
+//    are issued as soon as the current accumulators have been read out.
+//  * The epilogue rounds the accumulators to bf16 rows in shared memory.
+//    Each token is then compressed by a pair of threads (64 channels each)
+//    without warp-wide reductions: the r-th largest magnitude is found
+//    bitwise from the top, every step counting the 64 magnitudes >= the
+//    candidate two at a time in 32-bit words (guard-bit subtraction), and the
+//    pair adding its two counts with one shuffle.  So 16 tokens proceed
+//    independently in each warp.  Key items then fold the block min/max.
 namespace {
 constexpr int kRotRow = D + 8;                                  // padded bf16 row of the rotated tile
 constexpr int kBulkXBytes = kTileTokens * D * 2;                // 32 KB tensor-core A tile
 constexpr int kBulkRBytes = 3 * D * D * 2;                      // 96 KB: the three parts of R
-constexpr int kBulkRotBytes = 2 * kTileTokens * kRotRow * 2;    // rotated K and V rows
-constexpr int kBulkSmem = kBulkXBytes + kBulkRBytes + kBulkRotBytes + kTileTokens * 32;
+constexpr int kBulkRotBytes = kTileTokens * kRotRow * 2;        // one tensor's rotated rows
+constexpr int kBulkKeepBytes = kTileTokens * 16;                // keep bits of the key rows
+constexpr int kBulkMetaBytes = (kTileTokens / 16) * 2 * D * 2;  // block min/max rows for the compressed keys
+constexpr int kStageR = 68;                                     // packed rows staged for r <= 68
+constexpr int kBulkStageBytes = kTileTokens * kStageR * 3;      // values (bf16) then indices (u8)
+constexpr int kBulkSmem =
+    kBulkRBytes + 2 * kBulkXBytes + kBulkRotBytes + kBulkKeepBytes + kBulkMetaBytes + kBulkStageBytes;
+static_assert(kBulkSmem + 1024 <= 227 * 1024, "bulk append shared memory");
 constexpr uint32_t kBulkIdesc = umma_idesc_bf16(128, 128);
+
+// One work item: tensor (0 keys, 1 values), kv head, call sequence, and the
+// tile's positions [lo, hi) with its first input row.
+struct BulkItem {
+  int w, kvh, ci, lo, hi;
+  int64_t row0;
+};
+__device__ __forceinline__ BulkItem bulk_item(const Layout& L, const CallSeqs& cs, int total_tiles, int it) {
+  BulkItem b;
+  const int per_w = L.n_kv * total_tiles;
+  b.w = it / per_w;
+  const int rem = it - b.w * per_w;
+  b.kvh = rem / total_tiles;
+  const int tile = rem - b.kvh * total_tiles;
+  int lo = 0, hi = cs.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cs.tile_off[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  b.ci = lo;
+  const int T_old = cs.T_old[lo], T_new = T_old + cs.n_new[lo];
+  const int j = tile - cs.tile_off[lo];
+  const int f = tile_first_boundary(T_old, L.S);
+  b.lo = j == 0 ? T_old : f + (j - 1) * kTileTokens;
+  b.hi = min(T_new, j == 0 ? f : b.lo + kTileTokens);
+  b.row0 = cs.row_off[lo] + (b.lo - T_old);
+  return b;
+}
 }  // namespace
 
-__global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSeqs cs,
+__global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, CallSeqs cs,
                                                      const uint16_t* __restrict__ kin,
-                                                     const uint16_t* __restrict__ vin) {
+                                                     const uint16_t* __restrict__ vin, int total_tiles,
+                                                     int items_per_cta) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* Xs = smem;                                     // A: tile rows, K-major core matrices
-  unsigned char* Rp = smem + kBulkXBytes;                       // B: three parts of R
-  uint16_t* rot = reinterpret_cast<uint16_t*>(Rp + kBulkRBytes);  // [2][128][kRotRow]
-  uint8_t* keepk = reinterpret_cast<uint8_t*>(rot + 2 * kTileTokens * kRotRow);  // [128][32] nibbles
-  __shared__ UnitDesc ud;
-  __shared__ int s_ci, s_abort, s_fail;
+  unsigned char* Rp = smem;                                                  // B: three parts of R
+  unsigned char* Xb = smem + kBulkRBytes;                                    // A: two tile buffers
+  uint16_t* rot = reinterpret_cast<uint16_t*>(Xb + 2 * kBulkXBytes);        // [128][kRotRow]
+  uint32_t* keepw = reinterpret_cast<uint32_t*>(rot + kTileTokens * kRotRow);  // [128][4] keep bits
+  uint16_t* bm = reinterpret_cast<uint16_t*>(keepw) + kBulkKeepBytes / 2;         // [8][2][128]
+  uint16_t* stv = bm + kBulkMetaBytes / 2;                                        // [128][kStageR] packed values
+  uint8_t* sti = reinterpret_cast<uint8_t*>(stv + kTileTokens * kStageR);         // [128][kStageR] packed indices
+  __shared__ __align__(16) UnitDesc ud;
+  __shared__ int s_abort;
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t bar_copy, bar_mma;
+  __shared__ __align__(8) uint64_t bar_r, bar_mma;
 
-  const int tile = blockIdx.x, kvh = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_items = 2 * L.n_kv * total_tiles;
+  const int it0 = blockIdx.x * items_per_cta;
+  const int it1 = min(n_items, it0 + items_per_cta);
+  if (it0 >= it1) return;  // whole CTA, before any barrier
   if (tid == 0) {
-    int lo = 0, hi = cs.n - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (cs.tile_off[mid] <= tile) lo = mid; else hi = mid - 1;
-    }
-    s_ci = lo;
     s_abort = has_error(L);
-    s_fail = 0;
-    ud = L.desc[unit_index(L, layer, cs.seq[lo], kvh)];
-    mbar_init(&bar_copy, 1);
+    mbar_init(&bar_r, 1);
     mbar_init(&bar_mma, 1);
     mbar_init_fence();
   }
-  __syncthreads();
-  if (s_abort) return;
-  const int ci = s_ci;
-  const int seq = cs.seq[ci];
-  const int64_t u = unit_index(L, layer, seq, kvh);
-  const int T_old = cs.T_old[ci], T_new = T_old + cs.n_new[ci];
-  const int S = L.S, W = L.W, B = L.B;
-  const int j = tile - cs.tile_off[ci];
-  const int f = tile_first_boundary(T_old, S);
-  const int lo = j == 0 ? T_old : f + (j - 1) * kTileTokens;
-  const int hi = min(T_new, j == 0 ? f : lo + kTileTokens);
-  const int nt = hi - lo;
-  if (nt <= 0) return;
-  char* base = unit_base(L, u);
-  const int64_t in_stride = (int64_t)L.n_kv * D;
-  const int64_t row0 = cs.row_off[ci] + (lo - T_old);
-
-  if (warp == 0) tmem_alloc(&s_tmem, 256);  // K accumulators in columns 0-127, V in 128-255
+  if (warp == 0) tmem_alloc(&s_tmem, 128);
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
   const uint32_t tmem = s_tmem;
+  const int S = L.S, W = L.W, B = L.B;
+  const int64_t in_stride = (int64_t)L.n_kv * D;
 
-  for (int w = 0; w < 2; ++w) {
-    // R parts: one bulk copy (contiguous, already in operand layout).
-    if (tid == 0) {
-      fence_proxy_async();
-      mbar_expect_tx(&bar_copy, kBulkRBytes);
-      bulk_g2s(Rp, base + (w == 0 ? L.off_rkp : L.off_rvp), kBulkRBytes, &bar_copy);
-    }
-    // X: the tile's rows, 16 bytes (8 channels) per load, into core matrices;
-    // rows past the tile's tokens are zero.
-    const uint16_t* src = (w == 0 ? kin : vin) + (int64_t)kvh * D;
+  // The tile's rows of item b into operand buffer xb by 16-byte cp.async,
+  // in the tensor cores' K-major core-matrix layout; rows past its tokens zero.
+  auto load_x = [&](const BulkItem& b, unsigned char* xb) {
+    const uint16_t* src = (b.w == 0 ? kin : vin) + (int64_t)b.kvh * D;
+    const int nt = b.hi - b.lo;
     for (int i = tid; i < kTileTokens * (D / 8); i += blockDim.x) {
       const int t = i >> 4, c8 = i & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < nt) v = *reinterpret_cast<const uint4*>(src + (row0 + t) * in_stride + c8 * 8);
-      *reinterpret_cast<uint4*>(Xs + umma_kmajor_offset(t, c8 * 8)) = v;
+      unsigned char* dst = xb + umma_kmajor_offset(t, c8 * 8);
+      if (t < nt)
+        cp_async16(dst, src + (b.row0 + t) * in_stride + c8 * 8);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
-    fence_proxy_async();
-    __syncthreads();
-    if (!mbar_wait(&bar_copy, (unsigned)w)) {
-      if (tid == 0) s_fail = 1;
+    cp_async_commit();
+  };
+  // R parts of item b's tensor and head into Rp (no MMA may be reading Rp).
+  unsigned r_phase = 0, mma_phase = 0;
+  bool r_pending = false, mma_pending = false;
+  auto r_key = [&](const BulkItem& b) { return (b.w * MK_MAX_CALL_SEQS + b.ci) * L.n_kv + b.kvh; };
+  auto load_r = [&](const BulkItem& b) -> bool {
+    if (tid == 0) {
+      const char* ub = unit_base(L, unit_index(L, layer, cs.seq[b.ci], b.kvh));
+      fence_proxy_async();
+      mbar_expect_tx(&bar_r, kBulkRBytes);
+      bulk_g2s(Rp, ub + (b.w == 0 ? L.off_rkp : L.off_rvp), kBulkRBytes, &bar_r);
     }
-    __syncthreads();
-    if (s_fail) break;
+    r_pending = true;
+    const bool ok = __syncthreads_and(mbar_wait(&bar_r, r_phase) ? 1 : 0) != 0;
+    if (ok) {
+      r_phase ^= 1u;
+      r_pending = false;
+    }
+    return ok;
+  };
+  // 24 MMAs of one tile (tid 0), committed to bar_mma.
+  auto issue_mma = [&](const unsigned char* xb) {
     if (tid == 0) {
       tmem_fence_after_sync();
       for (int p = 0; p < 3; ++p)
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_bf16(tmem + (uint32_t)(w * 128), umma_desc(Xs + kk * 256, 128, 2048),
-                    umma_desc(Rp + p * D * D * 2 + kk * 256, 128, 2048), kBulkIdesc, p > 0 || kk > 0);
+          umma_bf16(tmem, umma_desc(xb + kk * 256, 128, 2048), umma_desc(Rp + p * D * D * 2 + kk * 256, 128, 2048),
+                    kBulkIdesc, p > 0 || kk > 0);
       umma_commit(&bar_mma);
     }
-    // The next tensor's X and R overwrite the operands: wait for the MMAs.
-    if (!mbar_wait(&bar_mma, (unsigned)w)) {
-      if (tid == 0) s_fail = 1;
-    }
-    tmem_fence_after_sync();
-    __syncthreads();
-    if (s_fail) break;
-  }
-  if (s_fail) {
-    // A copy or the MMAs did not complete in time: report it, give the
-    // hardware another bounded wait, free the tensor memory and stop.
-    if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -3, (int32_t)MK_ETIMEOUT);
-    (void)mbar_wait(&bar_copy, 0);
-    (void)mbar_wait(&bar_mma, 0);
-    tmem_fence_before_sync();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
-    return;
-  }
+    mma_pending = true;
+  };
 
-  // Epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (tokens), columns of
-  // half w / 4, rounds to bf16 and stores the rows.
-  {
-    const int q = warp & 3, h = warp >> 2;
-    const int t = 32 * q + lane;
-    for (int w = 0; w < 2; ++w)
+  const bool aborted = s_abort != 0;  // an earlier kernel set the error word: do nothing
+  bool ok = !aborted;
+  BulkItem cur = bulk_item(L, cs, total_tiles, it0), nxt = cur;
+  int rk = -1, xbuf = 0;
+  if (ok) {
+    load_x(cur, Xb);
+    ok = load_r(cur);
+    rk = r_key(cur);
+  }
+  if (ok) {
+    cp_async_wait_all();
+    fence_proxy_async();  // rows written by this thread, read by the tensor cores
+    __syncthreads();
+    issue_mma(Xb);
+    if (it0 + 1 < it1) {
+      nxt = bulk_item(L, cs, total_tiles, it0 + 1);
+      load_x(nxt, Xb + kBulkXBytes);
+    }
+  }
+  for (int it = it0; ok && it < it1; ++it) {
+    const bool have_next = it + 1 < it1;
+    // Accumulators of `cur` are complete.
+    ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase) ? 1 : 0) != 0;
+    if (!ok) break;
+    mma_phase ^= 1u;
+    mma_pending = false;
+    tmem_fence_after_sync();
+    const int seq = cs.seq[cur.ci];
+    const int64_t u = unit_index(L, layer, seq, cur.kvh);
+    if (tid == 0) ud = L.desc[u];
+    // Epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (tokens), columns
+    // of half w / 4, rounds to bf16 and stores the rows.
+    {
+      const int q = warp & 3, h = warp >> 2;
+      const int t = 32 * q + lane;
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         const int col = h * 64 + c * 32;
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(w * 128 + col), v);
-        uint4* dst = reinterpret_cast<uint4*>(rot + ((size_t)w * kTileTokens + t) * kRotRow + col);
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+        uint4* dst = reinterpret_cast<uint4*>(rot + (size_t)t * kRotRow + col);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t pk[4];
@@ -213,92 +267,288 @@ __global__ void __launch_bounds__(256) k_append_bulk(Layout L, int layer, CallSe
           dst[g] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
+    }
+    tmem_fence_before_sync();
+    cp_async_wait_all();  // the next item's rows
+    fence_proxy_async();
+    __syncthreads();      // rows of `cur` complete; TMEM read out; next rows visible
+    if (have_next) {
+      if (r_key(nxt) != rk) {  // another tensor, head or sequence: its rotation (the last MMA is done)
+        ok = load_r(nxt);
+        rk = r_key(nxt);
+        if (!ok) break;
+      }
+      issue_mma(Xb + (xbuf ^ 1) * kBulkXBytes);
+    }
+    BulkItem nn = nxt;
+    if (it + 2 < it1) {  // the item after next, into the buffer `cur` used (its MMAs are done)
+      nn = bulk_item(L, cs, total_tiles, it + 2);
+      load_x(nn, Xb + xbuf * kBulkXBytes);
+    }
+
+    // Compress `cur`: the thread pair (2t, 2t + 1) takes token t, each
+    // thread 64 channels (h = tid & 1: channels 64h .. 64h + 63).
+    char* base = unit_base(L, u);
+    const int T_new = cs.T_old[cur.ci] + cs.n_new[cur.ci];
+    const int nt = cur.hi - cur.lo, lo = cur.lo, is_v = cur.w;
+    const int mlo = max(lo, S), mhi = min(cur.hi, T_new - W);  // this tile's middle tokens
+    const int b0 = (mlo - S) / B, b1 = mlo < mhi ? (mhi - 1 - S) / B : b0 - 1;
+    {
+      const int t = tid >> 1, h = tid & 1;
+      const int p = lo + t;
+      const bool in = t < nt;
+      const bool live = in && p >= S && p < T_new - W;
+      const uint16_t* row = rot + (size_t)t * kRotRow + 64 * h;
+      const uint4* row4 = reinterpret_cast<const uint4*>(row);
+      if (in && !live) {  // sink or window: the rotated row, dense
+        uint16_t* d = reinterpret_cast<uint16_t*>(base + (is_v ? L.off_sink_v : L.off_sink_k));
+        if (p >= S) d = reinterpret_cast<uint16_t*>(base + (is_v ? L.off_win_v : L.off_win_k)) + (int64_t)((p - S) % W) * D;
+        else d += (int64_t)p * D;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) reinterpret_cast<uint4*>(d + 64 * h)[j] = row4[j];
+      }
+      const int m = live ? p - S : 0;
+      const int b = m / B, tt = m - b * B;
+      const int sg = seg_of_block(ud, b);
+      const int r = live ? ud.r[sg] : 0, kp = seg_keep(ud, sg);
+      uint32_t keep_lo = 0u, keep_hi = 0u;  // keep bits of channels 64h + 0..31 and 64h + 32..63
+      if (L.dense_pages) {
+        if (live) {
+          uint4* d = reinterpret_cast<uint4*>(base + L.off_pages + (int64_t)b * L.page_stride +
+                                              ((int64_t)(is_v * B + tt) * D + 64 * h) * 2);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) d[j] = row4[j];
+          keep_lo = keep_hi = ~0u;
+        }
+      } else {
+        keep_lo = 0u;
+        // 15-bit magnitudes, two per word, each under a guard bit: for a
+        // candidate c, bit 15 (31) of (word - c | c << 16) is set exactly
+        // when the low (high) magnitude is >= c.  Truncated channels count 0.
+        uint32_t kw[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 x = live ? row4[j] : make_uint4(0, 0, 0, 0);
+          const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c0 = 64 * h + 8 * j + 2 * e;
+            uint32_t w = xs[e] & 0x7fff7fffu;
+            if (c0 >= kp) w &= 0xffff0000u;
+            if (c0 + 1 >= kp) w &= 0x0000ffffu;
+            kw[4 * j + e] = w | 0x80008000u;
+          }
+        }
+        // The r-th largest magnitude thr: the largest value with at least r
+        // magnitudes >= it (bitwise from the top; the pair adds its counts).
+        uint32_t thr = 0u;
+#pragma unroll 1
+        for (int bit = 14; bit >= 0; --bit) {
+          const uint32_t cand = thr | (1u << bit);
+          const uint32_t cc = cand | (cand << 16);
+          uint32_t acc = 0u;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc += ((kw[j] - cc) >> 15) & 0x00010001u;
+          uint32_t n = (acc & 0xffffu) + (acc >> 16);
+          n += __shfl_xor_sync(FULL, n, 1);
+          if ((int)n >= r) thr = cand;
+        }
+        // Above thr: kept.  Equal to thr: the lowest channels, as many as the
+        // r - #above still needed (the lower half's ties come first).
+        uint64_t gt = 0ull, eq = 0ull;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t lo16 = kw[j] & 0x7fffu, hi16 = (kw[j] >> 16) & 0x7fffu;
+          gt |= (uint64_t)(lo16 > thr) << (2 * j) | (uint64_t)(hi16 > thr) << (2 * j + 1);
+          eq |= (uint64_t)(lo16 == thr) << (2 * j) | (uint64_t)(hi16 == thr) << (2 * j + 1);
+        }
+        const int n_gt = __popcll(gt), n_eq = __popcll(eq);
+        const int pair_gt = n_gt + __shfl_xor_sync(FULL, n_gt, 1);
+        const int eq_lower = __shfl_xor_sync(FULL, n_eq, 1);
+        const int need = r - pair_gt - (h ? eq_lower : 0);
+        int take = need < 0 ? 0 : (need > n_eq ? n_eq : need);
+        while (__popcll(eq) > take) eq &= ~(1ull << (63 - __clzll(eq)));  // keep the lowest channels
+        uint64_t keep = gt | eq;
+        if (!live) keep = 0ull;
+        keep_lo = (uint32_t)keep;
+        keep_hi = (uint32_t)(keep >> 32);
+        // Packed row, in channel order: thread 0 of the pair writes ranks
+        // 0 .. r2 - 1 from the lowest channel up, thread 1 ranks r - 1 down to
+        // r2 from the highest, so both do the same work.  Staged rows (r <=
+        // kStageR) go to the block's run in shared memory, [tt][r], written
+        // out below; else straight into the page.
+        const uint32_t o_lo = __shfl_xor_sync(FULL, keep_lo, 1), o_hi = __shfl_xor_sync(FULL, keep_hi, 1);
+        if (live) {
+          const uint64_t mine = (uint64_t)keep_lo | ((uint64_t)keep_hi << 32);
+          const uint64_t other = (uint64_t)o_lo | ((uint64_t)o_hi << 32);
+          const uint64_t m0 = h ? other : mine, m1 = h ? mine : other;  // channels 0-63, 64-127
+          const bool staged = r <= kStageR;
+          char* page = base + L.off_pages + (int64_t)b * L.page_stride;
+          const int Br = B * r;
+          uint16_t* val = staged ? stv + (b - b0) * B * kStageR + tt * r
+                                 : reinterpret_cast<uint16_t*>(page + (is_v ? 3 * Br : 0)) + tt * r;
+          uint8_t* idx = staged ? sti + (b - b0) * B * kStageR + tt * r
+                                : reinterpret_cast<uint8_t*>(page + (is_v ? 5 * Br : 2 * Br)) + tt * r;
+          const uint16_t* rowf = rot + (size_t)t * kRotRow;
+          const int r2 = (r + 1) >> 1;
+          if (h == 0) {
+            uint64_t mm = m0;
+            int cb = 0;
+            for (int k = 0; k < r2; ++k) {
+              if (mm == 0ull) {
+                mm = m1;
+                cb = 64;
+              }
+              const int c = cb + __ffsll((long long)mm) - 1;
+              mm &= mm - 1ull;
+              val[k] = rowf[c];
+              idx[k] = (uint8_t)c;
+            }
+          } else {
+            uint64_t mm = m1;
+            int cb = 64;
+            for (int k = r - 1; k >= r2; --k) {
+              if (mm == 0ull) {
+                mm = m0;
+                cb = 0;
+              }
+              const int bit = 63 - __clzll((long long)mm);
+              mm &= ~(1ull << bit);
+              val[k] = rowf[cb + bit];
+              idx[k] = (uint8_t)(cb + bit);
+            }
+          }
+        }
+      }
+      if (!is_v && in) {
+        keepw[t * 4 + 2 * h] = keep_lo;
+        keepw[t * 4 + 2 * h + 1] = keep_hi;
+      }
+    }
+    // Write the staged packed rows out, block by block: a block's new tokens
+    // [st, en) own one contiguous run of values (and of indices) in the page
+    // and in the staging area.  Whole blocks go out by bulk copies (16-byte
+    // aligned runs of B r values and B r indices); partial ones by
+    // consecutive threads.
+    fence_proxy_async();  // the staged rows are read by the bulk copies
+    __syncthreads();
+    if (!L.dense_pages)
+      for (int b = b0; b <= b1; ++b) {
+        const int r = ud.r[seg_of_block(ud, b)];
+        if (r > kStageR) continue;  // written directly above
+        const int blo = S + b * B;
+        const int st = max(blo, mlo), en = min(blo + B, mhi);
+        char* page = base + L.off_pages + (int64_t)b * L.page_stride;
+        const int Br = B * r;
+        uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? 3 * Br : 0)) + (st - blo) * r;
+        uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? 5 * Br : 2 * Br)) + (st - blo) * r;
+        const uint16_t* sv = stv + (b - b0) * B * kStageR + (st - blo) * r;
+        const uint8_t* si = sti + (b - b0) * B * kStageR + (st - blo) * r;
+        const int n = (en - st) * r;
+        if (st == blo && en == blo + B) {
+          if (tid == 0) {
+            bulk_s2g(val, sv, (unsigned)(2 * Br));
+            bulk_s2g(idx, si, (unsigned)Br);
+          }
+        } else {
+          for (int i = tid; i < n; i += blockDim.x) {
+            val[i] = sv[i];
+            idx[i] = si[i];
+          }
+        }
+      }
+    if (tid == 0) {
+      bulk_commit();
+      bulk_wait_read();  // the staging area is reused next (block min/max, next item)
+    }
+    __syncthreads();
+    if (!is_v) {
+      // Block min/max over the zero-filled compressed keys of this tile's middle tokens.
+      // Two threads per channel, each over half of a block's new tokens
+      // (four independent running min/max); the halves meet in the staging
+      // area, free once the packed rows are out.
+      float* pm = reinterpret_cast<float*>(stv);  // [block][half][min | max][128]
+      {
+        const int c = tid & (D - 1), hf = tid >> 7;
+        const uint32_t cbit = 1u << (c & 31);
+        for (int b = b0; b <= b1; ++b) {
+          const int blo = S + b * B;
+          const int st = max(blo, mlo), en = min(blo + B, mhi);
+          const int md = st + (en - st + 1) / 2;
+          const int a0 = hf ? md : st, a1 = hf ? en : md;
+          float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          int q = a0;
+          for (; q + 3 < a1; q += 4)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int t = q + e - lo;
+              const float kt = (keepw[t * 4 + (c >> 5)] & cbit) ? bf2f(rot[(size_t)t * kRotRow + c]) : 0.0f;
+              mn[e] = fminf(mn[e], kt);
+              mx[e] = fmaxf(mx[e], kt);
+            }
+          for (; q < a1; ++q) {
+            const int t = q - lo;
+            const float kt = (keepw[t * 4 + (c >> 5)] & cbit) ? bf2f(rot[(size_t)t * kRotRow + c]) : 0.0f;
+            mn[0] = fminf(mn[0], kt);
+            mx[0] = fmaxf(mx[0], kt);
+          }
+          float* dst = pm + ((b - b0) * 2 + hf) * 2 * D;
+          dst[c] = fminf(fminf(mn[0], mn[1]), fminf(mn[2], mn[3]));
+          dst[D + c] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        }
+      }
+      __syncthreads();
+      if (tid < D) {
+        const int c = tid;
+        uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta);
+        for (int b = b0; b <= b1; ++b) {
+          const int blo = S + b * B;
+          const float* h0 = pm + (b - b0) * 4 * D;
+          float mn = fminf(h0[c], h0[2 * D + c]), mx = fmaxf(h0[D + c], h0[3 * D + c]);
+          if (max(blo, mlo) > blo) {  // the block held tokens before this tile
+            mn = fminf(mn, bf2f(meta[(int64_t)b * 2 * D + c]));
+            mx = fmaxf(mx, bf2f(meta[(int64_t)b * 2 * D + D + c]));
+          }
+          meta[(int64_t)b * 2 * D + c] = f2bf(mn);
+          meta[(int64_t)b * 2 * D + D + c] = f2bf(mx);
+          if (L.meta_c > 0) {  // the rows for the compressed keys
+            uint16_t* row = bm + (b - b0) * 2 * D;
+            row[c] = f2bf(mn);
+            row[D + c] = f2bf(mx);
+          }
+        }
+      }
+      if (L.meta_c > 0 && mlo < mhi) {
+        __syncthreads();
+        for (int b = b0 + warp; b <= b1; b += 8) {
+          const uint16_t* row = bm + (b - b0) * 2 * D;
+          uint16_t mn[4], mx[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            mn[i] = row[4 * lane + i];
+            mx[i] = row[D + 4 * lane + i];
+          }
+          compress_key_row(L, base, b, mn, mx, lane);
+        }
+      }
+    }
+    __syncthreads();  // rot, keepw and ud are free for the next item
+    cur = nxt;
+    nxt = nn;
+    xbuf ^= 1;
   }
+  if (!ok && !aborted) {
+    // A copy or the MMAs did not complete in time: report it, give the
+    // hardware another bounded wait, then free the tensor memory.
+    if (tid == 0) set_error(L, ERR_COPY_WAIT, -1, -3, (int32_t)MK_ETIMEOUT);
+    if (mma_pending) (void)mbar_wait(&bar_mma, mma_phase);
+    if (r_pending) (void)mbar_wait(&bar_r, r_phase);
+  }
+  cp_async_wait_all();
+  if (tid == 0) bulk_wait_all();  // the pages' bulk stores are complete before the kernel ends
   tmem_fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
-
-  uint16_t* sink_k = reinterpret_cast<uint16_t*>(base + L.off_sink_k);
-  uint16_t* sink_v = reinterpret_cast<uint16_t*>(base + L.off_sink_v);
-  uint16_t* win_k = reinterpret_cast<uint16_t*>(base + L.off_win_k);
-  uint16_t* win_v = reinterpret_cast<uint16_t*>(base + L.off_win_v);
-  // One token: dense (sink or window) or compressed.
-  auto one_token = [&](int t) {
-    const int p = lo + t;
-    const uint16_t* rk = rot + (size_t)t * kRotRow;
-    const uint16_t* rv = rot + (size_t)(kTileTokens + t) * kRotRow;
-    if (p < S || p >= T_new - W) {
-      uint16_t* dk = p < S ? sink_k + (int64_t)p * D : win_k + (int64_t)((p - S) % W) * D;
-      uint16_t* dv = p < S ? sink_v + (int64_t)p * D : win_v + (int64_t)((p - S) % W) * D;
-      reinterpret_cast<uint2*>(dk)[lane] = reinterpret_cast<const uint2*>(rk)[lane];
-      reinterpret_cast<uint2*>(dv)[lane] = reinterpret_cast<const uint2*>(rv)[lane];
-    } else {
-      keepk[t * 32 + lane] = (uint8_t)compress_kv(L, ud, base, p, rk, rv, lane);
-    }
-  };
-  // Warp w takes tokens w, w + 8, ...; two middle tokens at a time share their
-  // top-r searches' reductions (four searches per chain).
-  const auto middle = [&](int t) { const int p = lo + t; return p >= S && p < T_new - W; };
-  for (int t = warp; t < nt; t += 16) {
-    const int t2 = t + 8;
-    if (t2 < nt && middle(t) && middle(t2)) {
-      unsigned ka, kb;
-      compress_kv2(L, ud, base, lo + t, lo + t2, rot + (size_t)t * kRotRow, rot + (size_t)(kTileTokens + t) * kRotRow,
-                   rot + (size_t)t2 * kRotRow, rot + (size_t)(kTileTokens + t2) * kRotRow, lane, ka, kb);
-      keepk[t * 32 + lane] = (uint8_t)ka;
-      keepk[t2 * 32 + lane] = (uint8_t)kb;
-    } else {
-      one_token(t);
-      if (t2 < nt) one_token(t2);
-    }
-  }
-  __syncthreads();
-
-  // Block min/max over the zero-filled compressed keys of this tile's middle tokens.
-  const int mlo = max(lo, S), mhi = min(hi, T_new - W);
-  if (mlo < mhi && tid < D) {
-    const int c = tid;
-    uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta);
-    const int b0 = (mlo - S) / B, b1 = (mhi - 1 - S) / B;
-    for (int b = b0; b <= b1; ++b) {
-      const int blo = S + b * B;
-      const int st = max(blo, mlo), en = min(blo + B, mhi);
-      float mn = 0.f, mx = 0.f;
-      bool have = st > blo;
-      if (have) {
-        mn = bf2f(meta[(int64_t)b * 2 * D + c]);
-        mx = bf2f(meta[(int64_t)b * 2 * D + D + c]);
-      }
-      for (int p = st; p < en; ++p) {
-        const int t = p - lo;
-        const bool kept = (keepk[t * 32 + (c >> 2)] >> (c & 3)) & 1;
-        const float kt = kept ? bf2f(rot[(size_t)t * kRotRow + c]) : 0.0f;
-        if (!have) { mn = kt; mx = kt; have = true; }
-        else { mn = fminf(mn, kt); mx = fmaxf(mx, kt); }
-      }
-      meta[(int64_t)b * 2 * D + c] = f2bf(mn);
-      meta[(int64_t)b * 2 * D + D + c] = f2bf(mx);
-      if (L.meta_c > 0) {  // the rows for the compressed keys, over the (now free) A tile
-        uint16_t* bm = reinterpret_cast<uint16_t*>(Xs) + (b - b0) * 2 * D;
-        bm[c] = f2bf(mn);
-        bm[D + c] = f2bf(mx);
-      }
-    }
-  }
-  if (L.meta_c > 0 && mlo < mhi) {
-    __syncthreads();
-    const int b0 = (mlo - S) / B, b1 = (mhi - 1 - S) / B;
-    for (int b = b0 + warp; b <= b1; b += 8) {
-      const uint16_t* bm = reinterpret_cast<const uint16_t*>(Xs) + (b - b0) * 2 * D;
-      uint16_t mn[4], mx[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        mn[i] = bm[4 * lane + i];
-        mx[i] = bm[D + 4 * lane + i];
-      }
-      compress_key_row(L, base, b, mn, mx, lane);
-    }
-  }
+  if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // A segment's channel count and truncation after a swap of its pages
@@ -331,10 +581,15 @@ cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, 
 
 cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
                                const uint16_t* v, int total_tiles, cudaStream_t s) {
-  cudaError_t e = kernel_smem_attr((const void*)k_append_bulk, kBulkSmem, 256, nullptr, nullptr);
+  int sms = 0;
+  cudaError_t e = kernel_smem_attr((const void*)k_append_bulk, kBulkSmem, 256, nullptr, &sms);
   if (e != cudaSuccess) return e;
-  dim3 grid(total_tiles, L.n_kv);
-  k_append_bulk<<<grid, 256, kBulkSmem, s>>>(L, layer, cs, k, v);
+  // Persistent: at most one CTA per SM, each with an equal run of items.
+  const int items = 2 * L.n_kv * total_tiles;
+  const int grid0 = std::max(1, std::min(items, std::max(sms, 1)));
+  const int per = (items + grid0 - 1) / grid0;
+  const int grid = (items + per - 1) / per;
+  k_append_bulk<<<grid, 256, kBulkSmem, s>>>(L, layer, cs, k, v, total_tiles, per);
   return cudaGetLastError();
 }
 

@@ -161,227 +161,6 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   return kbits;
 }
 
-// The same for a token's key and value at once (same r): both searches share
-// each warp reduction (counts packed as key | value << 16), which halves the
-// dependent reductions per vector.
-__device__ __forceinline__ void warp_topr2(const uint32_t mk[4], const uint32_t mv[4], int r, int lane,
-                                           unsigned& keep_k, unsigned& keep_v, int& rank_k, int& rank_v) {
-  uint32_t tk = 0, tv = 0;
-#pragma unroll
-  for (int bit = 14; bit >= 0; --bit) {
-    const uint32_t ck = tk | (1u << bit), cv = tv | (1u << bit);
-    const unsigned c = ((unsigned)(mk[0] >= ck) + (unsigned)(mk[1] >= ck) + (unsigned)(mk[2] >= ck) +
-                        (unsigned)(mk[3] >= ck)) |
-                       (((unsigned)(mv[0] >= cv) + (unsigned)(mv[1] >= cv) + (unsigned)(mv[2] >= cv) +
-                         (unsigned)(mv[3] >= cv))
-                        << 16);
-    const unsigned sum = __reduce_add_sync(FULL, c);
-    if ((int)(sum & 0xffffu) >= r) tk = ck;
-    if ((int)(sum >> 16) >= r) tv = cv;
-  }
-  unsigned gt = 0, eq = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    gt += (unsigned)(mk[i] > tk) | ((unsigned)(mv[i] > tv) << 16);
-    eq += (unsigned)(mk[i] == tk) | ((unsigned)(mv[i] == tv) << 16);
-  }
-  const unsigned gsum = __reduce_add_sync(FULL, gt);
-  const int need_k = r - (int)(gsum & 0xffffu), need_v = r - (int)(gsum >> 16);
-  const int run0 = warp_excl_scan((int)eq, lane);
-  int run_k = run0 & 0xffff, run_v = run0 >> 16;
-  keep_k = 0;
-  keep_v = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (mk[i] > tk) {
-      keep_k |= 1u << i;
-    } else if (mk[i] == tk) {
-      if (run_k < need_k) keep_k |= 1u << i;
-      ++run_k;
-    }
-    if (mv[i] > tv) {
-      keep_v |= 1u << i;
-    } else if (mv[i] == tv) {
-      if (run_v < need_v) keep_v |= 1u << i;
-      ++run_v;
-    }
-  }
-  const int rk0 = warp_excl_scan(__popc(keep_k) | (__popc(keep_v) << 16), lane);
-  rank_k = rk0 & 0xffff;
-  rank_v = rk0 >> 16;
-}
-
-// Compresses a token's rotated key and value (128 bf16 words each at rk, rv)
-// of middle position `pos` into its page (no block min/max: the caller
-// folds those).  Called by one full warp.  Returns the key's keep bits.
-__device__ __forceinline__ unsigned compress_kv(const Layout& L, const UnitDesc& ud, char* base, int pos,
-                                                const uint16_t* rk, const uint16_t* rv, int lane) {
-  const int m = pos - L.S;
-  const int b = m / L.B;
-  const int t = m - b * L.B;
-  const int sg = seg_of_block(ud, b);
-  const int r = ud.r[sg], keep = seg_keep(ud, sg);
-  char* page = base + L.off_pages + (int64_t)b * L.page_stride;
-  const int Br = L.B * r;
-  const uint2 rawk = *reinterpret_cast<const uint2*>(rk + 4 * lane);
-  const uint2 rawv = *reinterpret_cast<const uint2*>(rv + 4 * lane);
-  const uint16_t vk[4] = {(uint16_t)(rawk.x & 0xffff), (uint16_t)(rawk.x >> 16), (uint16_t)(rawk.y & 0xffff),
-                          (uint16_t)(rawk.y >> 16)};
-  const uint16_t vv[4] = {(uint16_t)(rawv.x & 0xffff), (uint16_t)(rawv.x >> 16), (uint16_t)(rawv.y & 0xffff),
-                          (uint16_t)(rawv.y >> 16)};
-  uint32_t mk[4], mv[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {  // channels from `keep` on are truncated (see compress_vec)
-    const bool live = 4 * lane + i < keep;
-    mk[i] = live ? vk[i] & 0x7fffu : 0u;
-    mv[i] = live ? vv[i] & 0x7fffu : 0u;
-  }
-  if (L.dense_pages) {
-    store_dense_row(L, base, b, t, 0, rawk, lane);
-    store_dense_row(L, base, b, t, 1, rawv, lane);
-    return 0xfu;
-  }
-  unsigned keep_k, keep_v;
-  int rank_k, rank_v;
-  warp_topr2(mk, mv, r, lane, keep_k, keep_v, rank_k, rank_v);
-  uint16_t* valk = reinterpret_cast<uint16_t*>(page);
-  uint8_t* idxk = reinterpret_cast<uint8_t*>(page + 2 * Br);
-  uint16_t* valv = reinterpret_cast<uint16_t*>(page + 3 * Br);
-  uint8_t* idxv = reinterpret_cast<uint8_t*>(page + 5 * Br);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (keep_k >> i & 1u) {
-      valk[t * r + rank_k] = vk[i];
-      idxk[t * r + rank_k] = (uint8_t)(4 * lane + i);
-      ++rank_k;
-    }
-    if (keep_v >> i & 1u) {
-      valv[t * r + rank_v] = vv[i];
-      idxv[t * r + rank_v] = (uint8_t)(4 * lane + i);
-      ++rank_v;
-    }
-  }
-  return keep_k;
-}
-
-// Four such searches at once (two tokens' keys and values, each with its own
-// r <= 128): every warp reduction carries four 8-bit counts (a lane adds at
-// most 4 to each, so no field overflows into the next).
-__device__ __forceinline__ void warp_topr4(const uint32_t m[4][4], const int r[4], int lane, unsigned keep[4],
-                                           int rank[4]) {
-  uint32_t t[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-  for (int bit = 14; bit >= 0; --bit) {
-    unsigned c = 0;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint32_t cand = t[v] | (1u << bit);
-      const unsigned n = (unsigned)(m[v][0] >= cand) + (unsigned)(m[v][1] >= cand) + (unsigned)(m[v][2] >= cand) +
-                         (unsigned)(m[v][3] >= cand);
-      c |= n << (8 * v);
-    }
-    const unsigned sum = __reduce_add_sync(FULL, c);
-#pragma unroll
-    for (int v = 0; v < 4; ++v)
-      if ((int)((sum >> (8 * v)) & 0xffu) >= r[v]) t[v] |= 1u << bit;
-  }
-  unsigned gt = 0, eq = 0;
-#pragma unroll
-  for (int v = 0; v < 4; ++v)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      gt += (unsigned)(m[v][i] > t[v]) << (8 * v);
-      eq += (unsigned)(m[v][i] == t[v]) << (8 * v);
-    }
-  const unsigned gsum = __reduce_add_sync(FULL, gt);
-  const unsigned run0 = (unsigned)warp_excl_scan((int)eq, lane);
-  unsigned pc = 0;
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const int need = r[v] - (int)((gsum >> (8 * v)) & 0xffu);
-    int run = (int)((run0 >> (8 * v)) & 0xffu);
-    unsigned k = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (m[v][i] > t[v]) {
-        k |= 1u << i;
-      } else if (m[v][i] == t[v]) {
-        if (run < need) k |= 1u << i;
-        ++run;
-      }
-    }
-    keep[v] = k;
-    pc |= (unsigned)__popc(k) << (8 * v);
-  }
-  const unsigned rk0 = (unsigned)warp_excl_scan((int)pc, lane);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) rank[v] = (int)((rk0 >> (8 * v)) & 0xffu);
-}
-
-// compress_kv for two middle tokens at once (positions pa, pb; rotated rows
-// at rka/rva and rkb/rvb): their four top-r searches share each reduction.
-// Returns each token's key keep bits.
-__device__ __forceinline__ void compress_kv2(const Layout& L, const UnitDesc& ud, char* base, int pa, int pb,
-                                             const uint16_t* rka, const uint16_t* rva, const uint16_t* rkb,
-                                             const uint16_t* rvb, int lane, unsigned& keep_a, unsigned& keep_b) {
-  const int pos[2] = {pa, pb};
-  const uint16_t* rows[4] = {rka, rva, rkb, rvb};
-  int rr[4], kp[2], bb[2], tt[2];
-#pragma unroll
-  for (int w = 0; w < 2; ++w) {
-    const int m = pos[w] - L.S;
-    bb[w] = m / L.B;
-    tt[w] = m - bb[w] * L.B;
-    const int sg = seg_of_block(ud, bb[w]);
-    rr[2 * w] = rr[2 * w + 1] = ud.r[sg];
-    kp[w] = seg_keep(ud, sg);
-  }
-  uint16_t vals[4][4];
-  uint32_t mag[4][4];
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(rows[v] + 4 * lane);
-    vals[v][0] = (uint16_t)(raw.x & 0xffff);
-    vals[v][1] = (uint16_t)(raw.x >> 16);
-    vals[v][2] = (uint16_t)(raw.y & 0xffff);
-    vals[v][3] = (uint16_t)(raw.y >> 16);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) mag[v][i] = 4 * lane + i < kp[v >> 1] ? vals[v][i] & 0x7fffu : 0u;  // truncated: 0
-  }
-  if (L.dense_pages) {
-#pragma unroll
-    for (int v = 0; v < 4; ++v)
-      store_dense_row(L, base, bb[v >> 1], tt[v >> 1], v & 1,
-                      make_uint2((uint32_t)vals[v][0] | ((uint32_t)vals[v][1] << 16),
-                                 (uint32_t)vals[v][2] | ((uint32_t)vals[v][3] << 16)),
-                      lane);
-    keep_a = keep_b = 0xfu;
-    return;
-  }
-  unsigned keep[4];
-  int rank[4];
-  warp_topr4(mag, rr, lane, keep, rank);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const int w = v >> 1, isv = v & 1, r = rr[v];
-    char* page = base + L.off_pages + (int64_t)bb[w] * L.page_stride;
-    const int Br = L.B * r;
-    uint16_t* val = reinterpret_cast<uint16_t*>(page + (isv ? 3 * Br : 0));
-    uint8_t* idx = reinterpret_cast<uint8_t*>(page + (isv ? 5 * Br : 2 * Br));
-    int rk = rank[v];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (keep[v] >> i & 1u) {
-        val[tt[w] * r + rk] = vals[v][i];
-        idx[tt[w] * r + rk] = (uint8_t)(4 * lane + i);
-        ++rk;
-      }
-    }
-  }
-  keep_a = keep[0];
-  keep_b = keep[2];
-}
-
 // Decode-path append of n new tokens to one (sequence, kv head) by one CTA of
 // 256 threads: evicts the window tokens that leave it into the middle
 // (select, pack, block min/max), then rotates the first n_rot (0 or n, at
