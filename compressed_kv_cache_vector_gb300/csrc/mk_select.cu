@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     const int h = i / D, c = i % D;
     const float v = qr[0][h][c] + qr[1][h][c];
     qr[0][h][c] = v;
+    qs[c][h] = v;  // q' channel-major too, for the direct scoring of compressed block keys
   }
   __syncthreads();
 
@@ -356,26 +357,37 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     tpend &= ~(1u << st);
     const uint16_t* tile = reinterpret_cast<const uint16_t*>(stg + (size_t)st * kMetaTile);
     if (cmp) {
-      // Zero-filled dense rows [min | max] from the compressed ones: the
-      // dropped channels count as zero in the score.
-      uint16_t* dt = reinterpret_cast<uint16_t*>(stg);
-      for (int i = lane; i < kMT * 32; i += 32)
-        *reinterpret_cast<uint4*>(dt + (i >> 5) * kMetaRow + (i & 31) * 8) = make_uint4(0, 0, 0, 0);
-      __syncwarp();
+      // Compressed rows, scored directly: lane (row, half) sums over half of
+      // the row's kept channels, q' gathered by channel from shared memory
+      // (the dropped channels contribute zero), and the halves add by one
+      // shuffle.
       const int nrow = min(kMT, nblk - t * kMT);
-      const unsigned char* cs = cstage(st);
-      for (int e = lane; e < nrow * mc; e += 32) {
-        const int row = e / mc, i = e - row * mc;
-        const unsigned char* crow = cs + row * L.cmeta_row;
+      const unsigned char* cst = cstage(st);
+      const int row = lane & 15, hf = lane >> 4;
+      float acc[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+      if (row < nrow) {
+        const unsigned char* crow = cst + row * L.cmeta_row;
         const uint16_t* cv = reinterpret_cast<const uint16_t*>(crow);
-        const int ch = crow[4 * mc + i];
-        dt[row * kMetaRow + ch] = cv[i];
-        dt[row * kMetaRow + D + ch] = cv[mc + i];
+        const int j0 = hf ? (mc + 1) / 2 : 0, j1 = hf ? mc : (mc + 1) / 2;
+        for (int j = j0; j < j1; ++j) {
+          const float mn = bf2f(cv[j]), mx = bf2f(cv[mc + j]);
+          const int ch = crow[4 * mc + j];
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float qv = qs[ch][h];
+            acc[h] += fmaxf(qv * mn, qv * mx);
+          }
+        }
       }
-      __syncwarp();
-      tile = dt;
+      float sc = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < G; ++h) sc = fmaxf(sc, acc[h] + __shfl_xor_sync(FULL, acc[h], 16));
+      if (hf == 0 && row < nrow) emit(t * kMT + row, sc * inv_sqrt_d);
+    } else {
+      score_tile(tile, t);
     }
-    score_tile(tile, t);
     __syncwarp();
     st ^= 1;
   }
