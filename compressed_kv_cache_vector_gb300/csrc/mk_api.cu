@@ -567,6 +567,11 @@ mk_status mk_clear_error(mk_ctx* ctx) {
   if (!ctx) return MK_EINVAL;
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemset(ctx->L.err, 0, 4 * sizeof(int32_t));
+  // Kernels that gave up may have left arrival counters and key histograms
+  // part-way: back to zero.
+  const size_t slots = (size_t)ctx->cfg.max_seqs * ctx->cfg.n_kv_heads;
+  if (e == cudaSuccess) e = cudaMemset(ctx->L.counters, 0, sizeof(int32_t) * 2 * slots);
+  if (e == cudaSuccess) e = cudaMemset(ctx->L.khist, 0, sizeof(uint32_t) * mk::kKeyBins * slots);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return cuda_status(e);
 }

@@ -6,8 +6,9 @@
 // with Dynamic Two-D KV Cache Compression" (paperlayer.ai), sec. 4.2 stage 2
 // (top-k token blocks before each decode attention layer).
 //
-// GB300 structure: one CTA of 1024 threads per (sequence, kv head), launched
-// right behind the scoring kernel (programmatic dependent launch).  The
+// GB300 structure: C CTAs of 1024 threads per (sequence, kv head) (one per
+// 4096 blocks of the context, up to 8), launched right behind the scoring
+// kernel (programmatic dependent launch).  The
 // scoring kernel leaves, per unit, an order-preserving 32-bit key per block
 // (0 = not a candidate) and a 4096-bin histogram of the keys' top 12 bits.
 //  * One bulk copy each stages the histogram and the keys; thread t takes
@@ -18,9 +19,11 @@
 //    last 10 bits (1024 bins each, atomics aggregated per warp over equal
 //    bins), and a block scan of each picks the bin that holds the k-th key:
 //    the threshold key and the number of its ties to take come out exact.
-//  * Output: a key above the threshold goes to position (keys above it
-//    before it) + min(ties before it, need); a tie is taken while fewer than
-//    `need` ties precede it.  The counts before a key come from per-round
+//  * Output: every CTA of the unit finds the same threshold and writes the
+//    ids of its share of the blocks.  A key above the threshold goes to
+//    position (keys above it before it) + min(ties before it, need); a tie is
+//    taken while fewer than `need` ties precede it.  The counts before a key
+//    come from a counting pass over the blocks below the share, per-round
 //    per-warp totals (one block scan) and warp scans.
 // This code runs once per launch on its SM, so the passes are short loops
 // (instructions not yet in the instruction cache cost a fetch each).
@@ -69,22 +72,24 @@ __device__ __forceinline__ int2 block_excl_scan2_1024(int a, int b, int2* wsum) 
 }
 }  // namespace
 
-// grid: one CTA per (sequence, kv head) of the call; 1024 threads.  With
-// APPEND the scoring kernel appended cs.n_new[ci] tokens first: the length
-// it read is advanced here, after every scoring CTA has read it.
+// grid: C CTAs per (sequence, kv head) of the call; 1024 threads.  Each
+// finds the threshold by itself and writes the ids of its share of the
+// blocks.  With APPEND the scoring kernel appended cs.n_new[ci] tokens first:
+// the length it read is advanced here, after every scoring CTA has read it.
 template <bool APPEND>
 __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, CallSeqs cs, int32_t* __restrict__ ids,
-                                                        int32_t* __restrict__ n_sel, int dyn_bytes) {
+                                                        int32_t* __restrict__ n_sel, int dyn_bytes, int C) {
   extern __shared__ __align__(16) unsigned char smem[];   // staged keys
   __shared__ __align__(16) uint32_t hc[kKeyBins];
   __shared__ __align__(16) uint32_t fh[2][1024];           // fine histograms
   __shared__ __align__(16) int2 wtab[kTkThreads];          // per (round, warp): totals, then their bases
   __shared__ int2 wsum[kTkWarps];
   __shared__ __align__(16) UnitDesc ud;
-  __shared__ int s_abort, s_bin, s_rem;
+  __shared__ int s_abort, s_bin, s_rem, s_last;
   __shared__ __align__(8) uint64_t bar;
 
-  const int ci = blockIdx.x / L.n_kv, kvh = blockIdx.x - ci * L.n_kv;
+  const int unit = blockIdx.x / C, part = blockIdx.x - unit * C;
+  const int ci = unit / L.n_kv, kvh = unit - ci * L.n_kv;
   const int seq = cs.seq[ci];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t u = unit_index(L, layer, seq, kvh);
@@ -137,14 +142,20 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
   }
   __syncthreads();
   if (s_abort) return;
-  // Clear the unit's histogram for the next call (the copy has landed);
-  // advance the length after the fused append.
-  reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);
-  if (APPEND && tid == 0) L.desc[u].T = T_cur;
+  // The last of the unit's CTAs to have staged the histogram clears it for
+  // the next call (no CTA waits); part 0 advances the length after the
+  // fused append.
+  int32_t* arrived = L.counters + (int64_t)L.max_seqs * L.n_kv + slot;
+  if (tid == 0) s_last = atomicAdd(arrived, 1) == C - 1;
+  __syncthreads();
+  if (s_last) {
+    reinterpret_cast<uint4*>(gh)[tid] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) *arrived = 0;
+  }
+  if (APPEND && part == 0 && tid == 0) L.desc[u].T = T_cur;
 
-  // This thread's chunk of round j, keys past nblk zero.
-  auto chunk = [&](int j) -> uint4 {
-    const int c = j * kTkThreads + tid;
+  // Chunk c (keys 4c .. 4c+3), keys past nblk zero.
+  auto chunk_at = [&](int c) -> uint4 {
     if (c >= nch) return make_uint4(0, 0, 0, 0);
     uint4 v = staged ? ks[c] : __ldcg(reinterpret_cast<const uint4*>(kw) + c);
     if (4 * c + 1 >= nblk) v.y = 0u;
@@ -159,7 +170,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
   auto fine_pass = [&](uint32_t* h, uint32_t pre, int shift) {
 #pragma unroll 1
     for (int j = 0; j < rounds; ++j) {
-      const uint4 v = chunk(j);
+      const uint4 v = chunk_at(j * kTkThreads + tid);
       const uint32_t e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -227,8 +238,8 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
 
   // Keys above thr (all candidates when every one is taken) and ties of one
   // chunk, as 4-bit masks.
-  auto masks = [&](int j, uint32_t& gm, uint32_t& em) {
-    const uint4 v = chunk(j);
+  auto masks = [&](int c, uint32_t& gm, uint32_t& em) {
+    const uint4 v = chunk_at(c);
     const uint32_t e[4] = {v.x, v.y, v.z, v.w};
     gm = 0u;
     em = 0u;
@@ -238,27 +249,48 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
       em |= (!all && e[q] == thr) ? 1u << q : 0u;
     }
   };
-  // Per (round, warp): totals of (above, ties); then their exclusive scan in
-  // (round, warp) order, one entry per thread.
+  // This CTA's share of the chunks, and the keys taken before it.
+  const int per = (nch + C - 1) / C;
+  const int c_lo = min(nch, part * per), c_hi = min(nch, c_lo + per);
+  const int own_rounds = (c_hi - c_lo + kTkThreads - 1) / kTkThreads;
+  int2 before;
+  {
+    int g0 = 0, e0 = 0;
+    for (int c = tid; c < c_lo; c += kTkThreads) {
+      uint32_t gm, em;
+      masks(c, gm, em);
+      g0 += __popc(gm);
+      e0 += __popc(em);
+    }
+    const int2 ex = block_excl_scan2_1024(g0, e0, wsum);
+    if (tid == kTkThreads - 1) wsum[0] = make_int2(ex.x + g0, ex.y + e0);
+    __syncthreads();
+    before = wsum[0];
+    __syncthreads();
+  }
+  // Per (round, warp) of the share: totals of (above, ties); then their
+  // exclusive scan in (round, warp) order, one entry per thread.
 #pragma unroll 1
-  for (int j = 0; j < rounds; ++j) {
-    uint32_t gm, em;
-    masks(j, gm, em);
+  for (int j = 0; j < own_rounds; ++j) {
+    uint32_t gm = 0u, em = 0u;
+    const int c = c_lo + j * kTkThreads + tid;
+    if (c < c_hi) masks(c, gm, em);
     const int tg = (int)__reduce_add_sync(FULL, (unsigned)__popc(gm));
     const int te = (int)__reduce_add_sync(FULL, (unsigned)__popc(em));
     if (lane == 0) wtab[j * kTkWarps + warp] = make_int2(tg, te);
   }
   __syncthreads();
   {
-    const int2 v = tid < rounds * kTkWarps ? wtab[tid] : make_int2(0, 0);
+    const int2 v = tid < own_rounds * kTkWarps ? wtab[tid] : make_int2(0, 0);
     const int2 ex = block_excl_scan2_1024(v.x, v.y, wsum);
-    wtab[tid] = ex;
+    wtab[tid] = make_int2(ex.x + before.x, ex.y + before.y);
   }
   __syncthreads();
 #pragma unroll 1
-  for (int j = 0; j < rounds; ++j) {
-    uint32_t gm, em;
-    masks(j, gm, em);
+  for (int j = 0; j < own_rounds; ++j) {
+    uint32_t gm = 0u, em = 0u;
+    const int c = c_lo + j * kTkThreads + tid;
+    if (c < c_hi) masks(c, gm, em);
     const int og = __popc(gm), oe = __popc(em);
     int ig = og, ie = oe;
 #pragma unroll
@@ -276,14 +308,13 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
     while (__popc(tm) > take_eq) tm &= ~(1u << (31 - __clz(tm)));  // keep the lowest ids
     const uint32_t take = gm | tm;
     const int p0 = g_before + min(e_before, need);
-    const int c = j * kTkThreads + tid;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int p = p0 + __popc(take & ((1u << q) - 1u));
       if (((take >> q) & 1u) && p < L.k_max) out[p] = 4 * c + q;
     }
   }
-  if (tid == 0) n_sel[(int64_t)ci * L.n_kv + kvh] = k;
+  if (part == 0 && tid == 0) n_sel[(int64_t)ci * L.n_kv + kvh] = k;
 }
 
 bool topk_plan_ok(const Layout& L) { return (L.nblk_cap + 3) / 4 <= kTkThreads * kTkRoundsMax; }
@@ -294,7 +325,12 @@ cudaError_t launch_topk(const Layout& L, int layer, const CallSeqs& cs, int32_t*
   auto kern = append ? k_topk<true> : k_topk<false>;
   cudaError_t e = kernel_smem_attr((const void*)kern, dyn, kTkThreads, nullptr, nullptr);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(cs.n * L.n_kv), dim3(kTkThreads), dyn, s, 0, L, layer, cs, ids, n_sel, dyn);
+  // CTAs per unit: one per round of 4096 keys (the output pass is then one
+  // round each), as many as the SMs allow.
+  const int units = cs.n * L.n_kv;
+  const int rounds = ((L.nblk_cap + 3) / 4 + kTkThreads - 1) / kTkThreads;
+  const int C = std::max(1, std::min(rounds, std::min(8, 152 / std::max(1, units))));
+  return launch_pdl(kern, dim3(units * C), dim3(kTkThreads), dyn, s, 0, L, layer, cs, ids, n_sel, dyn, C);
 }
 
 }  // namespace mk

@@ -368,7 +368,9 @@ mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_he
 /* Waits for the device and reads the sticky error word: MK_OK, MK_EDEVICE or
  * MK_ETIMEOUT; *detail (optional) receives the kernel's detail code. */
 mk_status mk_poll_error(mk_ctx* ctx, int32_t* detail);
-/* Clears the device error word (synchronising). */
+/* Clears the device error word and the workspace's arrival counters and key
+ * histograms, which a kernel that gave up may have left part-way
+ * (synchronising). */
 mk_status mk_clear_error(mk_ctx* ctx);
 /* Re-reads every sequence length from the device into the host view (needed
  * after replaying a captured CUDA graph of appends).  Synchronises. */
