@@ -341,17 +341,23 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
         }
         // The r-th largest magnitude thr: the largest value with at least r
         // magnitudes >= it (bitwise from the top; the pair adds its counts).
+        // The flags of 16 words (32 magnitudes) are gathered into one word
+        // (word j's two flags shifted right by j) and counted by one popc.
         uint32_t thr = 0u;
 #pragma unroll 1
         for (int bit = 14; bit >= 0; --bit) {
           const uint32_t cand = thr | (1u << bit);
           const uint32_t cc = cand | (cand << 16);
-          uint32_t acc = 0u;
+          int n = 0;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc += ((kw[j] - cc) >> 15) & 0x00010001u;
-          uint32_t n = (acc & 0xffffu) + (acc >> 16);
+          for (int g = 0; g < 2; ++g) {
+            uint32_t f = 0u;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f |= ((kw[16 * g + j] - cc) & 0x80008000u) >> j;
+            n += __popc(f);
+          }
           n += __shfl_xor_sync(FULL, n, 1);
-          if ((int)n >= r) thr = cand;
+          if (n >= r) thr = cand;
         }
         // Above thr: kept.  Equal to thr: the lowest channels, as many as the
         // r - #above still needed (the lower half's ties come first).
@@ -464,57 +470,79 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
     __syncthreads();
     if (!is_v) {
       // Block min/max over the zero-filled compressed keys of this tile's middle tokens.
-      // Two threads per channel, each over half of a block's new tokens
-      // (four independent running min/max); the halves meet in the staging
-      // area, free once the packed rows are out.
-      float* pm = reinterpret_cast<float*>(stv);  // [block][half][min | max][128]
+      // Four threads per channel pair, each over a quarter of a block's new
+      // tokens, with bf16x2 min/max (exact) on the zero-filled rows; the
+      // quarters meet in the staging area, free once the packed rows are out.
+      uint32_t* pm = reinterpret_cast<uint32_t*>(stv);  // [block][quarter][min | max][64 pairs]
       {
-        const int c = tid & (D - 1), hf = tid >> 7;
-        const uint32_t cbit = 1u << (c & 31);
+        const int cp = tid & 63, qq = tid >> 6;
+        const int sh = (2 * cp) & 31;
+        const uint32_t* rot2 = reinterpret_cast<const uint32_t*>(rot);
         for (int b = b0; b <= b1; ++b) {
           const int blo = S + b * B;
           const int st = max(blo, mlo), en = min(blo + B, mhi);
-          const int md = st + (en - st + 1) / 2;
-          const int a0 = hf ? md : st, a1 = hf ? en : md;
-          float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          const int len = en - st;
+          const int a0 = st + (len * qq) / 4, a1 = st + (len * (qq + 1)) / 4;
+          __nv_bfloat162 mn[2], mx[2];
+          mn[0] = mn[1] = __halves2bfloat162(__ushort_as_bfloat16(0x7f80), __ushort_as_bfloat16(0x7f80));
+          mx[0] = mx[1] = __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));
           int q = a0;
-          for (; q + 3 < a1; q += 4)
+          for (; q + 1 < a1; q += 2)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < 2; ++e) {
               const int t = q + e - lo;
-              const float kt = (keepw[t * 4 + (c >> 5)] & cbit) ? bf2f(rot[(size_t)t * kRotRow + c]) : 0.0f;
-              mn[e] = fminf(mn[e], kt);
-              mx[e] = fmaxf(mx[e], kt);
+              const uint32_t kb = keepw[t * 4 + (cp >> 4)] >> sh;
+              const uint32_t v = rot2[(size_t)t * (kRotRow / 2) + cp] &
+                                 ((kb & 1u ? 0x0000ffffu : 0u) | (kb & 2u ? 0xffff0000u : 0u));
+              const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&v);
+              mn[e] = __hmin2(mn[e], x);
+              mx[e] = __hmax2(mx[e], x);
             }
-          for (; q < a1; ++q) {
+          if (q < a1) {
             const int t = q - lo;
-            const float kt = (keepw[t * 4 + (c >> 5)] & cbit) ? bf2f(rot[(size_t)t * kRotRow + c]) : 0.0f;
-            mn[0] = fminf(mn[0], kt);
-            mx[0] = fmaxf(mx[0], kt);
+            const uint32_t kb = keepw[t * 4 + (cp >> 4)] >> sh;
+            const uint32_t v = rot2[(size_t)t * (kRotRow / 2) + cp] &
+                               ((kb & 1u ? 0x0000ffffu : 0u) | (kb & 2u ? 0xffff0000u : 0u));
+            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&v);
+            mn[0] = __hmin2(mn[0], x);
+            mx[0] = __hmax2(mx[0], x);
           }
-          float* dst = pm + ((b - b0) * 2 + hf) * 2 * D;
-          dst[c] = fminf(fminf(mn[0], mn[1]), fminf(mn[2], mn[3]));
-          dst[D + c] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          const __nv_bfloat162 m0 = __hmin2(mn[0], mn[1]), m1 = __hmax2(mx[0], mx[1]);
+          uint32_t* dst = pm + ((b - b0) * 4 + qq) * 128;
+          dst[cp] = *reinterpret_cast<const uint32_t*>(&m0);
+          dst[64 + cp] = *reinterpret_cast<const uint32_t*>(&m1);
         }
       }
       __syncthreads();
-      if (tid < D) {
-        const int c = tid;
-        uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta);
+      if (tid < 64) {
+        const int cp = tid;
+        uint32_t* meta2 = reinterpret_cast<uint32_t*>(base + L.off_meta);
         for (int b = b0; b <= b1; ++b) {
           const int blo = S + b * B;
-          const float* h0 = pm + (b - b0) * 4 * D;
-          float mn = fminf(h0[c], h0[2 * D + c]), mx = fmaxf(h0[D + c], h0[3 * D + c]);
-          if (max(blo, mlo) > blo) {  // the block held tokens before this tile
-            mn = fminf(mn, bf2f(meta[(int64_t)b * 2 * D + c]));
-            mx = fmaxf(mx, bf2f(meta[(int64_t)b * 2 * D + D + c]));
+          const uint32_t* src = pm + (b - b0) * 4 * 128;
+          uint32_t u = src[cp], w = src[64 + cp];
+          __nv_bfloat162 mn = *reinterpret_cast<const __nv_bfloat162*>(&u);
+          __nv_bfloat162 mx = *reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+          for (int k = 1; k < 4; ++k) {
+            u = src[k * 128 + cp];
+            w = src[k * 128 + 64 + cp];
+            mn = __hmin2(mn, *reinterpret_cast<const __nv_bfloat162*>(&u));
+            mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&w));
           }
-          meta[(int64_t)b * 2 * D + c] = f2bf(mn);
-          meta[(int64_t)b * 2 * D + D + c] = f2bf(mx);
+          if (max(blo, mlo) > blo) {  // the block held tokens before this tile
+            u = meta2[(int64_t)b * D + cp];
+            w = meta2[(int64_t)b * D + 64 + cp];
+            mn = __hmin2(mn, *reinterpret_cast<const __nv_bfloat162*>(&u));
+            mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&w));
+          }
+          const uint32_t mnu = *reinterpret_cast<const uint32_t*>(&mn), mxu = *reinterpret_cast<const uint32_t*>(&mx);
+          meta2[(int64_t)b * D + cp] = mnu;
+          meta2[(int64_t)b * D + 64 + cp] = mxu;
           if (L.meta_c > 0) {  // the rows for the compressed keys
-            uint16_t* row = bm + (b - b0) * 2 * D;
-            row[c] = f2bf(mn);
-            row[D + c] = f2bf(mx);
+            uint32_t* row = reinterpret_cast<uint32_t*>(bm + (b - b0) * 2 * D);
+            row[cp] = mnu;
+            row[64 + cp] = mxu;
           }
         }
       }
