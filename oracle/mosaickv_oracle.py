@@ -326,6 +326,7 @@ class OracleCache:
         self.n_mid = 0
         self.Rk = None
         self.Rv = None
+        self.seg_rot = {}   # segment -> (R_k, R_v) of a segment re-compressed under its own rotation
 
     def set_rotation(self, Rk, Rv):
         self.Rk = np.asarray(Rk, dtype=np.float64)
@@ -340,6 +341,11 @@ class OracleCache:
 
     def keep_of_block(self, b):
         return self.st.segments[block_segment(b, self.firsts)][3]
+
+    def rotations_of_block(self, b):
+        """(R_k, R_v) the block's tokens are stored in: the segment's own after a
+        re-compression under its own rotation ([S] sec. 5.4), else the head's."""
+        return self.seg_rot.get(block_segment(b, self.firsts), (self.Rk, self.Rv))
 
     def n_blocks(self):
         return n_middle_blocks(self.T, self.st)
@@ -398,6 +404,39 @@ class OracleCache:
     def n_blocks_mid(self):
         return (self.n_mid + self.st.block - 1) // self.st.block
 
+    # --- re-compression of a closed segment ([S] sec. 5.4) ---------------
+    def recompress_segment(self, seg, K_raw, V_raw, r, keep=0, Rk=None, Rv=None):
+        """[S] sec. 5.4: the CPU re-compresses a closed segment (not the last,
+        open one) with a new strategy and, from the per-segment SVD of [N]
+        Fig. 4, possibly its own rotation (rows = eigenvectors of the
+        segment's own K^T K and V^T V by descending eigenvalue); the result
+        replaces the segment.  K_raw, V_raw: the sequence's unrotated rows
+        (float64, at least up to the segment's end).  Its tokens are rotated
+        once more and rounded once, compressed to the new r (truncation keep,
+        0 = all channels), and its blocks' min/max recomputed."""
+        assert 0 <= seg < len(self.st.segments) - 1, "only a closed segment is re-compressed"
+        segs = list(self.st.segments)
+        begin, _, always, _ = segs[seg]
+        segs[seg] = (begin, r, always, keep if keep else self.d)
+        self.st = Strategy(self.st.n_sink, self.st.window, self.st.block, segs, self.st.topk_fixed,
+                           self.st.retain_permille, self.st.meta_channels)
+        if Rk is not None:
+            self.seg_rot[seg] = (np.asarray(Rk, dtype=np.float64), np.asarray(Rv, dtype=np.float64))
+        Rk_s, Rv_s = self.seg_rot.get(seg, (self.Rk, self.Rv))
+        S, B = self.st.n_sink, self.st.block
+        lo = S + self.firsts[seg] * B
+        hi = S + self.firsts[seg + 1] * B
+        if hi <= lo:
+            return
+        self.Kr[lo:hi] = rotate(np.asarray(K_raw, dtype=np.float64)[lo:hi], Rk_s, self.round)
+        self.Vr[lo:hi] = rotate(np.asarray(V_raw, dtype=np.float64)[lo:hi], Rv_s, self.round)
+        self._compress(lo, hi)
+        for b in range(self.firsts[seg], self.firsts[seg + 1]):
+            blo, bhi = self.block_tokens(b)
+            blk = self.Kt[blo:bhi].astype(np.float64)
+            self.mn[b] = blk.min(axis=0) + 0.0
+            self.mx[b] = blk.max(axis=0) + 0.0
+
     # --- views used by the tests ------------------------------------------
     def sink_positions(self):
         return np.arange(min(self.st.n_sink, self.T))
@@ -455,10 +494,17 @@ class OracleCache:
         return mn, mx
 
     def scores(self, q):
-        """Group scores over every middle block (always-blocks included)."""
+        """Group scores over every middle block (always-blocks included).  A
+        block stored under its segment's own rotation is scored with the query
+        rotated by that rotation."""
         mn, mx = self.score_keys()
         per, grp = block_scores(self.rotate_query(q), mn, mx)
-        return per, grp
+        for seg, (Rk_s, _) in self.seg_rot.items():
+            lo, hi = self.firsts[seg], min(self.firsts[seg + 1], self.n_blocks_mid())
+            if hi > lo:
+                p_s, _ = block_scores(np.asarray(q, dtype=np.float64) @ Rk_s.T, mn[lo:hi], mx[lo:hi])
+                per[:, lo:hi] = p_s
+        return per, per.max(axis=0)
 
     def select(self, q):
         cand = self.candidates()
@@ -480,9 +526,45 @@ class OracleCache:
 
     def attention(self, q, ids):
         """[N] Eq. (13) on the kept tokens, then Eq. (14) output = o R_v."""
-        Kt, Vt = self.attend_tokens(ids)
-        o = softmax_attention(self.rotate_query(q), Kt, Vt)
-        return o @ self.Rv
+        if not self.seg_rot:
+            Kt, Vt = self.attend_tokens(ids)
+            o = softmax_attention(self.rotate_query(q), Kt, Vt)
+            return o @ self.Rv
+        # Segments under their own rotation: each token's logit uses the query
+        # rotated into its basis, and each basis's weighted values are
+        # un-rotated by its own R_v; one softmax over all tokens.
+        q = np.asarray(q, dtype=np.float64)
+        groups = {}   # basis -> (rows of K~, rows of V~)
+        head = (id(self.Rk), id(self.Rv))
+        def add(key, k_rows, v_rows):
+            kk, vv = groups.setdefault(key, ([], []))
+            kk.append(k_rows)
+            vv.append(v_rows)
+        add(head, self.Kr[self.sink_positions()], self.Vr[self.sink_positions()])
+        add(head, self.Kr[self.window_positions()], self.Vr[self.window_positions()])
+        rot = {head: (self.Rk, self.Rv)}
+        for b in np.concatenate([np.asarray(ids, dtype=np.int64), self.always_blocks()]):
+            Rk_b, Rv_b = self.rotations_of_block(int(b))
+            key = (id(Rk_b), id(Rv_b))
+            rot[key] = (Rk_b, Rv_b)
+            lo, hi = self.block_tokens(int(b))
+            add(key, self.Kt[lo:hi], self.Vt[lo:hi])
+        logits, values = [], []
+        for key, (kk, vv) in groups.items():
+            Rk_b, Rv_b = rot[key]
+            Kb = np.concatenate(kk).astype(np.float64)
+            logits.append((q @ Rk_b.T) @ Kb.T / math.sqrt(self.d))
+            values.append((np.concatenate(vv).astype(np.float64), Rv_b))
+        lg = np.concatenate(logits, axis=1)
+        p = np.exp(lg - lg.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        out = np.zeros((q.shape[0], self.d))
+        c0 = 0
+        for Vb, Rv_b in values:
+            n = Vb.shape[0]
+            out += (p[:, c0:c0 + n] @ Vb) @ Rv_b
+            c0 += n
+        return out
 
 
 def quest_decode(q, K, V, st: Strategy, T0=None):

@@ -526,3 +526,83 @@ def test_quest_equals_the_method_with_every_channel_and_no_rotation(segments, G,
     _, out_all = O.quest_decode(q, K, V, st_all)
     ref = _sdpa(q, K, V)
     assert np.allclose(out_all, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+
+
+# ------------------------------------- segment re-compressed, own rotation ----
+def _seg_cache(round_bf16, r_all, seed, topk_fixed=10 ** 6):
+    st = O.Strategy(4, 40, 16, [(0, r_all, 0), (500, r_all, 0)], topk_fixed, 0)
+    K = _gen(1200, 0.9, seed)
+    V = _gen(1200, 0.9, seed + 1)
+    Rk, _ = O.rotation_from_keys(K)
+    Rv, _ = O.rotation_from_keys(V)
+    c = O.OracleCache(st, 1208, round_bf16=round_bf16)
+    c.set_rotation(Rk, Rv)
+    c.append(K[:1150], V[:1150])
+    c.append(K[1150:], V[1150:])
+    return c, K, V
+
+
+def test_own_rotation_segment_full_channels_equals_dense_attention():
+    # [S] sec. 5.4 / [N] Fig. 4: segment 0 re-compressed under its own
+    # rotation (eigenvectors of its own K^T K, V^T V).  With every channel
+    # kept, every block attended and no rounding, attention is still [N]
+    # Eq. (1) on the raw cache: each basis's logits use the query in that
+    # basis and its values are un-rotated by its own R_v.
+    c, K, V = _seg_cache(False, 128, 60)
+    lo = 4
+    hi = 4 + c.firsts[1] * 16
+    Rk_s, _ = O.rotation_from_keys(K[lo:hi])
+    Rv_s, _ = O.rotation_from_keys(V[lo:hi])
+    assert np.abs(Rk_s - c.Rk).max() > 0.1          # a genuinely different basis
+    c.recompress_segment(0, K, V, 128, 0, Rk_s, Rv_s)
+    q = np.random.default_rng(61).standard_normal((4, 128))
+    ids, _ = c.select(q)
+    got = c.attention(q, ids)
+    want = _sdpa(q, K, V)
+    assert np.allclose(got, want, rtol=0, atol=1e-12 * np.abs(want).max())
+    # a planted mistake: the segment's values un-rotated by the head's R_v
+    saved = c.seg_rot[0]
+    c.seg_rot[0] = (Rk_s, c.Rv)
+    assert not np.allclose(c.attention(q, ids), want, atol=1e-6)
+    c.seg_rot[0] = saved
+
+
+def test_own_rotation_segment_scores_and_storage():
+    # B = 1: a block's score is q'_s . k~ / sqrt(d) with q' rotated by the
+    # block's own basis ([N] Eq. (12)); the stored rows are the top-r of the
+    # raw rows rotated once by the segment's rotation and rounded once.
+    st = O.Strategy(4, 16, 1, [(0, 32, 0), (500, 32, 0)], 0, 100)
+    K = _gen(400, 0.9, 62)
+    V = _gen(400, 0.9, 63)
+    Rk, _ = O.rotation_from_keys(K)
+    Rv, _ = O.rotation_from_keys(V)
+    c = O.OracleCache(st, 408)
+    c.set_rotation(Rk, Rv)
+    c.append(K, V)
+    hi = 4 + c.firsts[1]
+    Rk_s, _ = O.rotation_from_keys(K[4:hi])
+    Rv_s, _ = O.rotation_from_keys(V[4:hi])
+    c.recompress_segment(0, K, V, 24, 0, Rk_s, Rv_s)
+    q = np.random.default_rng(64).standard_normal((2, 128))
+    _, grp = c.scores(q)
+    for b in range(c.n_blocks_mid()):
+        lo_t, hi_t = c.block_tokens(b)
+        Rq = Rk_s if b < c.firsts[1] else Rk
+        assert abs(grp[b] - O.block_max_exact(q @ Rq.T, c.Kt[lo_t:hi_t])) < 1e-12
+    for t in range(4, hi):
+        x = O.bf16_round(K[t] @ Rk_s.T)
+        keep = sorted(sorted(range(128), key=lambda j: (-abs(x[j]), j))[:24])
+        z = np.zeros(128)
+        z[keep] = x[keep]
+        assert np.array_equal(c.Kt[t].astype(np.float64), z)
+    assert c.r_of_block(0) == 24 and c.r_of_block(c.firsts[1]) == 32
+
+
+def test_recompress_with_head_rotation_reproduces_the_cache():
+    # Re-compressing a segment with the head's own rotation and strategy gives
+    # back exactly what the appends built.
+    a, K, V = _seg_cache(True, 38, 65, topk_fixed=0)
+    b, _, _ = _seg_cache(True, 38, 65, topk_fixed=0)
+    b.recompress_segment(0, K, V, 38)
+    for name in ("Kr", "Vr", "Kt", "Vt", "kidx", "vidx", "kval", "vval", "mn", "mx"):
+        assert np.array_equal(getattr(a, name), getattr(b, name)), name
