@@ -89,7 +89,7 @@ _SIGS = {
                           ctypes.POINTER(MkSegStats), ctypes.POINTER(c_i32)],
     "mk_host_pack_blocks": [c_vp, c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_i64, c_i32, c_vp, c_vp,
                             c_vp],
-    "mk_swap_segment": [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp],
+    "mk_swap_segment": [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp],
 }
 
 _lib = None
@@ -243,16 +243,21 @@ class MosaicKV:
             self.h, len(T), _i32(T), _ptr(q), _ptr(K), _ptr(V), K.shape[2], _ptr(out), _stream(stream)))
         return out
 
-    def swap_segment(self, layer, seq, kvh, segment, r, keep_channels, pages, meta, cmeta=None, stream=None):
+    def swap_segment(self, layer, seq, kvh, segment, r, keep_channels, pages, meta, cmeta=None, stream=None,
+                     R_k=None, R_v=None):
         """Replace a closed segment's pages and keys with host-packed ones (host_pack_blocks), under r from
-        then on.  The host arrays must live until the stream has run the copies."""
+        then on, and under the segment's own rotations R_k, R_v if given (the pages must be packed with
+        them).  The host arrays must live until the stream has run the copies."""
         pg = np.ascontiguousarray(pages, dtype=np.uint8)
         mt = np.ascontiguousarray(meta, dtype=np.uint16)
         cm = None if cmeta is None else np.ascontiguousarray(cmeta, dtype=np.uint8)
+        rk = None if R_k is None else np.ascontiguousarray(R_k, dtype=np.float32)
+        rv = None if R_v is None else np.ascontiguousarray(R_v, dtype=np.float32)
         self._swap_keep = (pg, mt, cm)   # kept alive until the next swap
         _check("mk_swap_segment", self.lib.mk_swap_segment(
-            self.h, layer, seq, kvh, segment, r, keep_channels, _np_ptr(pg), _np_ptr(mt),
-            _np_ptr(cm) if cm is not None else ctypes.c_void_p(0), _stream(stream)))
+            self.h, layer, seq, kvh, segment, r, keep_channels,
+            _np_ptr(rk) if rk is not None else ctypes.c_void_p(0), _np_ptr(rv) if rv is not None else ctypes.c_void_p(0),
+            _np_ptr(pg), _np_ptr(mt), _np_ptr(cm) if cm is not None else ctypes.c_void_p(0), _stream(stream)))
 
     def poll_error(self):
         d = c_i32()

@@ -27,6 +27,7 @@ struct mk_ctx {
   std::vector<int32_t> firsts;       // [layers][max_seqs][MK_MAX_SEGMENTS]
   std::vector<uint8_t> rot_set;      // [layers][max_seqs][n_kv]
   std::vector<std::vector<int32_t>> sel_seqs;  // per layer: sequence list of its last selection
+  std::vector<uint8_t> own_rot;      // [units][MK_MAX_SEGMENTS]: segment stored under its own rotation
 };
 
 namespace {
@@ -106,13 +107,17 @@ Plan make_plan(const mk_config* c) {
   L.meta_c = c->meta_channels;
   L.cmeta_row = L.meta_c > 0 ? (5 * L.meta_c + 15) / 16 * 16 : 0;
   L.off_cmeta = off; off = align_up(off + (int64_t)std::max(1, L.nblk_cap) * L.cmeta_row);
+  // Own rotations of the closed segments (re-compression under a segment's own rotation).
+  L.n_cls = c->n_segments > 1 ? c->n_segments : 1;
+  L.off_segrot = off; off = align_up(off + (int64_t)(L.n_cls - 1) * 2 * D * D * 4);
   L.unit_stride = off;
   p.n_units = (int64_t)c->n_layers * c->max_seqs * c->n_kv_heads;
   p.units_off = align_up(kAlign + p.n_units * (int64_t)sizeof(UnitDesc));
   p.arena_bytes = p.units_off + p.n_units * L.unit_stride;
   const int64_t slots = (int64_t)c->max_seqs * c->n_kv_heads;
   int64_t w = 0;
-  w = align_up(w + (int64_t)c->n_layers * slots * L.G * D * 4);  // qrot, per layer
+  w = align_up(w + (int64_t)L.n_cls * c->n_layers * slots * L.G * D * 4);  // qrot, per class and layer
+  w = align_up(w + (int64_t)c->n_layers * slots * MK_MAX_SEGMENTS * 4);     // seg_sel
   w = align_up(w + slots * (int64_t)L.keys_stride * 4);        // block keys
   w = align_up(w + slots * (int64_t)mk::kKeyBins * 4);         // coarse key histograms
   w = align_up(w + slots * MK_MAX_SPLITS * L.G * D * 4);       // part_acc
@@ -133,7 +138,8 @@ void bind_pointers(Plan& p, void* arena, void* ws) {
   const int64_t slots = (int64_t)L.max_seqs * L.n_kv;
   char* w = static_cast<char*>(ws);
   int64_t o = 0;
-  L.qrot = reinterpret_cast<float*>(w + o); o = align_up(o + (int64_t)L.n_layers * slots * L.G * D * 4);
+  L.qrot = reinterpret_cast<float*>(w + o); o = align_up(o + (int64_t)L.n_cls * L.n_layers * slots * L.G * D * 4);
+  L.seg_sel = reinterpret_cast<int32_t*>(w + o); o = align_up(o + (int64_t)L.n_layers * slots * MK_MAX_SEGMENTS * 4);
   L.keys = reinterpret_cast<uint32_t*>(w + o); o = align_up(o + slots * (int64_t)L.keys_stride * 4);
   L.khist = reinterpret_cast<uint32_t*>(w + o); o = align_up(o + slots * (int64_t)mk::kKeyBins * 4);
   L.part_acc = reinterpret_cast<float*>(w + o); o = align_up(o + slots * MK_MAX_SPLITS * L.G * D * 4);
@@ -195,6 +201,17 @@ mk_status check_seqs(const mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int
 }
 
 inline mk_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MK_OK : MK_ECUDA; }
+
+// Whether some unit of the call has a segment stored under its own rotation.
+bool call_has_own(const mk_ctx* ctx, int layer, int n_seqs, const int32_t* seq_ids) {
+  for (int i = 0; i < n_seqs; ++i)
+    for (int h = 0; h < ctx->cfg.n_kv_heads; ++h) {
+      const int64_t u = mk::unit_index(ctx->L, layer, seq_ids[i], h);
+      for (int sg = 0; sg < MK_MAX_SEGMENTS; ++sg)
+        if (ctx->own_rot[(size_t)u * MK_MAX_SEGMENTS + sg]) return true;
+    }
+  return false;
+}
 
 }  // namespace
 
@@ -303,6 +320,7 @@ mk_status mk_create(const mk_config* cfg, void* arena, size_t arena_bytes, void*
   ctx->firsts.assign(ls * MK_MAX_SEGMENTS, 0);
   ctx->rot_set.assign(ls * cfg->n_kv_heads, 0);
   ctx->sel_seqs.assign(cfg->n_layers, std::vector<int32_t>());
+  ctx->own_rot.assign((size_t)p.n_units * MK_MAX_SEGMENTS, 0);
   cudaError_t e = cudaMemset(arena, 0, (size_t)p.units_off);
   if (e == cudaSuccess) e = cudaMemset(ctx->L.counters, 0, sizeof(int32_t) * 2 * cfg->max_seqs * cfg->n_kv_heads);
   if (e == cudaSuccess)
@@ -450,7 +468,8 @@ mk_status mk_block_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int3
     max_nblk = std::max(max_nblk, mk::n_mid_blocks(ctx->L, ctx->T[ls]));
   }
   cudaError_t e = mk::launch_block_select(ctx->L, layer, *cs, static_cast<const uint16_t*>(q), ids, n_sel, scores,
-                                          std::max(1, max_nblk), (cudaStream_t)stream);
+                                          std::max(1, max_nblk), (cudaStream_t)stream, nullptr, nullptr,
+                                          call_has_own(ctx, layer, n_seqs, seq_ids));
   delete cs;
   if (e != cudaSuccess) return MK_ECUDA;
   ctx->sel_seqs[layer].assign(seq_ids, seq_ids + n_seqs);
@@ -484,7 +503,8 @@ mk_status mk_append_select(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int
   }
   cudaError_t e = mk::launch_block_select(ctx->L, layer, *cs, static_cast<const uint16_t*>(q), ids, n_sel, scores,
                                           std::max(1, max_nblk), (cudaStream_t)stream,
-                                          static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v));
+                                          static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v),
+                                          call_has_own(ctx, layer, n_seqs, seq_ids));
   delete cs;
   if (e != cudaSuccess) return MK_ECUDA;
   for (int i = 0; i < n_seqs; ++i) ctx->T[(size_t)layer * ctx->cfg.max_seqs + seq_ids[i]] += 1;
@@ -502,10 +522,18 @@ mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32
   CallSeqs* cs = new (std::nothrow) CallSeqs();
   if (!cs) return MK_ENOMEM;
   cs->n = n_seqs;
-  int32_t items[MK_MAX_CALL_SEQS];
+  int32_t items[MK_MAX_CALL_SEQS], min_parts[MK_MAX_CALL_SEQS];
   for (int i = 0; i < n_seqs; ++i) {
     cs->seq[i] = seq_ids[i];
     const size_t ls = (size_t)layer * ctx->cfg.max_seqs + seq_ids[i];
+    // one CTA per rotation class of the unit with the most own-rotation segments
+    min_parts[i] = 1;
+    for (int h = 0; h < ctx->cfg.n_kv_heads; ++h) {
+      const int64_t u = mk::unit_index(ctx->L, layer, seq_ids[i], h);
+      int n_own = 0;
+      for (int sg = 0; sg < MK_MAX_SEGMENTS; ++sg) n_own += ctx->own_rot[(size_t)u * MK_MAX_SEGMENTS + sg];
+      min_parts[i] = std::max(min_parts[i], 1 + n_own);
+    }
     const int T = ctx->T[ls];
     const int nblk = mk::n_mid_blocks(ctx->L, T);
     const UnitDesc d = host_desc(ctx, layer, seq_ids[i]);
@@ -516,7 +544,7 @@ mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32
                (mk::n_select(ctx->L, scored) + (nblk - scored)) * groups;
   }
   cudaError_t e = mk::launch_decode_attn(ctx->L, layer, *cs, ids, n_sel, static_cast<uint16_t*>(out), items,
-                                         (cudaStream_t)stream);
+                                         (cudaStream_t)stream, min_parts);
   delete cs;
   return cuda_status(e);
 }
@@ -637,8 +665,8 @@ mk_status mk_record_event(void* event, mk_stream stream) {
 }  // extern "C"
 
 mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, int32_t segment, int32_t r,
-                          int32_t keep_channels, const void* pages, const void* meta, const void* cmeta,
-                          mk_stream stream) {
+                          int32_t keep_channels, const float* R_k, const float* R_v, const void* pages,
+                          const void* meta, const void* cmeta, mk_stream stream) {
   if (!ctx || !pages || !meta) return MK_EINVAL;
   const mk_config& c = ctx->cfg;
   const Layout& L = ctx->L;
@@ -649,6 +677,7 @@ mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_he
   if (r < 1 || r > L.r_max) return MK_EINVAL;  // the pages hold at most r_max entries per token
   if (keep_channels != 0 && (keep_channels < r || keep_channels > MK_HEAD_DIM)) return MK_EINVAL;
   if (L.meta_c > 0 && !cmeta) return MK_EINVAL;
+  if ((R_k == nullptr) != (R_v == nullptr)) return MK_EINVAL;
   const size_t ls = (size_t)layer * c.max_seqs + seq;
   if (ctx->T0[ls] == 0 || segment == c.n_segments - 1) return MK_ESTATE;
   const int fb = ctx->firsts[ls * MK_MAX_SEGMENTS + segment], lb = ctx->firsts[ls * MK_MAX_SEGMENTS + segment + 1];
@@ -665,6 +694,24 @@ mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_he
   if (e == cudaSuccess && L.meta_c > 0)
     e = cudaMemcpyAsync(base + L.off_cmeta + (int64_t)fb * L.cmeta_row, cmeta, (size_t)n * (size_t)L.cmeta_row,
                         cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = mk::launch_set_segment(L, u, segment, r, keep_channels ? keep_channels : MK_HEAD_DIM, s);
+  const bool own = R_k != nullptr;
+  if (own && e == cudaSuccess) {
+    // The segment's rotation in the layouts the kernels read: R_k^T for the
+    // selection's query rotation, R_v for the attention's un-rotation.  The
+    // copy is from pageable memory, so the data has been taken when it
+    // returns (it waits for the stream's earlier work, as a rotation change
+    // should).
+    std::vector<float> rt((size_t)2 * MK_HEAD_DIM * MK_HEAD_DIM);
+    for (int i = 0; i < MK_HEAD_DIM; ++i)
+      for (int j = 0; j < MK_HEAD_DIM; ++j) {
+        rt[(size_t)j * MK_HEAD_DIM + i] = R_k[(size_t)i * MK_HEAD_DIM + j];
+        rt[(size_t)MK_HEAD_DIM * MK_HEAD_DIM + (size_t)i * MK_HEAD_DIM + j] = R_v[(size_t)i * MK_HEAD_DIM + j];
+      }
+    e = cudaMemcpyAsync(base + mk::segrot_off(L, segment), rt.data(), rt.size() * sizeof(float),
+                        cudaMemcpyHostToDevice, s);
+  }
+  if (e == cudaSuccess)
+    e = mk::launch_set_segment(L, u, segment, r, keep_channels ? keep_channels : MK_HEAD_DIM, own ? 1 : 0, s);
+  if (e == cudaSuccess) ctx->own_rot[(size_t)u * MK_MAX_SEGMENTS + segment] = own ? 1 : 0;
   return cuda_status(e);
 }

@@ -579,17 +579,17 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
-// A segment's channel count and truncation after a swap of its pages
-// (double-buffered re-compression); the flags keep the always bit.
-__global__ void k_set_segment(Layout L, int64_t u, int seg, int r, int keep) {
+// A segment's channel count, truncation and rotation flag after a swap of its
+// pages (double-buffered re-compression); the flags keep the always bit.
+__global__ void k_set_segment(Layout L, int64_t u, int seg, int r, int keep, int own) {
   if (threadIdx.x == 0) {
     L.desc[u].r[seg] = r;
-    L.desc[u].sflags[seg] = (L.desc[u].sflags[seg] & 1) | (keep << 8);
+    L.desc[u].sflags[seg] = (L.desc[u].sflags[seg] & 1) | (own ? 2 : 0) | (keep << 8);
   }
 }
 
-cudaError_t launch_set_segment(const Layout& L, int64_t u, int seg, int r, int keep, cudaStream_t s) {
-  k_set_segment<<<1, 32, 0, s>>>(L, u, seg, r, keep);
+cudaError_t launch_set_segment(const Layout& L, int64_t u, int seg, int r, int keep, int own, cudaStream_t s) {
+  k_set_segment<<<1, 32, 0, s>>>(L, u, seg, r, keep, own);
   return cudaGetLastError();
 }
 

@@ -235,7 +235,7 @@ int attn_max_parts(const Layout& L) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(MK_MAX_SPLITS, avail / ((int64_t)L.G * (D + 2) * 4)));
 }
 
-template <int G, bool DENSE, int MAXW>
+template <int G, bool DENSE, int MAXW, bool OWN>
 __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, CallSeqs cs, AttnSplit split,
                                                  const int32_t* __restrict__ ids,
                                                  const int32_t* __restrict__ n_sel_in,
@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
   uint16_t* zrow = reinterpret_cast<uint16_t*>(mlw + kWarps * 16);      // one zero row (272 B)
   __shared__ __align__(16) UnitDesc ud;
   __shared__ int s_abort, s_ns, s_last;
+  __shared__ int s_segsel[MK_MAX_SEGMENTS + 1];  // first position of each segment's ids (own-rotation segments)
   __shared__ float s_m[8], s_l[8];
   __shared__ int32_t s_ids[kIdsCap];
   __shared__ uint64_t s_bar, s_bar2;  // R_v staging (every CTA), partials staging (the merging CTA)  // this CTA's selected block ids (its j-th item: ids[part + j P])
@@ -299,8 +300,8 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
   // caller's q of the dense reference is read after it.
   const int hq = g % G;
   uint32_t aq[8][4];
-  auto load_q = [&]() {
-    const float* qrot = qrot_of(L, layer, slot);
+  auto load_q = [&](int cls_q) {
+    const float* qrot = qrot_of(L, layer, slot, cls_q);
     const uint16_t* qin = DENSE ? q_in + ((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D : nullptr;
     float2 qx[8][2];
 #pragma unroll
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) split2_bf16(qx[kc][hf].x, qx[kc][hf].y, aq[kc][2 * hf], aq[kc][2 * hf + 1]);
   };
-  if (!DENSE) load_q();
+  if (!DENSE) load_q(0);
   pdl_wait();
   pdl_trigger();
   // One round of independent loads (L2 path: the previous kernel wrote them):
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
   }
   if (!DENSE)
     for (int j = tid; j < kIdsCap && part + j * P < L.k_max; j += blockDim.x) s_ids[j] = __ldcg(my_ids + part + j * P);
-  if (DENSE) load_q();
+  if (DENSE) load_q(0);
   __syncthreads();
   bool skip = s_abort != 0;
 
@@ -366,8 +367,115 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
   // the dense chunks.  CTA `part` takes items part, part + P, ...; its warps
   // take its j-th items round robin (j = warp, warp + kWarps, ...).
   const int n_dch = (n_dense + kDC - 1) / kDC;
-  const int n_items = skip ? 0 : ns + n_always + n_dch;
-  const int n_mine = n_items > part ? (n_items - part + P - 1) / P : 0;
+  // Rotation classes.  With segments stored under their own rotation
+  // (re-compressed closed segments), every rotation gets its own CTAs of the
+  // unit: a CTA takes the items of one class only, rotates the query into
+  // that class's basis and un-rotates its partial by the class's R_v, so
+  // the merge stays a weighted sum.  Class 0 is the head's rotation (with the
+  // sinks and the window); class s + 1 is segment s's own.  Each class holds
+  // at least one CTA (the host gives such units enough), the rest go by the
+  // classes' work.  Without such segments: one class, the unit's P CTAs.
+  int cls = 0, pc = part, Pc = P;
+  int ns_c = ns, nalw_c = n_always, ndch_c = n_dch;
+  const bool own_mode = OWN && !DENSE && !skip && any_own(ud);
+  if (own_mode) {
+    if (tid == 0)
+      for (int i = 0; i < MK_MAX_SEGMENTS; ++i)
+        s_segsel[i] = __ldcg(L.seg_sel + (((int64_t)layer * L.max_seqs + seq) * L.n_kv + kvh) * MK_MAX_SEGMENTS + i);
+    __syncthreads();
+    const int nseg = ud.n_seg;
+    int ss[MK_MAX_SEGMENTS + 1];
+#pragma unroll
+    for (int i = 0; i <= MK_MAX_SEGMENTS; ++i) ss[i] = i < nseg ? min(max(s_segsel[i], 0), ns) : ns;
+    const int mine = tid <= MK_MAX_SEGMENTS ? (tid < nseg ? min(max(s_segsel[tid], 0), ns) : ns) : 0;
+    __syncthreads();
+    if (tid <= MK_MAX_SEGMENTS) s_segsel[tid] = mine;  // clamped, kept for the item mapping below
+    int csel[MK_MAX_SEGMENTS], calw[MK_MAX_SEGMENTS], wcls[MK_MAX_SEGMENTS];
+#pragma unroll
+    for (int c = 0; c < MK_MAX_SEGMENTS; ++c) csel[c] = calw[c] = 0;
+#pragma unroll
+    for (int sg = 0; sg < MK_MAX_SEGMENTS; ++sg) {
+      if (sg >= nseg) continue;
+      const int lo = min(ud.first_block[sg], nblk), hi = sg + 1 < nseg ? min(ud.first_block[sg + 1], nblk) : nblk;
+      const int c = seg_class(ud, sg);
+#pragma unroll
+      for (int k = 0; k < MK_MAX_SEGMENTS; ++k)
+        if (k == c) {
+          if (seg_always(ud, sg)) calw[k] += max(0, hi - lo);
+          else csel[k] += ss[sg + 1] - ss[sg];
+        }
+    }
+    int nact = 0, wsum_c = 0;
+#pragma unroll
+    for (int c = 0; c < MK_MAX_SEGMENTS; ++c) {
+      const bool act = c < nseg && (c == 0 || seg_own(ud, c - 1));
+      wcls[c] = act ? (csel[c] + calw[c]) * ((B + kDC - 1) / kDC) + (c == 0 ? n_dch : 0) : -1;
+      nact += act ? 1 : 0;
+      wsum_c += act ? wcls[c] : 0;
+    }
+    const int extra = max(0, P - nact);
+    int start = 0, used = 0;
+    int pcs[MK_MAX_SEGMENTS];
+#pragma unroll
+    for (int c = 0; c < MK_MAX_SEGMENTS; ++c) {
+      pcs[c] = wcls[c] < 0 ? 0 : 1 + (wsum_c > 0 ? (int)(((int64_t)extra * wcls[c]) / wsum_c) : 0);
+      used += pcs[c];
+    }
+    pcs[0] += max(0, P - used);  // what the rounding left
+#pragma unroll
+    for (int c = 0; c < MK_MAX_SEGMENTS; ++c) {
+      if (pcs[c] > 0 && part >= start && part < start + pcs[c]) {
+        cls = c;
+        pc = part - start;
+        Pc = pcs[c];
+        ns_c = csel[c];
+        nalw_c = calw[c];
+        ndch_c = c == 0 ? n_dch : 0;
+      }
+      start += pcs[c];
+    }
+    if (part >= start) {  // more CTAs than classes can use (cannot happen with P >= the class count): idle
+      ns_c = nalw_c = ndch_c = 0;
+    }
+  }
+  // The i-th selected id of this CTA's class: its position in the ids row.
+  auto sel_pos = [&](int i) -> int {
+    if (!own_mode) return i;
+    int pos = -1;
+#pragma unroll
+    for (int sg = 0; sg < MK_MAX_SEGMENTS; ++sg) {
+      if (sg < ud.n_seg && seg_class(ud, sg) == cls && !seg_always(ud, sg) && pos < 0) {
+        const int n = s_segsel[sg + 1] - s_segsel[sg];
+        if (i < n) pos = s_segsel[sg] + i;
+        else i -= n;
+      }
+    }
+    return pos;
+  };
+  // The i-th always-attended block of this CTA's class.
+  auto alw_block = [&](int i) -> int {
+    if (!own_mode) return always_block(ud, nblk, i);
+    int b = -1;
+#pragma unroll
+    for (int sg = 0; sg < MK_MAX_SEGMENTS; ++sg) {
+      if (sg < ud.n_seg && seg_class(ud, sg) == cls && seg_always(ud, sg) && b < 0) {
+        const int lo = min(ud.first_block[sg], nblk), hi = sg + 1 < ud.n_seg ? min(ud.first_block[sg + 1], nblk) : nblk;
+        const int n = max(0, hi - lo);
+        if (i < n) b = lo + i;
+        else i -= n;
+      }
+    }
+    return b;
+  };
+  if (own_mode) {
+    // This CTA's block ids and query, for its class.
+    __syncthreads();
+    for (int j = tid; j < kIdsCap && pc + j * Pc < ns_c; j += blockDim.x) s_ids[j] = __ldcg(my_ids + sel_pos(pc + j * Pc));
+    if (cls != 0) load_q(cls);
+    __syncthreads();
+  }
+  const int n_items = skip ? 0 : ns_c + nalw_c + ndch_c;
+  const int n_mine = n_items > pc ? (n_items - pc + Pc - 1) / Pc : 0;
 
   const char* base = DENSE ? nullptr : unit_base(L, u);
   unsigned char* my_area = warp_area + (size_t)warp * pwb;
@@ -378,15 +486,15 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
     Task t{};
     if (j >= n_mine) return t;
     t.item = j;
-    const int it = part + j * P;
-    if (it >= ns + n_always) {
+    const int it = pc + j * Pc;
+    if (it >= ns_c + nalw_c) {
       t.kind = 1;
       t.b = -1;
-      t.j0 = (it - ns - n_always) * kDC;
+      t.j0 = (it - ns_c - nalw_c) * kDC;
       t.nd = min(kDC, n_dense - t.j0);
       return t;
     }
-    const int b = it < ns ? (j < kIdsCap ? s_ids[j] : __ldcg(my_ids + it)) : always_block(ud, nblk, it - ns);
+    const int b = it < ns_c ? (j < kIdsCap ? s_ids[j] : __ldcg(my_ids + sel_pos(it))) : alw_block(it - ns_c);
     if (b < 0 || b >= nblk) {
       if (lane == 0) set_error(L, ERR_BAD_BLOCK, (int32_t)u, b);
       t.kind = 3;
@@ -689,7 +797,8 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
   if (!DENSE && tid == 0) {
     fence_proxy_async();  // the stages and tiles were written by the main loop
     mbar_expect_tx(&s_bar, (unsigned)(D * D * 4));
-    bulk_g2s(rvs, base + L.off_rv, (unsigned)(D * D * 4), &s_bar);
+    bulk_g2s(rvs, base + (cls == 0 ? L.off_rv : segrot_off(L, cls - 1) + (int64_t)D * D * 4), (unsigned)(D * D * 4),
+             &s_bar);
   }
   float* dump = reinterpret_cast<float*>(warp_area);  // [kWarps][G][D] (main loop is over)
   {
@@ -872,12 +981,12 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
 }
 
 namespace {
-template <int G, bool DENSE, int MAXW>
+template <int G, bool DENSE, int MAXW, bool OWN>
 cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                        const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
-                       const int32_t* items, size_t smem, cudaStream_t s) {
+                       const int32_t* items, const int32_t* min_parts, size_t smem, cudaStream_t s) {
   int occ = 1, sms = 0;
-  cudaError_t e = kernel_smem_attr((const void*)k_attn<G, DENSE, MAXW>, (int)smem, L.attn_nc * 32, &occ, &sms);
+  cudaError_t e = kernel_smem_attr((const void*)k_attn<G, DENSE, MAXW, OWN>, (int)smem, L.attn_nc * 32, &occ, &sms);
   if (e != cudaSuccess) return e;
   // CTAs per (sequence, kv head) in proportion to its items: one wave of
   // CTAs when the units fit on the SMs; with more units than CTA slots (many
@@ -896,6 +1005,7 @@ cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int
     const int it = std::max(1, items[i]);
     int P = (int)std::floor((double)it / per_cta);
     P = std::max(1, std::min(P, std::min(cap, std::max(1, it / 2))));
+    if (min_parts) P = std::max(P, std::min(cap, min_parts[i]));
     p_min = std::min(p_min, P);
     p_max = std::max(p_max, P);
     split.off[i + 1] = split.off[i] + P * L.n_kv;
@@ -903,43 +1013,55 @@ cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int
   if (std::getenv("MK_LOG"))
     std::fprintf(stderr, "[mosaickv] attention: %d units, %d to %d CTAs each, %d CTAs (%d per SM), %zu B smem\n",
                  units, p_min, p_max, split.off[cs.n], occ, smem);
-  return launch_pdl(k_attn<G, DENSE, MAXW>, dim3(split.off[cs.n]), dim3(L.attn_nc * 32), smem, s, 0, L, layer, cs,
+  return launch_pdl(k_attn<G, DENSE, MAXW, OWN>, dim3(split.off[cs.n]), dim3(L.attn_nc * 32), smem, s, 0, L, layer, cs,
                     split, ids, n_sel, q, K, V, t_stride, out);
 }
 
 template <bool DENSE>
 cudaError_t launch_attn_g(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                           const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
-                          const int32_t* items, cudaStream_t s) {
+                          const int32_t* items, const int32_t* min_parts, cudaStream_t s) {
   const size_t smem = attn_smem_bytes(L, 0);
   if (smem == 0 || smem > 227 * 1024) return cudaErrorInvalidConfiguration;
   const bool wide = L.attn_nc > 12;  // launch bounds of 16 warps (at most 128 registers)
+  // The variant with rotation classes only where some unit of the call has a
+  // segment under its own rotation (its CTAs need one per class).
+  bool own = false;
+  if (!DENSE && min_parts)
+    for (int i = 0; i < cs.n; ++i) own = own || min_parts[i] > 1;
+#define MK_ATTN_CASE(GG)                                                                                         \
+  case GG:                                                                                                       \
+    if constexpr (!DENSE) {                                                                                      \
+      if (own)                                                                                                   \
+        return wide ? launch_one<GG, DENSE, 16, true>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items,   \
+                                                      min_parts, smem, s)                                        \
+                    : launch_one<GG, DENSE, 12, true>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items,   \
+                                                      min_parts, smem, s);                                       \
+    }                                                                                                            \
+    return wide ? launch_one<GG, DENSE, 16, false>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items,      \
+                                                   min_parts, smem, s)                                           \
+                : launch_one<GG, DENSE, 12, false>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items,      \
+                                                   min_parts, smem, s);
   switch (L.G) {
-    case 1:
-      return wide ? launch_one<1, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s)
-                  : launch_one<1, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s);
-    case 2:
-      return wide ? launch_one<2, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s)
-                  : launch_one<2, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s);
-    case 4:
-      return wide ? launch_one<4, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s)
-                  : launch_one<4, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s);
-    case 8:
-      return wide ? launch_one<8, DENSE, 16>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s)
-                  : launch_one<8, DENSE, 12>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, smem, s);
+    MK_ATTN_CASE(1)
+    MK_ATTN_CASE(2)
+    MK_ATTN_CASE(4)
+    MK_ATTN_CASE(8)
     default: return cudaErrorInvalidValue;
   }
+#undef MK_ATTN_CASE
 }
 }  // namespace
 
 cudaError_t launch_decode_attn(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids,
-                               const int32_t* n_sel, uint16_t* out, const int32_t* items, cudaStream_t s) {
-  return launch_attn_g<false>(L, layer, cs, ids, n_sel, nullptr, nullptr, nullptr, 0, out, items, s);
+                               const int32_t* n_sel, uint16_t* out, const int32_t* items, cudaStream_t s,
+                               const int32_t* min_parts) {
+  return launch_attn_g<false>(L, layer, cs, ids, n_sel, nullptr, nullptr, nullptr, 0, out, items, min_parts, s);
 }
 
 cudaError_t launch_dense_attn(const Layout& L, const CallSeqs& cs, const uint16_t* q, const uint16_t* K,
                               const uint16_t* V, int64_t t_stride, uint16_t* out, const int32_t* items, cudaStream_t s) {
-  return launch_attn_g<true>(L, 0, cs, nullptr, nullptr, q, K, V, t_stride, out, items, s);
+  return launch_attn_g<true>(L, 0, cs, nullptr, nullptr, q, K, V, t_stride, out, items, nullptr, s);
 }
 
 }  // namespace mk

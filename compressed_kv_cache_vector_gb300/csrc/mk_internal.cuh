@@ -35,13 +35,23 @@ struct UnitDesc {
   int32_t rot_set;
   int32_t first_block[MK_MAX_SEGMENTS];
   int32_t r[MK_MAX_SEGMENTS];
-  int32_t sflags[MK_MAX_SEGMENTS];  // per segment: bit 0 always attended; bits 8-15 channels eligible for the top-r
+  int32_t sflags[MK_MAX_SEGMENTS];  // per segment: bit 0 always attended; bit 1 stored under its own rotation
+                                    // (a re-compressed closed segment); bits 8-15 channels eligible for the top-r
 };
 static_assert(sizeof(UnitDesc) == 64, "UnitDesc is 64 bytes");
 
 __host__ __device__ inline int32_t seg_flags(bool always, int keep) { return (always ? 1 : 0) | (keep << 8); }
 __host__ __device__ inline bool seg_always(const UnitDesc& u, int s) { return (u.sflags[s] & 1) != 0; }
 __host__ __device__ inline int seg_keep(const UnitDesc& u, int s) { return (u.sflags[s] >> 8) & 0xff; }
+__host__ __device__ inline bool seg_own(const UnitDesc& u, int s) { return (u.sflags[s] & 2) != 0; }
+// Rotation class of segment s: 0 for the head's rotation, s + 1 for a
+// segment stored under its own.
+__host__ __device__ inline int seg_class(const UnitDesc& u, int s) { return seg_own(u, s) ? s + 1 : 0; }
+__host__ __device__ inline bool any_own(const UnitDesc& u) {
+  bool a = false;
+  for (int s = 0; s < u.n_seg; ++s) a = a || seg_own(u, s);
+  return a;
+}
 
 // Everything a kernel needs to find data in the arena and workspace.
 struct Layout {
@@ -54,6 +64,8 @@ struct Layout {
   int64_t off_rkp, off_rvp;     // R_k, R_v as three bf16 parts each, tensor-core operand layout
   int64_t off_meta, off_pages;
   int64_t off_cmeta;            // compressed per-block keys (meta_c > 0): [nblk_cap][cmeta_row] bytes
+  int64_t off_segrot;           // own rotations of closed segments s < n_seg - 1: [s] x {R_k^T, R_v} fp32 [128][128]
+  int32_t n_cls;                // rotation classes: 1 + closed segments (1 with a single segment)
   int32_t meta_c, cmeta_row;    // channels a compressed key keeps (0 = none), bytes per row
   int64_t page_stride;
   int32_t S, W, B, n_kv, G, max_seqs, nblk_cap, cap_tokens, n_layers, k_max;
@@ -62,7 +74,10 @@ struct Layout {
   int32_t attn_tg;              // attention: tokens per staged page group (32 or 16)
   int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, warps per CTA, stage bytes
   // workspace
-  float* qrot;                  // [n_layers][max_seqs][n_kv][G][128]: q' of each layer's last selection
+  float* qrot;                  // [n_cls][n_layers][max_seqs][n_kv][G][128]: q' of each layer's last selection,
+                                // per rotation class
+  int32_t* seg_sel;             // [n_layers][max_seqs][n_kv][MK_MAX_SEGMENTS]: selected ids below each segment's
+                                // first block (written by the top-k when a segment has its own rotation)
   uint32_t* keys;               // [max_seqs][n_kv][keys_stride]: ordered block-score keys, 0 = not a candidate
   int32_t keys_stride;          // nblk_cap rounded up to a multiple of 4
   uint32_t* khist;              // [max_seqs][n_kv][kKeyBins]: key counts by top 12 bits (zero between calls)
@@ -85,8 +100,12 @@ __host__ __device__ inline int64_t unit_index(const Layout& L, int layer, int se
   return ((int64_t)layer * L.max_seqs + seq) * L.n_kv + kvh;
 }
 // q' of (layer, sequence slot), written by the selection, read by attention.
-__host__ __device__ inline float* qrot_of(const Layout& L, int layer, int64_t slot) {
-  return L.qrot + ((int64_t)layer * L.max_seqs * L.n_kv + slot) * L.G * 128;
+__host__ __device__ inline float* qrot_of(const Layout& L, int layer, int64_t slot, int cls = 0) {
+  return L.qrot + (((int64_t)cls * L.n_layers + layer) * L.max_seqs * L.n_kv + slot) * L.G * 128;
+}
+// Own rotation of closed segment s: R_k^T then R_v, fp32 [128][128] each.
+__host__ __device__ inline int64_t segrot_off(const Layout& L, int s) {
+  return L.off_segrot + (int64_t)s * 2 * 128 * 128 * 4;
 }
 __host__ __device__ inline int n_mid_tokens(const Layout& L, int T) {
   int m = T - L.W - L.S;
@@ -358,7 +377,7 @@ cudaError_t kernel_smem_attr(const void* fn, int bytes, int threads, int* occ, i
 
 // Kernel launchers (defined in the .cu files); they return cudaGetLastError().
 cudaError_t launch_init_desc(const Layout& L, int layer, int seq, const UnitDesc& d, cudaStream_t s);
-cudaError_t launch_set_segment(const Layout& L, int64_t u, int seg, int r, int keep, cudaStream_t s);
+cudaError_t launch_set_segment(const Layout& L, int64_t u, int seg, int r, int keep, int own, cudaStream_t s);
 cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
                                 const uint16_t* v, int evict_only, cudaStream_t s);
 cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
@@ -371,15 +390,20 @@ bool topk_plan_ok(const Layout& L);
 cudaError_t launch_topk(const Layout& L, int layer, const CallSeqs& cs, int32_t* ids, int32_t* n_sel, bool append,
                         cudaStream_t s);
 // kin/vin non-null: append one new token per sequence first (fused decode
-// append, see k_select).
+// append, see k_select).  own: some unit of the call has a segment stored
+// under its own rotation (the variant that scores by rotation class).
 cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,
                                 int32_t* ids, int32_t* n_sel, float* scores_out, int max_nblk,
-                                cudaStream_t s, const uint16_t* kin = nullptr, const uint16_t* vin = nullptr);
+                                cudaStream_t s, const uint16_t* kin = nullptr, const uint16_t* vin = nullptr,
+                                bool own = false);
 // items[i]: the attention work of each (sequence i, kv head) of the call, in
 // items of up to kDenseChunk tokens (dense chunks, page groups), host array.
 // A sequence gets CTAs per kv head in proportion to its items.
+// min_parts[i] (optional): the fewest CTAs per kv head sequence i needs (one
+// per rotation class when some segment is stored under its own rotation).
 cudaError_t launch_decode_attn(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids,
-                               const int32_t* n_sel, uint16_t* out, const int32_t* items, cudaStream_t s);
+                               const int32_t* n_sel, uint16_t* out, const int32_t* items, cudaStream_t s,
+                               const int32_t* min_parts = nullptr);
 cudaError_t launch_dense_attn(const Layout& L, const CallSeqs& cs, const uint16_t* q,
                               const uint16_t* K, const uint16_t* V, int64_t t_stride,
                               uint16_t* out, const int32_t* items, cudaStream_t s);

@@ -86,7 +86,7 @@ __device__ __forceinline__ void split3(float x, uint16_t (&p)[3]) {
 // unit's last tiles afterwards (the evicted token lands in the last block);
 // the top-k kernel advances the device length.  kin/vin: [n_seqs][n_kv][128]
 // bf16.
-template <int G, bool APPEND>
+template <int G, bool APPEND, bool OWN>
 __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs cs, int P,
                                                    const uint16_t* __restrict__ q, int32_t* __restrict__ ids,
                                                    int32_t* __restrict__ n_sel, float* __restrict__ scores_out,
@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   __shared__ __align__(8) uint64_t s_tbar[kSelWarps][2];  // each warp's two meta-tile stages
   __shared__ __align__(16) uint32_t bqs[3][16][2][32];  // B fragments, staged once (then: the early last tile)
   __shared__ __align__(8) uint64_t s_lbar;            // the early last tile's copy
+  // OWN (some segment stored under its own rotation): q, and q' in each such segment's basis.
+  __shared__ float qraw[OWN ? G : 1][OWN ? D : 1];
+  __shared__ float qrc[OWN ? MK_MAX_SEGMENTS - 1 : 1][OWN ? G : 1][OWN ? D : 1];
 
   const int unit_call = blockIdx.x / P, part = blockIdx.x - unit_call * P;
   const int ci = unit_call / L.n_kv, kvh = unit_call - ci * L.n_kv;
@@ -125,8 +128,11 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     mbar_expect_tx(&s_rbar, r_bytes);
     bulk_g2s(smem, base + L.off_rkt, r_bytes, &s_rbar);
   }
-  for (int i = tid; i < G * D; i += blockDim.x)
-    qs[i % D][i / D] = bf2f(q[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D + i]);
+  for (int i = tid; i < G * D; i += blockDim.x) {
+    const float x = bf2f(q[((int64_t)ci * L.n_kv * G + (int64_t)kvh * G) * D + i]);
+    qs[i % D][i / D] = x;
+    if constexpr (OWN) qraw[i / D][i % D] = x;
+  }
   for (int i = tid; i < kKeyBins / 4; i += blockDim.x) reinterpret_cast<uint4*>(hc)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();  // the barrier's initialisation is visible before anyone waits on it
   if (!mbar_wait(&s_rbar, 0)) {
@@ -219,7 +225,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
       // unit's last tile (which holds the leaving token's block) while the
       // append runs; warp 0 then patches that block's row with the new
       // min/max it computed, instead of reading back what it wrote.
-      early = one && P > 1 && L.meta_c == 0;
+      early = one && P > 1 && L.meta_c == 0 && !(OWN && any_own(ud));
       if (early) {
         const int nb_new = n_mid_blocks(L, T_cur + 1);
         tl = (nb_new - 1) / kMT;
@@ -255,6 +261,51 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
       }
     }
     T_cur += n;
+  }
+  // Segments stored under their own rotation (re-compressed closed
+  // segments): q'_c = q R_c^T for each, R_c^T staged by one bulk copy over
+  // the (now free) first 64 KB of the tile area; part 0 keeps q'_c in the
+  // workspace for the attention.
+  const bool own = OWN && any_own(ud);
+  unsigned r_phase = 1u;
+  if (own) {
+    __syncthreads();  // the append (part 0) is done with the staged rotations
+    for (int sg = 0; sg + 1 < ud.n_seg; ++sg) {
+      if (!seg_own(ud, sg)) continue;
+      if (tid == 0) {
+        fence_proxy_async();
+        mbar_expect_tx(&s_rbar, (unsigned)(D * D * 4));
+        bulk_g2s(smem, base + segrot_off(L, sg), (unsigned)(D * D * 4), &s_rbar);
+      }
+      if (!__syncthreads_and(mbar_wait(&s_rbar, r_phase & 1u) ? 1 : 0)) {
+        if (tid == 0) set_error(L, ERR_COPY_WAIT, (int32_t)u, -6, (int32_t)MK_ETIMEOUT);
+        (void)mbar_wait(&s_rbar, r_phase & 1u);
+        return;  // no CTA of this kernel waits on another
+      }
+      ++r_phase;
+      const float* Rs = reinterpret_cast<const float*>(smem);
+      {
+        const int c = tid & (D - 1), half = tid >> 7;
+        float acc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+        for (int j = half * 64; j < half * 64 + 64; ++j) {
+          const float rr = Rs[j * D + c];
+#pragma unroll
+          for (int h = 0; h < G; ++h) acc[h] = fmaf(qraw[OWN ? h : 0][OWN ? j : 0], rr, acc[h]);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) qr[half][h][c] = acc[h];
+      }
+      __syncthreads();
+      for (int i = tid; i < G * D; i += blockDim.x) {
+        const int h = i / D, c = i % D;
+        const float v = qr[0][h][c] + qr[1][h][c];
+        if constexpr (OWN) qrc[sg][h][c] = v;
+        if (part == 0) qrot_of(L, layer, slot, sg + 1)[i] = v;
+      }
+      __syncthreads();  // the staging area is read; qr is free again
+    }
   }
   const int nblk = n_mid_blocks(L, T_cur);
   const int ntiles = (nblk + kMT - 1) / kMT;
@@ -317,7 +368,9 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   };
   const float inv_sqrt_d = 0.08838834764831845f;
   // Scores of tile t (16 dense [min | max] rows) into keys, histogram, scores.
-  auto score_tile = [&](const uint16_t* tile, int t) {
+  // Scores of tile t; with cf >= 0 only the rows whose blocks belong to
+  // rotation class cf are written.
+  auto score_tile = [&](const uint16_t* tile, int t, int cf = -1) {
     float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const int mi = lane >> 3, ri = lane & 7;
     const uint16_t* arow = tile + (ri + (mi & 1) * 8) * kMetaRow + (mi >> 1) * 8;
@@ -339,8 +392,44 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
     b_hi = fmaxf(b_hi, __shfl_xor_sync(FULL, b_hi, 2));
     if (tig == 0) {
       const int b0 = t * kMT + g, b1 = b0 + 8;
-      if (b0 < nblk) emit(b0, b_lo * inv_sqrt_d);
-      if (b1 < nblk) emit(b1, b_hi * inv_sqrt_d);
+      if (b0 < nblk && (cf < 0 || seg_class(ud, seg_of_block(ud, b0)) == cf)) emit(b0, b_lo * inv_sqrt_d);
+      if (b1 < nblk && (cf < 0 || seg_class(ud, seg_of_block(ud, b1)) == cf)) emit(b1, b_hi * inv_sqrt_d);
+    }
+  };
+  // With segments under their own rotation, a tile is scored once per
+  // rotation class among its blocks; the B fragments are rebuilt (from the
+  // class's q') when the class changes.
+  int cur_cls = 0;
+  auto build_bq = [&](int c) {
+    const int n = lane >> 2;
+#pragma unroll
+    for (int kc = 0; kc < 16; ++kc)
+#pragma unroll
+      for (int hf2 = 0; hf2 < 2; ++hf2) {
+        const int k = kc * 16 + hf2 * 8 + 2 * (lane & 3);
+        uint16_t e0[3] = {0, 0, 0}, e1[3] = {0, 0, 0};
+        if (n < G) {
+          const float a0 = (!OWN || c == 0) ? qs[k % D][n] : qrc[OWN ? c - 1 : 0][OWN ? n : 0][OWN ? k % D : 0];
+          const float a1 = (!OWN || c == 0) ? qs[(k + 1) % D][n]
+                                            : qrc[OWN ? c - 1 : 0][OWN ? n : 0][OWN ? (k + 1) % D : 0];
+          split3(k < D ? fminf(a0, 0.0f) : fmaxf(a0, 0.0f), e0);
+          split3((k + 1) < D ? fminf(a1, 0.0f) : fmaxf(a1, 0.0f), e1);
+        }
+#pragma unroll
+        for (int p3 = 0; p3 < 3; ++p3) bq[p3][kc][hf2] = (uint32_t)e0[p3] | ((uint32_t)e1[p3] << 16);
+      }
+  };
+  auto score_tile_own = [&](const uint16_t* tile, int t) {
+    const int b0 = t * kMT + g, b1 = b0 + 8;
+    const int c0 = b0 < nblk ? seg_class(ud, seg_of_block(ud, b0)) : -1;
+    const int c1 = b1 < nblk ? seg_class(ud, seg_of_block(ud, b1)) : -1;
+    for (int c = 0; c < ud.n_seg; ++c) {
+      if (!__any_sync(FULL, c0 == c || c1 == c)) continue;
+      if (c != cur_cls) {
+        build_bq(c);
+        cur_cls = c;
+      }
+      score_tile(tile, t, c);
     }
   };
   if (early && warp == 0) score_tile(lt, tl);
@@ -371,12 +460,13 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
         const unsigned char* crow = cst + row * L.cmeta_row;
         const uint16_t* cv = reinterpret_cast<const uint16_t*>(crow);
         const int j0 = hf ? (mc + 1) / 2 : 0, j1 = hf ? mc : (mc + 1) / 2;
+        const int rc = own ? seg_class(ud, seg_of_block(ud, t * kMT + row)) : 0;
         for (int j = j0; j < j1; ++j) {
           const float mn = bf2f(cv[j]), mx = bf2f(cv[mc + j]);
           const int ch = crow[4 * mc + j];
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float qv = qs[ch][h];
+            const float qv = (!OWN || rc == 0) ? qs[ch][h] : qrc[OWN ? rc - 1 : 0][OWN ? h : 0][OWN ? ch : 0];
             acc[h] += fmaxf(qv * mn, qv * mx);
           }
         }
@@ -385,6 +475,8 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
 #pragma unroll
       for (int h = 0; h < G; ++h) sc = fmaxf(sc, acc[h] + __shfl_xor_sync(FULL, acc[h], 16));
       if (hf == 0 && row < nrow) emit(t * kMT + row, sc * inv_sqrt_d);
+    } else if (own) {
+      score_tile_own(tile, t);
     } else {
       score_tile(tile, t);
     }
@@ -410,7 +502,7 @@ bool select_plan_ok(const Layout& L) { return topk_plan_ok(L); }
 
 cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* q,
                                 int32_t* ids, int32_t* n_sel, float* scores_out, int max_nblk,
-                                cudaStream_t s, const uint16_t* kin, const uint16_t* vin) {
+                                cudaStream_t s, const uint16_t* kin, const uint16_t* vin, bool own) {
   const int units = cs.n * L.n_kv;
   const int tiles = (max_nblk + kMT - 1) / kMT;
   int P = std::max(1, 152 / units);
@@ -422,7 +514,8 @@ cudaError_t launch_block_select(const Layout& L, int layer, const CallSeqs& cs, 
   const bool append = kin != nullptr;
 #define MK_SEL_CASE(GG)                                                                                       \
   case GG: {                                                                                                  \
-    auto kern = append ? k_select<GG, true> : k_select<GG, false>;                                             \
+    auto kern = append ? (own ? k_select<GG, true, true> : k_select<GG, true, false>)                       \
+                       : (own ? k_select<GG, false, true> : k_select<GG, false, false>);                                             \
     cudaError_t e = kernel_smem_attr((const void*)kern, dyn, 256, nullptr, nullptr);                           \
     if (e != cudaSuccess) return e;                                                                            \
     e = launch_pdl(kern, grid, dim3(256), dyn, s, 0, L, layer, cs, P, q, ids, n_sel, scores_out,   \

@@ -315,6 +315,26 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
     }
   }
   if (part == 0 && tid == 0) n_sel[(int64_t)ci * L.n_kv + kvh] = k;
+  // With segments stored under their own rotation, part 0 also records where
+  // each segment's ids start in the ids row (the ids taken below its first
+  // block): the attention gives each rotation its own CTAs.
+  if (part == 0 && any_own(ud)) {
+    int32_t* dst = L.seg_sel + (((int64_t)layer * L.max_seqs + seq) * L.n_kv + kvh) * MK_MAX_SEGMENTS;
+    for (int sgi = 0; sgi < MK_MAX_SEGMENTS; ++sgi) {
+      const int bnd = sgi < ud.n_seg ? min(ud.first_block[sgi], nblk) : nblk;
+      int g0 = 0, e0 = 0;
+      for (int c = tid; 4 * c < bnd; c += kTkThreads) {
+        uint32_t gm, em;
+        masks(c, gm, em);
+        const uint32_t below = 4 * c + 4 <= bnd ? 0xfu : (1u << (bnd - 4 * c)) - 1u;
+        g0 += __popc(gm & below);
+        e0 += __popc(em & below);
+      }
+      const int2 ex = block_excl_scan2_1024(g0, e0, wsum);
+      if (tid == kTkThreads - 1) dst[sgi] = ex.x + g0 + min(ex.y + e0, need);
+      __syncthreads();
+    }
+  }
 }
 
 bool topk_plan_ok(const Layout& L) { return (L.nblk_cap + 3) / 4 <= kTkThreads * kTkRoundsMax; }

@@ -331,8 +331,8 @@ mk_status mk_alg2_segment_r(const void* seg, int64_t s, int64_t row_stride, int3
  * re-compresses the segment's tokens exactly (fp64 rotation, rounded once to
  * bf16), possibly under a new strategy (channel count r, truncation), and the
  * result replaces the GPU's version in the arena, stream-ordered and without
- * blocking the host.  Here a segment keeps the head's rotation; per-segment
- * rotations are not supported. */
+ * blocking the host.  The segment may keep the head's rotation or take its
+ * own (the per-segment SVD of [N] Fig. 4). */
 
 /* Packs n_blocks complete blocks of `block` tokens on the host, in the
  * arena's formats.  k, v: the blocks' raw (unrotated) bf16 rows, row i at
@@ -354,16 +354,24 @@ mk_status mk_host_pack_blocks(const float* R_k, const float* R_v, const void* k,
 /* Replaces strategy segment `segment` of one (layer, sequence, kv head) with
  * pages, meta (and cmeta) packed by mk_host_pack_blocks for all of its blocks
  * (mk_layout gives the segment's first blocks), under channel count r and
- * truncation keep_channels from then on.  The segment must be closed: not the
- * last one, which still receives appends.  r may not exceed the largest r of
- * the configuration (the page capacity).  Host copies and a descriptor update
- * are enqueued on `stream`; the host buffers must stay valid until they run
- * (pinned memory makes the copies asynchronous).  MK_EINVAL: bad ids, a null
- * buffer, r or keep_channels out of range; MK_ESTATE: the sequence has no
- * prefill yet, or the segment is the last or empty. */
+ * truncation keep_channels from then on.  R_k, R_v: NULL when the pages were
+ * packed with the head's rotations; else the segment's own rotations (host
+ * fp32 [128][128], rows = eigenvectors of the segment's own K^T K and V^T V by
+ * descending eigenvalue, the per-segment SVD of [N] Fig. 4), which the pages
+ * were packed with: from then on the segment's blocks are scored with the
+ * query rotated by its R_k and their weighted values un-rotated by its R_v.
+ * The rotations are copied before the call returns (from pageable memory,
+ * after the stream's earlier work); the pages, meta and cmeta copies and the
+ * descriptor update are enqueued on `stream`, and those host buffers must stay
+ * valid until they run (pinned memory makes the copies asynchronous).  The
+ * segment must be closed: not the last one, which still receives appends.  r
+ * may not exceed the largest r of the configuration (the page capacity).
+ * MK_EINVAL: bad ids, a null buffer, only one of R_k and R_v, r or
+ * keep_channels out of range; MK_ESTATE: the sequence has no prefill yet, or
+ * the segment is the last or empty; MK_ENOTSUP: uncompressed pages. */
 mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, int32_t segment, int32_t r,
-                          int32_t keep_channels, const void* pages, const void* meta, const void* cmeta,
-                          mk_stream stream);
+                          int32_t keep_channels, const float* R_k, const float* R_v, const void* pages,
+                          const void* meta, const void* cmeta, mk_stream stream);
 
 /* Waits for the device and reads the sticky error word: MK_OK, MK_EDEVICE or
  * MK_ETIMEOUT; *detail (optional) receives the kernel's detail code. */

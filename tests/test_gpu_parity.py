@@ -466,3 +466,91 @@ def test_append_select_equals_separate_calls(case):
                 n_live = min(B, mid - blk * B)
                 for g, w_ in zip(page_rows(pa[blk], B, r, n_live), page_rows(pb[blk], B, r, n_live)):
                     assert np.array_equal(g, w_), (s, h, blk)
+
+
+@pytest.mark.parametrize("segments,swaps", [
+    ([(0, 32, 0), (600, 32, 0)], [(0, 20, 96)]),
+    ([(0, 32, 0), (350, 64, 1), (650, 32, 0)], [(0, 24, 0), (1, 48, 0)]),
+], ids=["scored-segment", "scored-and-always-segments"])
+def test_swap_segments_under_their_own_rotation(segments, swaps):
+    """[S] sec. 5.4 with the per-segment SVD of [N] Fig. 4: closed segments
+    re-compressed on the host under their own rotations (eigenvectors of the
+    segment's own K^T K and V^T V) and a new r replace the GPU's version.  The
+    stored bytes then equal the oracle's re-compression; the scores use the
+    query rotated into each block's basis, and attention un-rotates each
+    basis's values by its own R_v (each rotation gets its own CTAs)."""
+    from compressed_kv_cache_vector_gb300 import binding, synth
+    # Head rotations exact in bf16 (signed permutations), so the GPU-rotated
+    # rows match the oracle bit for bit; the segments' own rotations are
+    # general (eigenvectors), packed exactly on the host as the oracle does.
+    case = Case(n_q=4, n_kv=2, seq_lens=[3000, 1800], rot="perm", block=32, window=64, segments=segments,
+                steps=[1] * 4, seed=41)
+    p = Pair(case)
+    for n in case.steps[:3]:
+        p.step(n)
+    S, B = case.n_sink, case.block
+    for (l, s, h) in p.units:
+        lay = p.mk.layout(l, s, h)
+        fb = lay["seg_first_block"]
+        Kraw = synth.bf16_values(p.K[(l, s, h)])
+        Vraw = synth.bf16_values(p.V[(l, s, h)])
+        for seg, r_new, keep in swaps:
+            rows = slice(S + fb[seg] * B, S + fb[seg + 1] * B)
+            Rk_s = O.rotation_from_keys(Kraw[rows])[0].astype(np.float32)
+            Rv_s = O.rotation_from_keys(Vraw[rows])[0].astype(np.float32)
+            pages, meta, _ = binding.host_pack_blocks(Rk_s, Rv_s, p.K[(l, s, h)][rows].cpu(),
+                                                      p.V[(l, s, h)][rows].cpu(), B, r_new, keep, lay["page_stride"])
+            p.mk.swap_segment(l, s, h, seg, r_new, keep, pages, meta, R_k=Rk_s, R_v=Rv_s)
+            torch.cuda.synchronize()
+            p.orc[(l, s, h)].recompress_segment(seg, Kraw, Vraw, r_new, keep, Rk_s.astype(np.float64),
+                                                Rv_s.astype(np.float64))
+    assert p.mk.poll_error() == (0, 0)
+    for u in p.units:
+        _check_storage(p, u)
+    # one more decode step through the fused call, then select and attend
+    seqs = [0, 1]
+    k = torch.stack([torch.stack([p.K[(0, s, h)][p.T[s]] for h in range(2)]) for s in seqs]).contiguous()
+    v = torch.stack([torch.stack([p.V[(0, s, h)][p.T[s]] for h in range(2)]) for s in seqs]).contiguous()
+    q = p.query(9)
+    p.mk.append_select(0, seqs, k, v, q)
+    for (l, s, h), oc in p.orc.items():
+        t = p.T[s]
+        oc.append(synth.bf16_values(p.K[(l, s, h)][t:t + 1]), synth.bf16_values(p.V[(l, s, h)][t:t + 1]))
+    for s in seqs:
+        p.T[s] += 1
+    q = p.query(10)
+    scores = torch.full((2, 2, p.mk.nblk_cap), float("nan"), dtype=torch.float32, device="cuda")
+    ids, n_sel = p.mk.block_select(0, seqs, q, scores=scores)
+    out = p.mk.decode_attn(0, seqs, ids, n_sel)
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    ids, n_sel = ids.cpu().numpy(), n_sel.cpu().numpy()
+    out, scores = out.cpu().to(torch.float64).numpy(), scores.cpu().numpy()
+    G = case.G
+    near = 0
+    for (l, s, h), oc in p.orc.items():
+        qs = q[s, h * G:(h + 1) * G].cpu().to(torch.float64).numpy()
+        cand = oc.candidates()
+        kk = O.n_select(len(cand), oc.st)
+        assert n_sel[s, h] == kk
+        per, grp = oc.scores(qs)
+        mn, mx = oc.score_keys()
+        nb = oc.n_blocks_mid()
+        tol = np.zeros(nb)
+        for b in range(nb):   # the fp32 bound of each block in its own basis
+            Rq = oc.rotations_of_block(b)[0]
+            tol[b] = score_tolerance(qs @ Rq.T, mn[b:b + 1], mx[b:b + 1])[0]
+        got_s = scores[s, h, :nb].astype(np.float64)
+        assert np.all(np.abs(got_s[cand] - grp[cand]) <= tol[cand]), (s, h)
+        got_ids = ids[s, h, :kk]
+        assert np.array_equal(got_ids, O.topk_blocks(got_s, cand, kk))
+        want_ids, _ = oc.select(qs)
+        if not np.array_equal(got_ids, want_ids):
+            srt = np.sort(grp[cand])[::-1]
+            assert srt[kk - 1] - srt[kk] <= 2 * tol.max()
+            near += 1
+        want = oc.attention(qs, got_ids)
+        for g in range(G):
+            assert rel_l2(out[s, h * G + g], want[g]) <= ATOL_REL, (s, h, g)
+    assert near <= 1
+
