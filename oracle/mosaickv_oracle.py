@@ -36,6 +36,10 @@ Readings where the pages are silent:
     begin_permille/1000 of the prefill length; the last one is open-ended;
   * decode append: the new token enters the window; the window's oldest
     token, once more than W are held, moves into the middle;
+  * sec. 5.1 bitmap (off by default): the indices are replaced by a bitmap
+    of d / g bits per vector, one bit per group of g adjacent channels; for
+    g > 1 the vector keeps the r / g groups of largest energy (fp32, summed
+    in channel order), ties to the lower group;
   * sec. 5.2 variants (off by default): "bottom channels truncated" = the
     per-vector top-r picks among the first keep_channels rotated channels
     only; "per-block keys channel-compressed" = each block keeps the m
@@ -137,6 +141,59 @@ def topr_select(X, r, keep=None):
     return idx.astype(np.uint8), vals
 
 
+def group_energy_f32(X, g):
+    """Energy of each group of g adjacent channels, sum_c x_c^2 over the group,
+    accumulated from the group's first channel to its last with every product
+    and every sum rounded to fp32: the precision the kernels decide the grouped
+    selection in (the bf16 inputs make each square exact in fp32).
+    X: [n, d]; returns float32 [n, d // g]."""
+    X32 = np.asarray(X, dtype=np.float32)
+    n, d = X32.shape
+    Xg = X32.reshape(n, d // g, g)
+    e = (Xg[:, :, 0] * Xg[:, :, 0]).astype(np.float32)
+    for i in range(1, g):
+        e = (e + (Xg[:, :, i] * Xg[:, :, i]).astype(np.float32)).astype(np.float32)
+    return e
+
+
+def topr_groups(X, r, g, keep=None):
+    """Per-vector top-r in groups of g adjacent channels ([S] sec. 5.1: a
+    variable-granularity bitmap has one bit per group of adjacent elements,
+    so the vector keeps whole groups; [S] sec. 4.3 lists the element-group
+    size in each segment's strategy).
+
+    g = 1 is the per-element top-r of [N] Eq. (9) (topr_select).  For g > 1
+    the r / g groups with the largest energy are kept (the grouped form of the
+    energy the top-r retains, [N] Eq. (5)), ties to the lower group; with
+    `keep` (a multiple of g) only the first keep / g groups are candidates.
+    Returns (idx uint8 [n, r], vals float64 [n, r]) in ascending channel order,
+    as topr_select does.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    if X.ndim == 1:
+        X = X[None, :]
+    if g == 1:
+        return topr_select(X, r, keep)
+    d = X.shape[1]
+    keep = d if keep is None else keep
+    assert r % g == 0 and keep % g == 0 and r <= keep
+    e = group_energy_f32(X, g)[:, :keep // g]
+    groups = np.sort(np.argsort(-e, axis=1, kind="stable")[:, :r // g], axis=1)
+    idx = (groups[:, :, None] * g + np.arange(g)[None, None, :]).reshape(X.shape[0], r)
+    vals = np.take_along_axis(X, idx, axis=1)
+    return idx.astype(np.uint8), vals
+
+
+def bitmap_bytes(idx, g, d=D_HEAD):
+    """Position bitmap of [S] sec. 5.1 for kept channels idx [n, r]: d / g bits
+    per vector, bit j set when group j (channels g j .. g j + g - 1) is kept;
+    bit j lives in byte j // 8 at bit j % 8.  Returns uint8 [n, d // g // 8]."""
+    idx = np.asarray(idx, dtype=np.int64)
+    bits = np.zeros((idx.shape[0], d // g), dtype=np.uint8)
+    np.put_along_axis(bits, idx // g, 1, axis=1)
+    return np.packbits(bits, axis=1, bitorder="little")
+
+
 def global_mask_energy(Xp, r):
     """ThinK-style shared mask by channel energy sum_i x_ij^2 (contrast only)."""
     e = np.sum(np.asarray(Xp, dtype=np.float64) ** 2, axis=0)
@@ -169,6 +226,8 @@ class Strategy:
     topk_fixed: int = 0
     retain_permille: int = 0
     meta_channels: int = 0    # > 0: channel-compressed per-block keys ([S] sec. 5.2)
+    bitmap_group: int = 0     # 0: uint8 channel indices; g >= 1: the D-bit (g = 1) or
+                              # grouped (one bit per g channels) bitmap of [S] sec. 5.1
 
     def __post_init__(self):
         # keep_channels: the first channels eligible for the top-r; 0 or
@@ -393,7 +452,7 @@ class OracleCache:
             r, keep = self.r_of_block(int(b)), self.keep_of_block(int(b))
             for src, dst_idx, dst_val, dense in ((self.Kr, self.kidx, self.kval, self.Kt),
                                                 (self.Vr, self.vidx, self.vval, self.Vt)):
-                idx, vals = topr_select(src[sel].astype(np.float64), r, keep)
+                idx, vals = topr_groups(src[sel].astype(np.float64), r, max(1, self.st.bitmap_group), keep)
                 dst_idx[sel, :r] = idx
                 dst_idx[sel, r:] = 0
                 dst_val[sel, :r] = vals
@@ -419,7 +478,7 @@ class OracleCache:
         begin, _, always, _ = segs[seg]
         segs[seg] = (begin, r, always, keep if keep else self.d)
         self.st = Strategy(self.st.n_sink, self.st.window, self.st.block, segs, self.st.topk_fixed,
-                           self.st.retain_permille, self.st.meta_channels)
+                           self.st.retain_permille, self.st.meta_channels, self.st.bitmap_group)
         if Rk is not None:
             self.seg_rot[seg] = (np.asarray(Rk, dtype=np.float64), np.asarray(Rv, dtype=np.float64))
         Rk_s, Rv_s = self.seg_rot.get(seg, (self.Rk, self.Rv))
@@ -452,23 +511,32 @@ class OracleCache:
         return self.mn[:nb].astype(np.float64), self.mx[:nb].astype(np.float64)
 
     def page_bytes(self, b):
-        """The packed page of block b: [Kval B*r bf16][Kidx B*r u8][Vval B*r bf16][Vidx B*r u8].
+        """The packed page of block b: [Kval B*r bf16][Kpos][Vval B*r bf16][Vpos].
 
+        Pos is B*r uint8 channel indices (the build's default contract), or
+        with bitmap_group g the B bitmaps of d / g bits ([S] sec. 5.1).
         Slots past the last live token are zero ([S] sec. 5.1 contiguous
-        packing; uint8 indices as the build's contract).
+        packing).
         """
         B = self.st.block
         r = self.r_of_block(b)
+        g = self.st.bitmap_group
         lo, hi = self.block_tokens(b)
-        kv = np.zeros((B, r), dtype=np.uint16)
-        ki = np.zeros((B, r), dtype=np.uint8)
-        vv = np.zeros((B, r), dtype=np.uint16)
-        vi = np.zeros((B, r), dtype=np.uint8)
         n = hi - lo
+        kv = np.zeros((B, r), dtype=np.uint16)
+        vv = np.zeros((B, r), dtype=np.uint16)
         kv[:n] = bf16_bits(self.kval[lo:hi, :r])
-        ki[:n] = self.kidx[lo:hi, :r]
         vv[:n] = bf16_bits(self.vval[lo:hi, :r])
-        vi[:n] = self.vidx[lo:hi, :r]
+        if g:
+            ki = np.zeros((B, self.d // g // 8), dtype=np.uint8)
+            vi = np.zeros_like(ki)
+            ki[:n] = bitmap_bytes(self.kidx[lo:hi, :r], g, self.d)
+            vi[:n] = bitmap_bytes(self.vidx[lo:hi, :r], g, self.d)
+        else:
+            ki = np.zeros((B, r), dtype=np.uint8)
+            vi = np.zeros((B, r), dtype=np.uint8)
+            ki[:n] = self.kidx[lo:hi, :r]
+            vi[:n] = self.vidx[lo:hi, :r]
         return np.concatenate([kv.reshape(-1).view(np.uint8), ki.reshape(-1),
                                vv.reshape(-1).view(np.uint8), vi.reshape(-1)])
 
@@ -621,6 +689,8 @@ def meta_overhead(block, d=D_HEAD, elem_bytes=2):
     return (2 * d * elem_bytes) / (2 * block * d * elem_bytes)
 
 
-def packed_bytes_per_token(r):
-    """K and V: r bf16 values plus r uint8 indices each."""
-    return 2 * (2 * r + r)
+def packed_bytes_per_token(r, bitmap_group=0, d=D_HEAD):
+    """K and V: r bf16 values plus r uint8 indices each, or with a bitmap of
+    d / g bits in place of the indices ([S] sec. 5.1)."""
+    pos = d // bitmap_group // 8 if bitmap_group else r
+    return 2 * (2 * r + pos)

@@ -606,3 +606,171 @@ def test_recompress_with_head_rotation_reproduces_the_cache():
     b.recompress_segment(0, K, V, 38)
     for name in ("Kr", "Vr", "Kt", "Vt", "kidx", "vidx", "kval", "vval", "mn", "mx"):
         assert np.array_equal(getattr(a, name), getattr(b, name)), name
+
+
+# ----------------------------------------- bitmap format ([S] sec. 5.1) ----
+def _brute_groups(x, r, g):
+    """Exact-arithmetic brute force: of all sets of r / g groups, the first (in
+    lexicographic order of sorted group ids) with the largest kept energy."""
+    e = [sum(float(v) * float(v) for v in x[j * g:(j + 1) * g]) for j in range(len(x) // g)]
+    best, best_e = None, -1.0
+    for S in itertools.combinations(range(len(e)), r // g):
+        tot = sum(e[j] for j in S)
+        if tot > best_e:
+            best, best_e = S, tot
+    return [j * g + i for j in best for i in range(g)]
+
+
+def test_grouped_topr_brute_force_with_ties():
+    # Small integers: every energy is exact in fp32, ties are frequent.
+    rng = np.random.default_rng(31)
+    for _ in range(400):
+        g = int(rng.choice([2, 4]))
+        n_groups = int(rng.integers(2, 6))
+        d = g * n_groups
+        r = g * int(rng.integers(1, n_groups + 1))
+        x = rng.integers(-3, 4, size=d).astype(np.float64)
+        idx, vals = O.topr_groups(x, r, g)
+        want = _brute_groups(x, r, g)
+        assert list(idx[0]) == want
+        assert np.array_equal(vals[0], x[want])
+
+
+def test_grouped_topr_with_one_nonzero_per_group_is_the_element_top_r():
+    # A group holding a single nonzero element has energy x^2, so taking the
+    # r / g best groups is the element top-(r / g) of [N] Eq. (9) by |x|.
+    rng = np.random.default_rng(32)
+    for g in (2, 4, 8):
+        for _ in range(50):
+            x = np.zeros(128)
+            pos = np.arange(0, 128, g) + rng.integers(0, g, size=128 // g)
+            x[pos] = O.bf16_round(rng.standard_normal(128 // g))
+            r = g * int(rng.integers(1, 128 // g + 1))
+            idx, _ = O.topr_groups(x, r, g)
+            el, _ = O.topr_select(x, r // g)
+            assert list(np.unique(idx[0] // g)) == sorted((el[0] // g).tolist())
+
+
+def test_grouped_topr_truncation_and_energy_bounds():
+    rng = np.random.default_rng(33)
+    X = O.bf16_round(rng.standard_normal((40, 128)) * np.exp(-0.03 * np.arange(128)))
+    for g, r, keep in ((2, 38, 96), (4, 40, 96), (8, 32, 128)):
+        idx, _ = O.topr_groups(X, r, g, keep)
+        assert idx.max() < keep
+        el, _ = O.topr_select(X, r, keep)
+        for i in range(X.shape[0]):
+            got = np.sum(X[i, idx[i]] ** 2)
+            # whole groups only, so at most the element top-r's energy
+            assert got <= np.sum(X[i, el[i]] ** 2) * (1 + 1e-12)
+            groups = np.unique(idx[i] // g)
+            assert len(groups) == r // g and np.array_equal(np.sort(idx[i]), idx[i])
+            e = [np.sum(X[i, j * g:(j + 1) * g] ** 2) for j in range(keep // g)]
+            # every kept group's energy is at least every dropped group's
+            dropped = [e[j] for j in range(keep // g) if j not in groups]
+            assert min(e[j] for j in groups) >= max(dropped) * (1 - 1e-6)
+
+
+def test_group_energy_is_fp32_in_channel_order():
+    # 4096^2 = 2^24: adding 1 in fp32 rounds back to 2^24 (ties to even), so
+    # [4096, 1, 1, 0] sums to 2^24 while [1, 1, 4096, 0] sums to 2^24 + 2.
+    e = O.group_energy_f32(np.array([[4096.0, 1, 1, 0, 1, 1, 4096, 0]]), 4)
+    assert e[0, 0] == 2.0 ** 24 and e[0, 1] == 2.0 ** 24 + 2
+    # The decision follows fp32: groups [4096, 1, 0, 0] and [4096, 1, 1, 0]
+    # both sum to 2^24, so the lower group wins, where exact sums would take
+    # the upper one.
+    x = np.array([4096.0, 1, 0, 0, 4096, 1, 1, 0])
+    assert list(O.topr_groups(x, 4, 4)[0][0]) == [0, 1, 2, 3]
+    assert _brute_groups(x, 4, 4) == [4, 5, 6, 7]
+
+
+def test_bitmap_bytes_hand_cases_and_round_trip():
+    bm = O.bitmap_bytes(np.array([[0, 1, 33, 127]]), 1)
+    want = np.zeros(16, dtype=np.uint8)
+    want[0], want[4], want[15] = 0x03, 0x02, 0x80
+    assert np.array_equal(bm[0], want)
+    bm = O.bitmap_bytes(np.array([[0, 1, 2, 3, 124, 125, 126, 127]]), 4)
+    assert list(bm[0]) == [0x01, 0, 0, 0x80]
+    bm = O.bitmap_bytes(np.array([[8, 9, 10, 11, 12, 13, 14, 15]]), 8)
+    assert list(bm[0]) == [0x02, 0]
+    rng = np.random.default_rng(34)
+    for g in (1, 2, 4, 8):
+        X = O.bf16_round(rng.standard_normal((20, 128)))
+        idx, _ = O.topr_groups(X, 8 * g, g)
+        bm = O.bitmap_bytes(idx, g)
+        assert bm.shape == (20, 16 // g)
+        bits = np.unpackbits(bm, axis=1, bitorder="little")
+        for i in range(20):
+            assert np.array_equal(np.flatnonzero(bits[i]), np.unique(idx[i] // g))
+
+
+def test_bitmap_page_byte_layout():
+    # [Kval B*r][K bitmaps B*d/g/8][Vval B*r][V bitmaps]; g = 2, r = 2.
+    st = O.Strategy(0, 1, 16, [(0, 2, 0)], bitmap_group=2)
+    c = O.OracleCache(st, 64)
+    c.set_rotation(np.eye(128), np.eye(128))
+    K = np.zeros((5, 128))
+    V = np.zeros((5, 128))
+    K[0, 6], K[0, 7], K[0, 100] = 1.5, -2.0, 0.25       # group 3 (energy 6.25) beats group 50
+    V[0, 126], V[0, 127] = 3.0, -1.0                     # group 63
+    c.append(K, V)
+    pg = c.page_bytes(0)
+    assert pg.size == 16 * (4 * 2 + 2 * 8)
+    kv = pg[:64].view(np.uint16).reshape(16, 2)
+    kb = pg[64:192].reshape(16, 8)
+    vv = pg[192:256].view(np.uint16).reshape(16, 2)
+    vb = pg[256:384].reshape(16, 8)
+    assert list(O.bits_to_value(kv[0])) == [1.5, -2.0] and list(kb[0]) == [0x08, 0, 0, 0, 0, 0, 0, 0]
+    assert list(O.bits_to_value(vv[0])) == [3.0, -1.0] and list(vb[0]) == [0, 0, 0, 0, 0, 0, 0, 0x80]
+    assert list(kb[1]) == [1, 0, 0, 0, 0, 0, 0, 0]       # all-zero token: ties keep group 0
+    assert not kb[4:].any() and not kv[4:].any()          # unused slots are zero
+    assert O.packed_bytes_per_token(38, 1) == 2 * (76 + 16)
+    assert O.packed_bytes_per_token(40, 4) == 2 * (80 + 4)
+
+
+@pytest.mark.parametrize("g", [1, 4])
+def test_bitmap_cache_rows_and_attention_by_explicit_sums(g):
+    # The zero-filled rows hold each token's kept groups; attention read from
+    # the page bytes (decoding the bitmaps by hand) equals the oracle's.
+    st = O.Strategy(4, 32, 16, [(0, 40, 0), (500, 16, 0)], 0, 100, bitmap_group=g)
+    c, _, _ = _cache(700, st, 71)
+    for t in range(4, 4 + c.n_mid, 5):
+        r = c.r_of_block((t - 4) // 16)
+        for rows, dense in ((c.Kr, c.Kt), (c.Vr, c.Vt)):
+            x = rows[t].astype(np.float64)
+            if g > 1:   # a Python sort of scalar fp32 energies, ties to the lower group
+                e = []
+                for j in range(128 // g):
+                    acc = np.float32(0.0)
+                    for i in range(g):
+                        acc = np.float32(acc + np.float32(x[j * g + i]) * np.float32(x[j * g + i]))
+                    e.append(acc)
+                best = sorted(sorted(range(128 // g), key=lambda j: (-e[j], j))[:r // g])
+                keep = [j * g + i for j in best for i in range(g)]
+            else:
+                keep = sorted(sorted(range(128), key=lambda j: (-abs(x[j]), j))[:r])
+            z = np.zeros(128)
+            z[keep] = x[keep]
+            assert np.array_equal(dense[t].astype(np.float64), z)
+    # decode every page by hand and compare with Kt / Vt
+    nb = 16 // g
+    for b in range(c.n_blocks_mid()):
+        r = c.r_of_block(b)
+        lo, hi = c.block_tokens(b)
+        pg = c.page_bytes(b)
+        Br = 16 * r
+        parts = [(pg[:2 * Br], pg[2 * Br:2 * Br + 16 * nb], c.Kt),
+                 (pg[2 * Br + 16 * nb:4 * Br + 16 * nb], pg[4 * Br + 16 * nb:], c.Vt)]
+        for vals_b, bm_b, dense in parts:
+            vals = O.bits_to_value(vals_b.view(np.uint16).reshape(16, r))
+            bms = bm_b.reshape(16, nb)
+            for t in range(hi - lo):
+                row = np.zeros(128)
+                k = 0
+                for byte in range(nb):
+                    for bit in range(8):
+                        if bms[t, byte] >> bit & 1:
+                            j = 8 * byte + bit
+                            row[j * g:(j + 1) * g] = vals[t, k:k + g]
+                            k += g
+                assert k == r
+                assert np.array_equal(row, dense[lo + t].astype(np.float64))
