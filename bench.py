@@ -72,6 +72,8 @@ def parse():
     ap.add_argument("--dense-ref", action="store_true", help="also time the uncompressed reference kernel")
     ap.add_argument("--no-quest", action="store_true", help="skip the Quest comparator (uncompressed pages)")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling runs)")
+    ap.add_argument("--bitmap", type=int, default=0, choices=[0, 1, 2, 4, 8],
+                    help="bitmap pages with this element-group size instead of uint8 indices")
     ap.add_argument("--meta-channels", type=int, default=0,
                     help="variant: channel-compressed per-block keys keeping this many channels")
     ap.add_argument("--separate", action="store_true",
@@ -95,7 +97,7 @@ def unit_bytes(wl, T, firsts):
         lo, hi = min(bounds[i], nblk), min(bounds[i + 1] if i + 1 < len(segs) else nblk, nblk)
         n = max(0, hi - lo)
         if always:
-            always_bytes += n * 6 * B * r
+            always_bytes += n * B * page_row(wl, r)
         else:
             scored += n
             r_scored = r
@@ -107,10 +109,18 @@ def unit_bytes(wl, T, firsts):
     mc = getattr(wl, "meta_channels", 0)
     key_row = (5 * mc + 15) // 16 * 16 if mc else 2 * D * 2   # a block's key as the scoring reads it
     sel = nblk * key_row + G * D * 2 + D * D * 4
-    attn = k * 6 * B * r_scored + always_bytes + dense * 2 * D * 2 + D * D * 4 + G * D * (4 + 2)
+    attn = k * B * page_row(wl, r_scored) + always_bytes + dense * 2 * D * 2 + D * D * 4 + G * D * (4 + 2)
     r_new = segs[-1][1]
-    app = 2 * D * 2 + 2 * D * D * 4 + 2 * D * 2 + 2 * D * 2 + 6 * r_new + 2 * 2 * D * 2 + (key_row if mc else 0)
+    app = (2 * D * 2 + 2 * D * D * 4 + 2 * D * 2 + 2 * D * 2 + page_row(wl, r_new) + 2 * 2 * D * 2 +
+           (key_row if mc else 0))
     return {"append": app, "select": sel, "attn": attn}
+
+
+def page_row(wl, r):
+    """Packed bytes of one token (K and V): r bf16 values each plus r uint8
+    indices each, or a bitmap of 128 / g bits each in the bitmap format."""
+    g = getattr(wl, "elem_group", 0)
+    return 2 * (2 * r + (D // g // 8 if g else r))
 
 
 def segment_firsts(wl, T0):
@@ -194,7 +204,7 @@ def _oracle_unit(job):
     Rk, _ = O.rotation_from_keys(K[:T0])
     Rv, _ = O.rotation_from_keys(V[:T0])
     st = O.Strategy(wl.n_sink, wl.window, wl.block, list(wl.segments), wl.topk_fixed, wl.retain_permille,
-                    wl.meta_channels)
+                    wl.meta_channels, wl.elem_group)
     oc = O.OracleCache(st, T0 + n_extra)
     oc.set_rotation(Rk, Rv)
     oc.append(K[:T0], V[:T0])
@@ -266,7 +276,7 @@ def build_gpu(wl, dev, rank, capacity_extra, quest=False):
     cfg = binding.make_config(wl.n_q_heads, wl.n_kv_heads, wl.n_layers, wl.n_seqs,
                               max(wl.seq_lens) + capacity_extra, wl.n_sink, wl.window, wl.block,
                               segments, wl.topk_fixed, wl.retain_permille, 0 if quest else wl.meta_channels,
-                              1 if quest else 0)
+                              1 if quest else (2 if wl.elem_group else 0), 0 if quest else wl.elem_group)
     mk = binding.MosaicKV(cfg, dev)
     eye = np.eye(D, dtype=np.float32)
     seqs = list(range(wl.n_seqs))
@@ -345,6 +355,12 @@ def main():
     if a.meta_channels:
         wl.meta_channels = a.meta_channels
         wl.name += f"-keys{a.meta_channels}ch"
+    if a.bitmap:
+        # Bitmap pages with element group g: each r rounded up to a multiple of g.
+        g = a.bitmap
+        wl.elem_group = g
+        wl.segments = [(sg[0], (sg[1] + g - 1) // g * g) + tuple(sg[2:]) for sg in wl.segments]
+        wl.name += f"-bitmap-g{g}-r{'-'.join(str(sg[1]) for sg in wl.segments)}"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

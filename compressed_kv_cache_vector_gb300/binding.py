@@ -21,6 +21,7 @@ HEADER = os.path.join(PKG, "..", "include", "mosaickv.h")
 MK_HEAD_DIM = 128
 MK_MAX_SEGMENTS = 4
 MK_MAX_SPLITS = 64
+MK_PAGES_PACKED, MK_PAGES_DENSE, MK_PAGES_BITMAP = 0, 1, 2
 STATUS = {0: "MK_OK", 1: "MK_EINVAL", 2: "MK_ENOMEM", 3: "MK_ESTATE", 4: "MK_ECUDA",
           5: "MK_EDEVICE", 6: "MK_ETIMEOUT", 7: "MK_ENOTSUP"}
 c_i32, c_i64, c_size, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
@@ -41,7 +42,7 @@ class MkConfig(ctypes.Structure):
                 ("max_seqs", c_i32), ("max_tokens", c_i32), ("n_sink", c_i32), ("window", c_i32),
                 ("block", c_i32), ("topk_fixed", c_i32), ("retain_permille", c_i32),
                 ("n_segments", c_i32), ("seg", MkSegment * MK_MAX_SEGMENTS), ("meta_channels", c_i32),
-                ("page_format", c_i32)]
+                ("page_format", c_i32), ("elem_group", c_i32)]
 
 
 class MkAlg2Params(ctypes.Structure):
@@ -87,8 +88,8 @@ _SIGS = {
     "mk_choose_r": [c_vp, c_i32, ctypes.c_double, ctypes.POINTER(c_i32)],
     "mk_alg2_segment_r": [c_vp, c_i64, c_i64, c_i32, ctypes.c_double, ctypes.POINTER(MkAlg2Params),
                           ctypes.POINTER(MkSegStats), ctypes.POINTER(c_i32)],
-    "mk_host_pack_blocks": [c_vp, c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_i64, c_i32, c_vp, c_vp,
-                            c_vp],
+    "mk_host_pack_blocks": [c_vp, c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_i64, c_i32, c_i32, c_i32,
+                            c_vp, c_vp, c_vp],
     "mk_swap_segment": [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp],
 }
 
@@ -139,7 +140,8 @@ def _stream(stream=None):
 
 
 def make_config(n_q_heads, n_kv_heads, n_layers, max_seqs, max_tokens, n_sink, window, block,
-                segments, topk_fixed=0, retain_permille=0, meta_channels=0, page_format=0) -> MkConfig:
+                segments, topk_fixed=0, retain_permille=0, meta_channels=0, page_format=0,
+                elem_group=0) -> MkConfig:
     c = MkConfig()
     c.head_dim = MK_HEAD_DIM
     c.n_q_heads, c.n_kv_heads, c.n_layers = n_q_heads, n_kv_heads, n_layers
@@ -148,6 +150,7 @@ def make_config(n_q_heads, n_kv_heads, n_layers, max_seqs, max_tokens, n_sink, w
     c.topk_fixed, c.retain_permille = topk_fixed, retain_permille
     c.meta_channels = meta_channels
     c.page_format = page_format
+    c.elem_group = elem_group
     c.n_segments = len(segments)
     for i, sg in enumerate(segments):
         b, r, a = sg[:3]
@@ -400,7 +403,8 @@ def alg2_segment_r(seg, budget, outlier_abs, outlier_ratio_max, alpha, r_min, r_
     return r.value, {"variance": st.variance, "outlier_ratio": st.outlier_ratio, "entropy": st.entropy}
 
 
-def host_pack_blocks(Rk, Rv, k, v, block, r, keep_channels, page_stride, meta_channels=0):
+def host_pack_blocks(Rk, Rv, k, v, block, r, keep_channels, page_stride, meta_channels=0, page_format=0,
+                     elem_group=0):
     """Exact host re-compression of complete blocks (raw bf16 rows k, v: n_blocks * block rows of 128):
     (pages uint8 [n, page_stride], meta uint16 [n, 2, 128], compressed keys uint8 [n, row] or None)."""
     kw, vw = _bf16_words(k), _bf16_words(v)
@@ -413,5 +417,6 @@ def host_pack_blocks(Rk, Rv, k, v, block, r, keep_channels, page_stride, meta_ch
     cmeta = np.empty((n, crow), dtype=np.uint8) if meta_channels else None
     _check("mk_host_pack_blocks", load().mk_host_pack_blocks(
         _np_ptr(Rk32), _np_ptr(Rv32), _np_ptr(kw), _np_ptr(vw), kw.shape[1], n, block, r, keep_channels, page_stride,
-        meta_channels, _np_ptr(pages), _np_ptr(meta), _np_ptr(cmeta) if cmeta is not None else ctypes.c_void_p(0)))
+        meta_channels, page_format, elem_group, _np_ptr(pages), _np_ptr(meta),
+        _np_ptr(cmeta) if cmeta is not None else ctypes.c_void_p(0)))
     return pages, meta, cmeta

@@ -29,6 +29,7 @@ class Workload:
     topk_fixed: int = 0     # > 0: select exactly this many blocks
     retain_permille: int = 0
     meta_channels: int = 0        # > 0: channel-compressed per-block keys (a variant; 0 in every listed workload)
+    elem_group: int = 0           # > 0: bitmap pages with this element-group size (a variant; 0 = uint8 indices)
     decay: float = 0.92
     append_per_step: int = 1
     description: str = ""

@@ -63,9 +63,20 @@ mk_status check_config(const mk_config* c) {
     if (s.begin_permille < prev) return MK_EINVAL;
     prev = s.begin_permille;
     if (c->page_format == MK_PAGES_DENSE && (s.r != MK_HEAD_DIM || s.keep_channels != 0)) return MK_EINVAL;
+    if (c->page_format == MK_PAGES_BITMAP) {
+      const int g = c->elem_group ? c->elem_group : 1;
+      if (s.r % g || s.keep_channels % g) return MK_EINVAL;
+    }
   }
-  if (c->page_format != MK_PAGES_PACKED && c->page_format != MK_PAGES_DENSE) return MK_EINVAL;
+  if (c->page_format != MK_PAGES_PACKED && c->page_format != MK_PAGES_DENSE && c->page_format != MK_PAGES_BITMAP)
+    return MK_EINVAL;
   if (c->page_format == MK_PAGES_DENSE && c->meta_channels != 0) return MK_EINVAL;
+  if (c->page_format == MK_PAGES_BITMAP) {
+    const int g = c->elem_group;
+    if (g != 0 && g != 1 && g != 2 && g != 4 && g != 8) return MK_EINVAL;
+  } else if (c->elem_group != 0) {
+    return MK_EINVAL;
+  }
   return MK_OK;
 }
 
@@ -89,8 +100,9 @@ Plan make_plan(const mk_config* c) {
   L.k_max = std::max(1, mk::n_select(L, L.nblk_cap));
   L.keys_stride = (std::max(1, L.nblk_cap) + 3) & ~3;
   L.dense_pages = c->page_format == MK_PAGES_DENSE ? 1 : 0;
-  // packed: 6 r bytes per token (K and V values and indices); dense: 2 x 256
-  L.page_stride = L.dense_pages ? (int64_t)4 * L.B * MK_HEAD_DIM : (int64_t)6 * L.B * r_max;
+  L.bm_g = c->page_format == MK_PAGES_BITMAP ? (c->elem_group ? c->elem_group : 1) : 0;
+  // packed: K and V values (2 r bytes each) and positions; dense: 2 x 256 bytes per token
+  L.page_stride = L.dense_pages ? (int64_t)4 * L.B * MK_HEAD_DIM : page_vpos(L, r_max) + (int64_t)L.B * pos_bytes(L, r_max);
   const int64_t D = MK_HEAD_DIM;
   int64_t off = 0;
   L.off_rkt = off; off += D * D * 4;
@@ -676,6 +688,7 @@ mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_he
   if (segment < 0 || segment >= c.n_segments) return MK_EINVAL;
   if (r < 1 || r > L.r_max) return MK_EINVAL;  // the pages hold at most r_max entries per token
   if (keep_channels != 0 && (keep_channels < r || keep_channels > MK_HEAD_DIM)) return MK_EINVAL;
+  if (L.bm_g > 1 && (r % L.bm_g || keep_channels % L.bm_g)) return MK_EINVAL;  // whole groups only
   if (L.meta_c > 0 && !cmeta) return MK_EINVAL;
   if ((R_k == nullptr) != (R_v == nullptr)) return MK_EINVAL;
   const size_t ls = (size_t)layer * c.max_seqs + seq;

@@ -134,6 +134,42 @@ __device__ __forceinline__ BulkItem bulk_item(const Layout& L, const CallSeqs& c
 }
 }  // namespace
 
+// Grouped bitmap ([S] sec. 5.1): the energies of the 64 / GG groups of g
+// adjacent channels in one thread's half row (channels 64 h ..), the fp32 sum
+// of squares in channel order, as key bits (non-negative floats order as
+// their bit patterns); groups from kp on count 0, slots past 64 / GG are 0.
+template <int GG>
+__device__ __forceinline__ void group_keys(const uint4* row4, int h, int kp, bool live, uint32_t kw[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) kw[j] = 0u;
+  float acc = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 x = live ? row4[j] : make_uint4(0, 0, 0, 0);
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int c = 8 * j + e;  // channel within the half
+      const float v = __uint_as_float((e & 1 ? xs[e >> 1] >> 16 : xs[e >> 1] & 0xffffu) << 16);
+      const float sq = __fmul_rn(v, v);
+      acc = c % GG == 0 ? sq : __fadd_rn(acc, sq);
+      if (c % GG == GG - 1) kw[c / GG] = 64 * h + c - (GG - 1) < kp ? __float_as_uint(acc) : 0u;
+    }
+  }
+}
+// Channel keep bits of a half row from its kept groups (bit j: group j).
+template <int GG>
+__device__ __forceinline__ uint64_t spread_groups(uint64_t kg) {
+  uint64_t out = 0ull;
+#pragma unroll
+  for (int j = 0; j < 64 / GG; ++j)
+    if (kg >> j & 1ull) out |= ((GG == 64 ? ~0ull : (1ull << GG) - 1ull)) << (GG * j);
+  return out;
+}
+
+// BM: bitmap pages (element group L.bm_g); the uint8-index and uncompressed
+// formats take BM = false, without the grouped search.
+template <bool BM>
 __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, CallSeqs cs,
                                                      const uint16_t* __restrict__ kin,
                                                      const uint16_t* __restrict__ vin, int total_tiles,
@@ -322,60 +358,93 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
         }
       } else {
         keep_lo = 0u;
-        // 15-bit magnitudes, two per word, each under a guard bit: for a
-        // candidate c, bit 15 (31) of (word - c | c << 16) is set exactly
-        // when the low (high) magnitude is >= c.  Truncated channels count 0.
         uint32_t kw[32];
+        uint64_t gt = 0ull, eq = 0ull;
+        const int gg = BM ? L.bm_g : 0;
+        int kneed = r;  // units to keep: channels, or groups of gg channels
+        if (gg <= 1) {
+          // 15-bit magnitudes, two per word, each under a guard bit: for a
+          // candidate c, bit 15 (31) of (word - c | c << 16) is set exactly
+          // when the low (high) magnitude is >= c.  Truncated channels count 0.
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 x = live ? row4[j] : make_uint4(0, 0, 0, 0);
-          const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+          for (int j = 0; j < 8; ++j) {
+            const uint4 x = live ? row4[j] : make_uint4(0, 0, 0, 0);
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c0 = 64 * h + 8 * j + 2 * e;
-            uint32_t w = xs[e] & 0x7fff7fffu;
-            if (c0 >= kp) w &= 0xffff0000u;
-            if (c0 + 1 >= kp) w &= 0x0000ffffu;
-            kw[4 * j + e] = w | 0x80008000u;
+            for (int e = 0; e < 4; ++e) {
+              const int c0 = 64 * h + 8 * j + 2 * e;
+              uint32_t w = xs[e] & 0x7fff7fffu;
+              if (c0 >= kp) w &= 0xffff0000u;
+              if (c0 + 1 >= kp) w &= 0x0000ffffu;
+              kw[4 * j + e] = w | 0x80008000u;
+            }
           }
-        }
-        // The r-th largest magnitude thr: the largest value with at least r
-        // magnitudes >= it (bitwise from the top; the pair adds its counts).
-        // The flags of 16 words (32 magnitudes) are gathered into one word
-        // (word j's two flags shifted right by j) and counted by one popc.
-        uint32_t thr = 0u;
+          // The r-th largest magnitude thr: the largest value with at least r
+          // magnitudes >= it (bitwise from the top; the pair adds its counts).
+          // The flags of 16 words (32 magnitudes) are gathered into one word
+          // (word j's two flags shifted right by j) and counted by one popc.
+          uint32_t thr = 0u;
 #pragma unroll 1
-        for (int bit = 14; bit >= 0; --bit) {
-          const uint32_t cand = thr | (1u << bit);
-          const uint32_t cc = cand | (cand << 16);
-          int n = 0;
+          for (int bit = 14; bit >= 0; --bit) {
+            const uint32_t cand = thr | (1u << bit);
+            const uint32_t cc = cand | (cand << 16);
+            int n = 0;
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
+            for (int g = 0; g < 2; ++g) {
+              uint32_t f = 0u;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) f |= ((kw[16 * g + j] - cc) & 0x80008000u) >> j;
+              n += __popc(f);
+            }
+            n += __shfl_xor_sync(FULL, n, 1);
+            if (n >= r) thr = cand;
+          }
+          // Above thr: kept.  Equal to thr: the lowest channels, as many as the
+          // r - #above still needed (the lower half's ties come first).
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t lo16 = kw[j] & 0x7fffu, hi16 = (kw[j] >> 16) & 0x7fffu;
+            gt |= (uint64_t)(lo16 > thr) << (2 * j) | (uint64_t)(hi16 > thr) << (2 * j + 1);
+            eq |= (uint64_t)(lo16 == thr) << (2 * j) | (uint64_t)(hi16 == thr) << (2 * j + 1);
+          }
+        } else {
+          // Grouped bitmap: the r / gg groups of largest energy, ties to the
+          // lower group.  31-bit keys, one per group (ng = 64 / gg of them
+          // per thread, the rest 0): the (r / gg)-th largest energy by a
+          // bitwise search, each step gathering the sign bits of key - cand
+          // (set when key < cand) into one word.
+          if (gg == 2) group_keys<2>(row4, h, kp, live, kw);
+          else if (gg == 4) group_keys<4>(row4, h, kp, live, kw);
+          else group_keys<8>(row4, h, kp, live, kw);
+          kneed = r / gg;
+          const int ng = 64 / gg;
+          uint32_t thr = 0u;
+#pragma unroll 1
+          for (int bit = 30; bit >= 0; --bit) {
+            const uint32_t cand = thr | (1u << bit);
             uint32_t f = 0u;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) f |= ((kw[16 * g + j] - cc) & 0x80008000u) >> j;
-            n += __popc(f);
+            for (int j = 0; j < 32; ++j) f |= ((kw[j] - cand) >> 31) << j;
+            int n = 32 - __popc(f);  // zero slots never reach cand >= 1
+            n += __shfl_xor_sync(FULL, n, 1);
+            if (n >= kneed) thr = cand;
           }
-          n += __shfl_xor_sync(FULL, n, 1);
-          if (n >= r) thr = cand;
-        }
-        // Above thr: kept.  Equal to thr: the lowest channels, as many as the
-        // r - #above still needed (the lower half's ties come first).
-        uint64_t gt = 0ull, eq = 0ull;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t lo16 = kw[j] & 0x7fffu, hi16 = (kw[j] >> 16) & 0x7fffu;
-          gt |= (uint64_t)(lo16 > thr) << (2 * j) | (uint64_t)(hi16 > thr) << (2 * j + 1);
-          eq |= (uint64_t)(lo16 == thr) << (2 * j) | (uint64_t)(hi16 == thr) << (2 * j + 1);
+          for (int j = 0; j < 32; ++j) {
+            gt |= (uint64_t)(kw[j] > thr) << j;
+            eq |= (uint64_t)(kw[j] == thr && j < ng) << j;
+          }
         }
         const int n_gt = __popcll(gt), n_eq = __popcll(eq);
         const int pair_gt = n_gt + __shfl_xor_sync(FULL, n_gt, 1);
         const int eq_lower = __shfl_xor_sync(FULL, n_eq, 1);
-        const int need = r - pair_gt - (h ? eq_lower : 0);
+        const int need = kneed - pair_gt - (h ? eq_lower : 0);
         int take = need < 0 ? 0 : (need > n_eq ? n_eq : need);
         while (__popcll(eq) > take) eq &= ~(1ull << (63 - __clzll(eq)));  // keep the lowest channels
-        uint64_t keep = gt | eq;
-        if (!live) keep = 0ull;
+        uint64_t keepg = gt | eq;  // channels, or groups of this half
+        if (!live) keepg = 0ull;
+        uint64_t keep = gg == 2 ? spread_groups<2>(keepg) : gg == 4 ? spread_groups<4>(keepg)
+                      : gg == 8 ? spread_groups<8>(keepg) : keepg;
         keep_lo = (uint32_t)keep;
         keep_hi = (uint32_t)(keep >> 32);
         // Packed row, in channel order: thread 0 of the pair writes ranks
@@ -390,11 +459,25 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
           const uint64_t m0 = h ? other : mine, m1 = h ? mine : other;  // channels 0-63, 64-127
           const bool staged = r <= kStageR;
           char* page = base + L.off_pages + (int64_t)b * L.page_stride;
-          const int Br = B * r;
+          const int pb = BM ? 16 / gg : r, Br = B * r, Bp = B * pb;  // page: [2Br][Bp][2Br][Bp]
           uint16_t* val = staged ? stv + (b - b0) * B * kStageR + tt * r
-                                 : reinterpret_cast<uint16_t*>(page + (is_v ? 3 * Br : 0)) + tt * r;
-          uint8_t* idx = staged ? sti + (b - b0) * B * kStageR + tt * r
-                                : reinterpret_cast<uint8_t*>(page + (is_v ? 5 * Br : 2 * Br)) + tt * r;
+                                 : reinterpret_cast<uint16_t*>(page + (is_v ? 2 * Br + Bp : 0)) + tt * r;
+          uint8_t* idx = staged ? sti + (b - b0) * B * kStageR + tt * pb
+                                : reinterpret_cast<uint8_t*>(page + (is_v ? 4 * Br + Bp : 2 * Br)) + tt * pb;
+          if (gg) {
+            // Bitmap ([S] sec. 5.1): this half's 64 / gg bits at byte 8 h / gg.
+            uint8_t* d = idx + h * (8 / gg);
+            if (gg == 1) {
+              reinterpret_cast<uint32_t*>(d)[0] = keep_lo;
+              reinterpret_cast<uint32_t*>(d)[1] = keep_hi;
+            } else if (gg == 2) {
+              *reinterpret_cast<uint32_t*>(d) = (uint32_t)keepg;
+            } else if (gg == 4) {
+              *reinterpret_cast<uint16_t*>(d) = (uint16_t)keepg;
+            } else {
+              *d = (uint8_t)keepg;
+            }
+          }
           const uint16_t* rowf = rot + (size_t)t * kRotRow;
           const int r2 = (r + 1) >> 1;
           if (h == 0) {
@@ -408,7 +491,7 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
               const int c = cb + __ffsll((long long)mm) - 1;
               mm &= mm - 1ull;
               val[k] = rowf[c];
-              idx[k] = (uint8_t)c;
+              if (!gg) idx[k] = (uint8_t)c;
             }
           } else {
             uint64_t mm = m1;
@@ -421,7 +504,7 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
               const int bit = 63 - __clzll((long long)mm);
               mm &= ~(1ull << bit);
               val[k] = rowf[cb + bit];
-              idx[k] = (uint8_t)(cb + bit);
+              if (!gg) idx[k] = (uint8_t)(cb + bit);
             }
           }
         }
@@ -445,22 +528,25 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
         const int blo = S + b * B;
         const int st = max(blo, mlo), en = min(blo + B, mhi);
         char* page = base + L.off_pages + (int64_t)b * L.page_stride;
-        const int Br = B * r;
-        uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? 3 * Br : 0)) + (st - blo) * r;
-        uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? 5 * Br : 2 * Br)) + (st - blo) * r;
+        const int pb = BM ? 16 / L.bm_g : r, Br = B * r, Bp = B * pb;  // page: [2Br][Bp][2Br][Bp]
+        uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? 2 * Br + Bp : 0)) + (st - blo) * r;
+        uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? 4 * Br + Bp : 2 * Br)) + (st - blo) * pb;
         const uint16_t* sv = stv + (b - b0) * B * kStageR + (st - blo) * r;
-        const uint8_t* si = sti + (b - b0) * B * kStageR + (st - blo) * r;
+        const uint8_t* si = sti + (b - b0) * B * kStageR + (st - blo) * pb;
         const int n = (en - st) * r;
         if (st == blo && en == blo + B) {
           if (tid == 0) {
             bulk_s2g(val, sv, (unsigned)(2 * Br));
-            bulk_s2g(idx, si, (unsigned)Br);
+            bulk_s2g(idx, si, (unsigned)Bp);
           }
-        } else {
+        } else if (!BM) {
           for (int i = tid; i < n; i += blockDim.x) {
             val[i] = sv[i];
             idx[i] = si[i];
           }
+        } else {
+          for (int i = tid; i < n; i += blockDim.x) val[i] = sv[i];
+          for (int i = tid; i < (en - st) * pb; i += blockDim.x) idx[i] = si[i];
         }
       }
     if (tid == 0) {
@@ -610,14 +696,15 @@ cudaError_t launch_append_small(const Layout& L, int layer, const CallSeqs& cs, 
 cudaError_t launch_append_bulk(const Layout& L, int layer, const CallSeqs& cs, const uint16_t* k,
                                const uint16_t* v, int total_tiles, cudaStream_t s) {
   int sms = 0;
-  cudaError_t e = kernel_smem_attr((const void*)k_append_bulk, kBulkSmem, 256, nullptr, &sms);
+  const auto kern = L.bm_g ? k_append_bulk<true> : k_append_bulk<false>;
+  cudaError_t e = kernel_smem_attr((const void*)kern, kBulkSmem, 256, nullptr, &sms);
   if (e != cudaSuccess) return e;
   // Persistent: at most one CTA per SM, each with an equal run of items.
   const int items = 2 * L.n_kv * total_tiles;
   const int grid0 = std::max(1, std::min(items, std::max(sms, 1)));
   const int per = (items + grid0 - 1) / grid0;
   const int grid = (items + per - 1) / per;
-  k_append_bulk<<<grid, 256, kBulkSmem, s>>>(L, layer, cs, k, v, total_tiles, per);
+  kern<<<grid, 256, kBulkSmem, s>>>(L, layer, cs, k, v, total_tiles, per);
   return cudaGetLastError();
 }
 

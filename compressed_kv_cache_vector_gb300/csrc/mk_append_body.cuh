@@ -56,6 +56,101 @@ __device__ __forceinline__ unsigned warp_topr(const uint32_t m[4], int r, int la
   return keep;
 }
 
+// Grouped top-r for the bitmap format ([S] sec. 5.1: one bit per group of g
+// adjacent channels), g = 2, 4 or 8, on a vector held 4 bf16 channels per lane
+// (4*lane .. 4*lane+3).  Keeps the r/g groups with the largest energy, the
+// fp32 sum of the group's squares in channel order (each product and sum
+// rounded: a bf16 square is exact), ties to the lower group.  Groups from
+// keep/g on count 0; with r <= keep the ties at 0 go to lower groups, so they
+// are never taken.  The energies are non-negative floats, ordered as their
+// bit patterns, so the (r/g)-th largest is found by a 31-bit search from the
+// top.  Returns this lane's channel keep bits.
+__device__ __forceinline__ unsigned warp_top_groups(const uint16_t v[4], int g, int r, int keep, int lane) {
+  float sq[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float x = bf2f(v[i]);
+    sq[i] = __fmul_rn(x, x);
+  }
+  uint32_t key[2] = {0u, 0u};
+  unsigned valid = 0u;  // bit s: key[s] is a group of this lane
+  if (g == 2) {         // groups 2 lane, 2 lane + 1
+    key[0] = 4 * lane < keep ? __float_as_uint(__fadd_rn(sq[0], sq[1])) : 0u;
+    key[1] = 4 * lane + 2 < keep ? __float_as_uint(__fadd_rn(sq[2], sq[3])) : 0u;
+    valid = 3u;
+  } else {
+    float e = __fadd_rn(__fadd_rn(__fadd_rn(sq[0], sq[1]), sq[2]), sq[3]);
+    if (g == 4) {       // group lane
+      key[0] = 4 * lane < keep ? __float_as_uint(e) : 0u;
+      valid = 1u;
+    } else {            // group lane / 2: the odd lane continues the even lane's sum
+      const float lo = __shfl_xor_sync(FULL, e, 1);
+      e = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(lo, sq[0]), sq[1]), sq[2]), sq[3]);
+      key[0] = 4 * (lane - 1) < keep ? __float_as_uint(e) : 0u;
+      valid = lane & 1;
+    }
+  }
+  const int k = r / g;
+  uint32_t t = 0u;
+#pragma unroll 1
+  for (int bit = 30; bit >= 0; --bit) {
+    const uint32_t cand = t | (1u << bit);
+    const unsigned c = (unsigned)((valid & 1u) && key[0] >= cand) + (unsigned)((valid & 2u) && key[1] >= cand);
+    if ((int)__reduce_add_sync(FULL, c) >= k) t = cand;
+  }
+  const unsigned gt = (unsigned)((valid & 1u) && key[0] > t) + (unsigned)((valid & 2u) && key[1] > t);
+  const unsigned eq = (unsigned)((valid & 1u) && key[0] == t) + (unsigned)((valid & 2u) && key[1] == t);
+  const int need = k - (int)__reduce_add_sync(FULL, gt);
+  int run = warp_excl_scan((int)eq, lane);
+  unsigned kg = 0u;  // kept groups of this lane (bit s: key[s])
+#pragma unroll
+  for (int s2 = 0; s2 < 2; ++s2) {
+    if (!(valid >> s2 & 1u)) continue;
+    if (key[s2] > t) {
+      kg |= 1u << s2;
+    } else if (key[s2] == t) {
+      if (run < need) kg |= 1u << s2;
+      ++run;
+    }
+  }
+  if (g == 2) return (kg & 1u ? 3u : 0u) | (kg & 2u ? 12u : 0u);
+  if (g == 8) kg = __shfl_sync(FULL, kg, lane | 1);
+  return kg ? 0xfu : 0u;
+}
+
+// Stores the position bitmap of one vector ([S] sec. 5.1): 128/g bits, bit j
+// (byte j/8, bit j%8) set when group j is kept.  kbits: this lane's channel
+// keep bits (channels 4*lane .. 4*lane+3, whole groups).  Called by one full
+// warp; dst is aligned to the bitmap's size.
+__device__ __forceinline__ void store_bitmap(uint8_t* dst, unsigned kbits, int g, int lane) {
+  uint32_t w;
+  int lpw;  // lanes whose group bits share one 32-bit word
+  if (g == 1) {
+    w = kbits << (4 * (lane & 7));
+    lpw = 8;
+  } else if (g == 2) {
+    w = ((kbits & 1u) | ((kbits >> 1) & 2u)) << (2 * (lane & 15));
+    lpw = 16;
+  } else if (g == 4) {
+    w = (kbits & 1u) << lane;
+    lpw = 32;
+  } else {
+    w = (kbits & 1u) << (lane >> 1);
+    lpw = 32;
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t o = __shfl_xor_sync(FULL, w, off);
+    if (off < lpw) w |= o;
+  }
+  if ((lane & (lpw - 1)) == 0) {
+    if (g == 8)
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w;
+    else
+      reinterpret_cast<uint32_t*>(dst)[lane / lpw] = w;
+  }
+}
+
 // Channel-compressed key of block b ([S] sec. 5.2: the per-block keys are
 // channel-compressed like the vectors): from the block's min/max row (four
 // channels per lane, 4*lane .. 4*lane+3), keep the L.meta_c channels with the
@@ -96,9 +191,8 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   const int sg = seg_of_block(ud, b);
   const int r = ud.r[sg], keep = seg_keep(ud, sg);
   char* page = base + L.off_pages + (int64_t)b * L.page_stride;
-  const int Br = L.B * r;
-  uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? 3 * Br : 0));
-  uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? 5 * Br : 2 * Br));
+  uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? page_vval(L, r) : 0));
+  uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? page_vpos(L, r) : page_kpos(L, r)));
   const uint2 raw = *reinterpret_cast<const uint2*>(row + 4 * lane);
   // The block's min/max are loaded with the row, ahead of the search.
   uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta) + (int64_t)b * 2 * D;
@@ -119,15 +213,21 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   if (L.dense_pages) {
     store_dense_row(L, base, b, t, is_v, raw, lane);
   } else {
-    kbits = warp_topr(mag, r, lane, rank);
+    if (L.bm_g > 1) {
+      kbits = warp_top_groups(v, L.bm_g, r, keep, lane);
+      rank = warp_excl_scan(__popc(kbits), lane);
+    } else {
+      kbits = warp_topr(mag, r, lane, rank);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       if (kbits >> i & 1u) {
         val[t * r + rank] = v[i];
-        idx[t * r + rank] = (uint8_t)(4 * lane + i);
+        if (!L.bm_g) idx[t * r + rank] = (uint8_t)(4 * lane + i);
         ++rank;
       }
     }
+    if (L.bm_g) store_bitmap(idx + t * pos_bytes(L, r), kbits, L.bm_g, lane);
   }
   if (update_meta) {
     const uint16_t pmn[4] = {(uint16_t)(omn.x & 0xffff), (uint16_t)(omn.x >> 16), (uint16_t)(omn.y & 0xffff),

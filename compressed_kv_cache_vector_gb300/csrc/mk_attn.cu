@@ -54,6 +54,10 @@
 namespace mk {
 
 namespace {
+// Kernel variants of the packed path: uint8 indices, every segment in the
+// head's rotation; uint8 indices with rotation classes (segments under their
+// own rotation); bitmap pages (rotation classes checked at run time).
+constexpr int kModePlain = 0, kModeOwn = 1, kModeBitmap = 2;
 constexpr int kMaxWarps = 16;                // one CTA per SM, 4 to 16 warps (shared memory decides)
 constexpr int kTG = 16;                      // tokens per packed group (one MMA tile)
 constexpr int kDC = 8;                       // tokens per dense chunk
@@ -160,6 +164,69 @@ __device__ __forceinline__ void scatter_kv(uint32_t tk, uint32_t tv, uint32_t kv
   }
 }
 
+// Rebuild one token's dense row from its position bitmap ([S] sec. 5.1; the
+// row is zero already).  Bit j of the bitmap (group j, channels GG j ..
+// GG j + GG - 1) takes the next GG packed values, so the lane walks its set
+// bits from the lowest and copies GG values per bit: n = r / GG iterations
+// for every live token.  vals, bm, row: shared-window byte addresses of the
+// token's packed values, its bitmap and its dense row.
+template <int GG>
+__device__ __forceinline__ void unpack_bitmap_row(uint32_t vals, uint32_t bm, uint32_t row, int r) {
+  uint64_t cur, nxt = 0ull;
+  if (GG == 1) {
+    uint32_t w0, w1, w2, w3;
+    asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(bm));
+    cur = (uint64_t)w0 | ((uint64_t)w1 << 32);
+    nxt = (uint64_t)w2 | ((uint64_t)w3 << 32);
+  } else if (GG == 2) {
+    uint32_t w0, w1;
+    asm("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(w0), "=r"(w1) : "r"(bm));
+    cur = (uint64_t)w0 | ((uint64_t)w1 << 32);
+  } else if (GG == 4) {
+    cur = lds_u32(bm);
+  } else {
+    cur = lds_u16(bm);
+  }
+  int cb = 0;
+  for (int k = 0; k < r; k += GG) {
+    if (GG == 1 && cur == 0ull) {
+      cur = nxt;
+      cb = 64;
+    }
+    // (the mask keeps a malformed bitmap with too few bits inside the row)
+    const int c = ((cb + __ffsll((long long)cur) - 1) & (128 / GG - 1)) * GG;
+    cur &= cur - 1ull;
+    const uint32_t src = vals + 2 * k, dst = row + 2 * c;
+    if (GG == 1) {
+      sts_u16(dst, lds_u16(src));
+    } else if (GG == 2) {
+      asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(dst), "r"(lds_u32(src)) : "memory");
+    } else if (GG == 4) {
+      uint32_t a, b;
+      asm("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(a), "=r"(b) : "r"(src));
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};\n" ::"r"(dst), "r"(a), "r"(b) : "memory");
+    } else {
+      uint32_t a, b, c2, d;
+      asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(a), "=r"(b), "=r"(c2), "=r"(d) : "r"(src));
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(a), "r"(b), "r"(c2), "r"(d)
+                   : "memory");
+    }
+  }
+}
+// Highest channel a token's bitmap keeps (0 for an empty bitmap).
+__device__ __forceinline__ int bitmap_top_channel(uint32_t bm, int gg) {
+  const int nw = gg == 1 ? 4 : gg == 2 ? 2 : 1;
+  int top = -1;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i < nw) {
+      const uint32_t w = gg == 8 ? lds_u16(bm) : lds_u32(bm + 4 * i);
+      if (w) top = 32 * i + 31 - __clz(w);
+    }
+  }
+  return top < 0 ? 0 : top * gg + gg - 1;
+}
+
 struct Task {
   int kind;      // 0 none, 1 dense chunk, 2 packed group, 3 skipped (bad block id)
                  // (kind 1 with b >= 0: rows j0.. of an uncompressed page, the Quest comparator)
@@ -169,7 +236,7 @@ struct Task {
 };
 
 int stage_bytes(const Layout& L) {
-  return (std::max(L.dense_pages ? 0 : 6 * kTG * L.r_max, kDenseStage) + 15) / 16 * 16;
+  return (std::max(L.dense_pages ? 0 : kTG * (4 * L.r_max + 2 * pos_bytes(L, L.r_max)), kDenseStage) + 15) / 16 * 16;
 }
 // Per warp: the stages, then the key tile and the value tile.
 size_t per_warp_bytes(const Layout& L, int nst) {
@@ -235,7 +302,7 @@ int attn_max_parts(const Layout& L) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(MK_MAX_SPLITS, avail / ((int64_t)L.G * (D + 2) * 4)));
 }
 
-template <int G, bool DENSE, int MAXW, bool OWN>
+template <int G, bool DENSE, int MAXW, int MODE>
 __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, CallSeqs cs, AttnSplit split,
                                                  const int32_t* __restrict__ ids,
                                                  const int32_t* __restrict__ n_sel_in,
@@ -377,7 +444,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
   // classes' work.  Without such segments: one class, the unit's P CTAs.
   int cls = 0, pc = part, Pc = P;
   int ns_c = ns, nalw_c = n_always, ndch_c = n_dch;
-  const bool own_mode = OWN && !DENSE && !skip && any_own(ud);
+  const bool own_mode = MODE != kModePlain && !DENSE && !skip && any_own(ud);
   if (own_mode) {
     if (tid == 0)
       for (int i = 0; i < MK_MAX_SEGMENTS; ++i)
@@ -570,18 +637,21 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
       // This group's rows of the page's four sub-arrays (B is a multiple of
       // 16, so a whole group stays inside the page; sizes and offsets are
       // multiples of 16 bytes), back to back in the stage:
-      // [K val 2gr][K idx gr][V val 2gr][V idx gr] bytes; lane q copies run q.
+      // [K val 2gr][K pos gp][V val 2gr][V pos gp] bytes (gp = 16 position
+      // rows: gr uint8 indices or 16 bitmaps); lane q copies run q.
+      const int gr = kTG * t.r, pb = MODE == kModeBitmap ? 16 / L.bm_g : t.r, gp = kTG * pb;
       if (lane == 0) {
         fence_proxy_async();
-        mbar_expect_tx(&bars[sidx], 6u * kTG * (unsigned)t.r);
+        mbar_expect_tx(&bars[sidx], (unsigned)(4 * gr + 2 * gp));
       }
       __syncwarp();
       if (lane < 4) {
-        const int Br = B * t.r, gr = kTG * t.r, tr = t.tg * t.r;
+        const int tr = t.tg * t.r, tp = t.tg * pb, Br = B * t.r, Bp = B * pb;  // page: [2Br][Bp][2Br][Bp]
         const char* page = base + L.off_pages + (int64_t)t.b * L.page_stride;
-        const int soff = lane == 0 ? 2 * tr : lane == 1 ? 2 * Br + tr : lane == 2 ? 3 * Br + 2 * tr : 5 * Br + tr;
-        const int doff = lane == 0 ? 0 : lane == 1 ? 2 * gr : lane == 2 ? 3 * gr : 5 * gr;
-        bulk_g2s(dst + doff, page + soff, (lane & 1) ? gr : 2 * gr, &bars[sidx]);
+        const int soff = lane == 0 ? 2 * tr : lane == 1 ? 2 * Br + tp : lane == 2 ? 2 * Br + Bp + 2 * tr
+                                                                                    : 4 * Br + Bp + tp;
+        const int doff = lane == 0 ? 0 : lane == 1 ? 2 * gr : lane == 2 ? 2 * gr + gp : 4 * gr + gp;
+        bulk_g2s(dst + doff, page + soff, (lane & 1) ? gp : 2 * gr, &bars[sidx]);
       }
     }
   };
@@ -656,19 +726,24 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
         vrow = (vtok < ntok ? vb + vtok * kRow : zrow) + vch;
       } else {
         ntok = min(kTG, cur.n_live - cur.tg);
-        const int r = cur.r, gr = kTG * r;
+        const int r = cur.r, gr = kTG * r, pb = MODE == kModeBitmap ? 16 / L.bm_g : r, gp = kTG * pb;
         const uint16_t* kval = reinterpret_cast<const uint16_t*>(buf);
         const uint8_t* kidx = buf + 2 * gr;
-        const uint16_t* vval = reinterpret_cast<const uint16_t*>(buf + 3 * gr);
-        const uint8_t* vidx = buf + 5 * gr;
+        const uint16_t* vval = reinterpret_cast<const uint16_t*>(buf + 2 * gr + gp);
+        const uint8_t* vidx = buf + 4 * gr + gp;
         // Kept channels are stored in ascending order, so a token's last
-        // index is its highest channel: the group's rows are zero from the
-        // chunk after the largest one on.
-        const int tt = lane & 15;
+        // index (its bitmap's top bit) is its highest channel: the group's
+        // rows are zero from the chunk after the largest one on.
+        const int tt = lane & 15, gg = MODE == kModeBitmap ? L.bm_g : 0;
         uint32_t hk = 0, hv = 0;
         if (tt < ntok) {
-          hk = kidx[tt * r + r - 1];
-          hv = vidx[tt * r + r - 1];
+          if (gg) {
+            const uint32_t hc = (uint32_t)bitmap_top_channel(smem_u32((lane >> 4) ? vidx : kidx) + tt * pb, gg);
+            (lane >> 4 ? hv : hk) = hc;
+          } else {
+            hk = kidx[tt * r + r - 1];
+            hv = vidx[tt * r + r - 1];
+          }
         }
         nck_k = (int)(__reduce_max_sync(FULL, hk) >> 4) + 1;
         nck_v = (int)(__reduce_max_sync(FULL, hv) >> 4) + 1;
@@ -681,10 +756,24 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
           if (c < nck_v) zv[2 * c] = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
-        const int n_el = ntok * r;
-        const uint32_t rm = (0x80000000u + (uint32_t)r - 1u) / (uint32_t)r;
-        scatter_kv(smem_u32(tk), smem_u32(tv), smem_u32(kval), smem_u32(kidx), smem_u32(vval), smem_u32(vidx), n_el,
-                   rm, lane);
+        if (gg) {
+          // Lane (token tt, tensor lane / 16) rebuilds that row.
+          if (tt < ntok) {
+            const bool isv = lane >> 4;
+            const uint32_t vals = smem_u32(isv ? vval : kval) + 2 * tt * r;
+            const uint32_t bm = smem_u32(isv ? vidx : kidx) + tt * pb;
+            const uint32_t row = smem_u32(isv ? tv : tk) + tt * kRow * 2;
+            if (gg == 1) unpack_bitmap_row<1>(vals, bm, row, r);
+            else if (gg == 2) unpack_bitmap_row<2>(vals, bm, row, r);
+            else if (gg == 4) unpack_bitmap_row<4>(vals, bm, row, r);
+            else unpack_bitmap_row<8>(vals, bm, row, r);
+          }
+        } else {
+          const int n_el = ntok * r;
+          const uint32_t rm = (0x80000000u + (uint32_t)r - 1u) / (uint32_t)r;
+          scatter_kv(smem_u32(tk), smem_u32(tv), smem_u32(kval), smem_u32(kidx), smem_u32(vval), smem_u32(vidx),
+                     n_el, rm, lane);
+        }
         __syncwarp();
         issue_next();  // the packed group now lives in the tiles
         krow = tk + ktok * kRow + kch;
@@ -981,12 +1070,12 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
 }
 
 namespace {
-template <int G, bool DENSE, int MAXW, bool OWN>
+template <int G, bool DENSE, int MAXW, int MODE>
 cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int32_t* ids, const int32_t* n_sel,
                        const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t t_stride, uint16_t* out,
                        const int32_t* items, const int32_t* min_parts, size_t smem, cudaStream_t s) {
   int occ = 1, sms = 0;
-  cudaError_t e = kernel_smem_attr((const void*)k_attn<G, DENSE, MAXW, OWN>, (int)smem, L.attn_nc * 32, &occ, &sms);
+  cudaError_t e = kernel_smem_attr((const void*)k_attn<G, DENSE, MAXW, MODE>, (int)smem, L.attn_nc * 32, &occ, &sms);
   if (e != cudaSuccess) return e;
   // CTAs per (sequence, kv head) in proportion to its items: one wave of
   // CTAs when the units fit on the SMs; with more units than CTA slots (many
@@ -1013,7 +1102,7 @@ cudaError_t launch_one(const Layout& L, int layer, const CallSeqs& cs, const int
   if (std::getenv("MK_LOG"))
     std::fprintf(stderr, "[mosaickv] attention: %d units, %d to %d CTAs each, %d CTAs (%d per SM), %zu B smem\n",
                  units, p_min, p_max, split.off[cs.n], occ, smem);
-  return launch_pdl(k_attn<G, DENSE, MAXW, OWN>, dim3(split.off[cs.n]), dim3(L.attn_nc * 32), smem, s, 0, L, layer, cs,
+  return launch_pdl(k_attn<G, DENSE, MAXW, MODE>, dim3(split.off[cs.n]), dim3(L.attn_nc * 32), smem, s, 0, L, layer, cs,
                     split, ids, n_sel, q, K, V, t_stride, out);
 }
 
@@ -1029,19 +1118,19 @@ cudaError_t launch_attn_g(const Layout& L, int layer, const CallSeqs& cs, const 
   bool own = false;
   if (!DENSE && min_parts)
     for (int i = 0; i < cs.n; ++i) own = own || min_parts[i] > 1;
+  const int mode = DENSE ? kModePlain : L.bm_g ? kModeBitmap : own ? kModeOwn : kModePlain;
+#define MK_ATTN_ONE(GG, MM)                                                                                      \
+  return wide ? launch_one<GG, DENSE, 16, MM>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, min_parts, \
+                                              smem, s)                                                           \
+              : launch_one<GG, DENSE, 12, MM>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items, min_parts, \
+                                              smem, s);
 #define MK_ATTN_CASE(GG)                                                                                         \
   case GG:                                                                                                       \
     if constexpr (!DENSE) {                                                                                      \
-      if (own)                                                                                                   \
-        return wide ? launch_one<GG, DENSE, 16, true>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items,   \
-                                                      min_parts, smem, s)                                        \
-                    : launch_one<GG, DENSE, 12, true>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items,   \
-                                                      min_parts, smem, s);                                       \
+      if (mode == kModeBitmap) MK_ATTN_ONE(GG, kModeBitmap)                                                      \
+      if (mode == kModeOwn) MK_ATTN_ONE(GG, kModeOwn)                                                            \
     }                                                                                                            \
-    return wide ? launch_one<GG, DENSE, 16, false>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items,      \
-                                                   min_parts, smem, s)                                           \
-                : launch_one<GG, DENSE, 12, false>(L, layer, cs, ids, n_sel, q, K, V, t_stride, out, items,      \
-                                                   min_parts, smem, s);
+    MK_ATTN_ONE(GG, kModePlain)
   switch (L.G) {
     MK_ATTN_CASE(1)
     MK_ATTN_CASE(2)
@@ -1050,6 +1139,7 @@ cudaError_t launch_attn_g(const Layout& L, int layer, const CallSeqs& cs, const 
     default: return cudaErrorInvalidValue;
   }
 #undef MK_ATTN_CASE
+#undef MK_ATTN_ONE
 }
 }  // namespace
 

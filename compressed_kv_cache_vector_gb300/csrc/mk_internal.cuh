@@ -71,6 +71,7 @@ struct Layout {
   int32_t S, W, B, n_kv, G, max_seqs, nblk_cap, cap_tokens, n_layers, k_max;
   int32_t topk_fixed, retain_permille, r_max;
   int32_t dense_pages;          // 1: uncompressed middle pages [K B x 128][V B x 128] (Quest comparator)
+  int32_t bm_g;                 // 0: uint8 channel indices; g = 1, 2, 4, 8: a bitmap of 128/g bits per vector
   int32_t attn_tg;              // attention: tokens per staged page group (32 or 16)
   int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, warps per CTA, stage bytes
   // workspace
@@ -102,6 +103,17 @@ __host__ __device__ inline int64_t unit_index(const Layout& L, int layer, int se
 // q' of (layer, sequence slot), written by the selection, read by attention.
 __host__ __device__ inline float* qrot_of(const Layout& L, int layer, int64_t slot, int cls = 0) {
   return L.qrot + (((int64_t)cls * L.n_layers + layer) * L.max_seqs * L.n_kv + slot) * L.G * 128;
+}
+// Packed page of a block with r kept channels: [K val B r bf16][K pos B pb]
+// [V val B r bf16][V pos B pb], pb = pos_bytes (r uint8 indices, or a bitmap
+// of 16/g bytes).
+__host__ __device__ inline int pos_bytes(const Layout& L, int r) { return L.bm_g ? 16 / L.bm_g : r; }
+__host__ __device__ inline int64_t page_kpos(const Layout& L, int r) { return (int64_t)2 * L.B * r; }
+__host__ __device__ inline int64_t page_vval(const Layout& L, int r) {
+  return (int64_t)2 * L.B * r + (int64_t)L.B * pos_bytes(L, r);
+}
+__host__ __device__ inline int64_t page_vpos(const Layout& L, int r) {
+  return (int64_t)4 * L.B * r + (int64_t)L.B * pos_bytes(L, r);
 }
 // Own rotation of closed segment s: R_k^T then R_v, fp32 [128][128] each.
 __host__ __device__ inline int64_t segrot_off(const Layout& L, int s) {

@@ -241,17 +241,50 @@ void top_r(const double* y, int keep, int r, int* out) {
   std::copy(c.begin(), c.begin() + r, out);
 }
 
+// Grouped top-r of the bitmap format ([S] sec. 5.1): the r / g groups of g
+// adjacent channels with the largest energy, summed in fp32 in channel order
+// (every bf16 square is exact in fp32, and the volatile keeps each sum a
+// separate rounding), ties to the lower group, among the first keep / g.
+void top_groups(const double* y, int keep, int r, int g, int* out) {
+  const int ng = keep / g;
+  std::vector<float> e((size_t)ng);
+  for (int j = 0; j < ng; ++j) {
+    float acc = 0.0f;
+    for (int i = 0; i < g; ++i) {
+      const float x = (float)y[g * j + i];
+      volatile float sq = x * x;
+      acc = i == 0 ? sq : acc + sq;
+    }
+    e[(size_t)j] = acc;
+  }
+  std::vector<int> c((size_t)ng);
+  std::iota(c.begin(), c.end(), 0);
+  std::stable_sort(c.begin(), c.end(), [&](int a, int b) { return e[(size_t)a] > e[(size_t)b]; });
+  std::sort(c.begin(), c.begin() + r / g);
+  for (int k = 0; k < r / g; ++k)
+    for (int i = 0; i < g; ++i) out[k * g + i] = c[(size_t)k] * g + i;
+}
+
 }  // namespace
 
 extern "C" mk_status mk_host_pack_blocks(const float* R_k, const float* R_v, const void* k, const void* v,
                                          int64_t row_stride, int32_t n_blocks, int32_t block, int32_t r,
                                          int32_t keep_channels, int64_t page_stride, int32_t meta_channels,
-                                         void* pages, void* meta, void* cmeta) {
+                                         int32_t page_format, int32_t elem_group, void* pages, void* meta,
+                                         void* cmeta) {
   constexpr int D = MK_HEAD_DIM;
   if (!R_k || !R_v || !k || !v || !pages || !meta || n_blocks < 0 || row_stride < D) return MK_EINVAL;
   if (block != 16 && block != 32 && block != 64) return MK_EINVAL;
   if (r < 1 || r > D || (keep_channels != 0 && (keep_channels < r || keep_channels > D))) return MK_EINVAL;
-  if (page_stride < (int64_t)6 * block * r) return MK_EINVAL;
+  if (page_format != MK_PAGES_PACKED && page_format != MK_PAGES_BITMAP) return MK_EINVAL;
+  if (page_format == MK_PAGES_PACKED ? elem_group != 0
+                                     : (elem_group != 0 && elem_group != 1 && elem_group != 2 && elem_group != 4 &&
+                                        elem_group != 8))
+    return MK_EINVAL;
+  const int g = page_format == MK_PAGES_BITMAP ? (elem_group ? elem_group : 1) : 0;
+  if (g > 1 && (r % g || keep_channels % g)) return MK_EINVAL;
+  const int pb = g ? D / g / 8 : r;  // position bytes per token: bitmap or uint8 indices
+  if (page_stride < (int64_t)block * (4 * r + 2 * pb)) return MK_EINVAL;
   if (meta_channels < 0 || meta_channels > MK_MAX_META_CHANNELS || (meta_channels > 0 && !cmeta)) return MK_EINVAL;
   const int keep = keep_channels ? keep_channels : D;
   const int64_t crow = meta_channels > 0 ? (5 * meta_channels + 15) / 16 * 16 : 0;
@@ -274,12 +307,21 @@ extern "C" mk_status mk_host_pack_blocks(const float* R_k, const float* R_v, con
           for (int j = 0; j < D; ++j) acc += x[j] * (double)R[(size_t)c * D + j];
           y[c] = bf16_round(acc);
         }
-        top_r(y.data(), keep, r, kept.data());
-        uint16_t* val = reinterpret_cast<uint16_t*>(page + (w == 0 ? 0 : 3 * Br));
-        uint8_t* idx = page + (w == 0 ? 2 * Br : 5 * Br);
+        if (g > 1)
+          top_groups(y.data(), keep, r, g, kept.data());
+        else
+          top_r(y.data(), keep, r, kept.data());
+        // [K values B r][K positions B pb][V values B r][V positions B pb]
+        uint16_t* val = reinterpret_cast<uint16_t*>(page + (w == 0 ? 0 : 2 * Br + block * pb));
+        uint8_t* pos = page + (w == 0 ? 2 * Br : 4 * Br + block * pb) + t * pb;
         for (int i = 0; i < r; ++i) {
           val[t * r + i] = bf16_bits(y[kept[i]]);
-          idx[t * r + i] = (uint8_t)kept[i];
+          if (g) {
+            const int j = kept[i] / g;  // bit j of the bitmap: byte j / 8, bit j % 8
+            pos[j >> 3] = (uint8_t)(pos[j >> 3] | (1u << (j & 7)));
+          } else {
+            pos[i] = (uint8_t)kept[i];
+          }
         }
         if (w == 0) {
           // min/max over the block of the zero-filled compressed key

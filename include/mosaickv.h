@@ -109,16 +109,36 @@ typedef struct mk_config {
                               keep_channels 0, and meta_channels must be 0.
                               Block min/max, scores, top-k and attention are the
                               same calls; with an identity rotation this is
-                              Quest's page selection on the raw keys. */
+                              Quest's page selection on the raw keys.
+                              MK_PAGES_BITMAP (2): the packed format of [S]
+                              sec. 5.1 with a position bitmap per vector in
+                              place of the uint8 indices (see elem_group). */
+  int32_t elem_group;      /* MK_PAGES_BITMAP only (else 0): the element-group
+                              size g, 1, 2, 4 or 8 (0 means 1).  Each vector
+                              stores a bitmap of 128/g bits, bit j set when
+                              channels g*j .. g*j+g-1 are kept (bit j in byte
+                              j/8 at bit j%8), followed by nothing else: the
+                              values stay r bf16 in ascending channel order.
+                              g = 1 keeps the per-vector top-r of [N] Eq. (9);
+                              g > 1 keeps the r/g groups with the largest
+                              energy (sum of squares over the group's channels,
+                              in fp32, summed in channel order), ties to the
+                              lower group ([S] sec. 5.1 variable-granularity
+                              bitmap, [S] sec. 4.3 element-group size).  Every
+                              segment's r and nonzero keep_channels must be
+                              multiples of g. */
 } mk_config;
 
 #define MK_PAGES_PACKED 0
 #define MK_PAGES_DENSE 1
+#define MK_PAGES_BITMAP 2
 
 /* Byte offsets of one (layer, sequence, kv head) inside the arena, for tests
  * and tools.  Pages: block b lives at pages + b*page_stride and holds
- * [K values B*r bf16][K indices B*r u8][V values B*r bf16][V indices B*r u8],
- * r being the block's segment r; token slot t of the block uses row t. */
+ * [K values B*r bf16][K positions][V values B*r bf16][V positions], r being
+ * the block's segment r and the positions B*r u8 channel indices
+ * (MK_PAGES_PACKED) or B bitmaps of 16/g bytes (MK_PAGES_BITMAP); token slot
+ * t of the block uses row t. */
 typedef struct mk_layout_info {
   int64_t rkt, rvt, rv;      /* fp32 [128][128]: R_k^T, R_v^T, R_v */
   int64_t sink_k, sink_v;    /* bf16 [S][128], rotated */
@@ -339,17 +359,23 @@ mk_status mk_alg2_segment_r(const void* seg, int64_t s, int64_t row_stride, int3
  * k + i * row_stride words; R_k, R_v: the head's rotations (as given to
  * mk_set_rotation).  Each token is rotated in fp64 (k' = k R^T) and rounded
  * to nearest-even bf16; its top-r over the first keep_channels channels
- * (0 = all) is kept as in mk_append_compress.  Outputs, all host memory:
- * pages (n_blocks x page_stride bytes: [K values B*r bf16][K indices B*r
- * u8][V values][V indices], the rest zero), meta (n_blocks x 2 x 128 bf16:
- * per-channel min and max of the zero-filled compressed keys), and, with
- * meta_channels > 0, cmeta (n_blocks rows of ((5 meta_channels + 15) / 16) *
- * 16 bytes, the compressed block keys).  MK_EINVAL: a null pointer, block not
- * 16, 32 or 64, r outside [1, 128], keep_channels outside {0} u [r, 128],
- * page_stride < 6 * block * r, meta_channels outside [0, 48]. */
+ * (0 = all) is kept as in mk_append_compress, in groups of elem_group
+ * channels for the bitmap format.  Outputs, all host memory: pages (n_blocks
+ * x page_stride bytes: [K values B*r bf16][K positions][V values][V
+ * positions], the positions being B*r u8 indices for MK_PAGES_PACKED or B
+ * bitmaps of 16/g bytes for MK_PAGES_BITMAP, the rest zero), meta (n_blocks
+ * x 2 x 128 bf16: per-channel min and max of the zero-filled compressed
+ * keys), and, with meta_channels > 0, cmeta (n_blocks rows of ((5
+ * meta_channels + 15) / 16) * 16 bytes, the compressed block keys).
+ * MK_EINVAL: a null pointer, block not 16, 32 or 64, page_format not
+ * MK_PAGES_PACKED or MK_PAGES_BITMAP, elem_group not as mk_config states, r
+ * outside [1, 128], keep_channels outside {0} u [r, 128], r or keep_channels
+ * not a multiple of g, page_stride below the page's size, meta_channels
+ * outside [0, 48]. */
 mk_status mk_host_pack_blocks(const float* R_k, const float* R_v, const void* k, const void* v, int64_t row_stride,
                               int32_t n_blocks, int32_t block, int32_t r, int32_t keep_channels, int64_t page_stride,
-                              int32_t meta_channels, void* pages, void* meta, void* cmeta);
+                              int32_t meta_channels, int32_t page_format, int32_t elem_group, void* pages, void* meta,
+                              void* cmeta);
 
 /* Replaces strategy segment `segment` of one (layer, sequence, kv head) with
  * pages, meta (and cmeta) packed by mk_host_pack_blocks for all of its blocks
@@ -367,7 +393,8 @@ mk_status mk_host_pack_blocks(const float* R_k, const float* R_v, const void* k,
  * segment must be closed: not the last one, which still receives appends.  r
  * may not exceed the largest r of the configuration (the page capacity).
  * MK_EINVAL: bad ids, a null buffer, only one of R_k and R_v, r or
- * keep_channels out of range; MK_ESTATE: the sequence has no prefill yet, or
+ * keep_channels out of range or not multiples of the element group; MK_ESTATE:
+ * the sequence has no prefill yet, or
  * the segment is the last or empty; MK_ENOTSUP: uncompressed pages. */
 mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, int32_t segment, int32_t r,
                           int32_t keep_channels, const float* R_k, const float* R_v, const void* pages,

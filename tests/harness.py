@@ -44,7 +44,8 @@ class Case:
     n_layers: int = 1
     oracle_units: list = None                     # [(layer, seq, kvh)]; None = all
     meta_channels: int = 0                        # > 0: channel-compressed per-block keys
-    page_format: int = 0                          # 1: uncompressed pages (the Quest comparator)
+    page_format: int = 0                          # 1: uncompressed pages (the Quest comparator); 2: bitmaps
+    elem_group: int = 0                           # bitmap pages: channels per bitmap bit (0 = 1)
 
     @property
     def G(self):
@@ -52,7 +53,14 @@ class Case:
 
     def strategy(self):
         return O.Strategy(self.n_sink, self.window, self.block, list(self.segments),
-                          self.topk_fixed, self.retain_permille, self.meta_channels)
+                          self.topk_fixed, self.retain_permille, self.meta_channels, self.bitmap_group)
+
+    @property
+    def bitmap_group(self):
+        return max(1, self.elem_group) if self.page_format == 2 else 0
+
+    def pos_bytes(self, r):
+        return 16 // self.bitmap_group if self.bitmap_group else r
 
 
 class Pair:
@@ -65,7 +73,7 @@ class Pair:
         self.T_total = [t + extra for t in case.seq_lens]
         cfg = make_config(case.n_q, case.n_kv, case.n_layers, len(case.seq_lens), max(self.T_total) + 1,
                           case.n_sink, case.window, case.block, case.segments, case.topk_fixed,
-                          case.retain_permille, case.meta_channels, case.page_format)
+                          case.retain_permille, case.meta_channels, case.page_format, case.elem_group)
         self.mk = MosaicKV(cfg, device)
         self.K, self.V, self.R = {}, {}, {}
         units = case.oracle_units
@@ -132,14 +140,16 @@ class Pair:
         return synth.query(len(c.seq_lens), c.n_q, D, synth.seed_for("q", c.seed, seed), device=self.dev)
 
 
-def page_rows(page_bytes, B, r, n_live):
-    """Split one packed page into (kval u16, kidx u8, vval u16, vidx u8) live rows."""
+def page_rows(page_bytes, B, r, n_live, pb=None):
+    """Split one packed page into (kval u16, kpos u8, vval u16, vpos u8) live rows; pb: position bytes per
+    token (r uint8 indices by default, or a bitmap's bytes)."""
     p = np.asarray(page_bytes, dtype=np.uint8)
-    Br = B * r
+    pb = r if pb is None else pb
+    Br, Bp = B * r, B * pb
     kv = p[:2 * Br].view(np.uint16).reshape(B, r)[:n_live]
-    ki = p[2 * Br:3 * Br].reshape(B, r)[:n_live]
-    vv = p[3 * Br:5 * Br].view(np.uint16).reshape(B, r)[:n_live]
-    vi = p[5 * Br:6 * Br].reshape(B, r)[:n_live]
+    ki = p[2 * Br:2 * Br + Bp].reshape(B, pb)[:n_live]
+    vv = p[2 * Br + Bp:4 * Br + Bp].view(np.uint16).reshape(B, r)[:n_live]
+    vi = p[4 * Br + Bp:4 * Br + 2 * Bp].reshape(B, pb)[:n_live]
     return kv, ki, vv, vi
 
 
@@ -190,7 +200,8 @@ def check_storage(p: Pair, unit):
     for b in range(nb):
         r = oc.r_of_block(b)
         lo, hi = oc.block_tokens(b)
-        got = page_rows(pages[b], B, r, hi - lo)
-        want = page_rows(oc.page_bytes(b), B, r, hi - lo)
+        pb = p.c.pos_bytes(r)
+        got = page_rows(pages[b], B, r, hi - lo, pb)
+        want = page_rows(oc.page_bytes(b), B, r, hi - lo, pb)
         for g, w_, name in zip(got, want, ("kval", "kidx", "vval", "vidx")):
             assert np.array_equal(g, w_), (b, name)

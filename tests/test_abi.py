@@ -97,8 +97,31 @@ def test_quest_comparator_config_rules(lib):
     nblk = (131072 + 64 - 4 - 256 + 31) // 32
     assert a > 8 * nblk * 4 * 32 * 128
     for bad in (dict(segments=[(0, 38, 0)]), dict(segments=[(0, 128, 0)], meta_channels=16),
-                dict(segments=[(0, 128, 0, 96)]), dict(segments=[(0, 128, 0)], page_format=2)):
+                dict(segments=[(0, 128, 0, 96)]), dict(segments=[(0, 128, 0)], page_format=3)):
         bad.setdefault("page_format", 1)
+        with pytest.raises(K.MosaicKVError) as e:
+            K.sizes(_cfg(**bad))
+        assert e.value.status == 1
+
+
+def test_bitmap_format_config_rules_and_page_size(lib):
+    # [S] sec. 5.1: a bitmap of 128 / g bits per vector in place of r uint8
+    # indices: pages of B (4 r + 2 * 16 / g) bytes instead of 6 B r.
+    nblk = (131072 + 64 - 4 - 256 + 31) // 32
+    a0, _, _ = K.sizes(_cfg())
+    for g, r in ((0, 38), (1, 38), (2, 38), (4, 40), (8, 40)):
+        a, _, _ = K.sizes(_cfg(segments=[(0, r, 0)], page_format=2, elem_group=g))
+        pb = 16 // max(1, g)
+        base = a0 - 8 * nblk * 6 * 32 * 38
+        assert abs(a - base - 8 * nblk * 32 * (4 * r + 2 * pb)) <= 8 * 4096
+    K.sizes(_cfg(segments=[(0, 40, 0, 96), (500, 16, 1)], page_format=2, elem_group=8, meta_channels=16))
+    for bad in (dict(elem_group=3), dict(elem_group=16), dict(elem_group=-1),
+                dict(elem_group=4, segments=[(0, 38, 0)]),           # r not a multiple of g
+                dict(elem_group=8, segments=[(0, 40, 0, 100)]),      # truncation not a multiple of g
+                dict(elem_group=2, page_format=0),                   # a group size needs bitmap pages
+                dict(elem_group=1, page_format=1, segments=[(0, 128, 0)])):
+        bad.setdefault("page_format", 2)
+        bad.setdefault("segments", [(0, 40, 0)])
         with pytest.raises(K.MosaicKVError) as e:
             K.sizes(_cfg(**bad))
         assert e.value.status == 1

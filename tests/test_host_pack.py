@@ -36,9 +36,12 @@ def _bf16_data(T, decay, seed):
     return Xb, O.bf16_bits(Xb)
 
 
-@pytest.mark.parametrize("rot,block,r,keep,mc", [("perm", 16, 32, 0, 0), ("identity", 32, 38, 96, 24),
-                                                 ("perm", 64, 20, 0, 48)])
-def test_host_pack_matches_oracle_bit_exact(rot, block, r, keep, mc):
+@pytest.mark.parametrize("rot,block,r,keep,mc,fmt,g", [
+    ("perm", 16, 32, 0, 0, 0, 0), ("identity", 32, 38, 96, 24, 0, 0), ("perm", 64, 20, 0, 48, 0, 0),
+    # bitmap pages ([S] sec. 5.1): one bit per channel, or per group of g channels
+    ("perm", 16, 38, 0, 0, 2, 1), ("perm", 32, 38, 96, 0, 2, 2), ("identity", 16, 40, 96, 24, 2, 4),
+    ("perm", 64, 24, 0, 0, 2, 8)])
+def test_host_pack_matches_oracle_bit_exact(rot, block, r, keep, mc, fmt, g):
     b = _lib()
     S, W = 4, 64
     T = S + W + 5 * block + 7                      # five complete middle blocks and a partial one
@@ -47,13 +50,15 @@ def test_host_pack_matches_oracle_bit_exact(rot, block, r, keep, mc):
     Rk = np.eye(D) if rot == "identity" else _signed_perm(3)
     Rv = np.eye(D) if rot == "identity" else _signed_perm(4)
     seg = (0, r, 0, keep)
-    oc = O.OracleCache(O.Strategy(S, W, block, [seg], 0, 100, mc), T)
+    bg = max(1, g) if fmt == 2 else 0
+    oc = O.OracleCache(O.Strategy(S, W, block, [seg], 0, 100, mc, bitmap_group=bg), T)
     oc.set_rotation(Rk, Rv)
     oc.append(K, V)
     n = 5
-    page_stride = 6 * block * r + 32                # any stride at least one page
+    pb = 16 // bg if bg else r
+    page_stride = block * (4 * r + 2 * pb) + 32     # any stride at least one page
     pages, meta, cmeta = b.host_pack_blocks(Rk, Rv, Kw[S:S + n * block], Vw[S:S + n * block], block, r, keep,
-                                            page_stride, mc)
+                                            page_stride, mc, fmt, g)
     mn, mx = oc.meta()
     for blk in range(n):
         want = oc.page_bytes(blk)
@@ -102,3 +107,13 @@ def test_host_pack_errors():
         b.host_pack_blocks(R, R, k, k, 16, 8, 4, 6 * 16 * 8)          # keep below r
     with pytest.raises(b.MosaicKVError):
         b.host_pack_blocks(R, R, k, k, 16, 8, 0, 6 * 16 * 8 - 1)      # page too small
+    with pytest.raises(b.MosaicKVError):
+        b.host_pack_blocks(R, R, k, k, 16, 8, 0, 6 * 16 * 8, 0, 0, 4)  # a group size needs bitmap pages
+    with pytest.raises(b.MosaicKVError):
+        b.host_pack_blocks(R, R, k, k, 16, 8, 0, 6 * 16 * 8, 0, 2, 3)  # group sizes are 1, 2, 4, 8
+    with pytest.raises(b.MosaicKVError):
+        b.host_pack_blocks(R, R, k, k, 16, 6, 0, 6 * 16 * 8, 0, 2, 4)  # r a multiple of the group
+    with pytest.raises(b.MosaicKVError):
+        b.host_pack_blocks(R, R, k, k, 16, 8, 12, 6 * 16 * 8, 0, 2, 8)  # keep a multiple of the group
+    with pytest.raises(b.MosaicKVError):
+        b.host_pack_blocks(R, R, k, k, 16, 8, 0, 16 * (4 * 8 + 2 * 16) - 1, 0, 2, 1)  # bitmap page too small
