@@ -25,7 +25,16 @@ Readings where the pages are silent:
   * Algorithm 2: "variance" is the mean over channels of each channel's
     population variance; the magnitude histogram has a given number of equal
     bins over [0, max |x|] (a value at the maximum goes to the last bin); the
-    entropy uses the natural log; the clamped r is rounded down.
+    entropy uses the natural log; the clamped r is rounded down;
+  * block size ([S] sec. 5.5 chooses block sizes under a variance
+    threshold): a candidate B cuts the segment into its complete blocks of B
+    consecutive tokens; its within-block variance is the mean over those
+    blocks of the mean over channels of each channel's population variance
+    inside the block (Algorithm 2's statistic, taken per block); the chosen B
+    is the largest candidate whose within-block variance is at most the
+    threshold, else the smallest candidate.  The statistic is the trace of
+    the within-block covariance over d, so it does not change under a
+    rotation of the channels.
 
 Parity status: every function is pinned by tests/test_strategy.py (brute
 force, closed forms, invariants, a library eigensolver).
@@ -97,3 +106,26 @@ def alg2_segment_r(S, budget, outlier_abs, outlier_ratio_max, alpha, r_min, r_ma
         r = budget / s * (1.0 + alpha * (1.0 - u))
     r = min(float(r_max), max(float(r_min), r))
     return int(np.floor(r)), st
+
+
+def within_block_variance(S, B):
+    """Mean over the complete blocks of B consecutive rows of S (s x d) of the
+    mean over channels of the population variance inside the block; None when
+    S holds no complete block."""
+    S = np.asarray(S, dtype=np.float64)
+    nb = S.shape[0] // B
+    if nb == 0:
+        return None
+    blocks = S[:nb * B].reshape(nb, B, S.shape[1])
+    return float(np.mean(np.var(blocks, axis=1)))
+
+
+def choose_block_size(S, candidates, threshold):
+    """[S] sec. 5.5: the largest candidate block size whose within-block
+    variance is at most the threshold, else the smallest candidate.
+    Returns (block size, [within-block variance or None per candidate])."""
+    cands = sorted(int(c) for c in candidates)
+    v = [within_block_variance(S, B) for B in cands]
+    ok = [B for B, x in zip(cands, v) if x is not None and x <= threshold]
+    return (max(ok) if ok else cands[0]), v
+

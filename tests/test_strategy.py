@@ -195,3 +195,62 @@ def test_native_alg2_errors():
     assert lib.mk_cov_update(None, None, 0, 0, 4) == 1     # MK_EINVAL
     r = ctypes.c_int32(0)
     assert lib.mk_choose_r(None, 4, ctypes.c_double(0.1), ctypes.byref(r)) == 1
+
+
+# ---- block-size choice ([S] sec. 5.5) ------------------------------------------
+def _within_loops(S, B):
+    """The statistic with explicit loops (per block, per channel, per token)."""
+    s, d = len(S), len(S[0])
+    nb = s // B
+    tot = 0.0
+    for b in range(nb):
+        acc = 0.0
+        for c in range(d):
+            col = [S[b * B + t][c] for t in range(B)]
+            m = sum(col) / B
+            acc += sum((x - m) ** 2 for x in col) / B
+        tot += acc / d
+    return tot / nb
+
+
+def test_oracle_within_block_variance_closed_forms_and_loops():
+    # Rows constant within 16-token runs, alternating +a / -a between runs:
+    # blocks of 16 have variance 0, blocks of 32 or 64 mix the two levels
+    # equally, so each channel's variance is a^2.
+    a = np.arange(2, 10) / 4.0           # dyadic: block means and variances exact
+    S = np.concatenate([np.tile(a if i % 2 == 0 else -a, (16, 1)) for i in range(8)])
+    assert SO.within_block_variance(S, 16) == 0.0
+    assert SO.within_block_variance(S, 32) == pytest.approx(np.mean(a ** 2), rel=1e-14)
+    assert SO.within_block_variance(S, 64) == pytest.approx(np.mean(a ** 2), rel=1e-14)
+    assert SO.within_block_variance(S[:10], 16) is None          # no complete block
+    rng = np.random.default_rng(40)
+    X = rng.standard_normal((70, 5)) * np.arange(1, 6)
+    for B in (1, 4, 16, 32):
+        assert SO.within_block_variance(X, B) == pytest.approx(_within_loops(X.tolist(), B), rel=1e-12)
+    # iid rows of variance sigma^2: the expected population variance of B samples is sigma^2 (1 - 1/B)
+    X = rng.standard_normal((64 * 2000, 4)) * 1.5
+    for B in (16, 64):
+        assert SO.within_block_variance(X, B) == pytest.approx(2.25 * (1 - 1 / B), rel=0.01)
+
+
+def test_oracle_within_block_variance_rotation_invariant():
+    rng = np.random.default_rng(41)
+    X = rng.standard_normal((256, 16)) * 0.8 ** np.arange(16)
+    Q, _ = np.linalg.qr(rng.standard_normal((16, 16)))
+    for B in (16, 32, 64):
+        assert SO.within_block_variance(X @ Q.T, B) == pytest.approx(SO.within_block_variance(X, B), rel=1e-12)
+
+
+def test_oracle_choose_block_size_rule():
+    a = np.arange(2, 10) / 4.0           # dyadic: block means and variances exact
+    S = np.concatenate([np.tile(a if i % 2 == 0 else -a, (16, 1)) for i in range(8)])
+    va2 = float(np.mean(a ** 2))
+    assert SO.choose_block_size(S, [16, 32, 64], 0.0)[0] == 16
+    assert SO.choose_block_size(S, [64, 16, 32], va2 * 1.001)[0] == 64   # largest under the threshold
+    assert SO.choose_block_size(-np.abs(S), [16, 32, 64], 0.0)[0] == 64  # constant rows: every size qualifies
+    assert SO.choose_block_size(S + np.arange(128)[:, None], [16, 32, 64], 0.0)[0] == 16  # none: smallest
+    B, v = SO.choose_block_size(S[:40], [16, 32, 64], 10.0)
+    assert B == 32 and v[2] is None                                      # 64 has no complete block
+    # a planted mistake (the smallest qualifying size) fails the rule above
+    ok = [Bc for Bc, x in zip([16, 32, 64], SO.choose_block_size(S, [16, 32, 64], va2 * 1.001)[1]) if x <= va2 * 1.001]
+    assert min(ok) != SO.choose_block_size(S, [16, 32, 64], va2 * 1.001)[0]
