@@ -88,6 +88,7 @@ _SIGS = {
     "mk_choose_r": [c_vp, c_i32, ctypes.c_double, ctypes.POINTER(c_i32)],
     "mk_alg2_segment_r": [c_vp, c_i64, c_i64, c_i32, ctypes.c_double, ctypes.POINTER(MkAlg2Params),
                           ctypes.POINTER(MkSegStats), ctypes.POINTER(c_i32)],
+    "mk_choose_block_size": [c_vp, c_i64, c_i64, c_i32, c_vp, c_i32, ctypes.c_double, c_vp, ctypes.POINTER(c_i32)],
     "mk_host_pack_blocks": [c_vp, c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_i32, c_i32, c_i64, c_i32, c_i32, c_i32,
                             c_vp, c_vp, c_vp],
     "mk_swap_segment": [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp],
@@ -401,6 +402,19 @@ def alg2_segment_r(seg, budget, outlier_abs, outlier_ratio_max, alpha, r_min, r_
                                                          float(budget), ctypes.byref(p), ctypes.byref(st),
                                                          ctypes.byref(r)))
     return r.value, {"variance": st.variance, "outlier_ratio": st.outlier_ratio, "entropy": st.entropy}
+
+
+def choose_block_size(seg, candidates, threshold):
+    """[S] sec. 5.5 block-size choice for one segment (seg: bf16 words as uint16, or a CPU bf16 tensor):
+    (block size, within-block variance per candidate, NaN where no complete block)."""
+    w = _bf16_words(seg)
+    cands = np.ascontiguousarray(candidates, dtype=np.int32)
+    var = np.empty(cands.shape[0], dtype=np.float64)
+    b = c_i32(0)
+    _check("mk_choose_block_size", load().mk_choose_block_size(
+        _np_ptr(w), w.shape[0], w.shape[1], w.shape[1], _np_ptr(cands), cands.shape[0], float(threshold),
+        _np_ptr(var), ctypes.byref(b)))
+    return b.value, var
 
 
 def host_pack_blocks(Rk, Rv, k, v, block, r, keep_channels, page_stride, meta_channels=0, page_format=0,

@@ -208,6 +208,57 @@ extern "C" mk_status mk_alg2_segment_r(const void* seg, int64_t s, int64_t row_s
   return MK_OK;
 }
 
+// [S] sec. 5.5: block sizes under a variance threshold.  Per candidate B, the
+// mean over the segment's complete blocks of the mean channel variance inside
+// each block; the largest B at or under the threshold wins.
+extern "C" mk_status mk_choose_block_size(const void* seg, int64_t s, int64_t row_stride, int32_t d,
+                                          const int32_t* cands, int32_t n_cands, double threshold,
+                                          double* within_var, int32_t* block) {
+  if (!seg || !cands || !block || s < 1 || d < 1 || row_stride < d || n_cands < 1 || n_cands > 16 ||
+      !(threshold >= 0.0))
+    return MK_EINVAL;
+  for (int32_t i = 0; i < n_cands; ++i) {
+    if (cands[i] < 1) return MK_EINVAL;
+    for (int32_t j = 0; j < i; ++j)
+      if (cands[j] == cands[i]) return MK_EINVAL;
+  }
+  int32_t best = -1, smallest = cands[0];
+  std::vector<double> mean((size_t)d), var((size_t)d);
+  for (int32_t i = 0; i < n_cands; ++i) {
+    const int32_t B = cands[i];
+    smallest = std::min(smallest, B);
+    const int64_t nb = s / B;
+    double v = std::nan("");
+    if (nb > 0) {
+      double tot = 0.0;
+      for (int64_t b = 0; b < nb; ++b) {
+        std::fill(mean.begin(), mean.end(), 0.0);
+        std::fill(var.begin(), var.end(), 0.0);
+        for (int32_t t = 0; t < B; ++t) {
+          const uint16_t* row = row_ptr(seg, b * B + t, row_stride);
+          for (int32_t c = 0; c < d; ++c) mean[c] += bf16_to_double(row[c]);
+        }
+        for (int32_t c = 0; c < d; ++c) mean[c] /= (double)B;
+        for (int32_t t = 0; t < B; ++t) {
+          const uint16_t* row = row_ptr(seg, b * B + t, row_stride);
+          for (int32_t c = 0; c < d; ++c) {
+            const double dx = bf16_to_double(row[c]) - mean[c];
+            var[c] += dx * dx;
+          }
+        }
+        double blk = 0.0;
+        for (int32_t c = 0; c < d; ++c) blk += var[c] / (double)B;
+        tot += blk / (double)d;
+      }
+      v = tot / (double)nb;
+      if (v <= threshold && B > best) best = B;
+    }
+    if (within_var) within_var[i] = v;
+  }
+  *block = best > 0 ? best : smallest;
+  return MK_OK;
+}
+
 // ---- Host re-compression of complete blocks ([S] sec. 5.4: the CPU side of
 // the double-buffered compression).  Same formats as the device path; the
 // rotation is exact fp64 rounded once to bf16.

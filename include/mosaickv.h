@@ -346,6 +346,23 @@ typedef struct mk_seg_stats {
 mk_status mk_alg2_segment_r(const void* seg, int64_t s, int64_t row_stride, int32_t d, double budget,
                             const mk_alg2_params* params, mk_seg_stats* stats, int32_t* r);
 
+/* Block-size choice of [S] sec. 5.5 (block sizes chosen under a variance
+ * threshold) for one segment of s vectors of d channels (seg: s rows of d
+ * bf16 words, row stride row_stride words; rotated or not: the statistic
+ * does not change under a rotation of the channels).  For each candidate B
+ * the segment is cut into its complete blocks of B consecutive vectors; the
+ * candidate's within-block variance is the mean over those blocks of the mean
+ * over channels of each channel's population variance inside the block
+ * (Algorithm 2's variance, per block).  *block receives the largest candidate
+ * whose within-block variance is at most threshold, else the smallest
+ * candidate.  within_var (optional, n_cands doubles, in the order given)
+ * receives each candidate's statistic, NaN for a candidate with no complete
+ * block (which never qualifies).  fp64 throughout.  MK_EINVAL: null seg or
+ * block or cands, s < 1, d < 1, row_stride < d, n_cands outside [1, 16], a
+ * candidate < 1 or repeated, threshold negative or NaN. */
+mk_status mk_choose_block_size(const void* seg, int64_t s, int64_t row_stride, int32_t d, const int32_t* cands,
+                               int32_t n_cands, double threshold, double* within_var, int32_t* block);
+
 /* ---- Double-buffered re-compression of a closed segment ([S] sec. 5.4) ----
  * While decoding goes on with the GPU's compression of a segment, the CPU
  * re-compresses the segment's tokens exactly (fp64 rotation, rounded once to

@@ -254,3 +254,40 @@ def test_oracle_choose_block_size_rule():
     # a planted mistake (the smallest qualifying size) fails the rule above
     ok = [Bc for Bc, x in zip([16, 32, 64], SO.choose_block_size(S, [16, 32, 64], va2 * 1.001)[1]) if x <= va2 * 1.001]
     assert min(ok) != SO.choose_block_size(S, [16, 32, 64], va2 * 1.001)[0]
+
+
+@pytest.mark.parametrize("seed,smooth", [(42, 0.0), (43, 0.9), (44, 0.99)])
+def test_native_choose_block_size_matches_oracle(seed, smooth):
+    # Keys that drift slowly along the sequence (an AR(1) walk of strength
+    # `smooth`) favour large blocks; iid keys favour none.
+    b = _lib()
+    rng = np.random.default_rng(seed)
+    n, d = 1000, 128
+    X = np.empty((n, d))
+    X[0] = rng.standard_normal(d)
+    for t in range(1, n):
+        X[t] = smooth * X[t - 1] + math.sqrt(1 - smooth ** 2) * rng.standard_normal(d)
+    X *= 0.92 ** np.arange(d)
+    words, vals = _bf16_words(X)
+    cands = [64, 16, 32, 512, 2048]
+    for thr in (0.0, 0.01, 0.05, 0.2, 1.0):
+        B, v = b.choose_block_size(words, cands, thr)
+        B_o, v_o = SO.choose_block_size(vals, cands, thr)
+        assert B == B_o
+        order = sorted(cands)
+        for i, c in enumerate(cands):
+            want = v_o[order.index(c)]
+            if want is None:
+                assert math.isnan(v[i])
+            else:
+                assert v[i] == pytest.approx(want, rel=1e-12, abs=1e-15)
+
+
+def test_native_choose_block_size_errors():
+    b = _lib()
+    w, _ = _bf16_words(np.ones((64, 8)))
+    for cands, thr in (([16, 16], 0.1), ([0, 16], 0.1), ([], 0.1), ([16], -1.0), ([16], float("nan")),
+                       (list(range(1, 18)), 0.1)):
+        with pytest.raises(b.MosaicKVError):
+            b.choose_block_size(w, cands, thr)
+    assert b.choose_block_size(w, [128, 16], 0.0)[0] == 16      # 128 has no complete block
