@@ -314,9 +314,15 @@ mk_status mk_create(const mk_config* cfg, void* arena, size_t arena_bytes, void*
   if (((uintptr_t)arena % kAlign) || ((uintptr_t)workspace % kAlign)) return MK_EINVAL;
   Plan p = make_plan(cfg);
   if ((int64_t)arena_bytes < p.arena_bytes || (int64_t)workspace_bytes < p.ws_bytes) return MK_ENOMEM;
-  int r_min = MK_HEAD_DIM;
-  for (int i = 0; i < cfg->n_segments; ++i) r_min = std::min(r_min, (int)cfg->seg[i].r);
-  if (mk::attn_plan(p.L, r_min) == 0) return MK_ENOTSUP;
+  // Page tokens a unit may attend: its selection plus the always-attended
+  // segments (a fraction of the prefill, at most of the capacity).
+  int64_t attend_max = (int64_t)p.L.k_max * cfg->block;
+  for (int i = 0; i < cfg->n_segments; ++i)
+    if (cfg->seg[i].always) {
+      const int end = i + 1 < cfg->n_segments ? cfg->seg[i + 1].begin_permille : 1000;
+      attend_max += (int64_t)(end - cfg->seg[i].begin_permille) * cfg->max_tokens / 1000 + 2 * cfg->block;
+    }
+  if (mk::attn_plan(p.L, attend_max) == 0) return MK_ENOTSUP;
   if (!mk::select_plan_ok(p.L)) return MK_ENOTSUP;
   bind_pointers(p, arena, workspace);
   mk_ctx* ctx = new (std::nothrow) mk_ctx();

@@ -249,30 +249,31 @@ size_t smem_for(const Layout& L, int nst, int nw) {
 
 // Shared-memory plan; fills attn_nst / attn_sb and returns the dynamic shared
 // memory size (0 if nothing fits).
-size_t attn_plan(Layout& L, int /*r_min*/) {
+size_t attn_plan(Layout& L, int64_t attend_max) {
   // Double-buffered stages first (they hide the copy latency), then as many
   // warps as fit.
   // Warps per CTA are a multiple of 4, an equal share for each of the SM's
   // four sub-partitions.
-  // Long selections (many 16-token groups per warp) are bound by the main
-  // loop's densify work: 16 warps with one stage each (the next copy goes out
-  // as soon as a stage is consumed) beat 12 warps with two.  Short ones are
-  // bound by each warp's latency chain: two stages, 12 warps (which also get
-  // more registers).
-  const bool long_sel = (int64_t)L.k_max * L.B >= kLongSelTokens;
+  // Long selections (many 16-token groups per warp; attend_max: the page
+  // tokens a unit may attend, selected and always-attended) are bound by the
+  // main loop's densify work: more warps with one stage each (the next copy
+  // goes out as soon as a stage is consumed) beat fewer with two.  Short ones
+  // are bound by each warp's latency chain: two stages, 12 warps (which also
+  // get more registers).
+  const bool long_sel = std::max<int64_t>((int64_t)L.k_max * L.B, attend_max) >= kLongSelTokens;
   int plans[8][2] = {{2, 12}, {2, 8}, {2, 4}, {0, 0}, {0, 0}, {0, 0}, {0, 0}, {0, 0}};
   if (long_sel) {
-    const int lp[4][2] = {{1, 16}, {2, 12}, {2, 8}, {2, 4}};
-    for (int i = 0; i < 4; ++i) {
+    const int lp[5][2] = {{1, 16}, {1, 12}, {2, 8}, {2, 4}, {1, 4}};
+    for (int i = 0; i < 5; ++i) {
       plans[i][0] = lp[i][0];
       plans[i][1] = lp[i][1];
     }
   }
   if (const char* e = std::getenv("MK_ATTN_PLAN")) {  // tuning override: "stages,warps"
     int a = 0, b = 0;
-    // one stage goes with 16 warps, two or more with at most 12
+    // one stage (the one-stage kernel, up to 16 warps) or two or more with at most 12 warps
     if (std::sscanf(e, "%d,%d", &a, &b) == 2 && b >= 4 && b <= kMaxWarps && b % 4 == 0 &&
-        ((b > 12 && a == 1) || (b <= 12 && a >= 2))) {
+        (a == 1 || (b <= 12 && a >= 2))) {
       plans[0][0] = a;
       plans[0][1] = b;
     }
@@ -1112,7 +1113,9 @@ cudaError_t launch_attn_g(const Layout& L, int layer, const CallSeqs& cs, const 
                           const int32_t* items, const int32_t* min_parts, cudaStream_t s) {
   const size_t smem = attn_smem_bytes(L, 0);
   if (smem == 0 || smem > 227 * 1024) return cudaErrorInvalidConfiguration;
-  const bool wide = L.attn_nc > 12;  // launch bounds of 16 warps (at most 128 registers)
+  // One stage per warp: the one-stage kernel (launch bounds of 16 warps, at
+  // most 128 registers), launched with the plan's 12 or 16 warps.
+  const bool wide = L.attn_nst == 1;
   // The variant with rotation classes only where some unit of the call has a
   // segment under its own rotation (its CTAs need one per class).
   bool own = false;

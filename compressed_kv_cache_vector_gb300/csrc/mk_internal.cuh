@@ -425,7 +425,7 @@ cudaError_t launch_dense_attn(const Layout& L, const CallSeqs& cs, const uint16_
 struct AttnSplit {
   int32_t off[MK_MAX_CALL_SEQS + 1];
 };
-size_t attn_plan(Layout& L, int r_min);
+size_t attn_plan(Layout& L, int64_t attend_max);
 cudaError_t launch_gram(const uint16_t* x, int64_t n_rows, int64_t row_stride, float* gram,
                         cudaStream_t s);
 size_t attn_smem_bytes(const Layout& L, int r_max);

@@ -84,7 +84,7 @@ extern "C" mk_status mk_dense_decode_attn_noalloc(int32_t n_q_heads, int32_t n_k
   L.counters = reinterpret_cast<int32_t*>(scratch + off_cnt);
   L.part_acc = reinterpret_cast<float*>(scratch + off_acc);
   L.part_ml = reinterpret_cast<float*>(scratch + off_ml);
-  if (mk::attn_plan(L, 1) == 0) return MK_ENOTSUP;
+  if (mk::attn_plan(L, 0) == 0) return MK_ENOTSUP;
 
   mk::CallSeqs cs{};  // on the stack: nothing is allocated, host or device
   cs.n = n_seqs;
