@@ -3,9 +3,10 @@
 The benchmark's decode step is mk_append_select (one new token per sequence,
 appended and compressed, then block selection: [N] Eq. (9), (12); [S] sec.
 4.2) followed by mk_decode_attn ([N] Eq. (13), (14); [S] sec. 5.3).  Here
-that same pair of calls runs after a bulk prefill at three workload shapes,
+that same pair of calls runs after a bulk prefill at four workload shapes,
 and a few (sequence, kv head) units are followed by the fp64 oracle:
 
+  * the 32K-token layer at batch 4 (block 16, window 128, 10% of blocks);
   * the 128K-token layer (T = 131072, 8 kv heads, GQA 4, r = 38, block 32,
     window 256, 10% of blocks), rotations exact in bf16 (signed permutations)
     so that every stored byte can be compared;
@@ -99,6 +100,20 @@ def _case_from(wl, **kw):
                 retain_permille=wl.retain_permille, decay=wl.decay)
     base.update(kw)
     return Case(**base)
+
+
+@pytest.mark.parametrize("rot", ["perm", "eigh"])
+def test_32k_layer_batch_4_fused_decode_steps(rot):
+    # The 32K-token layer at batch 4 (block 16, window 128, 10% of blocks,
+    # 2040 blocks and k = 204 per unit), two units of different sequences
+    # followed by the oracle.
+    wl = configs.get("c2")
+    case = _case_from(wl, rot=rot, steps=[1, 1], seed=201, oracle_units=[(0, 1, 2), (0, 3, 7)])
+    p = Pair(case)
+    assert _fused_steps(p, 2) <= 1
+    if rot == "perm":
+        for u in p.units:
+            check_storage(p, u)
 
 
 def test_128k_layer_fused_decode_steps():
