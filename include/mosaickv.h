@@ -57,7 +57,7 @@ typedef enum mk_status {
   MK_ECUDA = 4,    /* a CUDA runtime call failed */
   MK_EDEVICE = 5,  /* a kernel set the device error word */
   MK_ETIMEOUT = 6, /* a bounded device-side wait gave up */
-  MK_ENOTSUP = 7   /* valid but not supported by this build */
+  MK_ENOTSUP = 7   /* valid but not supported by the library */
 } mk_status;
 
 typedef struct mk_ctx mk_ctx;

@@ -1,6 +1,6 @@
 """fp64 oracle for the MosaicKV decode-time hot path.  TEST INFRASTRUCTURE.
 
-This module is the checker, not the product.  Only the test suite,
+This module is test infrastructure, not the product.  Only the test suite,
 ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference arm
 may import it.  The CUDA library and its Python binding never do, and this
 module imports nothing from them: the two sides share only the seeded input

@@ -1,9 +1,9 @@
 """fp64 oracle for MosaicKV's host-side strategy generation.  TEST INFRASTRUCTURE.
 
-This module is the checker, not the product: only the test suite may import
+This module is test infrastructure, not the product: only the test suite may import
 it.  The library's native strategy calls (mk_cov_update, mk_rotation_from_cov,
-mk_choose_r, mk_alg2_segment_r) never do, and this module imports nothing from
-them.
+mk_choose_r, mk_alg2_segment_r, mk_choose_block_size) never do, and this module
+imports nothing from them.
 
 Each function writes out the definition it follows in float64, with numpy's
 matmul and eigh as the only library steps.
@@ -15,7 +15,8 @@ Sources (cited by page title and equation/section):
       Algorithm 2 (per-segment channel count).
   [S] "MosaicKV: Serving Long-Context LLM with Dynamic Two-D KV Cache
       Compression" (paperlayer.ai summary): sec. 5.5 (incremental covariance,
-      channel parameters under a loss threshold).
+      channel parameters under a loss threshold, block sizes under a variance
+      threshold).
 
 Readings where the pages are silent:
   * the covariance is the uncentred second moment sum x^T x ([N] Eq. (4)
