@@ -39,7 +39,8 @@ Readings where the pages are silent:
   * sec. 5.1 bitmap (off by default): the indices are replaced by a bitmap
     of d / g bits per vector, one bit per group of g adjacent channels; for
     g > 1 the vector keeps the r / g groups of largest energy (fp32, summed
-    in channel order), ties to the lower group;
+    in channel order), ties to the lower group; g may differ per segment
+    (sec. 4.3), and a re-compressed segment keeps its g;
   * sec. 5.2 variants (off by default): "bottom channels truncated" = the
     per-vector top-r picks among the first keep_channels rotated channels
     only; "per-block keys channel-compressed" = each block keeps the m
@@ -222,7 +223,7 @@ class Strategy:
     n_sink: int
     window: int
     block: int
-    segments: list            # [(begin_permille, r, always[, keep_channels])]
+    segments: list            # [(begin_permille, r, always[, keep_channels[, elem_group]])]
     topk_fixed: int = 0
     retain_permille: int = 0
     meta_channels: int = 0    # > 0: channel-compressed per-block keys ([S] sec. 5.2)
@@ -232,7 +233,11 @@ class Strategy:
     def __post_init__(self):
         # keep_channels: the first channels eligible for the top-r; 0 or
         # absent means all of them ([S] sec. 5.2 truncates the bottom 25%).
-        self.segments = [(sg[0], sg[1], sg[2], (sg[3] if len(sg) > 3 and sg[3] else D_HEAD))
+        # elem_group (bitmap pages only): the segment's own element-group
+        # size ([S] sec. 4.3 lists it in each segment's strategy); 0 or
+        # absent means the cache's bitmap_group.
+        self.segments = [(sg[0], sg[1], sg[2], (sg[3] if len(sg) > 3 and sg[3] else D_HEAD),
+                          (sg[4] if len(sg) > 4 and sg[4] else self.bitmap_group) if self.bitmap_group else 0)
                          for sg in self.segments]
 
 
@@ -401,6 +406,10 @@ class OracleCache:
     def keep_of_block(self, b):
         return self.st.segments[block_segment(b, self.firsts)][3]
 
+    def group_of_block(self, b):
+        """The block's element-group size (bitmap pages), 0 for uint8 indices."""
+        return self.st.segments[block_segment(b, self.firsts)][4]
+
     def rotations_of_block(self, b):
         """(R_k, R_v) the block's tokens are stored in: the segment's own after a
         re-compression under its own rotation ([S] sec. 5.4), else the head's."""
@@ -450,9 +459,10 @@ class OracleCache:
         for b in np.unique(blocks):
             sel = pos[blocks == b]
             r, keep = self.r_of_block(int(b)), self.keep_of_block(int(b))
+            g = max(1, self.group_of_block(int(b)))
             for src, dst_idx, dst_val, dense in ((self.Kr, self.kidx, self.kval, self.Kt),
                                                 (self.Vr, self.vidx, self.vval, self.Vt)):
-                idx, vals = topr_groups(src[sel].astype(np.float64), r, max(1, self.st.bitmap_group), keep)
+                idx, vals = topr_groups(src[sel].astype(np.float64), r, g, keep)
                 dst_idx[sel, :r] = idx
                 dst_idx[sel, r:] = 0
                 dst_val[sel, :r] = vals
@@ -475,8 +485,8 @@ class OracleCache:
         0 = all channels), and its blocks' min/max recomputed."""
         assert 0 <= seg < len(self.st.segments) - 1, "only a closed segment is re-compressed"
         segs = list(self.st.segments)
-        begin, _, always, _ = segs[seg]
-        segs[seg] = (begin, r, always, keep if keep else self.d)
+        begin, _, always, _, g = segs[seg]          # the segment keeps its element-group size
+        segs[seg] = (begin, r, always, keep if keep else self.d, g)
         self.st = Strategy(self.st.n_sink, self.st.window, self.st.block, segs, self.st.topk_fixed,
                            self.st.retain_permille, self.st.meta_channels, self.st.bitmap_group)
         if Rk is not None:
@@ -520,7 +530,7 @@ class OracleCache:
         """
         B = self.st.block
         r = self.r_of_block(b)
-        g = self.st.bitmap_group
+        g = self.group_of_block(b)
         lo, hi = self.block_tokens(b)
         n = hi - lo
         kv = np.zeros((B, r), dtype=np.uint16)

@@ -727,34 +727,42 @@ def test_bitmap_page_byte_layout():
     assert O.packed_bytes_per_token(40, 4) == 2 * (80 + 4)
 
 
-@pytest.mark.parametrize("g", [1, 4])
-def test_bitmap_cache_rows_and_attention_by_explicit_sums(g):
-    # The zero-filled rows hold each token's kept groups; attention read from
-    # the page bytes (decoding the bitmaps by hand) equals the oracle's.
-    st = O.Strategy(4, 32, 16, [(0, 40, 0), (500, 16, 0)], 0, 100, bitmap_group=g)
-    c, _, _ = _cache(700, st, 71)
+@pytest.mark.parametrize("g,segs", [(1, [(0, 40, 0), (500, 16, 0)]), (4, [(0, 40, 0), (500, 16, 0)]),
+                                    (4, [(0, 40, 0, 0, 8), (400, 16, 0, 96, 2), (700, 40, 0, 0, 1)])],
+                         ids=["g1", "g4", "per-segment-g"])
+def test_bitmap_cache_rows_and_attention_by_explicit_sums(g, segs):
+    # The zero-filled rows hold each token's kept groups (each segment with
+    # its own group size where it gives one, [S] sec. 4.3); every page
+    # decoded by hand from its bytes gives back those rows.
+    st = O.Strategy(4, 32, 16, segs, 0, 100, bitmap_group=g)
+    c, _, _ = _cache(900, st, 71)
+    assert [c.st.segments[i][4] for i in range(len(segs))] == [sg[4] if len(sg) > 4 else g for sg in segs]
     for t in range(4, 4 + c.n_mid, 5):
-        r = c.r_of_block((t - 4) // 16)
+        b = (t - 4) // 16
+        r = c.r_of_block(b)
+        g = c.group_of_block(b)
+        kp = c.keep_of_block(b)
         for rows, dense in ((c.Kr, c.Kt), (c.Vr, c.Vt)):
             x = rows[t].astype(np.float64)
             if g > 1:   # a Python sort of scalar fp32 energies, ties to the lower group
                 e = []
-                for j in range(128 // g):
+                for j in range(kp // g):
                     acc = np.float32(0.0)
                     for i in range(g):
                         acc = np.float32(acc + np.float32(x[j * g + i]) * np.float32(x[j * g + i]))
                     e.append(acc)
-                best = sorted(sorted(range(128 // g), key=lambda j: (-e[j], j))[:r // g])
+                best = sorted(sorted(range(kp // g), key=lambda j: (-e[j], j))[:r // g])
                 keep = [j * g + i for j in best for i in range(g)]
             else:
-                keep = sorted(sorted(range(128), key=lambda j: (-abs(x[j]), j))[:r])
+                keep = sorted(sorted(range(kp), key=lambda j: (-abs(x[j]), j))[:r])
             z = np.zeros(128)
             z[keep] = x[keep]
             assert np.array_equal(dense[t].astype(np.float64), z)
     # decode every page by hand and compare with Kt / Vt
-    nb = 16 // g
     for b in range(c.n_blocks_mid()):
         r = c.r_of_block(b)
+        g = c.group_of_block(b)
+        nb = 16 // g
         lo, hi = c.block_tokens(b)
         pg = c.page_bytes(b)
         Br = 16 * r
