@@ -34,7 +34,8 @@ class MosaicKVError(RuntimeError):
 
 
 class MkSegment(ctypes.Structure):
-    _fields_ = [("begin_permille", c_i32), ("r", c_i32), ("always", c_i32), ("keep_channels", c_i32)]
+    _fields_ = [("begin_permille", c_i32), ("r", c_i32), ("always", c_i32), ("keep_channels", c_i32),
+                ("elem_group", c_i32)]
 
 
 class MkConfig(ctypes.Structure):
@@ -157,6 +158,7 @@ def make_config(n_q_heads, n_kv_heads, n_layers, max_seqs, max_tokens, n_sink, w
         b, r, a = sg[:3]
         keep = sg[3] if len(sg) > 3 else 0
         c.seg[i].begin_permille, c.seg[i].r, c.seg[i].always, c.seg[i].keep_channels = b, r, a, keep
+        c.seg[i].elem_group = sg[4] if len(sg) > 4 else 0   # bitmap pages: the segment's own group size
     return c
 
 

@@ -40,6 +40,13 @@ struct Plan {
   int64_t n_units, units_off, arena_bytes, ws_bytes;
 };
 
+// Element-group size of segment i of a bitmap-page configuration: its own,
+// else the configuration's, else 1.
+int seg_group_of(const mk_config* c, int i) {
+  return c->seg[i].elem_group ? c->seg[i].elem_group : (c->elem_group ? c->elem_group : 1);
+}
+int log2_group(int g) { return g >= 8 ? 3 : g >= 4 ? 2 : g >= 2 ? 1 : 0; }
+
 mk_status check_config(const mk_config* c) {
   if (!c) return MK_EINVAL;
   if (c->head_dim != MK_HEAD_DIM) return MK_EINVAL;
@@ -64,8 +71,11 @@ mk_status check_config(const mk_config* c) {
     prev = s.begin_permille;
     if (c->page_format == MK_PAGES_DENSE && (s.r != MK_HEAD_DIM || s.keep_channels != 0)) return MK_EINVAL;
     if (c->page_format == MK_PAGES_BITMAP) {
-      const int g = c->elem_group ? c->elem_group : 1;
+      const int g = seg_group_of(c, i);
+      if (g != 1 && g != 2 && g != 4 && g != 8) return MK_EINVAL;
       if (s.r % g || s.keep_channels % g) return MK_EINVAL;
+    } else if (s.elem_group != 0) {
+      return MK_EINVAL;
     }
   }
   if (c->page_format != MK_PAGES_PACKED && c->page_format != MK_PAGES_DENSE && c->page_format != MK_PAGES_BITMAP)
@@ -100,9 +110,15 @@ Plan make_plan(const mk_config* c) {
   L.k_max = std::max(1, mk::n_select(L, L.nblk_cap));
   L.keys_stride = (std::max(1, L.nblk_cap) + 3) & ~3;
   L.dense_pages = c->page_format == MK_PAGES_DENSE ? 1 : 0;
-  L.bm_g = c->page_format == MK_PAGES_BITMAP ? (c->elem_group ? c->elem_group : 1) : 0;
-  // packed: K and V values (2 r bytes each) and positions; dense: 2 x 256 bytes per token
-  L.page_stride = L.dense_pages ? (int64_t)4 * L.B * MK_HEAD_DIM : page_vpos(L, r_max) + (int64_t)L.B * pos_bytes(L, r_max);
+  L.bm_g = 0;
+  if (c->page_format == MK_PAGES_BITMAP) {  // the smallest group size: the largest bitmap
+    L.bm_g = 8;
+    for (int i = 0; i < c->n_segments; ++i) L.bm_g = std::min(L.bm_g, seg_group_of(c, i));
+  }
+  // packed: K and V values (2 r bytes each) and positions, sized for the
+  // largest r and the largest positions; dense: 2 x 256 bytes per token
+  L.page_stride = L.dense_pages ? (int64_t)4 * L.B * MK_HEAD_DIM
+                                : page_vpos(L, r_max, L.bm_g) + (int64_t)L.B * pos_bytes(L, r_max, L.bm_g);
   const int64_t D = MK_HEAD_DIM;
   int64_t off = 0;
   L.off_rkt = off; off += D * D * 4;
@@ -191,7 +207,9 @@ UnitDesc host_desc(const mk_ctx* ctx, int layer, int seq) {
     d.r[s] = s < ctx->cfg.n_segments ? ctx->cfg.seg[s].r : 0;
     if (s < ctx->cfg.n_segments) {
       const mk_segment& g = ctx->cfg.seg[s];
-      d.sflags[s] = mk::seg_flags(g.always != 0, g.keep_channels ? g.keep_channels : MK_HEAD_DIM);
+      d.sflags[s] = mk::seg_flags(g.always != 0, g.keep_channels ? g.keep_channels : MK_HEAD_DIM,
+                                  ctx->cfg.page_format == MK_PAGES_BITMAP ? log2_group(seg_group_of(&ctx->cfg, s))
+                                                                          : 0);
     } else {
       d.sflags[s] = mk::seg_flags(false, MK_HEAD_DIM);
     }
@@ -694,7 +712,10 @@ mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_he
   if (segment < 0 || segment >= c.n_segments) return MK_EINVAL;
   if (r < 1 || r > L.r_max) return MK_EINVAL;  // the pages hold at most r_max entries per token
   if (keep_channels != 0 && (keep_channels < r || keep_channels > MK_HEAD_DIM)) return MK_EINVAL;
-  if (L.bm_g > 1 && (r % L.bm_g || keep_channels % L.bm_g)) return MK_EINVAL;  // whole groups only
+  if (L.bm_g) {  // the segment keeps its element-group size: whole groups only
+    const int g = seg_group_of(&c, segment);
+    if (r % g || keep_channels % g) return MK_EINVAL;
+  }
   if (L.meta_c > 0 && !cmeta) return MK_EINVAL;
   if ((R_k == nullptr) != (R_v == nullptr)) return MK_EINVAL;
   const size_t ls = (size_t)layer * c.max_seqs + seq;

@@ -167,7 +167,7 @@ __device__ __forceinline__ uint64_t spread_groups(uint64_t kg) {
   return out;
 }
 
-// BM: bitmap pages (element group L.bm_g); the uint8-index and uncompressed
+// BM: bitmap pages (element group per segment); the uint8-index and uncompressed
 // formats take BM = false, without the grouped search.
 template <bool BM>
 __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, CallSeqs cs,
@@ -360,7 +360,12 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
         keep_lo = 0u;
         uint32_t kw[32];
         uint64_t gt = 0ull, eq = 0ull;
-        const int gg = BM ? L.bm_g : 0;
+        const int gg = BM ? seg_group(ud, sg) : 0;
+        // Threads of a pair hold the same token, so they take the same
+        // branch below; with bitmap pages the warp's tokens may span two
+        // segments of different group sizes, so the pair's shuffles name the
+        // pair only.
+        const unsigned pmask = BM ? 3u << (lane & 30) : FULL;
         int kneed = r;  // units to keep: channels, or groups of gg channels
         if (gg <= 1) {
           // 15-bit magnitudes, two per word, each under a guard bit: for a
@@ -396,7 +401,7 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
               for (int j = 0; j < 16; ++j) f |= ((kw[16 * g + j] - cc) & 0x80008000u) >> j;
               n += __popc(f);
             }
-            n += __shfl_xor_sync(FULL, n, 1);
+            n += __shfl_xor_sync(pmask, n, 1);
             if (n >= r) thr = cand;
           }
           // Above thr: kept.  Equal to thr: the lowest channels, as many as the
@@ -426,7 +431,7 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
 #pragma unroll
             for (int j = 0; j < 32; ++j) f |= ((kw[j] - cand) >> 31) << j;
             int n = 32 - __popc(f);  // zero slots never reach cand >= 1
-            n += __shfl_xor_sync(FULL, n, 1);
+            n += __shfl_xor_sync(pmask, n, 1);
             if (n >= kneed) thr = cand;
           }
 #pragma unroll
@@ -528,7 +533,7 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
         const int blo = S + b * B;
         const int st = max(blo, mlo), en = min(blo + B, mhi);
         char* page = base + L.off_pages + (int64_t)b * L.page_stride;
-        const int pb = BM ? 16 / L.bm_g : r, Br = B * r, Bp = B * pb;  // page: [2Br][Bp][2Br][Bp]
+        const int pb = BM ? 16 / seg_group(ud, seg_of_block(ud, b)) : r, Br = B * r, Bp = B * pb;  // [2Br][Bp][2Br][Bp]
         uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? 2 * Br + Bp : 0)) + (st - blo) * r;
         uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? 4 * Br + Bp : 2 * Br)) + (st - blo) * pb;
         const uint16_t* sv = stv + (b - b0) * B * kStageR + (st - blo) * r;
@@ -670,7 +675,7 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
 __global__ void k_set_segment(Layout L, int64_t u, int seg, int r, int keep, int own) {
   if (threadIdx.x == 0) {
     L.desc[u].r[seg] = r;
-    L.desc[u].sflags[seg] = (L.desc[u].sflags[seg] & 1) | (own ? 2 : 0) | (keep << 8);
+    L.desc[u].sflags[seg] = (L.desc[u].sflags[seg] & 0x31) | (own ? 2 : 0) | (keep << 8);  // keeps always and g
   }
 }
 

@@ -191,8 +191,9 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   const int sg = seg_of_block(ud, b);
   const int r = ud.r[sg], keep = seg_keep(ud, sg);
   char* page = base + L.off_pages + (int64_t)b * L.page_stride;
-  uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? page_vval(L, r) : 0));
-  uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? page_vpos(L, r) : page_kpos(L, r)));
+  const int gg = L.bm_g ? seg_group(ud, sg) : 0;  // bitmap pages: the segment's element-group size
+  uint16_t* val = reinterpret_cast<uint16_t*>(page + (is_v ? page_vval(L, r, gg) : 0));
+  uint8_t* idx = reinterpret_cast<uint8_t*>(page + (is_v ? page_vpos(L, r, gg) : page_kpos(L, r)));
   const uint2 raw = *reinterpret_cast<const uint2*>(row + 4 * lane);
   // The block's min/max are loaded with the row, ahead of the search.
   uint16_t* meta = reinterpret_cast<uint16_t*>(base + L.off_meta) + (int64_t)b * 2 * D;
@@ -213,8 +214,8 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   if (L.dense_pages) {
     store_dense_row(L, base, b, t, is_v, raw, lane);
   } else {
-    if (L.bm_g > 1) {
-      kbits = warp_top_groups(v, L.bm_g, r, keep, lane);
+    if (gg > 1) {
+      kbits = warp_top_groups(v, gg, r, keep, lane);
       rank = warp_excl_scan(__popc(kbits), lane);
     } else {
       kbits = warp_topr(mag, r, lane, rank);
@@ -223,11 +224,11 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
     for (int i = 0; i < 4; ++i) {
       if (kbits >> i & 1u) {
         val[t * r + rank] = v[i];
-        if (!L.bm_g) idx[t * r + rank] = (uint8_t)(4 * lane + i);
+        if (!gg) idx[t * r + rank] = (uint8_t)(4 * lane + i);
         ++rank;
       }
     }
-    if (L.bm_g) store_bitmap(idx + t * pos_bytes(L, r), kbits, L.bm_g, lane);
+    if (gg) store_bitmap(idx + t * pos_bytes(L, r, gg), kbits, gg, lane);
   }
   if (update_meta) {
     const uint16_t pmn[4] = {(uint16_t)(omn.x & 0xffff), (uint16_t)(omn.x >> 16), (uint16_t)(omn.y & 0xffff),

@@ -233,10 +233,12 @@ struct Task {
   int item;
   int j0, nd;    // dense: first dense token and count
   int b, r, tg, n_live;
+  int g;         // bitmap pages: the block's element-group size
 };
 
 int stage_bytes(const Layout& L) {
-  return (std::max(L.dense_pages ? 0 : kTG * (4 * L.r_max + 2 * pos_bytes(L, L.r_max)), kDenseStage) + 15) / 16 * 16;
+  return (std::max(L.dense_pages ? 0 : kTG * (4 * L.r_max + 2 * pos_bytes(L, L.r_max, L.bm_g)), kDenseStage) + 15) / 16 *
+         16;
 }
 // Per warp: the stages, then the key tile and the value tile.
 size_t per_warp_bytes(const Layout& L, int nst) {
@@ -577,7 +579,9 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
       return t;
     }
     t.kind = 2;
-    t.r = ud.r[seg_of_block(ud, b)];
+    const int sgb = seg_of_block(ud, b);
+    t.r = ud.r[sgb];
+    t.g = MODE == kModeBitmap ? seg_group(ud, sgb) : 0;
     t.tg = tg;
     return t;
   };
@@ -640,7 +644,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
       // multiples of 16 bytes), back to back in the stage:
       // [K val 2gr][K pos gp][V val 2gr][V pos gp] bytes (gp = 16 position
       // rows: gr uint8 indices or 16 bitmaps); lane q copies run q.
-      const int gr = kTG * t.r, pb = MODE == kModeBitmap ? 16 / L.bm_g : t.r, gp = kTG * pb;
+      const int gr = kTG * t.r, pb = MODE == kModeBitmap ? 16 / t.g : t.r, gp = kTG * pb;
       if (lane == 0) {
         fence_proxy_async();
         mbar_expect_tx(&bars[sidx], (unsigned)(4 * gr + 2 * gp));
@@ -727,7 +731,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
         vrow = (vtok < ntok ? vb + vtok * kRow : zrow) + vch;
       } else {
         ntok = min(kTG, cur.n_live - cur.tg);
-        const int r = cur.r, gr = kTG * r, pb = MODE == kModeBitmap ? 16 / L.bm_g : r, gp = kTG * pb;
+        const int r = cur.r, gr = kTG * r, pb = MODE == kModeBitmap ? 16 / cur.g : r, gp = kTG * pb;
         const uint16_t* kval = reinterpret_cast<const uint16_t*>(buf);
         const uint8_t* kidx = buf + 2 * gr;
         const uint16_t* vval = reinterpret_cast<const uint16_t*>(buf + 2 * gr + gp);
@@ -735,7 +739,7 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
         // Kept channels are stored in ascending order, so a token's last
         // index (its bitmap's top bit) is its highest channel: the group's
         // rows are zero from the chunk after the largest one on.
-        const int tt = lane & 15, gg = MODE == kModeBitmap ? L.bm_g : 0;
+        const int tt = lane & 15, gg = MODE == kModeBitmap ? cur.g : 0;
         uint32_t hk = 0, hv = 0;
         if (tt < ntok) {
           if (gg) {

@@ -36,11 +36,16 @@ struct UnitDesc {
   int32_t first_block[MK_MAX_SEGMENTS];
   int32_t r[MK_MAX_SEGMENTS];
   int32_t sflags[MK_MAX_SEGMENTS];  // per segment: bit 0 always attended; bit 1 stored under its own rotation
-                                    // (a re-compressed closed segment); bits 8-15 channels eligible for the top-r
+                                    // (a re-compressed closed segment); bits 4-5 log2 of the element-group size
+                                    // (bitmap pages); bits 8-15 channels eligible for the top-r
 };
 static_assert(sizeof(UnitDesc) == 64, "UnitDesc is 64 bytes");
 
-__host__ __device__ inline int32_t seg_flags(bool always, int keep) { return (always ? 1 : 0) | (keep << 8); }
+__host__ __device__ inline int32_t seg_flags(bool always, int keep, int g_log2 = 0) {
+  return (always ? 1 : 0) | (g_log2 << 4) | (keep << 8);
+}
+// Element-group size of segment s (bitmap pages: 1, 2, 4 or 8).
+__host__ __device__ inline int seg_group(const UnitDesc& u, int s) { return 1 << ((u.sflags[s] >> 4) & 3); }
 __host__ __device__ inline bool seg_always(const UnitDesc& u, int s) { return (u.sflags[s] & 1) != 0; }
 __host__ __device__ inline int seg_keep(const UnitDesc& u, int s) { return (u.sflags[s] >> 8) & 0xff; }
 __host__ __device__ inline bool seg_own(const UnitDesc& u, int s) { return (u.sflags[s] & 2) != 0; }
@@ -71,7 +76,8 @@ struct Layout {
   int32_t S, W, B, n_kv, G, max_seqs, nblk_cap, cap_tokens, n_layers, k_max;
   int32_t topk_fixed, retain_permille, r_max;
   int32_t dense_pages;          // 1: uncompressed middle pages [K B x 128][V B x 128] (Quest comparator)
-  int32_t bm_g;                 // 0: uint8 channel indices; g = 1, 2, 4, 8: a bitmap of 128/g bits per vector
+  int32_t bm_g;                 // 0: uint8 channel indices; else bitmap pages (128/g bits per vector, g per
+                                // segment), and this is the smallest g (the largest bitmap, for sizes)
   int32_t attn_tg;              // attention: tokens per staged page group (32 or 16)
   int32_t attn_nst, attn_nc, attn_sb;  // attention: stages per warp, warps per CTA, stage bytes
   // workspace
@@ -106,14 +112,14 @@ __host__ __device__ inline float* qrot_of(const Layout& L, int layer, int64_t sl
 }
 // Packed page of a block with r kept channels: [K val B r bf16][K pos B pb]
 // [V val B r bf16][V pos B pb], pb = pos_bytes (r uint8 indices, or a bitmap
-// of 16/g bytes).
-__host__ __device__ inline int pos_bytes(const Layout& L, int r) { return L.bm_g ? 16 / L.bm_g : r; }
+// of 16/g bytes, g the block's element-group size).
+__host__ __device__ inline int pos_bytes(const Layout& L, int r, int g) { return L.bm_g ? 16 / g : r; }
 __host__ __device__ inline int64_t page_kpos(const Layout& L, int r) { return (int64_t)2 * L.B * r; }
-__host__ __device__ inline int64_t page_vval(const Layout& L, int r) {
-  return (int64_t)2 * L.B * r + (int64_t)L.B * pos_bytes(L, r);
+__host__ __device__ inline int64_t page_vval(const Layout& L, int r, int g) {
+  return (int64_t)2 * L.B * r + (int64_t)L.B * pos_bytes(L, r, g);
 }
-__host__ __device__ inline int64_t page_vpos(const Layout& L, int r) {
-  return (int64_t)4 * L.B * r + (int64_t)L.B * pos_bytes(L, r);
+__host__ __device__ inline int64_t page_vpos(const Layout& L, int r, int g) {
+  return (int64_t)4 * L.B * r + (int64_t)L.B * pos_bytes(L, r, g);
 }
 // Own rotation of closed segment s: R_k^T then R_v, fp32 [128][128] each.
 __host__ __device__ inline int64_t segrot_off(const Layout& L, int s) {

@@ -77,6 +77,12 @@ typedef struct mk_segment {
                              keep_channels rotated channels only, the bottom
                              ones being truncated ([S] sec. 5.2 truncates the
                              bottom 25%: 96).  Sinks and window stay whole. */
+  int32_t elem_group;     /* MK_PAGES_BITMAP only (else 0): this segment's
+                             element-group size, 1, 2, 4 or 8 ([S] sec. 4.3:
+                             each segment's strategy has its own); 0 takes
+                             mk_config.elem_group.  r and keep_channels must be
+                             multiples of it.  A segment keeps it when it is
+                             re-compressed (mk_swap_segment). */
 } mk_segment;
 
 typedef struct mk_config {
@@ -114,7 +120,8 @@ typedef struct mk_config {
                               sec. 5.1 with a position bitmap per vector in
                               place of the uint8 indices (see elem_group). */
   int32_t elem_group;      /* MK_PAGES_BITMAP only (else 0): the element-group
-                              size g, 1, 2, 4 or 8 (0 means 1).  Each vector
+                              size g of the segments that give none, 1, 2, 4 or
+                              8 (0 means 1).  Each vector
                               stores a bitmap of 128/g bits, bit j set when
                               channels g*j .. g*j+g-1 are kept (bit j in byte
                               j/8 at bit j%8), followed by nothing else: the
@@ -126,7 +133,7 @@ typedef struct mk_config {
                               lower group ([S] sec. 5.1 variable-granularity
                               bitmap, [S] sec. 4.3 element-group size).  Every
                               segment's r and nonzero keep_channels must be
-                              multiples of g. */
+                              multiples of its g. */
 } mk_config;
 
 #define MK_PAGES_PACKED 0

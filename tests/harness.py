@@ -200,7 +200,8 @@ def check_storage(p: Pair, unit):
     for b in range(nb):
         r = oc.r_of_block(b)
         lo, hi = oc.block_tokens(b)
-        pb = p.c.pos_bytes(r)
+        g = oc.group_of_block(b)
+        pb = 16 // g if g else r
         got = page_rows(pages[b], B, r, hi - lo, pb)
         want = page_rows(oc.page_bytes(b), B, r, hi - lo, pb)
         for g, w_, name in zip(got, want, ("kval", "kidx", "vval", "vidx")):

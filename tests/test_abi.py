@@ -115,6 +115,17 @@ def test_bitmap_format_config_rules_and_page_size(lib):
         base = a0 - 8 * nblk * 6 * 32 * 38
         assert abs(a - base - 8 * nblk * 32 * (4 * r + 2 * pb)) <= 8 * 4096
     K.sizes(_cfg(segments=[(0, 40, 0, 96), (500, 16, 1)], page_format=2, elem_group=8, meta_channels=16))
+    # per segment: group sizes 8 and 2, the page sized for the largest bitmap (g = 2: 8 bytes)
+    a, _, _ = K.sizes(_cfg(segments=[(0, 40, 0, 0, 8), (500, 16, 0, 96, 2)], page_format=2, elem_group=4))
+    base = a0 - 8 * nblk * 6 * 32 * 38
+    own_rot = 8 * 2 * 128 * 128 * 4                   # room for the closed segment's own rotations
+    assert abs(a - base - own_rot - 8 * nblk * 32 * (4 * 40 + 2 * 8)) <= 8 * 4096
+    for bad in (dict(segments=[(0, 40, 0, 0, 3)]), dict(segments=[(0, 36, 0, 0, 8)]),     # g, r per segment
+                dict(segments=[(0, 40, 0, 98, 4)]), dict(page_format=0, segments=[(0, 40, 0, 0, 4)])):
+        bad.setdefault("page_format", 2)
+        with pytest.raises(K.MosaicKVError) as e:
+            K.sizes(_cfg(**bad))
+        assert e.value.status == 1
     for bad in (dict(elem_group=3), dict(elem_group=16), dict(elem_group=-1),
                 dict(elem_group=4, segments=[(0, 38, 0)]),           # r not a multiple of g
                 dict(elem_group=8, segments=[(0, 40, 0, 100)]),      # truncation not a multiple of g

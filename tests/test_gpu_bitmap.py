@@ -187,3 +187,88 @@ def test_bitmap_swap_closed_segment(own):
         want = oc.attention(qs, ids[s, h, :n_sel[s, h]])
         for gi in range(G):
             assert rel_l2(out[s, h * G + gi], want[gi]) <= ATOL_REL, (s, h, gi)
+
+
+# Per-segment element-group sizes ([S] sec. 4.3): 8, 2 and 1 in one cache (the
+# cache's default, 4, for none of them), one truncated, one above the
+# prefill's staging limit.  Prefill tiles and decode warps then hold tokens of
+# segments with different group sizes.
+_MIXED = [(0, 40, 0, 0, 8), (400, 16, 1, 96, 2), (700, 72, 0, 0, 1)]
+
+
+def test_bitmap_per_segment_groups_storage_and_attention():
+    case = Case(n_q=4, n_kv=2, seq_lens=[2300, 900], rot="perm", block=32, window=64, page_format=2, elem_group=4,
+                segments=_MIXED, steps=[1] * 20 + [5, 33, 1], seed=120)
+    p = Pair(case)
+    for u in p.units:
+        _check_storage(p, u)
+    p.run_steps()
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    for u in p.units:
+        _check_storage(p, u)
+        oc = p.orc[u]
+        assert [sg[4] for sg in oc.st.segments] == [8, 2, 1]
+    q = p.query(13)
+    ids, n_sel = p.mk.block_select(0, [0, 1], q)
+    out = p.mk.decode_attn(0, [0, 1], ids, n_sel)
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    out = out.cpu().to(torch.float64).numpy()
+    ids, n_sel = ids.cpu().numpy(), n_sel.cpu().numpy()
+    G = case.G
+    for (l, s, h), oc in p.orc.items():
+        qs = q[s, h * G:(h + 1) * G].cpu().to(torch.float64).numpy()
+        want = oc.attention(qs, ids[s, h, :n_sel[s, h]])
+        for gi in range(G):
+            assert rel_l2(out[s, h * G + gi], want[gi]) <= ATOL_REL, (s, h, gi)
+
+
+def test_bitmap_per_segment_groups_swap_own_rotation():
+    """Per-segment groups, then a closed segment
+    re-packed on the host under its own rotation: it keeps its group size
+    (8), takes a new r and truncation."""
+    from compressed_kv_cache_vector_gb300 import binding, synth
+    case = Case(n_q=4, n_kv=2, seq_lens=[3000, 1800], rot="perm", block=32, window=64, page_format=2, elem_group=4,
+                segments=[(0, 40, 0, 0, 8), (600, 38, 0, 0, 1)], steps=[1] * 3, seed=121)
+    p = Pair(case)
+    p.run_steps()
+    S, B = case.n_sink, case.block
+    r_new, keep = 24, 96
+    for (l, s, h) in p.units:
+        lay = p.mk.layout(l, s, h)
+        fb = lay["seg_first_block"]
+        rows = slice(S + fb[0] * B, S + fb[1] * B)
+        Kraw = synth.bf16_values(p.K[(l, s, h)])
+        Vraw = synth.bf16_values(p.V[(l, s, h)])
+        Rk_s = O.rotation_from_keys(Kraw[rows])[0].astype(np.float32)
+        Rv_s = O.rotation_from_keys(Vraw[rows])[0].astype(np.float32)
+        pages, meta, _ = binding.host_pack_blocks(Rk_s, Rv_s, p.K[(l, s, h)][rows].cpu(), p.V[(l, s, h)][rows].cpu(),
+                                                  B, r_new, keep, lay["page_stride"], 0, 2, 8)
+        p.mk.swap_segment(l, s, h, 0, r_new, keep, pages, meta, R_k=Rk_s, R_v=Rv_s)
+        torch.cuda.synchronize()
+        p.orc[(l, s, h)].recompress_segment(0, Kraw, Vraw, r_new, keep, Rk_s.astype(np.float64),
+                                            Rv_s.astype(np.float64))
+    assert p.mk.poll_error() == (0, 0)
+    for u in p.units:
+        _check_storage(p, u)
+        assert p.orc[u].st.segments[0][4] == 8
+    q = p.query(14)
+    ids, n_sel = p.mk.block_select(0, [0, 1], q)
+    out = p.mk.decode_attn(0, [0, 1], ids, n_sel)
+    torch.cuda.synchronize()
+    assert p.mk.poll_error() == (0, 0)
+    out = out.cpu().to(torch.float64).numpy()
+    ids, n_sel = ids.cpu().numpy(), n_sel.cpu().numpy()
+    G = case.G
+    for (l, s, h), oc in p.orc.items():
+        qs = q[s, h * G:(h + 1) * G].cpu().to(torch.float64).numpy()
+        want = oc.attention(qs, ids[s, h, :n_sel[s, h]])
+        for gi in range(G):
+            assert rel_l2(out[s, h * G + gi], want[gi]) <= ATOL_REL, (s, h, gi)
+    # a swap whose r is not a multiple of the segment's group is refused
+    lay = p.mk.layout(0, 0, 0)
+    pages = np.zeros((lay["seg_first_block"][1], lay["page_stride"]), dtype=np.uint8)
+    meta = np.zeros((lay["seg_first_block"][1], 2, 128), dtype=np.uint16)
+    with pytest.raises(binding.MosaicKVError):
+        p.mk.swap_segment(0, 0, 0, 0, 20, 0, pages, meta)
