@@ -223,7 +223,7 @@ class Strategy:
     n_sink: int
     window: int
     block: int
-    segments: list            # [(begin_permille, r, always[, keep_channels[, elem_group]])]
+    segments: list            # [(begin_permille, r, always[, keep_channels[, elem_group[, retain_permille]]])]
     topk_fixed: int = 0
     retain_permille: int = 0
     meta_channels: int = 0    # > 0: channel-compressed per-block keys ([S] sec. 5.2)
@@ -236,9 +236,17 @@ class Strategy:
         # elem_group (bitmap pages only): the segment's own element-group
         # size ([S] sec. 4.3 lists it in each segment's strategy); 0 or
         # absent means the cache's bitmap_group.
+        # retain_permille: the segment's own sequence retention ([S] sec. 4.3:
+        # each segment's strategy has one); 0 or absent means the cache's.
         self.segments = [(sg[0], sg[1], sg[2], (sg[3] if len(sg) > 3 and sg[3] else D_HEAD),
-                          (sg[4] if len(sg) > 4 and sg[4] else self.bitmap_group) if self.bitmap_group else 0)
+                          (sg[4] if len(sg) > 4 and sg[4] else self.bitmap_group) if self.bitmap_group else 0,
+                          sg[5] if len(sg) > 5 else 0)
                          for sg in self.segments]
+
+    def per_segment_retention(self):
+        """True when some scored segment gives its own retention: then every
+        scored segment keeps its own k (its own rate, else the cache's)."""
+        return any(sg[5] for sg in self.segments if not sg[2])
 
 
 def compress_key_rows(mn, mx, m):
@@ -290,13 +298,15 @@ def block_segment(b, firsts):
     return s
 
 
-def n_select(n_scored, st: Strategy):
-    """Number of blocks top-k keeps among n_scored candidates."""
+def n_select(n_scored, st: Strategy, retain_permille=None):
+    """Number of blocks top-k keeps among n_scored candidates (with a given
+    retention, that rate instead of the strategy's rule)."""
     if n_scored <= 0:
         return 0
-    if st.topk_fixed > 0:
+    if retain_permille is None and st.topk_fixed > 0:
         return min(st.topk_fixed, n_scored)
-    k = (st.retain_permille * n_scored + 999) // 1000
+    ret = st.retain_permille if retain_permille is None else retain_permille
+    k = (ret * n_scored + 999) // 1000
     return min(max(k, 1), n_scored)
 
 
@@ -485,8 +495,8 @@ class OracleCache:
         0 = all channels), and its blocks' min/max recomputed."""
         assert 0 <= seg < len(self.st.segments) - 1, "only a closed segment is re-compressed"
         segs = list(self.st.segments)
-        begin, _, always, _, g = segs[seg]          # the segment keeps its element-group size
-        segs[seg] = (begin, r, always, keep if keep else self.d, g)
+        begin, _, always, _, g, ret = segs[seg]     # the segment keeps its group size and retention
+        segs[seg] = (begin, r, always, keep if keep else self.d, g, ret)
         self.st = Strategy(self.st.n_sink, self.st.window, self.st.block, segs, self.st.topk_fixed,
                            self.st.retain_permille, self.st.meta_channels, self.st.bitmap_group)
         if Rk is not None:
@@ -584,11 +594,36 @@ class OracleCache:
                 per[:, lo:hi] = p_s
         return per, per.max(axis=0)
 
+    def segment_candidates(self, seg):
+        """The middle blocks of a scored segment (empty for an always-attended one)."""
+        if self.st.segments[seg][2]:
+            return np.zeros(0, dtype=np.int64)
+        nb = self.n_blocks_mid()
+        lo = min(self.firsts[seg], nb)
+        hi = min(self.firsts[seg + 1], nb) if seg + 1 < len(self.st.segments) else nb
+        return np.arange(lo, max(lo, hi), dtype=np.int64)
+
+    def n_selected(self):
+        """How many blocks the selection keeps."""
+        if not self.st.per_segment_retention():
+            return n_select(len(self.candidates()), self.st)
+        return sum(n_select(len(self.segment_candidates(s)), self.st, sg[5] or self.st.retain_permille)
+                   for s, sg in enumerate(self.st.segments) if not sg[2])
+
     def select(self, q):
-        cand = self.candidates()
-        k = n_select(len(cand), self.st)
+        """The blocks attended besides the always-attended ones: the k best
+        scored blocks; with per-segment retention, each scored segment's own
+        k best (each segment its own top-k, [S] sec. 4.3), ids ascending."""
         _, grp = self.scores(q)
-        return topk_blocks(grp, cand, k), grp
+        if not self.st.per_segment_retention():
+            cand = self.candidates()
+            return topk_blocks(grp, cand, n_select(len(cand), self.st)), grp
+        ids = []
+        for s, sg in enumerate(self.st.segments):
+            cand = self.segment_candidates(s)
+            if len(cand):
+                ids.append(topk_blocks(grp, cand, n_select(len(cand), self.st, sg[5] or self.st.retain_permille)))
+        return (np.sort(np.concatenate(ids)) if ids else np.zeros(0, dtype=np.int64)), grp
 
     def attend_tokens(self, ids):
         """Token rows (rotated K, rotated V) that attention reads for these blocks."""

@@ -782,3 +782,51 @@ def test_bitmap_cache_rows_and_attention_by_explicit_sums(g, segs):
                             k += g
                 assert k == r
                 assert np.array_equal(row, dense[lo + t].astype(np.float64))
+
+
+# ------------------------------------ per-segment sequence retention ----
+def test_per_segment_retention_brute_force_and_k_rule():
+    # [S] sec. 4.3: each segment's strategy has its own sequence retention.
+    # Each scored segment keeps its own k_s = ceil(rate * n_s / 1000) best
+    # blocks (clamped to [1, n_s]), ties to the lower id; always-attended
+    # segments are not scored.  Brute force: a Python sort per segment.
+    assert O.n_select(37, O.Strategy(4, 32, 16, [(0, 32, 0)], 0, 100), 150) == 6     # ceil(5.55)
+    assert O.n_select(5, O.Strategy(4, 32, 16, [(0, 32, 0)], 0, 100), 1) == 1        # at least one
+    assert O.n_select(0, O.Strategy(4, 32, 16, [(0, 32, 0)], 0, 100), 500) == 0
+    segs = [(0, 32, 0, 0, 0, 300), (300, 64, 1), (550, 32, 0, 0, 0, 50), (800, 24, 0)]
+    st = O.Strategy(4, 32, 16, segs, 0, 100)
+    assert st.per_segment_retention()
+    c, _, _ = _cache(3000, st, 80)
+    rng = np.random.default_rng(81)
+    for trial in range(5):
+        q = rng.standard_normal((4, 128))
+        ids, grp = c.select(q)
+        want, total = [], 0
+        for s, sg in enumerate(c.st.segments):
+            if sg[2]:
+                continue
+            nb = c.n_blocks_mid()
+            lo = min(c.firsts[s], nb)
+            hi = min(c.firsts[s + 1], nb) if s + 1 < len(segs) else nb
+            blocks = list(range(lo, hi))
+            rate = sg[5] or 100
+            k = min(max(-(-rate * len(blocks) // 1000), 1), len(blocks)) if blocks else 0
+            want += sorted(sorted(blocks, key=lambda b: (-grp[b], b))[:k])
+            total += k
+        assert list(ids) == sorted(want) and c.n_selected() == total == len(ids)
+    # a planted mistake: one top-k over all scored blocks with the same total
+    # picks another set (the segments' own rates are not kept)
+    cand = c.candidates()
+    glob = O.topk_blocks(grp, cand, len(ids))
+    assert not np.array_equal(glob, ids)
+
+
+def test_per_segment_retention_equal_rates_is_the_global_rule():
+    # One scored segment at the cache's own rate: the same blocks as the
+    # single top-k over the candidates.
+    st_g = O.Strategy(4, 32, 16, [(0, 32, 0), (500, 64, 1)], 0, 100)
+    st_s = O.Strategy(4, 32, 16, [(0, 32, 0, 0, 0, 100), (500, 64, 1)], 0, 100)
+    a, _, _ = _cache(2000, st_g, 82)
+    b, _, _ = _cache(2000, st_s, 82)
+    q = np.random.default_rng(83).standard_normal((4, 128))
+    assert np.array_equal(a.select(q)[0], b.select(q)[0])
