@@ -35,7 +35,7 @@ class MosaicKVError(RuntimeError):
 
 class MkSegment(ctypes.Structure):
     _fields_ = [("begin_permille", c_i32), ("r", c_i32), ("always", c_i32), ("keep_channels", c_i32),
-                ("elem_group", c_i32)]
+                ("elem_group", c_i32), ("retain_permille", c_i32)]
 
 
 class MkConfig(ctypes.Structure):
@@ -159,6 +159,7 @@ def make_config(n_q_heads, n_kv_heads, n_layers, max_seqs, max_tokens, n_sink, w
         keep = sg[3] if len(sg) > 3 else 0
         c.seg[i].begin_permille, c.seg[i].r, c.seg[i].always, c.seg[i].keep_channels = b, r, a, keep
         c.seg[i].elem_group = sg[4] if len(sg) > 4 else 0   # bitmap pages: the segment's own group size
+        c.seg[i].retain_permille = sg[5] if len(sg) > 5 else 0   # the segment's own sequence retention
     return c
 
 

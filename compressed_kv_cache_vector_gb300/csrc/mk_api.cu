@@ -66,6 +66,9 @@ mk_status check_config(const mk_config* c) {
     if (s.r < 1 || s.r > MK_HEAD_DIM || (s.always != 0 && s.always != 1)) return MK_EINVAL;
     if (s.keep_channels != 0 && (s.keep_channels < s.r || s.keep_channels > MK_HEAD_DIM)) return MK_EINVAL;
     if (s.begin_permille < 0 || s.begin_permille > 1000) return MK_EINVAL;
+    // Per-segment retention: a scored segment's own rate, not with a fixed k.
+    if (s.retain_permille < 0 || s.retain_permille > 1000 || (s.always && s.retain_permille)) return MK_EINVAL;
+    if (s.retain_permille && c->topk_fixed > 0) return MK_EINVAL;
     if (i == 0 && s.begin_permille != 0) return MK_EINVAL;
     if (s.begin_permille < prev) return MK_EINVAL;
     prev = s.begin_permille;
@@ -107,7 +110,20 @@ Plan make_plan(const mk_config* c) {
   for (int i = 0; i < c->n_segments; ++i) r_max = std::max(r_max, (int)c->seg[i].r);
   L.r_max = r_max;
   L.nblk_cap = mk::n_mid_blocks(L, c->max_tokens);
-  L.k_max = std::max(1, mk::n_select(L, L.nblk_cap));
+  L.per_seg_k = 0;
+  for (int i = 0; i < c->n_segments; ++i) {
+    L.seg_retain[i] = c->seg[i].retain_permille;
+    if (c->seg[i].retain_permille && !c->seg[i].always) L.per_seg_k = 1;
+  }
+  for (int i = c->n_segments; i < MK_MAX_SEGMENTS; ++i) L.seg_retain[i] = 0;
+  if (!L.per_seg_k) {
+    L.k_max = std::max(1, mk::n_select(L, L.nblk_cap));
+  } else {  // each scored segment's k is at most its rate of the capacity; all of them at most the blocks
+    int64_t km = 0;
+    for (int i = 0; i < c->n_segments; ++i)
+      if (!c->seg[i].always) km += mk::n_select_segment(L, i, L.nblk_cap);
+    L.k_max = (int)std::max<int64_t>(1, std::min<int64_t>(km, L.nblk_cap));
+  }
   L.keys_stride = (std::max(1, L.nblk_cap) + 3) & ~3;
   L.dense_pages = c->page_format == MK_PAGES_DENSE ? 1 : 0;
   L.bm_g = 0;
@@ -577,7 +593,7 @@ mk_status mk_decode_attn(mk_ctx* ctx, int32_t layer, int32_t n_seqs, const int32
     const int dense = std::min(ctx->L.S, T) + std::max(0, T - (ctx->L.S + mk::n_mid_tokens(ctx->L, T)));
     const int groups = (ctx->L.B + mk::kDenseChunk - 1) / mk::kDenseChunk;
     items[i] = (dense + mk::kDenseChunk - 1) / mk::kDenseChunk +
-               (mk::n_select(ctx->L, scored) + (nblk - scored)) * groups;
+               (mk::n_select_unit(ctx->L, d, nblk) + (nblk - scored)) * groups;
   }
   cudaError_t e = mk::launch_decode_attn(ctx->L, layer, *cs, ids, n_sel, static_cast<uint16_t*>(out), items,
                                          (cudaStream_t)stream, min_parts);

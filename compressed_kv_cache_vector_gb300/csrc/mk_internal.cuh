@@ -75,6 +75,8 @@ struct Layout {
   int64_t page_stride;
   int32_t S, W, B, n_kv, G, max_seqs, nblk_cap, cap_tokens, n_layers, k_max;
   int32_t topk_fixed, retain_permille, r_max;
+  int32_t per_seg_k;                         // 1: each scored segment keeps its own k (per-segment retention)
+  int32_t seg_retain[MK_MAX_SEGMENTS];       // per-segment retention (0: the cache's retain_permille)
   int32_t dense_pages;          // 1: uncompressed middle pages [K B x 128][V B x 128] (Quest comparator)
   int32_t bm_g;                 // 0: uint8 channel indices; else bitmap pages (128/g bits per vector, g per
                                 // segment), and this is the smallest g (the largest bitmap, for sizes)
@@ -150,6 +152,15 @@ __host__ __device__ inline int n_scored_blocks(const UnitDesc& u, int nblk) {
   }
   return n;
 }
+// k of scored segment s with n of its blocks present (per-segment retention).
+__host__ __device__ inline int n_select_segment(const Layout& L, int s, int n) {
+  if (n <= 0) return 0;
+  const int ret = L.seg_retain[s] ? L.seg_retain[s] : L.retain_permille;
+  long long k = ((long long)ret * n + 999) / 1000;
+  if (k < 1) k = 1;
+  if (k > n) k = n;
+  return (int)k;
+}
 __host__ __device__ inline int n_select(const Layout& L, int n_scored) {
   if (n_scored <= 0) return 0;
   if (L.topk_fixed > 0) return L.topk_fixed < n_scored ? L.topk_fixed : n_scored;
@@ -157,6 +168,22 @@ __host__ __device__ inline int n_select(const Layout& L, int n_scored) {
   if (k < 1) k = 1;
   if (k > n_scored) k = n_scored;
   return (int)k;
+}
+// Blocks a unit's selection keeps among its first nblk blocks: one top-k
+// over every scored block, or (per-segment retention) each scored segment's
+// own k.
+__host__ __device__ inline int n_select_unit(const Layout& L, const UnitDesc& u, int nblk) {
+  if (!L.per_seg_k) return n_select(L, n_scored_blocks(u, nblk));
+  int k = 0;
+  for (int i = 0; i < u.n_seg; ++i) {
+    if (seg_always(u, i)) continue;
+    int lo = u.first_block[i];
+    int hi = (i + 1 < u.n_seg) ? u.first_block[i + 1] : nblk;
+    if (hi > nblk) hi = nblk;
+    if (lo > nblk) lo = nblk;
+    if (hi > lo) k += n_select_segment(L, i, hi - lo);
+  }
+  return k;
 }
 // Bulk-append tiles: [T_old, f), [f, f+128), ... with f the first position
 // S + 128j (or S) past T_old, so that every middle block sits in one tile.

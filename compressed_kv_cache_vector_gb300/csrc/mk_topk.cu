@@ -76,7 +76,9 @@ __device__ __forceinline__ int2 block_excl_scan2_1024(int a, int b, int2* wsum) 
 // finds the threshold by itself and writes the ids of its share of the
 // blocks.  With APPEND the scoring kernel appended cs.n_new[ci] tokens first:
 // the length it read is advanced here, after every scoring CTA has read it.
-template <bool APPEND>
+// PERSEG: per-segment sequence retention, each scored segment selected on
+// its own (its own k over its own blocks); else one top-k over all of them.
+template <bool APPEND, bool PERSEG>
 __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, CallSeqs cs, int32_t* __restrict__ ids,
                                                         int32_t* __restrict__ n_sel, int dyn_bytes, int C) {
   extern __shared__ __align__(16) unsigned char smem[];   // staged keys
@@ -154,13 +156,23 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
   }
   if (APPEND && part == 0 && tid == 0) L.desc[u].T = T_cur;
 
-  // Chunk c (keys 4c .. 4c+3), keys past nblk zero.
+  // Chunk c (keys 4c .. 4c+3), keys past nblk zero; with PERSEG, keys
+  // outside the blocks [r_lo, r_hi) of the segment being selected zero too.
+  int r_lo = 0, r_hi = nblk;
   auto chunk_at = [&](int c) -> uint4 {
     if (c >= nch) return make_uint4(0, 0, 0, 0);
     uint4 v = staged ? ks[c] : __ldcg(reinterpret_cast<const uint4*>(kw) + c);
-    if (4 * c + 1 >= nblk) v.y = 0u;
-    if (4 * c + 2 >= nblk) v.z = 0u;
-    if (4 * c + 3 >= nblk) v.w = 0u;
+    if constexpr (PERSEG) {
+      const int b0 = 4 * c;
+      if (b0 < r_lo || b0 >= r_hi) v.x = 0u;
+      if (b0 + 1 < r_lo || b0 + 1 >= r_hi) v.y = 0u;
+      if (b0 + 2 < r_lo || b0 + 2 >= r_hi) v.z = 0u;
+      if (b0 + 3 < r_lo || b0 + 3 >= r_hi) v.w = 0u;
+    } else {
+      if (4 * c + 1 >= nblk) v.y = 0u;
+      if (4 * c + 2 >= nblk) v.z = 0u;
+      if (4 * c + 3 >= nblk) v.w = 0u;
+    }
     return v;
   };
   // Histogram into h, by bits [shift, shift + 10), of the keys whose bits
@@ -202,40 +214,12 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
     __syncthreads();
   };
 
+  // The selection of k_r keys of the current range (all of them when
+  // all_r), its ids written from out[out_off] on: thr, the threshold key;
+  // need, the ties at thr it takes.
   uint32_t thr = 1u;  // every candidate (key >= 1) when all are taken
   int need = 0;       // keys equal to thr to take
-  if (!all) {
-    // Coarse bin of the k-th largest key: thread t holds bins 4095 - 4t - 3 .. 4095 - 4t.
-    {
-      const uint4 h4 = reinterpret_cast<const uint4*>(hc)[kKeyBins / 4 - 1 - tid];
-      const int c = (int)(h4.x + h4.y + h4.z + h4.w);
-      const int ex = block_excl_scan2_1024(c, 0, wsum).x;  // keys in higher bins
-      if (ex < k && ex + c >= k) {
-        const uint32_t hv[4] = {h4.w, h4.z, h4.y, h4.x};  // descending bin order
-        int acc = ex;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (acc < k && acc + (int)hv[i] >= k) {
-            s_bin = kKeyBins - 1 - 4 * tid - i;
-            s_rem = k - acc;
-          }
-          acc += (int)hv[i];
-        }
-      }
-      __syncthreads();
-    }
-    const uint32_t b = (uint32_t)s_bin;
-    const int rem0 = s_rem;
-    fine_pass(fh[0], b, 10);
-    fine_find(fh[0], rem0);
-    const uint32_t ba = (uint32_t)s_bin;
-    const int rem1 = s_rem;
-    fine_pass(fh[1], (b << 10) | ba, 0);
-    fine_find(fh[1], rem1);
-    thr = (b << 20) | (ba << 10) | (uint32_t)s_bin;
-    need = s_rem;
-  }
-
+  bool all_r = all;
   // Keys above thr (all candidates when every one is taken) and ties of one
   // chunk, as 4-bit masks.
   auto masks = [&](int c, uint32_t& gm, uint32_t& em) {
@@ -245,74 +229,155 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
     em = 0u;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      gm |= (all ? e[q] != 0u : e[q] > thr) ? 1u << q : 0u;
-      em |= (!all && e[q] == thr) ? 1u << q : 0u;
+      gm |= (all_r ? e[q] != 0u : e[q] > thr) ? 1u << q : 0u;
+      em |= (!all_r && e[q] == thr) ? 1u << q : 0u;
     }
   };
-  // This CTA's share of the chunks, and the keys taken before it.
-  const int per = (nch + C - 1) / C;
-  const int c_lo = min(nch, part * per), c_hi = min(nch, c_lo + per);
-  const int own_rounds = (c_hi - c_lo + kTkThreads - 1) / kTkThreads;
-  int2 before;
-  {
-    int g0 = 0, e0 = 0;
-    for (int c = tid; c < c_lo; c += kTkThreads) {
-      uint32_t gm, em;
-      masks(c, gm, em);
-      g0 += __popc(gm);
-      e0 += __popc(em);
+  auto run_range = [&](int k_r, int out_off) {
+    thr = 1u;
+    need = 0;
+    if (!all_r) {
+      // Coarse bin of the k-th largest key: thread t holds bins 4095 - 4t - 3 .. 4095 - 4t.
+      {
+        const uint4 h4 = reinterpret_cast<const uint4*>(hc)[kKeyBins / 4 - 1 - tid];
+        const int c = (int)(h4.x + h4.y + h4.z + h4.w);
+        const int ex = block_excl_scan2_1024(c, 0, wsum).x;  // keys in higher bins
+        if (ex < k_r && ex + c >= k_r) {
+          const uint32_t hv[4] = {h4.w, h4.z, h4.y, h4.x};  // descending bin order
+          int acc = ex;
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (acc < k_r && acc + (int)hv[i] >= k_r) {
+              s_bin = kKeyBins - 1 - 4 * tid - i;
+              s_rem = k_r - acc;
+            }
+            acc += (int)hv[i];
+          }
+        }
+        __syncthreads();
+      }
+      const uint32_t b = (uint32_t)s_bin;
+      const int rem0 = s_rem;
+      fine_pass(fh[0], b, 10);
+      fine_find(fh[0], rem0);
+      const uint32_t ba = (uint32_t)s_bin;
+      const int rem1 = s_rem;
+      fine_pass(fh[1], (b << 10) | ba, 0);
+      fine_find(fh[1], rem1);
+      thr = (b << 20) | (ba << 10) | (uint32_t)s_bin;
+      need = s_rem;
     }
-    const int2 ex = block_excl_scan2_1024(g0, e0, wsum);
-    if (tid == kTkThreads - 1) wsum[0] = make_int2(ex.x + g0, ex.y + e0);
+
+
+
+    // This CTA's share of the chunks, and the keys taken before it.
+    const int per = (nch + C - 1) / C;
+    const int c_lo = min(nch, part * per), c_hi = min(nch, c_lo + per);
+    const int own_rounds = (c_hi - c_lo + kTkThreads - 1) / kTkThreads;
+    int2 before;
+    {
+      int g0 = 0, e0 = 0;
+      for (int c = tid; c < c_lo; c += kTkThreads) {
+        uint32_t gm, em;
+        masks(c, gm, em);
+        g0 += __popc(gm);
+        e0 += __popc(em);
+      }
+      const int2 ex = block_excl_scan2_1024(g0, e0, wsum);
+      if (tid == kTkThreads - 1) wsum[0] = make_int2(ex.x + g0, ex.y + e0);
+      __syncthreads();
+      before = wsum[0];
+      __syncthreads();
+    }
+    // Per (round, warp) of the share: totals of (above, ties); then their
+    // exclusive scan in (round, warp) order, one entry per thread.
+  #pragma unroll 1
+    for (int j = 0; j < own_rounds; ++j) {
+      uint32_t gm = 0u, em = 0u;
+      const int c = c_lo + j * kTkThreads + tid;
+      if (c < c_hi) masks(c, gm, em);
+      const int tg = (int)__reduce_add_sync(FULL, (unsigned)__popc(gm));
+      const int te = (int)__reduce_add_sync(FULL, (unsigned)__popc(em));
+      if (lane == 0) wtab[j * kTkWarps + warp] = make_int2(tg, te);
+    }
     __syncthreads();
-    before = wsum[0];
+    {
+      const int2 v = tid < own_rounds * kTkWarps ? wtab[tid] : make_int2(0, 0);
+      const int2 ex = block_excl_scan2_1024(v.x, v.y, wsum);
+      wtab[tid] = make_int2(ex.x + before.x, ex.y + before.y);
+    }
     __syncthreads();
-  }
-  // Per (round, warp) of the share: totals of (above, ties); then their
-  // exclusive scan in (round, warp) order, one entry per thread.
-#pragma unroll 1
-  for (int j = 0; j < own_rounds; ++j) {
-    uint32_t gm = 0u, em = 0u;
-    const int c = c_lo + j * kTkThreads + tid;
-    if (c < c_hi) masks(c, gm, em);
-    const int tg = (int)__reduce_add_sync(FULL, (unsigned)__popc(gm));
-    const int te = (int)__reduce_add_sync(FULL, (unsigned)__popc(em));
-    if (lane == 0) wtab[j * kTkWarps + warp] = make_int2(tg, te);
-  }
-  __syncthreads();
-  {
-    const int2 v = tid < own_rounds * kTkWarps ? wtab[tid] : make_int2(0, 0);
-    const int2 ex = block_excl_scan2_1024(v.x, v.y, wsum);
-    wtab[tid] = make_int2(ex.x + before.x, ex.y + before.y);
-  }
-  __syncthreads();
-#pragma unroll 1
-  for (int j = 0; j < own_rounds; ++j) {
-    uint32_t gm = 0u, em = 0u;
-    const int c = c_lo + j * kTkThreads + tid;
-    if (c < c_hi) masks(c, gm, em);
-    const int og = __popc(gm), oe = __popc(em);
-    int ig = og, ie = oe;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int yg = __shfl_up_sync(FULL, ig, o), ye = __shfl_up_sync(FULL, ie, o);
-      if (lane >= o) {
-        ig += yg;
-        ie += ye;
+  #pragma unroll 1
+    for (int j = 0; j < own_rounds; ++j) {
+      uint32_t gm = 0u, em = 0u;
+      const int c = c_lo + j * kTkThreads + tid;
+      if (c < c_hi) masks(c, gm, em);
+      const int og = __popc(gm), oe = __popc(em);
+      int ig = og, ie = oe;
+  #pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int yg = __shfl_up_sync(FULL, ig, o), ye = __shfl_up_sync(FULL, ie, o);
+        if (lane >= o) {
+          ig += yg;
+          ie += ye;
+        }
+      }
+      const int2 base = wtab[j * kTkWarps + warp];
+      const int g_before = base.x + ig - og, e_before = base.y + ie - oe;
+      const int take_eq = max(0, min(oe, need - e_before));  // ties still below `need`
+      uint32_t tm = em;
+      while (__popc(tm) > take_eq) tm &= ~(1u << (31 - __clz(tm)));  // keep the lowest ids
+      const uint32_t take = gm | tm;
+      const int p0 = g_before + min(e_before, need);
+  #pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int p = p0 + __popc(take & ((1u << q) - 1u));
+        if (((take >> q) & 1u) && out_off + p < L.k_max) out[out_off + p] = 4 * c + q;
       }
     }
-    const int2 base = wtab[j * kTkWarps + warp];
-    const int g_before = base.x + ig - og, e_before = base.y + ie - oe;
-    const int take_eq = max(0, min(oe, need - e_before));  // ties still below `need`
-    uint32_t tm = em;
-    while (__popc(tm) > take_eq) tm &= ~(1u << (31 - __clz(tm)));  // keep the lowest ids
-    const uint32_t take = gm | tm;
-    const int p0 = g_before + min(e_before, need);
+  };
+  if constexpr (!PERSEG) {
+    run_range(k, 0);
+  } else {
+    // Each scored segment on its own: its keys' coarse histogram (the
+    // scoring kernel's covers all segments), then its selection, its ids
+    // after those of the segments before it.
+    int32_t* ssel = L.seg_sel + (((int64_t)layer * L.max_seqs + seq) * L.n_kv + kvh) * MK_MAX_SEGMENTS;
+    int off = 0;
+    for (int sgi = 0; sgi < ud.n_seg; ++sgi) {
+      if (part == 0 && tid == 0 && any_own(ud)) ssel[sgi] = off;  // ids below the segment's first block
+      if (seg_always(ud, sgi)) continue;
+      const int lo = min(ud.first_block[sgi], nblk);
+      const int hi = sgi + 1 < ud.n_seg ? min(ud.first_block[sgi + 1], nblk) : nblk;
+      if (hi <= lo) continue;
+      const int k_s = n_select_segment(L, sgi, hi - lo);
+      r_lo = lo;
+      r_hi = hi;
+      all_r = k_s >= hi - lo;
+      fh[0][tid] = 0u;
+      fh[1][tid] = 0u;
+      if (!all_r) {
+        for (int i = tid; i < kKeyBins; i += kTkThreads) hc[i] = 0u;
+        __syncthreads();
+#pragma unroll 1
+        for (int j = 0; j < rounds; ++j) {
+          const uint4 v = chunk_at(j * kTkThreads + tid);
+          const uint32_t e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int p = p0 + __popc(take & ((1u << q) - 1u));
-      if (((take >> q) & 1u) && p < L.k_max) out[p] = 4 * c + q;
+          for (int q = 0; q < 4; ++q)
+            if (e[q] != 0u) atomicAdd(&hc[e[q] >> 20], 1u);
+        }
+      }
+      __syncthreads();
+      run_range(k_s, off);
+      off += k_s;
     }
+    if (part == 0 && tid == 0) {
+      n_sel[(int64_t)ci * L.n_kv + kvh] = off;
+      if (any_own(ud))
+        for (int sgi = ud.n_seg; sgi < MK_MAX_SEGMENTS; ++sgi) ssel[sgi] = off;
+    }
+    return;
   }
   if (part == 0 && tid == 0) n_sel[(int64_t)ci * L.n_kv + kvh] = k;
   // With segments stored under their own rotation, part 0 also records where
@@ -342,7 +407,8 @@ bool topk_plan_ok(const Layout& L) { return (L.nblk_cap + 3) / 4 <= kTkThreads *
 cudaError_t launch_topk(const Layout& L, int layer, const CallSeqs& cs, int32_t* ids, int32_t* n_sel, bool append,
                         cudaStream_t s) {
   const int dyn = (int)std::min<int64_t>(kTkSmemMax, (int64_t)16 * ((L.nblk_cap + 3) / 4));
-  auto kern = append ? k_topk<true> : k_topk<false>;
+  auto kern = append ? (L.per_seg_k ? k_topk<true, true> : k_topk<true, false>)
+                     : (L.per_seg_k ? k_topk<false, true> : k_topk<false, false>);
   cudaError_t e = kernel_smem_attr((const void*)kern, dyn, kTkThreads, nullptr, nullptr);
   if (e != cudaSuccess) return e;
   // CTAs per unit: one per round of 4096 keys (the output pass is then one

@@ -83,6 +83,15 @@ typedef struct mk_segment {
                              mk_config.elem_group.  r and keep_channels must be
                              multiples of it.  A segment keeps it when it is
                              re-compressed (mk_swap_segment). */
+  int32_t retain_permille; /* 0, or 1..1000 for a scored segment: its own
+                             sequence retention ([S] sec. 4.3).  When any scored
+                             segment gives one, each scored segment keeps its
+                             own ceil(rate * n / 1000) best blocks (n: its blocks
+                             present; clamped to [1, n]; rate: its own, else
+                             mk_config.retain_permille), ties to the lower id,
+                             and the ids of all segments come in ascending order
+                             in one row; mk_config.topk_fixed must then be 0.
+                             Must be 0 for an always-attended segment. */
 } mk_segment;
 
 typedef struct mk_config {

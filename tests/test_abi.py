@@ -136,3 +136,18 @@ def test_bitmap_format_config_rules_and_page_size(lib):
         with pytest.raises(K.MosaicKVError) as e:
             K.sizes(_cfg(**bad))
         assert e.value.status == 1
+
+
+def test_per_segment_retention_config_rules(lib):
+    # [S] sec. 4.3: a scored segment may give its own sequence retention;
+    # then each scored segment keeps its own k, and k_max bounds their sum.
+    nblk = (131072 + 64 - 4 - 256 + 31) // 32
+    segs = [(0, 38, 0, 0, 0, 200), (500, 38, 1), (700, 38, 0, 0, 0, 50)]
+    _, _, k = K.sizes(_cfg(segments=segs))
+    assert k == -(-200 * nblk // 1000) + -(-50 * nblk // 1000)
+    for bad in (dict(segments=[(0, 38, 0, 0, 0, 1001)]), dict(segments=[(0, 38, 0, 0, 0, -1)]),
+                dict(segments=[(0, 38, 0), (500, 38, 1, 0, 0, 100)]),          # always-attended: no rate
+                dict(segments=[(0, 38, 0, 0, 0, 100)], topk_fixed=64)):         # not with a fixed k
+        with pytest.raises(K.MosaicKVError) as e:
+            K.sizes(_cfg(**bad))
+        assert e.value.status == 1
