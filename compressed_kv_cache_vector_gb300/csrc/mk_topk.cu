@@ -364,8 +364,15 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
           const uint4 v = chunk_at(j * kTkThreads + tid);
           const uint32_t e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (e[q] != 0u) atomicAdd(&hc[e[q] >> 20], 1u);
+          for (int q = 0; q < 4; ++q) {
+            // lanes with equal bins add once (runs of equal keys, e.g. ties)
+            const bool in = e[q] != 0u;
+            const unsigned act = __ballot_sync(FULL, in);
+            if (in) {
+              const unsigned peers = __match_any_sync(act, e[q] >> 20);
+              if (lane == __ffs(peers) - 1) atomicAdd(&hc[e[q] >> 20], (uint32_t)__popc(peers));
+            }
+          }
         }
       }
       __syncthreads();

@@ -121,3 +121,39 @@ def test_per_segment_retention_fused_and_own_rotation():
     near = _check(p, seqs, q, ids.cpu().numpy(), n_sel.cpu().numpy(), scores.cpu().numpy(),
                   out.cpu().to(torch.float64).numpy())
     assert near <= 1
+
+
+def test_per_segment_retention_all_ties_long():
+    """Every token carries the same key, so every scored block ties; each
+    scored segment then keeps its k_s lowest block ids.  About 12,500 blocks:
+    the top-k runs in four CTAs and the segments' histograms hold one bin."""
+    from compressed_kv_cache_vector_gb300 import synth
+    from compressed_kv_cache_vector_gb300.binding import MosaicKV, make_config
+    from tests.harness import D, signed_permutation
+    T, S, W, B, G = 200_000, 4, 64, 16, 4
+    segments = [(0, 32, 0, 0, 0, 80), (400, 16, 1), (600, 32, 0, 0, 0, 150)]
+    st = O.Strategy(S, W, B, list(segments), 0, 100)
+    cfg = make_config(G, 1, 1, 1, T + 1, S, W, B, segments, 0, 100)
+    mk = MosaicKV(cfg, "cuda")
+    Rk, Rv = signed_permutation(41), signed_permutation(43)
+    mk.set_rotation(0, 0, 0, Rk.astype(np.float32), Rv.astype(np.float32))
+    rows = synth.lowrank_outlier(64, D, 0.9, 321, device="cuda")
+    k_row, v_row = rows[3:4], rows[7:8]
+    mk.append(0, [0], [T], k_row.expand(T, D).reshape(T, 1, D).contiguous(),
+              v_row.expand(T, D).reshape(T, 1, D).contiguous())
+    q = synth.query(1, G, D, 78, device="cuda")
+    ids, n_sel = mk.block_select(0, [0], q)
+    torch.cuda.synchronize()
+    assert mk.poll_error()[0] == 0
+    nb = O.n_middle_blocks(T, st)
+    firsts = O.segment_first_blocks(T, st)
+    want, total = [], 0
+    for s, sg in enumerate(st.segments):
+        if sg[2]:
+            continue
+        lo, hi = min(firsts[s], nb), (min(firsts[s + 1], nb) if s + 1 < len(firsts) else nb)
+        k_s = O.n_select(hi - lo, st, sg[5] or 100)
+        want += list(range(lo, lo + k_s))
+        total += k_s
+    assert int(n_sel[0, 0]) == total
+    assert np.array_equal(ids[0, 0, :total].cpu().numpy(), np.array(want))
