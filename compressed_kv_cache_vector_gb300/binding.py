@@ -15,7 +15,9 @@ import numpy as np
 import torch
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libmosaickv.so")
+# MOSAICKV_LIB names another build of the library to load (the tests use it
+# for the checked build, libmosaickv_checks.so).
+LIB_PATH = os.environ.get("MOSAICKV_LIB") or os.path.join(PKG, "libmosaickv.so")
 HEADER = os.path.join(PKG, "..", "include", "mosaickv.h")
 
 MK_HEAD_DIM = 128

@@ -17,6 +17,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmosaickv.so")
+# The checked build: every kernel's bounds checks compiled in (MK_CHECKS=1);
+# a failed check sets the error word and skips the access.  For the tests.
+LIB_CHECKS = os.path.join(PKG, "libmosaickv_checks.so")
+BUILD_CHECKS = os.path.join(PKG, "_build_checks")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xcompiler", "-Wall"]
@@ -38,22 +42,27 @@ def _deps():
         os.path.join(PKG, "..", "include", "mosaickv.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, checks: bool = False) -> str:
+    """Builds libmosaickv.so, or with checks=True the checked library
+    libmosaickv_checks.so (its own objects), and returns its path."""
+    lib, bdir = (LIB_CHECKS, BUILD_CHECKS) if checks else (LIB, BUILD)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if checks:
+        extra.append("-DMK_CHECKS=1")
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
@@ -64,13 +73,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"link failed:\n{p.stdout}\n{p.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

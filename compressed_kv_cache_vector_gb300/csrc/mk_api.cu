@@ -739,6 +739,33 @@ mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_he
   const int fb = ctx->firsts[ls * MK_MAX_SEGMENTS + segment], lb = ctx->firsts[ls * MK_MAX_SEGMENTS + segment + 1];
   const int n = lb - fb;
   if (n <= 0) return MK_ESTATE;
+  // The attention trusts the positions it reads from the pages: check them
+  // here, before any copy (a closed segment's blocks are complete).  uint8
+  // indices must name channels below 128; a bitmap row must hold exactly
+  // r / g groups.
+  {
+    const int g = L.bm_g ? seg_group_of(&c, segment) : 0;
+    const int pb = g ? MK_HEAD_DIM / g / 8 : r;
+    const int64_t Br = (int64_t)L.B * r, Bp = (int64_t)L.B * pb;
+    const unsigned char* pg = static_cast<const unsigned char*>(pages);
+    for (int b = 0; b < n; ++b) {
+      const unsigned char* page = pg + (int64_t)b * L.page_stride;
+      for (int w = 0; w < 2; ++w) {
+        const unsigned char* pos = page + (w == 0 ? 2 * Br : 4 * Br + Bp);
+        for (int t = 0; t < L.B; ++t) {
+          const unsigned char* row = pos + (int64_t)t * pb;
+          if (g) {
+            int bits = 0;
+            for (int i = 0; i < pb; ++i) bits += __builtin_popcount(row[i]);
+            if (bits != r / g) return MK_EINVAL;
+          } else {
+            for (int i = 0; i < r; ++i)
+              if (row[i] >= MK_HEAD_DIM) return MK_EINVAL;
+          }
+        }
+      }
+    }
+  }
   const int64_t u = mk::unit_index(L, layer, seq, kv_head);
   char* base = L.units + u * L.unit_stride;
   cudaStream_t s = (cudaStream_t)stream;

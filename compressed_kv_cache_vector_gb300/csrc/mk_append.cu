@@ -333,7 +333,8 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
       const int t = tid >> 1, h = tid & 1;
       const int p = lo + t;
       const bool in = t < nt;
-      const bool live = in && p >= S && p < T_new - W;
+      const bool live = in && p >= S && p < T_new - W &&
+                        in_bounds(L, (p - S) / B < L.nblk_cap && p - S - b0 * B < kTileTokens, SITE_PREFILL_PAGE, p);
       const uint16_t* row = rot + (size_t)t * kRotRow + 64 * h;
       const uint4* row4 = reinterpret_cast<const uint4*>(row);
       if (in && !live) {  // sink or window: the rotated row, dense
@@ -530,6 +531,7 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
       for (int b = b0; b <= b1; ++b) {
         const int r = ud.r[seg_of_block(ud, b)];
         if (r > kStageR) continue;  // written directly above
+        if (!in_bounds(L, b < L.nblk_cap, SITE_PREFILL_OUT, b)) continue;
         const int blo = S + b * B;
         const int st = max(blo, mlo), en = min(blo + B, mhi);
         char* page = base + L.off_pages + (int64_t)b * L.page_stride;
@@ -609,6 +611,7 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
         const int cp = tid;
         uint32_t* meta2 = reinterpret_cast<uint32_t*>(base + L.off_meta);
         for (int b = b0; b <= b1; ++b) {
+          if (!in_bounds(L, b < L.nblk_cap, SITE_PREFILL_META, b)) continue;
           const int blo = S + b * B;
           const uint32_t* src = pm + (b - b0) * 4 * 128;
           uint32_t u = src[cp], w = src[64 + cp];

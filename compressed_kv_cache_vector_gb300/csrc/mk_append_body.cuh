@@ -188,6 +188,7 @@ __device__ __forceinline__ unsigned compress_vec(const Layout& L, const UnitDesc
   const int m = pos - L.S;
   const int b = m / L.B;
   const int t = m - b * L.B;
+  if (!in_bounds(L, m >= 0 && b < L.nblk_cap, SITE_DECODE_PAGE, pos)) return 0u;  // (warp-uniform)
   const int sg = seg_of_block(ud, b);
   const int r = ud.r[sg], keep = seg_keep(ud, sg);
   char* page = base + L.off_pages + (int64_t)b * L.page_stride;
@@ -346,6 +347,7 @@ __device__ __forceinline__ void append_one_body(const Layout& L, const UnitDesc&
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e = T_old - L.W;
   const int slot = (e - L.S) % L.W;
+  if (!in_bounds(L, e >= L.S, SITE_WINDOW, e)) return;  // (block-uniform: the caller's full window)
   uint16_t* win_k = reinterpret_cast<uint16_t*>(base + L.off_win_k) + (int64_t)slot * D;
   uint16_t* win_v = reinterpret_cast<uint16_t*>(base + L.off_win_v) + (int64_t)slot * D;
   const int ch = tid - 64;  // warps 2-5: channel of k' and v'

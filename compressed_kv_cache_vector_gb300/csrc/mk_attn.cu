@@ -131,13 +131,13 @@ __device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v) {
 // loads and stores interleave.
 // Addresses are shared-window bytes: tk, tv (tiles), kv/ki/vv/vi (packed
 // values and indices); two pairs per lane per step, loads first.
-__device__ __forceinline__ void scatter_kv(uint32_t tk, uint32_t tv, uint32_t kv, uint32_t ki, uint32_t vv,
-                                           uint32_t vi, int n_el, uint32_t rm, int lane) {
+__device__ __forceinline__ void scatter_kv(const Layout& L, uint32_t tk, uint32_t tv, uint32_t kv, uint32_t ki,
+                                           uint32_t vv, uint32_t vi, int n_el, uint32_t rm, int lane) {
   for (int e = 2 * lane; e < n_el; e += 128) {
     const int e2 = e + 64;
     const bool has2 = e2 < n_el;
     const uint32_t kp = lds_u32(kv + 2 * e), vp = lds_u32(vv + 2 * e);
-    const uint32_t kx = lds_u16(ki + e), vx = lds_u16(vi + e);
+    uint32_t kx = lds_u16(ki + e), vx = lds_u16(vi + e);
     uint32_t kp2 = 0, vp2 = 0, kx2 = 0, vx2 = 0;
     if (has2) {
       kp2 = lds_u32(kv + 2 * e2);
@@ -145,6 +145,18 @@ __device__ __forceinline__ void scatter_kv(uint32_t tk, uint32_t tv, uint32_t kv
       kx2 = lds_u16(ki + e2);
       vx2 = lds_u16(vi + e2);
     }
+#if MK_CHECKS
+    // channels from the pages' index bytes stay inside the row (else the
+    // element goes to channel 0 and the error word records it)
+    if (!in_bounds(L, ((kx | vx | kx2 | vx2) & 0x8080u) == 0u, SITE_ATTN_TILE, (int64_t)(kx | vx << 16))) {
+      kx &= 0x7f7fu;
+      vx &= 0x7f7fu;
+      kx2 &= 0x7f7fu;
+      vx2 &= 0x7f7fu;
+    }
+#else
+    (void)L;
+#endif
     const uint32_t r0 = __umulhi(2u * (uint32_t)e, rm) * (kRow * 2), r1 = __umulhi(2u * (uint32_t)e + 2u, rm) * (kRow * 2);
     sts_u16(tk + r0 + 2 * (kx & 0xff), kp);
     sts_u16(tv + r0 + 2 * (vx & 0xff), vp);
@@ -776,8 +788,8 @@ __global__ void __launch_bounds__(MAXW * 32, 1) k_attn(Layout L, int layer, Call
         } else {
           const int n_el = ntok * r;
           const uint32_t rm = (0x80000000u + (uint32_t)r - 1u) / (uint32_t)r;
-          scatter_kv(smem_u32(tk), smem_u32(tv), smem_u32(kval), smem_u32(kidx), smem_u32(vval), smem_u32(vidx),
-                     n_el, rm, lane);
+          scatter_kv(L, smem_u32(tk), smem_u32(tv), smem_u32(kval), smem_u32(kidx), smem_u32(vval),
+                     smem_u32(vidx), n_el, rm, lane);
         }
         __syncwarp();
         issue_next();  // the packed group now lives in the tiles

@@ -25,6 +25,20 @@ enum DevErr : int32_t {
   ERR_BAD_NSEL = 3,    // n_sel larger than the ids row
   ERR_NO_ROTATION = 4,
   ERR_COPY_WAIT = 5,   // a bulk copy did not complete within the wait bound (status MK_ETIMEOUT)
+  ERR_BOUNDS = 6,      // checked build: an index failed its bounds check (unit = site, aux = index)
+};
+
+// Sites of the checked build's bounds checks (reported in the error word).
+enum CheckSite : int32_t {
+  SITE_DECODE_PAGE = 1,   // a decode-path packed row (page slot, rank)
+  SITE_DECODE_META = 2,   // a decode-path block min/max row
+  SITE_WINDOW = 3,        // a window ring or sink row
+  SITE_PREFILL_PAGE = 4,  // a prefill packed row (page, or its staging run)
+  SITE_PREFILL_OUT = 5,   // a prefill bulk store of a block's run
+  SITE_PREFILL_META = 6,  // a prefill block min/max row
+  SITE_ATTN_TILE = 7,     // an attention dense-tile element (token row, channel)
+  SITE_ATTN_PART = 8,     // an attention split-T partial or output row
+  SITE_SELECT_KEY = 9,    // a block-selection key or score
 };
 
 // Per (layer, seq, kv head) state kept on the device (64 bytes).
@@ -232,6 +246,24 @@ __device__ __forceinline__ void set_error(const Layout& L, int32_t detail, int32
     L.err[2] = unit;
     L.err[3] = aux;
   }
+}
+// The checked build (compiled with MK_CHECKS=1 into a separate library for
+// the tests) tests an index before its access: a failed check records the
+// site and the index in the error word and the caller skips the access.  The
+// default build compiles every check to true.
+#ifndef MK_CHECKS
+#define MK_CHECKS 0
+#endif
+__device__ __forceinline__ bool in_bounds(const Layout& L, bool ok, int32_t site, int64_t index) {
+#if MK_CHECKS
+  if (!ok) set_error(L, ERR_BOUNDS, site, (int32_t)index);
+  return ok;
+#else
+  (void)L;
+  (void)site;
+  (void)index;
+  return true;
+#endif
 }
 __device__ __forceinline__ bool has_error(const Layout& L) {
   return *(volatile int32_t*)L.err != 0;

@@ -361,6 +361,7 @@ __global__ void __launch_bounds__(256, 1) k_select(Layout L, int layer, CallSeqs
   };
   // Write block b's score: the user's fp32 copy, the key, the histogram count.
   auto emit = [&](int b, float sc) {
+    if (!in_bounds(L, b >= 0 && b < L.nblk_cap, SITE_SELECT_KEY, b)) return;
     if (so) so[b] = sc;
     const uint32_t key = seg_always(ud, seg_of_block(ud, b)) ? 0u : ordered_key(sc);
     kw[b] = key;

@@ -425,8 +425,11 @@ mk_status mk_host_pack_blocks(const float* R_k, const float* R_v, const void* k,
  * valid until they run (pinned memory makes the copies asynchronous).  The
  * segment must be closed: not the last one, which still receives appends.  r
  * may not exceed the largest r of the configuration (the page capacity).
+ * The pages' positions are checked on the host before any copy: every uint8
+ * index below 128, every bitmap row with exactly r/g bits set.
  * MK_EINVAL: bad ids, a null buffer, only one of R_k and R_v, r or
- * keep_channels out of range or not multiples of the element group; MK_ESTATE:
+ * keep_channels out of range or not multiples of the element group, a
+ * position outside those rules; MK_ESTATE:
  * the sequence has no prefill yet, or
  * the segment is the last or empty; MK_ENOTSUP: uncompressed pages. */
 mk_status mk_swap_segment(mk_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, int32_t segment, int32_t r,
