@@ -647,6 +647,7 @@ def main():
 
     if rank != 0:
         return
+    wcfg["l2"] = "inputs larger than L2: a step reads ~%.2f GB, the L2 holds 129 MB; no flush" % (step_bytes / 1e9)
     line = dict(base, value=value, ms_per_step=ms,
                 config=wcfg,
                 timing={"l2": "step reads ~%.2f GB across layers, far above the 129 MB L2, so no flush" %
