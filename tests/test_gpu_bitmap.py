@@ -60,11 +60,13 @@ def test_bitmap_storage_from_empty_and_compressed_keys(g):
     _check_storage(p, p.units[0])
 
 
-@pytest.mark.parametrize("g,seq_lens,topk", [(1, [3000, 900], 0), (2, [3000, 900], 0), (4, [3000, 900], 0),
-                                             (8, [3000, 900], 0), (4, [42000], 600)],
-                         ids=["g1", "g2", "g4", "g8", "g4-long-16warps"])
-def test_bitmap_decode_attention_matches_oracle(g, seq_lens, topk):
-    case = Case(n_q=4, n_kv=2 if len(seq_lens) > 1 else 1, seq_lens=seq_lens, rot="eigh",
+@pytest.mark.parametrize("g,seq_lens,topk,G", [(1, [3000, 900], 0, 4), (2, [3000, 900], 0, 4), (4, [3000, 900], 0, 4),
+                                               (8, [3000, 900], 0, 4), (4, [42000], 600, 4), (8, [3000, 900], 0, 8),
+                                               (2, [3000, 900], 0, 1)],
+                         ids=["g1", "g2", "g4", "g8", "g4-long-16warps", "g8-gqa8", "g2-gqa1"])
+def test_bitmap_decode_attention_matches_oracle(g, seq_lens, topk, G):
+    n_kv = 2 if len(seq_lens) > 1 else 1
+    case = Case(n_q=G * n_kv, n_kv=n_kv, seq_lens=seq_lens, rot="eigh",
                 block=32 if topk == 0 else 64, window=64 if topk == 0 else 128, page_format=2, elem_group=g,
                 segments=_segments(g) if topk == 0 else [(0, 40, 0)], topk_fixed=topk,
                 retain_permille=0 if topk else 100, steps=[1, 1, 2], seed=80 + g)

@@ -64,7 +64,9 @@ def _check(p, seqs, q, ids, n_sel, scores, out):
          steps=[1, 2], seed=130),
     Case(n_q=8, n_kv=1, seq_lens=[80000], rot="perm", block=16, window=128,
          segments=[(0, 38, 0, 0, 0, 20), (600, 38, 0, 0, 0, 150)], steps=[1], seed=131),   # 2 top-k CTAs
-], ids=["four-segments", "long-unit-two-ctas"])
+    Case(n_q=2, n_kv=2, seq_lens=[2600], rot="perm", block=32, window=64,
+         segments=[(0, 38, 0, 0, 0, 400), (500, 38, 0, 0, 0, 30)], steps=[1], seed=133),    # GQA 1
+], ids=["four-segments", "long-unit-two-ctas", "gqa1"])
 def test_per_segment_retention_select_and_attend(case):
     p = Pair(case)
     p.run_steps()
