@@ -2,7 +2,7 @@
 
 * The checked build (libmosaickv_checks.so: every kernel's bounds checks
   compiled in; a failed check records its site and index in the error word
-  and skips the access) runs the parity suites.  Those suites assert a clean
+  and skips the access) runs the parity suites and the random sweep.  Those suites assert a clean
   error word after every call, so a check that fires fails them; their
   results are compared with the oracle as in the default build.
 * mk_swap_segment checks the positions of the pages it is given before any
@@ -21,7 +21,7 @@ from compressed_kv_cache_vector_gb300 import build as Bld
 pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gpu_parity.py", "tests/test_gpu_bitmap.py", "tests/test_gpu_retention.py",
-          "tests/test_gpu_quest.py"]
+          "tests/test_gpu_quest.py", "tests/test_gpu_fuzz.py"]
 
 
 def test_checked_build_runs_the_parity_suites_clean():
