@@ -2,9 +2,10 @@
 
 * The checked build (libmosaickv_checks.so: every kernel's bounds checks
   compiled in; a failed check records its site and index in the error word
-  and skips the access) runs the parity suites and the random sweep.  Those suites assert a clean
-  error word after every call, so a check that fires fails them; their
-  results are compared with the oracle as in the default build.
+  and skips the access) runs the parity suites and the random sweep.  Those
+  suites assert a clean error word after every call, so a check that fires
+  fails them; their results are compared with the oracle as in the default
+  build.
 * mk_swap_segment checks the positions of the pages it is given before any
   copy, since the attention trusts them.
 """
