@@ -10,6 +10,7 @@
   copy, since the attention trusts them.
 """
 import os
+import re
 import subprocess
 import sys
 
@@ -35,6 +36,9 @@ def test_checked_build_runs_the_parity_suites_clean():
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider", *SUITES],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=3000)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+    m = re.search(r"(\d+) passed", r.stdout)
+    assert m and int(m.group(1)) >= 60, r.stdout[-2000:]     # the suites ran (about 70 tests)
+    print(r.stdout.strip().splitlines()[-1])
 
 
 @pytest.mark.parametrize("fmt", ["uint8", "bitmap"])
