@@ -51,3 +51,18 @@ def test_compressed_keys_shrink_the_selection_bytes():
     nblk = 4088
     assert full["select"] - comp["select"] == nblk * (2 * D * 2 - 160)
     assert comp["attn"] == full["attn"]
+
+
+def test_bitmap_pages_shrink_the_attention_bytes():
+    # Bitmap pages: 128 / g bits per vector in place of r index bytes, so a
+    # token's K and V cost 2 (2 r + 16 / g) bytes instead of 6 r.
+    wl = configs.get("c3")
+    T = wl.seq_lens[0]
+    base = bench.unit_bytes(wl, T, bench.segment_firsts(wl, T))
+    k, B = 409, 32
+    for g, r in ((1, 38), (4, 40), (8, 40)):
+        wl.elem_group = g
+        wl.segments = [(0, r, 0)]
+        got = bench.unit_bytes(wl, T, bench.segment_firsts(wl, T))
+        assert got["attn"] - base["attn"] == k * B * (2 * (2 * r + 16 // g) - 6 * 38)
+        assert got["append"] - base["append"] == 2 * (2 * r + 16 // g) - 6 * 38
