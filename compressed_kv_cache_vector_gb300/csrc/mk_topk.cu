@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
         if (ex < k_r && ex + c >= k_r) {
           const uint32_t hv[4] = {h4.w, h4.z, h4.y, h4.x};  // descending bin order
           int acc = ex;
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 4; ++i) {
             if (acc < k_r && acc + (int)hv[i] >= k_r) {
               s_bin = kKeyBins - 1 - 4 * tid - i;
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
     }
     // Per (round, warp) of the share: totals of (above, ties); then their
     // exclusive scan in (round, warp) order, one entry per thread.
-  #pragma unroll 1
+#pragma unroll 1
     for (int j = 0; j < own_rounds; ++j) {
       uint32_t gm = 0u, em = 0u;
       const int c = c_lo + j * kTkThreads + tid;
@@ -307,14 +307,14 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
       wtab[tid] = make_int2(ex.x + before.x, ex.y + before.y);
     }
     __syncthreads();
-  #pragma unroll 1
+#pragma unroll 1
     for (int j = 0; j < own_rounds; ++j) {
       uint32_t gm = 0u, em = 0u;
       const int c = c_lo + j * kTkThreads + tid;
       if (c < c_hi) masks(c, gm, em);
       const int og = __popc(gm), oe = __popc(em);
       int ig = og, ie = oe;
-  #pragma unroll
+#pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int yg = __shfl_up_sync(FULL, ig, o), ye = __shfl_up_sync(FULL, ie, o);
         if (lane >= o) {
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) k_topk(Layout L, int layer, Cal
       while (__popc(tm) > take_eq) tm &= ~(1u << (31 - __clz(tm)));  // keep the lowest ids
       const uint32_t take = gm | tm;
       const int p0 = g_before + min(e_before, need);
-  #pragma unroll
+#pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int p = p0 + __popc(take & ((1u << q) - 1u));
         if (((take >> q) & 1u) && out_off + p < L.k_max) out[out_off + p] = 4 * c + q;
