@@ -117,3 +117,40 @@ def test_host_pack_errors():
         b.host_pack_blocks(R, R, k, k, 16, 8, 12, 6 * 16 * 8, 0, 2, 8)  # keep a multiple of the group
     with pytest.raises(b.MosaicKVError):
         b.host_pack_blocks(R, R, k, k, 16, 8, 0, 16 * (4 * 8 + 2 * 16) - 1, 0, 2, 1)  # bitmap page too small
+
+
+@pytest.mark.parametrize("seed", list(range(2000, 2012)))
+def test_host_pack_random_formats_bit_exact(seed):
+    # Random block size, r, truncation, page format and group size; exact
+    # rotations (signed permutations), so the host's pages, block keys and
+    # compressed keys equal the oracle's byte for byte.
+    b = _lib()
+    rng = np.random.default_rng(seed)
+    block = int(rng.choice([16, 32, 64]))
+    fmt = int(rng.choice([0, 2]))
+    g = int(rng.choice([1, 2, 4, 8])) if fmt == 2 else 0
+    gg = max(1, g)
+    r = gg * int(rng.integers(max(1, 4 // gg), 96 // gg + 1))
+    keep = int(rng.choice([0, 96])) if r <= 96 else 0
+    mc = int(rng.choice([0, 16]))
+    S, W, n = 4, 32, int(rng.integers(1, 5))
+    T = S + W + n * block + 3
+    K, Kw = _bf16_data(T, 0.9, seed)
+    V, Vw = _bf16_data(T, 0.9, seed + 1)
+    Rk, Rv = _signed_perm(seed + 2), _signed_perm(seed + 3)
+    oc = O.OracleCache(O.Strategy(S, W, block, [(0, r, 0, keep)], 0, 100, mc, bitmap_group=g if fmt == 2 else 0), T)
+    oc.set_rotation(Rk, Rv)
+    oc.append(K, V)
+    pb = 16 // gg if fmt == 2 else r
+    page_stride = block * (4 * r + 2 * pb) + 16 * int(rng.integers(0, 3))
+    pages, meta, cmeta = b.host_pack_blocks(Rk, Rv, Kw[S:S + n * block], Vw[S:S + n * block], block, r, keep,
+                                            page_stride, mc, fmt, g)
+    mn, mx = oc.meta()
+    for blk in range(n):
+        want = oc.page_bytes(blk)
+        assert np.array_equal(pages[blk, :want.size], want), (seed, blk)
+        assert np.array_equal(meta[blk, 0], O.bf16_bits(mn[blk]))
+        assert np.array_equal(meta[blk, 1], O.bf16_bits(mx[blk]))
+    if mc:
+        idx, cmn, cmx = O.compress_key_rows(mn[:n], mx[:n], mc)
+        assert np.array_equal(cmeta[:, 4 * mc:5 * mc], idx.astype(np.uint8))
