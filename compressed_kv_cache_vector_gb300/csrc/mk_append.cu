@@ -422,8 +422,8 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
           if (gg == 2) group_keys<2>(row4, h, kp, live, kw);
           else if (gg == 4) group_keys<4>(row4, h, kp, live, kw);
           else group_keys<8>(row4, h, kp, live, kw);
-          kneed = r / gg;
-          const int ng = 64 / gg;
+          kneed = r / max(gg, 1);  // (gg >= 2 here; the bound keeps dead code of the uint8 instance clean)
+          const int ng = 64 / max(gg, 1);
           uint32_t thr = 0u;
 #pragma unroll 1
           for (int bit = 30; bit >= 0; --bit) {
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(256, 1) k_append_bulk(Layout L, int layer, Cal
                                 : reinterpret_cast<uint8_t*>(page + (is_v ? 4 * Br + Bp : 2 * Br)) + tt * pb;
           if (gg) {
             // Bitmap ([S] sec. 5.1): this half's 64 / gg bits at byte 8 h / gg.
-            uint8_t* d = idx + h * (8 / gg);
+            uint8_t* d = idx + h * (8 / max(gg, 1));
             if (gg == 1) {
               reinterpret_cast<uint32_t*>(d)[0] = keep_lo;
               reinterpret_cast<uint32_t*>(d)[1] = keep_hi;
